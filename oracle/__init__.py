@@ -1,0 +1,189 @@
+"""CPU oracle for the paged KV insert / dequant-gather path.
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package; the library in
+``gather_kv_rope_gb300`` never does, and the two share no code.
+
+The arithmetic lives in ``gkr_oracle.c`` (plain C, compiled with
+``-O2 -ffp-contract=off -fno-fast-math``); this module only compiles it with
+gcc and marshals numpy arrays through ctypes.  Every function cites the page
+passage it follows in the C source.
+
+Pinning status (what each function is checked against, on the CPU):
+  e4m3 encode / decode  -- torch.float8_e4m3fn casts (all codes, all midpoints)
+  bf16 encode / decode  -- torch.bfloat16 casts
+  UE8M0 scale byte      -- exact rational ceil(log2(amax/448)), all bf16 amax
+  RoPE pair             -- hand-computed exact cases, special angles
+  record encoders       -- hand-written golden records (tests/golden)
+  page placement        -- hand-computed byte offsets, brute-force tiny caches
+  gather / decode       -- exhaustive code x scale table vs decode definition
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+_SRC = _HERE / "gkr_oracle.c"
+_OUT = _HERE / "_build" / "liboracle.so"
+
+CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+          "-fvisibility=hidden", "-std=c11", "-Wall", "-Wextra"]
+
+ERR_SLOT = 1
+ERR_POS = 2
+ERR_INDEX = 4
+
+
+def build(force: bool = False) -> Path:
+    """Compile the oracle with gcc (a second or so).  Returns the .so path."""
+    if not force and _OUT.exists() and _OUT.stat().st_mtime >= _SRC.stat().st_mtime:
+        return _OUT
+    _OUT.parent.mkdir(parents=True, exist_ok=True)
+    tmp = _OUT.with_suffix(f".{os.getpid()}.tmp")
+    cmd = ["gcc", *CFLAGS, "-o", str(tmp), str(_SRC), "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _OUT)
+    return _OUT
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(str(build()))
+        u8, u16, i32, i64 = ctypes.c_uint8, ctypes.c_uint16, ctypes.c_int, ctypes.c_int64
+        vp, f32, f64 = ctypes.c_void_p, ctypes.c_float, ctypes.c_double
+        L.oracle_e4m3_value.argtypes, L.oracle_e4m3_value.restype = [u8], f64
+        L.oracle_e4m3_encode.argtypes, L.oracle_e4m3_encode.restype = [f64], u8
+        L.oracle_bf16_value.argtypes, L.oracle_bf16_value.restype = [u16], f64
+        L.oracle_bf16_encode.argtypes, L.oracle_bf16_encode.restype = [f64], u16
+        L.oracle_ue8m0_byte.argtypes, L.oracle_ue8m0_byte.restype = [f32], u8
+        L.oracle_rope_pair.argtypes = [f32, f32, f32, f32, vp, vp]
+        L.oracle_rope_pair.restype = None
+        L.oracle_encode_v41.argtypes = [vp, vp, vp, vp]
+        L.oracle_encode_v41.restype = None
+        L.oracle_encode_v4.argtypes = [vp, vp, vp, vp]
+        L.oracle_encode_v4.restype = None
+        L.oracle_insert.argtypes = [vp, i64, vp, i32, i32, i64, i64, vp, vp, vp, i64]
+        L.oracle_insert.restype = i32
+        L.oracle_decode.argtypes = [vp, vp, i32, vp]
+        L.oracle_decode.restype = None
+        L.oracle_gather.argtypes = [vp, i32, i32, i64, i64, vp, i64, vp]
+        L.oracle_gather.restype = i32
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data
+
+
+# --- scalar number-format helpers ------------------------------------------------
+
+def e4m3_value(code: int) -> float:
+    return lib().oracle_e4m3_value(code)
+
+
+def e4m3_encode(y: float) -> int:
+    return lib().oracle_e4m3_encode(float(y))
+
+
+def bf16_value(bits: int) -> float:
+    return lib().oracle_bf16_value(bits)
+
+
+def bf16_encode(y: float) -> int:
+    return lib().oracle_bf16_encode(float(y))
+
+
+def ue8m0_byte(amax: float) -> int:
+    return lib().oracle_ue8m0_byte(float(amax))
+
+
+def rope_pair(e: float, o: float, c: float, s: float) -> tuple[float, float]:
+    eo, oo = ctypes.c_float(), ctypes.c_float()
+    lib().oracle_rope_pair(e, o, c, s, ctypes.byref(eo), ctypes.byref(oo))
+    return eo.value, oo.value
+
+
+# --- records ----------------------------------------------------------------------
+
+def record_rows(record: int) -> tuple[int, int]:
+    """(data row bytes, scale row bytes) of a record, from its definition."""
+    if record == 528:
+        return 512, 16
+    if record == 584:
+        return 576, 8
+    raise ValueError(f"unknown record width {record}")
+
+
+def encode(record: int, kv_row: np.ndarray, csc_row: np.ndarray):
+    """Encode one token (bf16 bits [512], fp32 cos/sin row [64]) -> (data, scales)."""
+    kv_row = np.ascontiguousarray(kv_row, dtype=np.uint16)
+    csc_row = np.ascontiguousarray(csc_row, dtype=np.float32)
+    assert kv_row.shape == (512,) and csc_row.shape == (64,)
+    D, S = record_rows(record)
+    data = np.zeros(D, np.uint8)
+    scales = np.zeros(S, np.uint8)
+    fn = lib().oracle_encode_v41 if record == 528 else lib().oracle_encode_v4
+    fn(_ptr(kv_row), _ptr(csc_row), _ptr(data), _ptr(scales))
+    return data, scales
+
+
+def insert(kv: np.ndarray, cache: np.ndarray, record: int, block_size: int,
+           num_pages: int, page_stride: int, slots: np.ndarray,
+           positions: np.ndarray, csc: np.ndarray) -> int:
+    """Insert into a flat uint8 host cache of num_pages * page_stride bytes, in place.
+    Returns the error bits."""
+    kv = np.ascontiguousarray(kv, dtype=np.uint16).reshape(-1, 512)
+    slots = np.ascontiguousarray(slots, dtype=np.int64).reshape(-1)
+    positions = np.ascontiguousarray(positions, dtype=np.int64).reshape(-1)
+    csc = np.ascontiguousarray(csc, dtype=np.float32).reshape(-1, 64)
+    assert cache.dtype == np.uint8 and cache.flags["C_CONTIGUOUS"]
+    assert cache.size >= num_pages * page_stride
+    T = slots.shape[0]
+    assert kv.shape[0] == T and positions.shape[0] == T
+    err = lib().oracle_insert(_ptr(kv), T, _ptr(cache), record, block_size, num_pages,
+                              page_stride, _ptr(slots), _ptr(positions), _ptr(csc),
+                              csc.shape[0])
+    if err < 0:
+        raise ValueError(f"unknown record width {record}")
+    return err
+
+
+def decode(record: int, data: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    data = np.ascontiguousarray(data, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    out = np.zeros(512, np.uint16)
+    lib().oracle_decode(_ptr(data), _ptr(scales), record, _ptr(out))
+    return out
+
+
+def gather(cache: np.ndarray, record: int, block_size: int, num_pages: int,
+           page_stride: int, indices: np.ndarray):
+    """Returns (bf16 bits [*indices.shape, 512] as uint16, error bits)."""
+    idx = np.ascontiguousarray(indices, dtype=np.int32)
+    flat = idx.reshape(-1)
+    out = np.zeros((flat.shape[0], 512), np.uint16)
+    assert cache.dtype == np.uint8 and cache.flags["C_CONTIGUOUS"]
+    err = lib().oracle_gather(_ptr(cache), record, block_size, num_pages, page_stride,
+                              _ptr(flat), flat.shape[0], _ptr(out))
+    if err < 0:
+        raise ValueError(f"unknown record width {record}")
+    return out.reshape(*idx.shape, 512), err
+
+
+def page_stride(record: int, block_size: int) -> int:
+    """Page stride for a record: block_size * record bytes rounded up to the page
+    alignment (512 for the 528 B record, 576 for the 584 B record)."""
+    align = 512 if record == 528 else 576
+    need = block_size * record
+    return -(-need // align) * align

@@ -1,0 +1,360 @@
+/*
+ * Plain CPU oracle for the DeepSeek-V4.1 / V4 paged KV-cache hot path:
+ * RoPE + MXFP8 quantise + paged insert, and dequantise-gather.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header, table or constant generator
+ * with the CUDA library.
+ *
+ * Written to be read against the pages, not to be fast:
+ *   - number formats are decoded from their definitions and encoded by
+ *     "round the exact value to the format's grid, ties to even";
+ *   - the UE8M0 scale is the smallest power of two 2^e with 448 * 2^e >= amax,
+ *     found by walking e upwards (the definition of ceil(log2(amax / 448)));
+ *   - RoPE is four separately rounded fp32 products and two fp32 sums.
+ * Build: gcc -O2 -ffp-contract=off -fno-fast-math (no FMA contraction, no
+ * flush-to-zero), so every float operation below is one IEEE-754 binary32
+ * operation rounded to nearest even.
+ *
+ * Sources (page title, section):
+ *   [P1] "PR #56893 [DSv4.1] Store the whole KV in MXFP8 (FlashMLA V4.1 record)":
+ *        section "功能与动机" (record contents: 528 B = 512 B e4m3 + 16 UE8M0 scales
+ *        over 32-dim blocks; legacy 584 B = 448 B e4m3 NoPE + 128 B bf16 RoPE +
+ *        7 UE8M0 scales over 64-dim blocks + 1 pad; page strides 512 / 576);
+ *        section "关键源码片段", fused_compress_quant_cache.py kernel text
+ *        (slot < 0 skips; page = slot // block, row = slot % block; data region
+ *        then scale region in a page; adjacent-pair rotation of dims 448..511
+ *        with cos = row[pair], sin = row[32 + pair]; per-32-block amax, scale
+ *        2^ceil(log2(amax / 448)), biased exponent byte; clamp to +-448 and cast
+ *        to e4m3);
+ *        section "实现拆解" item 4 (gather dequantises fp8 * 2^(scale - 127)
+ *        per group; the same gather serves 448/64 and 512/32 with a bf16 tail).
+ *   [P2] "PR #56441 [Perf][DSpark] KV-only context insertion across V4.1 cache
+ *        formats", section "实现拆解" item 1 (input contract).
+ *   [P4] FlashMLA overview, DSA section (index -1 marks an invalid entry).
+ * Readings where the pages are silent (exact scale rule, amax 0 -> byte 0,
+ * RNE + saturation, fp32 RoPE op order, V4 page layout, pad byte 0, NaN
+ * output pattern, out-of-range handling) are listed in the design notes.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORACLE_EXPORT __attribute__((visibility("default")))
+
+/* Error bits reported by insert / gather for entries outside the cache. */
+#define ORACLE_ERR_SLOT 1     /* slot >= num_pages * block_size          */
+#define ORACLE_ERR_POS 2      /* position outside [0, max_pos)           */
+#define ORACLE_ERR_INDEX 4    /* gather index < -1 or >= num_pages * bs  */
+
+/* ------------------------------------------------------------------------ */
+/* Number formats                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* OCP FP8 E4M3 ("e4m3fn"): sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * no infinities; exponent 1111 with mantissa 111 is NaN.  Exponent field 0
+ * holds subnormals M * 2^-9; otherwise the value is (1 + M/8) * 2^(E-7). */
+ORACLE_EXPORT double oracle_e4m3_value(uint8_t code)
+{
+    int sign = code >> 7;
+    int E = (code >> 3) & 15;
+    int M = code & 7;
+    double mag;
+    if (E == 15 && M == 7)
+        return NAN;
+    if (E == 0)
+        mag = ldexp((double)M, -9);
+    else
+        mag = ldexp(1.0 + M / 8.0, E - 7);
+    return sign ? -mag : mag;
+}
+
+/* Round y to the nearest e4m3 value, ties to even, saturating at +-448
+ * (the largest finite e4m3 value).  The sign is kept, so -0 and negative
+ * values that round to zero give 0x80. */
+ORACLE_EXPORT uint8_t oracle_e4m3_encode(double y)
+{
+    uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    double a = fabs(y);
+    double quantum, v;
+    int k, code;
+
+    if (isnan(y))
+        return (uint8_t)(sign | 0x7F);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    /* In the binade [2^k, 2^(k+1)) e4m3 has 8 values, spaced 2^(k-3); below
+     * 2^-6 (the smallest normal) the spacing is the subnormal step 2^-9. */
+    if (a == 0.0) {
+        k = -6;
+    } else {
+        (void)frexp(a, &k); /* a = f * 2^k with f in [0.5, 1) */
+        k -= 1;             /* now a in [2^k, 2^(k+1))          */
+        if (k < -6)
+            k = -6;
+    }
+    quantum = ldexp(1.0, k - 3);
+    v = nearbyint(a / quantum) * quantum; /* a / quantum is exact; RNE */
+    /* Find the code whose value is v. */
+    for (code = 0; code <= 0x7E; code++)
+        if (oracle_e4m3_value((uint8_t)code) == v)
+            return (uint8_t)(sign | code);
+    return (uint8_t)(sign | 0x7F); /* unreachable for |y| < 448 */
+}
+
+/* bfloat16: sign, 8 exponent bits with bias 127, 7 mantissa bits. */
+ORACLE_EXPORT double oracle_bf16_value(uint16_t bits)
+{
+    int sign = bits >> 15;
+    int E = (bits >> 7) & 0xFF;
+    int M = bits & 0x7F;
+    double mag;
+    if (E == 0xFF)
+        return M ? NAN : (sign ? -INFINITY : INFINITY);
+    if (E == 0)
+        mag = ldexp((double)M, -133);
+    else
+        mag = ldexp(1.0 + M / 128.0, E - 127);
+    return sign ? -mag : mag;
+}
+
+/* Round y to the nearest bfloat16, ties to even; values that round past the
+ * largest finite bf16 become infinity.  Every NaN becomes 0x7FC0. */
+ORACLE_EXPORT uint16_t oracle_bf16_encode(double y)
+{
+    uint16_t sign = signbit(y) ? 0x8000 : 0x0000;
+    double a = fabs(y);
+    double quantum, v, f;
+    int k, e;
+
+    if (isnan(y))
+        return 0x7FC0;
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80);
+    if (a == 0.0)
+        return sign;
+    (void)frexp(a, &k);
+    k -= 1; /* a in [2^k, 2^(k+1)) */
+    if (k < -126)
+        k = -126; /* subnormal range: spacing 2^-133 */
+    quantum = ldexp(1.0, k - 7);
+    v = nearbyint(a / quantum) * quantum;
+    if (v >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80);
+    if (v < ldexp(1.0, -126)) /* subnormal (or zero): M = v / 2^-133 */
+        return (uint16_t)(sign | (uint16_t)(v / ldexp(1.0, -133)));
+    f = frexp(v, &e); /* v = f * 2^e, f in [0.5, 1): value = (1 + M/128) * 2^(e-1) */
+    return (uint16_t)(sign | (uint16_t)((e - 1 + 127) << 7) |
+                      (uint16_t)((f * 2.0 - 1.0) * 128.0));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Method steps                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* UE8M0 scale byte for a block whose largest magnitude is amax: the smallest
+ * e in [-127, 127] with 448 * 2^e >= amax (that is ceil(log2(amax / 448))
+ * clamped to [-127, 127]), stored as e + 127.  amax = 0 gives byte 0. */
+ORACLE_EXPORT uint8_t oracle_ue8m0_byte(float amax)
+{
+    int e = -127;
+    while (e < 127 && ldexp(448.0, e) < (double)amax)
+        e++;
+    return (uint8_t)(e + 127);
+}
+
+/* One adjacent-pair rotation in fp32: even' = e*c - o*s, odd' = o*c + e*s,
+ * each product and each sum rounded separately. */
+ORACLE_EXPORT void oracle_rope_pair(float e, float o, float c, float s,
+                                    float *e_out, float *o_out)
+{
+    float t1 = e * c;
+    float t2 = o * s;
+    float t3 = o * c;
+    float t4 = e * s;
+    *e_out = t1 - t2;
+    *o_out = t3 + t4;
+}
+
+/* Widen one token's 512 bf16 values to fp32 and rotate dims 448..511 with the
+ * cos/sin row csc[0..31] = cos, csc[32..63] = sin: pair j covers dims
+ * 448 + 2j and 449 + 2j. */
+static void load_and_rotate(const uint16_t *kv_row, const float *csc_row,
+                            float x[512])
+{
+    int d, j;
+    for (d = 0; d < 512; d++)
+        x[d] = (float)oracle_bf16_value(kv_row[d]);
+    for (j = 0; j < 32; j++) {
+        float e = x[448 + 2 * j];
+        float o = x[449 + 2 * j];
+        oracle_rope_pair(e, o, csc_row[j], csc_row[32 + j], &x[448 + 2 * j],
+                         &x[449 + 2 * j]);
+    }
+}
+
+static float block_amax(const float *x, int n)
+{
+    float m = 0.0f;
+    int i;
+    for (i = 0; i < n; i++)
+        if (fabsf(x[i]) > m)
+            m = fabsf(x[i]);
+    return m;
+}
+
+/* Quantise n values of one block with scale byte b: e4m3(x / 2^(b - 127)). */
+static void quantise_block(const float *x, int n, uint8_t b, uint8_t *q)
+{
+    int i;
+    for (i = 0; i < n; i++)
+        q[i] = oracle_e4m3_encode(ldexp((double)x[i], 127 - (int)b));
+}
+
+/* V4.1 record of one token: 512 e4m3 bytes (all dims, rotated) and 16 scale
+ * bytes, one per 32-dim block. */
+ORACLE_EXPORT void oracle_encode_v41(const uint16_t *kv_row, const float *csc_row,
+                                     uint8_t data[512], uint8_t scales[16])
+{
+    float x[512];
+    int b;
+    load_and_rotate(kv_row, csc_row, x);
+    for (b = 0; b < 16; b++) {
+        scales[b] = oracle_ue8m0_byte(block_amax(x + 32 * b, 32));
+        quantise_block(x + 32 * b, 32, scales[b], data + 32 * b);
+    }
+}
+
+/* V4 (legacy) record of one token: 448 e4m3 bytes for the NoPE dims in seven
+ * 64-dim blocks, then the 64 rotated RoPE dims as little-endian bf16 (128 B);
+ * scale row = 7 bytes + one pad byte 0x00. */
+ORACLE_EXPORT void oracle_encode_v4(const uint16_t *kv_row, const float *csc_row,
+                                    uint8_t data[576], uint8_t scales[8])
+{
+    float x[512];
+    int b, k;
+    load_and_rotate(kv_row, csc_row, x);
+    for (b = 0; b < 7; b++) {
+        scales[b] = oracle_ue8m0_byte(block_amax(x + 64 * b, 64));
+        quantise_block(x + 64 * b, 64, scales[b], data + 64 * b);
+    }
+    scales[7] = 0x00;
+    for (k = 0; k < 64; k++) {
+        uint16_t h = oracle_bf16_encode((double)x[448 + k]);
+        data[448 + 2 * k] = (uint8_t)(h & 0xFF);
+        data[449 + 2 * k] = (uint8_t)(h >> 8);
+    }
+}
+
+/* Row sizes of a record: data row D bytes, scale row S bytes. */
+static int record_rows(int record, int *D, int *S)
+{
+    if (record == 528) {
+        *D = 512;
+        *S = 16;
+        return 0;
+    }
+    if (record == 584) {
+        *D = 576;
+        *S = 8;
+        return 0;
+    }
+    return -1;
+}
+
+/* Insert T tokens into a paged cache (host memory).  A page starts at
+ * page * page_stride and holds the data region (block_size rows of D bytes)
+ * followed by the scale region (block_size rows of S bytes).  Tokens with a
+ * negative slot are skipped.  Tokens whose slot or position lies outside the
+ * cache / the cos-sin table are skipped too and set an error bit.
+ * Returns the OR of the error bits, or -1 for an unknown record width. */
+ORACLE_EXPORT int oracle_insert(const uint16_t *kv, int64_t num_tokens,
+                                uint8_t *cache, int record, int block_size,
+                                int64_t num_pages, int64_t page_stride,
+                                const int64_t *slots, const int64_t *positions,
+                                const float *csc, int64_t max_pos)
+{
+    int D, S, err = 0;
+    int64_t t;
+    if (record_rows(record, &D, &S))
+        return -1;
+    for (t = 0; t < num_tokens; t++) {
+        int64_t slot = slots[t], pos = positions[t], page, row;
+        uint8_t *base;
+        if (slot < 0)
+            continue;
+        if (slot >= num_pages * block_size) {
+            err |= ORACLE_ERR_SLOT;
+            continue;
+        }
+        if (pos < 0 || pos >= max_pos) {
+            err |= ORACLE_ERR_POS;
+            continue;
+        }
+        page = slot / block_size;
+        row = slot % block_size;
+        base = cache + page * page_stride;
+        if (record == 528)
+            oracle_encode_v41(kv + t * 512, csc + pos * 64, base + row * D,
+                              base + (int64_t)block_size * D + row * S);
+        else
+            oracle_encode_v4(kv + t * 512, csc + pos * 64, base + row * D,
+                             base + (int64_t)block_size * D + row * S);
+    }
+    return err;
+}
+
+/* Dequantise one stored record into 512 bf16 values.
+ * V4.1: out[d] = bf16(e4m3(data[d]) * 2^(scale[d/32] - 127)).
+ * V4:   d < 448 as above with scale[d/64]; d >= 448 copies the stored bf16.
+ * A scale byte of 255 is the UE8M0 NaN; NaN results are written as 0x7FC0. */
+ORACLE_EXPORT void oracle_decode(const uint8_t *data, const uint8_t *scales,
+                                 int record, uint16_t out[512])
+{
+    int d;
+    for (d = 0; d < 512; d++) {
+        int block;
+        double scale, v;
+        if (record == 584 && d >= 448) {
+            out[d] = (uint16_t)(data[448 + 2 * (d - 448)] |
+                                (data[449 + 2 * (d - 448)] << 8));
+            continue;
+        }
+        block = (record == 528) ? d / 32 : d / 64;
+        scale = (scales[block] == 255) ? NAN : ldexp(1.0, (int)scales[block] - 127);
+        v = oracle_e4m3_value(data[d]) * scale; /* exact in double */
+        out[d] = oracle_bf16_encode(v);
+    }
+}
+
+/* Gather: for each index, -1 emits 512 bf16 zeros; any other index is a slot
+ * number (page = index / block_size, row = index % block_size) whose record is
+ * dequantised.  Indices < -1 or past the cache emit zeros and set an error bit.
+ * Returns the OR of the error bits, or -1 for an unknown record width. */
+ORACLE_EXPORT int oracle_gather(const uint8_t *cache, int record, int block_size,
+                                int64_t num_pages, int64_t page_stride,
+                                const int32_t *indices, int64_t num_indices,
+                                uint16_t *out)
+{
+    int D, S, err = 0;
+    int64_t i;
+    if (record_rows(record, &D, &S))
+        return -1;
+    for (i = 0; i < num_indices; i++) {
+        int64_t idx = indices[i], page, row;
+        const uint8_t *base;
+        if (idx < 0 || idx >= num_pages * block_size) {
+            if (idx != -1)
+                err |= ORACLE_ERR_INDEX;
+            memset(out + i * 512, 0, 512 * sizeof(uint16_t));
+            continue;
+        }
+        page = idx / block_size;
+        row = idx % block_size;
+        base = cache + page * page_stride;
+        oracle_decode(base + row * D, base + (int64_t)block_size * D + row * S,
+                      record, out + i * 512);
+    }
+    return err;
+}
