@@ -1,0 +1,559 @@
+#!/usr/bin/env python3
+"""Benchmark: paged KV insert (RoPE + MXFP8) + dequant-gather round trip on GB300.
+
+One step = kv_insert of 16384 bf16 tokens into a V4.1 (528 B record) paged cache
+of 512 pages x 64 slots, then kv_gather of the same 16384 slot ids (the -1 ones
+come back as zeros) into bf16 [16384, 512].  Metric: tokens per second.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  Timing: W eager warm-up steps, then K steps run
+as replays of a captured CUDA graph of G steps, bracketed by a barrier and a
+device synchronise on both sides, timed with CUDA events on the launching stream
+(max over ranks).  Six input sets (~300 MB together, more than the 126 MB L2)
+rotate so no step finds its inputs in L2.  Per-kernel durations come from
+events captured inside the graph (last replay), or from a separate eager pass
+when torch cannot capture timing events.
+
+`--impl reference` times the CPU oracle (test infrastructure) on the same
+workload, a bounded sample of tokens per step, on the host cores.
+Under torchrun with N > 1 every rank runs its own replica (no collective on
+the data path; weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import shutil
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "KV insert+gather tokens/s and HBM GB/s (% of GB300 peak) at 1 GPU"
+WORKLOAD = "roundtrip_v41_16384"
+FALLBACK_HBM_GBS = 6800.0
+ROTATE = 6            # input sets rotated through the steps
+GRAPH_STEPS = 60      # steps per captured graph (a multiple of ROTATE)
+
+
+# ----------------------------------------------------------------------------- setup
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=48000)
+    ap.add_argument("--warmup", type=int, default=60)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the larger-workload kernel sweep")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU time budget of the oracle baseline sample")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def reduce_max(value: float, dist=None) -> float:
+    """Max of a host scalar over all ranks (a timing reduction, not a data-path
+    collective).  With no process group it returns the value unchanged."""
+    if dist is None:
+        return value
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist=None):
+    if dist is not None:
+        dist.barrier()
+
+
+def measured_peaks() -> tuple[float, str]:
+    p = ROOT / "MEASURED_PEAKS.json"
+    try:
+        v = float(json.loads(p.read_text())["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs: STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = ROOT / "gather_kv_rope_gb300" / "csrc"
+    for f in sorted(list(csrc.glob("*.cu")) + list(csrc.glob("*.cuh")) + list(csrc.glob("*.h"))):
+        h.update(f.name.encode())
+        h.update(f.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/ncu_traffic.txt),
+    or None when absent or taken on a different kernel source."""
+    f = ROOT / "profiles" / "ncu_traffic.txt"
+    if not f.exists():
+        return None
+    src = kernel_source_hash()
+    for line in f.read_text().splitlines():
+        kv = dict(p.split("=", 1) for p in line.split() if "=" in p)
+        if kv.get("kernel") == kernel and kv.get("workload") == workload \
+                and kv.get("source_hash") == src:
+            return int(kv["dram_bytes_per_launch"])
+    return None
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw",
+              "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.samples: list[tuple[float, list[str]]] = []
+        self.proc = None
+        self.error = None
+
+    def start(self):
+        exe = shutil.which("nvidia-smi")
+        if exe is None:
+            self.error = "nvidia-smi not found"
+            return self
+        try:
+            self.proc = subprocess.Popen(
+                [exe, f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+                 "-lms", "20", "-i", self.gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError as e:
+            self.error = str(e)
+            return self
+        first = threading.Event()
+
+        def reader():
+            for line in self.proc.stdout:
+                self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+                first.set()
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        first.wait(timeout=5.0)
+        return self
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        if self.error:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": self.error}
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        note = f"{len(inside)} samples at 20 ms during the timed region"
+        if not inside:     # region shorter than the sampling interval: nearest samples
+            inside = [s for t, s in self.samples if t0 - 0.25 <= t <= t1 + 0.25]
+            note = f"timed region shorter than the sampling interval; {len(inside)} samples within 0.25 s"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no samples"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in inside if num(s[1]) is not None]
+        smax = [num(s[2]) for s in inside if num(s[2]) is not None]
+        pw = [num(s[3]) for s in inside if num(s[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in inside for n, v in zip(names, s[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+# ----------------------------------------------------------------------------- bytes
+
+def insert_bytes(slots: np.ndarray, record: int) -> int:
+    """Algorithmic bytes of one insert: 16 B (slot + position) per token, plus the
+    1024 B bf16 row read and the record written for every valid slot.  The cos/sin
+    rows are not counted (a bandwidth-optimal kernel reads each row once)."""
+    return 16 * slots.size + int((slots >= 0).sum()) * (1024 + record)
+
+
+def gather_bytes(indices: np.ndarray, record: int) -> int:
+    """Algorithmic bytes of one gather: 4 B index + 1024 B bf16 row written per
+    index, plus the record read for every valid index."""
+    return indices.size * (4 + 1024) + int((indices >= 0).sum()) * record
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def _timing_event(torch, external: bool):
+    if external:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    return torch.cuda.Event(enable_timing=True)
+
+
+def _supports_external_events(torch) -> bool:
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        return True
+    except TypeError:
+        return False
+
+
+def device_sets(case, device, n_sets: int):
+    import torch
+    import gather_kv_rope_gb300 as gkr
+    kv = torch.from_numpy(case.kv.view(np.int16)).view(torch.bfloat16).to(device)
+    slots = torch.from_numpy(case.slots).to(device)
+    pos = torch.from_numpy(case.positions).to(device)
+    csc = torch.from_numpy(case.csc).to(device)
+    idx = torch.from_numpy(case.indices).to(device) if case.indices is not None else None
+    sets = []
+    for _ in range(n_sets):
+        sets.append(dict(
+            kv=kv.clone(), slots=slots.clone(), pos=pos.clone(), csc=csc,
+            idx=None if idx is None else idx.clone(),
+            cache=gkr.alloc_cache(case.num_pages, case.block_size, case.record, device, fill=0),
+            out=None if idx is None else torch.empty(case.indices.shape + (512,),
+                                                     dtype=torch.bfloat16, device=device)))
+    return sets
+
+
+def step(gkr, case, s, ev=None):
+    """One pass of the hot path on one input set; optional events around each kernel."""
+    if ev is not None:
+        ev[0].record()
+    gkr.kv_insert(s["kv"], s["cache"], s["slots"], s["pos"], s["csc"], case.block_size,
+                  case.record)
+    if ev is not None:
+        ev[1].record()
+    if s["idx"] is not None:
+        gkr.kv_gather(s["cache"], s["idx"], s["out"])
+        if ev is not None:
+            ev[2].record()
+
+
+def time_roundtrip(args, device, dist):
+    import torch
+    import gather_kv_rope_gb300 as gkr
+    import workloads as W
+
+    case = W.roundtrip_v41_16384()
+    sets = device_sets(case, device, ROTATE)
+    T = case.num_tokens
+    for k in range(args.warmup):
+        step(gkr, case, sets[k % ROTATE])
+    torch.cuda.synchronize(device)
+
+    G = GRAPH_STEPS
+    K = max(G, (args.steps + G - 1) // G * G)       # K is rounded up to whole graphs
+    replays = K // G
+    external = _supports_external_events(torch)
+    kev = [[_timing_event(torch, external) for _ in range(3)] for _ in range(G)] \
+        if external else None
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(cap):
+        step(gkr, case, sets[0])                    # side-stream warm-up before capture
+    torch.cuda.current_stream(device).wait_stream(cap)
+    torch.cuda.synchronize(device)
+    with torch.cuda.graph(graph):
+        for k in range(G):
+            step(gkr, case, sets[k % ROTATE], None if kev is None else kev[k])
+    graph.replay()                                   # one untimed replay
+    torch.cuda.synchronize(device)
+
+    sampler = ClockSampler(_gpu_id(torch, device)).start()
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    h0 = time.time()
+    e0.record(stream)
+    for _ in range(replays):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    h1 = time.time()
+    barrier(dist)
+    sampler.stop()
+    total_ms = e0.elapsed_time(e1)
+    total_ms_max = reduce_max(total_ms, dist)
+
+    # per-kernel durations: the events captured in the graph (its last replay), or an
+    # eager pass with the stream held back by a sleep so launches queue up first
+    if kev is not None:
+        ins = [kev[k][0].elapsed_time(kev[k][1]) for k in range(G)]
+        gat = [kev[k][1].elapsed_time(kev[k][2]) for k in range(G)]
+        how = "CUDA events captured in the graph, last replay of the timed region"
+    else:
+        ins, gat = eager_kernel_times(torch, gkr, case, sets, G, device)
+        how = "CUDA events around eager launches queued behind a device sleep"
+    clocks = sampler.summary(h0, h1)
+    return dict(case=case, K=K, total_ms=total_ms_max, ins_ms=float(np.mean(ins)),
+                gat_ms=float(np.mean(gat)), kernel_timing=how, clocks=clocks, T=T)
+
+
+def eager_kernel_times(torch, gkr, case, sets, n, device):
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    torch.cuda.synchronize(device)
+    torch.cuda._sleep(int(2e8))          # hold the stream while the launches queue up
+    for k in range(n):
+        step(gkr, case, sets[k % ROTATE], evs[k])
+    torch.cuda.synchronize(device)
+    return ([e[0].elapsed_time(e[1]) for e in evs], [e[1].elapsed_time(e[2]) for e in evs])
+
+
+def _gpu_id(torch, device) -> str:
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        return str(device.index or 0)
+
+
+def time_e2e(args, device, case):
+    """Same metric through the public API from pinned host buffers: every step
+    copies kv / slots / positions / indices to the device, inserts, gathers and
+    copies the gathered rows back, all inside the timed region."""
+    import torch
+    import gather_kv_rope_gb300 as gkr
+    pin = dict(
+        kv=torch.from_numpy(case.kv.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        slots=torch.from_numpy(case.slots).pin_memory(),
+        pos=torch.from_numpy(case.positions).pin_memory(),
+        idx=torch.from_numpy(case.indices).pin_memory())
+    out_h = torch.empty(case.indices.shape + (512,), dtype=torch.bfloat16).pin_memory()
+    d = {k: torch.empty_like(v, device=device) for k, v in pin.items()}
+    csc = torch.from_numpy(case.csc).to(device)
+    cache = gkr.alloc_cache(case.num_pages, case.block_size, case.record, device, fill=0)
+    out = torch.empty(case.indices.shape + (512,), dtype=torch.bfloat16, device=device)
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def one():
+        for k in pin:
+            d[k].copy_(pin[k], non_blocking=True)
+        gkr.kv_insert(d["kv"], cache, d["slots"], d["pos"], csc, case.block_size, case.record)
+        gkr.kv_gather(cache, d["idx"], out)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(5):
+        one()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.e2e_steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / args.e2e_steps
+    return {"value": case.num_tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "steps": args.e2e_steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "pinned host -> device copies, kv_insert, kv_gather, device -> pinned host"}
+
+
+def sweep(device, peak):
+    """Kernel-only timings of the larger workloads (each > L2 or rotated), median of
+    CUDA-event-timed launches after warm-up."""
+    import torch
+    import gather_kv_rope_gb300 as gkr
+    import workloads as W
+    res = {}
+
+    def timed(fn, sets, reps=20):
+        for k in range(3):
+            fn(sets[k % len(sets)])
+        torch.cuda.synchronize(device)
+        ts = []
+        for k in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn(sets[k % len(sets)])
+            b.record()
+            ts.append((a, b))
+        torch.cuda.synchronize(device)
+        return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+    for name, n_sets in (("insert_v4_65536", 3), ("insert_v41_262144", 1)):
+        case = getattr(W, name)()
+        sets = device_sets(case, device, n_sets)
+        ms = timed(lambda s: gkr.kv_insert(s["kv"], s["cache"], s["slots"], s["pos"], s["csc"],
+                                           case.block_size, case.record), sets)
+        b = insert_bytes(case.slots, case.record)
+        res[name] = {"kernel": "insert", "us": ms * 1e3, "tokens_per_s": case.num_tokens / (ms * 1e-3),
+                     "alg_bytes": b, "alg_gbs": b / (ms * 1e-3) / 1e9,
+                     "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
+        del sets
+        torch.cuda.empty_cache()
+
+    case = W.gather_v41_sparse()
+    kv = torch.from_numpy(case.kv.view(np.int16)).view(torch.bfloat16).to(device)
+    cache = gkr.alloc_cache(case.num_pages, 64, 528, device, fill=0)
+    gkr.kv_insert(kv, cache, torch.from_numpy(case.slots).to(device),
+                  torch.from_numpy(case.positions).to(device), torch.from_numpy(case.csc).to(device),
+                  64, 528)
+    del kv
+    idx = torch.from_numpy(case.indices).to(device)
+    outs = [torch.empty(case.indices.shape + (512,), dtype=torch.bfloat16, device=device)
+            for _ in range(2)]
+    ms = timed(lambda o: gkr.kv_gather(cache, idx, o), outs)
+    b = gather_bytes(case.indices, 528)
+    res["gather_v41_sparse"] = {"kernel": "gather", "us": ms * 1e3,
+                                "indices_per_s": case.indices.size / (ms * 1e-3), "alg_bytes": b,
+                                "alg_gbs": b / (ms * 1e-3) / 1e9,
+                                "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
+    return res
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_steps(case, tokens: int, steps: int):
+    """Run `steps` oracle steps (insert + gather of `tokens` tokens of the workload).
+    Returns seconds per step."""
+    import oracle
+    ps = oracle.page_stride(case.record, case.block_size)
+    cache = np.zeros(case.num_pages * ps, np.uint8)
+    kv, slots, pos = case.kv[:tokens], case.slots[:tokens], case.positions[:tokens]
+    idx = case.indices[:tokens]
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.insert(kv, cache, case.record, case.block_size, case.num_pages, ps, slots, pos,
+                      case.csc)
+        oracle.gather(cache, case.record, case.block_size, case.num_pages, ps, idx)
+    return (time.perf_counter() - t0) / steps
+
+
+def cpu_baseline(case, seconds: float) -> dict:
+    per = oracle_steps(case, 1024, 1)                 # calibrate on 1024 tokens
+    tok_s = 1024 / per
+    tokens = int(min(case.num_tokens, max(1024, tok_s * seconds / 3)))
+    steps = max(1, int(seconds / (tokens / tok_s)))
+    sec = oracle_steps(case, tokens, steps)
+    return {"value": tokens / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{steps} x insert+gather of the first {tokens} of the 16384 tokens "
+                      f"(single-threaded C oracle, {os.cpu_count()} host cores present)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import workloads as W
+    case = W.roundtrip_v41_16384()
+    per = oracle_steps(case, 512, 1)
+    budget = 150.0                                    # seconds for warm-up + timed steps
+    tokens = int(np.clip(512 / per * budget / max(1, args.steps + args.warmup), 16, 16384))
+    if args.warmup:
+        oracle_steps(case, tokens, args.warmup)
+    sec = oracle_steps(case, tokens, args.steps)
+    value = tokens / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "record": 528, "block_size": 64, "num_pages": 512,
+                       "tokens_per_step": tokens},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"insert+gather of the first {tokens} of the 16384 "
+                                       "tokens per step (single-threaded C oracle)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- main
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import gather_kv_rope_gb300 as gkr
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = init_dist(world, "nccl")
+    gkr.build()
+    gkr.lib()
+
+    peak, peak_src = measured_peaks()
+    r = time_roundtrip(args, device, dist)
+    case, K, T = r["case"], r["K"], r["T"]
+    ms_step = r["total_ms"] / K
+    value = world * K * T / (r["total_ms"] * 1e-3)
+
+    ib, gb = insert_bytes(case.slots, 528), gather_bytes(case.indices, 528)
+    kern = {"insert": {"us": r["ins_ms"] * 1e3, "alg_bytes": ib,
+                       "gbs": ib / (r["ins_ms"] * 1e-3) / 1e9},
+            "gather": {"us": r["gat_ms"] * 1e3, "alg_bytes": gb,
+                       "gbs": gb / (r["gat_ms"] * 1e-3) / 1e9}}
+    dom = "insert" if r["ins_ms"] >= r["gat_ms"] else "gather"
+    ach = kern[dom]["gbs"]
+    kname = {"insert": "insert_kernel", "gather": "gather_kernel"}[dom]
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "peak_source": peak_src,
+                "traffic": ncu_traffic(kname, WORKLOAD),
+                "alg_bytes_per_launch": kern[dom]["alg_bytes"],
+                "timing": r["kernel_timing"]}
+
+    out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+           "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "record": 528, "tokens": T, "block_size": 64,
+                      "num_pages": 512, "gathered": int(case.indices.size),
+                      "l2": f"inputs larger than L2: {ROTATE} rotating input sets",
+                      "launch": f"CUDA graph of {GRAPH_STEPS} steps, replayed {K // GRAPH_STEPS}x"},
+           "roofline": roofline, "kernels": kern, "gpu_launches": 2 * K,
+           "clocks": r["clocks"]}
+    if rank == 0:
+        out["e2e"] = time_e2e(args, device, case)
+        if not args.no_sweep and world == 1:
+            out["sweep"] = sweep(device, peak)
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

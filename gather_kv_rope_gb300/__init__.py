@@ -1,0 +1,22 @@
+"""GB300-native paged KV insert (RoPE + MXFP8) and dequant-gather.
+
+The compute runs in libgkr.so (hand-written sm_103a CUDA kernels behind a C ABI,
+declared in include/gkr.h); this package builds it in-tree and binds it with
+ctypes.  PyTorch supplies device memory and streams only.
+
+    kv_insert(kv, k_cache, slot_mapping, positions, cos_sin_cache, block_size, record)
+    kv_gather(k_cache, indices, out)
+"""
+from .build import build as _build_lib
+from ._binding import (CacheDesc, ERR_INDEX, ERR_POS, ERR_SLOT, GkrError, RECORDS, alloc_cache,
+                       cache_bytes, kv_gather, kv_insert, lib, library_path, page_stride,
+                       record_rows, status_string)
+
+__all__ = ["build", "kv_insert", "kv_gather", "page_stride", "record_rows", "alloc_cache",
+           "cache_bytes", "status_string", "GkrError", "CacheDesc", "RECORDS", "ERR_SLOT",
+           "ERR_POS", "ERR_INDEX", "lib", "library_path"]
+
+
+def build(force: bool = False):
+    """Compile libgkr.so for sm_103a in-tree (skipped when up to date)."""
+    return _build_lib(force=force)

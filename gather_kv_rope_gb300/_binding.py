@@ -1,0 +1,222 @@
+"""ctypes binding of libgkr.so: argument checks and marshalling only.
+
+Every step of the hot path runs in the library's CUDA kernels; this module
+only validates torch tensors, builds the cache descriptor and passes raw
+device pointers plus torch's current CUDA stream.  There is no fallback: if
+the library is not built, or a tensor is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from pathlib import Path
+
+import torch
+
+from .build import LIB
+
+GKR_OK = 0
+GKR_EINVAL = 1
+GKR_EUNSUPPORTED_RECORD = 2
+GKR_EBAD_PAGE_GEOMETRY = 3
+GKR_EALIGN = 4
+GKR_ECUDA = 5
+
+ERR_SLOT = 1
+ERR_POS = 2
+ERR_INDEX = 4
+
+RECORDS = (528, 584)
+HEAD_DIM = 512
+
+
+class GkrError(RuntimeError):
+    """A non-OK status returned by the C ABI."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"gkr status {status}: {message}")
+        self.status = status
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("record", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_pages", ctypes.c_int64), ("page_stride", ctypes.c_int64)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> Path:
+    return LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load libgkr.so (built in-tree by gather_kv_rope_gb300.build())."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not LIB.exists():
+                    raise RuntimeError(f"{LIB} is missing: run gather_kv_rope_gb300.build() "
+                                       "(the CUDA library is required; there is no fallback)")
+                L = ctypes.CDLL(str(LIB))
+                vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+                L.gkr_page_stride.argtypes, L.gkr_page_stride.restype = [i32, i32], i64
+                L.gkr_record_rows.argtypes = [i32, vp, vp, vp]
+                L.gkr_record_rows.restype = ctypes.c_int
+                L.gkr_kv_insert.argtypes = [vp, i64, vp, ctypes.POINTER(CacheDesc), vp, vp, vp,
+                                            i64, vp, vp]
+                L.gkr_kv_insert.restype = ctypes.c_int
+                L.gkr_kv_gather.argtypes = [vp, ctypes.POINTER(CacheDesc), vp, i64, vp, vp, vp]
+                L.gkr_kv_gather.restype = ctypes.c_int
+                L.gkr_status_string.argtypes, L.gkr_status_string.restype = [ctypes.c_int], \
+                    ctypes.c_char_p
+                L.gkr_last_cuda_error.argtypes, L.gkr_last_cuda_error.restype = [], i32
+                L.gkr_version.argtypes, L.gkr_version.restype = [], i32
+                _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gkr_status_string(status).decode()
+
+
+def _raise(status: int) -> None:
+    if status == GKR_OK:
+        return
+    msg = status_string(status)
+    if status == GKR_ECUDA:
+        msg += f" (cudaError {lib().gkr_last_cuda_error()})"
+        raise GkrError(status, msg)
+    raise ValueError(f"gkr status {status}: {msg}")
+
+
+def page_stride(record: int, block_size: int) -> int:
+    """Smallest valid page stride for a record and block size (-1 if unsupported)."""
+    return int(lib().gkr_page_stride(record, block_size))
+
+
+def record_rows(record: int) -> tuple[int, int, int]:
+    """(data row bytes, scale row bytes, page alignment) of a record."""
+    d, s, a = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _raise(lib().gkr_record_rows(record, ctypes.byref(d), ctypes.byref(s), ctypes.byref(a)))
+    return d.value, s.value, a.value
+
+
+def alloc_cache(num_pages: int, block_size: int, record: int, device="cuda",
+                page_stride_bytes: int | None = None, fill: int | None = None) -> torch.Tensor:
+    """Allocate a paged cache: a uint8 [num_pages, block_size, record] view whose
+    stride(0) is the page stride (padded to the record's alignment).  Inside a page
+    the bytes are laid out as data region then scale region, not row by row."""
+    ps = page_stride(record, block_size) if page_stride_bytes is None else int(page_stride_bytes)
+    if ps <= 0:
+        raise ValueError(f"unsupported record {record} / block_size {block_size}")
+    flat = torch.empty(num_pages * ps, dtype=torch.uint8, device=device)
+    if fill is not None:
+        flat.fill_(fill)
+    return torch.as_strided(flat, (num_pages, block_size, record), (ps, record, 1))
+
+
+def cache_bytes(k_cache: torch.Tensor) -> torch.Tensor:
+    """The flat byte view (num_pages * page_stride) behind a paged cache view."""
+    P = k_cache.shape[0]
+    return torch.as_strided(k_cache, (P * k_cache.stride(0),), (1,), k_cache.storage_offset())
+
+
+def _cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    if k_cache.dtype != torch.uint8 or k_cache.dim() != 3:
+        raise ValueError("k_cache must be a uint8 tensor [num_pages, block_size, record]")
+    P, bs, rec = k_cache.shape
+    if rec not in RECORDS:
+        raise ValueError(f"unsupported paged KV record width {rec} (expected 528 or 584)")
+    if k_cache.stride(2) != 1 or k_cache.stride(1) != rec:
+        raise ValueError("k_cache must have stride(2) == 1 and stride(1) == record")
+    return CacheDesc(rec, bs, P, k_cache.stride(0))
+
+
+def _check(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _same_cuda_device(*ts: torch.Tensor) -> torch.device:
+    dev = ts[0].device
+    if dev.type != "cuda":
+        raise ValueError("kv_insert / kv_gather need CUDA tensors (there is no CPU path)")
+    for t in ts[1:]:
+        if t is not None and t.device != dev:
+            raise ValueError(f"all tensors must be on {dev}; got one on {t.device}")
+    return dev
+
+
+def _check_err_flag(err_flag):
+    if err_flag is not None:
+        _check(err_flag.dtype == torch.int32 and err_flag.numel() >= 1 and err_flag.is_contiguous(),
+               "err_flag must be a contiguous int32 tensor with at least one element")
+
+
+def kv_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: torch.Tensor,
+              positions: torch.Tensor, cos_sin_cache: torch.Tensor, block_size: int,
+              record: int | None = None, err_flag: torch.Tensor | None = None) -> None:
+    """RoPE + MXFP8 quantise + paged insert, in place into k_cache.
+
+    kv             bf16 [tokens, 512], contiguous; not modified.
+    k_cache        uint8 [num_pages, block_size, record] (stride(0) = page stride).
+    slot_mapping   int64 [T] (T = number of tokens processed, <= tokens); -1 = skip.
+    positions      int64, contiguous, covering every kv row.
+    cos_sin_cache  fp32 [max_pos, 64], contiguous (cos 0..31 | sin 0..31).
+    block_size     must equal k_cache.size(1).
+    record         528 / 584, or None to take it from k_cache.size(2).
+    err_flag       optional int32 device tensor; error bits are OR-ed into element 0.
+    """
+    desc = _cache_desc(k_cache)
+    if record is not None:
+        _check(int(record) == desc.record,
+               f"record {record} does not match k_cache width {desc.record}")
+    _check(int(block_size) == desc.block_size,
+           f"block_size {block_size} != k_cache.size(1) {desc.block_size}")
+    _check(kv.dtype == torch.bfloat16 and kv.dim() == 2 and kv.shape[1] == HEAD_DIM
+           and kv.is_contiguous(), "kv must be a contiguous bf16 tensor [tokens, 512]")
+    _check(slot_mapping.dtype == torch.int64 and slot_mapping.dim() == 1
+           and slot_mapping.is_contiguous(), "slot_mapping must be a contiguous int64 [T] tensor")
+    _check(positions.dtype == torch.int64 and positions.dim() == 1 and positions.is_contiguous(),
+           "positions must be a contiguous int64 1-D tensor")
+    T = slot_mapping.shape[0]
+    _check(kv.shape[0] >= T, "kv has fewer rows than slot_mapping")
+    _check(positions.shape[0] >= kv.shape[0], "positions must cover every kv row")
+    _check(cos_sin_cache.dtype == torch.float32 and cos_sin_cache.dim() == 2
+           and cos_sin_cache.shape[1] == 64 and cos_sin_cache.is_contiguous(),
+           "cos_sin_cache must be a contiguous fp32 tensor [max_pos, 64]")
+    _check_err_flag(err_flag)
+    dev = _same_cuda_device(kv, k_cache, slot_mapping, positions, cos_sin_cache, err_flag)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        st = lib().gkr_kv_insert(_ptr(kv), T, _ptr(k_cache), ctypes.byref(desc),
+                                 _ptr(slot_mapping), _ptr(positions), _ptr(cos_sin_cache),
+                                 cos_sin_cache.shape[0], _ptr(err_flag), stream)
+    _raise(st)
+
+
+def kv_gather(k_cache: torch.Tensor, indices: torch.Tensor, out: torch.Tensor,
+              err_flag: torch.Tensor | None = None) -> torch.Tensor:
+    """Dequantise the records at `indices` into `out` (bf16 [*indices.shape, 512]).
+    An index of -1 writes zeros.  Returns out."""
+    desc = _cache_desc(k_cache)
+    _check(indices.dtype == torch.int32 and indices.is_contiguous(),
+           "indices must be a contiguous int32 tensor")
+    _check(out.dtype == torch.bfloat16 and out.is_contiguous()
+           and tuple(out.shape) == tuple(indices.shape) + (HEAD_DIM,),
+           "out must be a contiguous bf16 tensor of shape indices.shape + (512,)")
+    _check_err_flag(err_flag)
+    dev = _same_cuda_device(k_cache, indices, out, err_flag)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        st = lib().gkr_kv_gather(_ptr(k_cache), ctypes.byref(desc), _ptr(indices),
+                                 indices.numel(), _ptr(out), _ptr(err_flag), stream)
+    _raise(st)
+    return out

@@ -1,0 +1,140 @@
+// Host side of the C ABI declared in include/gkr.h: argument checks, geometry
+// and kernel dispatch.  No allocation, no synchronisation, no exceptions.
+#include "gkr.h"
+#include "launch.h"
+
+#include <cstdint>
+
+namespace {
+
+thread_local int32_t g_last_cuda_error = 0;
+
+struct RecordRows {
+    int32_t data, scale, align;
+};
+
+bool record_rows(int32_t record, RecordRows* r) {
+    // V4.1: 512 B e4m3 + 16 UE8M0; V4: 448 B e4m3 + 128 B bf16 + 7 UE8M0 + 1 pad.
+    // Pages align to 512 B (V4.1) and 576 B (V4) ("PR #56893 [DSv4.1] Store the whole
+    // KV in MXFP8 (FlashMLA V4.1 record)", section "功能与动机").
+    if (record == 528) { *r = {512, 16, 512}; return true; }
+    if (record == 584) { *r = {576, 8, 576}; return true; }
+    return false;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+gkr_status check_cache(const gkr_cache_desc* c, RecordRows* rows) {
+    if (c == nullptr) return GKR_EINVAL;
+    if (!record_rows(c->record, rows)) return GKR_EUNSUPPORTED_RECORD;
+    if (c->block_size <= 0 || c->block_size % 32 != 0) return GKR_EINVAL;
+    if (c->num_pages <= 0) return GKR_EINVAL;
+    if (c->num_pages > (INT64_C(0x7FFFFFFF) / c->block_size)) return GKR_EINVAL;  // slots < 2^31
+    const int64_t need = static_cast<int64_t>(c->block_size) * c->record;
+    if (c->page_stride < need || c->page_stride % rows->align != 0) return GKR_EBAD_PAGE_GEOMETRY;
+    if (c->page_stride > INT64_MAX / c->num_pages) return GKR_EBAD_PAGE_GEOMETRY;
+    return GKR_OK;
+}
+
+gkr_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return GKR_OK;
+    g_last_cuda_error = static_cast<int32_t>(e);
+    return GKR_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+GKR_API int64_t gkr_page_stride(int32_t record, int32_t block_size) {
+    RecordRows r;
+    if (!record_rows(record, &r) || block_size <= 0 || block_size % 32 != 0) return -1;
+    const int64_t need = static_cast<int64_t>(block_size) * record;
+    return (need + r.align - 1) / r.align * r.align;
+}
+
+GKR_API gkr_status gkr_record_rows(int32_t record, int32_t* data_row_bytes,
+                                   int32_t* scale_row_bytes, int32_t* page_align) {
+    RecordRows r;
+    if (!record_rows(record, &r)) return GKR_EUNSUPPORTED_RECORD;
+    if (data_row_bytes) *data_row_bytes = r.data;
+    if (scale_row_bytes) *scale_row_bytes = r.scale;
+    if (page_align) *page_align = r.align;
+    return GKR_OK;
+}
+
+GKR_API gkr_status gkr_kv_insert(const void* kv, int64_t num_tokens, void* k_cache,
+                                 const gkr_cache_desc* cache, const int64_t* slot_mapping,
+                                 const int64_t* positions, const float* cos_sin_cache,
+                                 int64_t max_pos, int32_t* err_flag, cudaStream_t stream) {
+    RecordRows rows;
+    const gkr_status st = check_cache(cache, &rows);
+    if (st != GKR_OK) return st;
+    if (num_tokens < 0 || max_pos <= 0) return GKR_EINVAL;
+    if (num_tokens == 0) return GKR_OK;
+    if (!kv || !k_cache || !slot_mapping || !positions || !cos_sin_cache) return GKR_EINVAL;
+    if (!aligned(kv, 16) || !aligned(k_cache, 16) || !aligned(cos_sin_cache, 16) ||
+        !aligned(slot_mapping, 8) || !aligned(positions, 8) || !aligned(err_flag, 4))
+        return GKR_EALIGN;
+
+    gkr::InsertParams p;
+    p.kv = kv;
+    p.num_tokens = num_tokens;
+    p.cache = static_cast<uint8_t*>(k_cache);
+    p.page_stride = cache->page_stride;
+    p.block_size = cache->block_size;
+    p.num_slots = static_cast<int32_t>(cache->num_pages * cache->block_size);
+    p.slots = slot_mapping;
+    p.positions = positions;
+    p.csc = cos_sin_cache;
+    p.max_pos = max_pos;
+    p.err = err_flag;
+    return cuda_status(cache->record == 528 ? gkr::launch_insert_v41(p, stream)
+                                            : gkr::launch_insert_v4(p, stream));
+}
+
+GKR_API gkr_status gkr_kv_gather(const void* k_cache, const gkr_cache_desc* cache,
+                                 const int32_t* indices, int64_t num_indices, void* out,
+                                 int32_t* err_flag, cudaStream_t stream) {
+    RecordRows rows;
+    const gkr_status st = check_cache(cache, &rows);
+    if (st != GKR_OK) return st;
+    if (num_indices < 0) return GKR_EINVAL;
+    if (num_indices == 0) return GKR_OK;
+    if (!k_cache || !indices || !out) return GKR_EINVAL;
+    if (!aligned(k_cache, 16) || !aligned(out, 16) || !aligned(indices, 4) ||
+        !aligned(err_flag, 4))
+        return GKR_EALIGN;
+
+    gkr::GatherParams p;
+    p.cache = static_cast<const uint8_t*>(k_cache);
+    p.page_stride = cache->page_stride;
+    p.block_size = cache->block_size;
+    p.num_slots = static_cast<int32_t>(cache->num_pages * cache->block_size);
+    p.indices = indices;
+    p.num_indices = num_indices;
+    p.out = out;
+    p.err = err_flag;
+    return cuda_status(cache->record == 528 ? gkr::launch_gather_v41(p, stream)
+                                            : gkr::launch_gather_v4(p, stream));
+}
+
+GKR_API const char* gkr_status_string(gkr_status status) {
+    switch (status) {
+        case GKR_OK: return "ok";
+        case GKR_EINVAL: return "invalid argument";
+        case GKR_EUNSUPPORTED_RECORD: return "unsupported record width (expected 528 or 584)";
+        case GKR_EBAD_PAGE_GEOMETRY:
+            return "bad page geometry (page_stride below block_size * record or not a "
+                   "multiple of the record's page alignment)";
+        case GKR_EALIGN: return "misaligned pointer";
+        case GKR_ECUDA: return "CUDA launch error";
+    }
+    return "unknown status";
+}
+
+GKR_API int32_t gkr_last_cuda_error(void) { return g_last_cuda_error; }
+
+GKR_API int32_t gkr_version(void) { return 10000; }
+
+}  // extern "C"

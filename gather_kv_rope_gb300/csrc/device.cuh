@@ -1,0 +1,204 @@
+// Device helpers shared by the insert and gather kernels (sm_103a).
+//
+// Lane layout used by every kernel: one warp owns one 512-dim token row.
+// Lane L holds two 8-dim chunks, A = dims [8L, 8L+8) and B = dims
+// [256+8L, 256+8L+8), so each warp-wide 16-byte bf16 access (or 8-byte e4m3
+// access) covers one contiguous 512-byte (256-byte) span: fully coalesced
+// 128-byte lines for loads and stores.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+namespace gkr {
+
+constexpr int kWarpsPerBlock = 8;
+constexpr int kThreads = kWarpsPerBlock * 32;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// ---------------------------------------------------------------- memory access
+
+// Streaming 16-byte load (read once: evict-first in L1 and L2).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+// Read-only 16 / 8-byte loads through the non-coherent path.
+__device__ __forceinline__ uint4 ld_ro16(const void* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ uint2 ld_ro8(const void* p) {
+    return __ldg(reinterpret_cast<const uint2*>(p));
+}
+__device__ __forceinline__ float4 ld_ro_f4(const float* p) {
+    return __ldg(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ void st16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+__device__ __forceinline__ void st8(void* p, uint2 v) { *reinterpret_cast<uint2*>(p) = v; }
+// Streaming 16-byte store (written once, not re-read by this kernel).
+__device__ __forceinline__ void st_stream16(void* p, uint4 v) {
+    __stcs(reinterpret_cast<uint4*>(p), v);
+}
+
+// ---------------------------------------------------------------- bf16 <-> fp32
+
+// Eight bf16 values packed in a uint4 -> fp32 (exact: bf16 is the top half of fp32).
+__device__ __forceinline__ void unpack_bf16x8(const uint4 v, float f[8]) {
+    f[0] = __uint_as_float(v.x << 16);
+    f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(v.y << 16);
+    f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    f[4] = __uint_as_float(v.z << 16);
+    f[5] = __uint_as_float(v.z & 0xFFFF0000u);
+    f[6] = __uint_as_float(v.w << 16);
+    f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+// Two fp32 -> packed bf16x2 (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------- RoPE
+
+// Rotate four adjacent pairs (f[0],f[1]) .. (f[6],f[7]) by (c[i], s[i]):
+// even' = e*c - o*s, odd' = o*c + e*s; every product and sum is a separately
+// rounded fp32 operation (the _rn intrinsics are never contracted into FMA).
+__device__ __forceinline__ void rope4(float f[8], const float4 c, const float4 s) {
+    const float cc[4] = {c.x, c.y, c.z, c.w};
+    const float ss[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float e = f[2 * i], o = f[2 * i + 1];
+        f[2 * i] = __fsub_rn(__fmul_rn(e, cc[i]), __fmul_rn(o, ss[i]));
+        f[2 * i + 1] = __fadd_rn(__fmul_rn(o, cc[i]), __fmul_rn(e, ss[i]));
+    }
+}
+
+// ---------------------------------------------------------------- MXFP8 encode
+
+__device__ __forceinline__ float amax8(const float f[8]) {
+    float m = fabsf(f[0]);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    return m;
+}
+
+// UE8M0 scale byte for a block maximum: clamp(ceil(log2(amax / 448)), -127, 127) + 127,
+// computed exactly from the fp32 fields of amax.  With amax = (1 + M/2^23) * 2^(E-127)
+// and 448 = 1.75 * 2^8: amax / 448 = ((1 + M/2^23) / 1.75) * 2^(E-135), and the ratio
+// in brackets lies in [0.57, 1.15), so the ceiling is E - 135 plus one exactly when
+// 1 + M/2^23 > 1.75, i.e. M > 0x600000.  Adding the bias 127 gives E - 8 + [M > 0x600000];
+// zero and subnormal maxima fall below the clamp and give byte 0.  Finite inputs never
+// exceed byte 247.  The byte is a non-decreasing function of amax, so the byte of a
+// block is the maximum of the bytes of its parts.
+__device__ __forceinline__ uint32_t ue8m0_byte(float amax) {
+    const uint32_t b = __float_as_uint(amax);
+    const int e = int(b >> 23) - 8 + int((b & 0x7FFFFFu) > 0x600000u);
+    return e > 0 ? uint32_t(e) : 0u;
+}
+
+// 2^(127 - byte) as fp32 (exact; byte <= 247 keeps it a normal number).
+__device__ __forceinline__ float inv_scale(uint32_t byte) {
+    return __uint_as_float((254u - byte) << 23);
+}
+
+// Four fp32 values (already divided by the block scale) -> four e4m3 bytes,
+// round to nearest even with saturation to +-448, first value in the low byte.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+// Quantise an 8-value chunk with the block's scale byte -> 8 e4m3 bytes.
+__device__ __forceinline__ uint2 quantise8(const float f[8], uint32_t byte) {
+    const float k = inv_scale(byte);
+    uint2 q;
+    q.x = e4m3x4(__fmul_rn(f[0], k), __fmul_rn(f[1], k), __fmul_rn(f[2], k), __fmul_rn(f[3], k));
+    q.y = e4m3x4(__fmul_rn(f[4], k), __fmul_rn(f[5], k), __fmul_rn(f[6], k), __fmul_rn(f[7], k));
+    return q;
+}
+
+// ---------------------------------------------------------------- MXFP8 decode
+
+// d = a * b on packed bf16x2, rounded to nearest even (subnormals kept).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Packed bf16x2 of 2^(byte - 127) for a UE8M0 byte in [0, 254]; byte 0 is the
+// bf16 subnormal 2^-127 (0x0040).
+__device__ __forceinline__ uint32_t ue8m0_to_bf16x2(uint32_t byte) {
+    const uint32_t h = byte ? (byte << 7) : 0x0040u;
+    return h | (h << 16);
+}
+
+constexpr uint32_t kBf16NaN = 0x7FC0u;
+constexpr uint32_t kTwoPow120x2 = 0x7B807B80u;  // bf16 2^120 in both halves
+
+// Two e4m3 codes (bytes sel of w) -> bf16x2 of e4m3 * 2^(byte-127).
+// An e4m3 byte s.EEEE.MMM moved to bf16 bit positions s.0000EEEE.MMM0000 reads as
+// (1 + M/8) * 2^(E-127) (E >= 1) or M * 2^-129 (E = 0): in both cases the e4m3 value
+// times 2^-120.  Multiplying by 2^120 is exact and restores the e4m3 value; the second
+// multiply by the power-of-two scale rounds once, to nearest even.  NaN codes are
+// handled by the caller.
+template <int kHigh>
+__device__ __forceinline__ uint32_t dequant2(uint32_t w, uint32_t scale2) {
+    const uint32_t h = __byte_perm(w, 0u, kHigh ? 0x3424u : 0x1404u);  // codes -> bytes 1, 3
+    const uint32_t bits = (h & 0x80008000u) | ((h >> 4) & 0x07F007F0u);
+    return bf16x2_mul(bf16x2_mul(bits, kTwoPow120x2), scale2);
+}
+
+// Bytes of w whose low 7 bits are all ones (the e4m3 NaN codes) -> 0x80 in that byte.
+__device__ __forceinline__ uint32_t e4m3_nan_bytes(uint32_t w) {
+    return ((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+}
+
+// Replace the bf16 halves of o[0..1] (codes 0..3 of a word) flagged in nanmask by NaN.
+__device__ __forceinline__ void patch_nan(uint32_t nanmask, uint32_t& o01, uint32_t& o23) {
+    if (nanmask & 0x00000080u) o01 = (o01 & 0xFFFF0000u) | kBf16NaN;
+    if (nanmask & 0x00008000u) o01 = (o01 & 0x0000FFFFu) | (kBf16NaN << 16);
+    if (nanmask & 0x00800000u) o23 = (o23 & 0xFFFF0000u) | kBf16NaN;
+    if (nanmask & 0x80000000u) o23 = (o23 & 0x0000FFFFu) | (kBf16NaN << 16);
+}
+
+// Eight e4m3 codes with one UE8M0 scale byte -> eight bf16 (uint4).
+__device__ __forceinline__ uint4 dequant8(const uint2 c, uint32_t byte) {
+    uint4 o;
+    if (byte == 255u) {  // the UE8M0 NaN
+        const uint32_t n = kBf16NaN | (kBf16NaN << 16);
+        return make_uint4(n, n, n, n);
+    }
+    const uint32_t s2 = ue8m0_to_bf16x2(byte);
+    o.x = dequant2<0>(c.x, s2);
+    o.y = dequant2<1>(c.x, s2);
+    o.z = dequant2<0>(c.y, s2);
+    o.w = dequant2<1>(c.y, s2);
+    const uint32_t n0 = e4m3_nan_bytes(c.x), n1 = e4m3_nan_bytes(c.y);
+    if (n0 | n1) {
+        patch_nan(n0, o.x, o.y);
+        patch_nan(n1, o.z, o.w);
+    }
+    return o;
+}
+
+// Byte k (0..15) of a 16-byte value.
+__device__ __forceinline__ uint32_t byte_of(const uint4 v, int k) {
+    const uint32_t w = (k < 8) ? ((k < 4) ? v.x : v.y) : ((k < 12) ? v.z : v.w);
+    return (w >> (8 * (k & 3))) & 0xFFu;
+}
+__device__ __forceinline__ uint32_t byte_of(const uint2 v, int k) {
+    const uint32_t w = (k < 4) ? v.x : v.y;
+    return (w >> (8 * (k & 3))) & 0xFFu;
+}
+
+__device__ __forceinline__ void report(int32_t* err, int32_t bits) {
+    if (err != nullptr) atomicOr(err, bits);
+}
+
+}  // namespace gkr

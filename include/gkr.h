@@ -1,0 +1,170 @@
+/*
+ * gkr.h -- C ABI of libgkr.so: the DeepSeek-V4.1 / V4 paged KV-cache hot path
+ * on NVIDIA GB300 (sm_103a).
+ *
+ *   gkr_kv_insert: bf16 latent [T, 512] -> RoPE on dims 448..511 -> MXFP8
+ *                  (e4m3 + UE8M0) encode -> scatter into a paged cache;
+ *   gkr_kv_gather: the inverse: dequantise listed slots back to bf16 [N, 512].
+ *
+ * Operations follow these passages (page title, section):
+ *   "PR #56893 [DSv4.1] Store the whole KV in MXFP8 (FlashMLA V4.1 record)",
+ *     section "功能与动机" (the two records and their page alignment), section
+ *     "关键源码片段" (the fused_compress_quant_cache.py insert kernel: skip on
+ *     slot < 0, page/row addressing, rotation, block scale, e4m3 cast), section
+ *     "实现拆解" item 4 (the dequant-gather parameterised by record);
+ *   "PR #56441 [Perf][DSpark] KV-only context insertion across V4.1 cache
+ *     formats", section "实现拆解" items 1-2 (the KV-only insert contract:
+ *     kv bf16 [tokens, 512], int64 slots and positions, fp32 cos_sin_cache
+ *     [max_pos, 64], paged cache written in place);
+ *   FlashMLA overview page, DSA section (index -1 marks an invalid entry).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device;
+ *     the caller owns and allocates all memory.  The library allocates
+ *     nothing, never synchronises the stream and keeps no per-call state.
+ *   - Work is enqueued on `stream` (0 = the legacy default stream); results
+ *     are visible after the stream's work completes.
+ *   - Host-side argument checks run before anything is enqueued; on failure
+ *     nothing is enqueued and a non-zero gkr_status is returned.  No C++
+ *     exception crosses this boundary.
+ *   - Out-of-range data found on the device (a slot past the cache, a
+ *     position outside the cos/sin table, an index < -1 or past the cache) is
+ *     never dereferenced: the token is skipped / the output row is zeroed, and
+ *     the matching GKR_ERR_* bit is OR-ed into *err_flag when err_flag is not
+ *     NULL.  The kernels never trap.
+ */
+#ifndef GKR_H
+#define GKR_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GKR_API __attribute__((visibility("default")))
+#else
+#define GKR_API
+#endif
+
+typedef enum gkr_status {
+    GKR_OK = 0,
+    GKR_EINVAL = 1,               /* null pointer, negative count, bad block size, ... */
+    GKR_EUNSUPPORTED_RECORD = 2,  /* record width not 528 or 584                        */
+    GKR_EBAD_PAGE_GEOMETRY = 3,   /* page stride too small or not a multiple of align   */
+    GKR_EALIGN = 4,               /* a pointer is not aligned as documented             */
+    GKR_ECUDA = 5                 /* the launch failed; see gkr_last_cuda_error()       */
+} gkr_status;
+
+/* Bits OR-ed into *err_flag by the kernels. */
+#define GKR_ERR_SLOT 1   /* insert: slot >= num_pages * block_size (token skipped)      */
+#define GKR_ERR_POS 2    /* insert: position < 0 or >= max_pos (token skipped)           */
+#define GKR_ERR_INDEX 4  /* gather: index < -1 or >= num_pages * block_size (row zeroed) */
+
+/*
+ * Paged cache geometry.  The cache is num_pages pages, page p starting at byte
+ * p * page_stride.  A page holds a data region (block_size rows of D bytes)
+ * followed by a scale region (block_size rows of S bytes); the remaining
+ * page_stride - block_size * record bytes are padding and are never touched.
+ *   record 528 (V4.1): D = 512 (e4m3 of dims 0..511), S = 16 (one UE8M0 byte
+ *                      per 32-dim block); page alignment 512.
+ *   record 584 (V4):   D = 576 (448 e4m3 bytes for dims 0..447, then dims
+ *                      448..511 as little-endian bf16), S = 8 (7 UE8M0 bytes
+ *                      per 64-dim block + 1 pad byte 0x00); page alignment 576.
+ * A slot s lives in page s / block_size, row s % block_size.
+ * Requirements: record in {528, 584}; block_size > 0 and a multiple of 32;
+ * num_pages > 0; page_stride >= block_size * record and a multiple of the
+ * record's page alignment; num_pages * block_size < 2^31.
+ */
+typedef struct gkr_cache_desc {
+    int32_t record;
+    int32_t block_size;
+    int64_t num_pages;
+    int64_t page_stride;
+} gkr_cache_desc;
+
+/*
+ * Smallest valid page stride: block_size * record rounded up to the record's
+ * page alignment (512 for 528, 576 for 584).  Returns -1 for an unsupported
+ * record or a block_size that is not a positive multiple of 32.
+ */
+GKR_API int64_t gkr_page_stride(int32_t record, int32_t block_size);
+
+/*
+ * Row sizes of a record: data row bytes, scale row bytes and page alignment.
+ * Any output pointer may be NULL.  GKR_EUNSUPPORTED_RECORD for other widths.
+ */
+GKR_API gkr_status gkr_record_rows(int32_t record, int32_t *data_row_bytes,
+                                   int32_t *scale_row_bytes, int32_t *page_align);
+
+/*
+ * kv_insert: for each token t in [0, num_tokens):
+ *   s = slot_mapping[t]; s < 0 -> skip the token (nothing read or written);
+ *   x = kv[t, 0..511] widened to fp32;
+ *   for pair j = 0..31 with c = cos_sin_cache[positions[t], j] and
+ *   n = cos_sin_cache[positions[t], 32 + j]:
+ *       x[448+2j], x[449+2j] = x[448+2j]*c - x[449+2j]*n, x[449+2j]*c + x[448+2j]*n
+ *     (fp32, each product and sum rounded to nearest even, no fused multiply-add);
+ *   each block (32 dims for 528, 64 NoPE dims for 584) gets the scale byte
+ *     b = clamp(ceil(log2(amax / 448)), -127, 127) + 127 (amax 0 -> b = 0),
+ *     and each value is stored as e4m3(x / 2^(b - 127)), round to nearest even,
+ *     saturating at +-448;
+ *   for 584 the rotated dims 448..511 are stored as bf16 (round to nearest even).
+ *
+ * kv             device, bf16 [num_tokens, 512] row-major, 16-byte aligned; read only.
+ * num_tokens     >= 0; 0 enqueues nothing (other pointers may then be NULL).
+ * k_cache        device, the cache described by *cache, 16-byte aligned; only the
+ *                data and scale rows of the slots written are modified.
+ * cache          host pointer to the geometry (read during the call only).
+ * slot_mapping   device, int64 [num_tokens]; slots must be distinct (duplicate
+ *                non-negative slots race and are outside the contract).
+ * positions      device, int64 [num_tokens]; row of cos_sin_cache for each token.
+ * cos_sin_cache  device, fp32 [max_pos, 64] row-major (cos 0..31 | sin 0..31),
+ *                16-byte aligned.
+ * max_pos        > 0, rows in cos_sin_cache.
+ * err_flag       device int32 or NULL; GKR_ERR_SLOT / GKR_ERR_POS bits are OR-ed in.
+ * stream         CUDA stream to enqueue on.
+ */
+GKR_API gkr_status gkr_kv_insert(const void *kv, int64_t num_tokens, void *k_cache,
+                                 const gkr_cache_desc *cache, const int64_t *slot_mapping,
+                                 const int64_t *positions, const float *cos_sin_cache,
+                                 int64_t max_pos, int32_t *err_flag, cudaStream_t stream);
+
+/*
+ * kv_gather: for each i in [0, num_indices):
+ *   indices[i] == -1 -> out[i, :] = +0 (bf16 0x0000);
+ *   otherwise slot s = indices[i]:
+ *     528: out[i, d] = bf16(e4m3(data[d]) * 2^(scale[d / 32] - 127));
+ *     584: d < 448 as above with scale[d / 64]; d >= 448 copies the stored bf16.
+ *   The product is exact in fp32 and rounded once to bf16 (nearest even,
+ *   subnormals kept).  An e4m3 NaN code (0x7F / 0xFF) or scale byte 255 (the
+ *   UE8M0 NaN) yields the bf16 NaN 0x7FC0.
+ *
+ * k_cache      device, the cache described by *cache, 16-byte aligned; read only.
+ * cache        host pointer to the geometry.
+ * indices      device, int32 [num_indices].
+ * num_indices  >= 0; 0 enqueues nothing.
+ * out          device, bf16 [num_indices, 512] row-major, 16-byte aligned.
+ * err_flag     device int32 or NULL; GKR_ERR_INDEX is OR-ed in.
+ * stream       CUDA stream to enqueue on.
+ */
+GKR_API gkr_status gkr_kv_gather(const void *k_cache, const gkr_cache_desc *cache,
+                                 const int32_t *indices, int64_t num_indices, void *out,
+                                 int32_t *err_flag, cudaStream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+GKR_API const char *gkr_status_string(gkr_status status);
+
+/* The cudaError_t of the last GKR_ECUDA returned on this host thread (0 if none). */
+GKR_API int32_t gkr_last_cuda_error(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+GKR_API int32_t gkr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GKR_H */

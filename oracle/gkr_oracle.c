@@ -96,10 +96,19 @@ ORACLE_EXPORT uint8_t oracle_e4m3_encode(double y)
     }
     quantum = ldexp(1.0, k - 3);
     v = nearbyint(a / quantum) * quantum; /* a / quantum is exact; RNE */
-    /* Find the code whose value is v. */
-    for (code = 0; code <= 0x7E; code++)
-        if (oracle_e4m3_value((uint8_t)code) == v)
-            return (uint8_t)(sign | code);
+    /* Find the code whose value is v (values of codes 0x00..0x7E, decoded once). */
+    {
+        static double value_of[0x7F];
+        static int filled = 0;
+        if (!filled) {
+            for (code = 0; code <= 0x7E; code++)
+                value_of[code] = oracle_e4m3_value((uint8_t)code);
+            filled = 1;
+        }
+        for (code = 0; code <= 0x7E; code++)
+            if (value_of[code] == v)
+                return (uint8_t)(sign | code);
+    }
     return (uint8_t)(sign | 0x7F); /* unreachable for |y| < 448 */
 }
 

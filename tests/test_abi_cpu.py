@@ -1,0 +1,167 @@
+"""The C ABI on the CPU: libgkr.so loads, exports every symbol include/gkr.h
+declares, and its host-side checks return the documented status codes before
+anything touches a GPU (no compute calls here)."""
+from __future__ import annotations
+
+import ctypes
+import re
+import subprocess
+from pathlib import Path
+
+import pytest
+import torch
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "gkr.h"
+
+
+def declared_symbols() -> set[str]:
+    text = HEADER.read_text()
+    return set(re.findall(r"GKR_API\s+[\w\s\*]*?\b(gkr_\w+)\s*\(", text))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    assert {"gkr_kv_insert", "gkr_kv_gather", "gkr_page_stride", "gkr_record_rows",
+            "gkr_status_string", "gkr_last_cuda_error", "gkr_version"} <= syms
+
+
+def test_library_exports_every_declared_symbol(gkr):
+    lib = gkr.lib()
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", str(gkr.library_path())],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l and "gkr_" in l}
+    assert declared_symbols() <= exported
+    # nothing else of ours leaks out of the library (hidden visibility)
+    assert {s for s in exported if s.startswith("gkr")} == declared_symbols()
+
+
+def test_page_stride_and_rows(gkr):
+    assert gkr.page_stride(528, 64) == 33792
+    assert gkr.page_stride(584, 64) == 37440
+    assert gkr.page_stride(528, 32) == 16896
+    assert gkr.page_stride(584, 32) == 19008
+    assert gkr.page_stride(500, 64) == -1
+    assert gkr.page_stride(528, 48) == -1
+    assert gkr.page_stride(528, 0) == -1
+    assert gkr.record_rows(528) == (512, 16, 512)
+    assert gkr.record_rows(584) == (576, 8, 576)
+    with pytest.raises(ValueError):
+        gkr.record_rows(512)
+    assert gkr.lib().gkr_version() == 10000
+    assert gkr.status_string(0) == "ok"
+
+
+# --- host-side checks through the raw ABI (fake device pointers never reach a kernel)
+
+A16 = 0x10000          # 16-byte aligned fake pointers: checks must fail before any launch
+A16b = 0x20000
+
+
+def desc(gkr, record=528, bs=64, pages=4, ps=None):
+    return gkr.CacheDesc(record, bs, pages, gkr.page_stride(record, bs) if ps is None else ps)
+
+
+def insert(gkr, d, T=8, kv=A16, cache=A16b, slots=A16, pos=A16, csc=A16, max_pos=16, err=None):
+    return gkr.lib().gkr_kv_insert(kv, T, cache, None if d is None else ctypes.byref(d),
+                                   slots, pos, csc, max_pos, err, None)
+
+
+def gather(gkr, d, N=8, cache=A16b, idx=A16, out=A16, err=None):
+    return gkr.lib().gkr_kv_gather(cache, None if d is None else ctypes.byref(d), idx, N,
+                                   out, err, None)
+
+
+@pytest.mark.parametrize("op", [insert, gather])
+def test_geometry_checks(gkr, op):
+    assert op(gkr, None) == 1                                        # null descriptor
+    assert op(gkr, desc(gkr, record=512)) == 2                       # unsupported record
+    assert op(gkr, desc(gkr, bs=48)) == 1                            # block size % 32
+    assert op(gkr, desc(gkr, bs=0)) == 1
+    assert op(gkr, desc(gkr, pages=0)) == 1
+    assert op(gkr, desc(gkr, pages=2 ** 30)) == 1                    # slots >= 2^31
+    assert op(gkr, desc(gkr, ps=33792 - 512)) == 3                   # stride too small
+    assert op(gkr, desc(gkr, ps=33792 + 16)) == 3                    # not a multiple of 512
+    assert op(gkr, desc(gkr, record=584, ps=37440 + 512)) == 3       # not a multiple of 576
+
+
+def test_insert_argument_checks(gkr):
+    d = desc(gkr)
+    assert insert(gkr, d, T=-1) == 1
+    assert insert(gkr, d, max_pos=0) == 1
+    assert insert(gkr, d, T=0, kv=None, cache=None, slots=None, pos=None, csc=None) == 0
+    assert insert(gkr, d, kv=None) == 1
+    assert insert(gkr, d, csc=None) == 1
+    assert insert(gkr, d, kv=A16 + 8) == 4                           # kv not 16-aligned
+    assert insert(gkr, d, cache=A16 + 4) == 4
+    assert insert(gkr, d, csc=A16 + 8) == 4
+    assert insert(gkr, d, slots=A16 + 4) == 4
+    assert insert(gkr, d, err=A16 + 2) == 4
+
+
+def test_gather_argument_checks(gkr):
+    d = desc(gkr)
+    assert gather(gkr, d, N=-1) == 1
+    assert gather(gkr, d, N=0, cache=None, idx=None, out=None) == 0
+    assert gather(gkr, d, out=None) == 1
+    assert gather(gkr, d, out=A16 + 8) == 4
+    assert gather(gkr, d, idx=A16 + 2) == 4
+    assert gather(gkr, d, cache=A16 + 8) == 4
+
+
+def test_status_strings(gkr):
+    for s in range(6):
+        assert gkr.status_string(s)
+    assert "unknown" in gkr.status_string(99)
+
+
+# --- Python binding checks (raise before calling into the library)
+
+def _cpu_args(T=4, record=528, bs=32):
+    kv = torch.zeros(T, 512, dtype=torch.bfloat16)
+    cache = torch.as_strided(torch.zeros(2 * 16896, dtype=torch.uint8), (2, bs, record),
+                             (16896, record, 1))
+    slots = torch.zeros(T, dtype=torch.int64)
+    pos = torch.zeros(T, dtype=torch.int64)
+    csc = torch.zeros(8, 64, dtype=torch.float32)
+    return kv, cache, slots, pos, csc
+
+
+def test_binding_rejects_bad_tensors(gkr):
+    kv, cache, slots, pos, csc = _cpu_args()
+    with pytest.raises(ValueError, match="kv must be"):
+        gkr.kv_insert(kv.float(), cache, slots, pos, csc, 32)
+    with pytest.raises(ValueError, match="kv must be"):
+        gkr.kv_insert(kv[:, :256], cache, slots, pos, csc, 32)
+    with pytest.raises(ValueError, match="slot_mapping"):
+        gkr.kv_insert(kv, cache, slots.int(), pos, csc, 32)
+    with pytest.raises(ValueError, match="cos_sin_cache"):
+        gkr.kv_insert(kv, cache, slots, pos, csc.double(), 32)
+    with pytest.raises(ValueError, match="block_size"):
+        gkr.kv_insert(kv, cache, slots, pos, csc, 64)
+    with pytest.raises(ValueError, match="record"):
+        gkr.kv_insert(kv, cache, slots, pos, csc, 32, record=584)
+    with pytest.raises(ValueError, match="width"):
+        bad = torch.zeros(2, 32, 512, dtype=torch.uint8)
+        gkr.kv_insert(kv, bad, slots, pos, csc, 32)
+    with pytest.raises(ValueError, match="positions must cover"):
+        gkr.kv_insert(kv, cache, slots, pos[:2], csc, 32)
+    with pytest.raises(ValueError, match="CUDA"):
+        gkr.kv_insert(kv, cache, slots, pos, csc, 32)          # CPU tensors: no CPU path
+    idx = torch.zeros(3, dtype=torch.int32)
+    with pytest.raises(ValueError, match="out must be"):
+        gkr.kv_gather(cache, idx, torch.zeros(3, 256, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="indices"):
+        gkr.kv_gather(cache, idx.long(), torch.zeros(3, 512, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="CUDA"):
+        gkr.kv_gather(cache, idx, torch.zeros(3, 512, dtype=torch.bfloat16))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    import gather_kv_rope_gb300._binding as b
+    monkeypatch.setattr(b, "LIB", tmp_path / "nope.so")
+    monkeypatch.setattr(b, "_lib", None)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        b.lib()
