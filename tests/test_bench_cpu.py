@@ -1,0 +1,74 @@
+"""Host logic of bench.py on the CPU: byte accounting, the max-over-ranks timing
+reduction with two gloo ranks, and the reference (oracle) arm's JSON line."""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import subprocess
+import sys
+from pathlib import Path
+
+import numpy as np
+import torch.multiprocessing as mp
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+def test_algorithmic_bytes():
+    import bench
+    slots = np.array([-1, 0, 5, -1, 7], np.int64)
+    assert bench.insert_bytes(slots, 528) == 5 * 16 + 3 * (1024 + 528)
+    assert bench.insert_bytes(slots, 584) == 5 * 16 + 3 * (1024 + 584)
+    idx = np.array([[-1, 2], [3, -1]], np.int32)
+    assert bench.gather_bytes(idx, 528) == 4 * 1028 + 2 * 528
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, str(ROOT))
+    import bench
+    dist = bench.init_dist(world, "gloo")
+    bench.barrier(dist)
+    got = bench.reduce_max(10.0 + 5.0 * rank, dist)
+    q.put((rank, got))
+    dist.destroy_process_group()
+
+
+def test_reduce_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in ps)
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == {0: 15.0, 1: 15.0}
+
+
+def test_reduce_max_single_process_is_identity():
+    import bench
+    assert bench.reduce_max(3.5, None) == 3.5
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference",
+                        "--steps", "2", "--warmup", "1"], capture_output=True, text=True,
+                       cwd=ROOT, timeout=600)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["config"]["workload"] == "roundtrip_v41_16384"
