@@ -11,9 +11,10 @@ Prints ONE JSON line on rank 0.  Timing: W eager warm-up steps, then K steps run
 as replays of a captured CUDA graph of G steps, bracketed by a barrier and a
 device synchronise on both sides, timed with CUDA events on the launching stream
 (max over ranks).  Six input sets (~300 MB together, more than the 126 MB L2)
-rotate so no step finds its inputs in L2.  Per-kernel durations come from
-events captured inside the graph (last replay), or from a separate eager pass
-when torch cannot capture timing events.
+rotate so no step finds its inputs in L2.  Per-kernel durations come from a
+second graph of the same steps with event nodes around every kernel (replayed
+after the timed region), or from an eager pass when torch cannot capture
+timing events.
 
 `--impl reference` times the CPU oracle (test infrastructure) on the same
 workload, a bounded sample of tokens per step, on the host cores.
@@ -281,19 +282,24 @@ def time_roundtrip(args, device, dist):
     G = GRAPH_STEPS
     K = max(G, (args.steps + G - 1) // G * G)       # K is rounded up to whole graphs
     replays = K // G
-    external = _supports_external_events(torch)
-    kev = [[_timing_event(torch, external) for _ in range(3)] for _ in range(G)] \
-        if external else None
-    graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream(device)
     cap.wait_stream(torch.cuda.current_stream(device))
     with torch.cuda.stream(cap):
         step(gkr, case, sets[0])                    # side-stream warm-up before capture
     torch.cuda.current_stream(device).wait_stream(cap)
     torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()                  # the timed graph: kernels only
     with torch.cuda.graph(graph):
         for k in range(G):
-            step(gkr, case, sets[k % ROTATE], None if kev is None else kev[k])
+            step(gkr, case, sets[k % ROTATE])
+    external = _supports_external_events(torch)
+    kev = None
+    if external:                                    # same steps with event nodes per kernel
+        kev = [[_timing_event(torch, True) for _ in range(3)] for _ in range(G)]
+        graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ev):
+            for k in range(G):
+                step(gkr, case, sets[k % ROTATE], kev[k])
     graph.replay()                                   # one untimed replay
     torch.cuda.synchronize(device)
 
@@ -314,12 +320,18 @@ def time_roundtrip(args, device, dist):
     total_ms = e0.elapsed_time(e1)
     total_ms_max = reduce_max(total_ms, dist)
 
-    # per-kernel durations: the events captured in the graph (its last replay), or an
+    # per-kernel durations: the event graph (each kernel bracketed by event nodes, so
+    # no launch overlap between kernels) replayed right after the timed region, or an
     # eager pass with the stream held back by a sleep so launches queue up first
     if kev is not None:
-        ins = [kev[k][0].elapsed_time(kev[k][1]) for k in range(G)]
-        gat = [kev[k][1].elapsed_time(kev[k][2]) for k in range(G)]
-        how = "CUDA events captured in the graph, last replay of the timed region"
+        ins, gat = [], []
+        for _ in range(5):
+            graph_ev.replay()
+            torch.cuda.synchronize(device)
+            ins += [kev[k][0].elapsed_time(kev[k][1]) for k in range(G)]
+            gat += [kev[k][1].elapsed_time(kev[k][2]) for k in range(G)]
+        how = (f"CUDA events captured around every kernel in a graph of the same {G} steps, "
+               "5 replays after the timed region")
     else:
         ins, gat = eager_kernel_times(torch, gkr, case, sets, G, device)
         how = "CUDA events around eager launches queued behind a device sleep"

@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
                     ctypes.c_char_p
                 L.gkr_last_cuda_error.argtypes, L.gkr_last_cuda_error.restype = [], i32
                 L.gkr_version.argtypes, L.gkr_version.restype = [], i32
+                L.gkr_set_pdl.argtypes, L.gkr_set_pdl.restype = [i32], None
+                L.gkr_get_pdl.argtypes, L.gkr_get_pdl.restype = [], i32
                 _lib = L
     return _lib
 
@@ -90,6 +92,15 @@ def _raise(status: int) -> None:
         msg += f" (cudaError {lib().gkr_last_cuda_error()})"
         raise GkrError(status, msg)
     raise ValueError(f"gkr status {status}: {msg}")
+
+
+def set_pdl(enable: bool) -> None:
+    """Turn programmatic dependent launch on or off for later launches (process-wide)."""
+    lib().gkr_set_pdl(1 if enable else 0)
+
+
+def get_pdl() -> bool:
+    return bool(lib().gkr_get_pdl())
 
 
 def page_stride(record: int, block_size: int) -> int:

@@ -3,11 +3,25 @@
 #include "gkr.h"
 #include "launch.h"
 
+#include <atomic>
 #include <cstdint>
+#include <mutex>
+#include <vector>
 
 namespace {
 
 thread_local int32_t g_last_cuda_error = 0;
+std::atomic<int> g_pdl{1};
+
+struct OccEntry {
+    int device;
+    const void* func;
+    size_t smem;
+    int threads;
+    int64_t warps;
+};
+std::mutex g_occ_mutex;
+std::vector<OccEntry> g_occ;
 
 struct RecordRows {
     int32_t data, scale, align;
@@ -44,7 +58,45 @@ gkr_status cuda_status(cudaError_t e) {
 
 }  // namespace
 
+namespace gkr {
+
+bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
+
+cudaError_t resident_warps(const void* func, int threads, size_t smem, int64_t* warps) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    for (const OccEntry& o : g_occ) {
+        if (o.device == dev && o.func == func && o.smem == smem && o.threads == threads) {
+            *warps = o.warps;
+            return cudaSuccess;
+        }
+    }
+    if (smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t w = static_cast<int64_t>(sms) * per_sm * (threads / 32);
+    g_occ.push_back({dev, func, smem, threads, w});
+    *warps = w;
+    return cudaSuccess;
+}
+
+}  // namespace gkr
+
 extern "C" {
+
+GKR_API void gkr_set_pdl(int32_t enable) { g_pdl.store(enable ? 1 : 0); }
+
+GKR_API int32_t gkr_get_pdl(void) { return g_pdl.load() ? 1 : 0; }
 
 GKR_API int64_t gkr_page_stride(int32_t record, int32_t block_size) {
     RecordRows r;

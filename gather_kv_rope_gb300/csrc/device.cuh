@@ -201,4 +201,57 @@ __device__ __forceinline__ void report(int32_t* err, int32_t bits) {
     if (err != nullptr) atomicOr(err, bits);
 }
 
+// ---------------------------------------------------------------- async copies (LDGSTS)
+//
+// Each lane copies the bytes it will itself consume (or the warp synchronises
+// before reading bytes copied by other lanes), one commit group per staged item,
+// so a per-warp ring of S items keeps S items in flight per warp without holding
+// them in registers.  The waits are hardware group counters: nothing spins.
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(smem)), "l"(gmem)
+                 : "memory");
+}
+// 16-byte copy with an L2 evict-first hint (data read exactly once).
+__device__ __forceinline__ void cp_async16_stream(void* smem, const void* gmem, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;\n"
+                 ::"r"(smem_addr(smem)), "l"(gmem), "l"(policy) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_addr(smem)), "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint4 lds16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ uint2 lds8(const void* p) { return *reinterpret_cast<const uint2*>(p); }
+
+// ---------------------------------------------------------------- programmatic dependent launch
+//
+// With the programmatic-stream-serialisation launch attribute, a kernel may be
+// scheduled while the previous kernel in the stream is finishing.  Every kernel
+// here waits for the previous grid's completion (and memory flush) before its
+// first global access, then lets the next grid start scheduling.  Without the
+// attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_wait_previous() {
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_release_next() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 }  // namespace gkr

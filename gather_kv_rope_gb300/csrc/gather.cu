@@ -6,9 +6,11 @@
 // V4.1, 448 dims in 64-dim groups plus a copied bf16 tail for V4; FlashMLA overview
 // page, DSA section: an index of -1 is an invalid entry, which emits zeros).
 //
-// Launch shape: one warp per index, U indices per warp with all record loads
-// issued before any is consumed, 8 warps per block.  Output rows are written with
-// streaming stores (each 1 KiB row is written once and not re-read here).
+// Launch shape: exactly one wave of warps; each warp walks a contiguous chunk of
+// indices, loading 32 indices with one coalesced load and keeping S records in
+// flight in a per-warp shared-memory ring filled by cp.async (the 512 / 576 data
+// bytes as one 16-byte piece per lane, the scale row by one lane).  Output rows are
+// written with streaming stores (each 1 KiB row is written once).
 #include "device.cuh"
 #include "launch.h"
 
@@ -16,103 +18,127 @@ namespace gkr {
 
 namespace {
 
-__device__ __forceinline__ bool index_ok(const GatherParams& p, int32_t idx, bool in, int lane) {
-    if (idx >= 0 && idx < p.num_slots) return true;
-    if (in && idx != -1 && lane == 0) report(p.err, 4);
-    return false;
-}
-
-struct RecordLoads {
-    uint2 a;      // e4m3 codes of chunk A
-    uint4 b;      // e4m3 codes of chunk B (.x/.y), or the V4 bf16 tail (all four words)
-    uint4 sc;     // scale row (V4.1: 16 bytes; V4: 8 bytes in .x/.y)
-};
+constexpr int kGatherDepth = 4;  // records in flight per warp
 
 template <int kRecord>
-__device__ __forceinline__ void load_record(const GatherParams& p, int32_t idx, int lane,
-                                            RecordLoads& L) {
-    constexpr uint32_t D = kRecord == 528 ? 512u : 576u;
-    constexpr uint32_t S = kRecord == 528 ? 16u : 8u;
-    const uint32_t s = static_cast<uint32_t>(idx);
-    const uint32_t bs = static_cast<uint32_t>(p.block_size);
-    const uint32_t page = s / bs, row = s - page * bs;
-    const uint8_t* base = p.cache + static_cast<int64_t>(page) * p.page_stride;
-    const uint8_t* data = base + row * D;
-    L.a = ld_ro8(data + 8 * lane);
-    if (kRecord == 528) {
-        const uint2 t = ld_ro8(data + 256 + 8 * lane);
-        L.b = make_uint4(t.x, t.y, 0u, 0u);
-        L.sc = ld_ro16(base + bs * D + row * S);
-    } else {
-        if (lane < 24) {
-            const uint2 t = ld_ro8(data + 256 + 8 * lane);
-            L.b = make_uint4(t.x, t.y, 0u, 0u);
-        } else {
-            L.b = ld_ro16(data + 448 + 16 * (lane - 24));
-        }
-        const uint2 t = ld_ro8(base + bs * D + row * S);
-        L.sc = make_uint4(t.x, t.y, 0u, 0u);
-    }
+struct Rec {
+    static constexpr uint32_t D = kRecord == 528 ? 512u : 576u;   // data row bytes
+    static constexpr uint32_t S = kRecord == 528 ? 16u : 8u;      // scale row bytes
+    static constexpr int kSlot = kRecord == 528 ? 528 : 592;      // ring slot (16 B multiple)
+};
+
+__device__ __forceinline__ int32_t load_index_group(const GatherParams& p, int64_t i_begin, int n,
+                                                    int g, int lane) {
+    const int i = 32 * g + lane;
+    return i < n ? __ldg(p.indices + i_begin + i) : -1;
 }
 
-template <int kRecord, int U>
-__global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p) {
-    const int lane = threadIdx.x & 31;
-    const int64_t i0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * U;
-    if (i0 >= p.num_indices) return;
-
-    int32_t idx[U];
-    bool in[U], ok[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        in[u] = i0 + u < p.num_indices;
-        idx[u] = in[u] ? __ldg(p.indices + i0 + u) : -1;
-    }
-    RecordLoads L[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        ok[u] = index_ok(p, idx[u], in[u], lane);
-        if (ok[u]) load_record<kRecord>(p, idx[u], lane, L[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        if (!in[u]) continue;
-        uint4 oa = make_uint4(0u, 0u, 0u, 0u), ob = oa;
-        if (ok[u]) {
-            if (kRecord == 528) {
-                oa = dequant8(L[u].a, byte_of(L[u].sc, lane >> 2));
-                ob = dequant8(make_uint2(L[u].b.x, L[u].b.y), byte_of(L[u].sc, 8 + (lane >> 2)));
-            } else {
-                const uint2 sc = make_uint2(L[u].sc.x, L[u].sc.y);
-                oa = dequant8(L[u].a, byte_of(sc, lane >> 3));
-                ob = (lane < 24) ? dequant8(make_uint2(L[u].b.x, L[u].b.y), byte_of(sc, 4 + (lane >> 3)))
-                                 : L[u].b;
-            }
+// Stage the record of slot idx into ring slot k % S, then close one commit group.
+template <int kRecord, int S>
+__device__ __forceinline__ void stage(const GatherParams& p, uint8_t* ring, int k, int32_t idx,
+                                      int lane) {
+    using R = Rec<kRecord>;
+    if (idx >= 0 && idx < p.num_slots) {
+        const uint32_t s = static_cast<uint32_t>(idx);
+        const uint32_t bs = static_cast<uint32_t>(p.block_size);
+        const uint32_t page = s / bs, row = s - page * bs;
+        const uint8_t* base = p.cache + static_cast<int64_t>(page) * p.page_stride;
+        const uint8_t* data = base + row * R::D;
+        const uint8_t* srow = base + bs * R::D + row * R::S;
+        uint8_t* dst = ring + (k % S) * R::kSlot;
+        cp_async16(dst + 16 * lane, data + 16 * lane);
+        if (kRecord == 528) {
+            if (lane == 0) cp_async16(dst + 512, srow);
+        } else {
+            if (lane < 4) cp_async16(dst + 512 + 16 * lane, data + 512 + 16 * lane);
+            if (lane == 4) cp_async8(dst + 576, srow);
         }
-        uint8_t* orow = static_cast<uint8_t*>(p.out) + (i0 + u) * 1024;
+    }
+    cp_async_commit();
+}
+
+template <int kRecord, int S>
+__global__ void __launch_bounds__(kThreads) gather_kernel(const GatherParams p, int64_t chunk) {
+    using R = Rec<kRecord>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    pdl_wait_previous();
+    pdl_release_next();
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const int64_t i_begin = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib) * chunk;
+    if (i_begin >= p.num_indices) return;  // warp-uniform
+    const int n = static_cast<int>(chunk < p.num_indices - i_begin ? chunk : p.num_indices - i_begin);
+    uint8_t* ring = smem + wib * (S * R::kSlot);
+
+    int32_t cur = load_index_group(p, i_begin, n, 0, lane);
+    int32_t nxt = load_index_group(p, i_begin, n, 1, lane);
+#pragma unroll
+    for (int k = 0; k < S - 1; ++k) {
+        const int32_t idx = __shfl_sync(kFull, cur, k);
+        if (k < n) stage<kRecord, S>(p, ring, k, idx, lane);
+        else cp_async_commit();
+    }
+    for (int j = 0; j < n; ++j) {
+        const int k = j + S - 1;
+        __syncwarp();                        // every lane is done reading ring slot k % S
+        if (k < n) {
+            const int32_t idx = __shfl_sync(kFull, ((k >> 5) == (j >> 5)) ? cur : nxt, k & 31);
+            stage<kRecord, S>(p, ring, k, idx, lane);
+        } else {
+            cp_async_commit();
+        }
+        cp_async_wait<S - 1>();              // this lane's pieces of record j have landed
+        __syncwarp();                        // ... and every other lane's
+
+        const int32_t idx = __shfl_sync(kFull, cur, j & 31);
+        uint4 oa = make_uint4(0u, 0u, 0u, 0u), ob = oa;
+        if (idx >= 0 && idx < p.num_slots) {
+            const uint8_t* src = ring + (j % S) * R::kSlot;
+            const uint2 ca = lds8(src + 8 * lane);
+            if (kRecord == 528) {
+                const uint4 sc = lds16(src + 512);
+                oa = dequant8(ca, byte_of(sc, lane >> 2));
+                ob = dequant8(lds8(src + 256 + 8 * lane), byte_of(sc, 8 + (lane >> 2)));
+            } else {
+                const uint2 sc = lds8(src + 576);
+                oa = dequant8(ca, byte_of(sc, lane >> 3));
+                ob = (lane < 24) ? dequant8(lds8(src + 256 + 8 * lane), byte_of(sc, 4 + (lane >> 3)))
+                                 : lds16(src + 448 + 16 * (lane - 24));
+            }
+        } else if (idx != -1 && lane == 0) {
+            report(p.err, 4);
+        }
+        uint8_t* orow = static_cast<uint8_t*>(p.out) + (i_begin + j) * 1024;
         st_stream16(orow + 16 * lane, oa);
         st_stream16(orow + 512 + 16 * lane, ob);
+        if ((j & 31) == 31) {
+            cur = nxt;
+            nxt = load_index_group(p, i_begin, n, (j >> 5) + 2, lane);
+        }
     }
+    cp_async_wait<0>();
 }
 
-template <int kRecord, int U>
+template <int kRecord, int S>
 cudaError_t launch(const GatherParams& p, cudaStream_t stream) {
     if (p.num_indices <= 0) return cudaSuccess;
-    const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * U;
-    const int64_t blocks = (p.num_indices + per_block - 1) / per_block;
-    gather_kernel<kRecord, U><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    auto kernel = gather_kernel<kRecord, S>;
+    const size_t smem = static_cast<size_t>(kWarpsPerBlock) * S * Rec<kRecord>::kSlot;
+    int64_t wave = 0;
+    cudaError_t e = resident_warps(reinterpret_cast<const void*>(kernel), kThreads, smem, &wave);
+    if (e != cudaSuccess) return e;
+    int64_t chunk = 0, blocks = 0;
+    one_wave_split(p.num_indices, wave, kWarpsPerBlock, &chunk, &blocks);
+    return launch_kernel(kernel, blocks, kThreads, smem, stream, p, chunk);
 }
 
 }  // namespace
 
-constexpr int kGatherIndicesPerWarp = 2;
-
 cudaError_t launch_gather_v41(const GatherParams& p, cudaStream_t stream) {
-    return launch<528, kGatherIndicesPerWarp>(p, stream);
+    return launch<528, kGatherDepth>(p, stream);
 }
 cudaError_t launch_gather_v4(const GatherParams& p, cudaStream_t stream) {
-    return launch<584, kGatherIndicesPerWarp>(p, stream);
+    return launch<584, kGatherDepth>(p, stream);
 }
 
 }  // namespace gkr

@@ -154,6 +154,17 @@ GKR_API gkr_status gkr_kv_gather(const void *k_cache, const gkr_cache_desc *cach
                                  const int32_t *indices, int64_t num_indices, void *out,
                                  int32_t *err_flag, cudaStream_t stream);
 
+/*
+ * Programmatic dependent launch (process-wide, default on).  When on, kernels are
+ * launched with the programmatic-stream-serialisation attribute: a launch may be
+ * scheduled while the previous kernel in the stream drains, and waits for that
+ * kernel's completion and memory flush before its first global memory access, so
+ * stream order semantics are unchanged.  The setting applies to launches made
+ * after the call (including launches recorded into CUDA graphs by stream capture).
+ */
+GKR_API void gkr_set_pdl(int32_t enable);
+GKR_API int32_t gkr_get_pdl(void);
+
 /* Static, NUL-terminated description of a status code. */
 GKR_API const char *gkr_status_string(gkr_status status);
 

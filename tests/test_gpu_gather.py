@@ -185,3 +185,34 @@ def test_gather_v41_sparse_sampled(gkr, oracle_mod):
             continue
         d, sc = oracle_mod.encode(528, case.kv[s], case.csc[case.positions[s]])
         assert np.array_equal(got2[i], oracle_mod.decode(528, d, sc)), i
+
+
+@pytest.mark.parametrize("pdl", [True, False])
+@pytest.mark.parametrize("record", [528, 584])
+def test_insert_then_gather_same_stream(gkr, oracle_mod, record, pdl):
+    """Back-to-back insert -> gather -> insert -> ... on one stream: every gather must
+    see the insert queued before it (the programmatic-launch wait keeps stream order)."""
+    gkr.set_pdl(pdl)
+    try:
+        bs, P = 64, 64
+        ps = oracle_mod.page_stride(record, bs)
+        cache = gkr.alloc_cache(P, bs, record, DEV, fill=0)
+        ref = np.zeros(P * ps, np.uint8)
+        outs, refs = [], []
+        for r in range(6):
+            case = W.random_insert("chain", 2048, record, bs, P, 256, 0.05, seed=40 + r)
+            kv = torch.from_numpy(case.kv.view(np.int16)).view(torch.bfloat16).to(DEV)
+            gkr.kv_insert(kv, cache, torch.from_numpy(case.slots).to(DEV),
+                          torch.from_numpy(case.positions).to(DEV),
+                          torch.from_numpy(case.csc).to(DEV), bs, record)
+            idx = np.random.default_rng(r).integers(-1, P * bs, 3000).astype(np.int32)
+            out = torch.empty(3000, 512, dtype=torch.bfloat16, device=DEV)
+            gkr.kv_gather(cache, torch.from_numpy(idx).to(DEV), out)
+            outs.append(out)
+            oracle_mod.insert(case.kv, ref, record, bs, P, ps, case.slots, case.positions, case.csc)
+            refs.append(oracle_mod.gather(ref, record, bs, P, ps, idx)[0])
+        torch.cuda.synchronize()
+        for out, r in zip(outs, refs):
+            _assert_bits_equal(bits_of(out), r)
+    finally:
+        gkr.set_pdl(True)
