@@ -62,6 +62,10 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU time budget of the oracle baseline sample")
+    ap.add_argument("--profile", default=None, metavar="WORKLOAD",
+                    help="run only this workload's kernel(s) a few times (for profiler "
+                         "captures) and print their CUDA-event times")
+    ap.add_argument("--launches", type=int, default=3)
     return ap.parse_args(argv)
 
 
@@ -508,12 +512,54 @@ def run_reference(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- profiling
+
+def run_profile(args):
+    """Run one workload's kernel(s): 2 warm-up launches then --launches timed ones.
+    Inserts go to a fresh zeroed cache per launch set; the sparse gathers read a cache
+    filled once by the insert (that fill is one extra insert launch before them)."""
+    import torch
+    import gather_kv_rope_gb300 as gkr
+    import workloads as W
+    dev = torch.device("cuda:0")
+    gkr.build()
+    case = W.PROFILE_WORKLOADS[args.profile]()
+    s = device_sets(case, dev, 1)[0]
+    res = {"workload": args.profile}
+    ins = lambda: gkr.kv_insert(s["kv"], s["cache"], s["slots"], s["pos"], s["csc"],
+                                case.block_size, case.record)
+    if args.profile.startswith("gather"):
+        ins()                                       # fill the cache once
+        fns = {"gather": lambda: gkr.kv_gather(s["cache"], s["idx"], s["out"])}
+    elif s["idx"] is not None:
+        fns = {"insert": ins, "gather": lambda: gkr.kv_gather(s["cache"], s["idx"], s["out"])}
+    else:
+        fns = {"insert": ins}
+    for name, fn in fns.items():
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.launches):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        res[name + "_us"] = [round(a.elapsed_time(b) * 1e3, 2) for a, b in ts]
+    print(json.dumps(res), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- main
 
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile:
+        return run_profile(args)
 
     import torch
     import gather_kv_rope_gb300 as gkr

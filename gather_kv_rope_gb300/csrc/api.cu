@@ -45,6 +45,7 @@ gkr_status check_cache(const gkr_cache_desc* c, RecordRows* rows) {
     if (c->num_pages <= 0) return GKR_EINVAL;
     if (c->num_pages > (INT64_C(0x7FFFFFFF) / c->block_size)) return GKR_EINVAL;  // slots < 2^31
     const int64_t need = static_cast<int64_t>(c->block_size) * c->record;
+    if (need > INT64_C(0x7FFFFFFF)) return GKR_EINVAL;                             // page < 2^31 B
     if (c->page_stride < need || c->page_stride % rows->align != 0) return GKR_EBAD_PAGE_GEOMETRY;
     if (c->page_stride > INT64_MAX / c->num_pages) return GKR_EBAD_PAGE_GEOMETRY;
     return GKR_OK;

@@ -1,10 +1,10 @@
 // Device helpers shared by the insert and gather kernels (sm_103a).
 //
-// Lane layout used by every kernel: one warp owns one 512-dim token row.
-// Lane L holds two 8-dim chunks, A = dims [8L, 8L+8) and B = dims
-// [256+8L, 256+8L+8), so each warp-wide 16-byte bf16 access (or 8-byte e4m3
-// access) covers one contiguous 512-byte (256-byte) span: fully coalesced
-// 128-byte lines for loads and stores.
+// Lane layout used by every kernel: a warp handles two items (tokens or gather
+// indices) at a time, one per half-warp; lane q = lane % 16 of a half owns dims
+// [32q, 32q + 32) of its item -- exactly one 32-dim scale block of the V4.1 record,
+// or half of a 64-dim block of the V4 record.  Rows are staged in shared memory by
+// cp.async, so global accesses stay 16-byte and line-contiguous per half-warp.
 #pragma once
 
 #include <cstdint>
@@ -14,7 +14,13 @@
 
 namespace gkr {
 
-constexpr int kWarpsPerBlock = 8;
+#ifndef GKR_WARPS_PER_BLOCK
+#define GKR_WARPS_PER_BLOCK 8
+#endif
+#ifndef GKR_MIN_BLOCKS
+#define GKR_MIN_BLOCKS 4      // resident blocks per SM the register budget is sized for
+#endif
+constexpr int kWarpsPerBlock = GKR_WARPS_PER_BLOCK;
 constexpr int kThreads = kWarpsPerBlock * 32;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -44,7 +50,7 @@ __device__ __forceinline__ void st_stream16(void* p, uint4 v) {
 // ---------------------------------------------------------------- bf16 <-> fp32
 
 // Eight bf16 values packed in a uint4 -> fp32 (exact: bf16 is the top half of fp32).
-__device__ __forceinline__ void unpack_bf16x8(const uint4 v, float f[8]) {
+__device__ __forceinline__ void unpack_bf16x8(const uint4 v, float* f) {
     f[0] = __uint_as_float(v.x << 16);
     f[1] = __uint_as_float(v.x & 0xFFFF0000u);
     f[2] = __uint_as_float(v.y << 16);
@@ -63,26 +69,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 
 // ---------------------------------------------------------------- RoPE
 
-// Rotate four adjacent pairs (f[0],f[1]) .. (f[6],f[7]) by (c[i], s[i]):
+// Rotate two adjacent pairs (f[0], f[1]) and (f[2], f[3]) by (c[i], s[i]):
 // even' = e*c - o*s, odd' = o*c + e*s; every product and sum is a separately
 // rounded fp32 operation (the _rn intrinsics are never contracted into FMA).
-__device__ __forceinline__ void rope4(float f[8], const float4 c, const float4 s) {
-    const float cc[4] = {c.x, c.y, c.z, c.w};
-    const float ss[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float e = f[2 * i], o = f[2 * i + 1];
-        f[2 * i] = __fsub_rn(__fmul_rn(e, cc[i]), __fmul_rn(o, ss[i]));
-        f[2 * i + 1] = __fadd_rn(__fmul_rn(o, cc[i]), __fmul_rn(e, ss[i]));
-    }
+__device__ __forceinline__ void rope2(float f[4], const float2 c, const float2 s) {
+    const float e0 = f[0], o0 = f[1], e1 = f[2], o1 = f[3];
+    f[0] = __fsub_rn(__fmul_rn(e0, c.x), __fmul_rn(o0, s.x));
+    f[1] = __fadd_rn(__fmul_rn(o0, c.x), __fmul_rn(e0, s.x));
+    f[2] = __fsub_rn(__fmul_rn(e1, c.y), __fmul_rn(o1, s.y));
+    f[3] = __fadd_rn(__fmul_rn(o1, c.y), __fmul_rn(e1, s.y));
 }
 
 // ---------------------------------------------------------------- MXFP8 encode
 
-__device__ __forceinline__ float amax8(const float f[8]) {
+__device__ __forceinline__ float amax32(const float* f) {
     float m = fabsf(f[0]);
 #pragma unroll
-    for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    for (int i = 1; i < 32; ++i) m = fmaxf(m, fabsf(f[i]));
     return m;
 }
 
@@ -113,13 +116,16 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
     return lo | (hi << 16);
 }
 
-// Quantise an 8-value chunk with the block's scale byte -> 8 e4m3 bytes.
-__device__ __forceinline__ uint2 quantise8(const float f[8], uint32_t byte) {
+// Quantise 32 values with their block's scale byte -> 32 e4m3 bytes (two uint4).
+__device__ __forceinline__ void quantise32(const float* f, uint32_t byte, uint4& lo, uint4& hi) {
     const float k = inv_scale(byte);
-    uint2 q;
-    q.x = e4m3x4(__fmul_rn(f[0], k), __fmul_rn(f[1], k), __fmul_rn(f[2], k), __fmul_rn(f[3], k));
-    q.y = e4m3x4(__fmul_rn(f[4], k), __fmul_rn(f[5], k), __fmul_rn(f[6], k), __fmul_rn(f[7], k));
-    return q;
+    uint32_t q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        q[i] = e4m3x4(__fmul_rn(f[4 * i], k), __fmul_rn(f[4 * i + 1], k),
+                      __fmul_rn(f[4 * i + 2], k), __fmul_rn(f[4 * i + 3], k));
+    lo = make_uint4(q[0], q[1], q[2], q[3]);
+    hi = make_uint4(q[4], q[5], q[6], q[7]);
 }
 
 // ---------------------------------------------------------------- MXFP8 decode
@@ -131,27 +137,49 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
     return d;
 }
 
-// Packed bf16x2 of 2^(byte - 127) for a UE8M0 byte in [0, 254]; byte 0 is the
-// bf16 subnormal 2^-127 (0x0040).
-__device__ __forceinline__ uint32_t ue8m0_to_bf16x2(uint32_t byte) {
-    const uint32_t h = byte ? (byte << 7) : 0x0040u;
-    return h | (h << 16);
-}
-
 constexpr uint32_t kBf16NaN = 0x7FC0u;
-constexpr uint32_t kTwoPow120x2 = 0x7B807B80u;  // bf16 2^120 in both halves
 
-// Two e4m3 codes (bytes sel of w) -> bf16x2 of e4m3 * 2^(byte-127).
+// Eight e4m3 codes -> eight bf16 values e4m3 * 2^(byte - 127), exactly rounded.
+//
 // An e4m3 byte s.EEEE.MMM moved to bf16 bit positions s.0000EEEE.MMM0000 reads as
 // (1 + M/8) * 2^(E-127) (E >= 1) or M * 2^-129 (E = 0): in both cases the e4m3 value
-// times 2^-120.  Multiplying by 2^120 is exact and restores the e4m3 value; the second
-// multiply by the power-of-two scale rounds once, to nearest even.  NaN codes are
-// handled by the caller.
-template <int kHigh>
-__device__ __forceinline__ uint32_t dequant2(uint32_t w, uint32_t scale2) {
-    const uint32_t h = __byte_perm(w, 0u, kHigh ? 0x3424u : 0x1404u);  // codes -> bytes 1, 3
-    const uint32_t bits = (h & 0x80008000u) | ((h >> 4) & 0x07F007F0u);
-    return bf16x2_mul(bf16x2_mul(bits, kTwoPow120x2), scale2);
+// times 2^-120.  One bf16 multiply by 2^(byte - 7) then gives the result, rounded once
+// to nearest even (subnormals kept).  2^(byte - 7) is a normal bf16 for byte <= 134;
+// above that the factor is split into 2^127 (exact step) and 2^(byte - 134).  The
+// e4m3 NaN codes (0x7F, 0xFF) and the UE8M0 NaN byte 255 give the bf16 NaN 0x7FC0.
+struct Dequant {
+    uint32_t m1, m2;   // packed bf16x2 factors; m2 used only when split
+    bool split, nan_scale;
+};
+
+__device__ __forceinline__ Dequant make_dequant(uint32_t byte) {
+    Dequant d;
+    d.nan_scale = byte == 255u;
+    d.split = byte > 134u;
+    const uint32_t e1 = d.split ? 254u : byte + 120u;   // biased exponent of the factor
+    const uint32_t e2 = byte - 7u;                       // 2^(byte-134), biased
+    d.m1 = (e1 << 7) * 0x00010001u;
+    d.m2 = (e2 << 7) * 0x00010001u;
+    return d;
+}
+
+// Four codes of one word -> two packed bf16x2 words (codes 0,1 and 2,3).
+__device__ __forceinline__ void dequant4(uint32_t w, const Dequant& d, uint32_t& o01,
+                                         uint32_t& o23) {
+    const uint32_t x = w & 0x7F7F7F7Fu;               // magnitudes
+    const uint32_t sg = w & 0x80808080u;              // signs
+    // magnitudes to bytes 0 and 2 (x16 puts them at bits 4..10 / 20..26), signs to
+    // bytes 1 and 3 (bit 15 / 31)
+    uint32_t a = __byte_perm(x, 0u, 0x4140u) * 16u + __byte_perm(sg, 0u, 0x1404u);
+    uint32_t b = __byte_perm(x, 0u, 0x4342u) * 16u + __byte_perm(sg, 0u, 0x3424u);
+    a = bf16x2_mul(a, d.m1);
+    b = bf16x2_mul(b, d.m1);
+    if (d.split) {
+        a = bf16x2_mul(a, d.m2);
+        b = bf16x2_mul(b, d.m2);
+    }
+    o01 = a;
+    o23 = b;
 }
 
 // Bytes of w whose low 7 bits are all ones (the e4m3 NaN codes) -> 0x80 in that byte.
@@ -159,7 +187,7 @@ __device__ __forceinline__ uint32_t e4m3_nan_bytes(uint32_t w) {
     return ((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
 }
 
-// Replace the bf16 halves of o[0..1] (codes 0..3 of a word) flagged in nanmask by NaN.
+// Replace the bf16 halves of o01 / o23 (codes 0..3 of a word) flagged in nanmask by NaN.
 __device__ __forceinline__ void patch_nan(uint32_t nanmask, uint32_t& o01, uint32_t& o23) {
     if (nanmask & 0x00000080u) o01 = (o01 & 0xFFFF0000u) | kBf16NaN;
     if (nanmask & 0x00008000u) o01 = (o01 & 0x0000FFFFu) | (kBf16NaN << 16);
@@ -167,34 +195,22 @@ __device__ __forceinline__ void patch_nan(uint32_t nanmask, uint32_t& o01, uint3
     if (nanmask & 0x80000000u) o23 = (o23 & 0x0000FFFFu) | (kBf16NaN << 16);
 }
 
-// Eight e4m3 codes with one UE8M0 scale byte -> eight bf16 (uint4).
-__device__ __forceinline__ uint4 dequant8(const uint2 c, uint32_t byte) {
-    uint4 o;
-    if (byte == 255u) {  // the UE8M0 NaN
-        const uint32_t n = kBf16NaN | (kBf16NaN << 16);
-        return make_uint4(n, n, n, n);
+// 32 e4m3 codes (8 words) with one UE8M0 scale byte -> 32 bf16 (16 words).
+__device__ __forceinline__ void dequant32(const uint32_t* c, uint32_t byte, uint32_t* o) {
+    const Dequant d = make_dequant(byte);
+    uint32_t acc = 0u;   // bit 7 of a byte ends up set iff some code in that lane is NaN
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        dequant4(c[i], d, o[2 * i], o[2 * i + 1]);
+        acc |= (c[i] & 0x7F7F7F7Fu) + 0x01010101u;
     }
-    const uint32_t s2 = ue8m0_to_bf16x2(byte);
-    o.x = dequant2<0>(c.x, s2);
-    o.y = dequant2<1>(c.x, s2);
-    o.z = dequant2<0>(c.y, s2);
-    o.w = dequant2<1>(c.y, s2);
-    const uint32_t n0 = e4m3_nan_bytes(c.x), n1 = e4m3_nan_bytes(c.y);
-    if (n0 | n1) {
-        patch_nan(n0, o.x, o.y);
-        patch_nan(n1, o.z, o.w);
+    if ((acc & 0x80808080u) != 0u || d.nan_scale) {   // rare: corrupt or NaN-marked records
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (d.nan_scale) o[2 * i] = o[2 * i + 1] = kBf16NaN | (kBf16NaN << 16);
+            else patch_nan(e4m3_nan_bytes(c[i]), o[2 * i], o[2 * i + 1]);
+        }
     }
-    return o;
-}
-
-// Byte k (0..15) of a 16-byte value.
-__device__ __forceinline__ uint32_t byte_of(const uint4 v, int k) {
-    const uint32_t w = (k < 8) ? ((k < 4) ? v.x : v.y) : ((k < 12) ? v.z : v.w);
-    return (w >> (8 * (k & 3))) & 0xFFu;
-}
-__device__ __forceinline__ uint32_t byte_of(const uint2 v, int k) {
-    const uint32_t w = (k < 4) ? v.x : v.y;
-    return (w >> (8 * (k & 3))) & 0xFFu;
 }
 
 __device__ __forceinline__ void report(int32_t* err, int32_t bits) {
@@ -215,11 +231,6 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(smem)), "l"(gmem)
                  : "memory");
 }
-// 16-byte copy with an L2 evict-first hint (data read exactly once).
-__device__ __forceinline__ void cp_async16_stream(void* smem, const void* gmem, uint64_t policy) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;\n"
-                 ::"r"(smem_addr(smem)), "l"(gmem), "l"(policy) : "memory");
-}
 __device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_addr(smem)), "l"(gmem)
                  : "memory");
@@ -231,12 +242,6 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ uint64_t l2_evict_first_policy() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
-    return p;
-}
-
 __device__ __forceinline__ uint4 lds16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 __device__ __forceinline__ uint2 lds8(const void* p) { return *reinterpret_cast<const uint2*>(p); }
 

@@ -61,14 +61,56 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), int64_t blocks, int threads,
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// Split `n` items over at most one wave of warps: returns the items per warp
-// (chunk) and the number of blocks of `warps_per_block` warps.
-inline void one_wave_split(int64_t n, int64_t wave_warps, int warps_per_block, int64_t* chunk,
-                           int64_t* blocks) {
+// How the items (tokens or indices) of a launch are dealt to its warps.  Warp w owns
+// items base(w) + j * step for j in [0, count(w)):
+//   chunked  (step 1):      base = w * chunk, a contiguous run of `chunk` items;
+//   cyclic   (step = warps): base = w, so the warps active at one moment touch one
+//                            contiguous window of items.
+// Either way the grid is at most one resident wave of warps.
+struct WorkMap {
+    int64_t n;        // items in the launch
+    int64_t chunk;    // chunked: items per warp
+    int64_t warps;    // warps launched
+    int32_t cyclic;   // 1 = cyclic, 0 = chunked
+};
+
+inline WorkMap make_work_map(int64_t n, int64_t wave_warps, bool cyclic, int64_t granule = 1) {
+    WorkMap m;
+    m.n = n;
+    m.cyclic = cyclic ? 1 : 0;
     if (wave_warps < 1) wave_warps = 1;
-    *chunk = (n + wave_warps - 1) / wave_warps;
-    const int64_t warps = (n + *chunk - 1) / *chunk;
-    *blocks = (warps + warps_per_block - 1) / warps_per_block;
+    m.chunk = (n + wave_warps - 1) / wave_warps;
+    m.chunk = (m.chunk + granule - 1) / granule * granule;   // whole warp iterations
+    m.warps = cyclic ? (n < wave_warps ? n : wave_warps) : (n + m.chunk - 1) / m.chunk;
+    return m;
+}
+
+// The items of warp `gw` under a work map: item j is base + j * step, j < n.
+struct WarpItems {
+    int64_t base, step;
+    int n;
+    __host__ __device__ int64_t at(int j) const { return base + j * step; }
+};
+
+__host__ __device__ inline WarpItems warp_items(const WorkMap& m, int64_t gw) {
+    WarpItems w;
+    if (gw >= m.warps) {         // spare warps of the last block
+        w.base = 0;
+        w.step = 1;
+        w.n = 0;
+        return w;
+    }
+    if (m.cyclic) {
+        w.base = gw;
+        w.step = m.warps;
+        w.n = gw < m.n ? static_cast<int>((m.n - 1 - gw) / m.warps + 1) : 0;
+    } else {
+        w.base = gw * m.chunk;
+        w.step = 1;
+        const int64_t r = m.n - w.base;
+        w.n = r <= 0 ? 0 : static_cast<int>(r < m.chunk ? r : m.chunk);
+    }
+    return w;
 }
 
 cudaError_t launch_insert_v41(const InsertParams& p, cudaStream_t stream);

@@ -167,10 +167,40 @@ def gather_v41_sparse(seed: int = 0, cache_tokens: int = 1 << 20, queries: int =
     return c
 
 
+def insert_v41_131072(seed: int = 0) -> InsertCase:
+    """Profiling-size contiguous insert: 4 sequences of 32768 tokens (positions
+    0..32767 each), sequence s writes slots s*32768 + [0, 32768); N(0, 0.5); bs 64,
+    2048 pages; 2% -> -1.  kv 134 MB + cache 69 MB, larger than L2."""
+    rng = np.random.default_rng(seed)
+    S, L = 4, 32768
+    T = S * L
+    kv = _kv_values(rng, T, "normal", sigma=0.5)
+    positions = np.tile(np.arange(L, dtype=np.int64), S)
+    slots = (np.repeat(np.arange(S, dtype=np.int64) * L, L) + np.tile(np.arange(L, dtype=np.int64), S))
+    slots[_skip_mask(rng, T, 0.02)] = -1
+    return InsertCase("insert_v41_131072", 528, 64, 2048, kv, slots, positions,
+                      cos_sin_table(L), None)
+
+
+def gather_v41_sparse_262144(seed: int = 0) -> InsertCase:
+    """Profiling-size sparse gather: a 262144-token cache (138 MB) and 32 queries x 2048."""
+    c = gather_v41_sparse(seed, cache_tokens=1 << 18, queries=32, topk=2048, min_ctx=8192)
+    c.name = "gather_v41_sparse_262144"
+    return c
+
+
 WORKLOADS = {
     "insert_v41_1024": insert_v41_1024,
     "roundtrip_v41_16384": roundtrip_v41_16384,
     "insert_v4_65536": insert_v4_65536,
     "insert_v41_262144": insert_v41_262144,
     "gather_v41_sparse": gather_v41_sparse,
+}
+
+# smaller cases of the same kernels, sized for profiler captures
+PROFILE_WORKLOADS = {
+    "insert_v41_131072": insert_v41_131072,
+    "insert_v4_65536": insert_v4_65536,
+    "gather_v41_sparse_262144": gather_v41_sparse_262144,
+    "roundtrip_v41_16384": roundtrip_v41_16384,
 }
