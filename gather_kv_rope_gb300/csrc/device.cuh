@@ -1,10 +1,11 @@
 // Device helpers shared by the insert and gather kernels (sm_103a).
 //
-// Lane layout used by every kernel: a warp handles two items (tokens or gather
-// indices) at a time, one per half-warp; lane q = lane % 16 of a half owns dims
-// [32q, 32q + 32) of its item -- exactly one 32-dim scale block of the V4.1 record,
-// or half of a 64-dim block of the V4 record.  Rows are staged in shared memory by
-// cp.async, so global accesses stay 16-byte and line-contiguous per half-warp.
+// Lane layout used by every kernel: one warp owns one 512-dim row (token or gather
+// index) at a time.  Lane L holds two 8-dim chunks, A = dims [8L, 8L+8) and
+// B = dims [256+8L, 256+8L+8), so every warp-wide access -- 16-byte bf16 pieces or
+// 8-byte e4m3 pieces -- covers one contiguous 512-byte (256-byte) span: whole
+// 128-byte lines per instruction for loads and stores.  A 32-dim V4.1 scale block is
+// four consecutive lanes; a 64-dim V4 block eight.
 #pragma once
 
 #include <cstdint>
@@ -69,6 +70,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 
 // ---------------------------------------------------------------- RoPE
 
+// Rotate four adjacent pairs (f[0], f[1]) .. (f[6], f[7]) by (c[i], s[i]):
+// even' = e*c - o*s, odd' = o*c + e*s; every product and sum is a separately
+// rounded fp32 operation (the _rn intrinsics are never contracted into FMA).
+__device__ __forceinline__ void rope4(float* f, const float4 c, const float4 s) {
+    const float cc[4] = {c.x, c.y, c.z, c.w};
+    const float ss[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float e = f[2 * i], o = f[2 * i + 1];
+        f[2 * i] = __fsub_rn(__fmul_rn(e, cc[i]), __fmul_rn(o, ss[i]));
+        f[2 * i + 1] = __fadd_rn(__fmul_rn(o, cc[i]), __fmul_rn(e, ss[i]));
+    }
+}
+
 // Rotate two adjacent pairs (f[0], f[1]) and (f[2], f[3]) by (c[i], s[i]):
 // even' = e*c - o*s, odd' = o*c + e*s; every product and sum is a separately
 // rounded fp32 operation (the _rn intrinsics are never contracted into FMA).
@@ -81,6 +96,13 @@ __device__ __forceinline__ void rope2(float f[4], const float2 c, const float2 s
 }
 
 // ---------------------------------------------------------------- MXFP8 encode
+
+__device__ __forceinline__ float amax8(const float* f) {
+    float m = fabsf(f[0]);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    return m;
+}
 
 __device__ __forceinline__ float amax32(const float* f) {
     float m = fabsf(f[0]);
@@ -114,6 +136,15 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
     const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
     const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
     return lo | (hi << 16);
+}
+
+// Quantise 8 values with their block's scale byte -> 8 e4m3 bytes.
+__device__ __forceinline__ uint2 quantise8(const float* f, uint32_t byte) {
+    const float k = inv_scale(byte);
+    uint2 q;
+    q.x = e4m3x4(__fmul_rn(f[0], k), __fmul_rn(f[1], k), __fmul_rn(f[2], k), __fmul_rn(f[3], k));
+    q.y = e4m3x4(__fmul_rn(f[4], k), __fmul_rn(f[5], k), __fmul_rn(f[6], k), __fmul_rn(f[7], k));
+    return q;
 }
 
 // Quantise 32 values with their block's scale byte -> 32 e4m3 bytes (two uint4).
@@ -156,10 +187,9 @@ __device__ __forceinline__ Dequant make_dequant(uint32_t byte) {
     Dequant d;
     d.nan_scale = byte == 255u;
     d.split = byte > 134u;
-    const uint32_t e1 = d.split ? 254u : byte + 120u;   // biased exponent of the factor
-    const uint32_t e2 = byte - 7u;                       // 2^(byte-134), biased
-    d.m1 = (e1 << 7) * 0x00010001u;
-    d.m2 = (e2 << 7) * 0x00010001u;
+    // bf16 bits of 2^(min(byte,134) - 7) in both halves: biased exponent min(byte,134) + 120
+    d.m1 = (min(byte, 134u) + 120u) * 0x00800080u;
+    d.m2 = (byte - 7u) * 0x00800080u;                // 2^(byte - 134), used when split
     return d;
 }
 
@@ -193,6 +223,24 @@ __device__ __forceinline__ void patch_nan(uint32_t nanmask, uint32_t& o01, uint3
     if (nanmask & 0x00008000u) o01 = (o01 & 0x0000FFFFu) | (kBf16NaN << 16);
     if (nanmask & 0x00800000u) o23 = (o23 & 0xFFFF0000u) | kBf16NaN;
     if (nanmask & 0x80000000u) o23 = (o23 & 0x0000FFFFu) | (kBf16NaN << 16);
+}
+
+// 8 e4m3 codes (2 words) with one UE8M0 scale byte -> 8 bf16 (uint4).
+__device__ __forceinline__ uint4 dequant8(const uint2 c, uint32_t byte) {
+    const Dequant d = make_dequant(byte);
+    uint4 o;
+    dequant4(c.x, d, o.x, o.y);
+    dequant4(c.y, d, o.z, o.w);
+    const uint32_t acc = ((c.x & 0x7F7F7F7Fu) + 0x01010101u) | ((c.y & 0x7F7F7F7Fu) + 0x01010101u);
+    if ((acc & 0x80808080u) != 0u || d.nan_scale) {   // rare: corrupt or NaN-marked records
+        if (d.nan_scale) {
+            const uint32_t n = kBf16NaN | (kBf16NaN << 16);
+            return make_uint4(n, n, n, n);
+        }
+        patch_nan(e4m3_nan_bytes(c.x), o.x, o.y);
+        patch_nan(e4m3_nan_bytes(c.y), o.z, o.w);
+    }
+    return o;
 }
 
 // 32 e4m3 codes (8 words) with one UE8M0 scale byte -> 32 bf16 (16 words).

@@ -7,14 +7,13 @@
 // page, DSA section: an index of -1 is an invalid entry, which emits zeros).
 //
 // Launch shape: at most one wave of warps, each walking its own list of indices
-// (see WorkMap), two indices per iteration -- one per half-warp, lane q of a half
-// owning output dims [32q, 32q + 32).  Per group of 32 indices, lane i decodes index
-// i once (validity, the record's byte offset, the distance to its scale row), so the
-// per-index cost is two shuffles, the copies and the dequantisation.  A per-warp ring
-// in shared memory, filled by cp.async, keeps S iterations (2S records) in flight;
-// each lane's slice of a staged record is padded by 16 bytes so the 16-byte shared
-// loads of 8 consecutive lanes fall in distinct bank groups.  Output rows are
-// written with streaming stores (each 1 KiB row is written once).
+// (see WorkMap); one warp per record, lane L owning output dims [8L, 8L+8) and
+// [256+8L, 256+8L+8).  Per group of 32 indices, lane i decodes index i once
+// (validity, the record's byte offset, the distance to its scale row), so a record
+// costs three shuffles, four coalesced loads (two 8-byte code pieces, two scale
+// bytes), the dequantisation and two 16-byte streaming stores.  Records are loaded
+// straight into registers in batches of P, the next batch's loads issued before the
+// current batch is converted, so 2P records per warp are in flight.
 #include "device.cuh"
 #include "launch.h"
 
@@ -22,22 +21,38 @@ namespace gkr {
 
 namespace {
 
-#ifndef GKR_GATHER_DEPTH
-#define GKR_GATHER_DEPTH 4
+#ifndef GKR_GATHER_BATCH
+#define GKR_GATHER_BATCH 2
 #endif
 #ifndef GKR_GATHER_CYCLIC
 #define GKR_GATHER_CYCLIC 0
 #endif
-constexpr int kGatherDepth = GKR_GATHER_DEPTH;  // iterations in flight per warp
+constexpr int kBatch = GKR_GATHER_BATCH;   // records per batch (a power of two <= 16)
 
 template <int kRecord>
 struct Rec {
-    static constexpr uint32_t D = kRecord == 528 ? 512u : 576u;    // data row bytes
-    static constexpr uint32_t S = kRecord == 528 ? 16u : 8u;       // scale row bytes
-    static constexpr int kLane = kRecord == 528 ? 48 : 80;         // staged bytes per lane (+16 pad)
-    static constexpr int kScale = 16 * kLane;                      // scale row offset in the item
-    static constexpr int kItem = kScale + 16;                      // staged bytes per record
+    static constexpr uint32_t D = kRecord == 528 ? 512u : 576u;   // data row bytes
+    static constexpr uint32_t S = kRecord == 528 ? 16u : 8u;      // scale row bytes
 };
+
+// Read-only loads that do not allocate in L1 (each record is read once).
+__device__ __forceinline__ uint2 ldg_na8(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint4 ldg_na16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_u8(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
 
 // Lane-parallel decode of one group of 32 indices: for this lane's index, the
 // record's byte offset in the cache (-1 when the index is -1 or out of range) and the
@@ -65,129 +80,129 @@ __device__ __forceinline__ void decode_group(const GatherParams& p, const WarpIt
     if (__ballot_sync(kFull, bad) != 0u && lane == 0) report(p.err, 4);
 }
 
-// Stage this half-warp's record (byte offset `off`, -1 = none) into ring slot
-// `it % S`, half `h`; then close one commit group (every lane, every iteration).
-template <int kRecord, int S>
-__device__ __forceinline__ void stage(const GatherParams& p, uint8_t* ring, int it, int h, int q,
-                                      int64_t off, int32_t delta) {
-    using R = Rec<kRecord>;
-    if (off >= 0) {
-        const uint8_t* data = p.cache + off;
-        uint8_t* dst = ring + (it & (S - 1)) * (2 * R::kItem) + h * R::kItem + q * R::kLane;
-        if (kRecord == 528 || q < 14) {
-            cp_async16(dst, data + 32 * q);
-            cp_async16(dst + 16, data + 32 * q + 16);
-        } else {                                   // V4 bf16 tail: dims 448..511
-            const uint8_t* t = data + 448 + 64 * (q - 14);
-            cp_async16(dst, t);
-            cp_async16(dst + 16, t + 16);
-            cp_async16(dst + 32, t + 32);
-            cp_async16(dst + 48, t + 48);
+struct Loaded {
+    uint2 a;        // codes of chunk A
+    uint4 b;        // codes of chunk B (.x, .y) or, for the V4 tail lanes, 8 bf16
+    uint32_t sa, sb;
+    bool valid;
+};
+
+template <int kRecord>
+__device__ __forceinline__ void load_record(const GatherParams& p, int64_t off, int32_t delta,
+                                            int lane, Loaded& r) {
+    r.valid = off >= 0;
+    if (!r.valid) return;
+    const uint8_t* data = p.cache + off;
+    const uint8_t* srow = data + delta;
+    r.a = ldg_na8(data + 8 * lane);
+    if (kRecord == 528) {
+        const uint2 t = ldg_na8(data + 256 + 8 * lane);
+        r.b = make_uint4(t.x, t.y, 0u, 0u);
+        r.sa = ldg_u8(srow + (lane >> 2));
+        r.sb = ldg_u8(srow + 8 + (lane >> 2));
+    } else {
+        if (lane < 24) {
+            const uint2 t = ldg_na8(data + 256 + 8 * lane);
+            r.b = make_uint4(t.x, t.y, 0u, 0u);
+            r.sb = ldg_u8(srow + 4 + (lane >> 3));
+        } else {
+            r.b = ldg_na16(data + 448 + 16 * (lane - 24));
+            r.sb = 0u;
         }
-        if (q == 0) {
-            uint8_t* sdst = ring + (it & (S - 1)) * (2 * R::kItem) + h * R::kItem + R::kScale;
-            if (kRecord == 528) cp_async16(sdst, data + delta);
-            else cp_async8(sdst, data + delta);
-        }
+        r.sa = ldg_u8(srow + (lane >> 3));
     }
-    cp_async_commit();
 }
 
-template <int kRecord, int S>
-__global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) gather_kernel(const GatherParams p, const WorkMap m) {
-    static_assert((S & (S - 1)) == 0 && S >= 2 && S <= 16, "ring depth: power of two <= 16");
-    using R = Rec<kRecord>;
-    extern __shared__ __align__(16) uint8_t smem[];
+template <int kRecord>
+__device__ __forceinline__ void convert_store(const Loaded& r, uint8_t* orow, int lane) {
+    uint4 oa = make_uint4(0u, 0u, 0u, 0u), ob = oa;
+    if (r.valid) {
+        oa = dequant8(r.a, r.sa);
+        if (kRecord == 528 || lane < 24) ob = dequant8(make_uint2(r.b.x, r.b.y), r.sb);
+        else ob = r.b;
+    }
+    st_stream16(orow + 16 * lane, oa);
+    st_stream16(orow + 512 + 16 * lane, ob);
+}
+
+template <int kRecord, int P>
+__device__ __forceinline__ void load_batch(const GatherParams& p, int j, int n, bool same,
+                                           int64_t cur_off, int32_t cur_delta, int64_t nxt_off,
+                                           int32_t nxt_delta, int lane, Loaded* r) {
+#pragma unroll
+    for (int u = 0; u < P; ++u) {
+        const int64_t off = __shfl_sync(kFull, same ? cur_off : nxt_off, (j + u) & 31);
+        const int32_t delta = __shfl_sync(kFull, same ? cur_delta : nxt_delta, (j + u) & 31);
+        load_record<kRecord>(p, j + u < n ? off : -1, delta, lane, r[u]);
+    }
+}
+
+template <int kRecord, int P>
+__global__ void __launch_bounds__(kThreads, kRecord == 584 ? 3 : GKR_MIN_BLOCKS) gather_kernel(const GatherParams p,
+                                                                          const WorkMap m) {
+    static_assert((P & (P - 1)) == 0 && P >= 1 && P <= 16, "batch: power of two <= 16");
     pdl_wait_previous();
     pdl_release_next();
     const int lane = threadIdx.x & 31;
-    const int h = lane >> 4, q = lane & 15;
-    const int wib = threadIdx.x >> 5;
-    const WarpItems w = warp_items(m, static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib);
+    const WarpItems w = warp_items(m, static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock +
+                                          (threadIdx.x >> 5));
     if (w.n <= 0) return;  // warp-uniform
     const int n = w.n;
-    const int iters = (n + 1) >> 1;
-    uint8_t* ring = smem + wib * (S * 2 * R::kItem);
+    uint8_t* out = static_cast<uint8_t*>(p.out);
 
+    // cur describes the group (32 items) holding the batch being converted, nxt the next
     int64_t cur_off, nxt_off;
     int32_t cur_delta, nxt_delta;
     decode_group<kRecord>(p, w, 0, lane, cur_off, cur_delta);
     decode_group<kRecord>(p, w, 1, lane, nxt_off, nxt_delta);
-#pragma unroll
-    for (int k = 0; k < S - 1; ++k) {        // prologue: iterations 0 .. S-2 (group 0)
-        const int64_t off = __shfl_sync(kFull, cur_off, 2 * k + h);
-        const int32_t delta = __shfl_sync(kFull, cur_delta, 2 * k + h);
-        stage<kRecord, S>(p, ring, k, h, q, k < iters ? off : -1, delta);
-    }
-    uint8_t* out = static_cast<uint8_t*>(p.out);
-    for (int it = 0; it < iters; ++it) {
-        const int k = it + S - 1;
-        __syncwarp();                         // every lane is done reading ring slot k % S
-        {
-            const bool same = (k >> 4) == (it >> 4);
-            const int src = (2 * k + h) & 31;
-            const int64_t off = __shfl_sync(kFull, same ? cur_off : nxt_off, src);
-            const int32_t delta = __shfl_sync(kFull, same ? cur_delta : nxt_delta, src);
-            stage<kRecord, S>(p, ring, k, h, q, k < iters ? off : -1, delta);
-        }
-        cp_async_wait<S - 1>();               // this lane's copies of iteration `it` landed
-        __syncwarp();                         // ... and every other lane's
 
-        const int i = 2 * it + h;             // this half's item
-        const int64_t off = __shfl_sync(kFull, cur_off, (2 * it + h) & 31);
-        const uint8_t* slot = ring + (it & (S - 1)) * (2 * R::kItem) + h * R::kItem;
-        uint32_t o[16];
+    // Batches of P items [j, j + P), aligned so a batch never straddles two groups.
+    Loaded A[P], B[P];
+    load_batch<kRecord, P>(p, 0, n, true, cur_off, cur_delta, nxt_off, nxt_delta, lane, A);
+    for (int j0 = 0; j0 < n; j0 += 2 * P) {
+        const int j1 = j0 + P, j2 = j0 + 2 * P;
+        load_batch<kRecord, P>(p, j1, n, (j1 >> 5) == (j0 >> 5), cur_off, cur_delta, nxt_off,
+                               nxt_delta, lane, B);
 #pragma unroll
-        for (int t = 0; t < 16; ++t) o[t] = 0u;
-        if (off >= 0) {
-            const uint8_t* src = slot + q * R::kLane;
-            if (kRecord == 528 || q < 14) {
-                const uint4 a = lds16(src), b = lds16(src + 16);
-                const uint32_t c[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                dequant32(c, slot[R::kScale + (kRecord == 528 ? q : (q >> 1))], o);
-            } else {
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const uint4 v = lds16(src + 16 * t);
-                    o[4 * t] = v.x; o[4 * t + 1] = v.y; o[4 * t + 2] = v.z; o[4 * t + 3] = v.w;
-                }
-            }
-        }
-        if (i < n) {
-            uint8_t* orow = out + w.at(i) * 1024 + 64 * q;
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-                st_stream16(orow + 16 * t, make_uint4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]));
-        }
-        if ((it & 15) == 15) {
+        for (int u = 0; u < P; ++u)
+            if (j0 + u < n) convert_store<kRecord>(A[u], out + w.at(j0 + u) * 1024, lane);
+        if ((j1 & 31) == 0) {                // batch j1 opens a new group
             cur_off = nxt_off;
             cur_delta = nxt_delta;
-            decode_group<kRecord>(p, w, (it >> 4) + 2, lane, nxt_off, nxt_delta);
+            decode_group<kRecord>(p, w, (j1 >> 5) + 1, lane, nxt_off, nxt_delta);
+        }
+        load_batch<kRecord, P>(p, j2, n, (j2 >> 5) == (j1 >> 5), cur_off, cur_delta, nxt_off,
+                               nxt_delta, lane, A);
+#pragma unroll
+        for (int u = 0; u < P; ++u)
+            if (j1 + u < n) convert_store<kRecord>(B[u], out + w.at(j1 + u) * 1024, lane);
+        if ((j2 & 31) == 0) {                // batch j2 opens a new group
+            cur_off = nxt_off;
+            cur_delta = nxt_delta;
+            decode_group<kRecord>(p, w, (j2 >> 5) + 1, lane, nxt_off, nxt_delta);
         }
     }
-    cp_async_wait<0>();
 }
 
-template <int kRecord, int S>
+template <int kRecord, int P>
 cudaError_t launch(const GatherParams& p, cudaStream_t stream) {
     if (p.num_indices <= 0) return cudaSuccess;
-    auto kernel = gather_kernel<kRecord, S>;
-    const size_t smem = static_cast<size_t>(kWarpsPerBlock) * S * 2 * Rec<kRecord>::kItem;
+    auto kernel = gather_kernel<kRecord, P>;
     int64_t wave = 0;
-    cudaError_t e = resident_warps(reinterpret_cast<const void*>(kernel), kThreads, smem, &wave);
+    cudaError_t e = resident_warps(reinterpret_cast<const void*>(kernel), kThreads, 0, &wave);
     if (e != cudaSuccess) return e;
-    const WorkMap m = make_work_map(p.num_indices, wave, GKR_GATHER_CYCLIC != 0, 2);
+    const WorkMap m = make_work_map(p.num_indices, wave, GKR_GATHER_CYCLIC != 0);
     const int64_t blocks = (m.warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    return launch_kernel(kernel, blocks, kThreads, smem, stream, p, m);
+    return launch_kernel(kernel, blocks, kThreads, 0, stream, p, m);
 }
 
 }  // namespace
 
 cudaError_t launch_gather_v41(const GatherParams& p, cudaStream_t stream) {
-    return launch<528, kGatherDepth>(p, stream);
+    return launch<528, kBatch>(p, stream);
 }
 cudaError_t launch_gather_v4(const GatherParams& p, cudaStream_t stream) {
-    return launch<584, kGatherDepth>(p, stream);
+    return launch<584, kBatch>(p, stream);
 }
 
 }  // namespace gkr

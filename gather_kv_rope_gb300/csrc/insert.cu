@@ -8,18 +8,16 @@
 // store e4m3 codes in the page's data region and the scale bytes in its scale region.
 //
 // Launch shape (GB300): at most one wave of warps (sized from the occupancy), each
-// walking its own list of tokens (see WorkMap), two tokens per iteration -- one per
-// half-warp, lane q of a half owning dims [32q, 32q + 32), i.e. one V4.1 scale block
-// (half a V4 block).  Per group of 32 tokens, lane i decodes token i's slot and
-// position once.  A per-warp shared-memory ring filled by cp.async keeps S iterations
-// in flight; each lane copies the 64 bytes of its block (padded by 16 bytes so the
-// 16-byte shared loads of 8 consecutive lanes hit distinct bank groups) and 16 bytes
-// of the cos/sin row.  The 32 rotated pairs are computed by all 16 lanes (two pairs
-// each) and handed to the two lanes owning dims 448..511 through a small per-warp
-// scratch area.  The grid depends only on T and the device, so large inserts keep
-// every SM streaming (the pages' reduced-grid kernel idled 7 of 8 warps above ~16k
-// tokens; page "PR #56441 [Perf][DSpark] KV-only context insertion across V4.1 cache
-// formats", review notes).
+// walking its own list of tokens (see WorkMap); one warp per token, lane L owning dims
+// [8L, 8L+8) and [256+8L, 256+8L+8).  Per group of 32 tokens, lane i decodes token i's
+// slot and position once (data-row offset, scale-row distance, checked position), so
+// a token costs a few shuffles plus its own work.  A per-warp shared-memory ring filled
+// by cp.async keeps S tokens in flight; every copy instruction moves one contiguous
+// 512-byte piece of the kv row (or the 128-byte cos/sin halves), and every store one
+// contiguous 256-byte piece of the record.  The grid depends only on T and the
+// device, so large inserts keep every SM streaming (the pages' reduced-grid kernel
+// idled 7 of 8 warps above ~16k tokens; page "PR #56441 [Perf][DSpark] KV-only context
+// insertion across V4.1 cache formats", review notes).
 #include "device.cuh"
 #include "launch.h"
 
@@ -28,18 +26,74 @@ namespace gkr {
 namespace {
 
 #ifndef GKR_INSERT_DEPTH
-#define GKR_INSERT_DEPTH 2
+#define GKR_INSERT_DEPTH 4
 #endif
 #ifndef GKR_INSERT_CYCLIC
 #define GKR_INSERT_CYCLIC 0
 #endif
-constexpr int kInsertDepth = GKR_INSERT_DEPTH;  // iterations (token pairs) in flight per warp
+constexpr int kInsertDepth = GKR_INSERT_DEPTH;  // tokens in flight per warp
+constexpr int kSlotBytes = 1024 + 256;          // staged kv row + cos/sin row
 
-constexpr int kKvLane = 80;                     // a lane's 64-byte block of the kv row + 16 pad
-constexpr int kCscOff = 16 * kKvLane;           // cos/sin row offset in a staged token
-constexpr int kTokBytes = kCscOff + 256;        // staged bytes per token
-constexpr int kRotSeg = 144;                    // 32 rotated fp32 (128 B) + 16 pad
-constexpr int kRotBytes = 4 * kRotSeg;          // per warp: 2 tokens x 2 rope lanes
+struct TokenLoads {
+    uint4 a, b;       // bf16 chunks A and B
+    float4 c, s;      // cos / sin of the 4 pairs in chunk B (lanes 24..31 only)
+};
+
+// V4.1: 16 blocks of 32 dims.  Chunk A of lane L is in block L/4, chunk B in 8 + L/4.
+__device__ __forceinline__ void encode_store_v41(const TokenLoads& L, uint8_t* data, uint8_t* srow,
+                                                 int lane) {
+    float a[8], b[8];
+    unpack_bf16x8(L.a, a);
+    unpack_bf16x8(L.b, b);
+    if (lane >= 24) rope4(b, L.c, L.s);  // dims 448..511 = pairs 4(L-24) .. 4(L-24)+3
+
+    float ma = amax8(a), mb = amax8(b);
+    ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, 1));
+    mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 1));
+    ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, 2));
+    mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 2));
+    const uint32_t ba = ue8m0_byte(ma), bb = ue8m0_byte(mb);
+
+    st8(data + 8 * lane, quantise8(a, ba));
+    st8(data + 256 + 8 * lane, quantise8(b, bb));
+    if ((lane & 3) == 0) {
+        srow[lane >> 2] = static_cast<uint8_t>(ba);
+        srow[8 + (lane >> 2)] = static_cast<uint8_t>(bb);
+    }
+}
+
+// V4: 7 blocks of 64 NoPE dims (chunk A of lane L in block L/8; chunk B of lanes 0..23
+// in block 4 + L/8), rotated dims 448..511 (chunk B of lanes 24..31) stored as bf16.
+__device__ __forceinline__ void encode_store_v4(const TokenLoads& L, uint8_t* data, uint8_t* srow,
+                                                int lane) {
+    float a[8], b[8];
+    unpack_bf16x8(L.a, a);
+    unpack_bf16x8(L.b, b);
+    const bool rope_lane = lane >= 24;
+    if (rope_lane) rope4(b, L.c, L.s);
+
+    float ma = amax8(a), mb = rope_lane ? 0.0f : amax8(b);
+#pragma unroll
+    for (int x = 1; x <= 4; x <<= 1) {
+        ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, x));
+        mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, x));
+    }
+    const uint32_t ba = ue8m0_byte(ma), bb = ue8m0_byte(mb);
+
+    st8(data + 8 * lane, quantise8(a, ba));
+    if (!rope_lane) {
+        st8(data + 256 + 8 * lane, quantise8(b, bb));
+    } else {
+        st16(data + 448 + 16 * (lane - 24),
+             make_uint4(pack_bf16x2_rn(b[0], b[1]), pack_bf16x2_rn(b[2], b[3]),
+                        pack_bf16x2_rn(b[4], b[5]), pack_bf16x2_rn(b[6], b[7])));
+    }
+    if ((lane & 7) == 0) {
+        srow[lane >> 3] = static_cast<uint8_t>(ba);                        // blocks 0..3
+        if (!rope_lane) srow[4 + (lane >> 3)] = static_cast<uint8_t>(bb);  // blocks 4..6
+        else srow[7] = 0;                                                  // pad byte
+    }
+}
 
 // Lane-parallel decode of one group of 32 tokens: for this lane's token, the byte
 // offset of its data row in the cache (-1 when the token is skipped or invalid), the
@@ -77,41 +131,37 @@ __device__ __forceinline__ void decode_group(const InsertParams& p, const WarpIt
     if (err != 0 && lane == 0) report(p.err, err);
 }
 
-// Stage this half-warp's token (item i, valid when off >= 0) into ring slot it % S:
-// lane q copies dims [32q, 32q + 32) of the kv row and bytes [16q, 16q + 16) of the
-// cos/sin row.  Then close one commit group (every lane, every iteration).
+// Stage token k (kv row + cos/sin row) into ring slot k % S, then close one group.
 template <int S>
 __device__ __forceinline__ void stage(const InsertParams& p, uint8_t* ring, const WarpItems& w,
-                                      int it, int h, int q, bool valid, int32_t pos) {
+                                      int k, bool valid, int32_t pos, int lane) {
     if (valid) {
-        uint8_t* dst = ring + (it & (S - 1)) * (2 * kTokBytes) + h * kTokBytes;
-        const uint8_t* row = static_cast<const uint8_t*>(p.kv) + w.at(2 * it + h) * 1024 + 64 * q;
-        uint8_t* d = dst + q * kKvLane;
-        cp_async16(d, row);
-        cp_async16(d + 16, row + 16);
-        cp_async16(d + 32, row + 32);
-        cp_async16(d + 48, row + 48);
-        cp_async16(dst + kCscOff + 16 * q,
-                   reinterpret_cast<const uint8_t*>(p.csc) + static_cast<int64_t>(pos) * 256 + 16 * q);
+        uint8_t* dst = ring + (k & (S - 1)) * kSlotBytes;
+        const uint8_t* row = static_cast<const uint8_t*>(p.kv) + w.at(k) * 1024;
+        cp_async16(dst + 16 * lane, row + 16 * lane);
+        cp_async16(dst + 512 + 16 * lane, row + 512 + 16 * lane);
+        if (lane >= 24) {
+            const float* cs = p.csc + static_cast<int64_t>(pos) * 64 + 4 * (lane - 24);
+            cp_async16(dst + 1024 + 16 * (lane - 24), cs);
+            cp_async16(dst + 1024 + 128 + 16 * (lane - 24), cs + 32);
+        }
     }
     cp_async_commit();
 }
 
 template <int kRecord, int S>
-__global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const InsertParams p, const WorkMap m) {
+__global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const InsertParams p,
+                                                                          const WorkMap m) {
     static_assert((S & (S - 1)) == 0 && S >= 2 && S <= 16, "ring depth: power of two <= 16");
     extern __shared__ __align__(16) uint8_t smem[];
     pdl_wait_previous();
     pdl_release_next();
     const int lane = threadIdx.x & 31;
-    const int h = lane >> 4, q = lane & 15;
     const int wib = threadIdx.x >> 5;
     const WarpItems w = warp_items(m, static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib);
     if (w.n <= 0) return;  // warp-uniform
-    const int iters = (w.n + 1) >> 1;
-    uint8_t* ring = smem + wib * (S * 2 * kTokBytes + kRotBytes);
-    uint8_t* rot = ring + S * 2 * kTokBytes;
-    const bool rope_lane = q >= 14;             // owns dims 448..479 (q = 14) or 480..511
+    const int n = w.n;
+    uint8_t* ring = smem + wib * (S * kSlotBytes);
 
     // lane i of cur describes token 32*g + i of the group being processed; nxt the next
     int64_t cur_off, nxt_off;
@@ -120,97 +170,41 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
     decode_group<kRecord>(p, w, 1, lane, nxt_off, nxt_delta, nxt_pos);
 
 #pragma unroll
-    for (int k = 0; k < S - 1; ++k) {           // prologue: iterations 0 .. S-2 (group 0)
-        const bool valid = __shfl_sync(kFull, cur_off, 2 * k + h) >= 0 && k < iters;
-        const int32_t pos = __shfl_sync(kFull, cur_pos, 2 * k + h);
-        stage<S>(p, ring, w, k, h, q, valid, pos);
+    for (int k = 0; k < S - 1; ++k) {          // prologue: tokens 0 .. S-2 (group 0)
+        const bool valid = __shfl_sync(kFull, cur_off, k) >= 0;
+        const int32_t pos = __shfl_sync(kFull, cur_pos, k);
+        stage<S>(p, ring, w, k, valid && k < n, pos, lane);
     }
-    for (int it = 0; it < iters; ++it) {
-        const int k = it + S - 1;
-        __syncwarp();                            // every lane is done reading ring slot k % S
+    for (int j = 0; j < n; ++j) {
+        const int k = j + S - 1;                // token staged this iteration
         {
-            const bool same = (k >> 4) == (it >> 4);
-            const int src = (2 * k + h) & 31;
-            const bool valid = __shfl_sync(kFull, same ? cur_off : nxt_off, src) >= 0 && k < iters;
-            const int32_t pos = __shfl_sync(kFull, same ? cur_pos : nxt_pos, src);
-            stage<S>(p, ring, w, k, h, q, valid, pos);
+            const bool same = (k >> 5) == (j >> 5);
+            const bool valid = __shfl_sync(kFull, same ? cur_off : nxt_off, k & 31) >= 0;
+            const int32_t pos = __shfl_sync(kFull, same ? cur_pos : nxt_pos, k & 31);
+            stage<S>(p, ring, w, k, valid && k < n, pos, lane);
         }
-        cp_async_wait<S - 1>();                  // this lane's copies of iteration `it` landed
-        __syncwarp();                            // ... and every other lane's
+        cp_async_wait<S - 1>();                 // this lane's copies of token j have landed
 
-        const int src = (2 * it + h) & 31;
-        const int64_t off = __shfl_sync(kFull, cur_off, src);
-        const int32_t delta = __shfl_sync(kFull, cur_delta, src);
-        const bool valid = off >= 0;             // uniform per half-warp
-        const uint8_t* tok = ring + (it & (S - 1)) * (2 * kTokBytes) + h * kTokBytes;
-
-        // RoPE, two pairs per lane: pairs 2q, 2q+1 = dims 448 + 4q .. 448 + 4q + 3, which
-        // sit in the staged block of lane 14 + q/8 at byte 8 * (q % 8).
-        if (valid) {
-            const uint2 e = lds8(tok + (14 + (q >> 3)) * kKvLane + 8 * (q & 7));
-            const uint2 cb = lds8(tok + kCscOff + 8 * q);
-            const uint2 sb = lds8(tok + kCscOff + 128 + 8 * q);
-            float f[4] = {__uint_as_float(e.x << 16), __uint_as_float(e.x & 0xFFFF0000u),
-                          __uint_as_float(e.y << 16), __uint_as_float(e.y & 0xFFFF0000u)};
-            rope2(f, make_float2(__uint_as_float(cb.x), __uint_as_float(cb.y)),
-                  make_float2(__uint_as_float(sb.x), __uint_as_float(sb.y)));
-            *reinterpret_cast<float4*>(rot + (2 * h + (q >> 3)) * kRotSeg + 16 * (q & 7)) =
-                make_float4(f[0], f[1], f[2], f[3]);
-        }
-        __syncwarp();
-
-        float v[32];
-        if (valid) {
-            if (!rope_lane) {
-                const uint8_t* b = tok + q * kKvLane;
-#pragma unroll
-                for (int t = 0; t < 4; ++t) unpack_bf16x8(lds16(b + 16 * t), v + 8 * t);
-            } else {
-                const uint8_t* r = rot + (2 * h + (q - 14)) * kRotSeg;
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const float4 x = *reinterpret_cast<const float4*>(r + 16 * t);
-                    v[4 * t] = x.x; v[4 * t + 1] = x.y; v[4 * t + 2] = x.z; v[4 * t + 3] = x.w;
-                }
+        const int64_t off = __shfl_sync(kFull, cur_off, j & 31);
+        const int32_t delta = __shfl_sync(kFull, cur_delta, j & 31);
+        if (off >= 0) {                         // warp-uniform
+            const uint8_t* src = ring + (j & (S - 1)) * kSlotBytes;
+            TokenLoads L;
+            L.a = lds16(src + 16 * lane);
+            L.b = lds16(src + 512 + 16 * lane);
+            if (lane >= 24) {
+                L.c = *reinterpret_cast<const float4*>(src + 1024 + 16 * (lane - 24));
+                L.s = *reinterpret_cast<const float4*>(src + 1024 + 128 + 16 * (lane - 24));
             }
-        } else {
-#pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] = 0.0f;
-        }
-        float amax = amax32(v);
-        if (kRecord == 584) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));  // 64-dim blocks
-        const uint32_t byte = ue8m0_byte(amax);
-
-        if (valid) {
             uint8_t* data = p.cache + off;
-            uint8_t* srow = data + delta;
-            if (kRecord == 528 || !rope_lane) {
-                uint4 lo, hi;
-                quantise32(v, byte, lo, hi);
-                st16(data + 32 * q, lo);
-                st16(data + 32 * q + 16, hi);
-            } else {                             // V4: rotated dims stored as bf16
-                uint8_t* t = data + 448 + 64 * (q - 14);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    st16(t + 16 * c, make_uint4(pack_bf16x2_rn(v[8 * c], v[8 * c + 1]),
-                                                pack_bf16x2_rn(v[8 * c + 2], v[8 * c + 3]),
-                                                pack_bf16x2_rn(v[8 * c + 4], v[8 * c + 5]),
-                                                pack_bf16x2_rn(v[8 * c + 6], v[8 * c + 7])));
-            }
-            if (kRecord == 528) {
-                srow[q] = static_cast<uint8_t>(byte);
-            } else if (q < 14) {
-                if ((q & 1) == 0) srow[q >> 1] = static_cast<uint8_t>(byte);   // blocks 0..6
-            } else if (q == 14) {
-                srow[7] = 0;                                                  // pad byte
-            }
+            if (kRecord == 528) encode_store_v41(L, data, data + delta, lane);
+            else encode_store_v4(L, data, data + delta, lane);
         }
-        if ((it & 15) == 15) {                   // move to the next group of 32 tokens
+        if ((j & 31) == 31) {                   // move to the next group of 32 tokens
             cur_off = nxt_off;
             cur_delta = nxt_delta;
             cur_pos = nxt_pos;
-            decode_group<kRecord>(p, w, (it >> 4) + 2, lane, nxt_off, nxt_delta, nxt_pos);
+            decode_group<kRecord>(p, w, (j >> 5) + 2, lane, nxt_off, nxt_delta, nxt_pos);
         }
     }
     cp_async_wait<0>();
@@ -220,11 +214,11 @@ template <int kRecord, int S>
 cudaError_t launch(const InsertParams& p, cudaStream_t stream) {
     if (p.num_tokens <= 0) return cudaSuccess;
     auto kernel = insert_kernel<kRecord, S>;
-    const size_t smem = static_cast<size_t>(kWarpsPerBlock) * (S * 2 * kTokBytes + kRotBytes);
+    const size_t smem = static_cast<size_t>(kWarpsPerBlock) * S * kSlotBytes;
     int64_t wave = 0;
     cudaError_t e = resident_warps(reinterpret_cast<const void*>(kernel), kThreads, smem, &wave);
     if (e != cudaSuccess) return e;
-    const WorkMap m = make_work_map(p.num_tokens, wave, GKR_INSERT_CYCLIC != 0, 2);
+    const WorkMap m = make_work_map(p.num_tokens, wave, GKR_INSERT_CYCLIC != 0);
     const int64_t blocks = (m.warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     return launch_kernel(kernel, blocks, kThreads, smem, stream, p, m);
 }
