@@ -76,6 +76,9 @@ def lib() -> ctypes.CDLL:
                 L.gkr_version.argtypes, L.gkr_version.restype = [], i32
                 L.gkr_set_pdl.argtypes, L.gkr_set_pdl.restype = [i32], None
                 L.gkr_get_pdl.argtypes, L.gkr_get_pdl.restype = [], i32
+                L.gkr_set_insert_stream_min.argtypes = [i64]
+                L.gkr_set_insert_stream_min.restype = None
+                L.gkr_get_insert_stream_min.argtypes, L.gkr_get_insert_stream_min.restype = [], i64
                 _lib = L
     return _lib
 
@@ -101,6 +104,15 @@ def set_pdl(enable: bool) -> None:
 
 def get_pdl() -> bool:
     return bool(lib().gkr_get_pdl())
+
+
+def set_insert_stream_min(tokens: int) -> None:
+    """Token count from which inserts use the streaming kernel (negative = default)."""
+    lib().gkr_set_insert_stream_min(int(tokens))
+
+
+def get_insert_stream_min() -> int:
+    return int(lib().gkr_get_insert_stream_min())
 
 
 def page_stride(record: int, block_size: int) -> int:

@@ -12,6 +12,8 @@ namespace {
 
 thread_local int32_t g_last_cuda_error = 0;
 std::atomic<int> g_pdl{1};
+constexpr int64_t kDefaultStreamMin = 131072;
+std::atomic<int64_t> g_stream_min{kDefaultStreamMin};
 
 struct OccEntry {
     int device;
@@ -63,6 +65,8 @@ namespace gkr {
 
 bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
 
+int64_t insert_stream_min() { return g_stream_min.load(std::memory_order_relaxed); }
+
 cudaError_t resident_warps(const void* func, int threads, size_t smem, int64_t* warps) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -98,6 +102,12 @@ extern "C" {
 GKR_API void gkr_set_pdl(int32_t enable) { g_pdl.store(enable ? 1 : 0); }
 
 GKR_API int32_t gkr_get_pdl(void) { return g_pdl.load() ? 1 : 0; }
+
+GKR_API void gkr_set_insert_stream_min(int64_t tokens) {
+    g_stream_min.store(tokens < 0 ? kDefaultStreamMin : tokens);
+}
+
+GKR_API int64_t gkr_get_insert_stream_min(void) { return g_stream_min.load(); }
 
 GKR_API int64_t gkr_page_stride(int32_t record, int32_t block_size) {
     RecordRows r;

@@ -84,30 +84,12 @@ __device__ __forceinline__ void rope4(float* f, const float4 c, const float4 s) 
     }
 }
 
-// Rotate two adjacent pairs (f[0], f[1]) and (f[2], f[3]) by (c[i], s[i]):
-// even' = e*c - o*s, odd' = o*c + e*s; every product and sum is a separately
-// rounded fp32 operation (the _rn intrinsics are never contracted into FMA).
-__device__ __forceinline__ void rope2(float f[4], const float2 c, const float2 s) {
-    const float e0 = f[0], o0 = f[1], e1 = f[2], o1 = f[3];
-    f[0] = __fsub_rn(__fmul_rn(e0, c.x), __fmul_rn(o0, s.x));
-    f[1] = __fadd_rn(__fmul_rn(o0, c.x), __fmul_rn(e0, s.x));
-    f[2] = __fsub_rn(__fmul_rn(e1, c.y), __fmul_rn(o1, s.y));
-    f[3] = __fadd_rn(__fmul_rn(o1, c.y), __fmul_rn(e1, s.y));
-}
-
 // ---------------------------------------------------------------- MXFP8 encode
 
 __device__ __forceinline__ float amax8(const float* f) {
     float m = fabsf(f[0]);
 #pragma unroll
     for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
-    return m;
-}
-
-__device__ __forceinline__ float amax32(const float* f) {
-    float m = fabsf(f[0]);
-#pragma unroll
-    for (int i = 1; i < 32; ++i) m = fmaxf(m, fabsf(f[i]));
     return m;
 }
 
@@ -145,18 +127,6 @@ __device__ __forceinline__ uint2 quantise8(const float* f, uint32_t byte) {
     q.x = e4m3x4(__fmul_rn(f[0], k), __fmul_rn(f[1], k), __fmul_rn(f[2], k), __fmul_rn(f[3], k));
     q.y = e4m3x4(__fmul_rn(f[4], k), __fmul_rn(f[5], k), __fmul_rn(f[6], k), __fmul_rn(f[7], k));
     return q;
-}
-
-// Quantise 32 values with their block's scale byte -> 32 e4m3 bytes (two uint4).
-__device__ __forceinline__ void quantise32(const float* f, uint32_t byte, uint4& lo, uint4& hi) {
-    const float k = inv_scale(byte);
-    uint32_t q[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        q[i] = e4m3x4(__fmul_rn(f[4 * i], k), __fmul_rn(f[4 * i + 1], k),
-                      __fmul_rn(f[4 * i + 2], k), __fmul_rn(f[4 * i + 3], k));
-    lo = make_uint4(q[0], q[1], q[2], q[3]);
-    hi = make_uint4(q[4], q[5], q[6], q[7]);
 }
 
 // ---------------------------------------------------------------- MXFP8 decode
@@ -202,14 +172,8 @@ __device__ __forceinline__ void dequant4(uint32_t w, const Dequant& d, uint32_t&
     // bytes 1 and 3 (bit 15 / 31)
     uint32_t a = __byte_perm(x, 0u, 0x4140u) * 16u + __byte_perm(sg, 0u, 0x1404u);
     uint32_t b = __byte_perm(x, 0u, 0x4342u) * 16u + __byte_perm(sg, 0u, 0x3424u);
-    a = bf16x2_mul(a, d.m1);
-    b = bf16x2_mul(b, d.m1);
-    if (d.split) {
-        a = bf16x2_mul(a, d.m2);
-        b = bf16x2_mul(b, d.m2);
-    }
-    o01 = a;
-    o23 = b;
+    o01 = bf16x2_mul(a, d.m1);
+    o23 = bf16x2_mul(b, d.m1);
 }
 
 // Bytes of w whose low 7 bits are all ones (the e4m3 NaN codes) -> 0x80 in that byte.
@@ -225,40 +189,47 @@ __device__ __forceinline__ void patch_nan(uint32_t nanmask, uint32_t& o01, uint3
     if (nanmask & 0x80000000u) o23 = (o23 & 0x0000FFFFu) | (kBf16NaN << 16);
 }
 
-// 8 e4m3 codes (2 words) with one UE8M0 scale byte -> 8 bf16 (uint4).
-__device__ __forceinline__ uint4 dequant8(const uint2 c, uint32_t byte) {
+// General path of dequant8: any scale byte (two multiplies above 134, NaN for 255)
+// and NaN codes.  Kept out of line: the common path handles bytes <= 134 without
+// NaN codes with one multiply per pair and a single test.
+#ifndef GKR_GENERAL_INLINE
+#define GKR_GENERAL_INLINE 1
+#endif
+#if GKR_GENERAL_INLINE
+__device__ __forceinline__
+#else
+__device__ __noinline__
+#endif
+uint4 dequant8_general(uint2 c, uint32_t byte) {
+    const uint32_t n = kBf16NaN | (kBf16NaN << 16);
+    if (byte == 255u) return make_uint4(n, n, n, n);
     const Dequant d = make_dequant(byte);
     uint4 o;
     dequant4(c.x, d, o.x, o.y);
     dequant4(c.y, d, o.z, o.w);
-    const uint32_t acc = ((c.x & 0x7F7F7F7Fu) + 0x01010101u) | ((c.y & 0x7F7F7F7Fu) + 0x01010101u);
-    if ((acc & 0x80808080u) != 0u || d.nan_scale) {   // rare: corrupt or NaN-marked records
-        if (d.nan_scale) {
-            const uint32_t n = kBf16NaN | (kBf16NaN << 16);
-            return make_uint4(n, n, n, n);
-        }
-        patch_nan(e4m3_nan_bytes(c.x), o.x, o.y);
-        patch_nan(e4m3_nan_bytes(c.y), o.z, o.w);
+    if (d.split) {
+        o.x = bf16x2_mul(o.x, d.m2);
+        o.y = bf16x2_mul(o.y, d.m2);
+        o.z = bf16x2_mul(o.z, d.m2);
+        o.w = bf16x2_mul(o.w, d.m2);
     }
+    patch_nan(e4m3_nan_bytes(c.x), o.x, o.y);
+    patch_nan(e4m3_nan_bytes(c.y), o.z, o.w);
     return o;
 }
 
-// 32 e4m3 codes (8 words) with one UE8M0 scale byte -> 32 bf16 (16 words).
-__device__ __forceinline__ void dequant32(const uint32_t* c, uint32_t byte, uint32_t* o) {
-    const Dequant d = make_dequant(byte);
-    uint32_t acc = 0u;   // bit 7 of a byte ends up set iff some code in that lane is NaN
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        dequant4(c[i], d, o[2 * i], o[2 * i + 1]);
-        acc |= (c[i] & 0x7F7F7F7Fu) + 0x01010101u;
-    }
-    if ((acc & 0x80808080u) != 0u || d.nan_scale) {   // rare: corrupt or NaN-marked records
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (d.nan_scale) o[2 * i] = o[2 * i + 1] = kBf16NaN | (kBf16NaN << 16);
-            else patch_nan(e4m3_nan_bytes(c[i]), o[2 * i], o[2 * i + 1]);
-        }
-    }
+// 8 e4m3 codes (2 words) with one UE8M0 scale byte -> 8 bf16 (uint4).
+__device__ __forceinline__ uint4 dequant8(const uint2 c, uint32_t byte) {
+    // bit 7 of a byte of acc is set iff that code is a NaN (low 7 bits all ones)
+    const uint32_t acc = ((c.x & 0x7F7F7F7Fu) + 0x01010101u) | ((c.y & 0x7F7F7F7Fu) + 0x01010101u);
+    if (__builtin_expect((acc & 0x80808080u) != 0u || byte > 134u, 0))
+        return dequant8_general(c, byte);
+    const uint32_t m = (byte + 120u) * 0x00800080u;   // bf16 2^(byte - 7), both halves
+    const Dequant d = {m, 0u, false, false};
+    uint4 o;
+    dequant4(c.x, d, o.x, o.y);
+    dequant4(c.y, d, o.z, o.w);
+    return o;
 }
 
 __device__ __forceinline__ void report(int32_t* err, int32_t bits) {

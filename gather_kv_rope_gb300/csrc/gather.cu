@@ -6,14 +6,11 @@
 // V4.1, 448 dims in 64-dim groups plus a copied bf16 tail for V4; FlashMLA overview
 // page, DSA section: an index of -1 is an invalid entry, which emits zeros).
 //
-// Launch shape: at most one wave of warps, each walking its own list of indices
-// (see WorkMap); one warp per record, lane L owning output dims [8L, 8L+8) and
-// [256+8L, 256+8L+8).  Per group of 32 indices, lane i decodes index i once
-// (validity, the record's byte offset, the distance to its scale row), so a record
-// costs three shuffles, four coalesced loads (two 8-byte code pieces, two scale
-// bytes), the dequantisation and two 16-byte streaming stores.  Records are loaded
-// straight into registers in batches of P, the next batch's loads issued before the
-// current batch is converted, so 2P records per warp are in flight.
+// Launch shape: one warp per record, lane L owning output dims [8L, 8L+8) and
+// [256+8L, 256+8L+8), U records per warp, all their loads issued before the first is
+// converted.  Every load and store instruction covers one contiguous 256- or 512-byte
+// span.  A random-record gather is latency-bound, so the kernel favours many resident
+// warps (few registers) over deep per-warp pipelines.
 #include "device.cuh"
 #include "launch.h"
 
@@ -21,13 +18,10 @@ namespace gkr {
 
 namespace {
 
-#ifndef GKR_GATHER_BATCH
-#define GKR_GATHER_BATCH 2
+#ifndef GKR_GATHER_PER_WARP
+#define GKR_GATHER_PER_WARP 2
 #endif
-#ifndef GKR_GATHER_CYCLIC
-#define GKR_GATHER_CYCLIC 0
-#endif
-constexpr int kBatch = GKR_GATHER_BATCH;   // records per batch (a power of two <= 16)
+constexpr int kPerWarp = GKR_GATHER_PER_WARP;   // records per warp
 
 template <int kRecord>
 struct Rec {
@@ -54,32 +48,6 @@ __device__ __forceinline__ uint32_t ldg_u8(const void* p) {
     return v;
 }
 
-// Lane-parallel decode of one group of 32 indices: for this lane's index, the
-// record's byte offset in the cache (-1 when the index is -1 or out of range) and the
-// distance from the data row to the scale row.  Out-of-range indices set GKR_ERR_INDEX.
-template <int kRecord>
-__device__ __forceinline__ void decode_group(const GatherParams& p, const WarpItems& w, int g,
-                                             int lane, int64_t& off, int32_t& delta) {
-    using R = Rec<kRecord>;
-    const int i = 32 * g + lane;
-    off = -1;
-    delta = 0;
-    bool bad = false;
-    if (i < w.n) {
-        const int32_t idx = __ldg(p.indices + w.at(i));
-        if (idx >= 0 && idx < p.num_slots) {
-            const uint32_t s = static_cast<uint32_t>(idx);
-            const uint32_t bs = static_cast<uint32_t>(p.block_size);
-            const uint32_t page = s / bs, row = s - page * bs;
-            off = static_cast<int64_t>(page) * p.page_stride + row * R::D;
-            delta = static_cast<int32_t>(bs * R::D + row * R::S - row * R::D);
-        } else {
-            bad = idx != -1;
-        }
-    }
-    if (__ballot_sync(kFull, bad) != 0u && lane == 0) report(p.err, 4);
-}
-
 struct Loaded {
     uint2 a;        // codes of chunk A
     uint4 b;        // codes of chunk B (.x, .y) or, for the V4 tail lanes, 8 bf16
@@ -87,29 +55,31 @@ struct Loaded {
     bool valid;
 };
 
+// Per-lane base pointers: every load of a record is one 64-bit add away.
+struct LaneBases {
+    const uint8_t* a;      // cache + 8L: chunk A codes (chunk B at +256)
+    const uint8_t* tail;   // V4, lanes 24..31: cache + 448 + 16 (L - 24)
+    const uint8_t* s;      // cache + scale byte of chunk A (chunk B's at +8 / +4)
+};
+
 template <int kRecord>
-__device__ __forceinline__ void load_record(const GatherParams& p, int64_t off, int32_t delta,
+__device__ __forceinline__ void load_record(int64_t off, int64_t soff, const LaneBases& lb,
                                             int lane, Loaded& r) {
     r.valid = off >= 0;
     if (!r.valid) return;
-    const uint8_t* data = p.cache + off;
-    const uint8_t* srow = data + delta;
-    r.a = ldg_na8(data + 8 * lane);
+    r.a = ldg_na8(lb.a + off);
+    r.sa = ldg_u8(lb.s + soff);
     if (kRecord == 528) {
-        const uint2 t = ldg_na8(data + 256 + 8 * lane);
+        const uint2 t = ldg_na8(lb.a + off + 256);
         r.b = make_uint4(t.x, t.y, 0u, 0u);
-        r.sa = ldg_u8(srow + (lane >> 2));
-        r.sb = ldg_u8(srow + 8 + (lane >> 2));
+        r.sb = ldg_u8(lb.s + soff + 8);
+    } else if (lane < 24) {
+        const uint2 t = ldg_na8(lb.a + off + 256);
+        r.b = make_uint4(t.x, t.y, 0u, 0u);
+        r.sb = ldg_u8(lb.s + soff + 4);
     } else {
-        if (lane < 24) {
-            const uint2 t = ldg_na8(data + 256 + 8 * lane);
-            r.b = make_uint4(t.x, t.y, 0u, 0u);
-            r.sb = ldg_u8(srow + 4 + (lane >> 3));
-        } else {
-            r.b = ldg_na16(data + 448 + 16 * (lane - 24));
-            r.sb = 0u;
-        }
-        r.sa = ldg_u8(srow + (lane >> 3));
+        r.b = ldg_na16(lb.tail + off);
+        r.sb = 0u;
     }
 }
 
@@ -121,88 +91,71 @@ __device__ __forceinline__ void convert_store(const Loaded& r, uint8_t* orow, in
         if (kRecord == 528 || lane < 24) ob = dequant8(make_uint2(r.b.x, r.b.y), r.sb);
         else ob = r.b;
     }
-    st_stream16(orow + 16 * lane, oa);
-    st_stream16(orow + 512 + 16 * lane, ob);
+    st_stream16(orow, oa);
+    st_stream16(orow + 512, ob);
 }
 
-template <int kRecord, int P>
-__device__ __forceinline__ void load_batch(const GatherParams& p, int j, int n, bool same,
-                                           int64_t cur_off, int32_t cur_delta, int64_t nxt_off,
-                                           int32_t nxt_delta, int lane, Loaded* r) {
-#pragma unroll
-    for (int u = 0; u < P; ++u) {
-        const int64_t off = __shfl_sync(kFull, same ? cur_off : nxt_off, (j + u) & 31);
-        const int32_t delta = __shfl_sync(kFull, same ? cur_delta : nxt_delta, (j + u) & 31);
-        load_record<kRecord>(p, j + u < n ? off : -1, delta, lane, r[u]);
-    }
-}
-
-template <int kRecord, int P>
-__global__ void __launch_bounds__(kThreads, kRecord == 584 ? 3 : GKR_MIN_BLOCKS) gather_kernel(const GatherParams p,
-                                                                          const WorkMap m) {
-    static_assert((P & (P - 1)) == 0 && P >= 1 && P <= 16, "batch: power of two <= 16");
+// One warp per U consecutive indices; lanes 0..U-1 decode them in parallel and the
+// offsets are broadcast with shuffles, so each record costs two shuffles, four loads,
+// the dequantisation and two stores.  Short-lived warps (U records each) keep many
+// warps resident and let the block scheduler balance the end of a large gather.
+template <int kRecord, int U>
+__global__ void __launch_bounds__(kThreads, kRecord == 584 ? 6 : 8)
+    gather_kernel(const GatherParams p) {
     pdl_wait_previous();
     pdl_release_next();
     const int lane = threadIdx.x & 31;
-    const WarpItems w = warp_items(m, static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock +
-                                          (threadIdx.x >> 5));
-    if (w.n <= 0) return;  // warp-uniform
-    const int n = w.n;
-    uint8_t* out = static_cast<uint8_t*>(p.out);
+    const int64_t i0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * U;
+    if (i0 >= p.num_indices) return;  // warp-uniform
 
-    // cur describes the group (32 items) holding the batch being converted, nxt the next
-    int64_t cur_off, nxt_off;
-    int32_t cur_delta, nxt_delta;
-    decode_group<kRecord>(p, w, 0, lane, cur_off, cur_delta);
-    decode_group<kRecord>(p, w, 1, lane, nxt_off, nxt_delta);
-
-    // Batches of P items [j, j + P), aligned so a batch never straddles two groups.
-    Loaded A[P], B[P];
-    load_batch<kRecord, P>(p, 0, n, true, cur_off, cur_delta, nxt_off, nxt_delta, lane, A);
-    for (int j0 = 0; j0 < n; j0 += 2 * P) {
-        const int j1 = j0 + P, j2 = j0 + 2 * P;
-        load_batch<kRecord, P>(p, j1, n, (j1 >> 5) == (j0 >> 5), cur_off, cur_delta, nxt_off,
-                               nxt_delta, lane, B);
-#pragma unroll
-        for (int u = 0; u < P; ++u)
-            if (j0 + u < n) convert_store<kRecord>(A[u], out + w.at(j0 + u) * 1024, lane);
-        if ((j1 & 31) == 0) {                // batch j1 opens a new group
-            cur_off = nxt_off;
-            cur_delta = nxt_delta;
-            decode_group<kRecord>(p, w, (j1 >> 5) + 1, lane, nxt_off, nxt_delta);
-        }
-        load_batch<kRecord, P>(p, j2, n, (j2 >> 5) == (j1 >> 5), cur_off, cur_delta, nxt_off,
-                               nxt_delta, lane, A);
-#pragma unroll
-        for (int u = 0; u < P; ++u)
-            if (j1 + u < n) convert_store<kRecord>(B[u], out + w.at(j1 + u) * 1024, lane);
-        if ((j2 & 31) == 0) {                // batch j2 opens a new group
-            cur_off = nxt_off;
-            cur_delta = nxt_delta;
-            decode_group<kRecord>(p, w, (j2 >> 5) + 1, lane, nxt_off, nxt_delta);
+    // lane u < U decodes index i0 + u: data-row offset (-1 = emit zeros), scale-row offset
+    int64_t off = -1, soff = 0;
+    bool bad = false;
+    if (lane < U && i0 + lane < p.num_indices) {
+        using R = Rec<kRecord>;
+        const int32_t idx = __ldg(p.indices + i0 + lane);
+        if (idx >= 0 && idx < p.num_slots) {
+            const uint32_t s = static_cast<uint32_t>(idx);
+            const uint32_t bs = static_cast<uint32_t>(p.block_size);
+            const uint32_t page = s / bs, row = s - page * bs;
+            const int64_t base = static_cast<int64_t>(page) * p.page_stride;
+            off = base + row * R::D;
+            soff = base + bs * R::D + row * R::S;
+        } else {
+            bad = idx != -1;
         }
     }
+    if (__ballot_sync(kFull, bad) != 0u && lane == 0) report(p.err, 4);
+
+    LaneBases lb;
+    lb.a = p.cache + 8 * lane;
+    lb.tail = p.cache + 448 + 16 * (lane >= 24 ? lane - 24 : 0);
+    lb.s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
+    Loaded r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        load_record<kRecord>(__shfl_sync(kFull, off, u), __shfl_sync(kFull, soff, u), lb, lane, r[u]);
+    uint8_t* orow = static_cast<uint8_t*>(p.out) + i0 * 1024 + 16 * lane;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (i0 + u < p.num_indices) convert_store<kRecord>(r[u], orow + u * 1024, lane);
 }
 
-template <int kRecord, int P>
+template <int kRecord, int U>
 cudaError_t launch(const GatherParams& p, cudaStream_t stream) {
     if (p.num_indices <= 0) return cudaSuccess;
-    auto kernel = gather_kernel<kRecord, P>;
-    int64_t wave = 0;
-    cudaError_t e = resident_warps(reinterpret_cast<const void*>(kernel), kThreads, 0, &wave);
-    if (e != cudaSuccess) return e;
-    const WorkMap m = make_work_map(p.num_indices, wave, GKR_GATHER_CYCLIC != 0);
-    const int64_t blocks = (m.warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    return launch_kernel(kernel, blocks, kThreads, 0, stream, p, m);
+    const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * U;
+    const int64_t blocks = (p.num_indices + per_block - 1) / per_block;
+    return launch_kernel(gather_kernel<kRecord, U>, blocks, kThreads, 0, stream, p);
 }
 
 }  // namespace
 
 cudaError_t launch_gather_v41(const GatherParams& p, cudaStream_t stream) {
-    return launch<528, kBatch>(p, stream);
+    return launch<528, kPerWarp>(p, stream);
 }
 cudaError_t launch_gather_v4(const GatherParams& p, cudaStream_t stream) {
-    return launch<584, kBatch>(p, stream);
+    return launch<584, kPerWarp>(p, stream);
 }
 
 }  // namespace gkr

@@ -28,6 +28,10 @@ namespace {
 #ifndef GKR_INSERT_DEPTH
 #define GKR_INSERT_DEPTH 4
 #endif
+#ifndef GKR_INSERT_MAX_CHUNK
+#define GKR_INSERT_MAX_CHUNK 16  // tokens per streaming warp at most (0 = one wave)
+#endif
+
 #ifndef GKR_INSERT_CYCLIC
 #define GKR_INSERT_CYCLIC 0
 #endif
@@ -40,7 +44,8 @@ struct TokenLoads {
 };
 
 // V4.1: 16 blocks of 32 dims.  Chunk A of lane L is in block L/4, chunk B in 8 + L/4.
-__device__ __forceinline__ void encode_store_v41(const TokenLoads& L, uint8_t* data, uint8_t* srow,
+// `da` = data row + 8L (chunk B's codes go to da + 256); `sl` = scale row + L/4.
+__device__ __forceinline__ void encode_store_v41(const TokenLoads& L, uint8_t* da, uint8_t* sl,
                                                  int lane) {
     float a[8], b[8];
     unpack_bf16x8(L.a, a);
@@ -54,17 +59,18 @@ __device__ __forceinline__ void encode_store_v41(const TokenLoads& L, uint8_t* d
     mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 2));
     const uint32_t ba = ue8m0_byte(ma), bb = ue8m0_byte(mb);
 
-    st8(data + 8 * lane, quantise8(a, ba));
-    st8(data + 256 + 8 * lane, quantise8(b, bb));
+    st8(da, quantise8(a, ba));
+    st8(da + 256, quantise8(b, bb));
     if ((lane & 3) == 0) {
-        srow[lane >> 2] = static_cast<uint8_t>(ba);
-        srow[8 + (lane >> 2)] = static_cast<uint8_t>(bb);
+        sl[0] = static_cast<uint8_t>(ba);
+        sl[8] = static_cast<uint8_t>(bb);
     }
 }
 
 // V4: 7 blocks of 64 NoPE dims (chunk A of lane L in block L/8; chunk B of lanes 0..23
 // in block 4 + L/8), rotated dims 448..511 (chunk B of lanes 24..31) stored as bf16.
-__device__ __forceinline__ void encode_store_v4(const TokenLoads& L, uint8_t* data, uint8_t* srow,
+// `da` = data row + 8L; `sl` = scale row + L/8.
+__device__ __forceinline__ void encode_store_v4(const TokenLoads& L, uint8_t* da, uint8_t* sl,
                                                 int lane) {
     float a[8], b[8];
     unpack_bf16x8(L.a, a);
@@ -80,33 +86,33 @@ __device__ __forceinline__ void encode_store_v4(const TokenLoads& L, uint8_t* da
     }
     const uint32_t ba = ue8m0_byte(ma), bb = ue8m0_byte(mb);
 
-    st8(data + 8 * lane, quantise8(a, ba));
+    st8(da, quantise8(a, ba));
     if (!rope_lane) {
-        st8(data + 256 + 8 * lane, quantise8(b, bb));
-    } else {
-        st16(data + 448 + 16 * (lane - 24),
+        st8(da + 256, quantise8(b, bb));
+    } else {  // dims 448 + 8(L-24) .. as bf16 at data + 448 + 16(L-24) = da + 64 + 8L
+        st16(da + 64 + 8 * lane,
              make_uint4(pack_bf16x2_rn(b[0], b[1]), pack_bf16x2_rn(b[2], b[3]),
                         pack_bf16x2_rn(b[4], b[5]), pack_bf16x2_rn(b[6], b[7])));
     }
     if ((lane & 7) == 0) {
-        srow[lane >> 3] = static_cast<uint8_t>(ba);                        // blocks 0..3
-        if (!rope_lane) srow[4 + (lane >> 3)] = static_cast<uint8_t>(bb);  // blocks 4..6
-        else srow[7] = 0;                                                  // pad byte
+        sl[0] = static_cast<uint8_t>(ba);                 // blocks 0..3
+        if (!rope_lane) sl[4] = static_cast<uint8_t>(bb);  // blocks 4..6
+        else sl[4] = 0;                                    // lane 24: L/8 = 3, byte 7 = pad
     }
 }
 
 // Lane-parallel decode of one group of 32 tokens: for this lane's token, the byte
-// offset of its data row in the cache (-1 when the token is skipped or invalid), the
-// distance from the data row to the scale row, and its position.  Invalid slots and
-// positions set GKR_ERR_SLOT / GKR_ERR_POS (one atomic per group at most).
+// offsets in the cache of its data row (-1 when the token is skipped or invalid) and
+// of its scale row, and its position.  Invalid slots and positions set GKR_ERR_SLOT /
+// GKR_ERR_POS (one atomic per group at most).
 template <int kRecord>
 __device__ __forceinline__ void decode_group(const InsertParams& p, const WarpItems& w, int g,
-                                             int lane, int64_t& off, int32_t& delta, int32_t& pos) {
+                                             int lane, int64_t& off, int64_t& soff, int32_t& pos) {
     constexpr uint32_t D = kRecord == 528 ? 512u : 576u;
     constexpr uint32_t S = kRecord == 528 ? 16u : 8u;
     const int i = 32 * g + lane;
     off = -1;
-    delta = 0;
+    soff = 0;
     pos = 0;
     int32_t err = 0;
     if (i < w.n) {
@@ -121,8 +127,9 @@ __device__ __forceinline__ void decode_group(const InsertParams& p, const WarpIt
                 const uint32_t s = static_cast<uint32_t>(slot);
                 const uint32_t bs = static_cast<uint32_t>(p.block_size);
                 const uint32_t page = s / bs, row = s - page * bs;
-                off = static_cast<int64_t>(page) * p.page_stride + row * D;
-                delta = static_cast<int32_t>(bs * D + row * S - row * D);
+                const int64_t base = static_cast<int64_t>(page) * p.page_stride;
+                off = base + row * D;
+                soff = base + bs * D + row * S;
                 pos = static_cast<int32_t>(q);
             }
         }
@@ -132,18 +139,21 @@ __device__ __forceinline__ void decode_group(const InsertParams& p, const WarpIt
 }
 
 // Stage token k (kv row + cos/sin row) into ring slot k % S, then close one group.
+// `kv_lane` = this warp's first kv row + 16L, `kv_step` = bytes between its rows,
+// `ring_lane` = ring + 16L, `csc_lane` = cos/sin table + 4(L-24) floats.
 template <int S>
-__device__ __forceinline__ void stage(const InsertParams& p, uint8_t* ring, const WarpItems& w,
-                                      int k, bool valid, int32_t pos, int lane) {
+__device__ __forceinline__ void stage(const uint8_t* kv_lane, int32_t kv_step, uint8_t* ring_lane,
+                                      const float* csc_lane, int k, bool valid, int32_t pos,
+                                      int lane) {
     if (valid) {
-        uint8_t* dst = ring + (k & (S - 1)) * kSlotBytes;
-        const uint8_t* row = static_cast<const uint8_t*>(p.kv) + w.at(k) * 1024;
-        cp_async16(dst + 16 * lane, row + 16 * lane);
-        cp_async16(dst + 512 + 16 * lane, row + 512 + 16 * lane);
-        if (lane >= 24) {
-            const float* cs = p.csc + static_cast<int64_t>(pos) * 64 + 4 * (lane - 24);
-            cp_async16(dst + 1024 + 16 * (lane - 24), cs);
-            cp_async16(dst + 1024 + 128 + 16 * (lane - 24), cs + 32);
+        uint8_t* dst = ring_lane + (k & (S - 1)) * kSlotBytes;
+        const uint8_t* row = kv_lane + static_cast<int64_t>(k) * kv_step;
+        cp_async16(dst, row);
+        cp_async16(dst + 512, row + 512);
+        if (lane >= 24) {  // cos / sin of pairs 4(L-24) .. +3 -> ring + 1024 + 16(L-24)
+            const float* cs = csc_lane + static_cast<int64_t>(pos) * 64;
+            cp_async16(dst + 1024 - 16 * 24, cs);
+            cp_async16(dst + 1024 + 128 - 16 * 24, cs + 32);
         }
     }
     cp_async_commit();
@@ -161,19 +171,24 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
     const WarpItems w = warp_items(m, static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib);
     if (w.n <= 0) return;  // warp-uniform
     const int n = w.n;
-    uint8_t* ring = smem + wib * (S * kSlotBytes);
+    uint8_t* const ring_lane = smem + wib * (S * kSlotBytes) + 16 * lane;
+    const uint8_t* const kv_lane = static_cast<const uint8_t*>(p.kv) + w.base * 1024 + 16 * lane;
+    const int32_t kv_step = static_cast<int32_t>(w.step * 1024);
+    const float* const csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
+    uint8_t* const cache_a = p.cache + 8 * lane;                                   // data row + 8L
+    uint8_t* const cache_s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3)); // scale byte
 
     // lane i of cur describes token 32*g + i of the group being processed; nxt the next
-    int64_t cur_off, nxt_off;
-    int32_t cur_delta, nxt_delta, cur_pos, nxt_pos;
-    decode_group<kRecord>(p, w, 0, lane, cur_off, cur_delta, cur_pos);
-    decode_group<kRecord>(p, w, 1, lane, nxt_off, nxt_delta, nxt_pos);
+    int64_t cur_off, nxt_off, cur_soff, nxt_soff;
+    int32_t cur_pos, nxt_pos;
+    decode_group<kRecord>(p, w, 0, lane, cur_off, cur_soff, cur_pos);
+    decode_group<kRecord>(p, w, 1, lane, nxt_off, nxt_soff, nxt_pos);
 
 #pragma unroll
     for (int k = 0; k < S - 1; ++k) {          // prologue: tokens 0 .. S-2 (group 0)
         const bool valid = __shfl_sync(kFull, cur_off, k) >= 0;
         const int32_t pos = __shfl_sync(kFull, cur_pos, k);
-        stage<S>(p, ring, w, k, valid && k < n, pos, lane);
+        stage<S>(kv_lane, kv_step, ring_lane, csc_lane, k, valid && k < n, pos, lane);
     }
     for (int j = 0; j < n; ++j) {
         const int k = j + S - 1;                // token staged this iteration
@@ -181,44 +196,123 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
             const bool same = (k >> 5) == (j >> 5);
             const bool valid = __shfl_sync(kFull, same ? cur_off : nxt_off, k & 31) >= 0;
             const int32_t pos = __shfl_sync(kFull, same ? cur_pos : nxt_pos, k & 31);
-            stage<S>(p, ring, w, k, valid && k < n, pos, lane);
+            stage<S>(kv_lane, kv_step, ring_lane, csc_lane, k, valid && k < n, pos, lane);
         }
         cp_async_wait<S - 1>();                 // this lane's copies of token j have landed
 
         const int64_t off = __shfl_sync(kFull, cur_off, j & 31);
-        const int32_t delta = __shfl_sync(kFull, cur_delta, j & 31);
         if (off >= 0) {                         // warp-uniform
-            const uint8_t* src = ring + (j & (S - 1)) * kSlotBytes;
+            const int64_t soff = __shfl_sync(kFull, cur_soff, j & 31);
+            const uint8_t* src = ring_lane + (j & (S - 1)) * kSlotBytes;
             TokenLoads L;
-            L.a = lds16(src + 16 * lane);
-            L.b = lds16(src + 512 + 16 * lane);
+            L.a = lds16(src);
+            L.b = lds16(src + 512);
             if (lane >= 24) {
-                L.c = *reinterpret_cast<const float4*>(src + 1024 + 16 * (lane - 24));
-                L.s = *reinterpret_cast<const float4*>(src + 1024 + 128 + 16 * (lane - 24));
+                L.c = *reinterpret_cast<const float4*>(src + 1024 - 16 * 24);
+                L.s = *reinterpret_cast<const float4*>(src + 1024 + 128 - 16 * 24);
             }
-            uint8_t* data = p.cache + off;
-            if (kRecord == 528) encode_store_v41(L, data, data + delta, lane);
-            else encode_store_v4(L, data, data + delta, lane);
+            if (kRecord == 528) encode_store_v41(L, cache_a + off, cache_s + soff, lane);
+            else encode_store_v4(L, cache_a + off, cache_s + soff, lane);
         }
         if ((j & 31) == 31) {                   // move to the next group of 32 tokens
             cur_off = nxt_off;
-            cur_delta = nxt_delta;
+            cur_soff = nxt_soff;
             cur_pos = nxt_pos;
-            decode_group<kRecord>(p, w, (j >> 5) + 2, lane, nxt_off, nxt_delta, nxt_pos);
+            decode_group<kRecord>(p, w, (j >> 5) + 2, lane, nxt_off, nxt_soff, nxt_pos);
         }
     }
     cp_async_wait<0>();
 }
 
-template <int kRecord, int S>
+// Short-lived warps for small and medium inserts: one warp per U consecutive tokens,
+// lanes 0..U-1 decode them in parallel, all loads (kv rows and cos/sin rows) go
+// straight to registers before the first token is encoded.  Below a few hundred
+// thousand tokens an insert is latency-bound, and many small resident warps beat a
+// deep per-warp pipeline.
+template <int kRecord, int U>
+__global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_short_kernel(const InsertParams p) {
+    pdl_wait_previous();
+    pdl_release_next();
+    const int lane = threadIdx.x & 31;
+    const int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * U;
+    if (t0 >= p.num_tokens) return;  // warp-uniform
+    constexpr uint32_t D = kRecord == 528 ? 512u : 576u;
+    constexpr uint32_t S = kRecord == 528 ? 16u : 8u;
+
+    // lane u < U decodes token t0 + u
+    int64_t off = -1, soff = 0;
+    int32_t pos = 0;
+    uint32_t err = 0;
+    if (lane < U && t0 + lane < p.num_tokens) {
+        const int64_t slot = __ldg(p.slots + t0 + lane);
+        const int64_t q = __ldg(p.positions + t0 + lane);
+        if (slot >= p.num_slots) {
+            err = 1;
+        } else if (slot >= 0) {
+            if (q < 0 || q >= p.max_pos) {
+                err = 2;
+            } else {
+                const uint32_t s = static_cast<uint32_t>(slot);
+                const uint32_t bs = static_cast<uint32_t>(p.block_size);
+                const uint32_t page = s / bs, row = s - page * bs;
+                const int64_t base = static_cast<int64_t>(page) * p.page_stride;
+                off = base + row * D;
+                soff = base + bs * D + row * S;
+                pos = static_cast<int32_t>(q);
+            }
+        }
+    }
+    err = __reduce_or_sync(kFull, err);
+    if (err != 0u && lane == 0) report(p.err, static_cast<int32_t>(err));
+
+    const uint8_t* kv_lane = static_cast<const uint8_t*>(p.kv) + t0 * 1024 + 16 * lane;
+    const float* csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
+    TokenLoads L[U];
+    bool valid[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        valid[u] = __shfl_sync(kFull, off, u) >= 0;
+        const int32_t q = __shfl_sync(kFull, pos, u);
+        if (valid[u]) {
+            L[u].a = ld_stream16(kv_lane + u * 1024);
+            L[u].b = ld_stream16(kv_lane + u * 1024 + 512);
+            if (lane >= 24) {
+                const float* cs = csc_lane + static_cast<int64_t>(q) * 64;
+                L[u].c = ld_ro_f4(cs);
+                L[u].s = ld_ro_f4(cs + 32);
+            }
+        }
+    }
+    uint8_t* const cache_a = p.cache + 8 * lane;
+    uint8_t* const cache_s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t o = __shfl_sync(kFull, off, u);
+        const int64_t so = __shfl_sync(kFull, soff, u);
+        if (valid[u]) {
+            if (kRecord == 528) encode_store_v41(L[u], cache_a + o, cache_s + so, lane);
+            else encode_store_v4(L[u], cache_a + o, cache_s + so, lane);
+        }
+    }
+}
+
+template <int kRecord>
 cudaError_t launch(const InsertParams& p, cudaStream_t stream) {
     if (p.num_tokens <= 0) return cudaSuccess;
+    if (p.num_tokens < insert_stream_min()) {
+        constexpr int U = 2;
+        const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * U;
+        const int64_t blocks = (p.num_tokens + per_block - 1) / per_block;
+        return launch_kernel(insert_short_kernel<kRecord, U>, blocks, kThreads, 0, stream, p);
+    }
+    constexpr int S = kInsertDepth;
     auto kernel = insert_kernel<kRecord, S>;
     const size_t smem = static_cast<size_t>(kWarpsPerBlock) * S * kSlotBytes;
     int64_t wave = 0;
     cudaError_t e = resident_warps(reinterpret_cast<const void*>(kernel), kThreads, smem, &wave);
     if (e != cudaSuccess) return e;
-    const WorkMap m = make_work_map(p.num_tokens, wave, GKR_INSERT_CYCLIC != 0);
+    const WorkMap m = make_work_map(p.num_tokens, wave, GKR_INSERT_CYCLIC != 0, 1,
+                                    GKR_INSERT_MAX_CHUNK);
     const int64_t blocks = (m.warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     return launch_kernel(kernel, blocks, kThreads, smem, stream, p, m);
 }
@@ -226,10 +320,10 @@ cudaError_t launch(const InsertParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_insert_v41(const InsertParams& p, cudaStream_t stream) {
-    return launch<528, kInsertDepth>(p, stream);
+    return launch<528>(p, stream);
 }
 cudaError_t launch_insert_v4(const InsertParams& p, cudaStream_t stream) {
-    return launch<584, kInsertDepth>(p, stream);
+    return launch<584>(p, stream);
 }
 
 }  // namespace gkr

@@ -43,6 +43,8 @@ struct GatherParams {
 cudaError_t resident_warps(const void* func, int threads, size_t smem, int64_t* warps);
 // Whether launches carry the programmatic-dependent-launch attribute.
 bool pdl_enabled();
+// Token count from which inserts use the streaming kernel.
+int64_t insert_stream_min();
 
 // Launch `kernel` with the PDL attribute when enabled.
 template <typename... KArgs, typename... Args>
@@ -74,12 +76,16 @@ struct WorkMap {
     int32_t cyclic;   // 1 = cyclic, 0 = chunked
 };
 
-inline WorkMap make_work_map(int64_t n, int64_t wave_warps, bool cyclic, int64_t granule = 1) {
+// max_chunk caps the items per warp (chunked maps only): larger launches then become
+// several waves of short-lived warps, which the block scheduler balances at the end.
+inline WorkMap make_work_map(int64_t n, int64_t wave_warps, bool cyclic, int64_t granule = 1,
+                             int64_t max_chunk = 0) {
     WorkMap m;
     m.n = n;
     m.cyclic = cyclic ? 1 : 0;
     if (wave_warps < 1) wave_warps = 1;
     m.chunk = (n + wave_warps - 1) / wave_warps;
+    if (!cyclic && max_chunk > 0 && m.chunk > max_chunk) m.chunk = max_chunk;
     m.chunk = (m.chunk + granule - 1) / granule * granule;   // whole warp iterations
     m.warps = cyclic ? (n < wave_warps ? n : wave_warps) : (n + m.chunk - 1) / m.chunk;
     return m;

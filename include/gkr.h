@@ -165,6 +165,16 @@ GKR_API gkr_status gkr_kv_gather(const void *k_cache, const gkr_cache_desc *cach
 GKR_API void gkr_set_pdl(int32_t enable);
 GKR_API int32_t gkr_get_pdl(void);
 
+/*
+ * Insert launch policy (process-wide).  Inserts of at least `tokens` tokens use the
+ * streaming kernel (a per-warp shared-memory pipeline over long runs of tokens);
+ * smaller inserts use short-lived warps of two tokens each.  Both write identical
+ * bytes; the split only trades latency against streaming depth.  Default 131072.
+ * A negative value restores the default.
+ */
+GKR_API void gkr_set_insert_stream_min(int64_t tokens);
+GKR_API int64_t gkr_get_insert_stream_min(void);
+
 /* Static, NUL-terminated description of a status code. */
 GKR_API const char *gkr_status_string(gkr_status status);
 

@@ -23,7 +23,8 @@ def declared_symbols() -> set[str]:
 def test_header_declares_the_boundary():
     syms = declared_symbols()
     assert {"gkr_kv_insert", "gkr_kv_gather", "gkr_page_stride", "gkr_record_rows",
-            "gkr_status_string", "gkr_last_cuda_error", "gkr_version"} <= syms
+            "gkr_status_string", "gkr_last_cuda_error", "gkr_version", "gkr_set_pdl",
+            "gkr_get_pdl", "gkr_set_insert_stream_min", "gkr_get_insert_stream_min"} <= syms
 
 
 def test_library_exports_every_declared_symbol(gkr):
@@ -51,6 +52,11 @@ def test_page_stride_and_rows(gkr):
     with pytest.raises(ValueError):
         gkr.record_rows(512)
     assert gkr.lib().gkr_version() == 10000
+    assert gkr.get_insert_stream_min() == 131072
+    gkr.set_insert_stream_min(5)
+    assert gkr.get_insert_stream_min() == 5
+    gkr.set_insert_stream_min(-1)
+    assert gkr.get_insert_stream_min() == 131072
     assert gkr.status_string(0) == "ok"
 
 

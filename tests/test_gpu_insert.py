@@ -18,6 +18,15 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
 
+@pytest.fixture(params=["short", "stream"], autouse=True)
+def insert_kernel_choice(request, gkr):
+    """Run every insert test with both insert kernels: short-lived warps (the default
+    below 131072 tokens) and the streaming pipeline (the default above)."""
+    gkr.set_insert_stream_min(1 << 62 if request.param == "short" else 0)
+    yield request.param
+    gkr.set_insert_stream_min(-1)
+
+
 def _compare_whole_cache(gkr, oracle_mod, case, pad_units=0):
     ps = case_page_stride(case, oracle_mod, pad_units)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
