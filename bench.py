@@ -585,7 +585,9 @@ def main(argv=None):
                        "gbs": gb / (r["gat_ms"] * 1e-3) / 1e9}}
     dom = "insert" if r["ins_ms"] >= r["gat_ms"] else "gather"
     ach = kern[dom]["gbs"]
-    kname = {"insert": "insert_kernel", "gather": "gather_kernel"}[dom]
+    stream_min = gkr.get_insert_stream_min()
+    kname = {"insert": "insert_kernel" if T >= stream_min else "insert_short_kernel",
+             "gather": "gather_kernel"}[dom]
     roofline = {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
                 "frac": ach / peak, "peak_source": peak_src,
                 "traffic": ncu_traffic(kname, WORKLOAD),
