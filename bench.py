@@ -66,6 +66,9 @@ def parse_args(argv=None):
                     help="run only this workload's kernel(s) a few times (for profiler "
                          "captures) and print their CUDA-event times")
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--insert-stream-min", type=int, default=None, metavar="TOKENS",
+                    help="token count from which inserts use the streaming kernel "
+                         "(default: the library's)")
     return ap.parse_args(argv)
 
 
@@ -403,26 +406,38 @@ def time_e2e(args, device, case):
 
 
 def sweep(device, peak):
-    """Kernel-only timings of the larger workloads (each > L2 or rotated), median of
-    CUDA-event-timed launches after warm-up."""
+    """Kernel-only timings of the larger workloads (each larger than L2, or rotated
+    over several input sets): launches captured back to back in a CUDA graph, the
+    graph replayed after warm-up, time per launch = CUDA-event time / launches.  No
+    host-side launch overhead is inside the measurement."""
     import torch
     import gather_kv_rope_gb300 as gkr
     import workloads as W
     res = {}
 
-    def timed(fn, sets, reps=20):
+    def timed(fn, sets, per_graph=12, replays=5):
         for k in range(3):
             fn(sets[k % len(sets)])
         torch.cuda.synchronize(device)
-        ts = []
-        for k in range(reps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn(sets[k % len(sets)])
-            b.record()
-            ts.append((a, b))
+        side = torch.cuda.Stream(device)
+        side.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(side):
+            fn(sets[0])
+        torch.cuda.current_stream(device).wait_stream(side)
         torch.cuda.synchronize(device)
-        return statistics.median(a.elapsed_time(b) for a, b in ts)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for k in range(per_graph):
+                fn(sets[k % len(sets)])
+        g.replay()
+        torch.cuda.synchronize(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(replays):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) / (per_graph * replays)
 
     for name, n_sets in (("insert_v4_65536", 3), ("insert_v41_262144", 1)):
         case = getattr(W, name)()
@@ -523,6 +538,8 @@ def run_profile(args):
     import workloads as W
     dev = torch.device("cuda:0")
     gkr.build()
+    if args.insert_stream_min is not None:
+        gkr.set_insert_stream_min(args.insert_stream_min)
     case = W.PROFILE_WORKLOADS[args.profile]()
     s = device_sets(case, dev, 1)[0]
     res = {"workload": args.profile}
@@ -571,6 +588,8 @@ def main(argv=None):
     dist = init_dist(world, "nccl")
     gkr.build()
     gkr.lib()
+    if args.insert_stream_min is not None:
+        gkr.set_insert_stream_min(args.insert_stream_min)
 
     peak, peak_src = measured_peaks()
     r = time_roundtrip(args, device, dist)

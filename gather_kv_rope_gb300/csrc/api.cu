@@ -12,7 +12,7 @@ namespace {
 
 thread_local int32_t g_last_cuda_error = 0;
 std::atomic<int> g_pdl{1};
-constexpr int64_t kDefaultStreamMin = 131072;
+constexpr int64_t kDefaultStreamMin = 32768;
 std::atomic<int64_t> g_stream_min{kDefaultStreamMin};
 
 struct OccEntry {

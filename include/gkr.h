@@ -169,7 +169,7 @@ GKR_API int32_t gkr_get_pdl(void);
  * Insert launch policy (process-wide).  Inserts of at least `tokens` tokens use the
  * streaming kernel (a per-warp shared-memory pipeline over long runs of tokens);
  * smaller inserts use short-lived warps of two tokens each.  Both write identical
- * bytes; the split only trades latency against streaming depth.  Default 131072.
+ * bytes; the split only trades latency against streaming depth.  Default 32768.
  * A negative value restores the default.
  */
 GKR_API void gkr_set_insert_stream_min(int64_t tokens);

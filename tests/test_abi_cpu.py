@@ -52,11 +52,11 @@ def test_page_stride_and_rows(gkr):
     with pytest.raises(ValueError):
         gkr.record_rows(512)
     assert gkr.lib().gkr_version() == 10000
-    assert gkr.get_insert_stream_min() == 131072
+    assert gkr.get_insert_stream_min() == 32768
     gkr.set_insert_stream_min(5)
     assert gkr.get_insert_stream_min() == 5
     gkr.set_insert_stream_min(-1)
-    assert gkr.get_insert_stream_min() == 131072
+    assert gkr.get_insert_stream_min() == 32768
     assert gkr.status_string(0) == "ok"
 
 

@@ -21,7 +21,7 @@ DEV = torch.device("cuda:0")
 @pytest.fixture(params=["short", "stream"], autouse=True)
 def insert_kernel_choice(request, gkr):
     """Run every insert test with both insert kernels: short-lived warps (the default
-    below 131072 tokens) and the streaming pipeline (the default above)."""
+    below 32768 tokens) and the streaming pipeline (the default from there on)."""
     gkr.set_insert_stream_min(1 << 62 if request.param == "short" else 0)
     yield request.param
     gkr.set_insert_stream_min(-1)
