@@ -343,8 +343,33 @@ def time_roundtrip(args, device, dist):
         ins, gat = eager_kernel_times(torch, gkr, case, sets, G, device)
         how = "CUDA events around eager launches queued behind a device sleep"
     clocks = sampler.summary(h0, h1)
-    return dict(case=case, K=K, total_ms=total_ms_max, ins_ms=float(np.mean(ins)),
-                gat_ms=float(np.mean(gat)), kernel_timing=how, clocks=clocks, T=T)
+    # per-kernel launch duration as the roofline uses it: the same kernel launched G
+    # times back to back over the rotating input sets in a graph of its own, CUDA
+    # events around 5 replays (no event nodes between the launches)
+    b2b = {}
+    for name, fn in (("insert", lambda s: gkr.kv_insert(s["kv"], s["cache"], s["slots"],
+                                                          s["pos"], s["csc"], case.block_size,
+                                                          case.record)),
+                     ("gather", lambda s: gkr.kv_gather(s["cache"], s["idx"], s["out"]))):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for k in range(G):
+                fn(sets[k % ROTATE])
+        g.replay()
+        torch.cuda.synchronize(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(5):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        b2b[name] = a.elapsed_time(b) / (5 * G)
+    return dict(case=case, K=K, total_ms=total_ms_max, ins_ms=b2b["insert"],
+                gat_ms=b2b["gather"], ins_iso_ms=float(np.mean(ins)),
+                gat_iso_ms=float(np.mean(gat)),
+                kernel_timing=(f"CUDA events around 5 replays of a graph of {G} back-to-back "
+                               "launches of the kernel alone over the same rotating input sets"),
+                iso_timing=how, clocks=clocks, T=T)
 
 
 def eager_kernel_times(torch, gkr, case, sets, n, device):
@@ -367,42 +392,99 @@ def _gpu_id(torch, device) -> str:
 def time_e2e(args, device, case):
     """Same metric through the public API from pinned host buffers: every step
     copies kv / slots / positions / indices to the device, inserts, gathers and
-    copies the gathered rows back, all inside the timed region."""
+    copies the gathered rows back, all inside the timed region.
+
+    Steps are pipelined the way a serving loop runs them: host->device copies on
+    one stream, kv_insert + kv_gather on another, device->host copies on a third,
+    with NB buffer sets so that step i+1's upload and step i-1's download overlap
+    step i's kernels.  Events order the three streams per buffer set (a set is
+    re-uploaded only after the kernels that read it finished, and its output is
+    overwritten only after its download finished).  The same steps issued one
+    after another on a single stream are timed too and reported as "serial"."""
     import torch
     import gather_kv_rope_gb300 as gkr
-    pin = dict(
-        kv=torch.from_numpy(case.kv.view(np.int16)).view(torch.bfloat16).pin_memory(),
-        slots=torch.from_numpy(case.slots).pin_memory(),
-        pos=torch.from_numpy(case.positions).pin_memory(),
-        idx=torch.from_numpy(case.indices).pin_memory())
-    out_h = torch.empty(case.indices.shape + (512,), dtype=torch.bfloat16).pin_memory()
-    d = {k: torch.empty_like(v, device=device) for k, v in pin.items()}
+    NB = 3
+    host = dict(
+        kv=torch.from_numpy(case.kv.view(np.int16)).view(torch.bfloat16),
+        slots=torch.from_numpy(case.slots),
+        pos=torch.from_numpy(case.positions),
+        idx=torch.from_numpy(case.indices))
+    pin = [{k: v.pin_memory() for k, v in host.items()} for _ in range(NB)]
+    out_shape = case.indices.shape + (512,)
+    out_h = [torch.empty(out_shape, dtype=torch.bfloat16).pin_memory() for _ in range(NB)]
+    d = [{k: torch.empty_like(v, device=device) for k, v in host.items()} for _ in range(NB)]
+    out = [torch.empty(out_shape, dtype=torch.bfloat16, device=device) for _ in range(NB)]
     csc = torch.from_numpy(case.csc).to(device)
     cache = gkr.alloc_cache(case.num_pages, case.block_size, case.record, device, fill=0)
-    out = torch.empty(case.indices.shape + (512,), dtype=torch.bfloat16, device=device)
-    h2d = sum(v.numel() * v.element_size() for v in pin.values())
-    d2h = out_h.numel() * out_h.element_size()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h[0].numel() * out_h[0].element_size()
+    s_up, s_run, s_down = (torch.cuda.Stream(device) for _ in range(3))
+    ev = lambda: torch.cuda.Event()
+    loaded, computed, drained = ([ev() for _ in range(NB)] for _ in range(3))
+    started = [False] * NB
 
-    def one():
-        for k in pin:
-            d[k].copy_(pin[k], non_blocking=True)
-        gkr.kv_insert(d["kv"], cache, d["slots"], d["pos"], csc, case.block_size, case.record)
-        gkr.kv_gather(cache, d["idx"], out)
-        out_h.copy_(out, non_blocking=True)
+    def kernels(b, stream):
+        with torch.cuda.stream(stream):
+            gkr.kv_insert(d[b]["kv"], cache, d[b]["slots"], d[b]["pos"], csc,
+                          case.block_size, case.record)
+            gkr.kv_gather(cache, d[b]["idx"], out[b])
 
-    for _ in range(5):
-        one()
-    torch.cuda.synchronize(device)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.e2e_steps):
-        one()
-    e1.record()
-    torch.cuda.synchronize(device)
-    ms = e0.elapsed_time(e1) / args.e2e_steps
+    def piped(i):
+        b = i % NB
+        if started[b]:
+            s_up.wait_event(computed[b])           # inputs of set b no longer read
+        with torch.cuda.stream(s_up):
+            for k in host:
+                d[b][k].copy_(pin[b][k], non_blocking=True)
+        loaded[b].record(s_up)
+        s_run.wait_event(loaded[b])
+        if started[b]:
+            s_run.wait_event(drained[b])           # out[b] downloaded by the last user
+        kernels(b, s_run)
+        computed[b].record(s_run)
+        s_down.wait_event(computed[b])
+        with torch.cuda.stream(s_down):
+            out_h[b].copy_(out[b], non_blocking=True)
+        drained[b].record(s_down)
+        started[b] = True
+
+    def serial(i):
+        b = i % NB
+        cur = torch.cuda.current_stream(device)
+        for k in host:
+            d[b][k].copy_(pin[b][k], non_blocking=True)
+        kernels(b, cur)
+        out_h[b].copy_(out[b], non_blocking=True)
+
+    def timed(step, n):
+        cur = torch.cuda.current_stream(device)
+        for i in range(5):
+            step(i)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        for s in (s_up, s_run, s_down):
+            s.wait_stream(cur)
+        for i in range(n):
+            step(i)
+        for s in (s_up, s_run, s_down):
+            cur.wait_stream(s)
+        e1.record(cur)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) / n
+
+    ms_serial = timed(serial, args.e2e_steps)
+    ms = timed(piped, args.e2e_steps)
+    # every step inserts and gathers the same inputs: each downloaded buffer must hold
+    # the same rows as the device-side result (a race between the streams shows here)
+    ref = out[0].cpu()
+    if not all(torch.equal(h.view(torch.int16), ref.view(torch.int16)) for h in out_h):
+        raise RuntimeError("pipelined end-to-end steps returned different results")
     return {"value": case.num_tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "steps": args.e2e_steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "path": "pinned host -> device copies, kv_insert, kv_gather, device -> pinned host"}
+            "serial": {"value": case.num_tokens / (ms_serial * 1e-3), "ms_per_step": ms_serial},
+            "path": "pinned host -> device copies, kv_insert, kv_gather, device -> pinned host; "
+                    f"three streams, {NB} buffer sets"}
 
 
 def sweep(device, peak):
@@ -599,9 +681,12 @@ def main(argv=None):
 
     ib, gb = insert_bytes(case.slots, 528), gather_bytes(case.indices, 528)
     kern = {"insert": {"us": r["ins_ms"] * 1e3, "alg_bytes": ib,
-                       "gbs": ib / (r["ins_ms"] * 1e-3) / 1e9},
+                       "gbs": ib / (r["ins_ms"] * 1e-3) / 1e9,
+                       "isolated_us": r["ins_iso_ms"] * 1e3},
             "gather": {"us": r["gat_ms"] * 1e3, "alg_bytes": gb,
-                       "gbs": gb / (r["gat_ms"] * 1e-3) / 1e9}}
+                       "gbs": gb / (r["gat_ms"] * 1e-3) / 1e9,
+                       "isolated_us": r["gat_iso_ms"] * 1e3},
+            "isolated_timing": r["iso_timing"]}
     dom = "insert" if r["ins_ms"] >= r["gat_ms"] else "gather"
     ach = kern[dom]["gbs"]
     stream_min = gkr.get_insert_stream_min()

@@ -17,6 +17,8 @@ Pinning status (what each function is checked against, on the CPU):
   record encoders       -- hand-written golden records (tests/golden)
   page placement        -- hand-computed byte offsets, brute-force tiny caches
   gather / decode       -- exhaustive code x scale table vs decode definition
+  compressed insert     -- hand-written golden records (group boundaries, the
+                           group's cos/sin row, NaN -> 0, infinite maxima)
 """
 from __future__ import annotations
 
@@ -73,6 +75,9 @@ def lib() -> ctypes.CDLL:
         L.oracle_encode_v4.restype = None
         L.oracle_insert.argtypes = [vp, i64, vp, i32, i32, i64, i64, vp, vp, vp, i64]
         L.oracle_insert.restype = i32
+        L.oracle_rope_quant_insert.argtypes = [vp, i64, vp, i32, i32, i64, i64, vp, vp, vp,
+                                               i64, i64, i32]
+        L.oracle_rope_quant_insert.restype = i32
         L.oracle_decode.argtypes = [vp, vp, i32, vp]
         L.oracle_decode.restype = None
         L.oracle_gather.argtypes = [vp, i32, i32, i64, i64, vp, i64, vp]
@@ -140,9 +145,12 @@ def encode(record: int, kv_row: np.ndarray, csc_row: np.ndarray):
 
 def insert(kv: np.ndarray, cache: np.ndarray, record: int, block_size: int,
            num_pages: int, page_stride: int, slots: np.ndarray,
-           positions: np.ndarray, csc: np.ndarray) -> int:
+           positions: np.ndarray, csc: np.ndarray, compress_ratio: int = 1,
+           sanitize_nans: bool = False) -> int:
     """Insert into a flat uint8 host cache of num_pages * page_stride bytes, in place.
-    Returns the error bits."""
+    compress_ratio > 1 or sanitize_nans selects the compressed-KV insert (a token is
+    written only at a group boundary, rotated with the group's first cos/sin row;
+    NaN -> 0 after rotation).  Returns the error bits."""
     kv = np.ascontiguousarray(kv, dtype=np.uint16).reshape(-1, 512)
     slots = np.ascontiguousarray(slots, dtype=np.int64).reshape(-1)
     positions = np.ascontiguousarray(positions, dtype=np.int64).reshape(-1)
@@ -151,11 +159,17 @@ def insert(kv: np.ndarray, cache: np.ndarray, record: int, block_size: int,
     assert cache.size >= num_pages * page_stride
     T = slots.shape[0]
     assert kv.shape[0] == T and positions.shape[0] == T
-    err = lib().oracle_insert(_ptr(kv), T, _ptr(cache), record, block_size, num_pages,
-                              page_stride, _ptr(slots), _ptr(positions), _ptr(csc),
-                              csc.shape[0])
+    if compress_ratio == 1 and not sanitize_nans:
+        err = lib().oracle_insert(_ptr(kv), T, _ptr(cache), record, block_size, num_pages,
+                                  page_stride, _ptr(slots), _ptr(positions), _ptr(csc),
+                                  csc.shape[0])
+    else:
+        err = lib().oracle_rope_quant_insert(_ptr(kv), T, _ptr(cache), record, block_size,
+                                             num_pages, page_stride, _ptr(slots),
+                                             _ptr(positions), _ptr(csc), csc.shape[0],
+                                             int(compress_ratio), int(bool(sanitize_nans)))
     if err < 0:
-        raise ValueError(f"unknown record width {record}")
+        raise ValueError(f"unknown record width {record} or compress ratio {compress_ratio}")
     return err
 
 

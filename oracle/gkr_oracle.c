@@ -30,6 +30,11 @@
  *        to e4m3);
  *        section "实现拆解" item 4 (gather dequantises fp8 * 2^(scale - 127)
  *        per group; the same gather serves 448/64 and 512/32 with a bf16 tail).
+ *        The same kernel text also fixes the compressed-KV variant: a token is
+ *        written only when (position + 1) % COMPRESS_RATIO == 0, rotated with the
+ *        cos/sin row position // COMPRESS_RATIO * COMPRESS_RATIO, and with
+ *        SANITIZE_CACHE_NANS every NaN of the rotated row becomes 0 before the
+ *        block maxima are taken (the scale byte then never exceeds 254).
  *   [P2] "PR #56441 [Perf][DSpark] KV-only context insertion across V4.1 cache
  *        formats", section "实现拆解" item 1 (input contract).
  *   [P4] FlashMLA overview, DSA section (index -1 marks an invalid entry).
@@ -188,9 +193,10 @@ ORACLE_EXPORT void oracle_rope_pair(float e, float o, float c, float s,
 
 /* Widen one token's 512 bf16 values to fp32 and rotate dims 448..511 with the
  * cos/sin row csc[0..31] = cos, csc[32..63] = sin: pair j covers dims
- * 448 + 2j and 449 + 2j. */
+ * 448 + 2j and 449 + 2j.  With sanitize, every NaN of the rotated row (all 512
+ * dims) is replaced by +0. */
 static void load_and_rotate(const uint16_t *kv_row, const float *csc_row,
-                            float x[512])
+                            int sanitize, float x[512])
 {
     int d, j;
     for (d = 0; d < 512; d++)
@@ -201,6 +207,10 @@ static void load_and_rotate(const uint16_t *kv_row, const float *csc_row,
         oracle_rope_pair(e, o, csc_row[j], csc_row[32 + j], &x[448 + 2 * j],
                          &x[449 + 2 * j]);
     }
+    if (sanitize)
+        for (d = 0; d < 512; d++)
+            if (isnan(x[d]))
+                x[d] = 0.0f;
 }
 
 static float block_amax(const float *x, int n)
@@ -223,12 +233,12 @@ static void quantise_block(const float *x, int n, uint8_t b, uint8_t *q)
 
 /* V4.1 record of one token: 512 e4m3 bytes (all dims, rotated) and 16 scale
  * bytes, one per 32-dim block. */
-ORACLE_EXPORT void oracle_encode_v41(const uint16_t *kv_row, const float *csc_row,
-                                     uint8_t data[512], uint8_t scales[16])
+static void encode_v41(const uint16_t *kv_row, const float *csc_row, int sanitize,
+                       uint8_t data[512], uint8_t scales[16])
 {
     float x[512];
     int b;
-    load_and_rotate(kv_row, csc_row, x);
+    load_and_rotate(kv_row, csc_row, sanitize, x);
     for (b = 0; b < 16; b++) {
         scales[b] = oracle_ue8m0_byte(block_amax(x + 32 * b, 32));
         quantise_block(x + 32 * b, 32, scales[b], data + 32 * b);
@@ -238,12 +248,12 @@ ORACLE_EXPORT void oracle_encode_v41(const uint16_t *kv_row, const float *csc_ro
 /* V4 (legacy) record of one token: 448 e4m3 bytes for the NoPE dims in seven
  * 64-dim blocks, then the 64 rotated RoPE dims as little-endian bf16 (128 B);
  * scale row = 7 bytes + one pad byte 0x00. */
-ORACLE_EXPORT void oracle_encode_v4(const uint16_t *kv_row, const float *csc_row,
-                                    uint8_t data[576], uint8_t scales[8])
+static void encode_v4(const uint16_t *kv_row, const float *csc_row, int sanitize,
+                      uint8_t data[576], uint8_t scales[8])
 {
     float x[512];
     int b, k;
-    load_and_rotate(kv_row, csc_row, x);
+    load_and_rotate(kv_row, csc_row, sanitize, x);
     for (b = 0; b < 7; b++) {
         scales[b] = oracle_ue8m0_byte(block_amax(x + 64 * b, 64));
         quantise_block(x + 64 * b, 64, scales[b], data + 64 * b);
@@ -254,6 +264,18 @@ ORACLE_EXPORT void oracle_encode_v4(const uint16_t *kv_row, const float *csc_row
         data[448 + 2 * k] = (uint8_t)(h & 0xFF);
         data[449 + 2 * k] = (uint8_t)(h >> 8);
     }
+}
+
+ORACLE_EXPORT void oracle_encode_v41(const uint16_t *kv_row, const float *csc_row,
+                                     uint8_t data[512], uint8_t scales[16])
+{
+    encode_v41(kv_row, csc_row, 0, data, scales);
+}
+
+ORACLE_EXPORT void oracle_encode_v4(const uint16_t *kv_row, const float *csc_row,
+                                    uint8_t data[576], uint8_t scales[8])
+{
+    encode_v4(kv_row, csc_row, 0, data, scales);
 }
 
 /* Row sizes of a record: data row D bytes, scale row S bytes. */
@@ -272,24 +294,34 @@ static int record_rows(int record, int *D, int *S)
     return -1;
 }
 
-/* Insert T tokens into a paged cache (host memory).  A page starts at
- * page * page_stride and holds the data region (block_size rows of D bytes)
- * followed by the scale region (block_size rows of S bytes).  Tokens with a
- * negative slot are skipped.  Tokens whose slot or position lies outside the
- * cache / the cos-sin table are skipped too and set an error bit.
- * Returns the OR of the error bits, or -1 for an unknown record width. */
-ORACLE_EXPORT int oracle_insert(const uint16_t *kv, int64_t num_tokens,
-                                uint8_t *cache, int record, int block_size,
-                                int64_t num_pages, int64_t page_stride,
-                                const int64_t *slots, const int64_t *positions,
-                                const float *csc, int64_t max_pos)
+/* Compressed-KV insert of T tokens into a paged cache (host memory).  A page
+ * starts at page * page_stride and holds the data region (block_size rows of D
+ * bytes) followed by the scale region (block_size rows of S bytes).  Per token,
+ * in this order:
+ *   1. slot < 0: skip;
+ *   2. slot >= num_pages * block_size: error bit ORACLE_ERR_SLOT, skip;
+ *   3. position < 0: error bit ORACLE_ERR_POS, skip;
+ *   4. (position + 1) % compress_ratio != 0: skip (not a group boundary);
+ *   5. cos/sin row r = position // compress_ratio * compress_ratio; r >= max_pos:
+ *      error bit ORACLE_ERR_POS, skip;
+ *   6. rotate with row r, replace NaN by 0 when sanitize is set, encode, store.
+ * Steps 1, 4, 5 (the table row) and 6 are the pages'; the error handling in 2, 3
+ * and 5 is this library's.  compress_ratio 1 without sanitize is the plain insert.
+ * Returns the OR of the error bits, or -1 for an unknown record width or a
+ * compress_ratio below 1. */
+ORACLE_EXPORT int oracle_rope_quant_insert(const uint16_t *kv, int64_t num_tokens,
+                                           uint8_t *cache, int record, int block_size,
+                                           int64_t num_pages, int64_t page_stride,
+                                           const int64_t *slots, const int64_t *positions,
+                                           const float *csc, int64_t max_pos,
+                                           int64_t compress_ratio, int sanitize)
 {
     int D, S, err = 0;
     int64_t t;
-    if (record_rows(record, &D, &S))
+    if (record_rows(record, &D, &S) || compress_ratio < 1)
         return -1;
     for (t = 0; t < num_tokens; t++) {
-        int64_t slot = slots[t], pos = positions[t], page, row;
+        int64_t slot = slots[t], pos = positions[t], page, row, r;
         uint8_t *base;
         if (slot < 0)
             continue;
@@ -297,7 +329,14 @@ ORACLE_EXPORT int oracle_insert(const uint16_t *kv, int64_t num_tokens,
             err |= ORACLE_ERR_SLOT;
             continue;
         }
-        if (pos < 0 || pos >= max_pos) {
+        if (pos < 0) {
+            err |= ORACLE_ERR_POS;
+            continue;
+        }
+        if ((pos + 1) % compress_ratio != 0)
+            continue;
+        r = pos / compress_ratio * compress_ratio;
+        if (r >= max_pos) {
             err |= ORACLE_ERR_POS;
             continue;
         }
@@ -305,13 +344,25 @@ ORACLE_EXPORT int oracle_insert(const uint16_t *kv, int64_t num_tokens,
         row = slot % block_size;
         base = cache + page * page_stride;
         if (record == 528)
-            oracle_encode_v41(kv + t * 512, csc + pos * 64, base + row * D,
-                              base + (int64_t)block_size * D + row * S);
+            encode_v41(kv + t * 512, csc + r * 64, sanitize, base + row * D,
+                       base + (int64_t)block_size * D + row * S);
         else
-            oracle_encode_v4(kv + t * 512, csc + pos * 64, base + row * D,
-                             base + (int64_t)block_size * D + row * S);
+            encode_v4(kv + t * 512, csc + r * 64, sanitize, base + row * D,
+                      base + (int64_t)block_size * D + row * S);
     }
     return err;
+}
+
+/* Plain insert: every token with a valid slot is written, rotated with the cos/sin
+ * row of its own position. */
+ORACLE_EXPORT int oracle_insert(const uint16_t *kv, int64_t num_tokens,
+                                uint8_t *cache, int record, int block_size,
+                                int64_t num_pages, int64_t page_stride,
+                                const int64_t *slots, const int64_t *positions,
+                                const float *csc, int64_t max_pos)
+{
+    return oracle_rope_quant_insert(kv, num_tokens, cache, record, block_size, num_pages,
+                                    page_stride, slots, positions, csc, max_pos, 1, 0);
 }
 
 /* Dequantise one stored record into 512 bf16 values.

@@ -1,4 +1,4 @@
-"""Parser for the hand-written golden fixture tests/golden/worked_records.txt."""
+"""Parser for the hand-written golden fixtures tests/golden/worked_*.txt."""
 from __future__ import annotations
 
 from dataclasses import dataclass, field
@@ -61,6 +61,9 @@ class Worked:
     tokens: list = field(default_factory=list)
     records: dict = field(default_factory=dict)   # record -> (page_stride, [Expect])
     gathers: dict = field(default_factory=dict)   # record -> (indices, out uint16 [n,512])
+    compress_ratio: int = 1
+    sanitize: bool = False
+    errors: int = 0                               # expected error bits of the insert
 
 
 def load_worked(path: Path = GOLDEN / "worked_records.txt") -> Worked:
@@ -78,6 +81,10 @@ def load_worked(path: Path = GOLDEN / "worked_records.txt") -> Worked:
         if f[0] == "geometry":
             w.block_size = int(kw["block_size"])
             w.num_pages = int(kw["num_pages"])
+        elif f[0] == "mode":
+            w.compress_ratio = int(kw.get("compress_ratio", 1))
+            w.sanitize = bool(int(kw.get("sanitize", 0)))
+            w.errors = int(kw.get("errors", 0))
         elif f[0] == "csc_row":
             w.csc_rows[int(f[1])] = (float(kw["cos"]), float(kw["sin"]))
         elif f[0] == "token":
@@ -118,9 +125,9 @@ def worked_inputs(w: Worked):
     import torch
     kv = np.stack([t.x for t in w.tokens]).astype(np.float32)
     kv_bits = torch.from_numpy(kv).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-    # every value in the fixture is exact in bf16
+    # every value in the fixture is exact in bf16 (NaN included: any NaN is NaN)
     assert np.array_equal(torch.from_numpy(kv_bits.view(np.int16)).view(torch.bfloat16)
-                          .float().numpy(), kv)
+                          .float().numpy(), kv, equal_nan=True)
     slots = np.array([t.slot for t in w.tokens], np.int64)
     pos = np.array([t.pos for t in w.tokens], np.int64)
     csc = np.zeros((max(w.csc_rows) + 1, 64), np.float32)

@@ -20,7 +20,7 @@ import numpy as np
 import pytest
 import torch
 
-from golden_parse import load_worked, worked_inputs
+from golden_parse import GOLDEN, load_worked, worked_inputs
 
 SENTINEL = 0xA5
 
@@ -200,14 +200,13 @@ def test_record_identities(oracle_mod):
 # hand-derived golden records
 # --------------------------------------------------------------------------------
 
-@pytest.mark.parametrize("record", [528, 584])
-def test_golden_worked_records(oracle_mod, record):
-    w = load_worked()
+def _check_golden_insert(oracle_mod, w, record):
     kv, slots, pos, csc = worked_inputs(w)
     ps, expects = w.records[record]
     cache = np.full(w.num_pages * ps, SENTINEL, np.uint8)
-    err = oracle_mod.insert(kv, cache, record, w.block_size, w.num_pages, ps, slots, pos, csc)
-    assert err == 0
+    err = oracle_mod.insert(kv, cache, record, w.block_size, w.num_pages, ps, slots, pos, csc,
+                            compress_ratio=w.compress_ratio, sanitize_nans=w.sanitize)
+    assert err == w.errors
     touched = np.zeros(cache.size, bool)
     for e in expects:
         D, S = e.data.size, e.scale.size
@@ -218,6 +217,21 @@ def test_golden_worked_records(oracle_mod, record):
         touched[e.data_offset:e.data_offset + D] = True
         touched[e.scale_offset:e.scale_offset + S] = True
     assert (cache[~touched] == SENTINEL).all()
+
+
+@pytest.mark.parametrize("record", [528, 584])
+def test_golden_worked_records(oracle_mod, record):
+    _check_golden_insert(oracle_mod, load_worked(), record)
+
+
+@pytest.mark.parametrize("record", [528, 584])
+def test_golden_compressed_records(oracle_mod, record):
+    """Compress ratio 4 with NaN sanitising: group boundaries, the group's first
+    cos/sin row (decoy rows at the tokens' own positions), NaN -> 0, infinite block
+    maxima (byte 254, +-inf -> +-448), error bits."""
+    w = load_worked(GOLDEN / "worked_compressed.txt")
+    assert w.compress_ratio == 4 and w.sanitize
+    _check_golden_insert(oracle_mod, w, record)
 
 
 @pytest.mark.parametrize("record", [528, 584])
