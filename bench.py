@@ -219,6 +219,15 @@ def insert_bytes(slots: np.ndarray, record: int) -> int:
     return 16 * slots.size + int((slots >= 0).sum()) * (1024 + record)
 
 
+def compressed_insert_bytes(slots: np.ndarray, positions: np.ndarray, ratio: int,
+                            record: int) -> int:
+    """Algorithmic bytes of one compressed-KV insert: 16 B (slot + position) per token,
+    plus the bf16 row read and the record written for every token that is written
+    (valid slot and (position + 1) % ratio == 0)."""
+    written = int(((slots >= 0) & ((positions + 1) % ratio == 0)).sum())
+    return 16 * slots.size + written * (1024 + record)
+
+
 def gather_bytes(indices: np.ndarray, record: int) -> int:
     """Algorithmic bytes of one gather: 4 B index + 1024 B bf16 row written per
     index, plus the record read for every valid index."""
@@ -528,6 +537,21 @@ def sweep(device, peak):
                                            case.block_size, case.record), sets)
         b = insert_bytes(case.slots, case.record)
         res[name] = {"kernel": "insert", "us": ms * 1e3, "tokens_per_s": case.num_tokens / (ms * 1e-3),
+                     "alg_bytes": b, "alg_gbs": b / (ms * 1e-3) / 1e9,
+                     "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
+        del sets
+        torch.cuda.empty_cache()
+
+    for name in ("compressed_v41_r4_262144", "compressed_v41_r128_262144"):
+        case = W.WORKLOADS[name]()
+        R = case.meta["compress_ratio"]
+        sets = device_sets(case, device, 1)
+        ms = timed(lambda s: gkr.rope_quant_insert(s["kv"], s["cache"], s["slots"], s["pos"],
+                                                   s["csc"], case.block_size, R, True,
+                                                   case.record), sets)
+        b = compressed_insert_bytes(case.slots, case.positions, R, case.record)
+        res[name] = {"kernel": "insert_sparse", "compress_ratio": R, "sanitize_nans": True,
+                     "us": ms * 1e3, "tokens_per_s": case.num_tokens / (ms * 1e-3),
                      "alg_bytes": b, "alg_gbs": b / (ms * 1e-3) / 1e9,
                      "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
         del sets

@@ -68,6 +68,9 @@ def lib() -> ctypes.CDLL:
                 L.gkr_kv_insert.argtypes = [vp, i64, vp, ctypes.POINTER(CacheDesc), vp, vp, vp,
                                             i64, vp, vp]
                 L.gkr_kv_insert.restype = ctypes.c_int
+                L.gkr_rope_quant_insert.argtypes = [vp, i64, vp, ctypes.POINTER(CacheDesc), vp,
+                                                    vp, vp, i64, i32, i32, vp, vp]
+                L.gkr_rope_quant_insert.restype = ctypes.c_int
                 L.gkr_kv_gather.argtypes = [vp, ctypes.POINTER(CacheDesc), vp, i64, vp, vp, vp]
                 L.gkr_kv_gather.restype = ctypes.c_int
                 L.gkr_status_string.argtypes, L.gkr_status_string.restype = [ctypes.c_int], \
@@ -183,20 +186,8 @@ def _check_err_flag(err_flag):
                "err_flag must be a contiguous int32 tensor with at least one element")
 
 
-def kv_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: torch.Tensor,
-              positions: torch.Tensor, cos_sin_cache: torch.Tensor, block_size: int,
-              record: int | None = None, err_flag: torch.Tensor | None = None) -> None:
-    """RoPE + MXFP8 quantise + paged insert, in place into k_cache.
-
-    kv             bf16 [tokens, 512], contiguous; not modified.
-    k_cache        uint8 [num_pages, block_size, record] (stride(0) = page stride).
-    slot_mapping   int64 [T] (T = number of tokens processed, <= tokens); -1 = skip.
-    positions      int64, contiguous, covering every kv row.
-    cos_sin_cache  fp32 [max_pos, 64], contiguous (cos 0..31 | sin 0..31).
-    block_size     must equal k_cache.size(1).
-    record         528 / 584, or None to take it from k_cache.size(2).
-    err_flag       optional int32 device tensor; error bits are OR-ed into element 0.
-    """
+def _insert_args(kv, k_cache, slot_mapping, positions, cos_sin_cache, block_size, record,
+                 err_flag):
     desc = _cache_desc(k_cache)
     if record is not None:
         _check(int(record) == desc.record,
@@ -217,11 +208,52 @@ def kv_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: torch.Tenso
            "cos_sin_cache must be a contiguous fp32 tensor [max_pos, 64]")
     _check_err_flag(err_flag)
     dev = _same_cuda_device(kv, k_cache, slot_mapping, positions, cos_sin_cache, err_flag)
+    return desc, T, dev
+
+
+def kv_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: torch.Tensor,
+              positions: torch.Tensor, cos_sin_cache: torch.Tensor, block_size: int,
+              record: int | None = None, err_flag: torch.Tensor | None = None) -> None:
+    """RoPE + MXFP8 quantise + paged insert, in place into k_cache.
+
+    kv             bf16 [tokens, 512], contiguous; not modified.
+    k_cache        uint8 [num_pages, block_size, record] (stride(0) = page stride).
+    slot_mapping   int64 [T] (T = number of tokens processed, <= tokens); -1 = skip.
+    positions      int64, contiguous, covering every kv row.
+    cos_sin_cache  fp32 [max_pos, 64], contiguous (cos 0..31 | sin 0..31).
+    block_size     must equal k_cache.size(1).
+    record         528 / 584, or None to take it from k_cache.size(2).
+    err_flag       optional int32 device tensor; error bits are OR-ed into element 0.
+    """
+    desc, T, dev = _insert_args(kv, k_cache, slot_mapping, positions, cos_sin_cache,
+                                block_size, record, err_flag)
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
         st = lib().gkr_kv_insert(_ptr(kv), T, _ptr(k_cache), ctypes.byref(desc),
                                  _ptr(slot_mapping), _ptr(positions), _ptr(cos_sin_cache),
                                  cos_sin_cache.shape[0], _ptr(err_flag), stream)
+    _raise(st)
+
+
+def rope_quant_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                      positions: torch.Tensor, cos_sin_cache: torch.Tensor, block_size: int,
+                      compress_ratio: int = 1, sanitize_nans: bool = False,
+                      record: int | None = None, err_flag: torch.Tensor | None = None) -> None:
+    """Compressed-KV insert, in place into k_cache: a token is written only when
+    (position + 1) % compress_ratio == 0, rotated with the cos/sin row of its group's
+    first position (position // compress_ratio * compress_ratio); with sanitize_nans
+    every NaN of the rotated row is stored as +0.  Arguments as for kv_insert."""
+    _check(isinstance(compress_ratio, int) and compress_ratio >= 1,
+           "compress_ratio must be an int >= 1")
+    desc, T, dev = _insert_args(kv, k_cache, slot_mapping, positions, cos_sin_cache,
+                                block_size, record, err_flag)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        st = lib().gkr_rope_quant_insert(_ptr(kv), T, _ptr(k_cache), ctypes.byref(desc),
+                                         _ptr(slot_mapping), _ptr(positions),
+                                         _ptr(cos_sin_cache), cos_sin_cache.shape[0],
+                                         int(compress_ratio), 1 if sanitize_nans else 0,
+                                         _ptr(err_flag), stream)
     _raise(st)
 
 

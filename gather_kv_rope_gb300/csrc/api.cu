@@ -126,34 +126,71 @@ GKR_API gkr_status gkr_record_rows(int32_t record, int32_t* data_row_bytes,
     return GKR_OK;
 }
 
-GKR_API gkr_status gkr_kv_insert(const void* kv, int64_t num_tokens, void* k_cache,
-                                 const gkr_cache_desc* cache, const int64_t* slot_mapping,
-                                 const int64_t* positions, const float* cos_sin_cache,
-                                 int64_t max_pos, int32_t* err_flag, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks shared by both insert entry points; fills `p` on success.  A GKR_OK status
+// with p.num_tokens == 0 means there is nothing to launch.
+gkr_status prepare_insert(const void* kv, int64_t num_tokens, void* k_cache,
+                          const gkr_cache_desc* cache, const int64_t* slot_mapping,
+                          const int64_t* positions, const float* cos_sin_cache, int64_t max_pos,
+                          int32_t* err_flag, gkr::InsertParams* p) {
     RecordRows rows;
     const gkr_status st = check_cache(cache, &rows);
     if (st != GKR_OK) return st;
-    if (num_tokens < 0 || max_pos <= 0) return GKR_EINVAL;
+    if (num_tokens < 0 || max_pos <= 0 || max_pos > INT64_C(0x7FFFFFFF)) return GKR_EINVAL;
+    p->num_tokens = num_tokens;
     if (num_tokens == 0) return GKR_OK;
     if (!kv || !k_cache || !slot_mapping || !positions || !cos_sin_cache) return GKR_EINVAL;
     if (!aligned(kv, 16) || !aligned(k_cache, 16) || !aligned(cos_sin_cache, 16) ||
         !aligned(slot_mapping, 8) || !aligned(positions, 8) || !aligned(err_flag, 4))
         return GKR_EALIGN;
+    p->kv = kv;
+    p->cache = static_cast<uint8_t*>(k_cache);
+    p->page_stride = cache->page_stride;
+    p->block_size = cache->block_size;
+    p->num_slots = static_cast<int32_t>(cache->num_pages * cache->block_size);
+    p->slots = slot_mapping;
+    p->positions = positions;
+    p->csc = cos_sin_cache;
+    p->max_pos = max_pos;
+    p->ratio = 1;
+    p->err = err_flag;
+    return GKR_OK;
+}
 
+}  // namespace
+
+extern "C" {
+
+GKR_API gkr_status gkr_kv_insert(const void* kv, int64_t num_tokens, void* k_cache,
+                                 const gkr_cache_desc* cache, const int64_t* slot_mapping,
+                                 const int64_t* positions, const float* cos_sin_cache,
+                                 int64_t max_pos, int32_t* err_flag, cudaStream_t stream) {
     gkr::InsertParams p;
-    p.kv = kv;
-    p.num_tokens = num_tokens;
-    p.cache = static_cast<uint8_t*>(k_cache);
-    p.page_stride = cache->page_stride;
-    p.block_size = cache->block_size;
-    p.num_slots = static_cast<int32_t>(cache->num_pages * cache->block_size);
-    p.slots = slot_mapping;
-    p.positions = positions;
-    p.csc = cos_sin_cache;
-    p.max_pos = max_pos;
-    p.err = err_flag;
+    const gkr_status st = prepare_insert(kv, num_tokens, k_cache, cache, slot_mapping,
+                                         positions, cos_sin_cache, max_pos, err_flag, &p);
+    if (st != GKR_OK || p.num_tokens == 0) return st;
     return cuda_status(cache->record == 528 ? gkr::launch_insert_v41(p, stream)
                                             : gkr::launch_insert_v4(p, stream));
+}
+
+GKR_API gkr_status gkr_rope_quant_insert(const void* kv, int64_t num_tokens, void* k_cache,
+                                         const gkr_cache_desc* cache,
+                                         const int64_t* slot_mapping, const int64_t* positions,
+                                         const float* cos_sin_cache, int64_t max_pos,
+                                         int32_t compress_ratio, int32_t sanitize_nans,
+                                         int32_t* err_flag, cudaStream_t stream) {
+    if (compress_ratio < 1 || (sanitize_nans != 0 && sanitize_nans != 1)) return GKR_EINVAL;
+    gkr::InsertParams p;
+    const gkr_status st = prepare_insert(kv, num_tokens, k_cache, cache, slot_mapping,
+                                         positions, cos_sin_cache, max_pos, err_flag, &p);
+    if (st != GKR_OK || p.num_tokens == 0) return st;
+    p.ratio = compress_ratio;
+    const bool san = sanitize_nans != 0;
+    return cuda_status(cache->record == 528 ? gkr::launch_rope_quant_insert_v41(p, san, stream)
+                                            : gkr::launch_rope_quant_insert_v4(p, san, stream));
 }
 
 GKR_API gkr_status gkr_kv_gather(const void* k_cache, const gkr_cache_desc* cache,

@@ -99,17 +99,26 @@ __device__ __forceinline__ float amax8(const float* f) {
 // in brackets lies in [0.57, 1.15), so the ceiling is E - 135 plus one exactly when
 // 1 + M/2^23 > 1.75, i.e. M > 0x600000.  Adding the bias 127 gives E - 8 + [M > 0x600000];
 // zero and subnormal maxima fall below the clamp and give byte 0.  Finite inputs never
-// exceed byte 247.  The byte is a non-decreasing function of amax, so the byte of a
-// block is the maximum of the bytes of its parts.
+// exceed byte 247; an infinite maximum (E = 255) is the clamp's upper end, exponent 127,
+// byte 254.  The byte is a non-decreasing function of amax, so the byte of a block is
+// the maximum of the bytes of its parts.
 __device__ __forceinline__ uint32_t ue8m0_byte(float amax) {
     const uint32_t b = __float_as_uint(amax);
-    const int e = int(b >> 23) - 8 + int((b & 0x7FFFFFu) > 0x600000u);
-    return e > 0 ? uint32_t(e) : 0u;
+    const uint32_t E = b >> 23;                    // amax >= 0
+    const int e = int(E) - 8 + int((b & 0x7FFFFFu) > 0x600000u);
+    return E == 255u ? 254u : (e > 0 ? uint32_t(e) : 0u);
 }
 
-// 2^(127 - byte) as fp32 (exact; byte <= 247 keeps it a normal number).
+// 2^(127 - byte) as fp32, exact: a normal number for byte <= 253, the subnormal 2^-127
+// (bit 22) for byte 254.
 __device__ __forceinline__ float inv_scale(uint32_t byte) {
-    return __uint_as_float((254u - byte) << 23);
+    return __uint_as_float(byte < 254u ? (254u - byte) << 23 : 0x00400000u);
+}
+
+// NaN -> +0 in place (every other value unchanged).
+__device__ __forceinline__ void zero_nans8(float* f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = f[i] == f[i] ? f[i] : 0.0f;
 }
 
 // Four fp32 values (already divided by the block scale) -> four e4m3 bytes,

@@ -45,12 +45,18 @@ struct TokenLoads {
 
 // V4.1: 16 blocks of 32 dims.  Chunk A of lane L is in block L/4, chunk B in 8 + L/4.
 // `da` = data row + 8L (chunk B's codes go to da + 256); `sl` = scale row + L/4.
+// kSanitize: NaN -> +0 over the whole rotated row before the block maxima.
+template <bool kSanitize = false>
 __device__ __forceinline__ void encode_store_v41(const TokenLoads& L, uint8_t* da, uint8_t* sl,
                                                  int lane) {
     float a[8], b[8];
     unpack_bf16x8(L.a, a);
     unpack_bf16x8(L.b, b);
     if (lane >= 24) rope4(b, L.c, L.s);  // dims 448..511 = pairs 4(L-24) .. 4(L-24)+3
+    if (kSanitize) {
+        zero_nans8(a);
+        zero_nans8(b);
+    }
 
     float ma = amax8(a), mb = amax8(b);
     ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, 1));
@@ -70,6 +76,7 @@ __device__ __forceinline__ void encode_store_v41(const TokenLoads& L, uint8_t* d
 // V4: 7 blocks of 64 NoPE dims (chunk A of lane L in block L/8; chunk B of lanes 0..23
 // in block 4 + L/8), rotated dims 448..511 (chunk B of lanes 24..31) stored as bf16.
 // `da` = data row + 8L; `sl` = scale row + L/8.
+template <bool kSanitize = false>
 __device__ __forceinline__ void encode_store_v4(const TokenLoads& L, uint8_t* da, uint8_t* sl,
                                                 int lane) {
     float a[8], b[8];
@@ -77,6 +84,10 @@ __device__ __forceinline__ void encode_store_v4(const TokenLoads& L, uint8_t* da
     unpack_bf16x8(L.b, b);
     const bool rope_lane = lane >= 24;
     if (rope_lane) rope4(b, L.c, L.s);
+    if (kSanitize) {
+        zero_nans8(a);
+        zero_nans8(b);
+    }
 
     float ma = amax8(a), mb = rope_lane ? 0.0f : amax8(b);
 #pragma unroll
@@ -296,6 +307,109 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_short_kernel(
     }
 }
 
+// ---------------------------------------------------------------- compressed-KV insert
+//
+// Operation (same page and kernel text as above): a token is written only when
+// (position + 1) % R == 0 -- the last token of a group of R positions -- rotated with
+// the cos/sin row of the group's first position, position // R * R = position + 1 - R;
+// with NaN sanitising every NaN of the rotated row becomes +0.  Checks, in order:
+// slot < 0 skips; a slot past the cache sets GKR_ERR_SLOT; a negative position sets
+// GKR_ERR_POS; a position that ends no group skips; a group row past the table sets
+// GKR_ERR_POS.
+
+// Decode token t: data-row / scale-row offsets (off = -1 when nothing is written) and
+// the cos/sin row; returns the error bits.
+template <int kRecord>
+__device__ __forceinline__ uint32_t decode_compressed(const InsertParams& p, int64_t t,
+                                                      int64_t& off, int64_t& soff,
+                                                      int32_t& row) {
+    constexpr uint32_t D = kRecord == 528 ? 512u : 576u;
+    constexpr uint32_t S = kRecord == 528 ? 16u : 8u;
+    const int64_t slot = __ldg(p.slots + t);
+    const int64_t q = __ldg(p.positions + t);
+    if (slot < 0) return 0u;
+    if (slot >= p.num_slots) return 1u;
+    if (q < 0) return 2u;
+    const uint64_t q1 = static_cast<uint64_t>(q) + 1u;
+    const uint64_t R = static_cast<uint64_t>(p.ratio);
+    const uint64_t rem = (q1 | R) >> 32 == 0u
+                             ? static_cast<uint64_t>(static_cast<uint32_t>(q1) %
+                                                     static_cast<uint32_t>(R))
+                             : q1 % R;
+    if (rem != 0u) return 0u;                        // not the last token of its group
+    const uint64_t g = q1 - R;                       // group's first position
+    if (g >= static_cast<uint64_t>(p.max_pos)) return 2u;
+    const uint32_t s = static_cast<uint32_t>(slot);
+    const uint32_t bs = static_cast<uint32_t>(p.block_size);
+    const uint32_t page = s / bs, r = s - page * bs;
+    const int64_t base = static_cast<int64_t>(page) * p.page_stride;
+    off = base + r * D;
+    soff = base + bs * D + r * S;
+    row = static_cast<int32_t>(g);
+    return 0u;
+}
+
+// One warp per `chunk` (<= 32) consecutive tokens: lane i decodes token t0 + i, a
+// ballot collects the tokens to write, and the warp encodes them two at a time with
+// both tokens' loads issued before the first is encoded.  With chunk about 2R a warp
+// writes about two records, and tokens that end no group cost only their 16 bytes of
+// slot and position.
+template <int kRecord, bool kSanitize>
+__global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS)
+    insert_sparse_kernel(const InsertParams p, const int32_t chunk) {
+    pdl_wait_previous();
+    pdl_release_next();
+    const int lane = threadIdx.x & 31;
+    const int64_t t0 =
+        (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * chunk;
+    if (t0 >= p.num_tokens) return;  // warp-uniform
+
+    int64_t off = -1, soff = 0;
+    int32_t row = 0;
+    uint32_t err = 0;
+    if (lane < chunk && t0 + lane < p.num_tokens)
+        err = decode_compressed<kRecord>(p, t0 + lane, off, soff, row);
+    err = __reduce_or_sync(kFull, err);
+    if (err != 0u && lane == 0) report(p.err, static_cast<int32_t>(err));
+    uint32_t todo = __ballot_sync(kFull, off >= 0);
+
+    const uint8_t* const kv_lane = static_cast<const uint8_t*>(p.kv) + t0 * 1024 + 16 * lane;
+    const float* const csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
+    uint8_t* const cache_a = p.cache + 8 * lane;
+    uint8_t* const cache_s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
+    while (todo != 0u) {                             // warp-uniform
+        int u[2];
+        u[0] = __ffs(todo) - 1;
+        todo &= todo - 1u;
+        const bool two = todo != 0u;
+        u[1] = two ? __ffs(todo) - 1 : u[0];
+        todo &= todo - 1u;
+        TokenLoads L[2];
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+            if (v == 0 || two) {
+                const int32_t r = __shfl_sync(kFull, row, u[v]);
+                L[v].a = ld_stream16(kv_lane + u[v] * 1024);
+                L[v].b = ld_stream16(kv_lane + u[v] * 1024 + 512);
+                if (lane >= 24) {
+                    const float* cs = csc_lane + static_cast<int64_t>(r) * 64;
+                    L[v].c = ld_ro_f4(cs);
+                    L[v].s = ld_ro_f4(cs + 32);
+                }
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+            const int64_t o = __shfl_sync(kFull, off, u[v]);
+            const int64_t so = __shfl_sync(kFull, soff, u[v]);
+            if (v == 0 || two) {
+                if (kRecord == 528) encode_store_v41<kSanitize>(L[v], cache_a + o, cache_s + so, lane);
+                else encode_store_v4<kSanitize>(L[v], cache_a + o, cache_s + so, lane);
+            }
+        }
+    }
+}
+
 template <int kRecord>
 cudaError_t launch(const InsertParams& p, cudaStream_t stream) {
     if (p.num_tokens <= 0) return cudaSuccess;
@@ -317,6 +431,20 @@ cudaError_t launch(const InsertParams& p, cudaStream_t stream) {
     return launch_kernel(kernel, blocks, kThreads, smem, stream, p, m);
 }
 
+template <int kRecord>
+cudaError_t launch_compressed(const InsertParams& p, bool sanitize, cudaStream_t stream) {
+    if (p.num_tokens <= 0) return cudaSuccess;
+    if (p.ratio == 1 && !sanitize) return launch<kRecord>(p, stream);
+    const int32_t chunk = static_cast<int32_t>(p.ratio >= 16 ? 32 : 2 * p.ratio);
+    const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * chunk;
+    const int64_t blocks = (p.num_tokens + per_block - 1) / per_block;
+    if (sanitize)
+        return launch_kernel(insert_sparse_kernel<kRecord, true>, blocks, kThreads, 0, stream, p,
+                             chunk);
+    return launch_kernel(insert_sparse_kernel<kRecord, false>, blocks, kThreads, 0, stream, p,
+                         chunk);
+}
+
 }  // namespace
 
 cudaError_t launch_insert_v41(const InsertParams& p, cudaStream_t stream) {
@@ -324,6 +452,14 @@ cudaError_t launch_insert_v41(const InsertParams& p, cudaStream_t stream) {
 }
 cudaError_t launch_insert_v4(const InsertParams& p, cudaStream_t stream) {
     return launch<584>(p, stream);
+}
+cudaError_t launch_rope_quant_insert_v41(const InsertParams& p, bool sanitize,
+                                         cudaStream_t stream) {
+    return launch_compressed<528>(p, sanitize, stream);
+}
+cudaError_t launch_rope_quant_insert_v4(const InsertParams& p, bool sanitize,
+                                        cudaStream_t stream) {
+    return launch_compressed<584>(p, sanitize, stream);
 }
 
 }  // namespace gkr

@@ -18,7 +18,8 @@ struct InsertParams {
     const int64_t* slots;
     const int64_t* positions;
     const float* csc;          // fp32 [max_pos, 64]
-    int64_t max_pos;
+    int64_t max_pos;           // < 2^31 (checked on the host)
+    int64_t ratio;             // compress ratio >= 1 (1 for the plain insert)
     int32_t* err;              // nullable
 };
 
@@ -121,6 +122,11 @@ __host__ __device__ inline WarpItems warp_items(const WorkMap& m, int64_t gw) {
 
 cudaError_t launch_insert_v41(const InsertParams& p, cudaStream_t stream);
 cudaError_t launch_insert_v4(const InsertParams& p, cudaStream_t stream);
+// Compressed-KV insert: only group-boundary tokens are written; NaN -> 0 if sanitize.
+cudaError_t launch_rope_quant_insert_v41(const InsertParams& p, bool sanitize,
+                                         cudaStream_t stream);
+cudaError_t launch_rope_quant_insert_v4(const InsertParams& p, bool sanitize,
+                                        cudaStream_t stream);
 cudaError_t launch_gather_v41(const GatherParams& p, cudaStream_t stream);
 cudaError_t launch_gather_v4(const GatherParams& p, cudaStream_t stream);
 

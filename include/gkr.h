@@ -4,7 +4,9 @@
  *
  *   gkr_kv_insert: bf16 latent [T, 512] -> RoPE on dims 448..511 -> MXFP8
  *                  (e4m3 + UE8M0) encode -> scatter into a paged cache;
- *   gkr_kv_gather: the inverse: dequantise listed slots back to bf16 [N, 512].
+ *   gkr_kv_gather: the inverse: dequantise listed slots back to bf16 [N, 512];
+ *   gkr_rope_quant_insert: the compressed-KV insert (one record per group of
+ *                  compress_ratio positions, optional NaN sanitising).
  *
  * Operations follow these passages (page title, section):
  *   "PR #56893 [DSv4.1] Store the whole KV in MXFP8 (FlashMLA V4.1 record)",
@@ -110,8 +112,10 @@ GKR_API gkr_status gkr_record_rows(int32_t record, int32_t *data_row_bytes,
  *   each block (32 dims for 528, 64 NoPE dims for 584) gets the scale byte
  *     b = clamp(ceil(log2(amax / 448)), -127, 127) + 127 (amax 0 -> b = 0),
  *     and each value is stored as e4m3(x / 2^(b - 127)), round to nearest even,
- *     saturating at +-448;
+ *     saturating at +-448 (an infinite amax gives b = 254 and +-inf -> +-448);
  *   for 584 the rotated dims 448..511 are stored as bf16 (round to nearest even).
+ *   NaN inputs, and non-finite inputs in dims 448..511 (whose rotation can give
+ *   NaN, e.g. inf * 0), are outside the contract here (see gkr_rope_quant_insert).
  *
  * kv             device, bf16 [num_tokens, 512] row-major, 16-byte aligned; read only.
  * num_tokens     >= 0; 0 enqueues nothing (other pointers may then be NULL).
@@ -123,7 +127,7 @@ GKR_API gkr_status gkr_record_rows(int32_t record, int32_t *data_row_bytes,
  * positions      device, int64 [num_tokens]; row of cos_sin_cache for each token.
  * cos_sin_cache  device, fp32 [max_pos, 64] row-major (cos 0..31 | sin 0..31),
  *                16-byte aligned.
- * max_pos        > 0, rows in cos_sin_cache.
+ * max_pos        rows in cos_sin_cache, 0 < max_pos < 2^31.
  * err_flag       device int32 or NULL; GKR_ERR_SLOT / GKR_ERR_POS bits are OR-ed in.
  * stream         CUDA stream to enqueue on.
  */
@@ -131,6 +135,31 @@ GKR_API gkr_status gkr_kv_insert(const void *kv, int64_t num_tokens, void *k_cac
                                  const gkr_cache_desc *cache, const int64_t *slot_mapping,
                                  const int64_t *positions, const float *cos_sin_cache,
                                  int64_t max_pos, int32_t *err_flag, cudaStream_t stream);
+
+/*
+ * rope_quant_insert: the compressed-KV insert ("PR #56893 [DSv4.1] Store the whole
+ * KV in MXFP8 (FlashMLA V4.1 record)", section "关键源码片段": the kernel text of
+ * fused_compress_quant_cache.py with COMPRESS_RATIO and SANITIZE_CACHE_NANS).  Per
+ * token t, with s = slot_mapping[t], q = positions[t], R = compress_ratio:
+ *   s < 0 -> skip;  s past the cache -> GKR_ERR_SLOT, skip;  q < 0 -> GKR_ERR_POS, skip;
+ *   (q + 1) % R != 0 -> skip (only the last position of each group is written);
+ *   r = q // R * R (the group's first position); r >= max_pos -> GKR_ERR_POS, skip;
+ *   otherwise the record is encoded exactly as in gkr_kv_insert but rotated with
+ *   cos/sin row r, and with sanitize_nans every NaN of the rotated row (all 512
+ *   dims) is replaced by +0 before the block maxima are taken; scale bytes are then
+ *   at most 254 (the UE8M0 NaN 255 is never written).
+ * R = 1 without sanitising is gkr_kv_insert.  Arguments as for gkr_kv_insert, plus
+ * compress_ratio  >= 1 (GKR_EINVAL otherwise);
+ * sanitize_nans   0 or 1 (GKR_EINVAL otherwise).
+ * Without sanitising, NaN inputs and non-finite inputs in dims 448..511 are outside
+ * the contract (as for gkr_kv_insert); with it every input value is.
+ */
+GKR_API gkr_status gkr_rope_quant_insert(const void *kv, int64_t num_tokens, void *k_cache,
+                                         const gkr_cache_desc *cache,
+                                         const int64_t *slot_mapping, const int64_t *positions,
+                                         const float *cos_sin_cache, int64_t max_pos,
+                                         int32_t compress_ratio, int32_t sanitize_nans,
+                                         int32_t *err_flag, cudaStream_t stream);
 
 /*
  * kv_gather: for each i in [0, num_indices):

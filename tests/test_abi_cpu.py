@@ -24,7 +24,8 @@ def test_header_declares_the_boundary():
     syms = declared_symbols()
     assert {"gkr_kv_insert", "gkr_kv_gather", "gkr_page_stride", "gkr_record_rows",
             "gkr_status_string", "gkr_last_cuda_error", "gkr_version", "gkr_set_pdl",
-            "gkr_get_pdl", "gkr_set_insert_stream_min", "gkr_get_insert_stream_min"} <= syms
+            "gkr_get_pdl", "gkr_set_insert_stream_min", "gkr_get_insert_stream_min",
+            "gkr_rope_quant_insert"} <= syms
 
 
 def test_library_exports_every_declared_symbol(gkr):
@@ -75,12 +76,18 @@ def insert(gkr, d, T=8, kv=A16, cache=A16b, slots=A16, pos=A16, csc=A16, max_pos
                                    slots, pos, csc, max_pos, err, None)
 
 
+def rq_insert(gkr, d, T=8, kv=A16, cache=A16b, slots=A16, pos=A16, csc=A16, max_pos=16,
+              ratio=4, sanitize=1, err=None):
+    return gkr.lib().gkr_rope_quant_insert(kv, T, cache, None if d is None else ctypes.byref(d),
+                                           slots, pos, csc, max_pos, ratio, sanitize, err, None)
+
+
 def gather(gkr, d, N=8, cache=A16b, idx=A16, out=A16, err=None):
     return gkr.lib().gkr_kv_gather(cache, None if d is None else ctypes.byref(d), idx, N,
                                    out, err, None)
 
 
-@pytest.mark.parametrize("op", [insert, gather])
+@pytest.mark.parametrize("op", [insert, rq_insert, gather])
 def test_geometry_checks(gkr, op):
     assert op(gkr, None) == 1                                        # null descriptor
     assert op(gkr, desc(gkr, record=512)) == 2                       # unsupported record
@@ -105,6 +112,27 @@ def test_insert_argument_checks(gkr):
     assert insert(gkr, d, csc=A16 + 8) == 4
     assert insert(gkr, d, slots=A16 + 4) == 4
     assert insert(gkr, d, err=A16 + 2) == 4
+
+
+def test_insert_max_pos_bound(gkr):
+    d = desc(gkr)
+    assert insert(gkr, d, max_pos=2 ** 31) == 1                       # table rows < 2^31
+    assert rq_insert(gkr, d, max_pos=2 ** 31) == 1
+
+
+def test_rope_quant_insert_argument_checks(gkr):
+    d = desc(gkr)
+    assert rq_insert(gkr, d, ratio=0) == 1
+    assert rq_insert(gkr, d, ratio=-3) == 1
+    assert rq_insert(gkr, d, sanitize=2) == 1
+    assert rq_insert(gkr, d, T=-1) == 1
+    assert rq_insert(gkr, d, max_pos=0) == 1
+    assert rq_insert(gkr, d, T=0, kv=None, cache=None, slots=None, pos=None, csc=None) == 0
+    assert rq_insert(gkr, d, kv=None) == 1
+    assert rq_insert(gkr, d, kv=A16 + 8) == 4
+    assert rq_insert(gkr, d, csc=A16 + 8) == 4
+    assert rq_insert(gkr, d, pos=A16 + 4) == 4
+    assert rq_insert(gkr, desc(gkr, record=584, ps=37440 + 16)) == 3
 
 
 def test_gather_argument_checks(gkr):
@@ -156,6 +184,12 @@ def test_binding_rejects_bad_tensors(gkr):
         gkr.kv_insert(kv, cache, slots, pos[:2], csc, 32)
     with pytest.raises(ValueError, match="CUDA"):
         gkr.kv_insert(kv, cache, slots, pos, csc, 32)          # CPU tensors: no CPU path
+    with pytest.raises(ValueError, match="compress_ratio"):
+        gkr.rope_quant_insert(kv, cache, slots, pos, csc, 32, compress_ratio=0)
+    with pytest.raises(ValueError, match="kv must be"):
+        gkr.rope_quant_insert(kv.float(), cache, slots, pos, csc, 32, 4)
+    with pytest.raises(ValueError, match="CUDA"):
+        gkr.rope_quant_insert(kv, cache, slots, pos, csc, 32, 4, True)
     idx = torch.zeros(3, dtype=torch.int32)
     with pytest.raises(ValueError, match="out must be"):
         gkr.kv_gather(cache, idx, torch.zeros(3, 256, dtype=torch.bfloat16))

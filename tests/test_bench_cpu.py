@@ -20,6 +20,10 @@ def test_algorithmic_bytes():
     slots = np.array([-1, 0, 5, -1, 7], np.int64)
     assert bench.insert_bytes(slots, 528) == 5 * 16 + 3 * (1024 + 528)
     assert bench.insert_bytes(slots, 584) == 5 * 16 + 3 * (1024 + 584)
+    pos = np.array([3, 3, 6, 5, 11], np.int64)
+    # ratio 4: tokens 1 (pos 3) and 4 (pos 11) are written; token 2 (pos 6) ends no group
+    assert bench.compressed_insert_bytes(slots, pos, 4, 528) == 5 * 16 + 2 * (1024 + 528)
+    assert bench.compressed_insert_bytes(slots, pos, 1, 584) == bench.insert_bytes(slots, 584)
     idx = np.array([[-1, 2], [3, -1]], np.int32)
     assert bench.gather_bytes(idx, 528) == 4 * 1028 + 2 * 528
 

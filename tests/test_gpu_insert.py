@@ -81,6 +81,15 @@ def test_insert_value_extremes(gkr, oracle_mod):
 
 
 @pytest.mark.parametrize("record", [528, 584])
+def test_insert_infinities(gkr, oracle_mod, record):
+    """+-inf entries in the NoPE dims: a block whose maximum is infinite gets byte 254
+    (the exponent clamp at 127) and +-inf is stored as +-448."""
+    case = W.compressed_insert(f"inf_{record}", 3, 700, 1, record, block_size=32,
+                               skip_rate=0.05, seed=12, inf_rate=0.003, nonfinite_dims=448)
+    _compare_whole_cache(gkr, oracle_mod, case)
+
+
+@pytest.mark.parametrize("record", [528, 584])
 def test_insert_golden_worked_example(gkr, record):
     w = load_worked()
     kv_bits, slots, pos, csc = worked_inputs(w)

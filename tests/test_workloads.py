@@ -41,3 +41,21 @@ def test_small_gather_sparse_structure():
         assert v.max() < c.meta["context_lengths"][q]
     assert (c.indices == -1).sum() == round(0.03 * 1024)
     assert np.array_equal(c.slots, np.arange(1 << 16))
+
+
+def test_compressed_insert_structure():
+    c = W.compressed_insert("c", 3, 100, 4, skip_rate=0.0, nan_rate=0.01, inf_rate=0.01)
+    assert c.kv.shape == (300, 512) and c.meta["compress_ratio"] == 4
+    assert np.array_equal(c.positions, np.tile(np.arange(100), 3))
+    # 25 groups per sequence, every token carries its group's slot
+    assert np.array_equal(c.slots[:100], np.arange(100) // 4)
+    assert c.slots.max() == 3 * 25 - 1 and c.num_pages == 2
+    bits = c.kv.reshape(-1)
+    exp, man = (bits >> 7) & 0xFF, bits & 0x7F
+    assert ((exp == 0xFF) & (man != 0)).sum() == round(0.01 * bits.size)   # NaN
+    assert ((exp == 0xFF) & (man == 0)).sum() == round(0.01 * bits.size)   # +-inf
+    d = W.compressed_insert("d", 2, 50, 1, inf_rate=0.02, nonfinite_dims=448)
+    exp = (d.kv >> 7) & 0xFF
+    assert (exp[:, 448:] != 0xFF).all() and (exp[:, :448] == 0xFF).sum() == round(0.02 * d.kv.size)
+    big = W.compressed_v41_r4_262144
+    assert big.__doc__ and "65536" in big.__doc__

@@ -22,6 +22,8 @@ Workloads (named by what they are):
   insert_v4_65536       65536 tokens, 584 B legacy record, 2048 pages
   insert_v41_262144     262144 tokens in 8 contiguous sequences, 8192 pages
   gather_v41_sparse     1,048,576-token cache; 128 queries x top-2048 indices
+  compressed_v41_r4_262144    8 sequences x 32768 positions, one record per 4
+  compressed_v41_r128_262144  the same with one record per 128 positions
 """
 from __future__ import annotations
 
@@ -189,12 +191,55 @@ def gather_v41_sparse_262144(seed: int = 0) -> InsertCase:
     return c
 
 
+def compressed_insert(name: str, S: int, L: int, ratio: int, record: int = 528,
+                      block_size: int = 64, skip_rate: float = 0.02, seed: int = 0,
+                      sigma: float = 0.5, nan_rate: float = 0.0, inf_rate: float = 0.0,
+                      dist: str = "normal", nonfinite_dims: int = 512) -> InsertCase:
+    """Compressed-KV insert input: S sequences of L tokens, positions 0..L-1 in each;
+    every token of sequence s carries the compressed slot s * ceil(L / ratio) +
+    position // ratio (the slot of its group), so only the group-boundary tokens
+    (position + 1) % ratio == 0 decide what is written.  A fraction skip_rate of the
+    tokens get slot -1; disjoint fractions nan_rate / inf_rate of the kv entries (drawn
+    after the skip mask, among dims [0, nonfinite_dims) of every row) are set to NaN /
+    +-inf with random signs.  Pages: ceil(S * ceil(L / ratio) / block_size)."""
+    rng = np.random.default_rng(seed)
+    T = S * L
+    kv = _kv_values(rng, T, dist, sigma=sigma)
+    positions = np.tile(np.arange(L, dtype=np.int64), S)
+    per_seq = -(-L // ratio)
+    slots = np.repeat(np.arange(S, dtype=np.int64) * per_seq, L) + positions // ratio
+    slots[_skip_mask(rng, T, skip_rate)] = -1
+    k_nan, k_inf = int(round(nan_rate * kv.size)), int(round(inf_rate * kv.size))
+    if k_nan + k_inf:
+        pick = rng.choice(T * nonfinite_dims, size=k_nan + k_inf, replace=False)  # disjoint
+        idx = pick // nonfinite_dims * 512 + pick % nonfinite_dims
+        sign = rng.integers(0, 2, size=k_nan + k_inf).astype(bool)
+        val = np.where(np.arange(k_nan + k_inf) < k_nan, np.nan, np.inf)
+        kv.reshape(-1)[idx] = to_bf16_bits(np.where(sign, -val, val).astype(np.float32))
+    pages = -(-S * per_seq // block_size)
+    c = InsertCase(name, record, block_size, pages, kv, slots, positions, cos_sin_table(L), None)
+    c.meta["compress_ratio"] = ratio
+    return c
+
+
+def compressed_v41_r4_262144(seed: int = 0) -> InsertCase:
+    """262144 tokens (8 x 32768), ratio 4: 65536 boundary tokens into 1024 pages."""
+    return compressed_insert("compressed_v41_r4_262144", 8, 32768, 4, seed=seed)
+
+
+def compressed_v41_r128_262144(seed: int = 0) -> InsertCase:
+    """262144 tokens (8 x 32768), ratio 128: 2048 boundary tokens into 32 pages."""
+    return compressed_insert("compressed_v41_r128_262144", 8, 32768, 128, seed=seed)
+
+
 WORKLOADS = {
     "insert_v41_1024": insert_v41_1024,
     "roundtrip_v41_16384": roundtrip_v41_16384,
     "insert_v4_65536": insert_v4_65536,
     "insert_v41_262144": insert_v41_262144,
     "gather_v41_sparse": gather_v41_sparse,
+    "compressed_v41_r4_262144": compressed_v41_r4_262144,
+    "compressed_v41_r128_262144": compressed_v41_r128_262144,
 }
 
 # smaller cases of the same kernels, sized for profiler captures
