@@ -19,6 +19,8 @@ Pinning status (what each function is checked against, on the CPU):
   gather / decode       -- exhaustive code x scale table vs decode definition
   compressed insert     -- hand-written golden records (group boundaries, the
                            group's cos/sin row, NaN -> 0, infinite maxima)
+  bf16 / fp8 caches     -- hand-written golden rows; torch bfloat16 / float8_e4m3fn
+                           casts of the numpy-float32 rotation and fp32 quotient
 """
 from __future__ import annotations
 
@@ -39,6 +41,7 @@ CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
 ERR_SLOT = 1
 ERR_POS = 2
 ERR_INDEX = 4
+ERR_SCALE = 8
 
 
 def build(force: bool = False) -> Path:
@@ -78,6 +81,10 @@ def lib() -> ctypes.CDLL:
         L.oracle_rope_quant_insert.argtypes = [vp, i64, vp, i32, i32, i64, i64, vp, vp, vp,
                                                i64, i64, i32]
         L.oracle_rope_quant_insert.restype = i32
+        L.oracle_kv_insert.argtypes = [vp, i64, vp, i32, i32, i64, i64, vp, vp, vp, i64, f32]
+        L.oracle_kv_insert.restype = i32
+        L.oracle_kv_gather.argtypes = [vp, i32, i32, i64, i64, vp, i64, f32, vp]
+        L.oracle_kv_gather.restype = i32
         L.oracle_decode.argtypes = [vp, vp, i32, vp]
         L.oracle_decode.restype = None
         L.oracle_gather.argtypes = [vp, i32, i32, i64, i64, vp, i64, vp]
@@ -122,11 +129,14 @@ def rope_pair(e: float, o: float, c: float, s: float) -> tuple[float, float]:
 # --- records ----------------------------------------------------------------------
 
 def record_rows(record: int) -> tuple[int, int]:
-    """(data row bytes, scale row bytes) of a record, from its definition."""
+    """(data row bytes, scale row bytes) of a cache format, from its definition:
+    528 / 584 packed MXFP8 records, 512 fp8 e4m3 rows, 1024 bf16 rows."""
     if record == 528:
         return 512, 16
     if record == 584:
         return 576, 8
+    if record in (512, 1024):
+        return record, 0
     raise ValueError(f"unknown record width {record}")
 
 
@@ -146,11 +156,12 @@ def encode(record: int, kv_row: np.ndarray, csc_row: np.ndarray):
 def insert(kv: np.ndarray, cache: np.ndarray, record: int, block_size: int,
            num_pages: int, page_stride: int, slots: np.ndarray,
            positions: np.ndarray, csc: np.ndarray, compress_ratio: int = 1,
-           sanitize_nans: bool = False) -> int:
+           sanitize_nans: bool = False, fp8_scale: float | None = None) -> int:
     """Insert into a flat uint8 host cache of num_pages * page_stride bytes, in place.
     compress_ratio > 1 or sanitize_nans selects the compressed-KV insert (a token is
     written only at a group boundary, rotated with the group's first cos/sin row;
-    NaN -> 0 after rotation).  Returns the error bits."""
+    NaN -> 0 after rotation).  Records 512 (fp8 e4m3 rows, fp8_scale required) and
+    1024 (bf16 rows) are the plain caches.  Returns the error bits."""
     kv = np.ascontiguousarray(kv, dtype=np.uint16).reshape(-1, 512)
     slots = np.ascontiguousarray(slots, dtype=np.int64).reshape(-1)
     positions = np.ascontiguousarray(positions, dtype=np.int64).reshape(-1)
@@ -159,7 +170,12 @@ def insert(kv: np.ndarray, cache: np.ndarray, record: int, block_size: int,
     assert cache.size >= num_pages * page_stride
     T = slots.shape[0]
     assert kv.shape[0] == T and positions.shape[0] == T
-    if compress_ratio == 1 and not sanitize_nans:
+    if record in (512, 1024):
+        assert compress_ratio == 1 and not sanitize_nans
+        err = lib().oracle_kv_insert(_ptr(kv), T, _ptr(cache), record, block_size, num_pages,
+                                     page_stride, _ptr(slots), _ptr(positions), _ptr(csc),
+                                     csc.shape[0], 1.0 if fp8_scale is None else fp8_scale)
+    elif compress_ratio == 1 and not sanitize_nans:
         err = lib().oracle_insert(_ptr(kv), T, _ptr(cache), record, block_size, num_pages,
                                   page_stride, _ptr(slots), _ptr(positions), _ptr(csc),
                                   csc.shape[0])
@@ -182,14 +198,20 @@ def decode(record: int, data: np.ndarray, scales: np.ndarray) -> np.ndarray:
 
 
 def gather(cache: np.ndarray, record: int, block_size: int, num_pages: int,
-           page_stride: int, indices: np.ndarray):
-    """Returns (bf16 bits [*indices.shape, 512] as uint16, error bits)."""
+           page_stride: int, indices: np.ndarray, fp8_scale: float | None = None):
+    """Returns (bf16 bits [*indices.shape, 512] as uint16, error bits).  fp8_scale is
+    required for record 512 (fp8 e4m3 rows)."""
     idx = np.ascontiguousarray(indices, dtype=np.int32)
     flat = idx.reshape(-1)
     out = np.zeros((flat.shape[0], 512), np.uint16)
     assert cache.dtype == np.uint8 and cache.flags["C_CONTIGUOUS"]
-    err = lib().oracle_gather(_ptr(cache), record, block_size, num_pages, page_stride,
-                              _ptr(flat), flat.shape[0], _ptr(out))
+    if record in (512, 1024):
+        err = lib().oracle_kv_gather(_ptr(cache), record, block_size, num_pages, page_stride,
+                                     _ptr(flat), flat.shape[0],
+                                     1.0 if fp8_scale is None else fp8_scale, _ptr(out))
+    else:
+        err = lib().oracle_gather(_ptr(cache), record, block_size, num_pages, page_stride,
+                                  _ptr(flat), flat.shape[0], _ptr(out))
     if err < 0:
         raise ValueError(f"unknown record width {record}")
     return out.reshape(*idx.shape, 512), err
@@ -197,7 +219,7 @@ def gather(cache: np.ndarray, record: int, block_size: int, num_pages: int,
 
 def page_stride(record: int, block_size: int) -> int:
     """Page stride for a record: block_size * record bytes rounded up to the page
-    alignment (512 for the 528 B record, 576 for the 584 B record)."""
-    align = 512 if record == 528 else 576
+    alignment (576 for the 584 B record, 512 for every other format)."""
+    align = 576 if record == 584 else 512
     need = block_size * record
     return -(-need // align) * align

@@ -38,6 +38,9 @@
  *   [P2] "PR #56441 [Perf][DSpark] KV-only context insertion across V4.1 cache
  *        formats", section "实现拆解" item 1 (input contract).
  *   [P4] FlashMLA overview, DSA section (index -1 marks an invalid entry).
+ *   [P2] section "实现拆解" item 1 also names the two other KV-only cache formats:
+ *        a bf16 cache and a plain fp8 e4m3fn cache with one fp32 scale, rows of 512
+ *        elements in pages whose stride may be padded.
  * Readings where the pages are silent (exact scale rule, amax 0 -> byte 0,
  * RNE + saturation, fp32 RoPE op order, V4 page layout, pad byte 0, NaN
  * output pattern, out-of-range handling) are listed in the design notes.
@@ -52,6 +55,7 @@
 #define ORACLE_ERR_SLOT 1     /* slot >= num_pages * block_size          */
 #define ORACLE_ERR_POS 2      /* position outside [0, max_pos)           */
 #define ORACLE_ERR_INDEX 4    /* gather index < -1 or >= num_pages * bs  */
+#define ORACLE_ERR_SCALE 8    /* fp8 scale not a positive finite number  */
 
 /* ------------------------------------------------------------------------ */
 /* Number formats                                                            */
@@ -278,7 +282,38 @@ ORACLE_EXPORT void oracle_encode_v4(const uint16_t *kv_row, const float *csc_row
     encode_v4(kv_row, csc_row, 0, data, scales);
 }
 
-/* Row sizes of a record: data row D bytes, scale row S bytes. */
+/* bf16 cache row of one token: the rotated row rounded to bf16 (nearest even),
+ * 512 little-endian values.  Dims 0..447 come back unchanged (bf16 -> fp32 -> bf16
+ * is exact). */
+static void encode_bf16_row(const uint16_t *kv_row, const float *csc_row, uint8_t row[1024])
+{
+    float x[512];
+    int d;
+    load_and_rotate(kv_row, csc_row, 0, x);
+    for (d = 0; d < 512; d++) {
+        uint16_t h = oracle_bf16_encode((double)x[d]);
+        row[2 * d] = (uint8_t)(h & 0xFF);
+        row[2 * d + 1] = (uint8_t)(h >> 8);
+    }
+}
+
+/* fp8 cache row of one token: e4m3(x / scale) per dim, the quotient one fp32
+ * division (nearest even), then rounded to e4m3 (nearest even, saturating). */
+static void encode_fp8_row(const uint16_t *kv_row, const float *csc_row, float scale,
+                           uint8_t row[512])
+{
+    float x[512];
+    int d;
+    load_and_rotate(kv_row, csc_row, 0, x);
+    for (d = 0; d < 512; d++) {
+        float y = x[d] / scale;
+        row[d] = oracle_e4m3_encode((double)y);
+    }
+}
+
+/* Row sizes of a cache format: data row D bytes, scale row S bytes.  528 and 584
+ * are the packed MXFP8 records; 512 is the fp8 e4m3 cache (512 codes, one scale
+ * for the whole cache), 1024 the bf16 cache. */
 static int record_rows(int record, int *D, int *S)
 {
     if (record == 528) {
@@ -291,7 +326,17 @@ static int record_rows(int record, int *D, int *S)
         *S = 8;
         return 0;
     }
+    if (record == 512 || record == 1024) {
+        *D = record;
+        *S = 0;
+        return 0;
+    }
     return -1;
+}
+
+static int scale_ok(float scale)
+{
+    return scale > 0.0f && isfinite(scale);
 }
 
 /* Compressed-KV insert of T tokens into a paged cache (host memory).  A page
@@ -309,17 +354,18 @@ static int record_rows(int record, int *D, int *S)
  * and 5 is this library's.  compress_ratio 1 without sanitize is the plain insert.
  * Returns the OR of the error bits, or -1 for an unknown record width or a
  * compress_ratio below 1. */
-ORACLE_EXPORT int oracle_rope_quant_insert(const uint16_t *kv, int64_t num_tokens,
-                                           uint8_t *cache, int record, int block_size,
-                                           int64_t num_pages, int64_t page_stride,
-                                           const int64_t *slots, const int64_t *positions,
-                                           const float *csc, int64_t max_pos,
-                                           int64_t compress_ratio, int sanitize)
+static int insert_general(const uint16_t *kv, int64_t num_tokens, uint8_t *cache,
+                          int record, int block_size, int64_t num_pages,
+                          int64_t page_stride, const int64_t *slots,
+                          const int64_t *positions, const float *csc, int64_t max_pos,
+                          int64_t compress_ratio, int sanitize, float fp8_scale)
 {
     int D, S, err = 0;
     int64_t t;
     if (record_rows(record, &D, &S) || compress_ratio < 1)
         return -1;
+    if (record == 512 && !scale_ok(fp8_scale))
+        return ORACLE_ERR_SCALE; /* nothing is written */
     for (t = 0; t < num_tokens; t++) {
         int64_t slot = slots[t], pos = positions[t], page, row, r;
         uint8_t *base;
@@ -346,11 +392,41 @@ ORACLE_EXPORT int oracle_rope_quant_insert(const uint16_t *kv, int64_t num_token
         if (record == 528)
             encode_v41(kv + t * 512, csc + r * 64, sanitize, base + row * D,
                        base + (int64_t)block_size * D + row * S);
-        else
+        else if (record == 584)
             encode_v4(kv + t * 512, csc + r * 64, sanitize, base + row * D,
                       base + (int64_t)block_size * D + row * S);
+        else if (record == 1024)
+            encode_bf16_row(kv + t * 512, csc + r * 64, base + row * D);
+        else
+            encode_fp8_row(kv + t * 512, csc + r * 64, fp8_scale, base + row * D);
     }
     return err;
+}
+
+ORACLE_EXPORT int oracle_rope_quant_insert(const uint16_t *kv, int64_t num_tokens,
+                                           uint8_t *cache, int record, int block_size,
+                                           int64_t num_pages, int64_t page_stride,
+                                           const int64_t *slots, const int64_t *positions,
+                                           const float *csc, int64_t max_pos,
+                                           int64_t compress_ratio, int sanitize)
+{
+    if (record != 528 && record != 584)
+        return -1; /* the compressed insert writes the packed records only */
+    return insert_general(kv, num_tokens, cache, record, block_size, num_pages, page_stride,
+                          slots, positions, csc, max_pos, compress_ratio, sanitize, 1.0f);
+}
+
+/* Plain insert into any of the four cache formats; fp8_scale is used by the fp8
+ * cache (record 512) only, and must there be a positive finite number, otherwise
+ * nothing is written and ORACLE_ERR_SCALE is returned. */
+ORACLE_EXPORT int oracle_kv_insert(const uint16_t *kv, int64_t num_tokens, uint8_t *cache,
+                                   int record, int block_size, int64_t num_pages,
+                                   int64_t page_stride, const int64_t *slots,
+                                   const int64_t *positions, const float *csc,
+                                   int64_t max_pos, float fp8_scale)
+{
+    return insert_general(kv, num_tokens, cache, record, block_size, num_pages, page_stride,
+                          slots, positions, csc, max_pos, 1, 0, fp8_scale);
 }
 
 /* Plain insert: every token with a valid slot is written, rotated with the cos/sin
@@ -361,8 +437,10 @@ ORACLE_EXPORT int oracle_insert(const uint16_t *kv, int64_t num_tokens,
                                 const int64_t *slots, const int64_t *positions,
                                 const float *csc, int64_t max_pos)
 {
-    return oracle_rope_quant_insert(kv, num_tokens, cache, record, block_size, num_pages,
-                                    page_stride, slots, positions, csc, max_pos, 1, 0);
+    if (record != 528 && record != 584)
+        return -1;
+    return insert_general(kv, num_tokens, cache, record, block_size, num_pages, page_stride,
+                          slots, positions, csc, max_pos, 1, 0, 1.0f);
 }
 
 /* Dequantise one stored record into 512 bf16 values.
@@ -388,19 +466,41 @@ ORACLE_EXPORT void oracle_decode(const uint8_t *data, const uint8_t *scales,
     }
 }
 
+/* bf16 cache row -> the stored values unchanged. */
+static void decode_bf16_row(const uint8_t *row, uint16_t out[512])
+{
+    int d;
+    for (d = 0; d < 512; d++)
+        out[d] = (uint16_t)(row[2 * d] | (row[2 * d + 1] << 8));
+}
+
+/* fp8 cache row -> bf16(e4m3 * scale): the product is one fp32 multiplication
+ * (nearest even), then rounded to bf16 (nearest even). */
+static void decode_fp8_row(const uint8_t *row, float scale, uint16_t out[512])
+{
+    int d;
+    for (d = 0; d < 512; d++) {
+        float v = (float)oracle_e4m3_value(row[d]) * scale;
+        out[d] = oracle_bf16_encode((double)v);
+    }
+}
+
 /* Gather: for each index, -1 emits 512 bf16 zeros; any other index is a slot
  * number (page = index / block_size, row = index % block_size) whose record is
  * dequantised.  Indices < -1 or past the cache emit zeros and set an error bit.
  * Returns the OR of the error bits, or -1 for an unknown record width. */
-ORACLE_EXPORT int oracle_gather(const uint8_t *cache, int record, int block_size,
-                                int64_t num_pages, int64_t page_stride,
-                                const int32_t *indices, int64_t num_indices,
-                                uint16_t *out)
+static int gather_general(const uint8_t *cache, int record, int block_size,
+                          int64_t num_pages, int64_t page_stride, const int32_t *indices,
+                          int64_t num_indices, float fp8_scale, uint16_t *out)
 {
     int D, S, err = 0;
     int64_t i;
     if (record_rows(record, &D, &S))
         return -1;
+    if (record == 512 && !scale_ok(fp8_scale)) {
+        memset(out, 0, (size_t)num_indices * 512 * sizeof(uint16_t));
+        return ORACLE_ERR_SCALE;
+    }
     for (i = 0; i < num_indices; i++) {
         int64_t idx = indices[i], page, row;
         const uint8_t *base;
@@ -413,8 +513,35 @@ ORACLE_EXPORT int oracle_gather(const uint8_t *cache, int record, int block_size
         page = idx / block_size;
         row = idx % block_size;
         base = cache + page * page_stride;
-        oracle_decode(base + row * D, base + (int64_t)block_size * D + row * S,
-                      record, out + i * 512);
+        if (record == 1024)
+            decode_bf16_row(base + row * D, out + i * 512);
+        else if (record == 512)
+            decode_fp8_row(base + row * D, fp8_scale, out + i * 512);
+        else
+            oracle_decode(base + row * D, base + (int64_t)block_size * D + row * S,
+                          record, out + i * 512);
     }
     return err;
+}
+
+ORACLE_EXPORT int oracle_gather(const uint8_t *cache, int record, int block_size,
+                                int64_t num_pages, int64_t page_stride,
+                                const int32_t *indices, int64_t num_indices,
+                                uint16_t *out)
+{
+    if (record != 528 && record != 584)
+        return -1;
+    return gather_general(cache, record, block_size, num_pages, page_stride, indices,
+                          num_indices, 1.0f, out);
+}
+
+/* Gather from any of the four cache formats (fp8_scale used by record 512 only;
+ * not a positive finite number -> every row zero and ORACLE_ERR_SCALE). */
+ORACLE_EXPORT int oracle_kv_gather(const uint8_t *cache, int record, int block_size,
+                                   int64_t num_pages, int64_t page_stride,
+                                   const int32_t *indices, int64_t num_indices,
+                                   float fp8_scale, uint16_t *out)
+{
+    return gather_general(cache, record, block_size, num_pages, page_stride, indices,
+                          num_indices, fp8_scale, out);
 }

@@ -60,6 +60,7 @@ class Worked:
     csc_rows: dict = field(default_factory=dict)
     tokens: list = field(default_factory=list)
     records: dict = field(default_factory=dict)   # record -> (page_stride, [Expect])
+    fp8_scale: dict = field(default_factory=dict)  # record -> fp32 scale (fp8 rows)
     gathers: dict = field(default_factory=dict)   # record -> (indices, out uint16 [n,512])
     compress_ratio: int = 1
     sanitize: bool = False
@@ -95,9 +96,11 @@ def load_worked(path: Path = GOLDEN / "worked_records.txt") -> Worked:
         elif f[0] == "record":
             cur_record = int(f[1])
             w.records[cur_record] = (int(kw["page_stride"]), [])
+            if "fp8_scale" in kw:
+                w.fp8_scale[cur_record] = float(kw["fp8_scale"])
         elif f[0] == "expect":
-            D, S = (512, 16) if cur_record == 528 else (576, 8)
-            cur_expect = Expect(f[1], int(kw["data_offset"]), int(kw["scale_offset"]),
+            D, S = {528: (512, 16), 584: (576, 8), 512: (512, 0), 1024: (1024, 0)}[cur_record]
+            cur_expect = Expect(f[1], int(kw["data_offset"]), int(kw.get("scale_offset", 0)),
                                 np.full(D, -1, np.int32), np.full(S, -1, np.int32))
             w.records[cur_record][1].append(cur_expect)
         elif f[0] in ("data", "scale"):

@@ -205,7 +205,8 @@ def _check_golden_insert(oracle_mod, w, record):
     ps, expects = w.records[record]
     cache = np.full(w.num_pages * ps, SENTINEL, np.uint8)
     err = oracle_mod.insert(kv, cache, record, w.block_size, w.num_pages, ps, slots, pos, csc,
-                            compress_ratio=w.compress_ratio, sanitize_nans=w.sanitize)
+                            compress_ratio=w.compress_ratio, sanitize_nans=w.sanitize,
+                            fp8_scale=w.fp8_scale.get(record))
     assert err == w.errors
     touched = np.zeros(cache.size, bool)
     for e in expects:
@@ -232,6 +233,23 @@ def test_golden_compressed_records(oracle_mod, record):
     w = load_worked(GOLDEN / "worked_compressed.txt")
     assert w.compress_ratio == 4 and w.sanitize
     _check_golden_insert(oracle_mod, w, record)
+
+
+@pytest.mark.parametrize("record", [1024, 512])
+def test_golden_full_cache_rows(oracle_mod, record):
+    """bf16 and fp8 (scale 0.5) cache rows and their gathers, derived by hand."""
+    w = load_worked(GOLDEN / "worked_full_caches.txt")
+    _check_golden_insert(oracle_mod, w, record)
+    kv, slots, pos, csc = worked_inputs(w)
+    ps, _ = w.records[record]
+    cache = np.full(w.num_pages * ps, SENTINEL, np.uint8)
+    oracle_mod.insert(kv, cache, record, w.block_size, w.num_pages, ps, slots, pos, csc,
+                      fp8_scale=w.fp8_scale.get(record))
+    idx, expect = w.gathers[record]
+    out, err = oracle_mod.gather(cache, record, w.block_size, w.num_pages, ps, idx,
+                                 fp8_scale=w.fp8_scale.get(record))
+    assert err == 0
+    assert np.array_equal(out.astype(np.int64), expect)
 
 
 @pytest.mark.parametrize("record", [528, 584])
