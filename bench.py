@@ -250,9 +250,12 @@ def _supports_external_events(torch) -> bool:
         return False
 
 
-def device_sets(case, device, n_sets: int):
+def device_sets(case, device, n_sets: int, record: int | None = None):
+    """n_sets copies of the case's inputs on the device, each with its own cache (of
+    the case's record, or of `record`) and gather output."""
     import torch
     import gather_kv_rope_gb300 as gkr
+    record = case.record if record is None else record
     kv = torch.from_numpy(case.kv.view(np.int16)).view(torch.bfloat16).to(device)
     slots = torch.from_numpy(case.slots).to(device)
     pos = torch.from_numpy(case.positions).to(device)
@@ -263,7 +266,7 @@ def device_sets(case, device, n_sets: int):
         sets.append(dict(
             kv=kv.clone(), slots=slots.clone(), pos=pos.clone(), csc=csc,
             idx=None if idx is None else idx.clone(),
-            cache=gkr.alloc_cache(case.num_pages, case.block_size, case.record, device, fill=0),
+            cache=gkr.alloc_cache(case.num_pages, case.block_size, record, device, fill=0),
             out=None if idx is None else torch.empty(case.indices.shape + (512,),
                                                      dtype=torch.bfloat16, device=device)))
     return sets
@@ -557,22 +560,41 @@ def sweep(device, peak):
         del sets
         torch.cuda.empty_cache()
 
+    # the plain KV-only caches: the 262144-token insert into bf16 rows and fp8 rows
+    case = W.insert_v41_262144()
+    scale = torch.tensor([0.01], dtype=torch.float32, device=device)
+    for record, fmt in ((1024, "bf16"), (512, "fp8")):
+        sets = device_sets(case, device, 1, record=record)
+        sc = scale if record == 512 else None
+        ms = timed(lambda s: gkr.kv_insert(s["kv"], s["cache"], s["slots"], s["pos"], s["csc"],
+                                           case.block_size, record, fp8_scale=sc), sets)
+        b = insert_bytes(case.slots, record)
+        res[f"insert_{fmt}_262144"] = {
+            "kernel": "insert", "record": record, "us": ms * 1e3,
+            "tokens_per_s": case.num_tokens / (ms * 1e-3), "alg_bytes": b,
+            "alg_gbs": b / (ms * 1e-3) / 1e9, "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
+        del sets
+        torch.cuda.empty_cache()
+
     case = W.gather_v41_sparse()
     kv = torch.from_numpy(case.kv.view(np.int16)).view(torch.bfloat16).to(device)
-    cache = gkr.alloc_cache(case.num_pages, 64, 528, device, fill=0)
-    gkr.kv_insert(kv, cache, torch.from_numpy(case.slots).to(device),
-                  torch.from_numpy(case.positions).to(device), torch.from_numpy(case.csc).to(device),
-                  64, 528)
-    del kv
     idx = torch.from_numpy(case.indices).to(device)
     outs = [torch.empty(case.indices.shape + (512,), dtype=torch.bfloat16, device=device)
             for _ in range(2)]
-    ms = timed(lambda o: gkr.kv_gather(cache, idx, o), outs)
-    b = gather_bytes(case.indices, 528)
-    res["gather_v41_sparse"] = {"kernel": "gather", "us": ms * 1e3,
-                                "indices_per_s": case.indices.size / (ms * 1e-3), "alg_bytes": b,
-                                "alg_gbs": b / (ms * 1e-3) / 1e9,
-                                "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
+    for record, name in ((528, "gather_v41_sparse"), (512, "gather_fp8_sparse")):
+        sc = scale if record == 512 else None
+        cache = gkr.alloc_cache(case.num_pages, 64, record, device, fill=0)
+        gkr.kv_insert(kv, cache, torch.from_numpy(case.slots).to(device),
+                      torch.from_numpy(case.positions).to(device),
+                      torch.from_numpy(case.csc).to(device), 64, record, fp8_scale=sc)
+        ms = timed(lambda o: gkr.kv_gather(cache, idx, o, fp8_scale=sc), outs)
+        b = gather_bytes(case.indices, record)
+        res[name] = {"kernel": "gather", "record": record, "us": ms * 1e3,
+                     "indices_per_s": case.indices.size / (ms * 1e-3), "alg_bytes": b,
+                     "alg_gbs": b / (ms * 1e-3) / 1e9,
+                     "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
+        del cache
+        torch.cuda.empty_cache()
     return res
 
 

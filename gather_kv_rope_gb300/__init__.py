@@ -4,21 +4,23 @@ The compute runs in libgkr.so (hand-written sm_103a CUDA kernels behind a C ABI,
 declared in include/gkr.h); this package builds it in-tree and binds it with
 ctypes.  PyTorch supplies device memory and streams only.
 
-    kv_insert(kv, k_cache, slot_mapping, positions, cos_sin_cache, block_size, record)
-    kv_gather(k_cache, indices, out)
+    kv_insert(kv, k_cache, slot_mapping, positions, cos_sin_cache, block_size, record,
+              fp8_scale=None)
+    kv_gather(k_cache, indices, out, fp8_scale=None)
     rope_quant_insert(kv, k_cache, slot_mapping, positions, cos_sin_cache, block_size,
                       compress_ratio, sanitize_nans)
 """
 from .build import build as _build_lib
-from ._binding import (CacheDesc, ERR_INDEX, ERR_POS, ERR_SLOT, GkrError, RECORDS, alloc_cache,
+from ._binding import (CacheDesc, ERR_INDEX, ERR_POS, ERR_SCALE, ERR_SLOT, GkrError, PACKED,
+                       RECORDS, alloc_cache,
                        cache_bytes, get_insert_stream_min, get_pdl, kv_gather, kv_insert,
                        lib, library_path, page_stride, record_rows, rope_quant_insert,
                        set_insert_stream_min, set_pdl, status_string)
 
 __all__ = ["build", "kv_insert", "kv_gather", "rope_quant_insert", "page_stride", "record_rows", "alloc_cache",
            "cache_bytes", "status_string", "set_pdl", "get_pdl", "set_insert_stream_min",
-           "get_insert_stream_min", "GkrError", "CacheDesc", "RECORDS", "ERR_SLOT",
-           "ERR_POS", "ERR_INDEX", "lib", "library_path"]
+           "get_insert_stream_min", "GkrError", "CacheDesc", "RECORDS", "PACKED", "ERR_SLOT",
+           "ERR_POS", "ERR_INDEX", "ERR_SCALE", "lib", "library_path"]
 
 
 def build(force: bool = False):

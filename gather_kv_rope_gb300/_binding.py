@@ -25,8 +25,13 @@ GKR_ECUDA = 5
 ERR_SLOT = 1
 ERR_POS = 2
 ERR_INDEX = 4
+ERR_SCALE = 8
 
-RECORDS = (528, 584)
+# cache formats by record width (bytes a token occupies): the packed MXFP8 records
+# (uint8 [pages, block, 528 | 584]) and the plain caches of 512 elements a row
+# (float8_e4m3fn [pages, block, 512] -> record 512; bfloat16 [...] -> record 1024)
+RECORDS = (528, 584, 512, 1024)
+PACKED = (528, 584)
 HEAD_DIM = 512
 
 
@@ -65,13 +70,15 @@ def lib() -> ctypes.CDLL:
                 L.gkr_page_stride.argtypes, L.gkr_page_stride.restype = [i32, i32], i64
                 L.gkr_record_rows.argtypes = [i32, vp, vp, vp]
                 L.gkr_record_rows.restype = ctypes.c_int
-                L.gkr_kv_insert.argtypes = [vp, i64, vp, ctypes.POINTER(CacheDesc), vp, vp, vp,
-                                            i64, vp, vp]
+                # kv, T, k_cache, desc, slots, positions, csc, max_pos, fp8_scale, err, stream
+                L.gkr_kv_insert.argtypes = [vp, i64, vp, ctypes.POINTER(CacheDesc), vp, vp, vp, i64,
+                                            vp, vp, vp]
                 L.gkr_kv_insert.restype = ctypes.c_int
                 L.gkr_rope_quant_insert.argtypes = [vp, i64, vp, ctypes.POINTER(CacheDesc), vp,
                                                     vp, vp, i64, i32, i32, vp, vp]
                 L.gkr_rope_quant_insert.restype = ctypes.c_int
-                L.gkr_kv_gather.argtypes = [vp, ctypes.POINTER(CacheDesc), vp, i64, vp, vp, vp]
+                L.gkr_kv_gather.argtypes = [vp, ctypes.POINTER(CacheDesc), vp, i64, vp, vp, vp,
+                                            vp]
                 L.gkr_kv_gather.restype = ctypes.c_int
                 L.gkr_status_string.argtypes, L.gkr_status_string.restype = [ctypes.c_int], \
                     ctypes.c_char_p
@@ -132,33 +139,53 @@ def record_rows(record: int) -> tuple[int, int, int]:
 
 def alloc_cache(num_pages: int, block_size: int, record: int, device="cuda",
                 page_stride_bytes: int | None = None, fill: int | None = None) -> torch.Tensor:
-    """Allocate a paged cache: a uint8 [num_pages, block_size, record] view whose
-    stride(0) is the page stride (padded to the record's alignment).  Inside a page
-    the bytes are laid out as data region then scale region, not row by row."""
+    """Allocate a paged cache whose stride(0) is the page stride (padded to the
+    record's alignment): uint8 [num_pages, block_size, record] for the packed records
+    (inside a page the bytes are a data region then a scale region, not row by row),
+    float8_e4m3fn [num_pages, block_size, 512] for record 512, bfloat16
+    [num_pages, block_size, 512] for record 1024.  `fill` sets every byte."""
     ps = page_stride(record, block_size) if page_stride_bytes is None else int(page_stride_bytes)
     if ps <= 0:
         raise ValueError(f"unsupported record {record} / block_size {block_size}")
     flat = torch.empty(num_pages * ps, dtype=torch.uint8, device=device)
     if fill is not None:
         flat.fill_(fill)
-    return torch.as_strided(flat, (num_pages, block_size, record), (ps, record, 1))
+    if record in PACKED:
+        return torch.as_strided(flat, (num_pages, block_size, record), (ps, record, 1))
+    dt, es = (torch.float8_e4m3fn, 1) if record == 512 else (torch.bfloat16, 2)
+    if ps % es:
+        raise ValueError("page stride must be a whole number of elements")
+    return torch.as_strided(flat.view(dt), (num_pages, block_size, HEAD_DIM),
+                            (ps // es, HEAD_DIM, 1))
 
 
 def cache_bytes(k_cache: torch.Tensor) -> torch.Tensor:
     """The flat byte view (num_pages * page_stride) behind a paged cache view."""
-    P = k_cache.shape[0]
-    return torch.as_strided(k_cache, (P * k_cache.stride(0),), (1,), k_cache.storage_offset())
+    u8 = k_cache if k_cache.dtype == torch.uint8 else k_cache.view(torch.uint8)
+    P = u8.shape[0]
+    return torch.as_strided(u8, (P * u8.stride(0),), (1,), u8.storage_offset())
 
 
 def _cache_desc(k_cache: torch.Tensor) -> CacheDesc:
-    if k_cache.dtype != torch.uint8 or k_cache.dim() != 3:
-        raise ValueError("k_cache must be a uint8 tensor [num_pages, block_size, record]")
-    P, bs, rec = k_cache.shape
-    if rec not in RECORDS:
-        raise ValueError(f"unsupported paged KV record width {rec} (expected 528 or 584)")
-    if k_cache.stride(2) != 1 or k_cache.stride(1) != rec:
-        raise ValueError("k_cache must have stride(2) == 1 and stride(1) == record")
-    return CacheDesc(rec, bs, P, k_cache.stride(0))
+    """The record width is the format selector: uint8 [pages, block, 528 | 584] are
+    the packed MXFP8 records; float8_e4m3fn / bfloat16 [pages, block, 512] the plain
+    caches (records 512 / 1024)."""
+    if k_cache.dim() != 3:
+        raise ValueError("k_cache must be a 3-D paged cache [num_pages, block_size, width]")
+    P, bs, w = k_cache.shape
+    if k_cache.dtype == torch.uint8:
+        if w not in PACKED:
+            raise ValueError(f"unsupported paged KV record width {w} (expected 528 or 584)")
+        rec, es = w, 1
+    elif k_cache.dtype in (torch.float8_e4m3fn, torch.bfloat16):
+        if w != HEAD_DIM:
+            raise ValueError(f"a {k_cache.dtype} cache must have width 512, not {w}")
+        rec, es = (512, 1) if k_cache.dtype == torch.float8_e4m3fn else (1024, 2)
+    else:
+        raise ValueError("k_cache must be uint8 (packed records), float8_e4m3fn or bfloat16")
+    if k_cache.stride(2) != 1 or k_cache.stride(1) != w:
+        raise ValueError("k_cache must have stride(2) == 1 and stride(1) == its width")
+    return CacheDesc(rec, bs, P, k_cache.stride(0) * es)
 
 
 def _check(cond: bool, msg: str) -> None:
@@ -178,6 +205,15 @@ def _same_cuda_device(*ts: torch.Tensor) -> torch.device:
         if t is not None and t.device != dev:
             raise ValueError(f"all tensors must be on {dev}; got one on {t.device}")
     return dev
+
+
+def _check_fp8_scale(desc: CacheDesc, fp8_scale):
+    if desc.record == 512:
+        _check(fp8_scale is not None and fp8_scale.dtype == torch.float32
+               and fp8_scale.numel() == 1, "an fp8 cache needs fp8_scale: a float32 tensor "
+               "with one element")
+    else:
+        _check(fp8_scale is None, "fp8_scale is only taken by an fp8 (float8_e4m3fn) cache")
 
 
 def _check_err_flag(err_flag):
@@ -213,25 +249,33 @@ def _insert_args(kv, k_cache, slot_mapping, positions, cos_sin_cache, block_size
 
 def kv_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: torch.Tensor,
               positions: torch.Tensor, cos_sin_cache: torch.Tensor, block_size: int,
-              record: int | None = None, err_flag: torch.Tensor | None = None) -> None:
+              record: int | None = None, err_flag: torch.Tensor | None = None,
+              fp8_scale: torch.Tensor | None = None) -> None:
     """RoPE + MXFP8 quantise + paged insert, in place into k_cache.
 
     kv             bf16 [tokens, 512], contiguous; not modified.
-    k_cache        uint8 [num_pages, block_size, record] (stride(0) = page stride).
+    k_cache        uint8 [num_pages, block_size, record] (stride(0) = page stride), or a
+                   plain float8_e4m3fn / bfloat16 [num_pages, block_size, 512] cache.
     slot_mapping   int64 [T] (T = number of tokens processed, <= tokens); -1 = skip.
     positions      int64, contiguous, covering every kv row.
     cos_sin_cache  fp32 [max_pos, 64], contiguous (cos 0..31 | sin 0..31).
     block_size     must equal k_cache.size(1).
     record         528 / 584, or None to take it from k_cache.size(2).
     err_flag       optional int32 device tensor; error bits are OR-ed into element 0.
+    fp8_scale      float32 device tensor of one element: required for an fp8 cache
+                   (stored codes are e4m3(x / scale)), None otherwise.
     """
     desc, T, dev = _insert_args(kv, k_cache, slot_mapping, positions, cos_sin_cache,
                                 block_size, record, err_flag)
+    _check_fp8_scale(desc, fp8_scale)
+    if fp8_scale is not None:
+        _same_cuda_device(kv, fp8_scale)
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
         st = lib().gkr_kv_insert(_ptr(kv), T, _ptr(k_cache), ctypes.byref(desc),
                                  _ptr(slot_mapping), _ptr(positions), _ptr(cos_sin_cache),
-                                 cos_sin_cache.shape[0], _ptr(err_flag), stream)
+                                 cos_sin_cache.shape[0], _ptr(fp8_scale), _ptr(err_flag),
+                                 stream)
     _raise(st)
 
 
@@ -247,6 +291,7 @@ def rope_quant_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: tor
            "compress_ratio must be an int >= 1")
     desc, T, dev = _insert_args(kv, k_cache, slot_mapping, positions, cos_sin_cache,
                                 block_size, record, err_flag)
+    _check(desc.record in PACKED, "the compressed insert writes the packed 528 / 584 records")
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
         st = lib().gkr_rope_quant_insert(_ptr(kv), T, _ptr(k_cache), ctypes.byref(desc),
@@ -258,20 +303,23 @@ def rope_quant_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: tor
 
 
 def kv_gather(k_cache: torch.Tensor, indices: torch.Tensor, out: torch.Tensor,
-              err_flag: torch.Tensor | None = None) -> torch.Tensor:
+              err_flag: torch.Tensor | None = None,
+              fp8_scale: torch.Tensor | None = None) -> torch.Tensor:
     """Dequantise the records at `indices` into `out` (bf16 [*indices.shape, 512]).
-    An index of -1 writes zeros.  Returns out."""
+    An index of -1 writes zeros.  An fp8 cache needs its fp8_scale.  Returns out."""
     desc = _cache_desc(k_cache)
+    _check_fp8_scale(desc, fp8_scale)
     _check(indices.dtype == torch.int32 and indices.is_contiguous(),
            "indices must be a contiguous int32 tensor")
     _check(out.dtype == torch.bfloat16 and out.is_contiguous()
            and tuple(out.shape) == tuple(indices.shape) + (HEAD_DIM,),
            "out must be a contiguous bf16 tensor of shape indices.shape + (512,)")
     _check_err_flag(err_flag)
-    dev = _same_cuda_device(k_cache, indices, out, err_flag)
+    dev = _same_cuda_device(k_cache, indices, out, err_flag, fp8_scale)
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
         st = lib().gkr_kv_gather(_ptr(k_cache), ctypes.byref(desc), _ptr(indices),
-                                 indices.numel(), _ptr(out), _ptr(err_flag), stream)
+                                 indices.numel(), _ptr(out), _ptr(fp8_scale), _ptr(err_flag),
+                                 stream)
     _raise(st)
     return out

@@ -32,10 +32,23 @@ struct RecordRows {
 bool record_rows(int32_t record, RecordRows* r) {
     // V4.1: 512 B e4m3 + 16 UE8M0; V4: 448 B e4m3 + 128 B bf16 + 7 UE8M0 + 1 pad.
     // Pages align to 512 B (V4.1) and 576 B (V4) ("PR #56893 [DSv4.1] Store the whole
-    // KV in MXFP8 (FlashMLA V4.1 record)", section "功能与动机").
+    // KV in MXFP8 (FlashMLA V4.1 record)", section "功能与动机").  The plain KV-only
+    // caches keep 512 elements a row: fp8 e4m3 (512 B) or bf16 (1024 B), pages aligned
+    // to 512 B ("PR #56441 [Perf][DSpark] KV-only context insertion across V4.1 cache
+    // formats", section "实现拆解" item 1).
     if (record == 528) { *r = {512, 16, 512}; return true; }
     if (record == 584) { *r = {576, 8, 576}; return true; }
+    if (record == 512) { *r = {512, 0, 512}; return true; }
+    if (record == 1024) { *r = {1024, 0, 512}; return true; }
     return false;
+}
+
+bool packed(int32_t record) { return record == 528 || record == 584; }
+
+// Packed records need block_size % 32 == 0 (the page geometry of the pages); the
+// plain caches take any block_size >= 1.
+bool block_size_ok(int32_t record, int32_t bs) {
+    return bs > 0 && (!packed(record) || bs % 32 == 0);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -43,7 +56,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 gkr_status check_cache(const gkr_cache_desc* c, RecordRows* rows) {
     if (c == nullptr) return GKR_EINVAL;
     if (!record_rows(c->record, rows)) return GKR_EUNSUPPORTED_RECORD;
-    if (c->block_size <= 0 || c->block_size % 32 != 0) return GKR_EINVAL;
+    if (!block_size_ok(c->record, c->block_size)) return GKR_EINVAL;
     if (c->num_pages <= 0) return GKR_EINVAL;
     if (c->num_pages > (INT64_C(0x7FFFFFFF) / c->block_size)) return GKR_EINVAL;  // slots < 2^31
     const int64_t need = static_cast<int64_t>(c->block_size) * c->record;
@@ -111,7 +124,7 @@ GKR_API int64_t gkr_get_insert_stream_min(void) { return g_stream_min.load(); }
 
 GKR_API int64_t gkr_page_stride(int32_t record, int32_t block_size) {
     RecordRows r;
-    if (!record_rows(record, &r) || block_size <= 0 || block_size % 32 != 0) return -1;
+    if (!record_rows(record, &r) || !block_size_ok(record, block_size)) return -1;
     const int64_t need = static_cast<int64_t>(block_size) * record;
     return (need + r.align - 1) / r.align * r.align;
 }
@@ -135,7 +148,7 @@ namespace {
 gkr_status prepare_insert(const void* kv, int64_t num_tokens, void* k_cache,
                           const gkr_cache_desc* cache, const int64_t* slot_mapping,
                           const int64_t* positions, const float* cos_sin_cache, int64_t max_pos,
-                          int32_t* err_flag, gkr::InsertParams* p) {
+                          const float* fp8_scale, int32_t* err_flag, gkr::InsertParams* p) {
     RecordRows rows;
     const gkr_status st = check_cache(cache, &rows);
     if (st != GKR_OK) return st;
@@ -143,8 +156,10 @@ gkr_status prepare_insert(const void* kv, int64_t num_tokens, void* k_cache,
     p->num_tokens = num_tokens;
     if (num_tokens == 0) return GKR_OK;
     if (!kv || !k_cache || !slot_mapping || !positions || !cos_sin_cache) return GKR_EINVAL;
+    if (cache->record == 512 && !fp8_scale) return GKR_EINVAL;
     if (!aligned(kv, 16) || !aligned(k_cache, 16) || !aligned(cos_sin_cache, 16) ||
-        !aligned(slot_mapping, 8) || !aligned(positions, 8) || !aligned(err_flag, 4))
+        !aligned(slot_mapping, 8) || !aligned(positions, 8) || !aligned(err_flag, 4) ||
+        !aligned(fp8_scale, 4))
         return GKR_EALIGN;
     p->kv = kv;
     p->cache = static_cast<uint8_t*>(k_cache);
@@ -156,8 +171,27 @@ gkr_status prepare_insert(const void* kv, int64_t num_tokens, void* k_cache,
     p->csc = cos_sin_cache;
     p->max_pos = max_pos;
     p->ratio = 1;
+    p->fp8_scale = cache->record == 512 ? fp8_scale : nullptr;
     p->err = err_flag;
     return GKR_OK;
+}
+
+cudaError_t launch_insert(int32_t record, const gkr::InsertParams& p, cudaStream_t stream) {
+    switch (record) {
+        case 528: return gkr::launch_insert_v41(p, stream);
+        case 584: return gkr::launch_insert_v4(p, stream);
+        case 512: return gkr::launch_insert_fp8(p, stream);
+        default: return gkr::launch_insert_bf16(p, stream);
+    }
+}
+
+cudaError_t launch_gather(int32_t record, const gkr::GatherParams& p, cudaStream_t stream) {
+    switch (record) {
+        case 528: return gkr::launch_gather_v41(p, stream);
+        case 584: return gkr::launch_gather_v4(p, stream);
+        case 512: return gkr::launch_gather_fp8(p, stream);
+        default: return gkr::launch_gather_bf16(p, stream);
+    }
 }
 
 }  // namespace
@@ -167,13 +201,14 @@ extern "C" {
 GKR_API gkr_status gkr_kv_insert(const void* kv, int64_t num_tokens, void* k_cache,
                                  const gkr_cache_desc* cache, const int64_t* slot_mapping,
                                  const int64_t* positions, const float* cos_sin_cache,
-                                 int64_t max_pos, int32_t* err_flag, cudaStream_t stream) {
+                                 int64_t max_pos, const float* fp8_scale, int32_t* err_flag,
+                                 cudaStream_t stream) {
     gkr::InsertParams p;
     const gkr_status st = prepare_insert(kv, num_tokens, k_cache, cache, slot_mapping,
-                                         positions, cos_sin_cache, max_pos, err_flag, &p);
+                                         positions, cos_sin_cache, max_pos, fp8_scale, err_flag,
+                                         &p);
     if (st != GKR_OK || p.num_tokens == 0) return st;
-    return cuda_status(cache->record == 528 ? gkr::launch_insert_v41(p, stream)
-                                            : gkr::launch_insert_v4(p, stream));
+    return cuda_status(launch_insert(cache->record, p, stream));
 }
 
 GKR_API gkr_status gkr_rope_quant_insert(const void* kv, int64_t num_tokens, void* k_cache,
@@ -183,9 +218,11 @@ GKR_API gkr_status gkr_rope_quant_insert(const void* kv, int64_t num_tokens, voi
                                          int32_t compress_ratio, int32_t sanitize_nans,
                                          int32_t* err_flag, cudaStream_t stream) {
     if (compress_ratio < 1 || (sanitize_nans != 0 && sanitize_nans != 1)) return GKR_EINVAL;
+    if (cache != nullptr && !packed(cache->record)) return GKR_EUNSUPPORTED_RECORD;
     gkr::InsertParams p;
     const gkr_status st = prepare_insert(kv, num_tokens, k_cache, cache, slot_mapping,
-                                         positions, cos_sin_cache, max_pos, err_flag, &p);
+                                         positions, cos_sin_cache, max_pos, nullptr, err_flag,
+                                         &p);
     if (st != GKR_OK || p.num_tokens == 0) return st;
     p.ratio = compress_ratio;
     const bool san = sanitize_nans != 0;
@@ -195,15 +232,17 @@ GKR_API gkr_status gkr_rope_quant_insert(const void* kv, int64_t num_tokens, voi
 
 GKR_API gkr_status gkr_kv_gather(const void* k_cache, const gkr_cache_desc* cache,
                                  const int32_t* indices, int64_t num_indices, void* out,
-                                 int32_t* err_flag, cudaStream_t stream) {
+                                 const float* fp8_scale, int32_t* err_flag,
+                                 cudaStream_t stream) {
     RecordRows rows;
     const gkr_status st = check_cache(cache, &rows);
     if (st != GKR_OK) return st;
     if (num_indices < 0) return GKR_EINVAL;
     if (num_indices == 0) return GKR_OK;
     if (!k_cache || !indices || !out) return GKR_EINVAL;
+    if (cache->record == 512 && !fp8_scale) return GKR_EINVAL;
     if (!aligned(k_cache, 16) || !aligned(out, 16) || !aligned(indices, 4) ||
-        !aligned(err_flag, 4))
+        !aligned(err_flag, 4) || !aligned(fp8_scale, 4))
         return GKR_EALIGN;
 
     gkr::GatherParams p;
@@ -214,19 +253,21 @@ GKR_API gkr_status gkr_kv_gather(const void* k_cache, const gkr_cache_desc* cach
     p.indices = indices;
     p.num_indices = num_indices;
     p.out = out;
+    p.fp8_scale = cache->record == 512 ? fp8_scale : nullptr;
     p.err = err_flag;
-    return cuda_status(cache->record == 528 ? gkr::launch_gather_v41(p, stream)
-                                            : gkr::launch_gather_v4(p, stream));
+    return cuda_status(launch_gather(cache->record, p, stream));
 }
 
 GKR_API const char* gkr_status_string(gkr_status status) {
     switch (status) {
         case GKR_OK: return "ok";
         case GKR_EINVAL: return "invalid argument";
-        case GKR_EUNSUPPORTED_RECORD: return "unsupported record width (expected 528 or 584)";
+        case GKR_EUNSUPPORTED_RECORD:
+            return "unsupported record width (expected 528 or 584, or 512 / 1024 for the fp8 "
+                   "and bf16 caches; the compressed insert writes 528 / 584 only)";
         case GKR_EBAD_PAGE_GEOMETRY:
             return "bad page geometry (page_stride below block_size * record or not a "
-                   "multiple of the record's page alignment)";
+                   "multiple of the record's page alignment: 576 for 584, else 512)";
         case GKR_EALIGN: return "misaligned pointer";
         case GKR_ECUDA: return "CUDA launch error";
     }

@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 namespace gkr {
@@ -238,6 +239,45 @@ __device__ __forceinline__ uint4 dequant8(const uint2 c, uint32_t byte) {
     uint4 o;
     dequant4(c.x, d, o.x, o.y);
     dequant4(c.y, d, o.z, o.w);
+    return o;
+}
+
+// ---------------------------------------------------------------- fp8 rows with one scale
+
+// Error bit for an fp8 cache scale that is not a positive finite number.
+constexpr int32_t kErrScale = 8;
+
+__device__ __forceinline__ bool scale_ok(float s) { return s > 0.0f && s <= 3.40282347e38f; }
+
+// Eight values -> e4m3(x / scale): one IEEE fp32 division each (nearest even), then the
+// saturating nearest-even e4m3 cast.
+__device__ __forceinline__ uint2 quantise8_div(const float* f, float scale) {
+    uint2 q;
+    q.x = e4m3x4(__fdiv_rn(f[0], scale), __fdiv_rn(f[1], scale), __fdiv_rn(f[2], scale),
+                 __fdiv_rn(f[3], scale));
+    q.y = e4m3x4(__fdiv_rn(f[4], scale), __fdiv_rn(f[5], scale), __fdiv_rn(f[6], scale),
+                 __fdiv_rn(f[7], scale));
+    return q;
+}
+
+// Two e4m3 codes (low 16 bits of w >> shift) -> bf16x2 of fl32(e4m3 * scale), nearest even.
+// e4m3 -> f16 -> f32 is exact for every finite code.
+__device__ __forceinline__ uint32_t fp8x2_scaled_bf16x2(uint32_t w16, float scale) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w16),
+                                                     __NV_E4M3);
+    const float2 f = __half22float2(__half2(h));
+    return pack_bf16x2_rn(__fmul_rn(f.x, scale), __fmul_rn(f.y, scale));
+}
+
+// Eight e4m3 codes with one fp32 scale -> eight bf16; NaN codes give 0x7FC0.
+__device__ __forceinline__ uint4 dequant8_scaled(const uint2 c, float scale) {
+    uint4 o;
+    o.x = fp8x2_scaled_bf16x2(c.x & 0xFFFFu, scale);
+    o.y = fp8x2_scaled_bf16x2(c.x >> 16, scale);
+    o.z = fp8x2_scaled_bf16x2(c.y & 0xFFFFu, scale);
+    o.w = fp8x2_scaled_bf16x2(c.y >> 16, scale);
+    patch_nan(e4m3_nan_bytes(c.x), o.x, o.y);
+    patch_nan(e4m3_nan_bytes(c.y), o.z, o.w);
     return o;
 }
 

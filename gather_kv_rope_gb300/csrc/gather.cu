@@ -1,4 +1,5 @@
-// Dequantise-and-gather of paged KV records back to bf16 [N, 512].
+// Dequantise-and-gather of paged KV records back to bf16 [N, 512] (also from the two
+// plain caches: bf16 rows are copied, fp8 e4m3 rows multiplied by the cache's scale).
 //
 // Operation (page "PR #56893 [DSv4.1] Store the whole KV in MXFP8 (FlashMLA V4.1
 // record)", section "实现拆解" item 4: the gather reads a record by its width and
@@ -23,12 +24,6 @@ namespace {
 #endif
 constexpr int kPerWarp = GKR_GATHER_PER_WARP;   // records per warp
 
-template <int kRecord>
-struct Rec {
-    static constexpr uint32_t D = kRecord == 528 ? 512u : 576u;   // data row bytes
-    static constexpr uint32_t S = kRecord == 528 ? 16u : 8u;      // scale row bytes
-};
-
 // Read-only loads that do not allocate in L1 (each record is read once).
 __device__ __forceinline__ uint2 ldg_na8(const void* p) {
     uint2 v;
@@ -49,15 +44,15 @@ __device__ __forceinline__ uint32_t ldg_u8(const void* p) {
 }
 
 struct Loaded {
-    uint2 a;        // codes of chunk A
-    uint4 b;        // codes of chunk B (.x, .y) or, for the V4 tail lanes, 8 bf16
+    uint4 a;        // codes of chunk A (.x, .y) or, for bf16 rows, 8 bf16
+    uint4 b;        // codes of chunk B (.x, .y) or, for the V4 tail lanes / bf16 rows, 8 bf16
     uint32_t sa, sb;
     bool valid;
 };
 
 // Per-lane base pointers: every load of a record is one 64-bit add away.
 struct LaneBases {
-    const uint8_t* a;      // cache + 8L: chunk A codes (chunk B at +256)
+    const uint8_t* a;      // cache + 8L (16L for bf16 rows): chunk A (chunk B at +256 / +512)
     const uint8_t* tail;   // V4, lanes 24..31: cache + 448 + 16 (L - 24)
     const uint8_t* s;      // cache + scale byte of chunk A (chunk B's at +8 / +4)
 };
@@ -67,7 +62,18 @@ __device__ __forceinline__ void load_record(int64_t off, int64_t soff, const Lan
                                             int lane, Loaded& r) {
     r.valid = off >= 0;
     if (!r.valid) return;
-    r.a = ldg_na8(lb.a + off);
+    if constexpr (kRecord == 1024) {
+        r.a = ldg_na16(lb.a + off);
+        r.b = ldg_na16(lb.a + off + 512);
+        return;
+    }
+    const uint2 ta = ldg_na8(lb.a + off);
+    r.a = make_uint4(ta.x, ta.y, 0u, 0u);
+    if constexpr (kRecord == 512) {
+        const uint2 t = ldg_na8(lb.a + off + 256);
+        r.b = make_uint4(t.x, t.y, 0u, 0u);
+        return;
+    }
     r.sa = ldg_u8(lb.s + soff);
     if (kRecord == 528) {
         const uint2 t = ldg_na8(lb.a + off + 256);
@@ -84,12 +90,21 @@ __device__ __forceinline__ void load_record(int64_t off, int64_t soff, const Lan
 }
 
 template <int kRecord>
-__device__ __forceinline__ void convert_store(const Loaded& r, uint8_t* orow, int lane) {
+__device__ __forceinline__ void convert_store(const Loaded& r, uint8_t* orow, int lane,
+                                              float scale) {
     uint4 oa = make_uint4(0u, 0u, 0u, 0u), ob = oa;
     if (r.valid) {
-        oa = dequant8(r.a, r.sa);
-        if (kRecord == 528 || lane < 24) ob = dequant8(make_uint2(r.b.x, r.b.y), r.sb);
-        else ob = r.b;
+        if constexpr (kRecord == 1024) {
+            oa = r.a;
+            ob = r.b;
+        } else if constexpr (kRecord == 512) {
+            oa = dequant8_scaled(make_uint2(r.a.x, r.a.y), scale);
+            ob = dequant8_scaled(make_uint2(r.b.x, r.b.y), scale);
+        } else {
+            oa = dequant8(make_uint2(r.a.x, r.a.y), r.sa);
+            if (kRecord == 528 || lane < 24) ob = dequant8(make_uint2(r.b.x, r.b.y), r.sb);
+            else ob = r.b;
+        }
     }
     st_stream16(orow, oa);
     st_stream16(orow + 512, ob);
@@ -108,11 +123,21 @@ __global__ void __launch_bounds__(kThreads, kRecord == 584 ? 6 : 8)
     const int64_t i0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * U;
     if (i0 >= p.num_indices) return;  // warp-uniform
 
+    // fp8 rows: the cache's scale, read once per warp; not a positive finite number ->
+    // every row of the warp is written as zeros and the error bit is set
+    float scale = 1.0f;
+    bool scale_bad = false;
+    if constexpr (kRecord == 512) {
+        scale = __ldg(p.fp8_scale);
+        scale_bad = !scale_ok(scale);
+        if (scale_bad && lane == 0) report(p.err, kErrScale);
+    }
+
     // lane u < U decodes index i0 + u: data-row offset (-1 = emit zeros), scale-row offset
     int64_t off = -1, soff = 0;
     bool bad = false;
-    if (lane < U && i0 + lane < p.num_indices) {
-        using R = Rec<kRecord>;
+    if (lane < U && i0 + lane < p.num_indices && !scale_bad) {
+        using R = Fmt<kRecord>;
         const int32_t idx = __ldg(p.indices + i0 + lane);
         if (idx >= 0 && idx < p.num_slots) {
             const uint32_t s = static_cast<uint32_t>(idx);
@@ -128,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, kRecord == 584 ? 6 : 8)
     if (__ballot_sync(kFull, bad) != 0u && lane == 0) report(p.err, 4);
 
     LaneBases lb;
-    lb.a = p.cache + 8 * lane;
+    lb.a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
     lb.tail = p.cache + 448 + 16 * (lane >= 24 ? lane - 24 : 0);
     lb.s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
     Loaded r[U];
@@ -138,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, kRecord == 584 ? 6 : 8)
     uint8_t* orow = static_cast<uint8_t*>(p.out) + i0 * 1024 + 16 * lane;
 #pragma unroll
     for (int u = 0; u < U; ++u)
-        if (i0 + u < p.num_indices) convert_store<kRecord>(r[u], orow + u * 1024, lane);
+        if (i0 + u < p.num_indices) convert_store<kRecord>(r[u], orow + u * 1024, lane, scale);
 }
 
 template <int kRecord, int U>
@@ -156,6 +181,12 @@ cudaError_t launch_gather_v41(const GatherParams& p, cudaStream_t stream) {
 }
 cudaError_t launch_gather_v4(const GatherParams& p, cudaStream_t stream) {
     return launch<584, kPerWarp>(p, stream);
+}
+cudaError_t launch_gather_fp8(const GatherParams& p, cudaStream_t stream) {
+    return launch<512, kPerWarp>(p, stream);
+}
+cudaError_t launch_gather_bf16(const GatherParams& p, cudaStream_t stream) {
+    return launch<1024, kPerWarp>(p, stream);
 }
 
 }  // namespace gkr

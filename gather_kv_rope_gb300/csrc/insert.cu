@@ -1,4 +1,7 @@
-// RoPE + MXFP8 quantise + paged KV insert (V4.1 528 B and legacy V4 584 B records).
+// RoPE + MXFP8 quantise + paged KV insert (V4.1 528 B and legacy V4 584 B records),
+// and the same rotation into the two plain KV-only caches (bf16 rows; fp8 e4m3 rows
+// with one fp32 scale: page "PR #56441 [Perf][DSpark] KV-only context insertion
+// across V4.1 cache formats", section "实现拆解" item 1).
 //
 // Operation (page "PR #56893 [DSv4.1] Store the whole KV in MXFP8 (FlashMLA V4.1
 // record)", section "关键源码片段", the insert kernel of fused_compress_quant_cache.py,
@@ -112,6 +115,58 @@ __device__ __forceinline__ void encode_store_v4(const TokenLoads& L, uint8_t* da
     }
 }
 
+// bf16 cache row (1024 B): the row with dims 448..511 rotated, rounded to bf16.  Lane L
+// owns bytes [16L, 16L+16) (chunk A, copied) and [512+16L, 512+16L+16) (chunk B,
+// rotated on lanes 24..31).  `da` = row + 16L.
+__device__ __forceinline__ void encode_store_bf16(const TokenLoads& L, uint8_t* da, int lane) {
+    st16(da, L.a);
+    if (lane < 24) {
+        st16(da + 512, L.b);
+    } else {
+        float b[8];
+        unpack_bf16x8(L.b, b);
+        rope4(b, L.c, L.s);
+        st16(da + 512, make_uint4(pack_bf16x2_rn(b[0], b[1]), pack_bf16x2_rn(b[2], b[3]),
+                                  pack_bf16x2_rn(b[4], b[5]), pack_bf16x2_rn(b[6], b[7])));
+    }
+}
+
+// fp8 cache row (512 B): e4m3(x / scale) of the rotated row.  `da` = row + 8L.
+__device__ __forceinline__ void encode_store_fp8(const TokenLoads& L, uint8_t* da, int lane,
+                                                 float scale) {
+    float a[8], b[8];
+    unpack_bf16x8(L.a, a);
+    unpack_bf16x8(L.b, b);
+    if (lane >= 24) rope4(b, L.c, L.s);
+    st8(da, quantise8_div(a, scale));
+    st8(da + 256, quantise8_div(b, scale));
+}
+
+template <int kRecord, bool kSanitize = false>
+__device__ __forceinline__ void encode_store(const TokenLoads& L, uint8_t* da, uint8_t* sl,
+                                             int lane, float scale) {
+    if constexpr (kRecord == 528) encode_store_v41<kSanitize>(L, da, sl, lane);
+    else if constexpr (kRecord == 584) encode_store_v4<kSanitize>(L, da, sl, lane);
+    else if constexpr (kRecord == 1024) encode_store_bf16(L, da, lane);
+    else encode_store_fp8(L, da, lane, scale);
+}
+
+// The fp8 cache's scale (read once per warp), or 1 for the other formats.  Returns
+// false -- after setting the error bit from lane 0 -- when an fp8 scale is not a
+// positive finite number: the warp then writes nothing.
+template <int kRecord>
+__device__ __forceinline__ bool load_scale(const InsertParams& p, int lane, float& scale) {
+    scale = 1.0f;
+    if constexpr (kRecord == 512) {
+        scale = __ldg(p.fp8_scale);
+        if (!scale_ok(scale)) {
+            if (lane == 0) report(p.err, kErrScale);
+            return false;
+        }
+    }
+    return true;
+}
+
 // Lane-parallel decode of one group of 32 tokens: for this lane's token, the byte
 // offsets in the cache of its data row (-1 when the token is skipped or invalid) and
 // of its scale row, and its position.  Invalid slots and positions set GKR_ERR_SLOT /
@@ -119,8 +174,8 @@ __device__ __forceinline__ void encode_store_v4(const TokenLoads& L, uint8_t* da
 template <int kRecord>
 __device__ __forceinline__ void decode_group(const InsertParams& p, const WarpItems& w, int g,
                                              int lane, int64_t& off, int64_t& soff, int32_t& pos) {
-    constexpr uint32_t D = kRecord == 528 ? 512u : 576u;
-    constexpr uint32_t S = kRecord == 528 ? 16u : 8u;
+    constexpr uint32_t D = Fmt<kRecord>::D;
+    constexpr uint32_t S = Fmt<kRecord>::S;
     const int i = 32 * g + lane;
     off = -1;
     soff = 0;
@@ -181,12 +236,14 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
     const int wib = threadIdx.x >> 5;
     const WarpItems w = warp_items(m, static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib);
     if (w.n <= 0) return;  // warp-uniform
+    float scale;
+    if (!load_scale<kRecord>(p, lane, scale)) return;  // warp-uniform
     const int n = w.n;
     uint8_t* const ring_lane = smem + wib * (S * kSlotBytes) + 16 * lane;
     const uint8_t* const kv_lane = static_cast<const uint8_t*>(p.kv) + w.base * 1024 + 16 * lane;
     const int32_t kv_step = static_cast<int32_t>(w.step * 1024);
     const float* const csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
-    uint8_t* const cache_a = p.cache + 8 * lane;                                   // data row + 8L
+    uint8_t* const cache_a = p.cache + Fmt<kRecord>::kLaneBytes * lane;            // lane's row part
     uint8_t* const cache_s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3)); // scale byte
 
     // lane i of cur describes token 32*g + i of the group being processed; nxt the next
@@ -222,8 +279,7 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
                 L.c = *reinterpret_cast<const float4*>(src + 1024 - 16 * 24);
                 L.s = *reinterpret_cast<const float4*>(src + 1024 + 128 - 16 * 24);
             }
-            if (kRecord == 528) encode_store_v41(L, cache_a + off, cache_s + soff, lane);
-            else encode_store_v4(L, cache_a + off, cache_s + soff, lane);
+            encode_store<kRecord>(L, cache_a + off, cache_s + soff, lane, scale);
         }
         if ((j & 31) == 31) {                   // move to the next group of 32 tokens
             cur_off = nxt_off;
@@ -247,8 +303,10 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_short_kernel(
     const int lane = threadIdx.x & 31;
     const int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * U;
     if (t0 >= p.num_tokens) return;  // warp-uniform
-    constexpr uint32_t D = kRecord == 528 ? 512u : 576u;
-    constexpr uint32_t S = kRecord == 528 ? 16u : 8u;
+    float scale;
+    if (!load_scale<kRecord>(p, lane, scale)) return;  // warp-uniform
+    constexpr uint32_t D = Fmt<kRecord>::D;
+    constexpr uint32_t S = Fmt<kRecord>::S;
 
     // lane u < U decodes token t0 + u
     int64_t off = -1, soff = 0;
@@ -294,16 +352,13 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_short_kernel(
             }
         }
     }
-    uint8_t* const cache_a = p.cache + 8 * lane;
+    uint8_t* const cache_a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
     uint8_t* const cache_s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int64_t o = __shfl_sync(kFull, off, u);
         const int64_t so = __shfl_sync(kFull, soff, u);
-        if (valid[u]) {
-            if (kRecord == 528) encode_store_v41(L[u], cache_a + o, cache_s + so, lane);
-            else encode_store_v4(L[u], cache_a + o, cache_s + so, lane);
-        }
+        if (valid[u]) encode_store<kRecord>(L[u], cache_a + o, cache_s + so, lane, scale);
     }
 }
 
@@ -323,8 +378,9 @@ template <int kRecord>
 __device__ __forceinline__ uint32_t decode_compressed(const InsertParams& p, int64_t t,
                                                       int64_t& off, int64_t& soff,
                                                       int32_t& row) {
-    constexpr uint32_t D = kRecord == 528 ? 512u : 576u;
-    constexpr uint32_t S = kRecord == 528 ? 16u : 8u;
+    static_assert(Fmt<kRecord>::kPacked, "the compressed insert writes the packed records");
+    constexpr uint32_t D = Fmt<kRecord>::D;
+    constexpr uint32_t S = Fmt<kRecord>::S;
     const int64_t slot = __ldg(p.slots + t);
     const int64_t q = __ldg(p.positions + t);
     if (slot < 0) return 0u;
@@ -402,10 +458,8 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS)
         for (int v = 0; v < 2; ++v) {
             const int64_t o = __shfl_sync(kFull, off, u[v]);
             const int64_t so = __shfl_sync(kFull, soff, u[v]);
-            if (v == 0 || two) {
-                if (kRecord == 528) encode_store_v41<kSanitize>(L[v], cache_a + o, cache_s + so, lane);
-                else encode_store_v4<kSanitize>(L[v], cache_a + o, cache_s + so, lane);
-            }
+            if (v == 0 || two)
+                encode_store<kRecord, kSanitize>(L[v], cache_a + o, cache_s + so, lane, 1.0f);
         }
     }
 }
@@ -452,6 +506,12 @@ cudaError_t launch_insert_v41(const InsertParams& p, cudaStream_t stream) {
 }
 cudaError_t launch_insert_v4(const InsertParams& p, cudaStream_t stream) {
     return launch<584>(p, stream);
+}
+cudaError_t launch_insert_fp8(const InsertParams& p, cudaStream_t stream) {
+    return launch<512>(p, stream);
+}
+cudaError_t launch_insert_bf16(const InsertParams& p, cudaStream_t stream) {
+    return launch<1024>(p, stream);
 }
 cudaError_t launch_rope_quant_insert_v41(const InsertParams& p, bool sanitize,
                                          cudaStream_t stream) {

@@ -20,6 +20,7 @@ struct InsertParams {
     const float* csc;          // fp32 [max_pos, 64]
     int64_t max_pos;           // < 2^31 (checked on the host)
     int64_t ratio;             // compress ratio >= 1 (1 for the plain insert)
+    const float* fp8_scale;    // fp8 rows (record 512): the cache's scale; else unused
     int32_t* err;              // nullable
 };
 
@@ -32,7 +33,24 @@ struct GatherParams {
     const int32_t* indices;
     int64_t num_indices;
     void* out;                 // bf16 [num_indices, 512]
+    const float* fp8_scale;    // fp8 rows (record 512): the cache's scale; else unused
     int32_t* err;              // nullable
+};
+
+// Row geometry of the four cache formats ("record" = bytes a token occupies):
+//   528  V4.1 MXFP8 record: 512 B e4m3 data row + 16 B scale row;
+//   584  V4 record: 576 B data row (448 e4m3 + 64 bf16) + 8 B scale row;
+//   512  fp8 e4m3 row, one fp32 scale for the whole cache, no scale row;
+//   1024 bf16 row, no scale row.
+// A page holds block_size data rows, then block_size scale rows.
+template <int kRecord>
+struct Fmt {
+    static constexpr uint32_t D =
+        kRecord == 528 ? 512u : kRecord == 584 ? 576u : static_cast<uint32_t>(kRecord);
+    static constexpr uint32_t S = kRecord == 528 ? 16u : kRecord == 584 ? 8u : 0u;
+    // bytes of a row that lane L owns at 8L-dim granularity: 8 e4m3 or 16 bf16 bytes
+    static constexpr int kLaneBytes = kRecord == 1024 ? 16 : 8;
+    static constexpr bool kPacked = kRecord == 528 || kRecord == 584;
 };
 
 // Launch-shape helpers (api.cu).  `resident_warps` returns how many warps of `func`
@@ -122,6 +140,8 @@ __host__ __device__ inline WarpItems warp_items(const WorkMap& m, int64_t gw) {
 
 cudaError_t launch_insert_v41(const InsertParams& p, cudaStream_t stream);
 cudaError_t launch_insert_v4(const InsertParams& p, cudaStream_t stream);
+cudaError_t launch_insert_fp8(const InsertParams& p, cudaStream_t stream);
+cudaError_t launch_insert_bf16(const InsertParams& p, cudaStream_t stream);
 // Compressed-KV insert: only group-boundary tokens are written; NaN -> 0 if sanitize.
 cudaError_t launch_rope_quant_insert_v41(const InsertParams& p, bool sanitize,
                                          cudaStream_t stream);
@@ -129,5 +149,7 @@ cudaError_t launch_rope_quant_insert_v4(const InsertParams& p, bool sanitize,
                                         cudaStream_t stream);
 cudaError_t launch_gather_v41(const GatherParams& p, cudaStream_t stream);
 cudaError_t launch_gather_v4(const GatherParams& p, cudaStream_t stream);
+cudaError_t launch_gather_fp8(const GatherParams& p, cudaStream_t stream);
+cudaError_t launch_gather_bf16(const GatherParams& p, cudaStream_t stream);
 
 }  // namespace gkr

@@ -3,7 +3,8 @@
  * on NVIDIA GB300 (sm_103a).
  *
  *   gkr_kv_insert: bf16 latent [T, 512] -> RoPE on dims 448..511 -> MXFP8
- *                  (e4m3 + UE8M0) encode -> scatter into a paged cache;
+ *                  (e4m3 + UE8M0) encode -> scatter into a paged cache (or
+ *                  into a plain bf16 / fp8 e4m3 cache);
  *   gkr_kv_gather: the inverse: dequantise listed slots back to bf16 [N, 512];
  *   gkr_rope_quant_insert: the compressed-KV insert (one record per group of
  *                  compress_ratio positions, optional NaN sanitising).
@@ -18,7 +19,9 @@
  *     formats", section "实现拆解" items 1-2 (the KV-only insert contract:
  *     kv bf16 [tokens, 512], int64 slots and positions, fp32 cos_sin_cache
  *     [max_pos, 64], paged cache written in place);
- *   FlashMLA overview page, DSA section (index -1 marks an invalid entry).
+ *   FlashMLA overview page, DSA section (index -1 marks an invalid entry);
+ *   "PR #56441 ...", section "实现拆解" item 1 also names the two plain KV-only
+ *     caches (bf16; fp8 e4m3fn with a required fp32 scalar scale).
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers on the current CUDA device;
@@ -54,7 +57,7 @@ extern "C" {
 typedef enum gkr_status {
     GKR_OK = 0,
     GKR_EINVAL = 1,               /* null pointer, negative count, bad block size, ... */
-    GKR_EUNSUPPORTED_RECORD = 2,  /* record width not 528 or 584                        */
+    GKR_EUNSUPPORTED_RECORD = 2,  /* record width not 528, 584, 512 or 1024             */
     GKR_EBAD_PAGE_GEOMETRY = 3,   /* page stride too small or not a multiple of align   */
     GKR_EALIGN = 4,               /* a pointer is not aligned as documented             */
     GKR_ECUDA = 5                 /* the launch failed; see gkr_last_cuda_error()       */
@@ -64,6 +67,8 @@ typedef enum gkr_status {
 #define GKR_ERR_SLOT 1   /* insert: slot >= num_pages * block_size (token skipped)      */
 #define GKR_ERR_POS 2    /* insert: position < 0 or >= max_pos (token skipped)           */
 #define GKR_ERR_INDEX 4  /* gather: index < -1 or >= num_pages * block_size (row zeroed) */
+#define GKR_ERR_SCALE 8  /* fp8 cache: *fp8_scale not a positive finite number (nothing
+                            written by the insert; every gathered row zeroed)           */
 
 /*
  * Paged cache geometry.  The cache is num_pages pages, page p starting at byte
@@ -75,10 +80,13 @@ typedef enum gkr_status {
  *   record 584 (V4):   D = 576 (448 e4m3 bytes for dims 0..447, then dims
  *                      448..511 as little-endian bf16), S = 8 (7 UE8M0 bytes
  *                      per 64-dim block + 1 pad byte 0x00); page alignment 576.
+ *   record 512 (fp8):  D = 512 e4m3 codes of x / scale, S = 0; the scale is one
+ *                      fp32 for the whole cache, passed as fp8_scale; align 512.
+ *   record 1024 (bf16): D = 1024 (512 little-endian bf16), S = 0; align 512.
  * A slot s lives in page s / block_size, row s % block_size.
- * Requirements: record in {528, 584}; block_size > 0 and a multiple of 32;
- * num_pages > 0; page_stride >= block_size * record and a multiple of the
- * record's page alignment; num_pages * block_size < 2^31.
+ * Requirements: record in {528, 584, 512, 1024}; block_size > 0, and a multiple
+ * of 32 for 528 / 584; num_pages > 0; page_stride >= block_size * record and a
+ * multiple of the record's page alignment; num_pages * block_size < 2^31.
  */
 typedef struct gkr_cache_desc {
     int32_t record;
@@ -89,8 +97,8 @@ typedef struct gkr_cache_desc {
 
 /*
  * Smallest valid page stride: block_size * record rounded up to the record's
- * page alignment (512 for 528, 576 for 584).  Returns -1 for an unsupported
- * record or a block_size that is not a positive multiple of 32.
+ * page alignment (576 for 584, 512 otherwise).  Returns -1 for an unsupported
+ * record or block_size.
  */
 GKR_API int64_t gkr_page_stride(int32_t record, int32_t block_size);
 
@@ -113,7 +121,10 @@ GKR_API gkr_status gkr_record_rows(int32_t record, int32_t *data_row_bytes,
  *     b = clamp(ceil(log2(amax / 448)), -127, 127) + 127 (amax 0 -> b = 0),
  *     and each value is stored as e4m3(x / 2^(b - 127)), round to nearest even,
  *     saturating at +-448 (an infinite amax gives b = 254 and +-inf -> +-448);
- *   for 584 the rotated dims 448..511 are stored as bf16 (round to nearest even).
+ *   for 584 the rotated dims 448..511 are stored as bf16 (round to nearest even);
+ *   record 1024 stores the rotated row as bf16 (dims 0..447 unchanged);
+ *   record 512 stores e4m3(fl32(x / *fp8_scale)) for all 512 dims (one IEEE fp32
+ *     division, then the saturating nearest-even cast).
  *   NaN inputs, and non-finite inputs in dims 448..511 (whose rotation can give
  *   NaN, e.g. inf * 0), are outside the contract here (see gkr_rope_quant_insert).
  *
@@ -128,13 +139,17 @@ GKR_API gkr_status gkr_record_rows(int32_t record, int32_t *data_row_bytes,
  * cos_sin_cache  device, fp32 [max_pos, 64] row-major (cos 0..31 | sin 0..31),
  *                16-byte aligned.
  * max_pos        rows in cos_sin_cache, 0 < max_pos < 2^31.
- * err_flag       device int32 or NULL; GKR_ERR_SLOT / GKR_ERR_POS bits are OR-ed in.
+ * fp8_scale      device pointer to one fp32 (4-byte aligned): required for record
+ *                512 (GKR_EINVAL if NULL), ignored otherwise (may be NULL).
+ * err_flag       device int32 or NULL; GKR_ERR_SLOT / GKR_ERR_POS / GKR_ERR_SCALE
+ *                bits are OR-ed in.
  * stream         CUDA stream to enqueue on.
  */
 GKR_API gkr_status gkr_kv_insert(const void *kv, int64_t num_tokens, void *k_cache,
                                  const gkr_cache_desc *cache, const int64_t *slot_mapping,
                                  const int64_t *positions, const float *cos_sin_cache,
-                                 int64_t max_pos, int32_t *err_flag, cudaStream_t stream);
+                                 int64_t max_pos, const float *fp8_scale, int32_t *err_flag,
+                                 cudaStream_t stream);
 
 /*
  * rope_quant_insert: the compressed-KV insert ("PR #56893 [DSv4.1] Store the whole
@@ -148,7 +163,8 @@ GKR_API gkr_status gkr_kv_insert(const void *kv, int64_t num_tokens, void *k_cac
  *   cos/sin row r, and with sanitize_nans every NaN of the rotated row (all 512
  *   dims) is replaced by +0 before the block maxima are taken; scale bytes are then
  *   at most 254 (the UE8M0 NaN 255 is never written).
- * R = 1 without sanitising is gkr_kv_insert.  Arguments as for gkr_kv_insert, plus
+ * R = 1 without sanitising is gkr_kv_insert.  Records 528 and 584 only
+ * (GKR_EUNSUPPORTED_RECORD otherwise).  Arguments as for gkr_kv_insert, plus
  * compress_ratio  >= 1 (GKR_EINVAL otherwise);
  * sanitize_nans   0 or 1 (GKR_EINVAL otherwise).
  * Without sanitising, NaN inputs and non-finite inputs in dims 448..511 are outside
@@ -167,8 +183,10 @@ GKR_API gkr_status gkr_rope_quant_insert(const void *kv, int64_t num_tokens, voi
  *   otherwise slot s = indices[i]:
  *     528: out[i, d] = bf16(e4m3(data[d]) * 2^(scale[d / 32] - 127));
  *     584: d < 448 as above with scale[d / 64]; d >= 448 copies the stored bf16.
- *   The product is exact in fp32 and rounded once to bf16 (nearest even,
- *   subnormals kept).  An e4m3 NaN code (0x7F / 0xFF) or scale byte 255 (the
+ *     1024: out[i, :] = the stored bf16 row;
+ *     512: out[i, d] = bf16(fl32(e4m3(data[d]) * *fp8_scale)).
+ *   For 528 / 584 the product is exact in fp32 and rounded once to bf16 (nearest
+ *   even, subnormals kept).  An e4m3 NaN code (0x7F / 0xFF) or scale byte 255 (the
  *   UE8M0 NaN) yields the bf16 NaN 0x7FC0.
  *
  * k_cache      device, the cache described by *cache, 16-byte aligned; read only.
@@ -176,12 +194,14 @@ GKR_API gkr_status gkr_rope_quant_insert(const void *kv, int64_t num_tokens, voi
  * indices      device, int32 [num_indices].
  * num_indices  >= 0; 0 enqueues nothing.
  * out          device, bf16 [num_indices, 512] row-major, 16-byte aligned.
- * err_flag     device int32 or NULL; GKR_ERR_INDEX is OR-ed in.
+ * fp8_scale    device pointer to one fp32: required for record 512, else ignored.
+ * err_flag     device int32 or NULL; GKR_ERR_INDEX / GKR_ERR_SCALE are OR-ed in.
  * stream       CUDA stream to enqueue on.
  */
 GKR_API gkr_status gkr_kv_gather(const void *k_cache, const gkr_cache_desc *cache,
                                  const int32_t *indices, int64_t num_indices, void *out,
-                                 int32_t *err_flag, cudaStream_t stream);
+                                 const float *fp8_scale, int32_t *err_flag,
+                                 cudaStream_t stream);
 
 /*
  * Programmatic dependent launch (process-wide, default on).  When on, kernels are

@@ -50,8 +50,13 @@ def test_page_stride_and_rows(gkr):
     assert gkr.page_stride(528, 0) == -1
     assert gkr.record_rows(528) == (512, 16, 512)
     assert gkr.record_rows(584) == (576, 8, 576)
+    assert gkr.record_rows(512) == (512, 0, 512)          # fp8 e4m3 rows
+    assert gkr.record_rows(1024) == (1024, 0, 512)        # bf16 rows
+    assert gkr.page_stride(512, 48) == 48 * 512           # plain caches: any block size
+    assert gkr.page_stride(1024, 1) == 1024
+    assert gkr.page_stride(1024, 0) == -1
     with pytest.raises(ValueError):
-        gkr.record_rows(512)
+        gkr.record_rows(500)
     assert gkr.lib().gkr_version() == 10000
     assert gkr.get_insert_stream_min() == 32768
     gkr.set_insert_stream_min(5)
@@ -61,7 +66,8 @@ def test_page_stride_and_rows(gkr):
     assert gkr.status_string(0) == "ok"
 
 
-# --- host-side checks through the raw ABI (fake device pointers never reach a kernel)
+# --- host-side checks through the raw ABI (fake device pointers never reach a kernel:
+# every call below fails a host check, or enqueues nothing, before any launch)
 
 A16 = 0x10000          # 16-byte aligned fake pointers: checks must fail before any launch
 A16b = 0x20000
@@ -71,9 +77,10 @@ def desc(gkr, record=528, bs=64, pages=4, ps=None):
     return gkr.CacheDesc(record, bs, pages, gkr.page_stride(record, bs) if ps is None else ps)
 
 
-def insert(gkr, d, T=8, kv=A16, cache=A16b, slots=A16, pos=A16, csc=A16, max_pos=16, err=None):
+def insert(gkr, d, T=8, kv=A16, cache=A16b, slots=A16, pos=A16, csc=A16, max_pos=16, err=None,
+           scale=None):
     return gkr.lib().gkr_kv_insert(kv, T, cache, None if d is None else ctypes.byref(d),
-                                   slots, pos, csc, max_pos, err, None)
+                                   slots, pos, csc, max_pos, scale, err, None)
 
 
 def rq_insert(gkr, d, T=8, kv=A16, cache=A16b, slots=A16, pos=A16, csc=A16, max_pos=16,
@@ -82,15 +89,15 @@ def rq_insert(gkr, d, T=8, kv=A16, cache=A16b, slots=A16, pos=A16, csc=A16, max_
                                            slots, pos, csc, max_pos, ratio, sanitize, err, None)
 
 
-def gather(gkr, d, N=8, cache=A16b, idx=A16, out=A16, err=None):
+def gather(gkr, d, N=8, cache=A16b, idx=A16, out=A16, err=None, scale=None):
     return gkr.lib().gkr_kv_gather(cache, None if d is None else ctypes.byref(d), idx, N,
-                                   out, err, None)
+                                   out, scale, err, None)
 
 
 @pytest.mark.parametrize("op", [insert, rq_insert, gather])
 def test_geometry_checks(gkr, op):
     assert op(gkr, None) == 1                                        # null descriptor
-    assert op(gkr, desc(gkr, record=512)) == 2                       # unsupported record
+    assert op(gkr, desc(gkr, record=500)) == 2                       # unsupported record
     assert op(gkr, desc(gkr, bs=48)) == 1                            # block size % 32
     assert op(gkr, desc(gkr, bs=0)) == 1
     assert op(gkr, desc(gkr, pages=0)) == 1
@@ -112,6 +119,20 @@ def test_insert_argument_checks(gkr):
     assert insert(gkr, d, csc=A16 + 8) == 4
     assert insert(gkr, d, slots=A16 + 4) == 4
     assert insert(gkr, d, err=A16 + 2) == 4
+
+
+@pytest.mark.parametrize("op", [insert, gather])
+def test_plain_cache_checks(gkr, op):
+    assert op(gkr, desc(gkr, record=1024, bs=48, ps=48 * 1024 + 256)) == 3   # not % 512
+    assert op(gkr, desc(gkr, record=1024, bs=48, ps=47 * 1024)) == 3
+    assert op(gkr, desc(gkr, record=512, bs=0)) == 1
+    assert op(gkr, desc(gkr, record=512)) == 1                        # fp8 without a scale
+    assert op(gkr, desc(gkr, record=512), scale=A16 + 2) == 4         # misaligned scale
+
+
+def test_compressed_insert_rejects_plain_caches(gkr):
+    assert rq_insert(gkr, desc(gkr, record=1024)) == 2
+    assert rq_insert(gkr, desc(gkr, record=512)) == 2
 
 
 def test_insert_max_pos_bound(gkr):

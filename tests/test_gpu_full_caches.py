@@ -1,0 +1,173 @@
+"""GPU parity for the two plain KV-only caches (bf16 rows, fp8 e4m3 rows with one fp32
+scale): kv_insert and kv_gather through the C ABI vs the CPU oracle, byte for byte over
+the whole sentinel-filled backing buffer, with both insert kernels."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from golden_parse import GOLDEN, load_worked, worked_inputs
+from helpers import SENTINEL, bf16_from_bits, device_inputs, first_mismatch
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(params=["short", "stream"], autouse=True)
+def insert_kernel_choice(request, gkr):
+    gkr.set_insert_stream_min(1 << 62 if request.param == "short" else 0)
+    yield request.param
+    gkr.set_insert_stream_min(-1)
+
+
+def _scale_t(scale):
+    return None if scale is None else torch.tensor([scale], dtype=torch.float32, device=DEV)
+
+
+def _insert(gkr, oracle_mod, case, record, scale=None, pad_units=0):
+    """GPU and oracle insert of `case` into a `record` cache; returns (got, ref, errs)."""
+    ps = oracle_mod.page_stride(record, case.block_size) + 512 * pad_units
+    kv, slots, pos, csc = device_inputs(case, DEV)
+    cache = gkr.alloc_cache(case.num_pages, case.block_size, record, DEV, page_stride_bytes=ps,
+                            fill=SENTINEL)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gkr.kv_insert(kv, cache, slots, pos, csc, case.block_size, record, err_flag=err,
+                  fp8_scale=_scale_t(scale))
+    ref = np.full(case.num_pages * ps, SENTINEL, np.uint8)
+    ref_err = oracle_mod.insert(case.kv, ref, record, case.block_size, case.num_pages, ps,
+                                case.slots, case.positions, case.csc, fp8_scale=scale)
+    return cache, gkr.cache_bytes(cache).cpu().numpy(), ref, int(err.item()), ref_err, ps
+
+
+def _case(T, bs, seed, sigma=1.0, inf_rate=0.0):
+    pages = max(2, -(-2 * T // bs))
+    c = W.compressed_insert(f"plain_{T}", 1, T, 1, 528, block_size=bs, skip_rate=0.1,
+                            seed=seed, sigma=sigma, dist="student_t3", inf_rate=inf_rate,
+                            nonfinite_dims=448)
+    c.positions = np.random.default_rng(seed).integers(0, c.csc.shape[0], T)
+    # distinct random slots over twice the needed pages
+    slots = np.random.default_rng(seed + 1).permutation(pages * bs)[:T].astype(np.int64)
+    c.slots = np.where(c.slots >= 0, slots, -1)
+    c.num_pages = pages
+    return c
+
+
+@pytest.mark.parametrize("record", [1024, 512])
+def test_plain_cache_golden(gkr, record):
+    w = load_worked(GOLDEN / "worked_full_caches.txt")
+    kv_bits, slots, pos, csc = worked_inputs(w)
+    ps, expects = w.records[record]
+    cache = gkr.alloc_cache(w.num_pages, w.block_size, record, DEV, page_stride_bytes=ps,
+                            fill=SENTINEL)
+    scale = _scale_t(w.fp8_scale.get(record))
+    gkr.kv_insert(bf16_from_bits(kv_bits, DEV), cache, torch.from_numpy(slots).to(DEV),
+                  torch.from_numpy(pos).to(DEV), torch.from_numpy(csc).to(DEV), w.block_size,
+                  record, fp8_scale=scale)
+    got = gkr.cache_bytes(cache).cpu().numpy()
+    touched = np.zeros(got.size, bool)
+    for e in expects:
+        assert np.array_equal(got[e.data_offset:e.data_offset + e.data.size], e.data), e.token
+        touched[e.data_offset:e.data_offset + e.data.size] = True
+    assert (got[~touched] == SENTINEL).all()
+    idx, expect = w.gathers[record]
+    out = torch.empty(idx.size, 512, dtype=torch.bfloat16, device=DEV)
+    gkr.kv_gather(cache, torch.from_numpy(idx).to(DEV), out, fp8_scale=scale)
+    got_out = out.cpu().view(torch.int16).numpy().view(np.uint16).astype(np.int64)
+    assert np.array_equal(got_out, expect)
+
+
+@pytest.mark.parametrize("record,scale", [(1024, None), (512, 0.0078125), (512, 0.37),
+                                          (512, 3.0), (512, 1.0 / 3.0)])
+@pytest.mark.parametrize("T,bs", [(1, 16), (17, 48), (1023, 64), (4099, 64)])
+def test_plain_cache_insert_and_gather_match_oracle(gkr, oracle_mod, record, scale, T, bs):
+    case = _case(T, bs, seed=T + bs, sigma=2.0, inf_rate=0.0005)
+    cache, got, ref, err, ref_err, ps = _insert(gkr, oracle_mod, case, record, scale,
+                                                pad_units=1)
+    n, first = first_mismatch(got, ref)
+    assert n == 0, f"{record} scale={scale}: {n} bytes differ, first {first}"
+    assert err == ref_err == 0
+    idx = np.concatenate([case.slots, [-1, 0, case.num_pages * bs - 1]]).astype(np.int32)
+    out = torch.empty(idx.size, 512, dtype=torch.bfloat16, device=DEV)
+    gkr.kv_gather(cache, torch.from_numpy(idx).to(DEV), out, fp8_scale=_scale_t(scale))
+    ref_out, _ = oracle_mod.gather(ref, record, bs, case.num_pages, ps, idx, fp8_scale=scale)
+    assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), ref_out)
+
+
+@pytest.mark.parametrize("scale", [0.0, -1.0, float("inf"), float("nan")])
+def test_fp8_bad_scale(gkr, oracle_mod, scale):
+    case = _case(300, 32, seed=3)
+    cache, got, ref, err, ref_err, ps = _insert(gkr, oracle_mod, case, 512, scale)
+    assert err == ref_err == 8 and (got == SENTINEL).all() and (ref == SENTINEL).all()
+    idx = torch.from_numpy(case.slots.astype(np.int32)).to(DEV)
+    out = torch.full((idx.numel(), 512), 1.0, dtype=torch.bfloat16, device=DEV)
+    e = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gkr.kv_gather(cache, idx, out, err_flag=e, fp8_scale=_scale_t(scale))
+    assert int(e.item()) == 8 and (out.view(torch.int16) == 0).all()
+
+
+@pytest.mark.parametrize("record", [1024, 512])
+def test_plain_cache_error_bits(gkr, oracle_mod, record):
+    case = _case(64, 32, seed=8)
+    case.slots[3] = case.num_pages * 32
+    case.positions[9] = case.csc.shape[0]
+    _, got, ref, err, ref_err, _ = _insert(gkr, oracle_mod, case, record,
+                                           0.5 if record == 512 else None)
+    assert err == ref_err == 3
+    assert first_mismatch(got, ref)[0] == 0
+
+
+def test_fp8_scale_is_read_on_the_device_at_replay(gkr, oracle_mod):
+    """The scale lives in device memory: a captured insert picks up a new value."""
+    case = _case(512, 64, seed=11)
+    ps = oracle_mod.page_stride(512, 64)
+    kv, slots, pos, csc = device_inputs(case, DEV)
+    cache = gkr.alloc_cache(case.num_pages, 64, 512, DEV, fill=SENTINEL)
+    scale = torch.tensor([1.0], dtype=torch.float32, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        gkr.kv_insert(kv, cache, slots, pos, csc, 64, 512, fp8_scale=scale)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        gkr.kv_insert(kv, cache, slots, pos, csc, 64, 512, fp8_scale=scale)
+    for value in (0.25, 3.0):
+        scale.fill_(value)
+        g.replay()
+        torch.cuda.synchronize()
+        ref = np.full(case.num_pages * ps, SENTINEL, np.uint8)
+        oracle_mod.insert(case.kv, ref, 512, 64, case.num_pages, ps, case.slots, case.positions,
+                          case.csc, fp8_scale=value)
+        assert first_mismatch(gkr.cache_bytes(cache).cpu().numpy(), ref)[0] == 0
+
+
+@pytest.mark.parametrize("record", [1024, 512])
+def test_plain_cache_full_size_sampled(gkr, oracle_mod, record):
+    """262144 tokens in 8 contiguous sequences (the large-insert layout) into a plain
+    cache: sampled rows against the oracle, every other byte untouched."""
+    case = W.insert_v41_262144()
+    scale = 0.01 if record == 512 else None
+    ps = oracle_mod.page_stride(record, 64)
+    kv, slots, pos, csc = device_inputs(case, DEV)
+    cache = gkr.alloc_cache(case.num_pages, 64, record, DEV, fill=SENTINEL)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gkr.kv_insert(kv, cache, slots, pos, csc, 64, record, err_flag=err, fp8_scale=_scale_t(scale))
+    got = gkr.cache_bytes(cache).cpu().numpy()
+    assert int(err.item()) == 0
+    rng = np.random.default_rng(2)
+    valid = np.nonzero(case.slots >= 0)[0]
+    pick = np.unique(np.concatenate([valid[:4], valid[-4:], rng.choice(valid, 2000, replace=False)]))
+    sub = W.InsertCase("sub", 528, 64, case.num_pages, case.kv[pick], case.slots[pick],
+                       case.positions[pick], case.csc)
+    ref = np.full(case.num_pages * ps, SENTINEL, np.uint8)
+    oracle_mod.insert(sub.kv, ref, record, 64, case.num_pages, ps, sub.slots, sub.positions,
+                      sub.csc, fp8_scale=scale)
+    rows = (case.slots[pick] // 64) * ps + (case.slots[pick] % 64) * record
+    for r in rows:
+        assert np.array_equal(got[r:r + record], ref[r:r + record]), r
+    assert ps == 64 * record                    # no padding: row r of the cache is slot r
+    written = np.zeros(case.num_pages * 64, bool)
+    written[case.slots[valid]] = True
+    assert (got.reshape(-1, record)[~written] == SENTINEL).all()
