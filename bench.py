@@ -746,8 +746,7 @@ def main(argv=None):
             "isolated_timing": r["iso_timing"]}
     dom = "insert" if r["ins_ms"] >= r["gat_ms"] else "gather"
     ach = kern[dom]["gbs"]
-    stream_min = gkr.get_insert_stream_min()
-    kname = {"insert": "insert_kernel" if T >= stream_min else "insert_short_kernel",
+    kname = {"insert": gkr.insert_kernel_for(T),
              "gather": "gather_kernel"}[dom]
     roofline = {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
                 "frac": ach / peak, "peak_source": peak_src,

@@ -89,6 +89,9 @@ def lib() -> ctypes.CDLL:
                 L.gkr_set_insert_stream_min.argtypes = [i64]
                 L.gkr_set_insert_stream_min.restype = None
                 L.gkr_get_insert_stream_min.argtypes, L.gkr_get_insert_stream_min.restype = [], i64
+                L.gkr_set_insert_staged_min.argtypes = [i64]
+                L.gkr_set_insert_staged_min.restype = None
+                L.gkr_get_insert_staged_min.argtypes, L.gkr_get_insert_staged_min.restype = [], i64
                 _lib = L
     return _lib
 
@@ -123,6 +126,24 @@ def set_insert_stream_min(tokens: int) -> None:
 
 def get_insert_stream_min() -> int:
     return int(lib().gkr_get_insert_stream_min())
+
+
+def set_insert_staged_min(tokens: int) -> None:
+    """Token count from which inserts below the streaming threshold use the staged
+    kernel (negative = default)."""
+    lib().gkr_set_insert_staged_min(int(tokens))
+
+
+def get_insert_staged_min() -> int:
+    return int(lib().gkr_get_insert_staged_min())
+
+
+def insert_kernel_for(num_tokens: int) -> str:
+    """Name of the kernel kv_insert launches for `num_tokens` under the current policy."""
+    if num_tokens < get_insert_stream_min():
+        return "insert_short_kernel" if num_tokens < get_insert_staged_min() else \
+            "insert_staged_kernel"
+    return "insert_kernel"
 
 
 def page_stride(record: int, block_size: int) -> int:

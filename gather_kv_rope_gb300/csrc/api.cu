@@ -12,7 +12,9 @@ namespace {
 
 thread_local int32_t g_last_cuda_error = 0;
 std::atomic<int> g_pdl{1};
-constexpr int64_t kDefaultStreamMin = 32768;
+constexpr int64_t kDefaultStagedMin = 24576;
+constexpr int64_t kDefaultStreamMin = 131072;
+std::atomic<int64_t> g_staged_min{kDefaultStagedMin};
 std::atomic<int64_t> g_stream_min{kDefaultStreamMin};
 
 struct OccEntry {
@@ -80,6 +82,8 @@ bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
 
 int64_t insert_stream_min() { return g_stream_min.load(std::memory_order_relaxed); }
 
+int64_t insert_staged_min() { return g_staged_min.load(std::memory_order_relaxed); }
+
 cudaError_t resident_warps(const void* func, int threads, size_t smem, int64_t* warps) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -121,6 +125,12 @@ GKR_API void gkr_set_insert_stream_min(int64_t tokens) {
 }
 
 GKR_API int64_t gkr_get_insert_stream_min(void) { return g_stream_min.load(); }
+
+GKR_API void gkr_set_insert_staged_min(int64_t tokens) {
+    g_staged_min.store(tokens < 0 ? kDefaultStagedMin : tokens);
+}
+
+GKR_API int64_t gkr_get_insert_staged_min(void) { return g_staged_min.load(); }
 
 GKR_API int64_t gkr_page_stride(int32_t record, int32_t block_size) {
     RecordRows r;

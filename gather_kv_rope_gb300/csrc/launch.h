@@ -62,7 +62,8 @@ struct Fmt {
 cudaError_t resident_warps(const void* func, int threads, size_t smem, int64_t* warps);
 // Whether launches carry the programmatic-dependent-launch attribute.
 bool pdl_enabled();
-// Token count from which inserts use the streaming kernel.
+// Token counts from which inserts use the staged kernel, and the streaming kernel.
+int64_t insert_staged_min();
 int64_t insert_stream_min();
 
 // Launch `kernel` with the PDL attribute when enabled.

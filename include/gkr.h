@@ -215,14 +215,21 @@ GKR_API void gkr_set_pdl(int32_t enable);
 GKR_API int32_t gkr_get_pdl(void);
 
 /*
- * Insert launch policy (process-wide).  Inserts of at least `tokens` tokens use the
- * streaming kernel (a per-warp shared-memory pipeline over long runs of tokens);
- * smaller inserts use short-lived warps of two tokens each.  Both write identical
- * bytes; the split only trades latency against streaming depth.  Default 32768.
- * A negative value restores the default.
+ * Insert launch policy (process-wide; gkr_kv_insert only).  Three kernels write
+ * identical bytes and differ only in how they hide memory latency:
+ *   T < staged_min (and < stream_min): short-lived warps of two tokens, loads to
+ *                                      registers;
+ *   staged_min <= T < stream_min:      short-lived warps of 1-3 tokens staged in
+ *                                      shared memory with cp.async;
+ *   T >= stream_min:                   warps streaming runs of up to 16 tokens through a
+ *                                      4-deep shared-memory ring.
+ * Defaults: staged_min 24576, stream_min 131072 (measured crossovers on GB300).  A
+ * negative value restores the default.
  */
 GKR_API void gkr_set_insert_stream_min(int64_t tokens);
 GKR_API int64_t gkr_get_insert_stream_min(void);
+GKR_API void gkr_set_insert_staged_min(int64_t tokens);
+GKR_API int64_t gkr_get_insert_staged_min(void);
 
 /* Static, NUL-terminated description of a status code. */
 GKR_API const char *gkr_status_string(gkr_status status);

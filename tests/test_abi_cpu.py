@@ -25,6 +25,7 @@ def test_header_declares_the_boundary():
     assert {"gkr_kv_insert", "gkr_kv_gather", "gkr_page_stride", "gkr_record_rows",
             "gkr_status_string", "gkr_last_cuda_error", "gkr_version", "gkr_set_pdl",
             "gkr_get_pdl", "gkr_set_insert_stream_min", "gkr_get_insert_stream_min",
+            "gkr_set_insert_staged_min", "gkr_get_insert_staged_min",
             "gkr_rope_quant_insert"} <= syms
 
 
@@ -58,11 +59,18 @@ def test_page_stride_and_rows(gkr):
     with pytest.raises(ValueError):
         gkr.record_rows(500)
     assert gkr.lib().gkr_version() == 10000
-    assert gkr.get_insert_stream_min() == 32768
+    assert gkr.get_insert_stream_min() == 131072
+    assert gkr.get_insert_staged_min() == 24576
+    assert gkr.insert_kernel_for(16384) == "insert_short_kernel"
+    assert gkr.insert_kernel_for(65536) == "insert_staged_kernel"
+    assert gkr.insert_kernel_for(262144) == "insert_kernel"
     gkr.set_insert_stream_min(5)
-    assert gkr.get_insert_stream_min() == 5
+    gkr.set_insert_staged_min(3)
+    assert gkr.get_insert_stream_min() == 5 and gkr.get_insert_staged_min() == 3
+    assert gkr.insert_kernel_for(4) == "insert_staged_kernel"
     gkr.set_insert_stream_min(-1)
-    assert gkr.get_insert_stream_min() == 32768
+    gkr.set_insert_staged_min(-1)
+    assert gkr.get_insert_stream_min() == 131072 and gkr.get_insert_staged_min() == 24576
     assert gkr.status_string(0) == "ok"
 
 

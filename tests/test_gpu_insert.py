@@ -18,12 +18,17 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
 
-@pytest.fixture(params=["short", "stream"], autouse=True)
+@pytest.fixture(params=["short", "staged", "stream"], autouse=True)
 def insert_kernel_choice(request, gkr):
-    """Run every insert test with both insert kernels: short-lived warps (the default
-    below 32768 tokens) and the streaming pipeline (the default from there on)."""
-    gkr.set_insert_stream_min(1 << 62 if request.param == "short" else 0)
+    """Run every insert test with each of the three insert kernels (register loads,
+    shared-memory staging, streaming ring) regardless of the token count."""
+    big = 1 << 62
+    staged_min, stream_min = {"short": (big, big), "staged": (0, big),
+                              "stream": (big, 0)}[request.param]
+    gkr.set_insert_staged_min(staged_min)
+    gkr.set_insert_stream_min(stream_min)
     yield request.param
+    gkr.set_insert_staged_min(-1)
     gkr.set_insert_stream_min(-1)
 
 
