@@ -249,9 +249,45 @@ constexpr int32_t kErrScale = 8;
 
 __device__ __forceinline__ bool scale_ok(float s) { return s > 0.0f && s <= 3.40282347e38f; }
 
-// Eight values -> e4m3(x / scale): one IEEE fp32 division each (nearest even), then the
-// saturating nearest-even e4m3 cast.
-__device__ __forceinline__ uint2 quantise8_div(const float* f, float scale) {
+// The quotient x / s for the fp8 cache, as the e4m3 cast sees it.  With y = RN(1/s) (the
+// correctly rounded reciprocal, computed once per warp) the quotient of |x| is the
+// product |x| * y refined by two correction steps q' = RN(q + RN(|x| - q s) * y), each a
+// fused multiply-add: Markstein's iteration ("Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  After the first step q
+// is a faithful rounding of |x|/s, so the second returns RN(|x|/s) whenever the residual
+// |x| - q s is exact, i.e. away from underflow.  For s in [2^-64, 2^64] an inexact
+// residual needs |x| < 2^-102 and then |x|/s < 2^-38, far below the smallest e4m3 value,
+// so the e4m3 code always equals that of the IEEE quotient.  Outside that range (and for
+// y == 0) the callers use the IEEE division instead.  The sign is carried separately so
+// that -0 and negative underflow keep it, as the division does.
+__device__ __forceinline__ float quotient(float x, float s, float y) {
+    const float a = fabsf(x);
+    const float q0 = __fmul_rn(a, y);
+    const float q1 = __fmaf_rn(__fmaf_rn(-q0, s, a), y, q0);
+    const float q2 = __fmaf_rn(__fmaf_rn(-q1, s, a), y, q1);
+    const float q = q0 <= 3.40282347e38f ? q2 : q0;  // q0 = inf: the quotient overflows
+    return copysignf(q, x);
+}
+
+// 1/s for the corrected quotient, or 0 (use the IEEE division) when s is outside
+// [2^-64, 2^64].
+__device__ __forceinline__ float quotient_reciprocal(float s) {
+    return (s >= 5.42101086e-20f && s <= 1.84467441e19f) ? __frcp_rn(s) : 0.0f;
+}
+
+// Eight values -> e4m3(x / scale): the IEEE fp32 quotient (nearest even) by the corrected
+// reciprocal y, then the saturating nearest-even e4m3 cast.
+__device__ __forceinline__ uint2 quantise8_div(const float* f, float scale, float y) {
+    uint2 q;
+    q.x = e4m3x4(quotient(f[0], scale, y), quotient(f[1], scale, y), quotient(f[2], scale, y),
+                 quotient(f[3], scale, y));
+    q.y = e4m3x4(quotient(f[4], scale, y), quotient(f[5], scale, y), quotient(f[6], scale, y),
+                 quotient(f[7], scale, y));
+    return q;
+}
+
+// The same with one IEEE division per value (scales outside [2^-64, 2^64]).
+__device__ __forceinline__ uint2 quantise8_ieee_div(const float* f, float scale) {
     uint2 q;
     q.x = e4m3x4(__fdiv_rn(f[0], scale), __fdiv_rn(f[1], scale), __fdiv_rn(f[2], scale),
                  __fdiv_rn(f[3], scale));

@@ -131,38 +131,61 @@ __device__ __forceinline__ void encode_store_bf16(const TokenLoads& L, uint8_t* 
     }
 }
 
+// The fp8 cache's scale s and y = RN(1/s) for the corrected quotient (0: divide).
+struct Scale {
+    float s, y;
+};
+
+// fp8 row by IEEE divisions: the rare path (a scale outside [2^-64, 2^64]), kept out of
+// line so that the common path keeps its registers.
+__device__ __noinline__ void encode_store_fp8_ieee(uint4 ta, uint4 tb, float4 c, float4 sn,
+                                                   uint8_t* da, int lane, float scale) {
+    float a[8], b[8];
+    unpack_bf16x8(ta, a);
+    unpack_bf16x8(tb, b);
+    if (lane >= 24) rope4(b, c, sn);
+    st8(da, quantise8_ieee_div(a, scale));
+    st8(da + 256, quantise8_ieee_div(b, scale));
+}
+
 // fp8 cache row (512 B): e4m3(x / scale) of the rotated row.  `da` = row + 8L.
 __device__ __forceinline__ void encode_store_fp8(const TokenLoads& L, uint8_t* da, int lane,
-                                                 float scale) {
+                                                 Scale sc) {
+    if (sc.y == 0.0f) {  // warp-uniform
+        encode_store_fp8_ieee(L.a, L.b, L.c, L.s, da, lane, sc.s);
+        return;
+    }
     float a[8], b[8];
     unpack_bf16x8(L.a, a);
     unpack_bf16x8(L.b, b);
     if (lane >= 24) rope4(b, L.c, L.s);
-    st8(da, quantise8_div(a, scale));
-    st8(da + 256, quantise8_div(b, scale));
+    st8(da, quantise8_div(a, sc.s, sc.y));
+    st8(da + 256, quantise8_div(b, sc.s, sc.y));
 }
 
 template <int kRecord, bool kSanitize = false>
 __device__ __forceinline__ void encode_store(const TokenLoads& L, uint8_t* da, uint8_t* sl,
-                                             int lane, float scale) {
+                                             int lane, Scale sc) {
     if constexpr (kRecord == 528) encode_store_v41<kSanitize>(L, da, sl, lane);
     else if constexpr (kRecord == 584) encode_store_v4<kSanitize>(L, da, sl, lane);
     else if constexpr (kRecord == 1024) encode_store_bf16(L, da, lane);
-    else encode_store_fp8(L, da, lane, scale);
+    else encode_store_fp8(L, da, lane, sc);
 }
 
-// The fp8 cache's scale (read once per warp), or 1 for the other formats.  Returns
-// false -- after setting the error bit from lane 0 -- when an fp8 scale is not a
-// positive finite number: the warp then writes nothing.
+// The fp8 cache's scale (read once per warp) and its reciprocal; unused for the other
+// formats.  Returns false -- after setting the error bit from lane 0 -- when an fp8 scale
+// is not a positive finite number: the warp then writes nothing.
 template <int kRecord>
-__device__ __forceinline__ bool load_scale(const InsertParams& p, int lane, float& scale) {
-    scale = 1.0f;
+__device__ __forceinline__ bool load_scale(const InsertParams& p, int lane, Scale& sc) {
+    sc.s = 1.0f;
+    sc.y = 1.0f;
     if constexpr (kRecord == 512) {
-        scale = __ldg(p.fp8_scale);
-        if (!scale_ok(scale)) {
+        sc.s = __ldg(p.fp8_scale);
+        if (!scale_ok(sc.s)) {
             if (lane == 0) report(p.err, kErrScale);
             return false;
         }
+        sc.y = quotient_reciprocal(sc.s);
     }
     return true;
 }
@@ -236,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
     const int wib = threadIdx.x >> 5;
     const WarpItems w = warp_items(m, static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib);
     if (w.n <= 0) return;  // warp-uniform
-    float scale;
+    Scale scale;
     if (!load_scale<kRecord>(p, lane, scale)) return;  // warp-uniform
     const int n = w.n;
     uint8_t* const ring_lane = smem + wib * (S * kSlotBytes) + 16 * lane;
@@ -296,14 +319,18 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
 // straight to registers before the first token is encoded.  Below a few hundred
 // thousand tokens an insert is latency-bound, and many small resident warps beat a
 // deep per-warp pipeline.
+#ifndef GKR_SHORT_MIN_BLOCKS
+#define GKR_SHORT_MIN_BLOCKS 5   // 48 registers: 5 blocks per SM (6.14 vs 6.32 us at 4, 16k tokens)
+#endif
 template <int kRecord, int U>
-__global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_short_kernel(const InsertParams p) {
+__global__ void __launch_bounds__(kThreads, GKR_SHORT_MIN_BLOCKS)
+    insert_short_kernel(const InsertParams p) {
     pdl_wait_previous();
     pdl_release_next();
     const int lane = threadIdx.x & 31;
     const int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * U;
     if (t0 >= p.num_tokens) return;  // warp-uniform
-    float scale;
+    Scale scale;
     if (!load_scale<kRecord>(p, lane, scale)) return;  // warp-uniform
     constexpr uint32_t D = Fmt<kRecord>::D;
     constexpr uint32_t S = Fmt<kRecord>::S;
@@ -459,7 +486,8 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS)
             const int64_t o = __shfl_sync(kFull, off, u[v]);
             const int64_t so = __shfl_sync(kFull, soff, u[v]);
             if (v == 0 || two)
-                encode_store<kRecord, kSanitize>(L[v], cache_a + o, cache_s + so, lane, 1.0f);
+                encode_store<kRecord, kSanitize>(L[v], cache_a + o, cache_s + so, lane,
+                                                 Scale{1.0f, 1.0f});
         }
     }
 }
@@ -467,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS)
 #ifndef GKR_STAGE_MIN_BLOCKS
 #define GKR_STAGE_MIN_BLOCKS 6
 #endif
+
 
 // Short-lived warps with shared-memory staging, for medium inserts: one warp per U
 // consecutive tokens, lanes 0..U-1 decode them, then every lane copies its own 16-byte
@@ -486,10 +515,12 @@ __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
     const int wib = threadIdx.x >> 5;
     const int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib) * U;
     if (t0 >= p.num_tokens) return;  // warp-uniform
-    float scale;
+    Scale scale;
     if (!load_scale<kRecord>(p, lane, scale)) return;  // warp-uniform
     constexpr uint32_t D = Fmt<kRecord>::D;
     constexpr uint32_t S = Fmt<kRecord>::S;
+    const uint8_t* const kv_lane = static_cast<const uint8_t*>(p.kv) + t0 * 1024 + 16 * lane;
+    uint8_t* const ring_lane = smem + wib * (U * kSlotBytes) + 16 * lane;
 
     int64_t off = -1, soff = 0;
     int32_t pos = 0;
@@ -516,9 +547,7 @@ __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
     err = __reduce_or_sync(kFull, err);
     if (err != 0u && lane == 0) report(p.err, static_cast<int32_t>(err));
 
-    const uint8_t* const kv_lane = static_cast<const uint8_t*>(p.kv) + t0 * 1024 + 16 * lane;
     const float* const csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
-    uint8_t* const ring_lane = smem + wib * (U * kSlotBytes) + 16 * lane;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const bool valid = __shfl_sync(kFull, off, u) >= 0;
@@ -672,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
                     L.c = *reinterpret_cast<const float4*>(src + 1024 - 16 * 24);
                     L.s = *reinterpret_cast<const float4*>(src + 1024 + 128 - 16 * 24);
                 }
-                encode_store<kRecord, kSanitize>(L, cache_a + o, cache_s + so, lane, 1.0f);
+                encode_store<kRecord, kSanitize>(L, cache_a + o, cache_s + so, lane, Scale{1.0f, 1.0f});
             }
         }
     }

@@ -178,3 +178,24 @@ def test_plain_cache_full_size_sampled(gkr, oracle_mod, record):
     written = np.zeros(case.num_pages * 64, bool)
     written[case.slots[valid]] = True
     assert (got.reshape(-1, record)[~written] == SENTINEL).all()
+
+
+@pytest.mark.parametrize("scale", [1e-30, 2.0 ** -64, float(np.nextafter(np.float32(2.0 ** -64), 0)),
+                                   2.0 ** 64, float(np.nextafter(np.float32(2.0 ** 64), np.inf)),
+                                   1e30, 7.0 / 3.0])
+def test_fp8_scales_across_the_quotient_paths(gkr, oracle_mod, scale):
+    """Scales inside [2^-64, 2^64] take the corrected-reciprocal quotient, scales outside
+    it the IEEE division: both must give the oracle's bytes.  kv is drawn around
+    50 * scale so the quotients land inside the e4m3 range (saturating tails included)."""
+    s32 = float(np.float32(scale))
+    case = _case(2000, 64, seed=21)
+    rng = np.random.default_rng(22)
+    case.kv = W.to_bf16_bits((rng.standard_t(3, (2000, 512)) * 50.0 * s32).astype(np.float32))
+    cache, got, ref, err, ref_err, ps = _insert(gkr, oracle_mod, case, 512, s32)
+    n, first = first_mismatch(got, ref)
+    assert n == 0 and err == ref_err == 0, first
+    idx = case.slots.astype(np.int32)
+    out = torch.empty(idx.size, 512, dtype=torch.bfloat16, device=DEV)
+    gkr.kv_gather(cache, torch.from_numpy(idx).to(DEV), out, fp8_scale=_scale_t(s32))
+    ref_out, _ = oracle_mod.gather(ref, 512, 64, case.num_pages, ps, idx, fp8_scale=s32)
+    assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), ref_out)
