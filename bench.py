@@ -627,15 +627,62 @@ def oracle_steps(case, tokens: int, steps: int):
     return (time.perf_counter() - t0) / steps
 
 
+def _oracle_chunk(job):
+    """Worker of the all-cores oracle timing: insert + gather of one disjoint token range
+    (its own copy of the cache), `steps` times.  Returns the seconds it took."""
+    kv, slots, pos, idx, csc, record, bs, pages, steps = job
+    import oracle
+    ps = oracle.page_stride(record, bs)
+    cache = np.zeros(pages * ps, np.uint8)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.insert(kv, cache, record, bs, pages, ps, slots, pos, csc)
+        oracle.gather(cache, record, bs, pages, ps, idx)
+    return time.perf_counter() - t0
+
+
+def _cpu_model() -> str:
+    try:
+        text = Path("/proc/cpuinfo").read_text()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "CPU part"):
+        for line in text.splitlines():
+            if line.startswith(key):
+                return f"{key}: {line.split(':', 1)[1].strip()}"
+    return "unknown"
+
+
 def cpu_baseline(case, seconds: float) -> dict:
+    """The oracle on the host: single-threaded (the line's value), and the same code run
+    on every core over disjoint token ranges (slots are unique, so the ranges write
+    disjoint records and each range gathers its own slots), in a spawn-started pool."""
+    import multiprocessing as mp
     per = oracle_steps(case, 1024, 1)                 # calibrate on 1024 tokens
     tok_s = 1024 / per
     tokens = int(min(case.num_tokens, max(1024, tok_s * seconds / 3)))
     steps = max(1, int(seconds / (tokens / tok_s)))
     sec = oracle_steps(case, tokens, steps)
-    return {"value": tokens / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{steps} x insert+gather of the first {tokens} of the 16384 tokens "
-                      f"(single-threaded C oracle, {os.cpu_count()} host cores present)"}
+    ncpu = os.cpu_count() or 1
+    out = {"value": tokens / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+           "sample": f"{steps} x insert+gather of the first {tokens} of the 16384 tokens "
+                     f"(single-threaded C oracle, {ncpu} host cores present)",
+           "cpu_model": _cpu_model()}
+    if ncpu > 1:
+        T = case.num_tokens
+        bounds = np.linspace(0, T, ncpu + 1).astype(int)
+        psteps = max(1, int(steps * ncpu * tokens / T))   # about the same total work
+        jobs = [(case.kv[a:b], case.slots[a:b], case.positions[a:b], case.indices[a:b],
+                 case.csc, case.record, case.block_size, case.num_pages, psteps)
+                for a, b in zip(bounds[:-1], bounds[1:])]
+        with mp.get_context("spawn").Pool(ncpu) as pool:
+            pool.map(_oracle_chunk, [j[:8] + (1,) for j in jobs])      # warm the workers
+            times = pool.map(_oracle_chunk, jobs)
+        out["all_cores"] = {"value": T * psteps / max(times), "unit": "tokens/s",
+                            "cores": ncpu,
+                            "sample": f"{psteps} x insert+gather of all {T} tokens, split "
+                                      f"into {ncpu} disjoint ranges, one process per core"}
+    return out
 
 
 def run_reference(args):
