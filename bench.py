@@ -64,7 +64,9 @@ def parse_args(argv=None):
                     help="CPU time budget of the oracle baseline sample")
     ap.add_argument("--profile", default=None, metavar="WORKLOAD",
                     help="run only this workload's kernel(s) a few times (for profiler "
-                         "captures) and print their CUDA-event times")
+                         "captures) and print their CUDA-event times; WORKLOAD is one of "
+                         "workloads.PROFILE_WORKLOADS, or fp8_<insert workload> for the same "
+                         "insert into an fp8 cache")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--insert-stream-min", type=int, default=None, metavar="TOKENS",
                     help="token count from which inserts use the streaming kernel "
@@ -726,11 +728,20 @@ def run_profile(args):
     gkr.build()
     if args.insert_stream_min is not None:
         gkr.set_insert_stream_min(args.insert_stream_min)
-    case = W.PROFILE_WORKLOADS[args.profile]()
-    s = device_sets(case, dev, 1)[0]
-    res = {"workload": args.profile}
-    ins = lambda: gkr.kv_insert(s["kv"], s["cache"], s["slots"], s["pos"], s["csc"],
-                                case.block_size, case.record)
+    name = args.profile
+    fp8 = name.startswith("fp8_")                     # the same case into an fp8 cache
+    case = W.PROFILE_WORKLOADS[name[4:] if fp8 else name]()
+    record = 512 if fp8 else case.record
+    s = device_sets(case, dev, 1, record=record)[0]
+    res = {"workload": name}
+    scale = torch.tensor([0.01], dtype=torch.float32, device=dev) if fp8 else None
+    R = case.meta.get("compress_ratio")
+    if R:                                             # compressed insert, with sanitising
+        ins = lambda: gkr.rope_quant_insert(s["kv"], s["cache"], s["slots"], s["pos"], s["csc"],
+                                            case.block_size, R, True, record)
+    else:
+        ins = lambda: gkr.kv_insert(s["kv"], s["cache"], s["slots"], s["pos"], s["csc"],
+                                    case.block_size, record, fp8_scale=scale)
     if args.profile.startswith("gather"):
         ins()                                       # fill the cache once
         fns = {"gather": lambda: gkr.kv_gather(s["cache"], s["idx"], s["out"])}

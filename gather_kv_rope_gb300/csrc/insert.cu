@@ -590,8 +590,12 @@ template <int kRecord, int U>
 cudaError_t launch_staged(const InsertParams& p, cudaStream_t stream) {
     const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * U;
     const int64_t blocks = (p.num_tokens + per_block - 1) / per_block;
-    return launch_kernel(insert_staged_kernel<kRecord, U>, blocks, kThreads,
-                         static_cast<size_t>(kWarpsPerBlock) * U * kSlotBytes, stream, p);
+    const size_t smem = static_cast<size_t>(kWarpsPerBlock) * U * kSlotBytes;
+    int64_t wave = 0;  // also raises the kernel's dynamic shared-memory limit above 48 KiB
+    cudaError_t e = resident_warps(reinterpret_cast<const void*>(insert_staged_kernel<kRecord, U>),
+                                   kThreads, smem, &wave);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(insert_staged_kernel<kRecord, U>, blocks, kThreads, smem, stream, p);
 }
 
 template <int kRecord>
@@ -716,11 +720,12 @@ cudaError_t launch_compressed(const InsertParams& p, bool sanitize, cudaStream_t
     const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * chunk;
     const int64_t blocks = (p.num_tokens + per_block - 1) / per_block;
     const size_t smem = static_cast<size_t>(kWarpsPerBlock) * kSparseBatch * kSlotBytes;
-    if (sanitize)
-        return launch_kernel(insert_sparse_staged_kernel<kRecord, true>, blocks, kThreads, smem,
-                             stream, p, chunk);
-    return launch_kernel(insert_sparse_staged_kernel<kRecord, false>, blocks, kThreads, smem,
-                         stream, p, chunk);
+    auto kernel = sanitize ? insert_sparse_staged_kernel<kRecord, true>
+                           : insert_sparse_staged_kernel<kRecord, false>;
+    int64_t wave = 0;  // also raises the kernel's dynamic shared-memory limit above 48 KiB
+    cudaError_t e = resident_warps(reinterpret_cast<const void*>(kernel), kThreads, smem, &wave);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kernel, blocks, kThreads, smem, stream, p, chunk);
 #else
     const int32_t chunk = static_cast<int32_t>(p.ratio >= 16 ? 32 : 2 * p.ratio);
     const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * chunk;

@@ -248,4 +248,5 @@ PROFILE_WORKLOADS = {
     "insert_v4_65536": insert_v4_65536,
     "gather_v41_sparse_262144": gather_v41_sparse_262144,
     "roundtrip_v41_16384": roundtrip_v41_16384,
+    "compressed_v41_r4_262144": compressed_v41_r4_262144,
 }
