@@ -252,9 +252,9 @@ def _supports_external_events(torch) -> bool:
         return False
 
 
-def device_sets(case, device, n_sets: int, record: int | None = None):
+def device_sets(case, device, n_sets: int, record: int | None = None, clone_kv: bool = True):
     """n_sets copies of the case's inputs on the device, each with its own cache (of
-    the case's record, or of `record`) and gather output."""
+    the case's record, or of `record`) and gather output (kv shared when not clone_kv)."""
     import torch
     import gather_kv_rope_gb300 as gkr
     record = case.record if record is None else record
@@ -266,7 +266,7 @@ def device_sets(case, device, n_sets: int, record: int | None = None):
     sets = []
     for _ in range(n_sets):
         sets.append(dict(
-            kv=kv.clone(), slots=slots.clone(), pos=pos.clone(), csc=csc,
+            kv=kv.clone() if clone_kv else kv, slots=slots.clone(), pos=pos.clone(), csc=csc,
             idx=None if idx is None else idx.clone(),
             cache=gkr.alloc_cache(case.num_pages, case.block_size, record, device, fill=0),
             out=None if idx is None else torch.empty(case.indices.shape + (512,),
@@ -513,29 +513,22 @@ def time_e2e(args, device, case):
 
 
 def sweep(device, peak):
-    """Kernel-only timings of the larger workloads (each larger than L2, or rotated
-    over several input sets): launches captured back to back in a CUDA graph, the
-    graph replayed after warm-up, time per launch = CUDA-event time / launches.  No
-    host-side launch overhead is inside the measurement."""
+    """Kernel-only timings of the larger workloads: launches captured back to back in a
+    CUDA graph, the graph replayed after warm-up, time per launch = CUDA-event time /
+    launches; no host-side launch overhead is inside the measurement.  Each launch
+    touches more than L2, or the launches rotate over input sets that together do."""
     import torch
     import gather_kv_rope_gb300 as gkr
     import workloads as W
     res = {}
 
-    def timed(fn, sets, per_graph=12, replays=5):
-        for k in range(3):
-            fn(sets[k % len(sets)])
-        torch.cuda.synchronize(device)
-        side = torch.cuda.Stream(device)
-        side.wait_stream(torch.cuda.current_stream(device))
-        with torch.cuda.stream(side):
-            fn(sets[0])
-        torch.cuda.current_stream(device).wait_stream(side)
-        torch.cuda.synchronize(device)
+    flush_buf = torch.ones(64 << 20, dtype=torch.int32, device=device)   # 256 MiB, 2x the L2
+
+    def graph_ms(body, per_graph, replays):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for k in range(per_graph):
-                fn(sets[k % len(sets)])
+                body(k)
         g.replay()
         torch.cuda.synchronize(device)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -545,6 +538,31 @@ def sweep(device, peak):
         b.record()
         torch.cuda.synchronize(device)
         return a.elapsed_time(b) / (per_graph * replays)
+
+    def timed(fn, sets, per_graph=12, replays=5, flush=False):
+        """ms per launch of fn, back to back in a CUDA graph.  With flush, every launch
+        follows a read of a 256 MiB buffer (a max-reduction) that leaves L2 holding only
+        clean lines of that buffer (for workloads that touch less than L2 per launch),
+        and the same graph of reads alone is timed and subtracted."""
+        for k in range(3):
+            fn(sets[k % len(sets)])
+        torch.cuda.synchronize(device)
+        side = torch.cuda.Stream(device)
+        side.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(side):
+            fn(sets[0])
+            flush_buf.max()
+        torch.cuda.current_stream(device).wait_stream(side)
+        torch.cuda.synchronize(device)
+        if not flush:
+            return graph_ms(lambda k: fn(sets[k % len(sets)]), per_graph, replays)
+
+        def both(k):
+            flush_buf.max()
+            fn(sets[k % len(sets)])
+        t_both = graph_ms(both, per_graph, replays)
+        t_flush = graph_ms(lambda k: flush_buf.max(), per_graph, replays)
+        return t_both - t_flush
 
     for name, n_sets in (("insert_v4_65536", 3), ("insert_v41_262144", 1)):
         case = getattr(W, name)()
@@ -558,19 +576,46 @@ def sweep(device, peak):
         del sets
         torch.cuda.empty_cache()
 
+    # the token counts the pages time on GB300 (16384 .. 65536; 262144 is above): V4.1
+    # inserts with random slots and positions, rotating over sets that exceed L2 together
+    for T in (16384, 32768, 65536):
+        case = W.random_insert(f"insert_v41_{T}", T, 528, 64, 2 * T // 64, 8192, 0.05, seed=1)
+        b = insert_bytes(case.slots, 528)
+        sets = device_sets(case, device, int(max(1, -(-320_000_000 // b))))
+        ms = timed(lambda s: gkr.kv_insert(s["kv"], s["cache"], s["slots"], s["pos"], s["csc"],
+                                           64, 528), sets)
+        res[f"insert_v41_{T}"] = {"kernel": "insert", "launch": gkr.insert_kernel_for(T),
+                                  "us": ms * 1e3, "tokens_per_s": T / (ms * 1e-3), "alg_bytes": b,
+                                  "alg_gbs": b / (ms * 1e-3) / 1e9,
+                                  "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+                                  "l2": f"{len(sets)} rotating input sets"}
+        del sets
+        torch.cuda.empty_cache()
+
     for name in ("compressed_v41_r4_262144", "compressed_v41_r128_262144"):
         case = W.WORKLOADS[name]()
         R = case.meta["compress_ratio"]
-        sets = device_sets(case, device, 1)
+        b = compressed_insert_bytes(case.slots, case.positions, R, case.record)
+        # a launch touches only the rows of the group-boundary tokens (less than L2): the
+        # sets read kv through windows of one buffer shifted by k rows (k < R, so each set
+        # reads other rows), with their own slots, positions and cache, until the sets
+        # together touch more than 320 MB
+        n_sets = int(min(R, max(1, -(-320_000_000 // b))))
+        T = case.num_tokens
+        kv_big = torch.from_numpy(
+            np.concatenate([case.kv, case.kv[:n_sets]]).view(np.int16)).view(torch.bfloat16).to(device)
+        sets = device_sets(case, device, n_sets, clone_kv=False)
+        for k, st in enumerate(sets):
+            st["kv"] = kv_big[k:k + T]
         ms = timed(lambda s: gkr.rope_quant_insert(s["kv"], s["cache"], s["slots"], s["pos"],
                                                    s["csc"], case.block_size, R, True,
                                                    case.record), sets)
-        b = compressed_insert_bytes(case.slots, case.positions, R, case.record)
-        res[name] = {"kernel": "insert_sparse", "compress_ratio": R, "sanitize_nans": True,
+        res[name] = {"kernel": "insert_sparse_staged", "compress_ratio": R, "sanitize_nans": True,
+                     "l2": f"{n_sets} rotating input sets touching {n_sets * b / 1e6:.0f} MB",
                      "us": ms * 1e3, "tokens_per_s": case.num_tokens / (ms * 1e-3),
                      "alg_bytes": b, "alg_gbs": b / (ms * 1e-3) / 1e9,
                      "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
-        del sets
+        del sets, kv_big
         torch.cuda.empty_cache()
 
     # the plain KV-only caches: the 262144-token insert into bf16 rows and fp8 rows

@@ -636,7 +636,10 @@ cudaError_t launch(const InsertParams& p, cudaStream_t stream) {
 #ifndef GKR_SPARSE_MIN_BLOCKS
 #define GKR_SPARSE_MIN_BLOCKS 5
 #endif
-constexpr int kSparseBatch = 3;  // tokens staged at once by the staged compressed insert
+#ifndef GKR_SPARSE_BATCH
+#define GKR_SPARSE_BATCH 3
+#endif
+constexpr int kSparseBatch = GKR_SPARSE_BATCH;  // tokens staged at once by the compressed insert
 
 // The compressed insert with shared-memory staging: as insert_sparse_kernel, but the
 // tokens to write are taken up to three at a time, their kv and cos/sin rows copied into
@@ -716,7 +719,8 @@ cudaError_t launch_compressed(const InsertParams& p, bool sanitize, cudaStream_t
     if (p.num_tokens <= 0) return cudaSuccess;
     if (p.ratio == 1 && !sanitize) return launch<kRecord>(p, stream);
 #if GKR_SPARSE_STAGED
-    const int32_t chunk = static_cast<int32_t>(p.ratio >= 10 ? 32 : kSparseBatch * p.ratio);
+    const int32_t chunk = static_cast<int32_t>(
+        p.ratio * kSparseBatch >= 32 ? 32 : kSparseBatch * p.ratio);
     const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * chunk;
     const int64_t blocks = (p.num_tokens + per_block - 1) / per_block;
     const size_t smem = static_cast<size_t>(kWarpsPerBlock) * kSparseBatch * kSlotBytes;
