@@ -589,6 +589,17 @@ def sweep(device, peak):
                                   "alg_gbs": b / (ms * 1e-3) / 1e9,
                                   "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
                                   "l2": f"{len(sets)} rotating input sets"}
+        if T == 65536:   # the round trip's gather at this size: the slots just written
+            for st in sets:
+                st["idx"] = st["slots"].to(torch.int32)
+                st["out"] = torch.empty(T, 512, dtype=torch.bfloat16, device=device)
+            ms = timed(lambda s: gkr.kv_gather(s["cache"], s["idx"], s["out"]), sets)
+            b = gather_bytes(case.slots.astype(np.int32), 528)
+            res[f"gather_v41_{T}"] = {"kernel": "gather", "us": ms * 1e3,
+                                      "indices_per_s": T / (ms * 1e-3), "alg_bytes": b,
+                                      "alg_gbs": b / (ms * 1e-3) / 1e9,
+                                      "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+                                      "l2": f"{len(sets)} rotating input sets"}
         del sets
         torch.cuda.empty_cache()
 

@@ -25,8 +25,10 @@
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers on the current CUDA device;
- *     the caller owns and allocates all memory.  The library allocates
- *     nothing, never synchronises the stream and keeps no per-call state.
+ *     the caller owns and allocates all memory.  The library allocates no
+ *     device memory and never synchronises the stream; the only state it keeps
+ *     is the process-wide launch policy (gkr_set_*) and a per-device cache of
+ *     occupancy queries.  Calls may be captured into CUDA graphs.
  *   - Work is enqueued on `stream` (0 = the legacy default stream); results
  *     are visible after the stream's work completes.
  *   - Host-side argument checks run before anything is enqueued; on failure
