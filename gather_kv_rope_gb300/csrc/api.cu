@@ -166,10 +166,11 @@ gkr_status prepare_insert(const void* kv, int64_t num_tokens, void* k_cache,
     p->num_tokens = num_tokens;
     if (num_tokens == 0) return GKR_OK;
     if (!kv || !k_cache || !slot_mapping || !positions || !cos_sin_cache) return GKR_EINVAL;
-    if (cache->record == 512 && !fp8_scale) return GKR_EINVAL;
+    const bool fp8 = cache->record == 512;  // fp8_scale is read for fp8 rows only
+    if (fp8 && !fp8_scale) return GKR_EINVAL;
     if (!aligned(kv, 16) || !aligned(k_cache, 16) || !aligned(cos_sin_cache, 16) ||
         !aligned(slot_mapping, 8) || !aligned(positions, 8) || !aligned(err_flag, 4) ||
-        !aligned(fp8_scale, 4))
+        (fp8 && !aligned(fp8_scale, 4)))
         return GKR_EALIGN;
     p->kv = kv;
     p->cache = static_cast<uint8_t*>(k_cache);
@@ -250,9 +251,10 @@ GKR_API gkr_status gkr_kv_gather(const void* k_cache, const gkr_cache_desc* cach
     if (num_indices < 0) return GKR_EINVAL;
     if (num_indices == 0) return GKR_OK;
     if (!k_cache || !indices || !out) return GKR_EINVAL;
-    if (cache->record == 512 && !fp8_scale) return GKR_EINVAL;
+    const bool fp8 = cache->record == 512;  // fp8_scale is read for fp8 rows only
+    if (fp8 && !fp8_scale) return GKR_EINVAL;
     if (!aligned(k_cache, 16) || !aligned(out, 16) || !aligned(indices, 4) ||
-        !aligned(err_flag, 4) || !aligned(fp8_scale, 4))
+        !aligned(err_flag, 4) || (fp8 && !aligned(fp8_scale, 4)))
         return GKR_EALIGN;
 
     gkr::GatherParams p;
