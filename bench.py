@@ -403,7 +403,7 @@ def _gpu_id(torch, device) -> str:
         return str(device.index or 0)
 
 
-def time_e2e(args, device, case):
+def time_e2e(args, device, case, dist=None):
     """Same metric through the public API from pinned host buffers: every step
     copies kv / slots / positions / indices to the device, inserts, gathers and
     copies the gathered rows back, all inside the timed region.
@@ -486,6 +486,7 @@ def time_e2e(args, device, case):
         for i in range(5):
             step(i)
         torch.cuda.synchronize(device)
+        barrier(dist)                      # every rank's copies share the host link
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(cur)
         for s in (s_up, s_run, s_down):
@@ -496,8 +497,9 @@ def time_e2e(args, device, case):
             cur.wait_stream(s)
         e1.record(cur)
         torch.cuda.synchronize(device)
-        return e0.elapsed_time(e1) / n
+        return reduce_max(e0.elapsed_time(e1) / n, dist)
 
+    world = 1 if dist is None else dist.get_world_size()
     ms_serial = timed(serial, args.e2e_steps)
     ms = timed(piped, args.e2e_steps)
     # every step inserts and gathers the same inputs: each downloaded buffer must hold
@@ -505,9 +507,11 @@ def time_e2e(args, device, case):
     ref = out[0].cpu()
     if not all(torch.equal(h.view(torch.int16), ref.view(torch.int16)) for h in out_h):
         raise RuntimeError("pipelined end-to-end steps returned different results")
-    return {"value": case.num_tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
-            "steps": args.e2e_steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "serial": {"value": case.num_tokens / (ms_serial * 1e-3), "ms_per_step": ms_serial},
+    return {"value": world * case.num_tokens / (ms * 1e-3), "unit": "tokens/s",
+            "ms_per_step": ms, "steps": args.e2e_steps, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "serial": {"value": world * case.num_tokens / (ms_serial * 1e-3),
+                       "ms_per_step": ms_serial},
             "path": "one pinned host -> device copy of the step's inputs, kv_insert, kv_gather, "
                     f"device -> pinned host copy of the rows; three streams, {NB} buffer sets"}
 
@@ -875,13 +879,13 @@ def main(argv=None):
                       "num_pages": 512, "gathered": int(case.indices.size),
                       "l2": f"inputs larger than L2: {ROTATE} rotating input sets",
                       "launch": f"CUDA graph of {GRAPH_STEPS} steps, replayed {K // GRAPH_STEPS}x"},
-           "roofline": roofline, "kernels": kern, "gpu_launches": 2 * K,
-           "clocks": r["clocks"]}
+           "roofline": roofline, "kernels": kern, "gpu_launches": 2 * K * world,
+           "gpu_launches_per_rank": 2 * K, "clocks": r["clocks"]}
+    out["e2e"] = time_e2e(args, device, case, dist)            # every rank, max over ranks
     if rank == 0:
-        out["e2e"] = time_e2e(args, device, case)
         if not args.no_sweep and world == 1:
             out["sweep"] = sweep(device, peak)
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and world == 1:
             out["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
         print(json.dumps(out), flush=True)
     if dist is not None:
