@@ -857,9 +857,13 @@ def main(argv=None):
     ib, gb = insert_bytes(case.slots, 528), gather_bytes(case.indices, 528)
     kern = {"insert": {"us": r["ins_ms"] * 1e3, "alg_bytes": ib,
                        "gbs": ib / (r["ins_ms"] * 1e-3) / 1e9,
+                       "frac_of_peak": ib / (r["ins_ms"] * 1e-3) / 1e9 / peak,
+                       "traffic": ncu_traffic(gkr.insert_kernel_for(T), WORKLOAD),
                        "isolated_us": r["ins_iso_ms"] * 1e3},
             "gather": {"us": r["gat_ms"] * 1e3, "alg_bytes": gb,
                        "gbs": gb / (r["gat_ms"] * 1e-3) / 1e9,
+                       "frac_of_peak": gb / (r["gat_ms"] * 1e-3) / 1e9 / peak,
+                       "traffic": ncu_traffic("gather_kernel", WORKLOAD),
                        "isolated_us": r["gat_iso_ms"] * 1e3},
             "isolated_timing": r["iso_timing"]}
     dom = "insert" if r["ins_ms"] >= r["gat_ms"] else "gather"
