@@ -200,17 +200,10 @@ __device__ __forceinline__ void patch_nan(uint32_t nanmask, uint32_t& o01, uint3
 }
 
 // General path of dequant8: any scale byte (two multiplies above 134, NaN for 255)
-// and NaN codes.  Kept out of line: the common path handles bytes <= 134 without
-// NaN codes with one multiply per pair and a single test.
-#ifndef GKR_GENERAL_INLINE
-#define GKR_GENERAL_INLINE 1
-#endif
-#if GKR_GENERAL_INLINE
-__device__ __forceinline__
-#else
-__device__ __noinline__
-#endif
-uint4 dequant8_general(uint2 c, uint32_t byte) {
+// and NaN codes.  Inlined behind a branch marked unlikely: the common path handles bytes
+// <= 134 without NaN codes with one multiply per pair and a single test (an out-of-line
+// version made the gather spill).
+__device__ __forceinline__ uint4 dequant8_general(uint2 c, uint32_t byte) {
     const uint32_t n = kBf16NaN | (kBf16NaN << 16);
     if (byte == 255u) return make_uint4(n, n, n, n);
     const Dequant d = make_dequant(byte);

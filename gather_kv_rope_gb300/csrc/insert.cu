@@ -35,9 +35,6 @@ namespace {
 #define GKR_INSERT_MAX_CHUNK 16  // tokens per streaming warp at most (0 = one wave)
 #endif
 
-#ifndef GKR_INSERT_CYCLIC
-#define GKR_INSERT_CYCLIC 0
-#endif
 constexpr int kInsertDepth = GKR_INSERT_DEPTH;  // tokens in flight per warp
 constexpr int kSlotBytes = 1024 + 256;          // staged kv row + cos/sin row
 
@@ -565,8 +562,7 @@ cudaError_t launch(const InsertParams& p, cudaStream_t stream) {
     int64_t wave = 0;
     cudaError_t e = resident_warps(reinterpret_cast<const void*>(kernel), kThreads, smem, &wave);
     if (e != cudaSuccess) return e;
-    const WorkMap m = make_work_map(p.num_tokens, wave, GKR_INSERT_CYCLIC != 0, 1,
-                                    GKR_INSERT_MAX_CHUNK);
+    const WorkMap m = make_work_map(p.num_tokens, wave, false, 1, GKR_INSERT_MAX_CHUNK);
     const int64_t blocks = (m.warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     return launch_kernel(kernel, blocks, kThreads, smem, stream, p, m);
 }

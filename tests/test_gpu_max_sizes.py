@@ -18,10 +18,12 @@ STRIDE = (1 << 31) - 512          # a multiple of 512, above every record's page
 
 @pytest.mark.parametrize("record", [528, 1024])
 def test_page_stride_near_two_gigabytes(gkr, oracle_mod, record):
-    bs, P, T = 32, 3, 96
+    bs, P, T = 32, 3, 80
     case = W.random_insert("max", T, 528, bs, P, 256, 0.0, seed=record)
-    case.slots[:] = np.random.default_rng(1).permutation(P * bs)[:T]
-    case.slots[0] = P * bs - 1                                   # last row of the last page
+    last = P * bs - 1                                            # last row of the last page
+    perm = np.random.default_rng(1).permutation(P * bs)
+    case.slots[:] = np.concatenate([[last], perm[perm != last]])[:T]   # distinct slots
+    assert len(np.unique(case.slots)) == T
     kv, slots, pos, csc = device_inputs(case, DEV)
     cache = gkr.alloc_cache(P, bs, record, DEV, page_stride_bytes=STRIDE, fill=SENTINEL)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
