@@ -39,7 +39,16 @@ def gpu_insert(gkr, case, device, page_stride: int, fill: int = SENTINEL, err=No
     return cache, kv
 
 
+def assert_distinct_slots(slots: np.ndarray) -> None:
+    """Valid slots must be distinct: two tokens writing one row race (outside the
+    contract), so a test built that way would compare an arbitrary winner."""
+    v = np.asarray(slots)
+    v = v[(v >= 0)]
+    assert len(np.unique(v)) == v.size, "test input writes one slot twice"
+
+
 def oracle_insert(oracle_mod, case, page_stride: int, fill: int = SENTINEL):
+    assert_distinct_slots(case.slots)
     cache = np.full(case.num_pages * page_stride, fill, np.uint8)
     err = oracle_mod.insert(case.kv, cache, case.record, case.block_size, case.num_pages,
                             page_stride, case.slots, case.positions, case.csc)

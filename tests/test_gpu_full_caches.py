@@ -9,7 +9,7 @@ import torch
 
 import workloads as W
 from golden_parse import GOLDEN, load_worked, worked_inputs
-from helpers import SENTINEL, bf16_from_bits, device_inputs, first_mismatch
+from helpers import SENTINEL, assert_distinct_slots, bf16_from_bits, device_inputs, first_mismatch
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -35,6 +35,7 @@ def _scale_t(scale):
 
 def _insert(gkr, oracle_mod, case, record, scale=None, pad_units=0):
     """GPU and oracle insert of `case` into a `record` cache; returns (got, ref, errs)."""
+    assert_distinct_slots(case.slots)
     ps = oracle_mod.page_stride(record, case.block_size) + 512 * pad_units
     kv, slots, pos, csc = device_inputs(case, DEV)
     cache = gkr.alloc_cache(case.num_pages, case.block_size, record, DEV, page_stride_bytes=ps,

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import workloads as W
-from helpers import SENTINEL, device_inputs, first_mismatch
+from helpers import SENTINEL, assert_distinct_slots, device_inputs, first_mismatch
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -47,6 +47,7 @@ def test_random_configuration_matches_oracle(gkr, oracle_mod, seed):
         case = W.random_insert(f"fuzz{seed}", c["T"], 528, c["bs"], c["pages"], c["max_pos"],
                                c["skip"], seed=seed, dist=c["dist"], outlier_rate=c["outliers"])
         record, bs, P = c["record"], c["bs"], c["pages"]
+        assert_distinct_slots(case.slots)
         align = 576 if record == 584 else 512
         ps = oracle_mod.page_stride(record, bs) + c["pad"] * align
         kv, slots, pos, csc = device_inputs(case, DEV)

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import workloads as W
-from helpers import SENTINEL, device_inputs
+from helpers import SENTINEL, assert_distinct_slots, device_inputs
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 DEV = torch.device("cuda:0")
@@ -23,7 +23,7 @@ def test_page_stride_near_two_gigabytes(gkr, oracle_mod, record):
     last = P * bs - 1                                            # last row of the last page
     perm = np.random.default_rng(1).permutation(P * bs)
     case.slots[:] = np.concatenate([[last], perm[perm != last]])[:T]   # distinct slots
-    assert len(np.unique(case.slots)) == T
+    assert_distinct_slots(case.slots)
     kv, slots, pos, csc = device_inputs(case, DEV)
     cache = gkr.alloc_cache(P, bs, record, DEV, page_stride_bytes=STRIDE, fill=SENTINEL)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
