@@ -288,6 +288,6 @@ GKR_API const char* gkr_status_string(gkr_status status) {
 
 GKR_API int32_t gkr_last_cuda_error(void) { return g_last_cuda_error; }
 
-GKR_API int32_t gkr_version(void) { return 10000; }
+GKR_API int32_t gkr_version(void) { return 20000; }
 
 }  // extern "C"

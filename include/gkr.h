@@ -239,7 +239,9 @@ GKR_API const char *gkr_status_string(gkr_status status);
 /* The cudaError_t of the last GKR_ECUDA returned on this host thread (0 if none). */
 GKR_API int32_t gkr_last_cuda_error(void);
 
-/* ABI version: major * 10000 + minor * 100 + patch. */
+/* ABI version: major * 10000 + minor * 100 + patch.  2.0.0: gkr_kv_insert and
+ * gkr_kv_gather take fp8_scale (the plain fp8 / bf16 caches); gkr_rope_quant_insert and
+ * gkr_set_insert_staged_min / gkr_get_insert_staged_min were added. */
 GKR_API int32_t gkr_version(void);
 
 #ifdef __cplusplus

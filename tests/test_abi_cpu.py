@@ -58,7 +58,7 @@ def test_page_stride_and_rows(gkr):
     assert gkr.page_stride(1024, 0) == -1
     with pytest.raises(ValueError):
         gkr.record_rows(500)
-    assert gkr.lib().gkr_version() == 10000
+    assert gkr.lib().gkr_version() == 20000
     assert gkr.get_insert_stream_min() == 131072
     assert gkr.get_insert_staged_min() == 24576
     assert gkr.insert_kernel_for(16384) == "insert_short_kernel"
