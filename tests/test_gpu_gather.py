@@ -216,3 +216,48 @@ def test_insert_then_gather_same_stream(gkr, oracle_mod, record, pdl):
             _assert_bits_equal(bits_of(out), r)
     finally:
         gkr.set_pdl(True)
+
+
+@pytest.mark.parametrize("record", [528, 584, 512, 1024])
+def test_gather_cuda_graph_replay(gkr, oracle_mod, record):
+    """Capture one gather in a CUDA graph, then replay it over three rounds of new
+    indices copied into the captured buffer (the last round all -1); for the fp8 cache a
+    new scale is also written between replays (it is read on the device)."""
+    bs, P, N = 64, 40, 1500
+    case = W.random_insert("ggraph", 2000, 528, bs, P, 512, 0.0, seed=record)
+    ps = oracle_mod.page_stride(record, bs)
+    scale0 = 0.05
+    sc = torch.tensor([scale0], dtype=torch.float32, device=DEV) if record == 512 else None
+    cache = gkr.alloc_cache(P, bs, record, DEV, fill=SENTINEL)
+    kv, slots, pos, csc = (torch.from_numpy(case.kv.view(np.int16)).view(torch.bfloat16).to(DEV),
+                           torch.from_numpy(case.slots).to(DEV),
+                           torch.from_numpy(case.positions).to(DEV),
+                           torch.from_numpy(case.csc).to(DEV))
+    gkr.kv_insert(kv, cache, slots, pos, csc, bs, record, fp8_scale=sc)
+    ref = np.full(P * ps, SENTINEL, np.uint8)
+    oracle_mod.insert(case.kv, ref, record, bs, P, ps, case.slots, case.positions, case.csc,
+                      fp8_scale=scale0 if record == 512 else None)
+    idx = torch.full((N,), -1, dtype=torch.int32, device=DEV)
+    out = torch.empty(N, 512, dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        gkr.kv_gather(cache, idx, out, fp8_scale=sc)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        gkr.kv_gather(cache, idx, out, fp8_scale=sc)
+    rng = np.random.default_rng(record)
+    for r, scale in enumerate([scale0, 0.5, 2.0]):
+        ind = rng.integers(-1, P * bs, N).astype(np.int32)
+        if r == 2:
+            ind[:] = -1
+        idx.copy_(torch.from_numpy(ind))
+        if sc is not None:
+            sc.fill_(scale)
+        g.replay()
+        torch.cuda.synchronize()
+        want, _ = oracle_mod.gather(ref, record, bs, P, ps, ind,
+                                    fp8_scale=scale if record == 512 else None)
+        got = out.cpu().view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, want), (record, r)
