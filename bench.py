@@ -7,19 +7,25 @@ come back as zeros) into bf16 [16384, 512].  Metric: tokens per second.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints ONE JSON line on rank 0.  Timing: W eager warm-up steps, then K steps run
-as replays of a captured CUDA graph of G steps, bracketed by a barrier and a
-device synchronise on both sides, timed with CUDA events on the launching stream
-(max over ranks).  Six input sets (~300 MB together, more than the 126 MB L2)
-rotate so no step finds its inputs in L2.  Per-kernel durations come from a
-second graph of the same steps with event nodes around every kernel (replayed
-after the timed region), or from an eager pass when torch cannot capture
-timing events.
+Prints ONE JSON line on rank 0:
+  value      K steps run as replays of a captured CUDA graph of G steps, bracketed by a
+             barrier and a device synchronise on both sides, timed with CUDA events on
+             the launching stream (max over ranks); six input sets (~300 MB together,
+             more than the 126 MB L2) rotate so no step finds its inputs in L2;
+  roofline   the dominant kernel's algorithmic bytes over its mean launch time, timed as
+             back-to-back launches of that kernel alone in a graph over the same sets,
+             against the measured HBM copy bandwidth; DRAM traffic from the recorded ncu
+             capture while the kernel sources are unchanged;
+  e2e        the same step through the public API from pinned host memory, uploads,
+             kernels and downloads pipelined on three streams (serial figure beside it);
+  sweep      kernel-only times of the larger workloads (N = 1);
+  cpu_baseline  the CPU oracle on one core and on every core (N = 1);
+  clocks     nvidia-smi samples during the timed region.
 
-`--impl reference` times the CPU oracle (test infrastructure) on the same
-workload, a bounded sample of tokens per step, on the host cores.
-Under torchrun with N > 1 every rank runs its own replica (no collective on
-the data path; weak scaling).
+`--impl reference` times the CPU oracle (test infrastructure) on the same workload on
+every host core, each run held to a few minutes.  `--profile WORKLOAD` runs one
+workload's kernels a few times for profiler captures.  Under torchrun with N > 1 every
+rank runs its own replica (no collective on the data path; weak scaling).
 """
 from __future__ import annotations
 
