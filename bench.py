@@ -660,7 +660,8 @@ def sweep(device, peak):
     idx = torch.from_numpy(case.indices).to(device)
     outs = [torch.empty(case.indices.shape + (512,), dtype=torch.bfloat16, device=device)
             for _ in range(2)]
-    for record, name in ((528, "gather_v41_sparse"), (512, "gather_fp8_sparse")):
+    for record, name in ((528, "gather_v41_sparse"), (584, "gather_v4_sparse"),
+                         (512, "gather_fp8_sparse"), (1024, "gather_bf16_sparse")):
         sc = scale if record == 512 else None
         cache = gkr.alloc_cache(case.num_pages, 64, record, device, fill=0)
         gkr.kv_insert(kv, cache, torch.from_numpy(case.slots).to(device),
