@@ -236,6 +236,14 @@ def compressed_insert_bytes(slots: np.ndarray, positions: np.ndarray, ratio: int
     return 16 * slots.size + written * (1024 + record)
 
 
+def csc_bytes(slots: np.ndarray, positions: np.ndarray, ratio: int = 1) -> int:
+    """The cos/sin rows an insert reads, reported beside (not inside) the algorithmic
+    bytes: 256 B per distinct row among the tokens it writes (the row of position pos,
+    or of the group start pos + 1 - ratio in the compressed insert)."""
+    w = (slots >= 0) & ((positions + 1) % ratio == 0)
+    return 256 * int(np.unique(positions[w] + 1 - ratio).size)
+
+
 def gather_bytes(indices: np.ndarray, record: int) -> int:
     """Algorithmic bytes of one gather: 4 B index + 1024 B bf16 row written per
     index, plus the record read for every valid index."""
@@ -294,6 +302,31 @@ def step(gkr, case, s, ev=None):
             ev[2].record()
 
 
+def capture_steps(torch, device, body, n: int):
+    """body(0) once on a side stream (lazy set-up stays out of the capture), then
+    body(0) .. body(n-1) captured into one CUDA graph, replayed once untimed."""
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        body(0)
+    torch.cuda.current_stream(device).wait_stream(side)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for k in range(n):
+            body(k)
+    g.replay()
+    torch.cuda.synchronize(device)
+    return g
+
+
+def roundtrip_graph(torch, gkr, case, sets, device, events=None):
+    """The timed launch configuration: GRAPH_STEPS steps over the rotating input sets in
+    one CUDA graph (with event nodes around every kernel when `events` is given)."""
+    return capture_steps(torch, device, lambda k: step(
+        gkr, case, sets[k % len(sets)], None if events is None else events[k]), GRAPH_STEPS)
+
+
 def time_roundtrip(args, device, dist):
     import torch
     import gather_kv_rope_gb300 as gkr
@@ -309,26 +342,12 @@ def time_roundtrip(args, device, dist):
     G = GRAPH_STEPS
     K = max(G, (args.steps + G - 1) // G * G)       # K is rounded up to whole graphs
     replays = K // G
-    cap = torch.cuda.Stream(device)
-    cap.wait_stream(torch.cuda.current_stream(device))
-    with torch.cuda.stream(cap):
-        step(gkr, case, sets[0])                    # side-stream warm-up before capture
-    torch.cuda.current_stream(device).wait_stream(cap)
-    torch.cuda.synchronize(device)
-    graph = torch.cuda.CUDAGraph()                  # the timed graph: kernels only
-    with torch.cuda.graph(graph):
-        for k in range(G):
-            step(gkr, case, sets[k % ROTATE])
+    graph = roundtrip_graph(torch, gkr, case, sets, device)     # the timed graph
     external = _supports_external_events(torch)
     kev = None
     if external:                                    # same steps with event nodes per kernel
         kev = [[_timing_event(torch, True) for _ in range(3)] for _ in range(G)]
-        graph_ev = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph_ev):
-            for k in range(G):
-                step(gkr, case, sets[k % ROTATE], kev[k])
-    graph.replay()                                   # one untimed replay
-    torch.cuda.synchronize(device)
+        graph_ev = roundtrip_graph(torch, gkr, case, sets, device, kev)
 
     sampler = ClockSampler(_gpu_id(torch, device)).start()
     stream = torch.cuda.current_stream(device)
@@ -371,12 +390,7 @@ def time_roundtrip(args, device, dist):
                                                           s["pos"], s["csc"], case.block_size,
                                                           case.record)),
                      ("gather", lambda s: gkr.kv_gather(s["cache"], s["idx"], s["out"]))):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for k in range(G):
-                fn(sets[k % ROTATE])
-        g.replay()
-        torch.cuda.synchronize(device)
+        g = capture_steps(torch, device, lambda k: fn(sets[k % ROTATE]), G)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(5):
@@ -532,15 +546,8 @@ def sweep(device, peak):
     import workloads as W
     res = {}
 
-    flush_buf = torch.ones(64 << 20, dtype=torch.int32, device=device)   # 256 MiB, 2x the L2
-
     def graph_ms(body, per_graph, replays):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for k in range(per_graph):
-                body(k)
-        g.replay()
-        torch.cuda.synchronize(device)
+        g = capture_steps(torch, device, body, per_graph)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         for _ in range(replays):
@@ -549,30 +556,46 @@ def sweep(device, peak):
         torch.cuda.synchronize(device)
         return a.elapsed_time(b) / (per_graph * replays)
 
-    def timed(fn, sets, per_graph=12, replays=5, flush=False):
-        """ms per launch of fn, back to back in a CUDA graph.  With flush, every launch
-        follows a read of a 256 MiB buffer (a max-reduction) that leaves L2 holding only
-        clean lines of that buffer (for workloads that touch less than L2 per launch),
-        and the same graph of reads alone is timed and subtracted."""
+    def timed(fn, sets, replays=5):
+        """ms per launch of fn, launched back to back over `sets` (at least 12 launches,
+        every set at least once) in a CUDA graph."""
         for k in range(3):
             fn(sets[k % len(sets)])
         torch.cuda.synchronize(device)
-        side = torch.cuda.Stream(device)
-        side.wait_stream(torch.cuda.current_stream(device))
-        with torch.cuda.stream(side):
-            fn(sets[0])
-            flush_buf.max()
-        torch.cuda.current_stream(device).wait_stream(side)
-        torch.cuda.synchronize(device)
-        if not flush:
-            return graph_ms(lambda k: fn(sets[k % len(sets)]), per_graph, replays)
+        return graph_ms(lambda k: fn(sets[k % len(sets)]), max(12, len(sets)), replays)
 
-        def both(k):
-            flush_buf.max()
-            fn(sets[k % len(sets)])
-        t_both = graph_ms(both, per_graph, replays)
-        t_flush = graph_ms(lambda k: flush_buf.max(), per_graph, replays)
-        return t_both - t_flush
+    def stream_same_bytes(nbytes):
+        """torch's elementwise kernel (fp32 negation, nbytes/2 read and nbytes/2 written)
+        over rotating buffer pairs that together exceed L2: what a plain streaming kernel
+        reaches at that transfer size, launch and ramp-up included."""
+        n = nbytes // 8
+        pairs = [(torch.ones(n, dtype=torch.float32, device=device),
+                  torch.empty(n, dtype=torch.float32, device=device))
+                 for _ in range(int(max(1, -(-320_000_000 // (8 * n)))))]
+        ms = timed(lambda pr: torch.neg(pr[0], out=pr[1]), pairs)
+        del pairs
+        torch.cuda.empty_cache()
+        return {"bytes": 8 * n, "us": ms * 1e3, "gbs": 8 * n / (ms * 1e-3) / 1e9,
+                "frac_of_peak": 8 * n / (ms * 1e-3) / 1e9 / peak,
+                "kernel": "torch elementwise (fp32 negation)",
+                "l2": "rotating buffer pairs touching more than 320 MB"}
+
+    # the smallest configuration: 1024 tokens, launch- and latency-bound
+    case = W.insert_v41_1024()
+    b = insert_bytes(case.slots, 528)
+    sets = device_sets(case, device, int(max(1, -(-320_000_000 // b))))
+    ms = timed(lambda s: gkr.kv_insert(s["kv"], s["cache"], s["slots"], s["pos"], s["csc"],
+                                       case.block_size, 528), sets)
+    res["insert_v41_1024"] = {"kernel": "insert", "launch": gkr.insert_kernel_for(1024),
+                              "us": ms * 1e3, "tokens_per_s": 1024 / (ms * 1e-3), "alg_bytes": b,
+                              "alg_gbs": b / (ms * 1e-3) / 1e9,
+                              "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+                              "csc_bytes": csc_bytes(case.slots, case.positions),
+                              "l2": f"{len(sets)} rotating input sets"}
+    del sets
+    torch.cuda.empty_cache()
+    res["stream_same_bytes_as_roundtrip_insert"] = stream_same_bytes(
+        insert_bytes(W.roundtrip_v41_16384().slots, 528))
 
     for name, n_sets in (("insert_v4_65536", 3), ("insert_v41_262144", 1)):
         case = getattr(W, name)()
@@ -582,7 +605,9 @@ def sweep(device, peak):
         b = insert_bytes(case.slots, case.record)
         res[name] = {"kernel": "insert", "us": ms * 1e3, "tokens_per_s": case.num_tokens / (ms * 1e-3),
                      "alg_bytes": b, "alg_gbs": b / (ms * 1e-3) / 1e9,
-                     "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
+                     "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+                     "csc_bytes": csc_bytes(case.slots, case.positions)}
+        res[f"stream_same_bytes_as_{name}"] = stream_same_bytes(b)   # a plain kernel, same bytes
         del sets
         torch.cuda.empty_cache()
 
@@ -598,6 +623,7 @@ def sweep(device, peak):
                                   "us": ms * 1e3, "tokens_per_s": T / (ms * 1e-3), "alg_bytes": b,
                                   "alg_gbs": b / (ms * 1e-3) / 1e9,
                                   "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+                                  "csc_bytes": csc_bytes(case.slots, case.positions),
                                   "l2": f"{len(sets)} rotating input sets"}
         if T == 65536:   # the round trip's gather at this size: the slots just written
             for st in sets:
@@ -635,7 +661,8 @@ def sweep(device, peak):
                      "l2": f"{n_sets} rotating input sets touching {n_sets * b / 1e6:.0f} MB",
                      "us": ms * 1e3, "tokens_per_s": case.num_tokens / (ms * 1e-3),
                      "alg_bytes": b, "alg_gbs": b / (ms * 1e-3) / 1e9,
-                     "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
+                     "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+                     "csc_bytes": csc_bytes(case.slots, case.positions, R)}
         del sets, kv_big
         torch.cuda.empty_cache()
 
@@ -651,7 +678,8 @@ def sweep(device, peak):
         res[f"insert_{fmt}_262144"] = {
             "kernel": "insert", "record": record, "us": ms * 1e3,
             "tokens_per_s": case.num_tokens / (ms * 1e-3), "alg_bytes": b,
-            "alg_gbs": b / (ms * 1e-3) / 1e9, "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
+            "alg_gbs": b / (ms * 1e-3) / 1e9, "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+            "csc_bytes": csc_bytes(case.slots, case.positions)}
         del sets
         torch.cuda.empty_cache()
 
@@ -935,6 +963,7 @@ def main(argv=None):
                        "gbs": ib / (r["ins_ms"] * 1e-3) / 1e9,
                        "frac_of_peak": ib / (r["ins_ms"] * 1e-3) / 1e9 / peak,
                        "traffic": ncu_traffic(gkr.insert_kernel_for(T), WORKLOAD),
+                       "csc_bytes": csc_bytes(case.slots, case.positions),
                        "isolated_us": r["ins_iso_ms"] * 1e3},
             "gather": {"us": r["gat_ms"] * 1e3, "alg_bytes": gb,
                        "gbs": gb / (r["gat_ms"] * 1e-3) / 1e9,

@@ -26,6 +26,13 @@ def test_algorithmic_bytes():
     assert bench.compressed_insert_bytes(slots, pos, 1, 584) == bench.insert_bytes(slots, 584)
     idx = np.array([[-1, 2], [3, -1]], np.int32)
     assert bench.gather_bytes(idx, 528) == 4 * 1028 + 2 * 528
+    # cos/sin rows: one per distinct row among the written tokens (tokens 1 and 2 share
+    # position 3's row; the skipped token's position 5 is not read)
+    pos = np.array([3, 3, 3, 5, 11], np.int64)
+    assert bench.csc_bytes(slots, pos) == 2 * 256
+    # ratio 4: tokens 1, 2 (pos 3) and 4 (pos 11) read the rows of group starts 0 and 8
+    assert bench.csc_bytes(slots, pos, 4) == 2 * 256
+    assert bench.csc_bytes(slots, np.array([3, 2, 6, 5, 10], np.int64), 4) == 0
 
 
 def _free_port() -> int:

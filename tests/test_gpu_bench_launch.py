@@ -1,0 +1,64 @@
+"""GPU parity in the launch configuration the benchmark times: the round-trip step
+(insert 16384 tokens, gather the same slot ids) captured GRAPH_STEPS times over the
+rotating input sets in one CUDA graph, and the V4 65536-token insert captured back to
+back over its sets as the sweep launches it.  Every set's whole cache and gather output
+are compared with the oracle after the replays."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+import workloads as W
+from helpers import bits_of, first_mismatch
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _distinct_buffers(sets, keys):
+    for key in keys:
+        ptrs = [s[key].data_ptr() for s in sets]
+        assert len(set(ptrs)) == len(ptrs), key
+
+
+def test_timed_roundtrip_graph_matches_oracle(gkr, oracle_mod):
+    case = W.roundtrip_v41_16384()
+    sets = bench.device_sets(case, DEV, bench.ROTATE)
+    _distinct_buffers(sets, ("kv", "slots", "pos", "idx", "cache", "out"))   # no set shares L2 lines
+    g = bench.roundtrip_graph(torch, gkr, case, sets, DEV)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    ps = oracle_mod.page_stride(528, case.block_size)
+    ref = np.zeros(case.num_pages * ps, np.uint8)            # device_sets fills caches with 0
+    assert oracle_mod.insert(case.kv, ref, 528, case.block_size, case.num_pages, ps, case.slots,
+                             case.positions, case.csc) == 0
+    ref_out, ref_err = oracle_mod.gather(ref, 528, case.block_size, case.num_pages, ps,
+                                         case.indices)
+    assert ref_err == 0
+    for k, s in enumerate(sets):
+        n, first = first_mismatch(gkr.cache_bytes(s["cache"]).cpu().numpy(), ref)
+        assert n == 0, f"set {k}: {n} cache bytes differ, first {first}"
+        got = bits_of(s["out"])
+        assert np.array_equal(got, ref_out), f"set {k}: gather output differs"
+
+
+@pytest.mark.slow
+def test_sweep_v4_65536_graph_matches_oracle(gkr, oracle_mod):
+    case = W.insert_v4_65536()
+    sets = bench.device_sets(case, DEV, 3)
+    _distinct_buffers(sets, ("kv", "cache"))
+    g = bench.capture_steps(torch, DEV, lambda k: gkr.kv_insert(
+        sets[k % 3]["kv"], sets[k % 3]["cache"], sets[k % 3]["slots"], sets[k % 3]["pos"],
+        sets[k % 3]["csc"], case.block_size, case.record), 12)
+    g.replay()
+    torch.cuda.synchronize()
+    ps = oracle_mod.page_stride(584, case.block_size)
+    ref = np.zeros(case.num_pages * ps, np.uint8)
+    assert oracle_mod.insert(case.kv, ref, 584, case.block_size, case.num_pages, ps, case.slots,
+                             case.positions, case.csc) == 0
+    for k, s in enumerate(sets):
+        n, first = first_mismatch(gkr.cache_bytes(s["cache"]).cpu().numpy(), ref)
+        assert n == 0, f"set {k}: {n} cache bytes differ, first {first}"
