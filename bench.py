@@ -494,6 +494,13 @@ def time_e2e(args, device, case, dist=None):
         drained[b].record(s_down)
         started[b] = True
 
+    def copies_only(i):                            # the step's two transfers, no kernels
+        b = i % NB
+        with torch.cuda.stream(s_up):
+            dbuf[b].copy_(pin[b], non_blocking=True)
+        with torch.cuda.stream(s_down):
+            out_h[b].copy_(out[b], non_blocking=True)
+
     def serial(i):
         b = i % NB
         cur = torch.cuda.current_stream(device)
@@ -521,6 +528,7 @@ def time_e2e(args, device, case, dist=None):
 
     world = 1 if dist is None else dist.get_world_size()
     ms_serial = timed(serial, args.e2e_steps)
+    ms_copies = timed(copies_only, args.e2e_steps)
     ms = timed(piped, args.e2e_steps)
     # every step inserts and gathers the same inputs: each downloaded buffer must hold
     # the same rows as the device-side result (a race between the streams shows here)
@@ -532,6 +540,10 @@ def time_e2e(args, device, case, dist=None):
             "d2h_bytes_per_step": d2h,
             "serial": {"value": world * case.num_tokens / (ms_serial * 1e-3),
                        "ms_per_step": ms_serial},
+            "copies_only": {"ms_per_step": ms_copies,
+                            "host_link_gbs": (h2d + d2h) / (ms_copies * 1e-3) / 1e9,
+                            "what": "the step's upload and download alone, concurrent on "
+                                    "their two streams: the host-link bound of the step"},
             "path": "one pinned host -> device copy of the step's inputs, kv_insert, kv_gather, "
                     f"device -> pinned host copy of the rows; three streams, {NB} buffer sets"}
 

@@ -396,17 +396,15 @@ __global__ void __launch_bounds__(kThreads, GKR_SHORT_MIN_BLOCKS)
 // GKR_ERR_POS; a position that ends no group skips; a group row past the table sets
 // GKR_ERR_POS.
 
-// Decode token t: data-row / scale-row offsets (off = -1 when nothing is written) and
-// the cos/sin row; returns the error bits.
+// Decode one token from its slot and position: data-row / scale-row offsets (off = -1
+// when nothing is written) and the cos/sin row; returns the error bits.
 template <int kRecord>
-__device__ __forceinline__ uint32_t decode_compressed(const InsertParams& p, int64_t t,
-                                                      int64_t& off, int64_t& soff,
+__device__ __forceinline__ uint32_t decode_compressed(const InsertParams& p, int64_t slot,
+                                                      int64_t q, int64_t& off, int64_t& soff,
                                                       int32_t& row) {
     static_assert(Fmt<kRecord>::kPacked, "the compressed insert writes the packed records");
     constexpr uint32_t D = Fmt<kRecord>::D;
     constexpr uint32_t S = Fmt<kRecord>::S;
-    const int64_t slot = __ldg(p.slots + t);
-    const int64_t q = __ldg(p.positions + t);
     if (slot < 0) return 0u;
     if (slot >= p.num_slots) return 1u;
     if (q < 0) return 2u;
@@ -568,21 +566,26 @@ cudaError_t launch(const InsertParams& p, cudaStream_t stream) {
 }
 
 #ifndef GKR_SPARSE_MIN_BLOCKS
-#define GKR_SPARSE_MIN_BLOCKS 5
+#define GKR_SPARSE_MIN_BLOCKS 4   // up to 64 registers: the 48-register build spills
 #endif
 #ifndef GKR_SPARSE_BATCH
 #define GKR_SPARSE_BATCH 3
 #endif
 constexpr int kSparseBatch = GKR_SPARSE_BATCH;  // tokens staged at once by the compressed insert
 
-// The compressed insert: one warp per `chunk` (<= 32) consecutive tokens, lane i decodes
-// token t0 + i, and a ballot collects the tokens to write.  They are taken up to three at
-// a time, their kv and cos/sin rows copied into the warp's shared-memory staging area with
-// cp.async (each lane its own 16-byte pieces) and encoded after one wait.  No payload
-// register is live during the loads (5 blocks per SM; loading two tokens to registers
-// allowed 4 and measured 28.0 against 23.0 us at 262144 tokens, ratio 4), and with chunk
-// about 3R a warp usually writes its tokens in one batch, while tokens that end no group
-// cost only their 16 bytes of slot and position.
+// The compressed insert: the grid is at most one wave, and each warp takes chunks of
+// `chunk` (<= 32) consecutive tokens, striding by the grid's token count.  In a chunk,
+// lane i decodes token t0 + i and a ballot collects the tokens to write; they are taken
+// up to three at a time, their kv and cos/sin rows copied into the warp's shared-memory
+// staging area with cp.async (each lane its own 16-byte pieces) and encoded after one
+// wait.  The slot and position loads of the warp's next chunk are issued before this
+// chunk's copies, so their latency hides behind its writes.  With chunk about 3R a chunk
+// is usually one batch, while tokens that end no group cost only their 16 bytes of slot
+// and position.  Measured on GB300 at 262144 tokens, ratio 4, against one chunk per
+// warp: 21.5 against 23.1 us back to back, 29.4-29.8 against 30.1-30.4 us after an
+// L2-flushing kernel, 26.2-26.6 against 26.9 us launched alone; at ratio 128, 4.4 against
+// 4.9 us back to back.  48 registers (5 blocks per SM) spill and measured slower, as did
+// chunks of 8R.
 template <int kRecord, bool kSanitize>
 __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
     insert_sparse_staged_kernel(const InsertParams p, const int32_t chunk) {
@@ -591,62 +594,79 @@ __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
     pdl_release_next();
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
-    const int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib) * chunk;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock * chunk;
+    int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib) * chunk;
     if (t0 >= p.num_tokens) return;  // warp-uniform
 
-    int64_t off = -1, soff = 0;
-    int32_t row = 0;
-    uint32_t err = 0;
-    if (lane < chunk && t0 + lane < p.num_tokens)
-        err = decode_compressed<kRecord>(p, t0 + lane, off, soff, row);
-    err = __reduce_or_sync(kFull, err);
-    if (err != 0u && lane == 0) report(p.err, static_cast<int32_t>(err));
-    uint32_t todo = __ballot_sync(kFull, off >= 0);
-
-    const uint8_t* const kv_lane = static_cast<const uint8_t*>(p.kv) + t0 * 1024 + 16 * lane;
     const float* const csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
     uint8_t* const ring_lane = smem + wib * (kSparseBatch * kSlotBytes) + 16 * lane;
     uint8_t* const cache_a = p.cache + 8 * lane;
     uint8_t* const cache_s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
-    while (todo != 0u) {                             // warp-uniform
-        int u[kSparseBatch];
-#pragma unroll
-        for (int v = 0; v < kSparseBatch; ++v) {
-            u[v] = todo != 0u ? __ffs(todo) - 1 : -1;
-            todo &= todo - 1u;
+    int64_t slot = -1, q = 0;
+    if (lane < chunk && t0 + lane < p.num_tokens) {
+        slot = __ldg(p.slots + t0 + lane);
+        q = __ldg(p.positions + t0 + lane);
+    }
+    while (true) {
+        int64_t off = -1, soff = 0;
+        int32_t row = 0;
+        uint32_t err = decode_compressed<kRecord>(p, slot, q, off, soff, row);
+        err = __reduce_or_sync(kFull, err);
+        if (err != 0u && lane == 0) report(p.err, static_cast<int32_t>(err));
+        uint32_t todo = __ballot_sync(kFull, off >= 0);
+        const uint8_t* const kv_lane = static_cast<const uint8_t*>(p.kv) + t0 * 1024 + 16 * lane;
+        // the next chunk's slot / position loads fly while this chunk is written
+        const int64_t t1 = t0 + stride;
+        slot = -1;
+        q = 0;
+        if (lane < chunk && t1 + lane < p.num_tokens) {
+            slot = __ldg(p.slots + t1 + lane);
+            q = __ldg(p.positions + t1 + lane);
         }
+        while (todo != 0u) {                             // warp-uniform
+            int u[kSparseBatch];
 #pragma unroll
-        for (int v = 0; v < kSparseBatch; ++v) {
-            if (u[v] >= 0) {                         // warp-uniform
-                const int32_t r = __shfl_sync(kFull, row, u[v]);
-                uint8_t* dst = ring_lane + v * kSlotBytes;
-                cp_async16(dst, kv_lane + u[v] * 1024);
-                cp_async16(dst + 512, kv_lane + u[v] * 1024 + 512);
-                if (lane >= 24) {
-                    const float* cs = csc_lane + static_cast<int64_t>(r) * 64;
-                    cp_async16(dst + 1024 - 16 * 24, cs);
-                    cp_async16(dst + 1024 + 128 - 16 * 24, cs + 32);
+            for (int v = 0; v < kSparseBatch; ++v) {
+                u[v] = todo != 0u ? __ffs(todo) - 1 : -1;
+                todo &= todo - 1u;
+            }
+#pragma unroll
+            for (int v = 0; v < kSparseBatch; ++v) {
+                if (u[v] >= 0) {                         // warp-uniform
+                    const int32_t r = __shfl_sync(kFull, row, u[v]);
+                    uint8_t* dst = ring_lane + v * kSlotBytes;
+                    cp_async16(dst, kv_lane + u[v] * 1024);
+                    cp_async16(dst + 512, kv_lane + u[v] * 1024 + 512);
+                    if (lane >= 24) {
+                        const float* cs = csc_lane + static_cast<int64_t>(r) * 64;
+                        cp_async16(dst + 1024 - 16 * 24, cs);
+                        cp_async16(dst + 1024 + 128 - 16 * 24, cs + 32);
+                    }
+                }
+            }
+            cp_async_commit();
+            cp_async_wait<0>();  // this lane's copies have landed; each lane reads only its own
+#pragma unroll
+            for (int v = 0; v < kSparseBatch; ++v) {
+                if (u[v] >= 0) {                         // warp-uniform
+                    const int64_t o = __shfl_sync(kFull, off, u[v]);
+                    const int64_t so = __shfl_sync(kFull, soff, u[v]);
+                    const uint8_t* src = ring_lane + v * kSlotBytes;
+                    TokenLoads L;
+                    L.a = lds16(src);
+                    L.b = lds16(src + 512);
+                    if (lane >= 24) {
+                        L.c = *reinterpret_cast<const float4*>(src + 1024 - 16 * 24);
+                        L.s = *reinterpret_cast<const float4*>(src + 1024 + 128 - 16 * 24);
+                    }
+                    encode_store<kRecord, kSanitize>(L, cache_a + o, cache_s + so, lane,
+                                                     Scale{1.0f, 1.0f});
                 }
             }
         }
-        cp_async_commit();
-        cp_async_wait<0>();  // this lane's copies have landed; each lane reads only its own
-#pragma unroll
-        for (int v = 0; v < kSparseBatch; ++v) {
-            if (u[v] >= 0) {                         // warp-uniform
-                const int64_t o = __shfl_sync(kFull, off, u[v]);
-                const int64_t so = __shfl_sync(kFull, soff, u[v]);
-                const uint8_t* src = ring_lane + v * kSlotBytes;
-                TokenLoads L;
-                L.a = lds16(src);
-                L.b = lds16(src + 512);
-                if (lane >= 24) {
-                    L.c = *reinterpret_cast<const float4*>(src + 1024 - 16 * 24);
-                    L.s = *reinterpret_cast<const float4*>(src + 1024 + 128 - 16 * 24);
-                }
-                encode_store<kRecord, kSanitize>(L, cache_a + o, cache_s + so, lane, Scale{1.0f, 1.0f});
-            }
-        }
+        if (t1 >= p.num_tokens) break;  // warp-uniform
+        __syncwarp();  // reconverge before the next chunk's shuffles
+        t0 = t1;
     }
 }
 
@@ -664,7 +684,9 @@ cudaError_t launch_compressed(const InsertParams& p, bool sanitize, cudaStream_t
     int64_t wave = 0;  // also raises the kernel's dynamic shared-memory limit above 48 KiB
     cudaError_t e = resident_warps(reinterpret_cast<const void*>(kernel), kThreads, smem, &wave);
     if (e != cudaSuccess) return e;
-    return launch_kernel(kernel, blocks, kThreads, smem, stream, p, chunk);
+    const int64_t resident = wave / kWarpsPerBlock;          // the grid is at most one wave
+    return launch_kernel(kernel, blocks < resident ? blocks : resident, kThreads, smem, stream, p,
+                         chunk);
 }
 
 }  // namespace
