@@ -288,6 +288,23 @@ def device_sets(case, device, n_sets: int, record: int | None = None, clone_kv: 
     return sets
 
 
+def compressed_sets(case, device, alg_bytes: int):
+    """Input sets for a compressed insert, which reads only its group-boundary tokens' rows:
+    set k reads kv through the window [k, k + T) of one buffer of T + n rows (k < R, so each
+    set's boundary tokens read other rows) and owns its slots, positions and cache; n sets
+    together touch more than 320 MB (or n = R)."""
+    import torch
+    R = case.meta["compress_ratio"]
+    n_sets = int(min(R, max(1, -(-320_000_000 // alg_bytes))))
+    T = case.num_tokens
+    kv_big = torch.from_numpy(np.concatenate([case.kv, case.kv[:n_sets]]).view(np.int16)) \
+        .view(torch.bfloat16).to(device)
+    sets = device_sets(case, device, n_sets, clone_kv=False)
+    for k, st in enumerate(sets):
+        st["kv"] = kv_big[k:k + T]
+    return sets
+
+
 def step(gkr, case, s, ev=None):
     """One pass of the hot path on one input set; optional events around each kernel."""
     if ev is not None:
@@ -318,6 +335,33 @@ def capture_steps(torch, device, body, n: int):
     g.replay()
     torch.cuda.synchronize(device)
     return g
+
+
+def stream_same_bytes(torch, device, nbytes: int, peak: float, replays: int = 5) -> dict:
+    """torch's elementwise kernel (fp32 negation, nbytes/2 read and nbytes/2 written)
+    launched back to back in a CUDA graph over rotating buffer pairs that together exceed
+    L2: what a plain streaming kernel reaches at that transfer size, launch and ramp-up
+    included."""
+    n = nbytes // 8
+    pairs = [(torch.ones(n, dtype=torch.float32, device=device),
+              torch.empty(n, dtype=torch.float32, device=device))
+             for _ in range(int(max(1, -(-320_000_000 // (8 * n)))))]
+    per_graph = max(12, len(pairs))
+    g = capture_steps(torch, device, lambda k: torch.neg(pairs[k % len(pairs)][0],
+                                                         out=pairs[k % len(pairs)][1]), per_graph)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(replays):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / (per_graph * replays)
+    del g, pairs
+    torch.cuda.empty_cache()
+    return {"bytes": 8 * n, "us": ms * 1e3, "gbs": 8 * n / (ms * 1e-3) / 1e9,
+            "frac_of_peak": 8 * n / (ms * 1e-3) / 1e9 / peak,
+            "kernel": "torch elementwise (fp32 negation)",
+            "l2": "rotating buffer pairs touching more than 320 MB"}
 
 
 def roundtrip_graph(torch, gkr, case, sets, device, events=None):
@@ -576,22 +620,6 @@ def sweep(device, peak):
         torch.cuda.synchronize(device)
         return graph_ms(lambda k: fn(sets[k % len(sets)]), max(12, len(sets)), replays)
 
-    def stream_same_bytes(nbytes):
-        """torch's elementwise kernel (fp32 negation, nbytes/2 read and nbytes/2 written)
-        over rotating buffer pairs that together exceed L2: what a plain streaming kernel
-        reaches at that transfer size, launch and ramp-up included."""
-        n = nbytes // 8
-        pairs = [(torch.ones(n, dtype=torch.float32, device=device),
-                  torch.empty(n, dtype=torch.float32, device=device))
-                 for _ in range(int(max(1, -(-320_000_000 // (8 * n)))))]
-        ms = timed(lambda pr: torch.neg(pr[0], out=pr[1]), pairs)
-        del pairs
-        torch.cuda.empty_cache()
-        return {"bytes": 8 * n, "us": ms * 1e3, "gbs": 8 * n / (ms * 1e-3) / 1e9,
-                "frac_of_peak": 8 * n / (ms * 1e-3) / 1e9 / peak,
-                "kernel": "torch elementwise (fp32 negation)",
-                "l2": "rotating buffer pairs touching more than 320 MB"}
-
     # the smallest configuration: 1024 tokens, launch- and latency-bound
     case = W.insert_v41_1024()
     b = insert_bytes(case.slots, 528)
@@ -606,8 +634,6 @@ def sweep(device, peak):
                               "l2": f"{len(sets)} rotating input sets"}
     del sets
     torch.cuda.empty_cache()
-    res["stream_same_bytes_as_roundtrip_insert"] = stream_same_bytes(
-        insert_bytes(W.roundtrip_v41_16384().slots, 528))
 
     for name, n_sets in (("insert_v4_65536", 3), ("insert_v41_262144", 1)):
         case = getattr(W, name)()
@@ -619,7 +645,7 @@ def sweep(device, peak):
                      "alg_bytes": b, "alg_gbs": b / (ms * 1e-3) / 1e9,
                      "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
                      "csc_bytes": csc_bytes(case.slots, case.positions)}
-        res[f"stream_same_bytes_as_{name}"] = stream_same_bytes(b)   # a plain kernel, same bytes
+        res[f"stream_same_bytes_as_{name}"] = stream_same_bytes(torch, device, b, peak)
         del sets
         torch.cuda.empty_cache()
 
@@ -659,13 +685,8 @@ def sweep(device, peak):
         # sets read kv through windows of one buffer shifted by k rows (k < R, so each set
         # reads other rows), with their own slots, positions and cache, until the sets
         # together touch more than 320 MB
-        n_sets = int(min(R, max(1, -(-320_000_000 // b))))
-        T = case.num_tokens
-        kv_big = torch.from_numpy(
-            np.concatenate([case.kv, case.kv[:n_sets]]).view(np.int16)).view(torch.bfloat16).to(device)
-        sets = device_sets(case, device, n_sets, clone_kv=False)
-        for k, st in enumerate(sets):
-            st["kv"] = kv_big[k:k + T]
+        sets = compressed_sets(case, device, b)
+        n_sets = len(sets)
         ms = timed(lambda s: gkr.rope_quant_insert(s["kv"], s["cache"], s["slots"], s["pos"],
                                                    s["csc"], case.block_size, R, True,
                                                    case.record), sets)
@@ -675,7 +696,7 @@ def sweep(device, peak):
                      "alg_bytes": b, "alg_gbs": b / (ms * 1e-3) / 1e9,
                      "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
                      "csc_bytes": csc_bytes(case.slots, case.positions, R)}
-        del sets, kv_big
+        del sets
         torch.cuda.empty_cache()
 
     # the plain KV-only caches: the 262144-token insert into bf16 rows and fp8 rows
@@ -987,11 +1008,17 @@ def main(argv=None):
     ach = kern[dom]["gbs"]
     kname = {"insert": gkr.insert_kernel_for(T),
              "gather": "gather_kernel"}[dom]
+    same = stream_same_bytes(torch, device, kern[dom]["alg_bytes"], peak)
     roofline = {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
                 "frac": ach / peak, "peak_source": peak_src,
                 "traffic": ncu_traffic(kname, WORKLOAD),
                 "alg_bytes_per_launch": kern[dom]["alg_bytes"],
-                "timing": r["kernel_timing"]}
+                "timing": r["kernel_timing"],
+                "stream_same_bytes": {"gbs": same["gbs"], "us": same["us"],
+                                      "frac_of_peak": same["frac_of_peak"],
+                                      "kernel_vs_stream": ach / same["gbs"],
+                                      "what": "torch's elementwise kernel moving the same bytes "
+                                              "per launch, back to back over rotating buffers"}}
 
     out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,

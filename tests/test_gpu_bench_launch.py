@@ -1,8 +1,8 @@
-"""GPU parity in the launch configuration the benchmark times: the round-trip step
+"""GPU parity in the launch configurations the benchmark times: the round-trip step
 (insert 16384 tokens, gather the same slot ids) captured GRAPH_STEPS times over the
-rotating input sets in one CUDA graph, and the V4 65536-token insert captured back to
-back over its sets as the sweep launches it.  Every set's whole cache and gather output
-are compared with the oracle after the replays."""
+rotating input sets in one CUDA graph; the V4 65536-token insert and the ratio-4
+compressed insert captured back to back over their sets as the sweep launches them.
+Caches and gather outputs are compared with the oracle in full after the replays."""
 from __future__ import annotations
 
 import numpy as np
@@ -62,3 +62,30 @@ def test_sweep_v4_65536_graph_matches_oracle(gkr, oracle_mod):
     for k, s in enumerate(sets):
         n, first = first_mismatch(gkr.cache_bytes(s["cache"]).cpu().numpy(), ref)
         assert n == 0, f"set {k}: {n} cache bytes differ, first {first}"
+
+
+@pytest.mark.slow
+def test_sweep_compressed_r4_graph_matches_oracle(gkr, oracle_mod):
+    """The compressed insert as the sweep launches it: input sets reading kv through
+    shifted windows of one buffer, 12 launches back to back in a CUDA graph."""
+    case = W.compressed_v41_r4_262144()
+    R, T = case.meta["compress_ratio"], case.num_tokens
+    sets = bench.compressed_sets(case, DEV, bench.compressed_insert_bytes(
+        case.slots, case.positions, R, case.record))
+    n = len(sets)
+    assert n > 1
+    _distinct_buffers(sets, ("kv", "slots", "cache"))
+    g = bench.capture_steps(torch, DEV, lambda k: gkr.rope_quant_insert(
+        sets[k % n]["kv"], sets[k % n]["cache"], sets[k % n]["slots"], sets[k % n]["pos"],
+        sets[k % n]["csc"], case.block_size, R, True, case.record), 12)
+    g.replay()
+    torch.cuda.synchronize()
+    ps = oracle_mod.page_stride(case.record, case.block_size)
+    kv_all = np.concatenate([case.kv, case.kv[:n]])
+    for k in (0, n - 1):
+        ref = np.zeros(case.num_pages * ps, np.uint8)
+        assert oracle_mod.insert(kv_all[k:k + T], ref, case.record, case.block_size,
+                                 case.num_pages, ps, case.slots, case.positions, case.csc,
+                                 compress_ratio=R, sanitize_nans=True) == 0
+        n_bad, first = first_mismatch(gkr.cache_bytes(sets[k]["cache"]).cpu().numpy(), ref)
+        assert n_bad == 0, f"set {k}: {n_bad} cache bytes differ, first {first}"
