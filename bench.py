@@ -429,7 +429,8 @@ def time_roundtrip(args, device, dist):
     # per-kernel launch duration as the roofline uses it: the same kernel launched G
     # times back to back over the rotating input sets in a graph of its own, CUDA
     # events around 5 replays (no event nodes between the launches)
-    b2b = {}
+    b2b, flushed = {}, {}
+    flush = torch.ones(64 << 20, dtype=torch.int32, device=device)      # 256 MiB, 2x the L2
     for name, fn in (("insert", lambda s: gkr.kv_insert(s["kv"], s["cache"], s["slots"],
                                                           s["pos"], s["csc"], case.block_size,
                                                           case.record)),
@@ -442,9 +443,23 @@ def time_roundtrip(args, device, dist):
         b.record(stream)
         torch.cuda.synchronize(device)
         b2b[name] = a.elapsed_time(b) / (5 * G)
+        # the same kernel launched alone after an L2 flush, CUDA events around it only:
+        # median over 25 launches, each after a max-reduction over 256 MiB (L2 then holds
+        # clean lines of that buffer, so the kernel pays no write-backs of the flush)
+        ev = []
+        for k in range(25):
+            flush.max()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn(sets[k % ROTATE])
+            e1.record(stream)
+            ev.append((e0, e1))
+        torch.cuda.synchronize(device)
+        flushed[name] = statistics.median(x.elapsed_time(y) for x, y in ev)
     return dict(case=case, K=K, total_ms=total_ms_max, ins_ms=b2b["insert"],
                 gat_ms=b2b["gather"], ins_iso_ms=float(np.mean(ins)),
-                gat_iso_ms=float(np.mean(gat)),
+                gat_iso_ms=float(np.mean(gat)), ins_flushed_ms=flushed["insert"],
+                gat_flushed_ms=flushed["gather"],
                 kernel_timing=(f"CUDA events around 5 replays of a graph of {G} back-to-back "
                                "launches of the kernel alone over the same rotating input sets"),
                 iso_timing=how, clocks=clocks, T=T)
@@ -997,13 +1012,17 @@ def main(argv=None):
                        "frac_of_peak": ib / (r["ins_ms"] * 1e-3) / 1e9 / peak,
                        "traffic": ncu_traffic(gkr.insert_kernel_for(T), WORKLOAD),
                        "csc_bytes": csc_bytes(case.slots, case.positions),
-                       "isolated_us": r["ins_iso_ms"] * 1e3},
+                       "isolated_us": r["ins_iso_ms"] * 1e3,
+                       "after_l2_flush_us": r["ins_flushed_ms"] * 1e3},
             "gather": {"us": r["gat_ms"] * 1e3, "alg_bytes": gb,
                        "gbs": gb / (r["gat_ms"] * 1e-3) / 1e9,
                        "frac_of_peak": gb / (r["gat_ms"] * 1e-3) / 1e9 / peak,
                        "traffic": ncu_traffic("gather_kernel", WORKLOAD),
-                       "isolated_us": r["gat_iso_ms"] * 1e3},
-            "isolated_timing": r["iso_timing"]}
+                       "isolated_us": r["gat_iso_ms"] * 1e3,
+                       "after_l2_flush_us": r["gat_flushed_ms"] * 1e3},
+            "isolated_timing": r["iso_timing"],
+            "after_l2_flush_timing": ("median of 25 launches, each alone after a max-reduction "
+                                      "over a 256 MiB buffer, CUDA events around the kernel")}
     dom = "insert" if r["ins_ms"] >= r["gat_ms"] else "gather"
     ach = kern[dom]["gbs"]
     kname = {"insert": gkr.insert_kernel_for(T),
