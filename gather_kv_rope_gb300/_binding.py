@@ -308,8 +308,8 @@ def rope_quant_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: tor
     (position + 1) % compress_ratio == 0, rotated with the cos/sin row of its group's
     first position (position // compress_ratio * compress_ratio); with sanitize_nans
     every NaN of the rotated row is stored as +0.  Arguments as for kv_insert."""
-    _check(isinstance(compress_ratio, int) and compress_ratio >= 1,
-           "compress_ratio must be an int >= 1")
+    _check(isinstance(compress_ratio, int) and 1 <= compress_ratio <= 0x7FFFFFFF,
+           "compress_ratio must be an int in [1, 2^31 - 1]")
     desc, T, dev = _insert_args(kv, k_cache, slot_mapping, positions, cos_sin_cache,
                                 block_size, record, err_flag)
     _check(desc.record in PACKED, "the compressed insert writes the packed 528 / 584 records")

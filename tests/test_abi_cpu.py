@@ -215,6 +215,8 @@ def test_binding_rejects_bad_tensors(gkr):
         gkr.kv_insert(kv, cache, slots, pos, csc, 32)          # CPU tensors: no CPU path
     with pytest.raises(ValueError, match="compress_ratio"):
         gkr.rope_quant_insert(kv, cache, slots, pos, csc, 32, compress_ratio=0)
+    with pytest.raises(ValueError, match="compress_ratio"):             # would wrap in int32
+        gkr.rope_quant_insert(kv, cache, slots, pos, csc, 32, compress_ratio=2**32 + 4)
     with pytest.raises(ValueError, match="kv must be"):
         gkr.rope_quant_insert(kv.float(), cache, slots, pos, csc, 32, 4)
     with pytest.raises(ValueError, match="CUDA"):

@@ -115,6 +115,22 @@ def test_compressed_error_bits(gkr, oracle_mod, record):
 
 
 @pytest.mark.parametrize("record", [528, 584])
+@pytest.mark.parametrize("ratio", [2**31 - 1, 2**31 - 2])
+def test_compressed_largest_ratios(gkr, oracle_mod, record, ratio):
+    """Ratios near 2^31 with positions near 2^32: the boundary test takes its 64-bit
+    form, a group-end position R - 1 maps to cos/sin row 0, and 2R - 1 to row R (past
+    the table: error bit, nothing written)."""
+    case = W.compressed_insert("bigR", 2, 64, 4, record, block_size=32, skip_rate=0.0, seed=11)
+    rng = np.random.default_rng(12)
+    case.positions = rng.integers(0, 4 * ratio, case.positions.size).astype(np.int64)
+    case.positions[::7] = ratio - 1              # group ends, row 0
+    case.positions[3::11] = 2 * ratio - 1        # group ends, row R: past the table
+    case.positions[5::13] = 3 * ratio - 2        # ends no group
+    ref = _compare(gkr, oracle_mod, case, ratio, True)
+    assert (ref != SENTINEL).any()               # some records were written
+
+
+@pytest.mark.parametrize("record", [528, 584])
 def test_compressed_cuda_graph_replay(gkr, oracle_mod, record):
     T, bs, ratio = 1024, 32, 4
     cases = [W.compressed_insert("graph", 4, 256, ratio, record, block_size=bs, seed=30 + r,
