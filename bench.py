@@ -714,17 +714,20 @@ def sweep(device, peak):
         del sets
         torch.cuda.empty_cache()
 
-    # the plain KV-only caches: the 262144-token insert into bf16 rows and fp8 rows
+    # the plain KV-only caches: the 262144-token insert into bf16 rows and fp8 rows (at a
+    # general scale, and at 1.0, a power of two, which takes the single-product quotient)
     case = W.insert_v41_262144()
     scale = torch.tensor([0.01], dtype=torch.float32, device=device)
-    for record, fmt in ((1024, "bf16"), (512, "fp8")):
+    scale_one = torch.tensor([1.0], dtype=torch.float32, device=device)
+    for record, fmt, sc in ((1024, "bf16", None), (512, "fp8", scale),
+                            (512, "fp8_scale1", scale_one)):
         sets = device_sets(case, device, 1, record=record)
-        sc = scale if record == 512 else None
         ms = timed(lambda s: gkr.kv_insert(s["kv"], s["cache"], s["slots"], s["pos"], s["csc"],
                                            case.block_size, record, fp8_scale=sc), sets)
         b = insert_bytes(case.slots, record)
         res[f"insert_{fmt}_262144"] = {
             "kernel": "insert", "record": record, "us": ms * 1e3,
+            "fp8_scale": None if sc is None else float(sc.item()),
             "tokens_per_s": case.num_tokens / (ms * 1e-3), "alg_bytes": b,
             "alg_gbs": b / (ms * 1e-3) / 1e9, "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
             "csc_bytes": csc_bytes(case.slots, case.positions)}

@@ -279,6 +279,27 @@ __device__ __forceinline__ uint2 quantise8_div(const float* f, float scale, floa
     return q;
 }
 
+// True for a power of two in [2^-126, 2^126] (a normal number with a zero mantissa,
+// whose reciprocal is a normal power of two too).
+__device__ __forceinline__ bool exact_power_of_two(float s) {
+    const uint32_t b = __float_as_uint(s);
+    const uint32_t E = b >> 23;                    // s > 0
+    return (b & 0x7FFFFFu) == 0u && E >= 1u && E <= 253u;
+}
+
+// Eight values -> e4m3(x / scale) for a power-of-two scale: with y = 1/scale exact, the
+// rounded product |x| * y is the rounded quotient, so one multiply per value replaces
+// the corrected reciprocal; the sign is carried as in quotient().
+__device__ __forceinline__ uint2 quantise8_pow2(const float* f, float y) {
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = copysignf(__fmul_rn(fabsf(f[i]), y), f[i]);
+    uint2 r;
+    r.x = e4m3x4(q[0], q[1], q[2], q[3]);
+    r.y = e4m3x4(q[4], q[5], q[6], q[7]);
+    return r;
+}
+
 // The same with one IEEE division per value (scales outside [2^-64, 2^64]).
 __device__ __forceinline__ uint2 quantise8_ieee_div(const float* f, float scale) {
     uint2 q;

@@ -128,9 +128,12 @@ __device__ __forceinline__ void encode_store_bf16(const TokenLoads& L, uint8_t* 
     }
 }
 
-// The fp8 cache's scale s and y = RN(1/s) for the corrected quotient (0: divide).
+// The fp8 cache's scale s and y = RN(1/s) for the corrected quotient (0: divide);
+// pow2: s is a power of two in [2^-126, 2^126], so y = 1/s exactly and |x| * y is the
+// quotient itself.
 struct Scale {
     float s, y;
+    bool pow2;
 };
 
 // fp8 row by IEEE divisions: the rare path (a scale outside [2^-64, 2^64]), kept out of
@@ -150,6 +153,15 @@ __device__ __forceinline__ void encode_store_fp8(const TokenLoads& L, uint8_t* d
                                                  Scale sc) {
     if (sc.y == 0.0f) {  // warp-uniform
         encode_store_fp8_ieee(L.a, L.b, L.c, L.s, da, lane, sc.s);
+        return;
+    }
+    if (sc.pow2) {  // warp-uniform; each branch holds the whole row, so neither is predicated
+        float a[8], b[8];
+        unpack_bf16x8(L.a, a);
+        unpack_bf16x8(L.b, b);
+        if (lane >= 24) rope4(b, L.c, L.s);
+        st8(da, quantise8_pow2(a, sc.y));
+        st8(da + 256, quantise8_pow2(b, sc.y));
         return;
     }
     float a[8], b[8];
@@ -176,13 +188,15 @@ template <int kRecord>
 __device__ __forceinline__ bool load_scale(const InsertParams& p, int lane, Scale& sc) {
     sc.s = 1.0f;
     sc.y = 1.0f;
+    sc.pow2 = false;
     if constexpr (kRecord == 512) {
         sc.s = __ldg(p.fp8_scale);
         if (!scale_ok(sc.s)) {
             if (lane == 0) report(p.err, kErrScale);
             return false;
         }
-        sc.y = quotient_reciprocal(sc.s);
+        sc.pow2 = exact_power_of_two(sc.s);
+        sc.y = sc.pow2 ? __frcp_rn(sc.s) : quotient_reciprocal(sc.s);
     }
     return true;
 }
@@ -660,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
                         L.s = *reinterpret_cast<const float4*>(src + 1024 + 128 - 16 * 24);
                     }
                     encode_store<kRecord, kSanitize>(L, cache_a + o, cache_s + so, lane,
-                                                     Scale{1.0f, 1.0f});
+                                                     Scale{1.0f, 1.0f, false});
                 }
             }
         }

@@ -183,15 +183,19 @@ def test_plain_cache_full_size_sampled(gkr, oracle_mod, record):
 
 @pytest.mark.parametrize("scale", [1e-30, 2.0 ** -64, float(np.nextafter(np.float32(2.0 ** -64), 0)),
                                    2.0 ** 64, float(np.nextafter(np.float32(2.0 ** 64), np.inf)),
-                                   1e30, 7.0 / 3.0])
+                                   1e30, 7.0 / 3.0, 1.0, 2.0 ** -126, 2.0 ** 126, 2.0 ** 127,
+                                   2.0 ** -127])
 def test_fp8_scales_across_the_quotient_paths(gkr, oracle_mod, scale):
-    """Scales inside [2^-64, 2^64] take the corrected-reciprocal quotient, scales outside
-    it the IEEE division: both must give the oracle's bytes.  kv is drawn around
-    50 * scale so the quotients land inside the e4m3 range (saturating tails included)."""
+    """Powers of two in [2^-126, 2^126] take the single exact product, other scales inside
+    [2^-64, 2^64] the corrected-reciprocal quotient, the rest (2^127, the subnormal 2^-127,
+    1e-30, 1e30) the IEEE division: all must give the oracle's bytes.  kv is drawn around
+    50 * scale (at most 1e36) so the quotients land inside the e4m3 range (saturating
+    tails included)."""
     s32 = float(np.float32(scale))
     case = _case(2000, 64, seed=21)
     rng = np.random.default_rng(22)
-    case.kv = W.to_bf16_bits((rng.standard_t(3, (2000, 512)) * 50.0 * s32).astype(np.float32))
+    case.kv = W.to_bf16_bits((rng.standard_t(3, (2000, 512)) * min(50.0 * s32, 1e36))
+                             .astype(np.float32))
     cache, got, ref, err, ref_err, ps = _insert(gkr, oracle_mod, case, 512, s32)
     n, first = first_mismatch(got, ref)
     assert n == 0 and err == ref_err == 0, first
