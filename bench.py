@@ -410,6 +410,24 @@ def time_roundtrip(args, device, dist):
     total_ms = e0.elapsed_time(e1)
     total_ms_max = reduce_max(total_ms, dist)
 
+    # the same step with early metadata reads (set_early_metadata): the slot lists,
+    # positions and indices are inputs that no kernel of the step writes
+    gkr.set_early_metadata(True)
+    try:
+        graph_em = roundtrip_graph(torch, gkr, case, sets, device)
+        n_em = max(1, replays // 4)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        a.record(stream)
+        for _ in range(n_em):
+            graph_em.replay()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        em_ms = reduce_max(a.elapsed_time(b) / (n_em * G), dist)
+        del graph_em
+    finally:
+        gkr.set_early_metadata(False)
+
     # per-kernel durations: the event graph (each kernel bracketed by event nodes, so
     # no launch overlap between kernels) replayed right after the timed region, or an
     # eager pass with the stream held back by a sleep so launches queue up first
@@ -456,7 +474,7 @@ def time_roundtrip(args, device, dist):
             ev.append((e0, e1))
         torch.cuda.synchronize(device)
         flushed[name] = statistics.median(x.elapsed_time(y) for x, y in ev)
-    return dict(case=case, K=K, total_ms=total_ms_max, ins_ms=b2b["insert"],
+    return dict(case=case, K=K, total_ms=total_ms_max, em_ms=em_ms, ins_ms=b2b["insert"],
                 gat_ms=b2b["gather"], ins_iso_ms=float(np.mean(ins)),
                 gat_iso_ms=float(np.mean(gat)), ins_flushed_ms=flushed["insert"],
                 gat_flushed_ms=flushed["gather"],
@@ -1049,6 +1067,13 @@ def main(argv=None):
                       "num_pages": 512, "gathered": int(case.indices.size),
                       "l2": f"inputs larger than L2: {ROTATE} rotating input sets",
                       "launch": f"CUDA graph of {GRAPH_STEPS} steps, replayed {K // GRAPH_STEPS}x"},
+           "early_metadata": {"value": world * T / (r["em_ms"] * 1e-3), "unit": "tokens/s",
+                              "ms_per_step": r["em_ms"],
+                              "what": "the same step with set_early_metadata(True): the "
+                                      "kernels read slot_mapping, positions and indices "
+                                      "before waiting for the kernel ahead of them (off by "
+                                      "default; valid here, no kernel of the step writes "
+                                      "them)"},
            "roofline": roofline, "kernels": kern, "gpu_launches": 2 * K * world,
            "gpu_launches_per_rank": 2 * K, "clocks": r["clocks"]}
     out["e2e"] = time_e2e(args, device, case, dist)            # every rank, max over ranks

@@ -12,14 +12,15 @@ ctypes.  PyTorch supplies device memory and streams only.
 """
 from .build import build as _build_lib
 from ._binding import (CacheDesc, ERR_INDEX, ERR_POS, ERR_SCALE, ERR_SLOT, GkrError, PACKED,
-                       RECORDS, alloc_cache,
-                       cache_bytes, get_insert_stream_min, get_pdl, kv_gather, kv_insert,
-                       get_insert_staged_min, insert_kernel_for, lib, library_path,
-                       page_stride, record_rows, rope_quant_insert, set_insert_staged_min,
-                       set_insert_stream_min, set_pdl, status_string)
+                       RECORDS, alloc_cache, cache_bytes, get_early_metadata,
+                       get_insert_staged_min, get_insert_stream_min, get_pdl,
+                       insert_kernel_for, kv_gather, kv_insert, lib, library_path,
+                       page_stride, record_rows, rope_quant_insert, set_early_metadata,
+                       set_insert_staged_min, set_insert_stream_min, set_pdl, status_string)
 
-__all__ = ["build", "kv_insert", "kv_gather", "rope_quant_insert", "page_stride", "record_rows", "alloc_cache",
-           "cache_bytes", "status_string", "set_pdl", "get_pdl", "set_insert_stream_min",
+__all__ = ["build", "kv_insert", "kv_gather", "rope_quant_insert", "page_stride", "record_rows",
+           "alloc_cache", "cache_bytes", "status_string", "set_pdl", "get_pdl",
+           "set_early_metadata", "get_early_metadata", "set_insert_stream_min",
            "get_insert_stream_min", "set_insert_staged_min", "get_insert_staged_min",
            "insert_kernel_for", "GkrError", "CacheDesc", "RECORDS", "PACKED", "ERR_SLOT",
            "ERR_POS", "ERR_INDEX", "ERR_SCALE", "lib", "library_path"]

@@ -86,6 +86,9 @@ def lib() -> ctypes.CDLL:
                 L.gkr_version.argtypes, L.gkr_version.restype = [], i32
                 L.gkr_set_pdl.argtypes, L.gkr_set_pdl.restype = [i32], None
                 L.gkr_get_pdl.argtypes, L.gkr_get_pdl.restype = [], i32
+                L.gkr_set_early_metadata.argtypes = [i32]
+                L.gkr_set_early_metadata.restype = None
+                L.gkr_get_early_metadata.argtypes, L.gkr_get_early_metadata.restype = [], i32
                 L.gkr_set_insert_stream_min.argtypes = [i64]
                 L.gkr_set_insert_stream_min.restype = None
                 L.gkr_get_insert_stream_min.argtypes, L.gkr_get_insert_stream_min.restype = [], i64
@@ -117,6 +120,17 @@ def set_pdl(enable: bool) -> None:
 
 def get_pdl() -> bool:
     return bool(lib().gkr_get_pdl())
+
+
+def set_early_metadata(enable: bool) -> None:
+    """Let later inserts read slot_mapping / positions, and gathers read indices, before
+    waiting for the kernel ahead of them in the stream (process-wide, default off).  Only
+    for streams where that kernel never writes those arrays."""
+    lib().gkr_set_early_metadata(1 if enable else 0)
+
+
+def get_early_metadata() -> bool:
+    return bool(lib().gkr_get_early_metadata())
 
 
 def set_insert_stream_min(tokens: int) -> None:

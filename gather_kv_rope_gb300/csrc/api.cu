@@ -12,6 +12,7 @@ namespace {
 
 thread_local int32_t g_last_cuda_error = 0;
 std::atomic<int> g_pdl{1};
+std::atomic<int> g_early_metadata{0};
 constexpr int64_t kDefaultStagedMin = 24576;
 constexpr int64_t kDefaultStreamMin = 131072;
 std::atomic<int64_t> g_staged_min{kDefaultStagedMin};
@@ -120,6 +121,10 @@ GKR_API void gkr_set_pdl(int32_t enable) { g_pdl.store(enable ? 1 : 0); }
 
 GKR_API int32_t gkr_get_pdl(void) { return g_pdl.load() ? 1 : 0; }
 
+GKR_API void gkr_set_early_metadata(int32_t enable) { g_early_metadata.store(enable ? 1 : 0); }
+
+GKR_API int32_t gkr_get_early_metadata(void) { return g_early_metadata.load() ? 1 : 0; }
+
 GKR_API void gkr_set_insert_stream_min(int64_t tokens) {
     g_stream_min.store(tokens < 0 ? kDefaultStreamMin : tokens);
 }
@@ -184,6 +189,7 @@ gkr_status prepare_insert(const void* kv, int64_t num_tokens, void* k_cache,
     p->ratio = 1;
     p->fp8_scale = cache->record == 512 ? fp8_scale : nullptr;
     p->err = err_flag;
+    p->early_metadata = g_early_metadata.load(std::memory_order_relaxed);
     return GKR_OK;
 }
 
@@ -267,6 +273,7 @@ GKR_API gkr_status gkr_kv_gather(const void* k_cache, const gkr_cache_desc* cach
     p.out = out;
     p.fp8_scale = cache->record == 512 ? fp8_scale : nullptr;
     p.err = err_flag;
+    p.early_metadata = g_early_metadata.load(std::memory_order_relaxed);
     return cuda_status(launch_gather(cache->record, p, stream));
 }
 
@@ -288,6 +295,6 @@ GKR_API const char* gkr_status_string(gkr_status status) {
 
 GKR_API int32_t gkr_last_cuda_error(void) { return g_last_cuda_error; }
 
-GKR_API int32_t gkr_version(void) { return 20000; }
+GKR_API int32_t gkr_version(void) { return 20100; }
 
 }  // extern "C"

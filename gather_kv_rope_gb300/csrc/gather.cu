@@ -114,13 +114,20 @@ __device__ __forceinline__ void convert_store(const Loaded& r, uint8_t* orow, in
 // offsets are broadcast with shuffles, so each record costs two shuffles, four loads,
 // the dequantisation and two stores.  Short-lived warps (U records each) keep many
 // warps resident and let the block scheduler balance the end of a large gather.
-template <int kRecord, int U>
+template <int kRecord, int U, bool kEarly>
 __global__ void __launch_bounds__(kThreads, kRecord == 584 ? 6 : 8)
     gather_kernel(const GatherParams p) {
-    pdl_wait_previous();
-    pdl_release_next();
     const int lane = threadIdx.x & 31;
     const int64_t i0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * U;
+    // lane u < U decodes index i0 + u; with early metadata (gkr_set_early_metadata, the
+    // kEarly instantiation) the index is read before waiting for the previous kernel,
+    // every other access after
+    int32_t idx = -1;
+    if constexpr (kEarly) {
+        if (lane < U && i0 + lane < p.num_indices) idx = __ldg(p.indices + i0 + lane);
+    }
+    pdl_wait_previous();
+    pdl_release_next();
     if (i0 >= p.num_indices) return;  // warp-uniform
 
     // fp8 rows: the cache's scale, read once per warp; not a positive finite number ->
@@ -133,12 +140,12 @@ __global__ void __launch_bounds__(kThreads, kRecord == 584 ? 6 : 8)
         if (scale_bad && lane == 0) report(p.err, kErrScale);
     }
 
-    // lane u < U decodes index i0 + u: data-row offset (-1 = emit zeros), scale-row offset
+    // data-row offset (-1 = emit zeros), scale-row offset
     int64_t off = -1, soff = 0;
     bool bad = false;
     if (lane < U && i0 + lane < p.num_indices && !scale_bad) {
         using R = Fmt<kRecord>;
-        const int32_t idx = __ldg(p.indices + i0 + lane);
+        if constexpr (!kEarly) idx = __ldg(p.indices + i0 + lane);
         if (idx >= 0 && idx < p.num_slots) {
             const uint32_t s = static_cast<uint32_t>(idx);
             const uint32_t bs = static_cast<uint32_t>(p.block_size);
@@ -171,7 +178,9 @@ cudaError_t launch(const GatherParams& p, cudaStream_t stream) {
     if (p.num_indices <= 0) return cudaSuccess;
     const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * U;
     const int64_t blocks = (p.num_indices + per_block - 1) / per_block;
-    return launch_kernel(gather_kernel<kRecord, U>, blocks, kThreads, 0, stream, p);
+    return p.early_metadata != 0
+               ? launch_kernel(gather_kernel<kRecord, U, true>, blocks, kThreads, 0, stream, p)
+               : launch_kernel(gather_kernel<kRecord, U, false>, blocks, kThreads, 0, stream, p);
 }
 
 }  // namespace

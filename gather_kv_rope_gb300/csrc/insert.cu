@@ -325,6 +325,15 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
     cp_async_wait<0>();
 }
 
+// Slot and position of token t.  With early metadata (gkr_set_early_metadata) the kernels
+// below read them before waiting for the previous kernel in the stream; all other reads
+// and every write come after the wait.
+__device__ __forceinline__ void load_slot_position(const InsertParams& p, int64_t t,
+                                                   int64_t& slot, int64_t& q) {
+    slot = __ldg(p.slots + t);
+    q = __ldg(p.positions + t);
+}
+
 // Short-lived warps for small and medium inserts: one warp per U consecutive tokens,
 // lanes 0..U-1 decode them in parallel, all loads (kv rows and cos/sin rows) go
 // straight to registers before the first token is encoded.  Below a few hundred
@@ -336,23 +345,24 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
 template <int kRecord, int U>
 __global__ void __launch_bounds__(kThreads, GKR_SHORT_MIN_BLOCKS)
     insert_short_kernel(const InsertParams p) {
-    pdl_wait_previous();
-    pdl_release_next();
     const int lane = threadIdx.x & 31;
     const int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * U;
     if (t0 >= p.num_tokens) return;  // warp-uniform
+    const bool mine = lane < U && t0 + lane < p.num_tokens;  // lane u decodes token t0 + u
+    int64_t slot = -1, q = 0;
+    if (p.early_metadata != 0 && mine) load_slot_position(p, t0 + lane, slot, q);
+    pdl_wait_previous();
+    pdl_release_next();
+    if (p.early_metadata == 0 && mine) load_slot_position(p, t0 + lane, slot, q);
     Scale scale;
     if (!load_scale<kRecord>(p, lane, scale)) return;  // warp-uniform
     constexpr uint32_t D = Fmt<kRecord>::D;
     constexpr uint32_t S = Fmt<kRecord>::S;
 
-    // lane u < U decodes token t0 + u
     int64_t off = -1, soff = 0;
     int32_t pos = 0;
     uint32_t err = 0;
-    if (lane < U && t0 + lane < p.num_tokens) {
-        const int64_t slot = __ldg(p.slots + t0 + lane);
-        const int64_t q = __ldg(p.positions + t0 + lane);
+    if (mine) {
         if (slot >= p.num_slots) {
             err = 1;
         } else if (slot >= 0) {
@@ -459,12 +469,16 @@ template <int kRecord, int U>
 __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
     insert_staged_kernel(const InsertParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
-    pdl_wait_previous();
-    pdl_release_next();
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
     const int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib) * U;
     if (t0 >= p.num_tokens) return;  // warp-uniform
+    const bool mine = lane < U && t0 + lane < p.num_tokens;  // lane u decodes token t0 + u
+    int64_t slot = -1, q = 0;
+    if (p.early_metadata != 0 && mine) load_slot_position(p, t0 + lane, slot, q);
+    pdl_wait_previous();
+    pdl_release_next();
+    if (p.early_metadata == 0 && mine) load_slot_position(p, t0 + lane, slot, q);
     Scale scale;
     if (!load_scale<kRecord>(p, lane, scale)) return;  // warp-uniform
     constexpr uint32_t D = Fmt<kRecord>::D;
@@ -475,9 +489,7 @@ __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
     int64_t off = -1, soff = 0;
     int32_t pos = 0;
     uint32_t err = 0;
-    if (lane < U && t0 + lane < p.num_tokens) {
-        const int64_t slot = __ldg(p.slots + t0 + lane);
-        const int64_t q = __ldg(p.positions + t0 + lane);
+    if (mine) {
         if (slot >= p.num_slots) {
             err = 1;
         } else if (slot >= 0) {
@@ -604,23 +616,22 @@ template <int kRecord, bool kSanitize>
 __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
     insert_sparse_staged_kernel(const InsertParams p, const int32_t chunk) {
     extern __shared__ __align__(16) uint8_t smem[];
-    pdl_wait_previous();
-    pdl_release_next();
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock * chunk;
     int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib) * chunk;
     if (t0 >= p.num_tokens) return;  // warp-uniform
+    const bool mine = lane < chunk && t0 + lane < p.num_tokens;  // lane i decodes t0 + i
+    int64_t slot = -1, q = 0;
+    if (p.early_metadata != 0 && mine) load_slot_position(p, t0 + lane, slot, q);
+    pdl_wait_previous();
+    pdl_release_next();
+    if (p.early_metadata == 0 && mine) load_slot_position(p, t0 + lane, slot, q);
 
     const float* const csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
     uint8_t* const ring_lane = smem + wib * (kSparseBatch * kSlotBytes) + 16 * lane;
     uint8_t* const cache_a = p.cache + 8 * lane;
     uint8_t* const cache_s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
-    int64_t slot = -1, q = 0;
-    if (lane < chunk && t0 + lane < p.num_tokens) {
-        slot = __ldg(p.slots + t0 + lane);
-        q = __ldg(p.positions + t0 + lane);
-    }
     while (true) {
         int64_t off = -1, soff = 0;
         int32_t row = 0;

@@ -22,6 +22,7 @@ struct InsertParams {
     int64_t ratio;             // compress ratio >= 1 (1 for the plain insert)
     const float* fp8_scale;    // fp8 rows (record 512): the cache's scale; else unused
     int32_t* err;              // nullable
+    int32_t early_metadata;    // 1: slots / positions may be read before the PDL wait
 };
 
 // Validated arguments of one gather launch.
@@ -35,6 +36,7 @@ struct GatherParams {
     void* out;                 // bf16 [num_indices, 512]
     const float* fp8_scale;    // fp8 rows (record 512): the cache's scale; else unused
     int32_t* err;              // nullable
+    int32_t early_metadata;    // 1: indices may be read before the PDL wait
 };
 
 // Row geometry of the four cache formats ("record" = bytes a token occupies):

@@ -26,7 +26,7 @@ def test_header_declares_the_boundary():
             "gkr_status_string", "gkr_last_cuda_error", "gkr_version", "gkr_set_pdl",
             "gkr_get_pdl", "gkr_set_insert_stream_min", "gkr_get_insert_stream_min",
             "gkr_set_insert_staged_min", "gkr_get_insert_staged_min",
-            "gkr_rope_quant_insert"} <= syms
+            "gkr_rope_quant_insert", "gkr_set_early_metadata", "gkr_get_early_metadata"} <= syms
 
 
 def test_library_exports_every_declared_symbol(gkr):
@@ -58,12 +58,24 @@ def test_page_stride_and_rows(gkr):
     assert gkr.page_stride(1024, 0) == -1
     with pytest.raises(ValueError):
         gkr.record_rows(500)
-    assert gkr.lib().gkr_version() == 20000
+    assert gkr.lib().gkr_version() == 20100
     assert gkr.get_insert_stream_min() == 131072
     assert gkr.get_insert_staged_min() == 24576
     assert gkr.insert_kernel_for(16384) == "insert_short_kernel"
     assert gkr.insert_kernel_for(65536) == "insert_staged_kernel"
     assert gkr.insert_kernel_for(262144) == "insert_kernel"
+
+
+def test_early_metadata_setting_round_trips(gkr):
+    assert gkr.get_early_metadata() is False               # off by default
+    try:
+        gkr.set_early_metadata(True)
+        assert gkr.get_early_metadata() is True
+        gkr.lib().gkr_set_early_metadata(7)                # any non-zero value means on
+        assert gkr.lib().gkr_get_early_metadata() == 1
+    finally:
+        gkr.set_early_metadata(False)
+    assert gkr.get_early_metadata() is False
     gkr.set_insert_stream_min(5)
     gkr.set_insert_staged_min(3)
     assert gkr.get_insert_stream_min() == 5 and gkr.get_insert_staged_min() == 3

@@ -44,6 +44,8 @@ def test_bench_prints_one_json_line_with_the_contract_keys():
     assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] == 16384 * 1024
     assert e["value"] < d["value"]                       # host copies inside the step
     assert d["gpu_launches"] == 2 * d["steps"]
+    em = d["early_metadata"]
+    assert em["value"] > 0 and abs(em["value"] * em["ms_per_step"] * 1e-3 / 16384 - 1) < 1e-6
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     for k in ("insert", "gather"):
         kk = d["kernels"][k]
