@@ -52,12 +52,16 @@ def up_to_date() -> bool:
 def build(force: bool = False, verbose_ptxas: bool = False) -> Path:
     if not force and up_to_date():
         return LIB
-    BUILD.mkdir(parents=True, exist_ok=True)
+    # objects go to a directory of this process, so that concurrent builds (one per rank
+    # of a multi-process launch) never link each other's half-written objects; the
+    # library is replaced atomically
+    objdir = BUILD / f"obj.{os.getpid()}"
+    objdir.mkdir(parents=True, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
 
     def compile_one(src: Path) -> Path:
-        obj = BUILD / (src.stem + ".o")
+        obj = objdir / (src.stem + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", str(src), "-o", str(obj)]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -74,6 +78,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> Path:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    shutil.rmtree(objdir, ignore_errors=True)
     return LIB
 
 
