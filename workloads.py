@@ -244,6 +244,8 @@ WORKLOADS = {
 
 # smaller cases of the same kernels, sized for profiler captures
 PROFILE_WORKLOADS = {
+    "insert_v41_262144": insert_v41_262144,
+    "gather_v41_sparse": gather_v41_sparse,
     "insert_v41_131072": insert_v41_131072,
     "insert_v4_65536": insert_v4_65536,
     "gather_v41_sparse_262144": gather_v41_sparse_262144,
