@@ -2,9 +2,9 @@
 fp8 rows, bf16 rows), every insert kernel (register loads, shared-memory staging,
 streaming ring), the compressed insert (ratios 1-8 and 128, with and without NaN
 sanitising), padded page strides, block sizes, skip rates, value distributions and fp8
-scales; each insert is compared byte for byte with the oracle over the whole
-sentinel-filled backing buffer, then a gather of random indices (valid, -1 and out of
-range) bit for bit."""
+scales, with early metadata reads on or off; each insert is compared byte for byte with
+the oracle over the whole sentinel-filled backing buffer, then a gather of random indices
+(valid, -1 and out of range) bit for bit."""
 from __future__ import annotations
 
 import numpy as np
@@ -34,7 +34,8 @@ def _config(seed: int) -> dict:
         compressed=compressed, ratio=int(rng.choice([1, 2, 3, 4, 8, 128])) if compressed else 1,
         sanitize=bool(rng.random() < 0.5) if compressed else False,
         scale=float(np.float32(2.0 ** rng.uniform(-10, 10))) if record == 512 else None,
-        max_pos=int(rng.choice([64, 1000, 5000])))
+        max_pos=int(rng.choice([64, 1000, 5000])),
+        early=bool(rng.random() < 0.5))      # drawn last: the earlier draws are unchanged
 
 
 @pytest.mark.parametrize("seed", range(48))
@@ -43,6 +44,7 @@ def test_random_configuration_matches_oracle(gkr, oracle_mod, seed):
     staged_min, stream_min = {"short": (BIG, BIG), "staged": (0, BIG), "stream": (BIG, 0)}[c["mode"]]
     gkr.set_insert_staged_min(staged_min)
     gkr.set_insert_stream_min(stream_min)
+    gkr.set_early_metadata(c["early"])
     try:
         case = W.random_insert(f"fuzz{seed}", c["T"], 528, c["bs"], c["pages"], c["max_pos"],
                                c["skip"], seed=seed, dist=c["dist"], outlier_rate=c["outliers"])
@@ -83,3 +85,4 @@ def test_random_configuration_matches_oracle(gkr, oracle_mod, seed):
     finally:
         gkr.set_insert_staged_min(-1)
         gkr.set_insert_stream_min(-1)
+        gkr.set_early_metadata(False)
