@@ -12,13 +12,18 @@ Prints ONE JSON line on rank 0:
              barrier and a device synchronise on both sides, timed with CUDA events on
              the launching stream (max over ranks); six input sets (~300 MB together,
              more than the 126 MB L2) rotate so no step finds its inputs in L2;
+  early_metadata  the same graph with set_early_metadata(True) (reported beside value);
   roofline   the dominant kernel's algorithmic bytes over its mean launch time, timed as
              back-to-back launches of that kernel alone in a graph over the same sets,
              against the measured HBM copy bandwidth; DRAM traffic from the recorded ncu
-             capture while the kernel sources are unchanged;
+             capture while the kernel sources are unchanged; torch's elementwise kernel
+             moving the same bytes, for scale;
+  kernels    both kernels back to back, with event nodes around them, and alone after an
+             L2 flush;
   e2e        the same step through the public API from pinned host memory, uploads,
-             kernels and downloads pipelined on three streams (serial figure beside it);
-  sweep      kernel-only times of the larger workloads (N = 1);
+             kernels and downloads pipelined on three streams (serial and copies-only
+             figures beside it);
+  sweep      kernel-only times of the other workloads (N = 1);
   cpu_baseline  the CPU oracle on one core and on every core (N = 1);
   clocks     nvidia-smi samples during the timed region.
 
