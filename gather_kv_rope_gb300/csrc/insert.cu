@@ -205,9 +205,19 @@ __device__ __forceinline__ bool load_scale(const InsertParams& p, int lane, Scal
 // offsets in the cache of its data row (-1 when the token is skipped or invalid) and
 // of its scale row, and its position.  Invalid slots and positions set GKR_ERR_SLOT /
 // GKR_ERR_POS (one atomic per group at most).
+// Slot and position of token t.  With early metadata (gkr_set_early_metadata) the kernels
+// below read them before waiting for the previous kernel in the stream; all other reads
+// and every write come after the wait.
+__device__ __forceinline__ void load_slot_position(const InsertParams& p, int64_t t,
+                                                   int64_t& slot, int64_t& q) {
+    slot = __ldg(p.slots + t);
+    q = __ldg(p.positions + t);
+}
+
 template <int kRecord>
 __device__ __forceinline__ void decode_group(const InsertParams& p, const WarpItems& w, int g,
-                                             int lane, int64_t& off, int64_t& soff, int32_t& pos) {
+                                             int lane, int64_t& off, int64_t& soff, int32_t& pos,
+                                             const int64_t* pre = nullptr) {
     constexpr uint32_t D = Fmt<kRecord>::D;
     constexpr uint32_t S = Fmt<kRecord>::S;
     const int i = 32 * g + lane;
@@ -216,8 +226,8 @@ __device__ __forceinline__ void decode_group(const InsertParams& p, const WarpIt
     pos = 0;
     int32_t err = 0;
     if (i < w.n) {
-        const int64_t slot = __ldg(p.slots + w.at(i));
-        const int64_t q = __ldg(p.positions + w.at(i));
+        const int64_t slot = pre != nullptr ? pre[0] : __ldg(p.slots + w.at(i));
+        const int64_t q = pre != nullptr ? pre[1] : __ldg(p.positions + w.at(i));
         if (slot >= p.num_slots) {
             err = 1;
         } else if (slot >= 0) {
@@ -264,12 +274,15 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
                                                                           const WorkMap m) {
     static_assert((S & (S - 1)) == 0 && S >= 2 && S <= 16, "ring depth: power of two <= 16");
     extern __shared__ __align__(16) uint8_t smem[];
-    pdl_wait_previous();
-    pdl_release_next();
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
     const WarpItems w = warp_items(m, static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib);
     if (w.n <= 0) return;  // warp-uniform
+    int64_t pre[2] = {-1, 0};  // slot and position of this lane's token in the first group
+    if (p.early_metadata != 0 && lane < w.n) load_slot_position(p, w.at(lane), pre[0], pre[1]);
+    pdl_wait_previous();
+    pdl_release_next();
+    if (p.early_metadata == 0 && lane < w.n) load_slot_position(p, w.at(lane), pre[0], pre[1]);
     Scale scale;
     if (!load_scale<kRecord>(p, lane, scale)) return;  // warp-uniform
     const int n = w.n;
@@ -283,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
     // lane i of cur describes token 32*g + i of the group being processed; nxt the next
     int64_t cur_off, nxt_off, cur_soff, nxt_soff;
     int32_t cur_pos, nxt_pos;
-    decode_group<kRecord>(p, w, 0, lane, cur_off, cur_soff, cur_pos);
+    decode_group<kRecord>(p, w, 0, lane, cur_off, cur_soff, cur_pos, pre);
     decode_group<kRecord>(p, w, 1, lane, nxt_off, nxt_soff, nxt_pos);
 
 #pragma unroll
@@ -323,15 +336,6 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
         }
     }
     cp_async_wait<0>();
-}
-
-// Slot and position of token t.  With early metadata (gkr_set_early_metadata) the kernels
-// below read them before waiting for the previous kernel in the stream; all other reads
-// and every write come after the wait.
-__device__ __forceinline__ void load_slot_position(const InsertParams& p, int64_t t,
-                                                   int64_t& slot, int64_t& q) {
-    slot = __ldg(p.slots + t);
-    q = __ldg(p.positions + t);
 }
 
 // Short-lived warps for small and medium inserts: one warp per U consecutive tokens,
