@@ -35,6 +35,28 @@ def test_algorithmic_bytes():
     assert bench.csc_bytes(slots, np.array([3, 2, 6, 5, 10], np.int64), 4) == 0
 
 
+def test_compressed_input_sets_read_shifted_windows():
+    """The sweep's compressed-insert sets: set k reads kv rows k .. k + T - 1 of one buffer
+    (so each set's boundary tokens read other rows) and owns its slots, positions and
+    cache; the number of sets is capped at the ratio."""
+    import torch
+    import bench
+    import workloads as W
+    case = W.compressed_insert("sets", 2, 32, 4, 528, block_size=32, seed=1)
+    T = case.num_tokens
+    sets = bench.compressed_sets(case, "cpu", 1000)           # 320 MB / 1000 B > R: R sets
+    assert len(sets) == 4
+    kv0 = torch.from_numpy(case.kv.view(np.int16))
+    for k, s in enumerate(sets):
+        assert s["kv"].shape == (T, 512)
+        assert s["kv"].data_ptr() - sets[0]["kv"].data_ptr() == k * 1024
+        assert torch.equal(s["kv"][: T - k].view(torch.int16), kv0[k:])
+        assert torch.equal(s["kv"][T - k:].view(torch.int16), kv0[:k])
+    for key in ("slots", "pos", "cache"):
+        assert len({s[key].data_ptr() for s in sets}) == 4
+    assert len(bench.compressed_sets(case, "cpu", 400_000_000)) == 1
+
+
 def _free_port() -> int:
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
