@@ -134,9 +134,10 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch recorded from an ncu capture (profiles/ncu_traffic.txt),
-    or None when absent or taken on a different kernel source."""
+def ncu_record(kernel: str, workload: str):
+    """The line of profiles/ncu_traffic.txt recorded from an ncu capture of `kernel` on
+    `workload` (DRAM bytes per launch, and the serialised launch time where recorded), or
+    None when absent or taken on a different kernel source."""
     f = ROOT / "profiles" / "ncu_traffic.txt"
     if not f.exists():
         return None
@@ -145,8 +146,27 @@ def ncu_traffic(kernel: str, workload: str):
         kv = dict(p.split("=", 1) for p in line.split() if "=" in p)
         if kv.get("kernel") == kernel and kv.get("workload") == workload \
                 and kv.get("source_hash") == src:
-            return int(kv["dram_bytes_per_launch"])
+            return kv
     return None
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture, or None."""
+    kv = ncu_record(kernel, workload)
+    return None if kv is None else int(kv["dram_bytes_per_launch"])
+
+
+def ncu_dram_rate(kernel: str, workload: str, peak: float):
+    """DRAM bytes over the serialised, cold launch time of a full-size ncu capture, as
+    GB/s and as a fraction of the measured peak; None when not recorded."""
+    kv = ncu_record(kernel, workload)
+    if kv is None or "ncu_us" not in kv:
+        return None
+    b, us = int(kv["dram_bytes_per_launch"]), float(kv["ncu_us"])
+    return {"dram_bytes": b, "us": us, "gbs": b / (us * 1e-6) / 1e9,
+            "frac_of_peak": b / (us * 1e-6) / 1e9 / peak,
+            "what": "ncu DRAM read + write bytes of one launch over its duration, serialised "
+                    "with cold caches (profiles/ncu_traffic.txt)"}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -682,7 +702,8 @@ def sweep(device, peak):
         res[name] = {"kernel": "insert", "us": ms * 1e3, "tokens_per_s": case.num_tokens / (ms * 1e-3),
                      "alg_bytes": b, "alg_gbs": b / (ms * 1e-3) / 1e9,
                      "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
-                     "csc_bytes": csc_bytes(case.slots, case.positions)}
+                     "csc_bytes": csc_bytes(case.slots, case.positions),
+                     "ncu": ncu_dram_rate(gkr.insert_kernel_for(case.num_tokens), name, peak)}
         res[f"stream_same_bytes_as_{name}"] = stream_same_bytes(torch, device, b, peak)
         del sets
         torch.cuda.empty_cache()
@@ -774,7 +795,9 @@ def sweep(device, peak):
         res[name] = {"kernel": "gather", "record": record, "us": ms * 1e3,
                      "indices_per_s": case.indices.size / (ms * 1e-3), "alg_bytes": b,
                      "alg_gbs": b / (ms * 1e-3) / 1e9,
-                     "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
+                     "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+                     "ncu": ncu_dram_rate("gather_kernel", "gather_v41_sparse", peak)
+                     if record == 528 else None}
         del cache
         torch.cuda.empty_cache()
     return res
