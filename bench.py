@@ -8,10 +8,13 @@ come back as zeros) into bf16 [16384, 512].  Metric: tokens per second.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints ONE JSON line on rank 0:
-  value      K steps run as replays of a captured CUDA graph of G steps, bracketed by a
-             barrier and a device synchronise on both sides, timed with CUDA events on
-             the launching stream (max over ranks); six input sets (~300 MB together,
-             more than the 126 MB L2) rotate so no step finds its inputs in L2;
+  value      exactly K steps per timed region, as replays of captured CUDA graphs of at
+             most 60 steps; consecutive regions fill at least 0.3 s (CUDA events around
+             each region on the launching stream, a barrier and a device synchronise on
+             both sides of the whole timed span); value = K steps over the median region
+             (max over ranks), `timing` gives the spread; six input sets (~300 MB
+             together, more than the 126 MB L2) rotate across steps and regions so no
+             step finds its inputs in L2;
   early_metadata  the same graph with set_early_metadata(True) (reported beside value);
   roofline   the dominant kernel's algorithmic bytes over its mean launch time, timed as
              back-to-back launches of that kernel alone in a graph over the same sets,
@@ -56,7 +59,27 @@ METRIC = "KV insert+gather tokens/s and HBM GB/s (% of GB300 peak) at 1 GPU"
 WORKLOAD = "roundtrip_v41_16384"
 FALLBACK_HBM_GBS = 6800.0
 ROTATE = 6            # input sets rotated through the steps
-GRAPH_STEPS = 60      # steps per captured graph (a multiple of ROTATE)
+GRAPH_STEPS = 60      # steps per captured graph at most (a multiple of ROTATE)
+REGION_SECONDS = 0.3  # the timed regions together last at least this long
+MAX_REGIONS = 20000
+
+
+# the arithmetic type the path computes in: bf16 inputs are widened exactly to fp32, the
+# rotation and the scale decision run on fp32 values, e4m3 codes are cast from fp32; the
+# storage types of every stage are listed beside it
+DTYPE = "fp32"
+DTYPES = {"arithmetic": "fp32", "kv_in": "bf16", "cos_sin": "fp32",
+          "record": "e4m3 codes + ue8m0 scales (528 B)", "gather_out": "bf16"}
+
+
+def workload_config(case) -> dict:
+    """The workload of a bench line: the same dict for both arms (the GPU kernels and the
+    CPU oracle run the same step over the same inputs)."""
+    return {"workload": WORKLOAD, "record": case.record, "tokens": int(case.num_tokens),
+            "block_size": case.block_size, "num_pages": case.num_pages,
+            "gathered": int(case.indices.size),
+            "l2": f"GPU arm: inputs larger than L2 ({ROTATE} input sets rotated through the "
+                  "steps, ~300 MB together)"}
 
 
 # ----------------------------------------------------------------------------- setup
@@ -389,11 +412,53 @@ def stream_same_bytes(torch, device, nbytes: int, peak: float, replays: int = 5)
             "l2": "rotating buffer pairs touching more than 320 MB"}
 
 
-def roundtrip_graph(torch, gkr, case, sets, device, events=None):
-    """The timed launch configuration: GRAPH_STEPS steps over the rotating input sets in
-    one CUDA graph (with event nodes around every kernel when `events` is given)."""
+def roundtrip_graph(torch, gkr, case, sets, device, events=None, n: int = GRAPH_STEPS,
+                    offset: int = 0):
+    """The timed launch configuration: n steps over the rotating input sets in one CUDA
+    graph, step k on set (offset + k) % len(sets) (with event nodes around every kernel
+    when `events` is given)."""
     return capture_steps(torch, device, lambda k: step(
-        gkr, case, sets[k % len(sets)], None if events is None else events[k]), GRAPH_STEPS)
+        gkr, case, sets[(offset + k) % len(sets)], None if events is None else events[k]), n)
+
+
+class TimedRegion:
+    """Exactly K steps of the hot path, as replays of captured graphs of at most
+    GRAPH_STEPS steps (whole graphs, then one graph of the remainder).  Global step j runs
+    on input set j % ROTATE, and consecutive regions continue the rotation, so no step
+    finds its inputs in L2 however K divides.  Graphs are captured once per (first set,
+    length)."""
+
+    def __init__(self, torch, gkr, case, sets, device, K: int):
+        self.torch, self.gkr, self.case, self.sets, self.device = torch, gkr, case, sets, device
+        self.K = K
+        self.G = min(K, GRAPH_STEPS)
+        self.graphs = {}
+        self.next_step = 0
+
+    def _graph(self, offset: int, n: int):
+        key = (offset % len(self.sets), n)
+        if key not in self.graphs:
+            self.graphs[key] = roundtrip_graph(self.torch, self.gkr, self.case, self.sets,
+                                               self.device, n=n, offset=key[0])
+        return self.graphs[key]
+
+    def prepare(self, regions: int) -> None:
+        """Capture every graph that `regions` consecutive regions replay."""
+        j = self.next_step
+        for _ in range(regions):
+            for n in self.pieces():
+                self._graph(j, n)
+                j += n
+
+    def pieces(self):
+        q, rem = divmod(self.K, self.G)
+        return [self.G] * q + ([rem] if rem else [])
+
+    def run(self) -> None:
+        """Enqueue one region (K steps); no host synchronisation."""
+        for n in self.pieces():
+            self._graph(self.next_step, n).replay()
+            self.next_step += n
 
 
 def time_roundtrip(args, device, dist):
@@ -409,9 +474,22 @@ def time_roundtrip(args, device, dist):
     torch.cuda.synchronize(device)
 
     G = GRAPH_STEPS
-    K = max(G, (args.steps + G - 1) // G * G)       # K is rounded up to whole graphs
-    replays = K // G
-    graph = roundtrip_graph(torch, gkr, case, sets, device)     # the timed graph
+    K = max(1, args.steps)                          # exactly the requested steps
+    region = TimedRegion(torch, gkr, case, sets, device, K)
+    # one region, untimed, sizes the number of regions timed: enough to fill
+    # REGION_SECONDS (and at least 3), so the clock sampler sees the timed work
+    region.prepare(ROTATE)
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    region.run()
+    b.record()
+    torch.cuda.synchronize(device)
+    one = max(a.elapsed_time(b), 1e-3)
+    repeats = int(min(MAX_REGIONS, max(3, -(-REGION_SECONDS * 1e3 // one))))
+    repeats = int(reduce_max(float(repeats), dist))  # every rank times the same regions
+    region.prepare(repeats)
+    graph = roundtrip_graph(torch, gkr, case, sets, device)     # G steps (supplementary timings)
     external = _supports_external_events(torch)
     kev = None
     if external:                                    # same steps with event nodes per kernel
@@ -420,27 +498,37 @@ def time_roundtrip(args, device, dist):
 
     sampler = ClockSampler(_gpu_id(torch, device)).start()
     stream = torch.cuda.current_stream(device)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(repeats)]
     barrier(dist)
     torch.cuda.synchronize(device)
     h0 = time.time()
-    e0.record(stream)
-    for _ in range(replays):
-        graph.replay()
-    e1.record(stream)
+    for e0, e1 in evs:                              # back to back: no host sync between regions
+        e0.record(stream)
+        region.run()
+        e1.record(stream)
     torch.cuda.synchronize(device)
     h1 = time.time()
     barrier(dist)
     sampler.stop()
-    total_ms = e0.elapsed_time(e1)
-    total_ms_max = reduce_max(total_ms, dist)
+    region_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    total_ms_max = reduce_max(statistics.median(region_ms), dist)
+    spread = {"regions": repeats, "steps_per_region": K,
+              "median_ms": statistics.median(region_ms), "min_ms": min(region_ms),
+              "max_ms": max(region_ms),
+              "p10_ms": float(np.percentile(region_ms, 10)),
+              "p90_ms": float(np.percentile(region_ms, 90)),
+              "timed_region_s": h1 - h0,
+              "what": f"{repeats} consecutive timed regions of exactly {K} steps each (graph "
+                      f"replays: {len(region.pieces())} per region), CUDA events around each "
+                      "region; value uses the median region (max over ranks)"}
 
     # the same step with early metadata reads (set_early_metadata): the slot lists,
     # positions and indices are inputs that no kernel of the step writes
     gkr.set_early_metadata(True)
     try:
         graph_em = roundtrip_graph(torch, gkr, case, sets, device)
-        n_em = max(1, replays // 4)
+        n_em = 100
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(device)
         a.record(stream)
@@ -499,7 +587,7 @@ def time_roundtrip(args, device, dist):
             ev.append((e0, e1))
         torch.cuda.synchronize(device)
         flushed[name] = statistics.median(x.elapsed_time(y) for x, y in ev)
-    return dict(case=case, K=K, total_ms=total_ms_max, em_ms=em_ms, ins_ms=b2b["insert"],
+    return dict(case=case, K=K, total_ms=total_ms_max, spread=spread, em_ms=em_ms, ins_ms=b2b["insert"],
                 gat_ms=b2b["gather"], ins_iso_ms=float(np.mean(ins)),
                 gat_iso_ms=float(np.mean(gat)), ins_flushed_ms=flushed["insert"],
                 gat_flushed_ms=flushed["gather"],
@@ -693,6 +781,8 @@ def sweep(device, peak):
     del sets
     torch.cuda.empty_cache()
 
+    res["floor"] = launch_floors(torch, gkr, W, device, timed)
+
     for name, n_sets in (("insert_v4_65536", 3), ("insert_v41_262144", 1)):
         case = getattr(W, name)()
         sets = device_sets(case, device, n_sets)
@@ -801,6 +891,40 @@ def sweep(device, peak):
         del cache
         torch.cuda.empty_cache()
     return res
+
+
+def launch_floors(torch, gkr, W, device, timed) -> dict:
+    """What a launch costs before its row traffic, timed like every kernel here (back to
+    back in a CUDA graph, programmatic dependent launch on): a 1-token insert and a
+    1-index gather, with the token skipped / the index -1 (the launch, the wait for the
+    previous kernel and one dependent load of the slot or index) and valid (plus the
+    dependent row loads and the stores); and the 16384-token insert of the benchmark step
+    with every slot -1 (the whole grid's slot and position round trip, no row traffic)."""
+    case = W.roundtrip_v41_16384()
+    out = {}
+    for label, slot in (("skipped", -1), ("valid", int(case.slots[case.slots >= 0][0]))):
+        one = W.InsertCase("one", 528, 64, case.num_pages, case.kv[:1].copy(),
+                           np.array([slot], np.int64), case.positions[:1].copy(), case.csc)
+        one.indices = one.slots.astype(np.int32)
+        sets = device_sets(one, device, 1)
+        ms = timed(lambda s: gkr.kv_insert(s["kv"], s["cache"], s["slots"], s["pos"],
+                                           s["csc"], 64, 528), sets)
+        out[f"insert_1_token_{label}_us"] = ms * 1e3
+        ms = timed(lambda s: gkr.kv_gather(s["cache"], s["idx"], s["out"]), sets)
+        out[f"gather_1_index_{label}_us"] = ms * 1e3
+        del sets
+    skip = W.InsertCase("skip", 528, 64, case.num_pages, case.kv, np.full_like(case.slots, -1),
+                        case.positions, case.csc)
+    sets = device_sets(skip, device, ROTATE)
+    ms = timed(lambda s: gkr.kv_insert(s["kv"], s["cache"], s["slots"], s["pos"], s["csc"],
+                                       64, 528), sets)
+    out["insert_16384_tokens_all_skipped_us"] = ms * 1e3
+    del sets
+    torch.cuda.empty_cache()
+    out["what"] = ("launch floors, back to back in a CUDA graph with programmatic dependent "
+                   "launch: 1-token inserts / 1-index gathers (skipped or valid) and the "
+                   "benchmark step's 16384-token insert with every slot -1")
+    return out
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -965,9 +1089,8 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "record": 528, "block_size": 64, "num_pages": 512,
-                       "tokens_per_step": tokens},
+            "vs_baseline": None, "dtype": DTYPE, "dtypes": DTYPES, "data": "synthetic",
+            "config": workload_config(case),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": how, "cpu_model": _cpu_model(), "single_core": single},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -1090,11 +1213,9 @@ def main(argv=None):
 
     out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
-           "config": {"workload": WORKLOAD, "record": 528, "tokens": T, "block_size": 64,
-                      "num_pages": 512, "gathered": int(case.indices.size),
-                      "l2": f"inputs larger than L2: {ROTATE} rotating input sets",
-                      "launch": f"CUDA graph of {GRAPH_STEPS} steps, replayed {K // GRAPH_STEPS}x"},
+           "scaling": "weak", "vs_baseline": None, "dtype": DTYPE, "dtypes": DTYPES,
+           "data": "synthetic", "config": workload_config(case),
+           "timing": r["spread"],
            "early_metadata": {"value": world * T / (r["em_ms"] * 1e-3), "unit": "tokens/s",
                               "ms_per_step": r["em_ms"],
                               "what": "the same step with set_early_metadata(True): the "
@@ -1103,7 +1224,11 @@ def main(argv=None):
                                       "default; valid here, no kernel of the step writes "
                                       "them)"},
            "roofline": roofline, "kernels": kern, "gpu_launches": 2 * K * world,
-           "gpu_launches_per_rank": 2 * K, "clocks": r["clocks"]}
+           "gpu_launches_per_rank": 2 * K,
+           "gpu_launches_note": "launches of this library's kernels per timed region of K "
+                                "steps (one insert and one gather per step); "
+                                f"{r['spread']['regions']} such regions were timed",
+           "clocks": r["clocks"]}
     out["e2e"] = time_e2e(args, device, case, dist)            # every rank, max over ranks
     if rank == 0:
         if not args.no_sweep and world == 1:

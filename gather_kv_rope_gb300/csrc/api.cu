@@ -167,9 +167,10 @@ gkr_status prepare_insert(const void* kv, int64_t num_tokens, void* k_cache,
     RecordRows rows;
     const gkr_status st = check_cache(cache, &rows);
     if (st != GKR_OK) return st;
-    if (num_tokens < 0 || max_pos <= 0 || max_pos > INT64_C(0x7FFFFFFF)) return GKR_EINVAL;
+    if (num_tokens < 0) return GKR_EINVAL;
     p->num_tokens = num_tokens;
-    if (num_tokens == 0) return GKR_OK;
+    if (num_tokens == 0) return GKR_OK;  // the descriptor is checked; nothing else is read
+    if (max_pos <= 0 || max_pos > INT64_C(0x7FFFFFFF)) return GKR_EINVAL;
     if (!kv || !k_cache || !slot_mapping || !positions || !cos_sin_cache) return GKR_EINVAL;
     const bool fp8 = cache->record == 512;  // fp8_scale is read for fp8 rows only
     if (fp8 && !fp8_scale) return GKR_EINVAL;

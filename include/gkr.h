@@ -131,7 +131,8 @@ GKR_API gkr_status gkr_record_rows(int32_t record, int32_t *data_row_bytes,
  *   NaN, e.g. inf * 0), are outside the contract here (see gkr_rope_quant_insert).
  *
  * kv             device, bf16 [num_tokens, 512] row-major, 16-byte aligned; read only.
- * num_tokens     >= 0; 0 enqueues nothing (other pointers may then be NULL).
+ * num_tokens     >= 0; 0 enqueues nothing: *cache is still validated, every other
+ *                argument is ignored (pointers may be NULL, max_pos any value).
  * k_cache        device, the cache described by *cache, 16-byte aligned; only the
  *                data and scale rows of the slots written are modified.
  * cache          host pointer to the geometry (read during the call only).
@@ -194,7 +195,8 @@ GKR_API gkr_status gkr_rope_quant_insert(const void *kv, int64_t num_tokens, voi
  * k_cache      device, the cache described by *cache, 16-byte aligned; read only.
  * cache        host pointer to the geometry.
  * indices      device, int32 [num_indices].
- * num_indices  >= 0; 0 enqueues nothing.
+ * num_indices  >= 0; 0 enqueues nothing: *cache is still validated, every other
+ *              argument is ignored (pointers may be NULL).
  * out          device, bf16 [num_indices, 512] row-major, 16-byte aligned.
  * fp8_scale    device pointer to one fp32: required for record 512, else ignored.
  * err_flag     device int32 or NULL; GKR_ERR_INDEX / GKR_ERR_SCALE are OR-ed in.

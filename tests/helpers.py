@@ -1,6 +1,9 @@
 """Shared helpers for the GPU parity tests (CUDA path vs oracle on the same inputs)."""
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -60,16 +63,78 @@ def first_mismatch(a: np.ndarray, b: np.ndarray, n: int = 8):
     return d.size, [(int(i), int(a[i]), int(b[i])) for i in d[:n]]
 
 
-def written_mask(case, page_stride: int) -> np.ndarray:
-    """Bytes of the flat cache covered by the records of the valid slots."""
-    D, S = (512, 16) if case.record == 528 else (576, 8)
-    bs = case.block_size
-    m = np.zeros(case.num_pages * page_stride, bool)
-    v = case.slots[case.slots >= 0]
-    page, row = v // bs, v % bs
-    d0 = page * page_stride + row * D
-    s0 = page * page_stride + bs * D + row * S
-    for off, n in ((d0, D), (s0, S)):
-        idx = (off[:, None] + np.arange(n)[None, :]).reshape(-1)
-        m[idx] = True
-    return m
+# ---------------------------------------------------------------- the oracle at full size
+#
+# The C oracle runs without the GIL (ctypes releases it for the call), so a full-size
+# reference is computed by host threads on disjoint token (index) ranges.  Valid slots are
+# distinct, so the ranges write disjoint records of the one shared host cache.
+
+def _ranges(n: int, parts: int):
+    edges = np.linspace(0, n, parts + 1).astype(np.int64)
+    return [(int(a), int(b)) for a, b in zip(edges[:-1], edges[1:]) if b > a]
+
+
+def _threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def oracle_insert_parallel(oracle_mod, kv, cache, record, bs, num_pages, ps, slots, positions,
+                           csc, **kw) -> int:
+    """oracle_mod.insert over every token, split over host threads; returns the OR of the
+    error bits.  kw: compress_ratio, sanitize_nans, fp8_scale."""
+    if kw.get("compress_ratio", 1) == 1:
+        assert_distinct_slots(slots)      # distinct records: the ranges never overlap
+    oracle_mod.e4m3_encode(1.0)        # the oracle fills its e4m3 value table on first use
+
+    def run(r):
+        a, b = r
+        return oracle_mod.insert(kv[a:b], cache, record, bs, num_pages, ps, slots[a:b],
+                                 positions[a:b], csc, **kw)
+    n = _threads()
+    with ThreadPoolExecutor(n) as ex:
+        errs = list(ex.map(run, _ranges(len(slots), 4 * n)))
+    err = 0
+    for e in errs:
+        err |= e
+    return err
+
+
+def oracle_gather_parallel(oracle_mod, cache, record, bs, num_pages, ps, indices, **kw):
+    """oracle_mod.gather over every index, split over host threads: (bf16 bits
+    [*indices.shape, 512] as uint16, error bits).  kw: fp8_scale."""
+    flat = np.ascontiguousarray(indices, dtype=np.int32).reshape(-1)
+    out = np.empty((flat.size, 512), np.uint16)
+
+    def run(r):
+        a, b = r
+        o, e = oracle_mod.gather(cache, record, bs, num_pages, ps, flat[a:b], **kw)
+        out[a:b] = o
+        return e
+    n = _threads()
+    with ThreadPoolExecutor(n) as ex:
+        errs = list(ex.map(run, _ranges(flat.size, 4 * n)))
+    err = 0
+    for e in errs:
+        err |= e
+    return out.reshape(tuple(indices.shape) + (512,)), err
+
+
+_REFERENCE_CACHES = {}
+
+
+def oracle_full_cache(oracle_mod, case, record=None, fill=SENTINEL, **kw):
+    """The oracle's whole cache for a workload (flat uint8, every byte; kept for the
+    session, so the tests that run a workload under several kernels or launch shapes
+    compute it once): (cache, error bits, page stride)."""
+    record = case.record if record is None else record
+    key = (case.name, case.num_tokens, record, fill, tuple(sorted(kw.items())))
+    if key not in _REFERENCE_CACHES:
+        if len(_REFERENCE_CACHES) >= 2:
+            _REFERENCE_CACHES.clear()
+        ps = oracle_mod.page_stride(record, case.block_size)
+        ref = np.full(case.num_pages * ps, fill, np.uint8)
+        err = oracle_insert_parallel(oracle_mod, case.kv, ref, record, case.block_size,
+                                     case.num_pages, ps, case.slots, case.positions, case.csc,
+                                     **kw)
+        _REFERENCE_CACHES[key] = (ref, err, ps)
+    return _REFERENCE_CACHES[key]

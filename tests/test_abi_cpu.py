@@ -132,6 +132,13 @@ def test_insert_argument_checks(gkr):
     assert insert(gkr, d, T=-1) == 1
     assert insert(gkr, d, max_pos=0) == 1
     assert insert(gkr, d, T=0, kv=None, cache=None, slots=None, pos=None, csc=None) == 0
+    # an empty call reads no cos/sin table: max_pos is not checked, the descriptor is
+    assert insert(gkr, d, T=0, max_pos=0, kv=None, cache=None, slots=None, pos=None,
+                  csc=None) == 0
+    assert rq_insert(gkr, d, T=0, max_pos=0, kv=None, cache=None, slots=None, pos=None,
+                     csc=None) == 0
+    assert insert(gkr, desc(gkr, record=500), T=0, max_pos=0) == 2
+    assert gather(gkr, desc(gkr, bs=48), N=0, cache=None, idx=None, out=None) == 1
     assert insert(gkr, d, kv=None) == 1
     assert insert(gkr, d, csc=None) == 1
     assert insert(gkr, d, kv=A16 + 8) == 4                           # kv not 16-aligned

@@ -105,3 +105,42 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["config"]["workload"] == "roundtrip_v41_16384"
+    import bench
+    import workloads as W
+    # the same workload dict as the GPU arm's line
+    assert d["config"] == bench.workload_config(W.roundtrip_v41_16384())
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["dtype"] == bench.DTYPE
+
+
+def test_timed_region_runs_exactly_k_steps_and_continues_the_rotation(monkeypatch):
+    """The timed region is K steps (whole graphs of at most GRAPH_STEPS, then the
+    remainder), and region after region the input sets keep rotating: global step j runs
+    on set j % ROTATE whatever K is."""
+    import bench
+    seen = []
+
+    class FakeGraph:
+        def __init__(self, n, offset):
+            self.n, self.offset = n, offset
+
+        def replay(self):
+            seen.extend((self.offset + k) % bench.ROTATE for k in range(self.n))
+
+    captured = []
+
+    def fake_graph(torch, gkr, case, sets, device, events=None, n=bench.GRAPH_STEPS, offset=0):
+        captured.append((offset, n))
+        return FakeGraph(n, offset)
+
+    monkeypatch.setattr(bench, "roundtrip_graph", fake_graph)
+    for K in (1, 20, 60, 61, 125):
+        seen.clear()
+        captured.clear()
+        r = bench.TimedRegion(None, None, None, list(range(bench.ROTATE)), None, K)
+        assert sum(r.pieces()) == K and max(r.pieces()) <= bench.GRAPH_STEPS
+        r.prepare(4)
+        n_captured = len(captured)
+        for _ in range(4):
+            r.run()
+        assert len(captured) == n_captured          # every graph was captured up front
+        assert seen == [j % bench.ROTATE for j in range(4 * K)]

@@ -15,7 +15,7 @@ ROOT = Path(__file__).resolve().parents[1]
 
 
 def test_bench_prints_one_json_line_with_the_contract_keys():
-    steps, warmup = 120, 3
+    steps, warmup = 20, 3                   # not a multiple of the graph length
     r = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--steps", str(steps),
                         "--warmup", str(warmup), "--no-sweep", "--no-cpu-baseline",
                         "--e2e-steps", "10"], capture_output=True, text=True, cwd=ROOT,
@@ -29,7 +29,12 @@ def test_bench_prints_one_json_line_with_the_contract_keys():
                 "roofline", "e2e", "gpu_launches", "clocks"):
         assert key in d, key
     assert d["unit"] == "tokens/s" and d["value"] > 0 and d["higher_is_better"] is True
-    assert d["n_gpus"] == 1 and d["steps"] >= steps and d["steps"] % 60 == 0
+    assert d["n_gpus"] == 1 and d["steps"] == steps        # exactly the requested steps
+    t = d["timing"]
+    assert t["steps_per_region"] == steps and t["regions"] >= 3
+    assert t["min_ms"] <= t["median_ms"] <= t["max_ms"] and t["timed_region_s"] >= 0.25
+    assert abs(d["ms_per_step"] * steps - t["median_ms"]) < 1e-9
+    assert d["clocks"]["samples"] >= 3 and "shorter" not in d["clocks"]["note"]
     assert d["warmup"] == warmup and d["scaling"] == "weak" and d["data"] == "synthetic"
     assert d["config"]["workload"] == "roundtrip_v41_16384"
     # value = tokens per step / seconds per step

@@ -9,7 +9,8 @@ import torch
 
 import workloads as W
 from golden_parse import GOLDEN, load_worked, worked_inputs
-from helpers import SENTINEL, assert_distinct_slots, bf16_from_bits, device_inputs, first_mismatch
+from helpers import (SENTINEL, assert_distinct_slots, bf16_from_bits, device_inputs,
+                     first_mismatch, oracle_full_cache)
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -151,34 +152,22 @@ def test_fp8_scale_is_read_on_the_device_at_replay(gkr, oracle_mod):
         assert first_mismatch(gkr.cache_bytes(cache).cpu().numpy(), ref)[0] == 0
 
 
+@pytest.mark.slow
 @pytest.mark.parametrize("record", [1024, 512])
-def test_plain_cache_full_size_sampled(gkr, oracle_mod, record):
+def test_plain_cache_full_size(gkr, oracle_mod, record):
     """262144 tokens in 8 contiguous sequences (the large-insert layout) into a plain
-    cache: sampled rows against the oracle, every other byte untouched."""
+    cache: every byte of the cache against the oracle's (fp8 at scale 0.01)."""
     case = W.insert_v41_262144()
     scale = 0.01 if record == 512 else None
-    ps = oracle_mod.page_stride(record, 64)
+    kw = {} if scale is None else {"fp8_scale": scale}
+    ref, ref_err, ps = oracle_full_cache(oracle_mod, case, record=record, **kw)
     kv, slots, pos, csc = device_inputs(case, DEV)
-    cache = gkr.alloc_cache(case.num_pages, 64, record, DEV, fill=SENTINEL)
+    cache = gkr.alloc_cache(case.num_pages, 64, record, DEV, page_stride_bytes=ps, fill=SENTINEL)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     gkr.kv_insert(kv, cache, slots, pos, csc, 64, record, err_flag=err, fp8_scale=_scale_t(scale))
-    got = gkr.cache_bytes(cache).cpu().numpy()
-    assert int(err.item()) == 0
-    rng = np.random.default_rng(2)
-    valid = np.nonzero(case.slots >= 0)[0]
-    pick = np.unique(np.concatenate([valid[:4], valid[-4:], rng.choice(valid, 2000, replace=False)]))
-    sub = W.InsertCase("sub", 528, 64, case.num_pages, case.kv[pick], case.slots[pick],
-                       case.positions[pick], case.csc)
-    ref = np.full(case.num_pages * ps, SENTINEL, np.uint8)
-    oracle_mod.insert(sub.kv, ref, record, 64, case.num_pages, ps, sub.slots, sub.positions,
-                      sub.csc, fp8_scale=scale)
-    rows = (case.slots[pick] // 64) * ps + (case.slots[pick] % 64) * record
-    for r in rows:
-        assert np.array_equal(got[r:r + record], ref[r:r + record]), r
-    assert ps == 64 * record                    # no padding: row r of the cache is slot r
-    written = np.zeros(case.num_pages * 64, bool)
-    written[case.slots[valid]] = True
-    assert (got.reshape(-1, record)[~written] == SENTINEL).all()
+    n, first = first_mismatch(gkr.cache_bytes(cache).cpu().numpy(), ref)
+    assert n == 0, f"{n} bytes differ, first {first}"
+    assert int(err.item()) == ref_err == 0
 
 
 @pytest.mark.parametrize("scale", [1e-30, 2.0 ** -64, float(np.nextafter(np.float32(2.0 ** -64), 0)),
