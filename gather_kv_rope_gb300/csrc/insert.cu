@@ -43,8 +43,12 @@ struct TokenLoads {
     float4 c, s;      // cos / sin of the 4 pairs in chunk B (lanes 24..31 only)
 };
 
+// Scale rows go through the warp's shared-memory staging rows (ScaleRows below): the
+// encoders write the token's scale bytes into its staging row `sl`, and the rows of a
+// batch of tokens are stored to the cache together, one lane per row.
+
 // V4.1: 16 blocks of 32 dims.  Chunk A of lane L is in block L/4, chunk B in 8 + L/4.
-// `da` = data row + 8L (chunk B's codes go to da + 256); `sl` = scale row + L/4.
+// `da` = data row + 8L (chunk B's codes go to da + 256); `sl` = staging row + L/4.
 // kSanitize: NaN -> +0 over the whole rotated row before the block maxima.
 template <bool kSanitize = false>
 __device__ __forceinline__ void encode_store_v41(const TokenLoads& L, uint8_t* da, uint8_t* sl,
@@ -75,7 +79,8 @@ __device__ __forceinline__ void encode_store_v41(const TokenLoads& L, uint8_t* d
 
 // V4: 7 blocks of 64 NoPE dims (chunk A of lane L in block L/8; chunk B of lanes 0..23
 // in block 4 + L/8), rotated dims 448..511 (chunk B of lanes 24..31) stored as bf16.
-// `da` = data row + 8L; `sl` = scale row + L/8.
+// `da` = data row + 8L; `sl` = staging row + L/8 (all 8 bytes of the row are written,
+// the pad byte 7 by lane 24).
 template <bool kSanitize = false>
 __device__ __forceinline__ void encode_store_v4(const TokenLoads& L, uint8_t* da, uint8_t* sl,
                                                 int lane) {
@@ -181,6 +186,40 @@ __device__ __forceinline__ void encode_store(const TokenLoads& L, uint8_t* da, u
     else encode_store_fp8(L, da, lane, sc);
 }
 
+// Scale rows of a batch of tokens, staged in the warp's shared memory.  A V4.1 scale row
+// is 16 bytes and a V4 row 8, so 8 (16) rows of consecutive slots fill one 128-byte line
+// of the page's scale region.  Each lane's encoder writes its block's bytes into the
+// token's staging row (two 1-byte shared stores from 8 or 4 lanes); `store` then writes
+// the batch with one instruction: lane l stores row l (16 or 8 bytes) to the cache when
+// its token was written.  Rows of consecutive slots thus leave as whole 32-byte sectors
+// (whole lines for a batch starting on a line), instead of 8-byte pieces, and a token
+// costs no global byte stores.  The plain caches have no scale rows (kRows = 0).
+template <int kRecord>
+struct ScaleRows {
+    static constexpr int S = static_cast<int>(Fmt<kRecord>::S);
+    static constexpr int kRows = S == 0 ? 0 : 128 / S;   // rows per 128-byte line
+    static constexpr int kBytes = S == 0 ? 16 : 128;     // staging bytes per warp
+
+    // Staging row of batch row r, offset to this lane's first byte (block L/4 or L/8).
+    __device__ __forceinline__ static uint8_t* row(uint8_t* warp_rows, int r, int lane) {
+        return warp_rows + r * S + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
+    }
+
+    // Store batch rows 0 .. n-1: lane l < n stores row l at cache + soff when `mine`
+    // (its token was encoded).  Call from all 32 lanes.
+    __device__ __forceinline__ static void store(const uint8_t* warp_rows, uint8_t* cache,
+                                                 int64_t soff, bool mine, int n, int lane) {
+        if constexpr (S != 0) {
+            __syncwarp();                              // the encoders' bytes are visible
+            if (lane < n && mine) {
+                if constexpr (S == 16) st16(cache + soff, lds16(warp_rows + 16 * lane));
+                else st8(cache + soff, lds8(warp_rows + 8 * lane));
+            }
+            __syncwarp();                              // the rows may be reused
+        }
+    }
+};
+
 // The fp8 cache's scale (read once per warp) and its reciprocal; unused for the other
 // formats.  Returns false -- after setting the error bit from lane 0 -- when an fp8 scale
 // is not a positive finite number: the warp then writes nothing.
@@ -274,6 +313,8 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
                                                                           const WorkMap m) {
     static_assert((S & (S - 1)) == 0 && S >= 2 && S <= 16, "ring depth: power of two <= 16");
     extern __shared__ __align__(16) uint8_t smem[];
+    using Rows = ScaleRows<kRecord>;
+    __shared__ __align__(16) uint8_t srows[kWarpsPerBlock][Rows::kBytes];
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
     const WarpItems w = warp_items(m, static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib);
@@ -291,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
     const int32_t kv_step = static_cast<int32_t>(w.step * 1024);
     const float* const csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
     uint8_t* const cache_a = p.cache + Fmt<kRecord>::kLaneBytes * lane;            // lane's row part
-    uint8_t* const cache_s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3)); // scale byte
+    constexpr int B = Rows::kRows > 0 ? Rows::kRows : 1;   // tokens per scale-row batch
 
     // lane i of cur describes token 32*g + i of the group being processed; nxt the next
     int64_t cur_off, nxt_off, cur_soff, nxt_soff;
@@ -326,7 +367,16 @@ __global__ void __launch_bounds__(kThreads, GKR_MIN_BLOCKS) insert_kernel(const 
                 L.c = *reinterpret_cast<const float4*>(src + 1024 - 16 * 24);
                 L.s = *reinterpret_cast<const float4*>(src + 1024 + 128 - 16 * 24);
             }
-            encode_store<kRecord>(L, cache_a + off, cache_s + soff, lane, scale);
+            encode_store<kRecord>(L, cache_a + off, Rows::row(srows[wib], j % B, lane), lane,
+                                  scale);
+        }
+        if constexpr (Rows::kRows > 0) {
+            if (j % B == B - 1 || j == n - 1) {  // store the batch's scale rows (B | 32)
+                const int src = ((j - j % B) & 31) + lane;
+                const int64_t so = __shfl_sync(kFull, cur_soff, src & 31);
+                const bool mine = __shfl_sync(kFull, cur_off, src & 31) >= 0;
+                Rows::store(srows[wib], p.cache, so, mine, j % B + 1, lane);
+            }
         }
         if ((j & 31) == 31) {                   // move to the next group of 32 tokens
             cur_off = nxt_off;
@@ -351,6 +401,8 @@ __global__ void __launch_bounds__(kThreads, GKR_SHORT_MIN_BLOCKS)
     insert_short_kernel(const InsertParams p) {
     const int lane = threadIdx.x & 31;
     const int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * U;
+    using Rows = ScaleRows<kRecord>;
+    __shared__ __align__(16) uint8_t srows[kWarpsPerBlock][Rows::kBytes];
     if (t0 >= p.num_tokens) return;  // warp-uniform
     const bool mine = lane < U && t0 + lane < p.num_tokens;  // lane u decodes token t0 + u
     int64_t slot = -1, q = 0;
@@ -362,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, GKR_SHORT_MIN_BLOCKS)
     if (!load_scale<kRecord>(p, lane, scale)) return;  // warp-uniform
     constexpr uint32_t D = Fmt<kRecord>::D;
     constexpr uint32_t S = Fmt<kRecord>::S;
+    uint8_t* const wrows = srows[threadIdx.x >> 5];
 
     int64_t off = -1, soff = 0;
     int32_t pos = 0;
@@ -405,13 +458,13 @@ __global__ void __launch_bounds__(kThreads, GKR_SHORT_MIN_BLOCKS)
         }
     }
     uint8_t* const cache_a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
-    uint8_t* const cache_s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int64_t o = __shfl_sync(kFull, off, u);
-        const int64_t so = __shfl_sync(kFull, soff, u);
-        if (valid[u]) encode_store<kRecord>(L[u], cache_a + o, cache_s + so, lane, scale);
+        if (valid[u]) encode_store<kRecord>(L[u], cache_a + o, Rows::row(wrows, u, lane), lane,
+                                            scale);
     }
+    Rows::store(wrows, p.cache, soff, off >= 0, U, lane);   // lane u: token t0 + u's row
 }
 
 // ---------------------------------------------------------------- compressed-KV insert
@@ -473,6 +526,8 @@ template <int kRecord, int U>
 __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
     insert_staged_kernel(const InsertParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
+    using Rows = ScaleRows<kRecord>;
+    __shared__ __align__(16) uint8_t srows[kWarpsPerBlock][Rows::kBytes];
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
     const int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib) * U;
@@ -533,11 +588,9 @@ __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
     cp_async_wait<0>();  // this lane's copies have landed; each lane reads only its own
 
     uint8_t* const cache_a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
-    uint8_t* const cache_s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int64_t o = __shfl_sync(kFull, off, u);
-        const int64_t so = __shfl_sync(kFull, soff, u);
         if (o >= 0) {  // warp-uniform
             const uint8_t* src = ring_lane + u * kSlotBytes;
             TokenLoads L;
@@ -547,9 +600,10 @@ __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
                 L.c = *reinterpret_cast<const float4*>(src + 1024 - 16 * 24);
                 L.s = *reinterpret_cast<const float4*>(src + 1024 + 128 - 16 * 24);
             }
-            encode_store<kRecord>(L, cache_a + o, cache_s + so, lane, scale);
+            encode_store<kRecord>(L, cache_a + o, Rows::row(srows[wib], u, lane), lane, scale);
         }
     }
+    Rows::store(srows[wib], p.cache, soff, off >= 0, U, lane);   // lane u: token t0 + u's row
 }
 
 template <int kRecord, int U>
@@ -620,6 +674,9 @@ template <int kRecord, bool kSanitize>
 __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
     insert_sparse_staged_kernel(const InsertParams p, const int32_t chunk) {
     extern __shared__ __align__(16) uint8_t smem[];
+    using Rows = ScaleRows<kRecord>;
+    static_assert(kSparseBatch <= Rows::kRows, "a batch's scale rows fit one staging line");
+    __shared__ __align__(16) uint8_t srows[kWarpsPerBlock][Rows::kBytes];
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock * chunk;
@@ -635,7 +692,6 @@ __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
     const float* const csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
     uint8_t* const ring_lane = smem + wib * (kSparseBatch * kSlotBytes) + 16 * lane;
     uint8_t* const cache_a = p.cache + 8 * lane;
-    uint8_t* const cache_s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
     while (true) {
         int64_t off = -1, soff = 0;
         int32_t row = 0;
@@ -679,7 +735,6 @@ __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
             for (int v = 0; v < kSparseBatch; ++v) {
                 if (u[v] >= 0) {                         // warp-uniform
                     const int64_t o = __shfl_sync(kFull, off, u[v]);
-                    const int64_t so = __shfl_sync(kFull, soff, u[v]);
                     const uint8_t* src = ring_lane + v * kSlotBytes;
                     TokenLoads L;
                     L.a = lds16(src);
@@ -688,10 +743,23 @@ __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
                         L.c = *reinterpret_cast<const float4*>(src + 1024 - 16 * 24);
                         L.s = *reinterpret_cast<const float4*>(src + 1024 + 128 - 16 * 24);
                     }
-                    encode_store<kRecord, kSanitize>(L, cache_a + o, cache_s + so, lane,
+                    encode_store<kRecord, kSanitize>(L, cache_a + o,
+                                                     Rows::row(srows[wib], v, lane), lane,
                                                      Scale{1.0f, 1.0f, false});
                 }
             }
+            // lane v < kSparseBatch stores staged row v, the row of chunk token u[v]
+            int src = 0;
+            bool has = false;
+#pragma unroll
+            for (int v = 0; v < kSparseBatch; ++v) {
+                if (lane == v) {
+                    src = u[v] < 0 ? 0 : u[v];
+                    has = u[v] >= 0;
+                }
+            }
+            Rows::store(srows[wib], p.cache, __shfl_sync(kFull, soff, src), has, kSparseBatch,
+                        lane);
         }
         if (t1 >= p.num_tokens) break;  // warp-uniform
         __syncwarp();  // reconverge before the next chunk's shuffles

@@ -184,6 +184,15 @@ def insert_v41_131072(seed: int = 0) -> InsertCase:
                       cos_sin_table(L), None)
 
 
+def roundtrip_v41_65536(seed: int = 1) -> InsertCase:
+    """65536 tokens with random slots (2048 pages, 5% -> -1) and positions U[0, 8192),
+    N(0,1); the gather list is the slot list: the token count the pages time on GB300,
+    for profiler captures of the insert and of the gather at >= 65536 items."""
+    c = random_insert("roundtrip_v41_65536", 65536, 528, 64, 2048, 8192, 0.05, seed)
+    c.indices = c.slots.astype(np.int32)
+    return c
+
+
 def gather_v41_sparse_262144(seed: int = 0) -> InsertCase:
     """Profiling-size sparse gather: a 262144-token cache (138 MB) and 32 queries x 2048."""
     c = gather_v41_sparse(seed, cache_tokens=1 << 18, queries=32, topk=2048, min_ctx=8192)
@@ -250,5 +259,6 @@ PROFILE_WORKLOADS = {
     "insert_v4_65536": insert_v4_65536,
     "gather_v41_sparse_262144": gather_v41_sparse_262144,
     "roundtrip_v41_16384": roundtrip_v41_16384,
+    "roundtrip_v41_65536": roundtrip_v41_65536,
     "compressed_v41_r4_262144": compressed_v41_r4_262144,
 }
