@@ -40,7 +40,11 @@
  *   [P4] FlashMLA overview, DSA section (index -1 marks an invalid entry).
  *   [P2] section "实现拆解" item 1 also names the two other KV-only cache formats:
  *        a bf16 cache and a plain fp8 e4m3fn cache with one fp32 scale, rows of 512
- *        elements in pages whose stride may be padded.
+ *        elements in pages whose stride may be padded.  The same item says the
+ *        KV-only op is the attention write op with its query inputs (q_in,
+ *        q_head_padded, eps, apply_q_norm) removed; [P1] section "实现拆解" item 3
+ *        and the attention.py listing call that op with q, the padded head count
+ *        and eps beside the KV insert arguments.
  * Readings where the pages are silent (exact scale rule, amax 0 -> byte 0,
  * RNE + saturation, fp32 RoPE op order, V4 page layout, pad byte 0, NaN
  * output pattern, out-of-range handling) are listed in the design notes.
@@ -544,4 +548,110 @@ ORACLE_EXPORT int oracle_kv_gather(const uint8_t *cache, int record, int block_s
 {
     return gather_general(cache, record, block_size, num_pages, page_stride, indices,
                           num_indices, fp8_scale, out);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Fused query-side write ([P1] "实现拆解" item 3; [P2] "实现拆解" item 1)      */
+/* ------------------------------------------------------------------------ */
+
+/* The pages name the op (q norm, q rotation, the KV insert in one call) and its
+ * arguments (q, the padded head count, eps, apply_q_norm) but print neither the
+ * norm nor the q layout.  Reading taken here: q is bf16 [T, H, 512]; each head's
+ * 512 values x are divided by sqrt(mean(x^2) + eps) (an RMS norm without a weight)
+ * when apply_q_norm is set; dims 448..511 are then rotated in adjacent pairs with
+ * the token's cos/sin row, as for the KV row; the result is written as bf16 to
+ * q_out [T, Hp, 512]; heads H .. Hp-1 of q_out are written as +0.  The arithmetic
+ * order inside the norm is not fixed by anything, so the oracle evaluates the
+ * definition in double (every step exact or correctly rounded in binary64), and a
+ * result counts as right when it is one of the two bf16 values around that exact
+ * value (a faithful rounding); the rounded-to-nearest one is returned too. */
+
+/* The bf16 value next to `rn` in the direction of y (rn itself when it equals y).
+ * rn is the nearest-even bf16 of y. */
+static uint16_t bf16_toward(uint16_t rn, double y)
+{
+    double v = oracle_bf16_value(rn);
+    int neg = rn >> 15;
+    int zero = (rn & 0x7FFF) == 0;
+    if (isnan(y) || v == y)
+        return rn;
+    if (v < y) /* the smallest bf16 above v */
+        return zero ? (uint16_t)0x0001 : (uint16_t)(neg ? rn - 1 : rn + 1);
+    return zero ? (uint16_t)0x8001 : (uint16_t)(neg ? rn + 1 : rn - 1);
+}
+
+/* One query head: exact[d] = the normed and rotated value of dim d (double);
+ * rn[d] = its nearest-even bf16, alt[d] = the other faithful bf16 (== rn when the
+ * value is a bf16).  eps >= 0; a zero row with eps = 0 is outside the contract. */
+ORACLE_EXPORT void oracle_q_head(const uint16_t *q_row, const float *csc_row, double eps,
+                                 int apply_norm, double exact[512], uint16_t rn[512],
+                                 uint16_t alt[512])
+{
+    double x[512], r = 1.0, ss = 0.0;
+    int d, j;
+    for (d = 0; d < 512; d++)
+        x[d] = oracle_bf16_value(q_row[d]);
+    if (apply_norm) {
+        for (d = 0; d < 512; d++)
+            ss += x[d] * x[d];
+        r = 1.0 / sqrt(ss / 512.0 + eps);
+        for (d = 0; d < 512; d++)
+            x[d] *= r;
+    }
+    for (j = 0; j < 32; j++) {
+        double e = x[448 + 2 * j], o = x[449 + 2 * j];
+        double c = csc_row[j], s = csc_row[32 + j];
+        x[448 + 2 * j] = e * c - o * s;
+        x[449 + 2 * j] = o * c + e * s;
+    }
+    for (d = 0; d < 512; d++) {
+        exact[d] = x[d];
+        rn[d] = oracle_bf16_encode(x[d]);
+        alt[d] = bf16_toward(rn[d], x[d]);
+    }
+}
+
+/* The fused op: for every token t (slot and position checks as the KV insert, but the
+ * query side needs only the position):
+ *   position outside [0, max_pos): ORACLE_ERR_POS; the token's query heads are
+ *     written as +0 (rn = alt = 0) and its KV row is not inserted;
+ *   otherwise heads h < num_heads are written by oracle_q_head, heads
+ *     num_heads .. num_heads_padded - 1 as +0;
+ *   the KV row is inserted exactly as oracle_kv_insert does (slot < 0 skips it).
+ * q_rn / q_alt: uint16 [T, num_heads_padded, 512].  Returns the error bits, or -1
+ * for an unknown record width. */
+ORACLE_EXPORT int oracle_qnorm_rope_kv_insert(const uint16_t *q_in, int num_heads,
+                                              int num_heads_padded, double eps,
+                                              int apply_norm, uint16_t *q_rn,
+                                              uint16_t *q_alt, const uint16_t *kv,
+                                              int64_t num_tokens, uint8_t *cache, int record,
+                                              int block_size, int64_t num_pages,
+                                              int64_t page_stride, const int64_t *slots,
+                                              const int64_t *positions, const float *csc,
+                                              int64_t max_pos, float fp8_scale)
+{
+    int64_t t;
+    int h, err;
+    double exact[512];
+    err = insert_general(kv, num_tokens, cache, record, block_size, num_pages, page_stride,
+                         slots, positions, csc, max_pos, 1, 0, fp8_scale);
+    if (err < 0)
+        return err;
+    for (t = 0; t < num_tokens; t++) {
+        int64_t pos = positions[t];
+        for (h = 0; h < num_heads_padded; h++) {
+            uint16_t *rn = q_rn + (t * num_heads_padded + h) * 512;
+            uint16_t *alt = q_alt + (t * num_heads_padded + h) * 512;
+            if (h >= num_heads || pos < 0 || pos >= max_pos) {
+                memset(rn, 0, 512 * sizeof(uint16_t));
+                memset(alt, 0, 512 * sizeof(uint16_t));
+                continue;
+            }
+            oracle_q_head(q_in + (t * num_heads + h) * 512, csc + pos * 64, eps, apply_norm,
+                          exact, rn, alt);
+        }
+        if (num_heads > 0 && (pos < 0 || pos >= max_pos))
+            err |= ORACLE_ERR_POS;
+    }
+    return err;
 }
