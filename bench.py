@@ -15,7 +15,7 @@ Prints ONE JSON line on rank 0:
              (max over ranks), `timing` gives the spread; six input sets (~300 MB
              together, more than the 126 MB L2) rotate across steps and regions so no
              step finds its inputs in L2;
-  early_metadata  the same graph with set_early_metadata(True) (reported beside value);
+  early_metadata  the same graph with the early_metadata launch option (beside value);
   roofline   the dominant kernel's algorithmic bytes over its mean launch time, timed as
              back-to-back launches of that kernel alone in a graph over the same sets,
              against the measured HBM copy bandwidth; DRAM traffic from the recorded ncu
@@ -292,6 +292,14 @@ def csc_bytes(slots: np.ndarray, positions: np.ndarray, ratio: int = 1) -> int:
     return 256 * int(np.unique(positions[w] + 1 - ratio).size)
 
 
+def qside_bytes(slots: np.ndarray, record: int, num_heads: int, num_heads_padded: int) -> int:
+    """Algorithmic bytes of one fused attention write: the KV insert's bytes plus, per
+    token, the query heads read (num_heads x 1024 B) and written (num_heads_padded x
+    1024 B, padded heads included)."""
+    T = int(np.asarray(slots).size)
+    return insert_bytes(slots, record) + T * 1024 * (num_heads + num_heads_padded)
+
+
 def gather_bytes(indices: np.ndarray, record: int) -> int:
     """Algorithmic bytes of one gather: 4 B index + 1024 B bf16 row written per
     index, plus the record read for every valid index."""
@@ -523,10 +531,9 @@ def time_roundtrip(args, device, dist):
                       f"replays: {len(region.pieces())} per region), CUDA events around each "
                       "region; value uses the median region (max over ranks)"}
 
-    # the same step with early metadata reads (set_early_metadata): the slot lists,
+    # the same step with early metadata reads (the early_metadata launch option): the slot lists,
     # positions and indices are inputs that no kernel of the step writes
-    gkr.set_early_metadata(True)
-    try:
+    with gkr.launch_policy(early_metadata=True):
         graph_em = roundtrip_graph(torch, gkr, case, sets, device)
         n_em = 100
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -538,8 +545,6 @@ def time_roundtrip(args, device, dist):
         torch.cuda.synchronize(device)
         em_ms = reduce_max(a.elapsed_time(b) / (n_em * G), dist)
         del graph_em
-    finally:
-        gkr.set_early_metadata(False)
 
     # per-kernel durations: the event graph (each kernel bracketed by event nodes, so
     # no launch overlap between kernels) replayed right after the timed region, or an
@@ -865,6 +870,29 @@ def sweep(device, peak):
             "tokens_per_s": case.num_tokens / (ms * 1e-3), "alg_bytes": b,
             "alg_gbs": b / (ms * 1e-3) / 1e9, "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
             "csc_bytes": csc_bytes(case.slots, case.positions)}
+        del sets
+        torch.cuda.empty_cache()
+
+    # the fused attention write (query heads normed and rotated, padded heads zeroed, the
+    # KV rows inserted into the V4.1 cache): a decode batch (256 tokens x 128 heads) and a
+    # prefill chunk (8192 tokens x 16 heads padded to 64), random slots and positions
+    for name, T, H, Hp in (("qnorm_rope_kv_insert_decode_256x128", 256, 128, 128),
+                           ("qnorm_rope_kv_insert_prefill_8192x16p64", 8192, 16, 64)):
+        case = W.random_insert(name, T, 528, 64, 2 * T // 64 + 2, 8192, 0.05, seed=3)
+        b = qside_bytes(case.slots, 528, H, Hp)
+        sets = device_sets(case, device, int(max(1, -(-320_000_000 // b))))
+        g = torch.Generator(device="cpu").manual_seed(0)
+        for st in sets:
+            st["q"] = torch.randn(T, H, 512, generator=g).to(torch.bfloat16).to(device)
+            st["q_out"] = torch.empty(T, Hp, 512, dtype=torch.bfloat16, device=device)
+        ms = timed(lambda st: gkr.qnorm_rope_kv_insert(
+            st["q"], st["kv"], st["cache"], st["slots"], st["pos"], st["csc"], Hp, 1e-6, 64,
+            True, q_out=st["q_out"]), sets)
+        res[name] = {"kernel": "qnorm_rope_kv_insert", "tokens": T, "heads": H,
+                     "heads_padded": Hp, "us": ms * 1e3, "tokens_per_s": T / (ms * 1e-3),
+                     "alg_bytes": b, "alg_gbs": b / (ms * 1e-3) / 1e9,
+                     "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+                     "l2": f"{len(sets)} rotating input sets"}
         del sets
         torch.cuda.empty_cache()
 
@@ -1218,7 +1246,7 @@ def main(argv=None):
            "timing": r["spread"],
            "early_metadata": {"value": world * T / (r["em_ms"] * 1e-3), "unit": "tokens/s",
                               "ms_per_step": r["em_ms"],
-                              "what": "the same step with set_early_metadata(True): the "
+                              "what": "the same step with the early_metadata launch option: the "
                                       "kernels read slot_mapping, positions and indices "
                                       "before waiting for the kernel ahead of them (off by "
                                       "default; valid here, no kernel of the step writes "

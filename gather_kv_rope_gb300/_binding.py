@@ -7,6 +7,8 @@ the library is not built, or a tensor is not on a CUDA device, the call raises.
 """
 from __future__ import annotations
 
+import contextlib
+import contextvars
 import ctypes
 import threading
 from pathlib import Path
@@ -48,6 +50,58 @@ class CacheDesc(ctypes.Structure):
                 ("num_pages", ctypes.c_int64), ("page_stride", ctypes.c_int64)]
 
 
+class LaunchOpts(ctypes.Structure):
+    """gkr_launch_opts: per-call launch options; -1 = the process-wide default."""
+    _fields_ = [("pdl", ctypes.c_int32), ("early_metadata", ctypes.c_int32),
+                ("insert_staged_min", ctypes.c_int64), ("insert_stream_min", ctypes.c_int64)]
+
+    def __init__(self, pdl=None, early_metadata=None, insert_staged_min=None,
+                 insert_stream_min=None):
+        def flag(v):
+            return -1 if v is None else int(bool(v))
+
+        def count(v):
+            return -1 if v is None else int(v)
+        super().__init__(flag(pdl), flag(early_metadata), count(insert_staged_min),
+                         count(insert_stream_min))
+
+    def merged(self, other: "LaunchOpts | None") -> "LaunchOpts":
+        """These options with every field that `other` sets taken from `other`."""
+        out = LaunchOpts()
+        for name, _ in self._fields_:
+            v = getattr(other, name) if other is not None else -1
+            setattr(out, name, v if v != -1 else getattr(self, name))
+        return out
+
+
+# Launch options of the calls made in the current thread / context (launch_policy), so
+# that concurrent users of the library never change each other's launches.
+_POLICY: contextvars.ContextVar = contextvars.ContextVar("gkr_launch_policy", default=None)
+
+
+@contextlib.contextmanager
+def launch_policy(**fields):
+    """Within the block, calls from this thread (context) pass these launch options
+    (pdl, early_metadata, insert_staged_min, insert_stream_min) to the library, on top
+    of any enclosing launch_policy; an explicit launch_opts= argument wins over both."""
+    cur = _POLICY.get()
+    new = (cur or LaunchOpts()).merged(LaunchOpts(**fields))
+    token = _POLICY.set(new)
+    try:
+        yield new
+    finally:
+        _POLICY.reset(token)
+
+
+def _opts(launch_opts):
+    """The options pointer of a call: launch_opts over the context's launch_policy."""
+    cur = _POLICY.get()
+    if launch_opts is not None and not isinstance(launch_opts, LaunchOpts):
+        raise ValueError("launch_opts must be a LaunchOpts")
+    eff = launch_opts if cur is None else cur.merged(launch_opts)
+    return None if eff is None else ctypes.byref(eff)
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -70,16 +124,23 @@ def lib() -> ctypes.CDLL:
                 L.gkr_page_stride.argtypes, L.gkr_page_stride.restype = [i32, i32], i64
                 L.gkr_record_rows.argtypes = [i32, vp, vp, vp]
                 L.gkr_record_rows.restype = ctypes.c_int
-                # kv, T, k_cache, desc, slots, positions, csc, max_pos, fp8_scale, err, stream
+                opt = ctypes.POINTER(LaunchOpts)
+                # kv, T, k_cache, desc, slots, positions, csc, max_pos, fp8_scale, err, opts,
+                # stream
                 L.gkr_kv_insert.argtypes = [vp, i64, vp, ctypes.POINTER(CacheDesc), vp, vp, vp, i64,
-                                            vp, vp, vp]
+                                            vp, vp, opt, vp]
                 L.gkr_kv_insert.restype = ctypes.c_int
                 L.gkr_rope_quant_insert.argtypes = [vp, i64, vp, ctypes.POINTER(CacheDesc), vp,
-                                                    vp, vp, i64, i32, i32, vp, vp]
+                                                    vp, vp, i64, i32, i32, vp, opt, vp]
                 L.gkr_rope_quant_insert.restype = ctypes.c_int
                 L.gkr_kv_gather.argtypes = [vp, ctypes.POINTER(CacheDesc), vp, i64, vp, vp, vp,
-                                            vp]
+                                            opt, vp]
                 L.gkr_kv_gather.restype = ctypes.c_int
+                # q_in, H, Hp, q_out, eps, apply_q_norm, then gkr_kv_insert's arguments
+                L.gkr_qnorm_rope_kv_insert.argtypes = [vp, i32, i32, vp, ctypes.c_float, i32, vp,
+                                                       i64, vp, ctypes.POINTER(CacheDesc), vp, vp,
+                                                       vp, i64, vp, vp, opt, vp]
+                L.gkr_qnorm_rope_kv_insert.restype = ctypes.c_int
                 L.gkr_status_string.argtypes, L.gkr_status_string.restype = [ctypes.c_int], \
                     ctypes.c_char_p
                 L.gkr_last_cuda_error.argtypes, L.gkr_last_cuda_error.restype = [], i32
@@ -153,10 +214,15 @@ def get_insert_staged_min() -> int:
 
 
 def insert_kernel_for(num_tokens: int) -> str:
-    """Name of the kernel kv_insert launches for `num_tokens` under the current policy."""
-    if num_tokens < get_insert_stream_min():
-        return "insert_short_kernel" if num_tokens < get_insert_staged_min() else \
-            "insert_staged_kernel"
+    """Name of the kernel kv_insert launches for `num_tokens` under the current policy
+    (the process defaults, overridden by the context's launch_policy)."""
+    cur = _POLICY.get()
+    stream_min = get_insert_stream_min() if cur is None or cur.insert_stream_min < 0 \
+        else cur.insert_stream_min
+    staged_min = get_insert_staged_min() if cur is None or cur.insert_staged_min < 0 \
+        else cur.insert_staged_min
+    if num_tokens < stream_min:
+        return "insert_short_kernel" if num_tokens < staged_min else "insert_staged_kernel"
     return "insert_kernel"
 
 
@@ -285,7 +351,8 @@ def _insert_args(kv, k_cache, slot_mapping, positions, cos_sin_cache, block_size
 def kv_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: torch.Tensor,
               positions: torch.Tensor, cos_sin_cache: torch.Tensor, block_size: int,
               record: int | None = None, err_flag: torch.Tensor | None = None,
-              fp8_scale: torch.Tensor | None = None) -> None:
+              fp8_scale: torch.Tensor | None = None,
+              launch_opts: LaunchOpts | None = None) -> None:
     """RoPE + MXFP8 quantise + paged insert, in place into k_cache.
 
     kv             bf16 [tokens, 512], contiguous; not modified.
@@ -299,6 +366,7 @@ def kv_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: torch.Tenso
     err_flag       optional int32 device tensor; error bits are OR-ed into element 0.
     fp8_scale      float32 device tensor of one element: required for an fp8 cache
                    (stored codes are e4m3(x / scale)), None otherwise.
+    launch_opts    this call's LaunchOpts (over the context's launch_policy), or None.
     """
     desc, T, dev = _insert_args(kv, k_cache, slot_mapping, positions, cos_sin_cache,
                                 block_size, record, err_flag)
@@ -310,14 +378,15 @@ def kv_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: torch.Tenso
         st = lib().gkr_kv_insert(_ptr(kv), T, _ptr(k_cache), ctypes.byref(desc),
                                  _ptr(slot_mapping), _ptr(positions), _ptr(cos_sin_cache),
                                  cos_sin_cache.shape[0], _ptr(fp8_scale), _ptr(err_flag),
-                                 stream)
+                                 _opts(launch_opts), stream)
     _raise(st)
 
 
 def rope_quant_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: torch.Tensor,
                       positions: torch.Tensor, cos_sin_cache: torch.Tensor, block_size: int,
                       compress_ratio: int = 1, sanitize_nans: bool = False,
-                      record: int | None = None, err_flag: torch.Tensor | None = None) -> None:
+                      record: int | None = None, err_flag: torch.Tensor | None = None,
+                      launch_opts: LaunchOpts | None = None) -> None:
     """Compressed-KV insert, in place into k_cache: a token is written only when
     (position + 1) % compress_ratio == 0, rotated with the cos/sin row of its group's
     first position (position // compress_ratio * compress_ratio); with sanitize_nans
@@ -333,13 +402,14 @@ def rope_quant_insert(kv: torch.Tensor, k_cache: torch.Tensor, slot_mapping: tor
                                          _ptr(slot_mapping), _ptr(positions),
                                          _ptr(cos_sin_cache), cos_sin_cache.shape[0],
                                          int(compress_ratio), 1 if sanitize_nans else 0,
-                                         _ptr(err_flag), stream)
+                                         _ptr(err_flag), _opts(launch_opts), stream)
     _raise(st)
 
 
 def kv_gather(k_cache: torch.Tensor, indices: torch.Tensor, out: torch.Tensor,
               err_flag: torch.Tensor | None = None,
-              fp8_scale: torch.Tensor | None = None) -> torch.Tensor:
+              fp8_scale: torch.Tensor | None = None,
+              launch_opts: LaunchOpts | None = None) -> torch.Tensor:
     """Dequantise the records at `indices` into `out` (bf16 [*indices.shape, 512]).
     An index of -1 writes zeros.  An fp8 cache needs its fp8_scale.  Returns out."""
     desc = _cache_desc(k_cache)
@@ -355,6 +425,46 @@ def kv_gather(k_cache: torch.Tensor, indices: torch.Tensor, out: torch.Tensor,
         stream = torch.cuda.current_stream(dev).cuda_stream
         st = lib().gkr_kv_gather(_ptr(k_cache), ctypes.byref(desc), _ptr(indices),
                                  indices.numel(), _ptr(out), _ptr(fp8_scale), _ptr(err_flag),
-                                 stream)
+                                 _opts(launch_opts), stream)
     _raise(st)
     return out
+
+
+def qnorm_rope_kv_insert(q: torch.Tensor, kv: torch.Tensor, k_cache: torch.Tensor,
+                         slot_mapping: torch.Tensor, positions: torch.Tensor,
+                         cos_sin_cache: torch.Tensor, num_heads_padded: int, eps: float,
+                         block_size: int, apply_q_norm: bool = True,
+                         q_out: torch.Tensor | None = None, record: int | None = None,
+                         err_flag: torch.Tensor | None = None,
+                         fp8_scale: torch.Tensor | None = None,
+                         launch_opts: LaunchOpts | None = None) -> torch.Tensor:
+    """The fused attention write: each query head of q (bf16 [T, H, 512]) divided by
+    sqrt(mean(q^2) + eps) when apply_q_norm, dims 448..511 rotated with the token's
+    cos/sin row, written as bf16 to q_out [T, num_heads_padded, 512] (padded heads +0),
+    and the KV rows inserted into k_cache exactly as kv_insert does, in one launch.
+    q_out may be q itself when num_heads_padded == H.  Returns q_out (allocated when
+    None).  The other arguments are kv_insert's."""
+    _check(q.dtype == torch.bfloat16 and q.dim() == 3 and q.shape[2] == HEAD_DIM
+           and q.is_contiguous(), "q must be a contiguous bf16 tensor [tokens, heads, 512]")
+    desc, T, dev = _insert_args(kv, k_cache, slot_mapping, positions, cos_sin_cache,
+                                block_size, record, err_flag)
+    _check_fp8_scale(desc, fp8_scale)
+    H, Hp = int(q.shape[1]), int(num_heads_padded)
+    _check(q.shape[0] >= T, "q has fewer tokens than slot_mapping")
+    _check(Hp >= H, "num_heads_padded must be at least q.shape[1]")
+    if q_out is None:
+        q_out = torch.empty(T, Hp, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    _check(q_out.dtype == torch.bfloat16 and q_out.is_contiguous() and q_out.dim() == 3
+           and q_out.shape[0] >= T and q_out.shape[1] == Hp and q_out.shape[2] == HEAD_DIM,
+           "q_out must be a contiguous bf16 tensor [tokens, num_heads_padded, 512]")
+    _same_cuda_device(kv, q, q_out, fp8_scale)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        st = lib().gkr_qnorm_rope_kv_insert(_ptr(q), H, Hp, _ptr(q_out), float(eps),
+                                            1 if apply_q_norm else 0, _ptr(kv), T, _ptr(k_cache),
+                                            ctypes.byref(desc), _ptr(slot_mapping),
+                                            _ptr(positions), _ptr(cos_sin_cache),
+                                            cos_sin_cache.shape[0], _ptr(fp8_scale),
+                                            _ptr(err_flag), _opts(launch_opts), stream)
+    _raise(st)
+    return q_out

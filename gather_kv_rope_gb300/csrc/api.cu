@@ -15,6 +15,7 @@ std::atomic<int> g_pdl{1};
 std::atomic<int> g_early_metadata{0};
 constexpr int64_t kDefaultStagedMin = 24576;
 constexpr int64_t kDefaultStreamMin = 131072;
+constexpr int32_t kMaxQHeads = 4096;   // query heads per token (padded) at most
 std::atomic<int64_t> g_staged_min{kDefaultStagedMin};
 std::atomic<int64_t> g_stream_min{kDefaultStreamMin};
 
@@ -75,15 +76,33 @@ gkr_status cuda_status(cudaError_t e) {
     return GKR_ECUDA;
 }
 
+// The launch policy of one call: the process-wide defaults (gkr_set_*), overridden by
+// the fields of `o` that are not -1.  GKR_EINVAL for any other negative value, or a
+// flag other than -1, 0 or 1.
+struct Policy {
+    int32_t pdl, early_metadata;
+    int64_t staged_min, stream_min;
+};
+
+gkr_status resolve_policy(const gkr_launch_opts* o, Policy* out) {
+    out->pdl = g_pdl.load(std::memory_order_relaxed);
+    out->early_metadata = g_early_metadata.load(std::memory_order_relaxed);
+    out->staged_min = g_staged_min.load(std::memory_order_relaxed);
+    out->stream_min = g_stream_min.load(std::memory_order_relaxed);
+    if (o == nullptr) return GKR_OK;
+    if (o->pdl < -1 || o->pdl > 1 || o->early_metadata < -1 || o->early_metadata > 1 ||
+        o->insert_staged_min < -1 || o->insert_stream_min < -1)
+        return GKR_EINVAL;
+    if (o->pdl >= 0) out->pdl = o->pdl;
+    if (o->early_metadata >= 0) out->early_metadata = o->early_metadata;
+    if (o->insert_staged_min >= 0) out->staged_min = o->insert_staged_min;
+    if (o->insert_stream_min >= 0) out->stream_min = o->insert_stream_min;
+    return GKR_OK;
+}
+
 }  // namespace
 
 namespace gkr {
-
-bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
-
-int64_t insert_stream_min() { return g_stream_min.load(std::memory_order_relaxed); }
-
-int64_t insert_staged_min() { return g_staged_min.load(std::memory_order_relaxed); }
 
 cudaError_t resident_warps(const void* func, int threads, size_t smem, int64_t* warps) {
     int dev = 0;
@@ -158,14 +177,18 @@ GKR_API gkr_status gkr_record_rows(int32_t record, int32_t* data_row_bytes,
 
 namespace {
 
-// Checks shared by both insert entry points; fills `p` on success.  A GKR_OK status
+// Checks shared by the insert entry points; fills `p` on success.  A GKR_OK status
 // with p.num_tokens == 0 means there is nothing to launch.
 gkr_status prepare_insert(const void* kv, int64_t num_tokens, void* k_cache,
                           const gkr_cache_desc* cache, const int64_t* slot_mapping,
                           const int64_t* positions, const float* cos_sin_cache, int64_t max_pos,
-                          const float* fp8_scale, int32_t* err_flag, gkr::InsertParams* p) {
+                          const float* fp8_scale, int32_t* err_flag,
+                          const gkr_launch_opts* opts, gkr::InsertParams* p) {
     RecordRows rows;
-    const gkr_status st = check_cache(cache, &rows);
+    gkr_status st = check_cache(cache, &rows);
+    if (st != GKR_OK) return st;
+    Policy pol;
+    st = resolve_policy(opts, &pol);
     if (st != GKR_OK) return st;
     if (num_tokens < 0) return GKR_EINVAL;
     p->num_tokens = num_tokens;
@@ -190,7 +213,10 @@ gkr_status prepare_insert(const void* kv, int64_t num_tokens, void* k_cache,
     p->ratio = 1;
     p->fp8_scale = cache->record == 512 ? fp8_scale : nullptr;
     p->err = err_flag;
-    p->early_metadata = g_early_metadata.load(std::memory_order_relaxed);
+    p->early_metadata = pol.early_metadata;
+    p->pdl = pol.pdl;
+    p->staged_min = pol.staged_min;
+    p->stream_min = pol.stream_min;
     return GKR_OK;
 }
 
@@ -220,11 +246,11 @@ GKR_API gkr_status gkr_kv_insert(const void* kv, int64_t num_tokens, void* k_cac
                                  const gkr_cache_desc* cache, const int64_t* slot_mapping,
                                  const int64_t* positions, const float* cos_sin_cache,
                                  int64_t max_pos, const float* fp8_scale, int32_t* err_flag,
-                                 cudaStream_t stream) {
+                                 const gkr_launch_opts* opts, cudaStream_t stream) {
     gkr::InsertParams p;
     const gkr_status st = prepare_insert(kv, num_tokens, k_cache, cache, slot_mapping,
                                          positions, cos_sin_cache, max_pos, fp8_scale, err_flag,
-                                         &p);
+                                         opts, &p);
     if (st != GKR_OK || p.num_tokens == 0) return st;
     return cuda_status(launch_insert(cache->record, p, stream));
 }
@@ -234,13 +260,14 @@ GKR_API gkr_status gkr_rope_quant_insert(const void* kv, int64_t num_tokens, voi
                                          const int64_t* slot_mapping, const int64_t* positions,
                                          const float* cos_sin_cache, int64_t max_pos,
                                          int32_t compress_ratio, int32_t sanitize_nans,
-                                         int32_t* err_flag, cudaStream_t stream) {
+                                         int32_t* err_flag, const gkr_launch_opts* opts,
+                                         cudaStream_t stream) {
     if (compress_ratio < 1 || (sanitize_nans != 0 && sanitize_nans != 1)) return GKR_EINVAL;
     if (cache != nullptr && !packed(cache->record)) return GKR_EUNSUPPORTED_RECORD;
     gkr::InsertParams p;
     const gkr_status st = prepare_insert(kv, num_tokens, k_cache, cache, slot_mapping,
                                          positions, cos_sin_cache, max_pos, nullptr, err_flag,
-                                         &p);
+                                         opts, &p);
     if (st != GKR_OK || p.num_tokens == 0) return st;
     p.ratio = compress_ratio;
     const bool san = sanitize_nans != 0;
@@ -251,9 +278,12 @@ GKR_API gkr_status gkr_rope_quant_insert(const void* kv, int64_t num_tokens, voi
 GKR_API gkr_status gkr_kv_gather(const void* k_cache, const gkr_cache_desc* cache,
                                  const int32_t* indices, int64_t num_indices, void* out,
                                  const float* fp8_scale, int32_t* err_flag,
-                                 cudaStream_t stream) {
+                                 const gkr_launch_opts* opts, cudaStream_t stream) {
     RecordRows rows;
-    const gkr_status st = check_cache(cache, &rows);
+    gkr_status st = check_cache(cache, &rows);
+    if (st != GKR_OK) return st;
+    Policy pol;
+    st = resolve_policy(opts, &pol);
     if (st != GKR_OK) return st;
     if (num_indices < 0) return GKR_EINVAL;
     if (num_indices == 0) return GKR_OK;
@@ -274,8 +304,41 @@ GKR_API gkr_status gkr_kv_gather(const void* k_cache, const gkr_cache_desc* cach
     p.out = out;
     p.fp8_scale = cache->record == 512 ? fp8_scale : nullptr;
     p.err = err_flag;
-    p.early_metadata = g_early_metadata.load(std::memory_order_relaxed);
+    p.early_metadata = pol.early_metadata;
+    p.pdl = pol.pdl;
     return cuda_status(launch_gather(cache->record, p, stream));
+}
+
+GKR_API gkr_status gkr_qnorm_rope_kv_insert(const void* q_in, int32_t num_heads,
+                                            int32_t num_heads_padded, void* q_out, float eps,
+                                            int32_t apply_q_norm, const void* kv,
+                                            int64_t num_tokens, void* k_cache,
+                                            const gkr_cache_desc* cache,
+                                            const int64_t* slot_mapping,
+                                            const int64_t* positions,
+                                            const float* cos_sin_cache, int64_t max_pos,
+                                            const float* fp8_scale, int32_t* err_flag,
+                                            const gkr_launch_opts* opts,
+                                            cudaStream_t stream) {
+    if (num_heads < 0 || num_heads_padded < num_heads || num_heads_padded > kMaxQHeads ||
+        (apply_q_norm != 0 && apply_q_norm != 1) || !(eps >= 0.0f && eps <= 3.40282347e38f))
+        return GKR_EINVAL;
+    gkr::InsertParams p;
+    const gkr_status st = prepare_insert(kv, num_tokens, k_cache, cache, slot_mapping,
+                                         positions, cos_sin_cache, max_pos, fp8_scale, err_flag,
+                                         opts, &p);
+    if (st != GKR_OK || p.num_tokens == 0) return st;
+    if (num_heads_padded == 0) return cuda_status(launch_insert(cache->record, p, stream));
+    if ((num_heads > 0 && q_in == nullptr) || q_out == nullptr) return GKR_EINVAL;
+    if ((num_heads > 0 && !aligned(q_in, 16)) || !aligned(q_out, 16)) return GKR_EALIGN;
+    gkr::QSideParams qp;
+    qp.q_in = q_in;
+    qp.q_out = q_out;
+    qp.num_heads = num_heads;
+    qp.num_heads_padded = num_heads_padded;
+    qp.eps = eps;
+    qp.apply_norm = apply_q_norm;
+    return cuda_status(gkr::launch_qnorm_rope_kv_insert(cache->record, p, qp, stream));
 }
 
 GKR_API const char* gkr_status_string(gkr_status status) {
@@ -296,6 +359,6 @@ GKR_API const char* gkr_status_string(gkr_status status) {
 
 GKR_API int32_t gkr_last_cuda_error(void) { return g_last_cuda_error; }
 
-GKR_API int32_t gkr_version(void) { return 20100; }
+GKR_API int32_t gkr_version(void) { return 30000; }
 
 }  // extern "C"

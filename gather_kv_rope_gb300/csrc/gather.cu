@@ -179,8 +179,8 @@ cudaError_t launch(const GatherParams& p, cudaStream_t stream) {
     const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * U;
     const int64_t blocks = (p.num_indices + per_block - 1) / per_block;
     return p.early_metadata != 0
-               ? launch_kernel(gather_kernel<kRecord, U, true>, blocks, kThreads, 0, stream, p)
-               : launch_kernel(gather_kernel<kRecord, U, false>, blocks, kThreads, 0, stream, p);
+               ? launch_kernel(gather_kernel<kRecord, U, true>, blocks, kThreads, 0, stream, p.pdl, p)
+               : launch_kernel(gather_kernel<kRecord, U, false>, blocks, kThreads, 0, stream, p.pdl, p);
 }
 
 }  // namespace

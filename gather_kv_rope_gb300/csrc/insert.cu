@@ -22,6 +22,7 @@
 // idled 7 of 8 warps above ~16k tokens; page "PR #56441 [Perf][DSpark] KV-only context
 // insertion across V4.1 cache formats", review notes).
 #include "device.cuh"
+#include "encode.cuh"
 #include "launch.h"
 
 namespace gkr {
@@ -38,212 +39,7 @@ namespace {
 constexpr int kInsertDepth = GKR_INSERT_DEPTH;  // tokens in flight per warp
 constexpr int kSlotBytes = 1024 + 256;          // staged kv row + cos/sin row
 
-struct TokenLoads {
-    uint4 a, b;       // bf16 chunks A and B
-    float4 c, s;      // cos / sin of the 4 pairs in chunk B (lanes 24..31 only)
-};
 
-// Scale rows go through the warp's shared-memory staging rows (ScaleRows below): the
-// encoders write the token's scale bytes into its staging row `sl`, and the rows of a
-// batch of tokens are stored to the cache together, one lane per row.
-
-// V4.1: 16 blocks of 32 dims.  Chunk A of lane L is in block L/4, chunk B in 8 + L/4.
-// `da` = data row + 8L (chunk B's codes go to da + 256); `sl` = staging row + L/4.
-// kSanitize: NaN -> +0 over the whole rotated row before the block maxima.
-template <bool kSanitize = false>
-__device__ __forceinline__ void encode_store_v41(const TokenLoads& L, uint8_t* da, uint8_t* sl,
-                                                 int lane) {
-    float a[8], b[8];
-    unpack_bf16x8(L.a, a);
-    unpack_bf16x8(L.b, b);
-    if (lane >= 24) rope4(b, L.c, L.s);  // dims 448..511 = pairs 4(L-24) .. 4(L-24)+3
-    if (kSanitize) {
-        zero_nans8(a);
-        zero_nans8(b);
-    }
-
-    float ma = amax8(a), mb = amax8(b);
-    ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, 1));
-    mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 1));
-    ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, 2));
-    mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 2));
-    const uint32_t ba = ue8m0_byte(ma), bb = ue8m0_byte(mb);
-
-    st8(da, quantise8(a, ba));
-    st8(da + 256, quantise8(b, bb));
-    if ((lane & 3) == 0) {
-        sl[0] = static_cast<uint8_t>(ba);
-        sl[8] = static_cast<uint8_t>(bb);
-    }
-}
-
-// V4: 7 blocks of 64 NoPE dims (chunk A of lane L in block L/8; chunk B of lanes 0..23
-// in block 4 + L/8), rotated dims 448..511 (chunk B of lanes 24..31) stored as bf16.
-// `da` = data row + 8L; `sl` = staging row + L/8 (all 8 bytes of the row are written,
-// the pad byte 7 by lane 24).
-template <bool kSanitize = false>
-__device__ __forceinline__ void encode_store_v4(const TokenLoads& L, uint8_t* da, uint8_t* sl,
-                                                int lane) {
-    float a[8], b[8];
-    unpack_bf16x8(L.a, a);
-    unpack_bf16x8(L.b, b);
-    const bool rope_lane = lane >= 24;
-    if (rope_lane) rope4(b, L.c, L.s);
-    if (kSanitize) {
-        zero_nans8(a);
-        zero_nans8(b);
-    }
-
-    float ma = amax8(a), mb = rope_lane ? 0.0f : amax8(b);
-#pragma unroll
-    for (int x = 1; x <= 4; x <<= 1) {
-        ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, x));
-        mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, x));
-    }
-    const uint32_t ba = ue8m0_byte(ma), bb = ue8m0_byte(mb);
-
-    st8(da, quantise8(a, ba));
-    if (!rope_lane) {
-        st8(da + 256, quantise8(b, bb));
-    } else {  // dims 448 + 8(L-24) .. as bf16 at data + 448 + 16(L-24) = da + 64 + 8L
-        st16(da + 64 + 8 * lane,
-             make_uint4(pack_bf16x2_rn(b[0], b[1]), pack_bf16x2_rn(b[2], b[3]),
-                        pack_bf16x2_rn(b[4], b[5]), pack_bf16x2_rn(b[6], b[7])));
-    }
-    if ((lane & 7) == 0) {
-        sl[0] = static_cast<uint8_t>(ba);                 // blocks 0..3
-        if (!rope_lane) sl[4] = static_cast<uint8_t>(bb);  // blocks 4..6
-        else sl[4] = 0;                                    // lane 24: L/8 = 3, byte 7 = pad
-    }
-}
-
-// bf16 cache row (1024 B): the row with dims 448..511 rotated, rounded to bf16.  Lane L
-// owns bytes [16L, 16L+16) (chunk A, copied) and [512+16L, 512+16L+16) (chunk B,
-// rotated on lanes 24..31).  `da` = row + 16L.
-__device__ __forceinline__ void encode_store_bf16(const TokenLoads& L, uint8_t* da, int lane) {
-    st16(da, L.a);
-    if (lane < 24) {
-        st16(da + 512, L.b);
-    } else {
-        float b[8];
-        unpack_bf16x8(L.b, b);
-        rope4(b, L.c, L.s);
-        st16(da + 512, make_uint4(pack_bf16x2_rn(b[0], b[1]), pack_bf16x2_rn(b[2], b[3]),
-                                  pack_bf16x2_rn(b[4], b[5]), pack_bf16x2_rn(b[6], b[7])));
-    }
-}
-
-// The fp8 cache's scale s and y = RN(1/s) for the corrected quotient (0: divide);
-// pow2: s is a power of two in [2^-126, 2^126], so y = 1/s exactly and |x| * y is the
-// quotient itself.
-struct Scale {
-    float s, y;
-    bool pow2;
-};
-
-// fp8 row by IEEE divisions: the rare path (a scale outside [2^-64, 2^64]), kept out of
-// line so that the common path keeps its registers.
-__device__ __noinline__ void encode_store_fp8_ieee(uint4 ta, uint4 tb, float4 c, float4 sn,
-                                                   uint8_t* da, int lane, float scale) {
-    float a[8], b[8];
-    unpack_bf16x8(ta, a);
-    unpack_bf16x8(tb, b);
-    if (lane >= 24) rope4(b, c, sn);
-    st8(da, quantise8_ieee_div(a, scale));
-    st8(da + 256, quantise8_ieee_div(b, scale));
-}
-
-// fp8 cache row (512 B): e4m3(x / scale) of the rotated row.  `da` = row + 8L.
-__device__ __forceinline__ void encode_store_fp8(const TokenLoads& L, uint8_t* da, int lane,
-                                                 Scale sc) {
-    if (sc.y == 0.0f) {  // warp-uniform
-        encode_store_fp8_ieee(L.a, L.b, L.c, L.s, da, lane, sc.s);
-        return;
-    }
-    if (sc.pow2) {  // warp-uniform; each branch holds the whole row, so neither is predicated
-        float a[8], b[8];
-        unpack_bf16x8(L.a, a);
-        unpack_bf16x8(L.b, b);
-        if (lane >= 24) rope4(b, L.c, L.s);
-        st8(da, quantise8_pow2(a, sc.y));
-        st8(da + 256, quantise8_pow2(b, sc.y));
-        return;
-    }
-    float a[8], b[8];
-    unpack_bf16x8(L.a, a);
-    unpack_bf16x8(L.b, b);
-    if (lane >= 24) rope4(b, L.c, L.s);
-    st8(da, quantise8_div(a, sc.s, sc.y));
-    st8(da + 256, quantise8_div(b, sc.s, sc.y));
-}
-
-template <int kRecord, bool kSanitize = false>
-__device__ __forceinline__ void encode_store(const TokenLoads& L, uint8_t* da, uint8_t* sl,
-                                             int lane, Scale sc) {
-    if constexpr (kRecord == 528) encode_store_v41<kSanitize>(L, da, sl, lane);
-    else if constexpr (kRecord == 584) encode_store_v4<kSanitize>(L, da, sl, lane);
-    else if constexpr (kRecord == 1024) encode_store_bf16(L, da, lane);
-    else encode_store_fp8(L, da, lane, sc);
-}
-
-// Scale rows of a batch of tokens, staged in the warp's shared memory.  A V4.1 scale row
-// is 16 bytes and a V4 row 8, so 8 (16) rows of consecutive slots fill one 128-byte line
-// of the page's scale region.  Each lane's encoder writes its block's bytes into the
-// token's staging row (two 1-byte shared stores from 8 or 4 lanes); `store` then writes
-// the batch with one instruction: lane l stores row l (16 or 8 bytes) to the cache when
-// its token was written.  Rows of consecutive slots thus leave as whole 32-byte sectors
-// (whole lines for a batch starting on a line), instead of 8-byte pieces, and a token
-// costs no global byte stores.  The plain caches have no scale rows (kRows = 0).
-template <int kRecord>
-struct ScaleRows {
-    static constexpr int S = static_cast<int>(Fmt<kRecord>::S);
-    static constexpr int kRows = S == 0 ? 0 : 128 / S;   // rows per 128-byte line
-    static constexpr int kBytes = S == 0 ? 16 : 128;     // staging bytes per warp
-
-    // Staging row of batch row r, offset to this lane's first byte (block L/4 or L/8).
-    __device__ __forceinline__ static uint8_t* row(uint8_t* warp_rows, int r, int lane) {
-        return warp_rows + r * S + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
-    }
-
-    // Store batch rows 0 .. n-1: lane l < n stores row l at cache + soff when `mine`
-    // (its token was encoded).  Call from all 32 lanes.
-    __device__ __forceinline__ static void store(const uint8_t* warp_rows, uint8_t* cache,
-                                                 int64_t soff, bool mine, int n, int lane) {
-        if constexpr (S != 0) {
-            __syncwarp();                              // the encoders' bytes are visible
-            if (lane < n && mine) {
-                if constexpr (S == 16) st16(cache + soff, lds16(warp_rows + 16 * lane));
-                else st8(cache + soff, lds8(warp_rows + 8 * lane));
-            }
-            __syncwarp();                              // the rows may be reused
-        }
-    }
-};
-
-// The fp8 cache's scale (read once per warp) and its reciprocal; unused for the other
-// formats.  Returns false -- after setting the error bit from lane 0 -- when an fp8 scale
-// is not a positive finite number: the warp then writes nothing.
-template <int kRecord>
-__device__ __forceinline__ bool load_scale(const InsertParams& p, int lane, Scale& sc) {
-    sc.s = 1.0f;
-    sc.y = 1.0f;
-    sc.pow2 = false;
-    if constexpr (kRecord == 512) {
-        sc.s = __ldg(p.fp8_scale);
-        if (!scale_ok(sc.s)) {
-            if (lane == 0) report(p.err, kErrScale);
-            return false;
-        }
-        sc.pow2 = exact_power_of_two(sc.s);
-        sc.y = sc.pow2 ? __frcp_rn(sc.s) : quotient_reciprocal(sc.s);
-    }
-    return true;
-}
-
-// Lane-parallel decode of one group of 32 tokens: for this lane's token, the byte
-// offsets in the cache of its data row (-1 when the token is skipped or invalid) and
-// of its scale row, and its position.  Invalid slots and positions set GKR_ERR_SLOT /
-// GKR_ERR_POS (one atomic per group at most).
 // Slot and position of token t.  With early metadata (gkr_set_early_metadata) the kernels
 // below read them before waiting for the previous kernel in the stream; all other reads
 // and every write come after the wait.
@@ -253,6 +49,10 @@ __device__ __forceinline__ void load_slot_position(const InsertParams& p, int64_
     q = __ldg(p.positions + t);
 }
 
+// Lane-parallel decode of one group of 32 tokens: for this lane's token, the byte
+// offsets in the cache of its data row (-1 when the token is skipped or invalid) and
+// of its scale row, and its position.  Invalid slots and positions set GKR_ERR_SLOT /
+// GKR_ERR_POS (one atomic per group at most).
 template <int kRecord>
 __device__ __forceinline__ void decode_group(const InsertParams& p, const WarpItems& w, int g,
                                              int lane, int64_t& off, int64_t& soff, int32_t& pos,
@@ -401,8 +201,6 @@ __global__ void __launch_bounds__(kThreads, GKR_SHORT_MIN_BLOCKS)
     insert_short_kernel(const InsertParams p) {
     const int lane = threadIdx.x & 31;
     const int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * U;
-    using Rows = ScaleRows<kRecord>;
-    __shared__ __align__(16) uint8_t srows[kWarpsPerBlock][Rows::kBytes];
     if (t0 >= p.num_tokens) return;  // warp-uniform
     const bool mine = lane < U && t0 + lane < p.num_tokens;  // lane u decodes token t0 + u
     int64_t slot = -1, q = 0;
@@ -414,7 +212,6 @@ __global__ void __launch_bounds__(kThreads, GKR_SHORT_MIN_BLOCKS)
     if (!load_scale<kRecord>(p, lane, scale)) return;  // warp-uniform
     constexpr uint32_t D = Fmt<kRecord>::D;
     constexpr uint32_t S = Fmt<kRecord>::S;
-    uint8_t* const wrows = srows[threadIdx.x >> 5];
 
     int64_t off = -1, soff = 0;
     int32_t pos = 0;
@@ -458,13 +255,13 @@ __global__ void __launch_bounds__(kThreads, GKR_SHORT_MIN_BLOCKS)
         }
     }
     uint8_t* const cache_a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
+    uint8_t* const cache_s = p.cache + ScaleRows<kRecord>::lane_byte(lane);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int64_t o = __shfl_sync(kFull, off, u);
-        if (valid[u]) encode_store<kRecord>(L[u], cache_a + o, Rows::row(wrows, u, lane), lane,
-                                            scale);
+        const int64_t so = __shfl_sync(kFull, soff, u);
+        if (valid[u]) encode_store<kRecord>(L[u], cache_a + o, cache_s + so, lane, scale);
     }
-    Rows::store(wrows, p.cache, soff, off >= 0, U, lane);   // lane u: token t0 + u's row
 }
 
 // ---------------------------------------------------------------- compressed-KV insert
@@ -526,8 +323,6 @@ template <int kRecord, int U>
 __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
     insert_staged_kernel(const InsertParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
-    using Rows = ScaleRows<kRecord>;
-    __shared__ __align__(16) uint8_t srows[kWarpsPerBlock][Rows::kBytes];
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
     const int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + wib) * U;
@@ -588,9 +383,11 @@ __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
     cp_async_wait<0>();  // this lane's copies have landed; each lane reads only its own
 
     uint8_t* const cache_a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
+    uint8_t* const cache_s = p.cache + ScaleRows<kRecord>::lane_byte(lane);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int64_t o = __shfl_sync(kFull, off, u);
+        const int64_t so = __shfl_sync(kFull, soff, u);
         if (o >= 0) {  // warp-uniform
             const uint8_t* src = ring_lane + u * kSlotBytes;
             TokenLoads L;
@@ -600,10 +397,9 @@ __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
                 L.c = *reinterpret_cast<const float4*>(src + 1024 - 16 * 24);
                 L.s = *reinterpret_cast<const float4*>(src + 1024 + 128 - 16 * 24);
             }
-            encode_store<kRecord>(L, cache_a + o, Rows::row(srows[wib], u, lane), lane, scale);
+            encode_store<kRecord>(L, cache_a + o, cache_s + so, lane, scale);
         }
     }
-    Rows::store(srows[wib], p.cache, soff, off >= 0, U, lane);   // lane u: token t0 + u's row
 }
 
 template <int kRecord, int U>
@@ -615,19 +411,19 @@ cudaError_t launch_staged(const InsertParams& p, cudaStream_t stream) {
     cudaError_t e = resident_warps(reinterpret_cast<const void*>(insert_staged_kernel<kRecord, U>),
                                    kThreads, smem, &wave);
     if (e != cudaSuccess) return e;
-    return launch_kernel(insert_staged_kernel<kRecord, U>, blocks, kThreads, smem, stream, p);
+    return launch_kernel(insert_staged_kernel<kRecord, U>, blocks, kThreads, smem, stream, p.pdl, p);
 }
 
 template <int kRecord>
 cudaError_t launch(const InsertParams& p, cudaStream_t stream) {
     if (p.num_tokens <= 0) return cudaSuccess;
-    if (p.num_tokens < insert_staged_min() && p.num_tokens < insert_stream_min()) {
+    if (p.num_tokens < p.staged_min && p.num_tokens < p.stream_min) {
         constexpr int U = 2;
         const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * U;
         const int64_t blocks = (p.num_tokens + per_block - 1) / per_block;
-        return launch_kernel(insert_short_kernel<kRecord, U>, blocks, kThreads, 0, stream, p);
+        return launch_kernel(insert_short_kernel<kRecord, U>, blocks, kThreads, 0, stream, p.pdl, p);
     }
-    if (p.num_tokens < insert_stream_min()) {
+    if (p.num_tokens < p.stream_min) {
         // tokens per warp: the fewest (1..3) that fit the launch in one wave of warps
         int64_t wave = 0;
         cudaError_t e = resident_warps(reinterpret_cast<const void*>(insert_staged_kernel<kRecord, 3>),
@@ -646,7 +442,7 @@ cudaError_t launch(const InsertParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const WorkMap m = make_work_map(p.num_tokens, wave, false, 1, GKR_INSERT_MAX_CHUNK);
     const int64_t blocks = (m.warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    return launch_kernel(kernel, blocks, kThreads, smem, stream, p, m);
+    return launch_kernel(kernel, blocks, kThreads, smem, stream, p.pdl, p, m);
 }
 
 #ifndef GKR_SPARSE_MIN_BLOCKS
@@ -674,9 +470,6 @@ template <int kRecord, bool kSanitize>
 __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
     insert_sparse_staged_kernel(const InsertParams p, const int32_t chunk) {
     extern __shared__ __align__(16) uint8_t smem[];
-    using Rows = ScaleRows<kRecord>;
-    static_assert(kSparseBatch <= Rows::kRows, "a batch's scale rows fit one staging line");
-    __shared__ __align__(16) uint8_t srows[kWarpsPerBlock][Rows::kBytes];
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock * chunk;
@@ -692,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
     const float* const csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
     uint8_t* const ring_lane = smem + wib * (kSparseBatch * kSlotBytes) + 16 * lane;
     uint8_t* const cache_a = p.cache + 8 * lane;
+    uint8_t* const cache_s = p.cache + ScaleRows<kRecord>::lane_byte(lane);
     while (true) {
         int64_t off = -1, soff = 0;
         int32_t row = 0;
@@ -735,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
             for (int v = 0; v < kSparseBatch; ++v) {
                 if (u[v] >= 0) {                         // warp-uniform
                     const int64_t o = __shfl_sync(kFull, off, u[v]);
+                    const int64_t so = __shfl_sync(kFull, soff, u[v]);
                     const uint8_t* src = ring_lane + v * kSlotBytes;
                     TokenLoads L;
                     L.a = lds16(src);
@@ -743,23 +538,10 @@ __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
                         L.c = *reinterpret_cast<const float4*>(src + 1024 - 16 * 24);
                         L.s = *reinterpret_cast<const float4*>(src + 1024 + 128 - 16 * 24);
                     }
-                    encode_store<kRecord, kSanitize>(L, cache_a + o,
-                                                     Rows::row(srows[wib], v, lane), lane,
+                    encode_store<kRecord, kSanitize>(L, cache_a + o, cache_s + so, lane,
                                                      Scale{1.0f, 1.0f, false});
                 }
             }
-            // lane v < kSparseBatch stores staged row v, the row of chunk token u[v]
-            int src = 0;
-            bool has = false;
-#pragma unroll
-            for (int v = 0; v < kSparseBatch; ++v) {
-                if (lane == v) {
-                    src = u[v] < 0 ? 0 : u[v];
-                    has = u[v] >= 0;
-                }
-            }
-            Rows::store(srows[wib], p.cache, __shfl_sync(kFull, soff, src), has, kSparseBatch,
-                        lane);
         }
         if (t1 >= p.num_tokens) break;  // warp-uniform
         __syncwarp();  // reconverge before the next chunk's shuffles
@@ -782,7 +564,7 @@ cudaError_t launch_compressed(const InsertParams& p, bool sanitize, cudaStream_t
     cudaError_t e = resident_warps(reinterpret_cast<const void*>(kernel), kThreads, smem, &wave);
     if (e != cudaSuccess) return e;
     const int64_t resident = wave / kWarpsPerBlock;          // the grid is at most one wave
-    return launch_kernel(kernel, blocks < resident ? blocks : resident, kThreads, smem, stream, p,
+    return launch_kernel(kernel, blocks < resident ? blocks : resident, kThreads, smem, stream, p.pdl, p,
                          chunk);
 }
 

@@ -23,6 +23,9 @@ struct InsertParams {
     const float* fp8_scale;    // fp8 rows (record 512): the cache's scale; else unused
     int32_t* err;              // nullable
     int32_t early_metadata;    // 1: slots / positions may be read before the PDL wait
+    int32_t pdl;               // 1: launch with the programmatic-dependent-launch attribute
+    int64_t staged_min;        // token counts from which the insert stages rows in shared
+    int64_t stream_min;        //   memory / streams them (launch policy of this call)
 };
 
 // Validated arguments of one gather launch.
@@ -37,6 +40,17 @@ struct GatherParams {
     const float* fp8_scale;    // fp8 rows (record 512): the cache's scale; else unused
     int32_t* err;              // nullable
     int32_t early_metadata;    // 1: indices may be read before the PDL wait
+    int32_t pdl;               // 1: launch with the programmatic-dependent-launch attribute
+};
+
+// Query side of the fused attention write (gkr_qnorm_rope_kv_insert).
+struct QSideParams {
+    const void* q_in;          // bf16 [num_tokens, num_heads, 512]
+    void* q_out;               // bf16 [num_tokens, num_heads_padded, 512]
+    int32_t num_heads;
+    int32_t num_heads_padded;  // >= num_heads, > 0 (0 is the plain KV insert)
+    float eps;
+    int32_t apply_norm;        // 1: divide each head by sqrt(mean(x^2) + eps)
 };
 
 // Row geometry of the four cache formats ("record" = bytes a token occupies):
@@ -62,16 +76,11 @@ struct Fmt {
 // on a device also raises its dynamic shared-memory limit when it needs more than
 // the default 48 KiB.
 cudaError_t resident_warps(const void* func, int threads, size_t smem, int64_t* warps);
-// Whether launches carry the programmatic-dependent-launch attribute.
-bool pdl_enabled();
-// Token counts from which inserts use the staged kernel, and the streaming kernel.
-int64_t insert_staged_min();
-int64_t insert_stream_min();
 
-// Launch `kernel` with the PDL attribute when enabled.
+// Launch `kernel`, with the programmatic-dependent-launch attribute when `pdl` is set.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), int64_t blocks, int threads, size_t smem,
-                          cudaStream_t stream, Args&&... args) {
+                          cudaStream_t stream, int32_t pdl, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
     cfg.blockDim = dim3(static_cast<unsigned>(threads));
@@ -79,7 +88,7 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), int64_t blocks, int threads,
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl != 0 ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
@@ -150,6 +159,10 @@ cudaError_t launch_rope_quant_insert_v41(const InsertParams& p, bool sanitize,
                                          cudaStream_t stream);
 cudaError_t launch_rope_quant_insert_v4(const InsertParams& p, bool sanitize,
                                         cudaStream_t stream);
+// Query heads normed and rotated, padded heads zeroed, and the KV rows inserted (any of
+// the four cache formats), in one launch.
+cudaError_t launch_qnorm_rope_kv_insert(int32_t record, const InsertParams& p,
+                                        const QSideParams& qp, cudaStream_t stream);
 cudaError_t launch_gather_v41(const GatherParams& p, cudaStream_t stream);
 cudaError_t launch_gather_v4(const GatherParams& p, cudaStream_t stream);
 cudaError_t launch_gather_fp8(const GatherParams& p, cudaStream_t stream);

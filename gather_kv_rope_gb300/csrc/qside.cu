@@ -1,0 +1,217 @@
+// The fused attention write: query-side norm and rotation beside the KV insert, in one
+// launch.
+//
+// Operation (page "PR #56893 [DSv4.1] Store the whole KV in MXFP8 (FlashMLA V4.1
+// record)", section "实现拆解" item 3 and the attention.py listing: one op takes q, the
+// KV row, the cache, slots, positions, the cos/sin table, the padded head count and eps;
+// page "PR #56441 [Perf][DSpark] KV-only context insertion across V4.1 cache formats",
+// section "实现拆解" item 1: the KV-only insert is that op without q_in, q_head_padded,
+// eps and apply_q_norm).  Per token t, with position p = positions[t]:
+//   query heads h < H: x = q_in[t, h, :] in fp32; with the norm, x /= sqrt(mean(x^2) + eps)
+//     (an RMS norm without a weight: the pages print neither the norm nor the q layout,
+//     this is the reading the library takes); dims 448..511 rotated in adjacent pairs
+//     with cos/sin row p, exactly as the KV row; q_out[t, h, :] = bf16(x);
+//   heads H .. Hp-1 of q_out: +0;  a position outside the table: every head of the
+//     token +0 and GKR_ERR_POS;
+//   the KV row: as gkr_kv_insert (slot -1 skips it).
+//
+// Launch shape: rows of 512 dims, one warp per row at a time and two rows per warp (the
+// lane layout of device.cuh).  Token t owns rows t*(Hp+1) .. t*(Hp+1)+Hp: first its KV
+// row, then its Hp query heads, so a warp's rows are consecutive in q_in / q_out and the
+// grid depends only on T * (Hp + 1).  Lanes 0..1 decode their row (token, kind, slot,
+// position) in parallel; every row's loads are issued before the first is converted.
+#include "device.cuh"
+#include "encode.cuh"
+#include "launch.h"
+
+namespace gkr {
+
+namespace {
+
+constexpr int kRowsPerWarp = 2;
+
+#ifndef GKR_QSIDE_MIN_BLOCKS
+#define GKR_QSIDE_MIN_BLOCKS 4
+#endif
+
+enum RowKind : int32_t { kNone = 0, kKvRow = 1, kQHead = 2, kZeroHead = 3 };
+
+// One query head on one warp: chunks A and B of the head (16 bf16 per lane) -> normed
+// (optionally) and rotated -> 16 bf16 per lane.  The sum of squares is taken per lane in
+// dim order, then over the warp by a butterfly (every lane ends with the same sum);
+// mean = sum * 2^-9 (exact); factor = the correctly rounded 1/sqrt(mean + eps); every
+// operation is one fp32 operation rounded to nearest even (no contraction).
+__device__ __forceinline__ void q_head(const uint4 ta, const uint4 tb, const float4 c,
+                                       const float4 s, bool norm, float eps, int lane,
+                                       uint4& oa, uint4& ob) {
+    float a[8], b[8];
+    unpack_bf16x8(ta, a);
+    unpack_bf16x8(tb, b);
+    if (norm) {
+        float ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(a[i], a[i]));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(b[i], b[i]));
+#pragma unroll
+        for (int x = 16; x >= 1; x >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, x));
+        const float r = __frsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / 512.0f), eps));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            a[i] = __fmul_rn(a[i], r);
+            b[i] = __fmul_rn(b[i], r);
+        }
+    }
+    if (lane >= 24) rope4(b, c, s);   // dims 448..511 = pairs 4(L-24) .. 4(L-24)+3
+    oa = make_uint4(pack_bf16x2_rn(a[0], a[1]), pack_bf16x2_rn(a[2], a[3]),
+                    pack_bf16x2_rn(a[4], a[5]), pack_bf16x2_rn(a[6], a[7]));
+    ob = make_uint4(pack_bf16x2_rn(b[0], b[1]), pack_bf16x2_rn(b[2], b[3]),
+                    pack_bf16x2_rn(b[4], b[5]), pack_bf16x2_rn(b[6], b[7]));
+}
+
+template <int kRecord>
+__global__ void __launch_bounds__(kThreads, GKR_QSIDE_MIN_BLOCKS)
+    qnorm_rope_kv_insert_kernel(const InsertParams p, const QSideParams qp) {
+    constexpr int U = kRowsPerWarp;
+    constexpr uint32_t D = Fmt<kRecord>::D;
+    constexpr uint32_t S = Fmt<kRecord>::S;
+    const int lane = threadIdx.x & 31;
+    const int64_t per_token = static_cast<int64_t>(qp.num_heads_padded) + 1;
+    const int64_t n_rows = p.num_tokens * per_token;
+    const int64_t r0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * U;
+    if (r0 >= n_rows) return;  // warp-uniform
+
+    // lane u < U decodes row r0 + u: its token and kind (j = 0: the KV row; 1..H: query
+    // head j - 1; H+1..Hp: a padded head)
+    const bool mine = lane < U && r0 + lane < n_rows;
+    int64_t t = 0;
+    int32_t j = -1;
+    if (mine) {
+        t = (r0 + lane) / per_token;
+        j = static_cast<int32_t>(r0 + lane - t * per_token);
+    }
+    const bool reads_pos = mine && j <= qp.num_heads;   // the KV row and the query heads
+    int64_t slot = -1, q = 0;
+    if (p.early_metadata != 0 && reads_pos) {
+        if (j == 0) slot = __ldg(p.slots + t);
+        q = __ldg(p.positions + t);
+    }
+    pdl_wait_previous();
+    pdl_release_next();
+    if (p.early_metadata == 0 && reads_pos) {
+        if (j == 0) slot = __ldg(p.slots + t);
+        q = __ldg(p.positions + t);
+    }
+    // the fp8 cache's scale, for warps with a KV row (a bad scale skips only KV rows)
+    Scale scale{1.0f, 1.0f, false};
+    bool scale_good = true;
+    if (__ballot_sync(kFull, mine && j == 0) != 0u) scale_good = load_scale<kRecord>(p, lane, scale);
+
+    int64_t off = -1, soff = 0;
+    int32_t pos = 0, kind = kNone;
+    uint32_t err = 0;
+    if (mine) {
+        if (j == 0) {
+            if (scale_good) {
+                if (slot >= p.num_slots) {
+                    err = 1;
+                } else if (slot >= 0) {
+                    if (q < 0 || q >= p.max_pos) {
+                        err = 2;
+                    } else {
+                        const uint32_t s = static_cast<uint32_t>(slot);
+                        const uint32_t bs = static_cast<uint32_t>(p.block_size);
+                        const uint32_t page = s / bs, row = s - page * bs;
+                        const int64_t base = static_cast<int64_t>(page) * p.page_stride;
+                        off = base + row * D;
+                        soff = base + bs * D + row * S;
+                        pos = static_cast<int32_t>(q);
+                        kind = kKvRow;
+                    }
+                }
+            }
+        } else if (j <= qp.num_heads) {
+            if (q < 0 || q >= p.max_pos) {
+                err = 2;
+                kind = kZeroHead;
+            } else {
+                pos = static_cast<int32_t>(q);
+                kind = kQHead;
+            }
+        } else {
+            kind = kZeroHead;
+        }
+    }
+    err = __reduce_or_sync(kFull, err);
+    if (err != 0u && lane == 0) report(p.err, static_cast<int32_t>(err));
+
+    // every row's loads first: the KV row or the query head, and the cos/sin row
+    const float* const csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
+    const uint8_t* const kv = static_cast<const uint8_t*>(p.kv);
+    const uint8_t* const qin = static_cast<const uint8_t*>(qp.q_in);
+    uint8_t* const qout = static_cast<uint8_t*>(qp.q_out);
+    TokenLoads L[U];
+    int32_t kinds[U];
+    int64_t tok[U];
+    int32_t head[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        kinds[u] = __shfl_sync(kFull, kind, u);
+        tok[u] = __shfl_sync(kFull, t, u);
+        head[u] = __shfl_sync(kFull, j, u) - 1;
+        const int32_t pu = __shfl_sync(kFull, pos, u);
+        if (kinds[u] == kKvRow || kinds[u] == kQHead) {   // warp-uniform
+            const uint8_t* row = kinds[u] == kKvRow
+                                     ? kv + tok[u] * 1024
+                                     : qin + (tok[u] * qp.num_heads + head[u]) * 1024;
+            L[u].a = ld_stream16(row + 16 * lane);
+            L[u].b = ld_stream16(row + 512 + 16 * lane);
+            if (lane >= 24) {
+                const float* cs = csc_lane + static_cast<int64_t>(pu) * 64;
+                L[u].c = ld_ro_f4(cs);
+                L[u].s = ld_ro_f4(cs + 32);
+            }
+        }
+    }
+    uint8_t* const cache_a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
+    uint8_t* const cache_s = p.cache + ScaleRows<kRecord>::lane_byte(lane);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        if (kinds[u] == kKvRow) {
+            const int64_t o = __shfl_sync(kFull, off, u);
+            const int64_t so = __shfl_sync(kFull, soff, u);
+            encode_store<kRecord>(L[u], cache_a + o, cache_s + so, lane, scale);
+        } else if (kinds[u] == kQHead || kinds[u] == kZeroHead) {
+            uint4 oa = make_uint4(0u, 0u, 0u, 0u), ob = oa;
+            if (kinds[u] == kQHead)
+                q_head(L[u].a, L[u].b, L[u].c, L[u].s, qp.apply_norm != 0, qp.eps, lane, oa, ob);
+            uint8_t* dst = qout + (tok[u] * qp.num_heads_padded + head[u]) * 1024 + 16 * lane;
+            st_stream16(dst, oa);
+            st_stream16(dst + 512, ob);
+        }
+    }
+}
+
+template <int kRecord>
+cudaError_t launch(const InsertParams& p, const QSideParams& qp, cudaStream_t stream) {
+    if (p.num_tokens <= 0) return cudaSuccess;
+    const int64_t rows = p.num_tokens * (static_cast<int64_t>(qp.num_heads_padded) + 1);
+    const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * kRowsPerWarp;
+    const int64_t blocks = (rows + per_block - 1) / per_block;
+    return launch_kernel(qnorm_rope_kv_insert_kernel<kRecord>, blocks, kThreads, 0, stream,
+                         p.pdl, p, qp);
+}
+
+}  // namespace
+
+cudaError_t launch_qnorm_rope_kv_insert(int32_t record, const InsertParams& p,
+                                        const QSideParams& qp, cudaStream_t stream) {
+    switch (record) {
+        case 528: return launch<528>(p, qp, stream);
+        case 584: return launch<584>(p, qp, stream);
+        case 512: return launch<512>(p, qp, stream);
+        default: return launch<1024>(p, qp, stream);
+    }
+}
+
+}  // namespace gkr

@@ -7,7 +7,10 @@
  *                  into a plain bf16 / fp8 e4m3 cache);
  *   gkr_kv_gather: the inverse: dequantise listed slots back to bf16 [N, 512];
  *   gkr_rope_quant_insert: the compressed-KV insert (one record per group of
- *                  compress_ratio positions, optional NaN sanitising).
+ *                  compress_ratio positions, optional NaN sanitising);
+ *   gkr_qnorm_rope_kv_insert: the fused attention write: query heads normed and
+ *                  rotated (bf16 out, padded heads zeroed) beside the KV insert, in one
+ *                  launch.
  *
  * Operations follow these passages (page title, section):
  *   "PR #56893 [DSv4.1] Store the whole KV in MXFP8 (FlashMLA V4.1 record)",
@@ -27,8 +30,9 @@
  *   - All tensor pointers are DEVICE pointers on the current CUDA device;
  *     the caller owns and allocates all memory.  The library allocates no
  *     device memory and never synchronises the stream; the only state it keeps
- *     is the process-wide launch policy (gkr_set_*) and a per-device cache of
- *     occupancy queries.  Calls may be captured into CUDA graphs.
+ *     is the process-wide default launch policy (gkr_set_*), which a call's
+ *     gkr_launch_opts overrides, and a per-device cache of occupancy queries.
+ *     Calls may be captured into CUDA graphs.
  *   - Work is enqueued on `stream` (0 = the legacy default stream); results
  *     are visible after the stream's work completes.
  *   - Host-side argument checks run before anything is enqueued; on failure
@@ -98,6 +102,29 @@ typedef struct gkr_cache_desc {
 } gkr_cache_desc;
 
 /*
+ * Launch options of one call (every entry point that launches takes a nullable
+ * `const gkr_launch_opts *opts`).  A field of -1, or a NULL opts, takes the
+ * process-wide default set by the matching gkr_set_* call; GKR_EINVAL for any other
+ * negative value or a flag other than -1, 0, 1.  Options apply to the launch of that
+ * call only, so threads or libraries that share the process can each use their own.
+ *   pdl                1: launch with programmatic dependent launch (see gkr_set_pdl)
+ *   early_metadata     1: read slots / positions / indices before waiting for the kernel
+ *                      ahead (see gkr_set_early_metadata for when this is safe)
+ *   insert_staged_min  token count from which gkr_kv_insert stages rows in shared memory
+ *   insert_stream_min  token count from which gkr_kv_insert streams (see
+ *                      gkr_set_insert_stream_min)
+ */
+typedef struct gkr_launch_opts {
+    int32_t pdl;
+    int32_t early_metadata;
+    int64_t insert_staged_min;
+    int64_t insert_stream_min;
+} gkr_launch_opts;
+
+/* Every field "take the process default". */
+#define GKR_LAUNCH_OPTS_INIT {-1, -1, -1, -1}
+
+/*
  * Smallest valid page stride: block_size * record rounded up to the record's
  * page alignment (576 for 584, 512 otherwise).  Returns -1 for an unsupported
  * record or block_size.
@@ -146,13 +173,14 @@ GKR_API gkr_status gkr_record_rows(int32_t record, int32_t *data_row_bytes,
  *                512 (GKR_EINVAL if NULL), ignored otherwise (may be NULL).
  * err_flag       device int32 or NULL; GKR_ERR_SLOT / GKR_ERR_POS / GKR_ERR_SCALE
  *                bits are OR-ed in.
+ * opts           host pointer to this call's launch options, or NULL (defaults).
  * stream         CUDA stream to enqueue on.
  */
 GKR_API gkr_status gkr_kv_insert(const void *kv, int64_t num_tokens, void *k_cache,
                                  const gkr_cache_desc *cache, const int64_t *slot_mapping,
                                  const int64_t *positions, const float *cos_sin_cache,
                                  int64_t max_pos, const float *fp8_scale, int32_t *err_flag,
-                                 cudaStream_t stream);
+                                 const gkr_launch_opts *opts, cudaStream_t stream);
 
 /*
  * rope_quant_insert: the compressed-KV insert ("PR #56893 [DSv4.1] Store the whole
@@ -178,7 +206,54 @@ GKR_API gkr_status gkr_rope_quant_insert(const void *kv, int64_t num_tokens, voi
                                          const int64_t *slot_mapping, const int64_t *positions,
                                          const float *cos_sin_cache, int64_t max_pos,
                                          int32_t compress_ratio, int32_t sanitize_nans,
-                                         int32_t *err_flag, cudaStream_t stream);
+                                         int32_t *err_flag, const gkr_launch_opts *opts,
+                                         cudaStream_t stream);
+
+/*
+ * qnorm_rope_kv_insert: the fused attention write ("PR #56893 [DSv4.1] Store the whole
+ * KV in MXFP8 (FlashMLA V4.1 record)", section "实现拆解" item 3 and the attention.py
+ * listing: one op takes q, the KV row, the cache, slots, positions, the cos/sin table,
+ * the padded head count and eps; "PR #56441 [Perf][DSpark] KV-only context insertion
+ * across V4.1 cache formats", section "实现拆解" item 1: gkr_kv_insert is this op with
+ * q_in, the padded head count, eps and apply_q_norm removed).  The pages print neither
+ * the norm nor the q layout; this library's reading, per token t at position p:
+ *   query head h < num_heads: x = q_in[t, h, 0..511] in fp32; with apply_q_norm,
+ *     x = x * 1/sqrt(mean(x^2) + eps) (an RMS norm over the head's 512 dims, no
+ *     weight); dims 448..511 rotated in adjacent pairs with cos/sin row p exactly as
+ *     the KV row is; q_out[t, h, :] = bf16(x), round to nearest even;
+ *   heads num_heads .. num_heads_padded - 1 of q_out: +0;
+ *   p outside [0, max_pos) (with num_heads > 0): every head of q_out[t] is +0 and
+ *     GKR_ERR_POS is set;
+ *   the KV row: exactly gkr_kv_insert (slot -1 skips it; the query heads are written
+ *     whatever the slot).
+ * Accuracy: the norm's arithmetic order is the kernel's (per-lane sums, a warp
+ * butterfly, a correctly rounded reciprocal square root), so each q_out value is one of
+ * the two bf16 values around the exact result (a faithful rounding; nearest in all but
+ * rare ties of the fp32 error), while the KV record is bit-exact.  The contract needs
+ * sum(x^2) < 2^128 and mean(x^2) + eps >= 2^-126 per head (eps = 0 with a zero head is
+ * outside it).  num_heads_padded == 0 is exactly gkr_kv_insert (q pointers ignored).
+ *
+ * q_in              device, bf16 [num_tokens, num_heads, 512] row-major, 16-byte
+ *                   aligned; read only (may be NULL when num_heads == 0).
+ * num_heads         >= 0.
+ * num_heads_padded  num_heads <= num_heads_padded <= 4096.
+ * q_out             device, bf16 [num_tokens, num_heads_padded, 512], 16-byte aligned.
+ *                   It may be q_in itself when num_heads_padded == num_heads (in place);
+ *                   any other overlap with an input races.
+ * eps               finite, >= 0.
+ * apply_q_norm      0 or 1.
+ * The other arguments are gkr_kv_insert's, for the KV row (any of the four records).
+ */
+GKR_API gkr_status gkr_qnorm_rope_kv_insert(const void *q_in, int32_t num_heads,
+                                            int32_t num_heads_padded, void *q_out, float eps,
+                                            int32_t apply_q_norm, const void *kv,
+                                            int64_t num_tokens, void *k_cache,
+                                            const gkr_cache_desc *cache,
+                                            const int64_t *slot_mapping,
+                                            const int64_t *positions,
+                                            const float *cos_sin_cache, int64_t max_pos,
+                                            const float *fp8_scale, int32_t *err_flag,
+                                            const gkr_launch_opts *opts, cudaStream_t stream);
 
 /*
  * kv_gather: for each i in [0, num_indices):
@@ -200,15 +275,20 @@ GKR_API gkr_status gkr_rope_quant_insert(const void *kv, int64_t num_tokens, voi
  * out          device, bf16 [num_indices, 512] row-major, 16-byte aligned.
  * fp8_scale    device pointer to one fp32: required for record 512, else ignored.
  * err_flag     device int32 or NULL; GKR_ERR_INDEX / GKR_ERR_SCALE are OR-ed in.
+ * opts         host pointer to this call's launch options, or NULL (defaults).
  * stream       CUDA stream to enqueue on.
  */
 GKR_API gkr_status gkr_kv_gather(const void *k_cache, const gkr_cache_desc *cache,
                                  const int32_t *indices, int64_t num_indices, void *out,
                                  const float *fp8_scale, int32_t *err_flag,
-                                 cudaStream_t stream);
+                                 const gkr_launch_opts *opts, cudaStream_t stream);
 
 /*
- * Programmatic dependent launch (process-wide, default on).  When on, kernels are
+ * Process-wide defaults of the launch options (gkr_launch_opts fields left at -1 take
+ * them).  Setting them while another thread launches is safe (atomics) but changes that
+ * thread's later calls too; per-call options do not.
+ *
+ * Programmatic dependent launch (default on).  When on, kernels are
  * launched with the programmatic-stream-serialisation attribute: a launch may be
  * scheduled while the previous kernel in the stream drains, and waits for that
  * kernel's completion and memory flush before its first global memory access, so
@@ -260,7 +340,8 @@ GKR_API int32_t gkr_last_cuda_error(void);
 /* ABI version: major * 10000 + minor * 100 + patch.  2.0.0: gkr_kv_insert and
  * gkr_kv_gather take fp8_scale (the plain fp8 / bf16 caches); gkr_rope_quant_insert and
  * gkr_set_insert_staged_min / gkr_get_insert_staged_min were added.  2.1.0:
- * gkr_set_early_metadata / gkr_get_early_metadata. */
+ * gkr_set_early_metadata / gkr_get_early_metadata.  3.0.0: every launching entry point
+ * takes a gkr_launch_opts pointer before the stream; gkr_qnorm_rope_kv_insert. */
 GKR_API int32_t gkr_version(void);
 
 #ifdef __cplusplus

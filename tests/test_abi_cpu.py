@@ -26,7 +26,8 @@ def test_header_declares_the_boundary():
             "gkr_status_string", "gkr_last_cuda_error", "gkr_version", "gkr_set_pdl",
             "gkr_get_pdl", "gkr_set_insert_stream_min", "gkr_get_insert_stream_min",
             "gkr_set_insert_staged_min", "gkr_get_insert_staged_min",
-            "gkr_rope_quant_insert", "gkr_set_early_metadata", "gkr_get_early_metadata"} <= syms
+            "gkr_rope_quant_insert", "gkr_set_early_metadata", "gkr_get_early_metadata",
+            "gkr_qnorm_rope_kv_insert"} <= syms
 
 
 def test_library_exports_every_declared_symbol(gkr):
@@ -58,7 +59,7 @@ def test_page_stride_and_rows(gkr):
     assert gkr.page_stride(1024, 0) == -1
     with pytest.raises(ValueError):
         gkr.record_rows(500)
-    assert gkr.lib().gkr_version() == 20100
+    assert gkr.lib().gkr_version() == 30000
     assert gkr.get_insert_stream_min() == 131072
     assert gkr.get_insert_staged_min() == 24576
     assert gkr.insert_kernel_for(16384) == "insert_short_kernel"
@@ -97,24 +98,37 @@ def desc(gkr, record=528, bs=64, pages=4, ps=None):
     return gkr.CacheDesc(record, bs, pages, gkr.page_stride(record, bs) if ps is None else ps)
 
 
+def _o(opts):
+    return None if opts is None else ctypes.byref(opts)
+
+
 def insert(gkr, d, T=8, kv=A16, cache=A16b, slots=A16, pos=A16, csc=A16, max_pos=16, err=None,
-           scale=None):
+           scale=None, opts=None):
     return gkr.lib().gkr_kv_insert(kv, T, cache, None if d is None else ctypes.byref(d),
-                                   slots, pos, csc, max_pos, scale, err, None)
+                                   slots, pos, csc, max_pos, scale, err, _o(opts), None)
 
 
 def rq_insert(gkr, d, T=8, kv=A16, cache=A16b, slots=A16, pos=A16, csc=A16, max_pos=16,
-              ratio=4, sanitize=1, err=None):
+              ratio=4, sanitize=1, err=None, opts=None):
     return gkr.lib().gkr_rope_quant_insert(kv, T, cache, None if d is None else ctypes.byref(d),
-                                           slots, pos, csc, max_pos, ratio, sanitize, err, None)
+                                           slots, pos, csc, max_pos, ratio, sanitize, err,
+                                           _o(opts), None)
 
 
-def gather(gkr, d, N=8, cache=A16b, idx=A16, out=A16, err=None, scale=None):
+def gather(gkr, d, N=8, cache=A16b, idx=A16, out=A16, err=None, scale=None, opts=None):
     return gkr.lib().gkr_kv_gather(cache, None if d is None else ctypes.byref(d), idx, N,
-                                   out, scale, err, None)
+                                   out, scale, err, _o(opts), None)
 
 
-@pytest.mark.parametrize("op", [insert, rq_insert, gather])
+def qinsert(gkr, d, T=8, q=A16b + 0x1000, H=2, Hp=4, qout=A16b + 0x2000, eps=1e-6, norm=1,
+            kv=A16, cache=A16b, slots=A16, pos=A16, csc=A16, max_pos=16, err=None, scale=None,
+            opts=None):
+    return gkr.lib().gkr_qnorm_rope_kv_insert(q, H, Hp, qout, eps, norm, kv, T, cache,
+                                              None if d is None else ctypes.byref(d), slots, pos,
+                                              csc, max_pos, scale, err, _o(opts), None)
+
+
+@pytest.mark.parametrize("op", [insert, rq_insert, gather, qinsert])
 def test_geometry_checks(gkr, op):
     assert op(gkr, None) == 1                                        # null descriptor
     assert op(gkr, desc(gkr, record=500)) == 2                       # unsupported record
@@ -191,6 +205,69 @@ def test_gather_argument_checks(gkr):
     assert gather(gkr, d, out=A16 + 8) == 4
     assert gather(gkr, d, idx=A16 + 2) == 4
     assert gather(gkr, d, cache=A16 + 8) == 4
+
+
+def test_qnorm_rope_kv_insert_argument_checks(gkr):
+    d = desc(gkr)
+    assert qinsert(gkr, d, H=-1) == 1
+    assert qinsert(gkr, d, H=4, Hp=3) == 1                            # padded below heads
+    assert qinsert(gkr, d, Hp=4097) == 1
+    assert qinsert(gkr, d, norm=2) == 1
+    assert qinsert(gkr, d, eps=-1e-6) == 1
+    assert qinsert(gkr, d, eps=float("nan")) == 1
+    assert qinsert(gkr, d, eps=float("inf")) == 1
+    assert qinsert(gkr, d, T=-1) == 1
+    assert qinsert(gkr, d, T=0, q=None, qout=None, kv=None, cache=None, slots=None, pos=None,
+                   csc=None, max_pos=0) == 0                           # nothing to do
+    assert qinsert(gkr, d, q=None) == 1
+    assert qinsert(gkr, d, qout=None) == 1
+    assert qinsert(gkr, d, q=A16 + 8) == 4
+    assert qinsert(gkr, d, qout=A16 + 8) == 4
+    assert qinsert(gkr, d, kv=A16 + 8) == 4
+    assert qinsert(gkr, d, kv=None) == 1
+    assert qinsert(gkr, desc(gkr, record=512)) == 1                   # fp8 without a scale
+    assert qinsert(gkr, desc(gkr, record=500)) == 2
+
+
+@pytest.mark.parametrize("op", [insert, rq_insert, gather, qinsert])
+def test_launch_options_are_checked(gkr, op):
+    """Per-call launch options: -1 takes the process default; other negative values and
+    flags other than 0 / 1 are rejected before anything is enqueued."""
+    O = gkr.LaunchOpts
+    bad = [O(), O(), O(), O()]
+    bad[0].pdl = 2
+    bad[1].early_metadata = -2
+    bad[2].insert_staged_min = -5
+    bad[3].insert_stream_min = -2
+    for o in bad:
+        assert op(gkr, desc(gkr), opts=o) == 1
+    # valid options reach the next check (a misaligned pointer here), not a launch
+    misaligned = {insert: dict(kv=A16 + 8), rq_insert: dict(kv=A16 + 8),
+                  gather: dict(out=A16 + 8), qinsert: dict(kv=A16 + 8)}[op]
+    for o in (O(), O(pdl=False, early_metadata=True, insert_staged_min=0, insert_stream_min=7)):
+        assert op(gkr, desc(gkr), opts=o, **misaligned) == 4
+
+
+def test_launch_policy_is_context_local(gkr):
+    """launch_policy sets the options of this thread's calls only (the process defaults
+    stay as they are) and nests; an explicit LaunchOpts wins over it."""
+    import threading
+    assert gkr.insert_kernel_for(16384) == "insert_short_kernel"
+    seen = {}
+    with gkr.launch_policy(insert_staged_min=0):
+        assert gkr.insert_kernel_for(16384) == "insert_staged_kernel"
+        with gkr.launch_policy(insert_stream_min=100):
+            assert gkr.insert_kernel_for(16384) == "insert_kernel"
+            assert gkr.insert_kernel_for(50) == "insert_staged_kernel"
+        t = threading.Thread(target=lambda: seen.update(k=gkr.insert_kernel_for(16384)))
+        t.start()
+        t.join()
+        assert gkr.get_insert_staged_min() == 24576            # the process default is untouched
+        eff = gkr._binding._opts(gkr.LaunchOpts(insert_staged_min=30000))._obj
+        assert eff.insert_staged_min == 30000 and eff.insert_stream_min == -1
+    assert seen["k"] == "insert_short_kernel"                   # the other thread saw defaults
+    assert gkr.insert_kernel_for(16384) == "insert_short_kernel"
+    assert gkr._binding._opts(None) is None
 
 
 def test_status_strings(gkr):

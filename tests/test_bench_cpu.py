@@ -26,6 +26,10 @@ def test_algorithmic_bytes():
     assert bench.compressed_insert_bytes(slots, pos, 1, 584) == bench.insert_bytes(slots, 584)
     idx = np.array([[-1, 2], [3, -1]], np.int32)
     assert bench.gather_bytes(idx, 528) == 4 * 1028 + 2 * 528
+    # the fused attention write: the insert's bytes plus every token's heads read and
+    # padded heads written (skipped slots still carry their query heads)
+    assert bench.qside_bytes(slots, 528, 3, 8) == bench.insert_bytes(slots, 528) + 5 * 11 * 1024
+    assert bench.qside_bytes(slots, 584, 0, 0) == bench.insert_bytes(slots, 584)
     # cos/sin rows: one per distinct row among the written tokens (tokens 1 and 2 share
     # position 3's row; the skipped token's position 5 is not read)
     pos = np.array([3, 3, 3, 5, 11], np.int64)

@@ -1,4 +1,4 @@
-"""GPU parity with early metadata reads on (gkr_set_early_metadata): inserts of every
+"""GPU parity with early metadata reads on (the early_metadata launch option): inserts of every
 format through the register-load and staged kernels, the compressed insert, gathers and
 the benchmark's round-trip graph give the oracle's bytes, and data the kernel just ahead
 in the stream writes (kv, the cache) is still read after the wait.  The metadata itself
@@ -22,9 +22,8 @@ DEV = torch.device("cuda:0")
 @pytest.fixture(autouse=True)
 def early_metadata(gkr):
     assert gkr.get_pdl()
-    gkr.set_early_metadata(True)
-    yield
-    gkr.set_early_metadata(False)
+    with gkr.launch_policy(early_metadata=True):
+        yield
 
 
 @pytest.mark.parametrize("record", [528, 584, 512, 1024])

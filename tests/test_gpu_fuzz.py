@@ -42,10 +42,8 @@ def _config(seed: int) -> dict:
 def test_random_configuration_matches_oracle(gkr, oracle_mod, seed):
     c = _config(seed)
     staged_min, stream_min = {"short": (BIG, BIG), "staged": (0, BIG), "stream": (BIG, 0)}[c["mode"]]
-    gkr.set_insert_staged_min(staged_min)
-    gkr.set_insert_stream_min(stream_min)
-    gkr.set_early_metadata(c["early"])
-    try:
+    with gkr.launch_policy(insert_staged_min=staged_min, insert_stream_min=stream_min,
+                           early_metadata=c["early"]):
         case = W.random_insert(f"fuzz{seed}", c["T"], 528, c["bs"], c["pages"], c["max_pos"],
                                c["skip"], seed=seed, dist=c["dist"], outlier_rate=c["outliers"])
         record, bs, P = c["record"], c["bs"], c["pages"]
@@ -82,7 +80,3 @@ def test_random_configuration_matches_oracle(gkr, oracle_mod, seed):
         n, first = first_mismatch(got_out.reshape(-1), ref_out.reshape(-1))
         assert n == 0, f"{c}: gather differs at {n} values, first {first}"
         assert int(gerr.item()) == ref_gerr
-    finally:
-        gkr.set_insert_staged_min(-1)
-        gkr.set_insert_stream_min(-1)
-        gkr.set_early_metadata(False)

@@ -176,8 +176,7 @@ def test_gather_v41_sparse_full(gkr, oracle_mod):
 def test_insert_then_gather_same_stream(gkr, oracle_mod, record, pdl):
     """Back-to-back insert -> gather -> insert -> ... on one stream: every gather must
     see the insert queued before it (the programmatic-launch wait keeps stream order)."""
-    gkr.set_pdl(pdl)
-    try:
+    with gkr.launch_policy(pdl=pdl):
         bs, P = 64, 64
         ps = oracle_mod.page_stride(record, bs)
         cache = gkr.alloc_cache(P, bs, record, DEV, fill=0)
@@ -198,8 +197,6 @@ def test_insert_then_gather_same_stream(gkr, oracle_mod, record, pdl):
         torch.cuda.synchronize()
         for out, r in zip(outs, refs):
             _assert_bits_equal(bits_of(out), r)
-    finally:
-        gkr.set_pdl(True)
 
 
 @pytest.mark.parametrize("record", [528, 584, 512, 1024])

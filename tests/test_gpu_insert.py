@@ -25,11 +25,8 @@ def insert_kernel_choice(request, gkr):
     big = 1 << 62
     staged_min, stream_min = {"short": (big, big), "staged": (0, big),
                               "stream": (big, 0)}[request.param]
-    gkr.set_insert_staged_min(staged_min)
-    gkr.set_insert_stream_min(stream_min)
-    yield request.param
-    gkr.set_insert_staged_min(-1)
-    gkr.set_insert_stream_min(-1)
+    with gkr.launch_policy(insert_staged_min=staged_min, insert_stream_min=stream_min):
+        yield request.param
 
 
 def _compare_whole_cache(gkr, oracle_mod, case, pad_units=0):

@@ -73,14 +73,21 @@ def _captured_step(gkr):
     return g
 
 
+@pytest.mark.parametrize("how", ["per_call", "process_default"])
 @pytest.mark.parametrize("pdl", [True, False])
-def test_insert_to_gather_edge_follows_the_pdl_setting(gkr, pdl):
-    before = gkr.get_pdl()
-    gkr.set_pdl(pdl)
-    try:
-        g = _captured_step(gkr)
-    finally:
-        gkr.set_pdl(before)
+def test_insert_to_gather_edge_follows_the_pdl_setting(gkr, pdl, how):
+    """The pdl launch option of the calls (launch_policy), or the process-wide default
+    (gkr_set_pdl) when the calls leave it unset."""
+    if how == "per_call":
+        with gkr.launch_policy(pdl=pdl):
+            g = _captured_step(gkr)
+    else:
+        before = gkr.get_pdl()
+        gkr.set_pdl(pdl)
+        try:
+            g = _captured_step(gkr)
+        finally:
+            gkr.set_pdl(before)
     types = _edge_types(g)
     assert len(types) == 1, types                    # insert -> gather, nothing else
     assert types[0] == (PROGRAMMATIC if pdl else 0), types

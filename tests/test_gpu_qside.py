@@ -1,0 +1,197 @@
+"""GPU parity of the fused attention write (qnorm_rope_kv_insert through the C ABI):
+the KV records byte for byte against the oracle over the whole sentinel-filled cache,
+every query value one of the oracle's two faithful bf16 roundings of the exact result
+(and nearly always the nearest), padded heads zero, the error bits equal."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from helpers import SENTINEL, bf16_from_bits, bits_of, device_inputs, first_mismatch
+from test_oracle_qside import _parse_cases, bf16_bits, csc_row
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _q_case(T, H, record=528, bs=64, seed=0, sigma=2.0, skip=0.1, max_pos=4096):
+    pages = max(2, -(-2 * T // bs))
+    c = W.random_insert(f"q{T}_{H}", T, record, bs, pages, max_pos, skip, seed)
+    rng = np.random.default_rng(seed + 7)
+    q = bf16_bits(rng.standard_normal((T, H, 512)).astype(np.float32) * np.float32(sigma))
+    return c, q
+
+
+def _run(gkr, oracle_mod, c, q, Hp, eps, norm, record, scale=None, in_place=False, **kw):
+    ps = oracle_mod.page_stride(record, c.block_size)
+    kv, slots, pos, csc = device_inputs(c, DEV)
+    cache = gkr.alloc_cache(c.num_pages, c.block_size, record, DEV, fill=SENTINEL)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    qt = bf16_from_bits(q, DEV)
+    sc = None if scale is None else torch.tensor([scale], dtype=torch.float32, device=DEV)
+    q_out = qt if in_place else torch.full((c.num_tokens, Hp, 512), float("nan"),
+                                           dtype=torch.bfloat16, device=DEV)
+    gkr.qnorm_rope_kv_insert(qt, kv, cache, slots, pos, csc, Hp, eps, c.block_size, norm,
+                             q_out=q_out, record=record, err_flag=err, fp8_scale=sc, **kw)
+    torch.cuda.synchronize()
+    ref = np.full(c.num_pages * ps, SENTINEL, np.uint8)
+    rn, alt, ref_err = oracle_mod.qnorm_rope_kv_insert(q, Hp, eps, norm, c.kv, ref, record,
+                                                       c.block_size, c.num_pages, ps, c.slots,
+                                                       c.positions, c.csc, fp8_scale=scale)
+    return gkr.cache_bytes(cache).cpu().numpy(), ref, bits_of(q_out), rn, alt, \
+        int(err.item()), ref_err
+
+
+def _assert_faithful(got, rn, alt, min_nearest=0.999):
+    ok = (got == rn) | (got == alt)
+    bad = np.nonzero(~ok)
+    assert bad[0].size == 0, (f"{bad[0].size} query values off by more than one bf16 step; "
+                              f"first {list(zip(*bad))[:4]} got {got[bad][:4]} "
+                              f"rn {rn[bad][:4]} alt {alt[bad][:4]}")
+    if got.size:
+        assert np.mean(got == rn) >= min_nearest
+
+
+@pytest.mark.parametrize("case", _parse_cases(), ids=lambda c: c["name"])
+def test_golden_heads(gkr, case):
+    """The hand-derived heads through the whole op (one token, slot -1: no KV write)."""
+    q = bf16_bits(case["x"]).reshape(1, 1, 512)
+    kv = torch.zeros(1, 512, dtype=torch.bfloat16, device=DEV)
+    cache = gkr.alloc_cache(2, 32, 528, DEV, fill=SENTINEL)
+    csc = torch.from_numpy(csc_row(case["cos"], case["sin"]).reshape(1, 64)).to(DEV)
+    out = gkr.qnorm_rope_kv_insert(bf16_from_bits(q, DEV), kv, cache,
+                                   torch.tensor([-1], device=DEV), torch.tensor([0], device=DEV),
+                                   csc, 1, case["eps"], 32, case["norm"])
+    got = bits_of(out).reshape(-1)
+    ok = (got == case["rn"]) | (got == case["alt"])
+    assert ok.all(), np.nonzero(~ok)
+    assert (gkr.cache_bytes(cache).cpu().numpy() == SENTINEL).all()
+
+
+@pytest.mark.parametrize("record", [528, 584, 512, 1024])
+@pytest.mark.parametrize("T,H,Hp", [(1, 1, 1), (37, 3, 8), (300, 16, 16), (1000, 5, 64)])
+@pytest.mark.parametrize("norm", [True, False])
+def test_matches_oracle(gkr, oracle_mod, record, T, H, Hp, norm):
+    c, q = _q_case(T, H, seed=T + H + record)
+    scale = 0.05 if record == 512 else None
+    got, ref, qo, rn, alt, err, ref_err = _run(gkr, oracle_mod, c, q, Hp, 1e-6, norm, record,
+                                               scale=scale)
+    n, first = first_mismatch(got, ref)
+    assert n == 0, f"cache: {n} bytes differ, first {first}"
+    assert err == ref_err == 0
+    _assert_faithful(qo, rn, alt)
+    assert (qo[:, H:] == 0).all()
+
+
+@pytest.mark.parametrize("eps", [0.0, 0.5, 30.0])
+@pytest.mark.parametrize("sigma", [1e-12, 1.0, 1e12])
+def test_eps_and_magnitudes(gkr, oracle_mod, eps, sigma):
+    """eps 0 (a pure RMS norm), eps of the data's size, eps dominating; heads from
+    1e-12 to 1e12 (the sum of squares stays inside fp32's normal range)."""
+    c, q = _q_case(200, 4, seed=3, sigma=sigma)
+    got, ref, qo, rn, alt, err, ref_err = _run(gkr, oracle_mod, c, q, 4, eps, True, 528)
+    assert first_mismatch(got, ref)[0] == 0 and err == ref_err == 0
+    _assert_faithful(qo, rn, alt)
+
+
+@pytest.mark.parametrize("record", [528, 584])
+def test_zero_heads_is_kv_insert(gkr, oracle_mod, record):
+    """num_heads_padded = 0: exactly gkr_kv_insert (the KV-only op of the pages)."""
+    c, _ = _q_case(3000, 0, record=record, seed=11)
+    kv, slots, pos, csc = device_inputs(c, DEV)
+    a = gkr.alloc_cache(c.num_pages, 64, record, DEV, fill=SENTINEL)
+    b = gkr.alloc_cache(c.num_pages, 64, record, DEV, fill=SENTINEL)
+    q = torch.empty(c.num_tokens, 0, 512, dtype=torch.bfloat16, device=DEV)
+    gkr.qnorm_rope_kv_insert(q, kv, a, slots, pos, csc, 0, 1e-6, 64, True, record=record)
+    gkr.kv_insert(kv, b, slots, pos, csc, 64, record)
+    torch.cuda.synchronize()
+    assert torch.equal(gkr.cache_bytes(a), gkr.cache_bytes(b))
+
+
+def test_padded_heads_without_query_heads(gkr, oracle_mod):
+    """H = 0, Hp = 4: every q_out head is +0, the KV rows as kv_insert."""
+    c, q = _q_case(50, 0, seed=12)
+    got, ref, qo, rn, alt, err, ref_err = _run(gkr, oracle_mod, c, q, 4, 1e-6, True, 528)
+    assert first_mismatch(got, ref)[0] == 0 and err == ref_err == 0
+    assert (qo == 0).all()
+
+
+def test_in_place(gkr, oracle_mod):
+    """q_out = q (num_heads_padded == num_heads): the heads are replaced by the result."""
+    c, q = _q_case(777, 8, seed=13)
+    got, ref, qo, rn, alt, err, ref_err = _run(gkr, oracle_mod, c, q, 8, 1e-6, True, 528,
+                                               in_place=True)
+    assert first_mismatch(got, ref)[0] == 0
+    _assert_faithful(qo, rn, alt)
+
+
+def test_bad_positions_zero_the_heads_and_flag(gkr, oracle_mod):
+    c, q = _q_case(120, 3, seed=14)
+    c.positions[[5, 50]] = [c.csc.shape[0], -3]
+    c.slots[5] = -1                       # the query side flags it even without a KV write
+    got, ref, qo, rn, alt, err, ref_err = _run(gkr, oracle_mod, c, q, 6, 1e-6, True, 584)
+    assert first_mismatch(got, ref)[0] == 0
+    assert err == ref_err == oracle_mod.ERR_POS
+    assert (qo[[5, 50]] == 0).all()
+    _assert_faithful(qo, rn, alt)
+
+
+def test_bad_fp8_scale_skips_only_the_kv_rows(gkr, oracle_mod):
+    c, q = _q_case(90, 2, seed=15)
+    got, ref, qo, rn, alt, err, ref_err = _run(gkr, oracle_mod, c, q, 2, 1e-6, True, 512,
+                                               scale=float("nan"))
+    assert (got == SENTINEL).all() and first_mismatch(got, ref)[0] == 0
+    assert err == ref_err == oracle_mod.ERR_SCALE
+    _assert_faithful(qo, rn, alt)
+
+
+@pytest.mark.parametrize("opts", [dict(pdl=False), dict(early_metadata=True)])
+def test_launch_options(gkr, oracle_mod, opts):
+    c, q = _q_case(400, 4, seed=16)
+    got, ref, qo, rn, alt, err, ref_err = _run(gkr, oracle_mod, c, q, 8, 1e-6, True, 528,
+                                               launch_opts=gkr.LaunchOpts(**opts))
+    assert first_mismatch(got, ref)[0] == 0
+    _assert_faithful(qo, rn, alt)
+
+
+def test_cuda_graph_replay(gkr, oracle_mod):
+    """Captured once, replayed over new queries / KV rows / slots copied into the captured
+    buffers (the last round with every slot -1)."""
+    T, H, Hp = 500, 4, 8
+    c0, q0 = _q_case(T, H, seed=20)
+    kv, slots, pos, csc = device_inputs(c0, DEV)
+    qt = bf16_from_bits(q0, DEV)
+    cache = gkr.alloc_cache(c0.num_pages, 64, 528, DEV, fill=SENTINEL)
+    out = torch.empty(T, Hp, 512, dtype=torch.bfloat16, device=DEV)
+    fn = lambda: gkr.qnorm_rope_kv_insert(qt, kv, cache, slots, pos, csc, Hp, 1e-6, 64, True,
+                                          q_out=out)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    ps = oracle_mod.page_stride(528, 64)
+    for r in range(3):
+        c, q = _q_case(T, H, seed=21 + r)
+        if r == 2:
+            c.slots[:] = -1
+        cache_bytes = gkr.cache_bytes(cache)
+        cache_bytes.fill_(SENTINEL)
+        kv.copy_(bf16_from_bits(c.kv, DEV))
+        slots.copy_(torch.from_numpy(c.slots))
+        pos.copy_(torch.from_numpy(c.positions))
+        qt.copy_(bf16_from_bits(q, DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = np.full(c.num_pages * ps, SENTINEL, np.uint8)
+        rn, alt, _ = oracle_mod.qnorm_rope_kv_insert(q, Hp, 1e-6, True, c.kv, ref, 528, 64,
+                                                     c.num_pages, ps, c.slots, c.positions,
+                                                     c.csc)
+        assert first_mismatch(cache_bytes.cpu().numpy(), ref)[0] == 0, r
+        _assert_faithful(bits_of(out), rn, alt)
