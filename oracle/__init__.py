@@ -21,6 +21,9 @@ Pinning status (what each function is checked against, on the CPU):
                            group's cos/sin row, NaN -> 0, infinite maxima)
   bf16 / fp8 caches     -- hand-written golden rows; torch bfloat16 / float8_e4m3fn
                            casts of the numpy-float32 rotation and fp32 quotient
+  sparse logits         -- the pinned gather followed by a float64 matrix product (a
+                           library routine); one-hot queries reduce it to the gather,
+                           hand-built records give closed-form sums
   query side (q norm + q rotation) -- closed forms (constant rows, sqrt(2) cases),
                            unit RMS, scale invariance, rotation invariants, hand-written
                            golden heads; zero heads reduce to the KV insert.  The norm
@@ -281,3 +284,40 @@ def qnorm_rope_kv_insert(q: np.ndarray, num_heads_padded: int, eps: float, apply
     if err < 0:
         raise ValueError(f"unknown record width {record}")
     return q_rn, q_alt, err
+
+
+# --- sparse decode logits (the gather fused into its consumer) --------------------
+
+def bf16_to_float(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float64 values (a bf16 is the top half of an fp32)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    with np.errstate(invalid="ignore"):          # NaN patterns stay NaN
+        return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def sparse_logits(q: np.ndarray, cache: np.ndarray, record: int, block_size: int,
+                  num_pages: int, page_stride: int, indices: np.ndarray, sm_scale: float,
+                  fp8_scale: float | None = None):
+    """FlashMLA overview page, DSA section: each query i attends to the entries its
+    index row lists (-1 = invalid), the FP8 entries dequantised to bf16 before the
+    product.  Here: logits[i, h, k] = sm_scale * sum_d q[i, h, d] * K[i, k, d], K the bf16
+    rows of the oracle's gather, computed in float64 (every product of two bf16 values is
+    exact there, and the 512-term sum is within 2^-44 of the exact value relative to the
+    sum of |terms|).  An entry whose gather row is not a record (index -1 or outside the
+    cache, or every entry of an fp8 cache with a bad scale) gives -inf.
+    q: bf16 bits [Q, H, 512]; indices int32 [Q, K].  Returns (logits float64 [Q, H, K],
+    bound float64 [Q, H, K] = |sm_scale| * sum_d |q d * K d|, error bits)."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    idx = np.ascontiguousarray(indices, dtype=np.int32)
+    Q, H = q.shape[0], q.shape[1]
+    rows, err = gather(cache, record, block_size, num_pages, page_stride, idx.reshape(-1),
+                       fp8_scale=fp8_scale)
+    keys = bf16_to_float(rows).reshape(Q, idx.shape[1], 512)
+    qv = bf16_to_float(q)
+    logits = np.matmul(qv, keys.transpose(0, 2, 1)) * float(sm_scale)
+    bound = np.matmul(np.abs(qv), np.abs(keys).transpose(0, 2, 1)) * abs(float(sm_scale))
+    valid = (idx >= 0) & (idx < num_pages * block_size)
+    if record == 512 and not (fp8_scale is not None and np.isfinite(fp8_scale) and fp8_scale > 0):
+        valid[:] = False
+    logits = np.where(valid[:, None, :], logits, -np.inf)
+    return logits, bound, err

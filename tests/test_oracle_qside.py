@@ -228,3 +228,4 @@ def test_bad_position_zeroes_the_heads_and_flags(oracle_mod):
     assert err == oracle_mod.ERR_POS
     assert (rn[[3, 7]] == 0).all() and (alt[[3, 7]] == 0).all()
     assert (rn[[0, 1, 2, 4]] != 0).any()
+
