@@ -98,10 +98,11 @@ def lib() -> ctypes.CDLL:
         L.oracle_decode.restype = None
         L.oracle_gather.argtypes = [vp, i32, i32, i64, i64, vp, i64, vp]
         L.oracle_gather.restype = i32
-        L.oracle_q_head.argtypes = [vp, vp, f64, i32, vp, vp, vp]
+        L.oracle_q_head.argtypes = [vp, vp, f64, i32, vp, vp, vp, vp, vp]
         L.oracle_q_head.restype = None
-        L.oracle_qnorm_rope_kv_insert.argtypes = [vp, i32, i32, f64, i32, vp, vp, vp, i64, vp,
-                                                  i32, i32, i64, i64, vp, vp, vp, i64, f32]
+        L.oracle_qnorm_rope_kv_insert.argtypes = [vp, i32, i32, f64, i32, vp, vp, vp, vp, vp,
+                                                  i64, vp, i32, i32, i64, i64, vp, vp, vp, i64,
+                                                  f32]
         L.oracle_qnorm_rope_kv_insert.restype = i32
         _lib = L
     return _lib
@@ -241,18 +242,19 @@ def page_stride(record: int, block_size: int) -> int:
 
 # --- fused query-side write ------------------------------------------------------
 
-def q_head(q_row: np.ndarray, csc_row: np.ndarray, eps: float, apply_norm: bool = True):
+def q_head(q_row: np.ndarray, csc_row: np.ndarray, eps: float, apply_norm: bool = True,
+           bounds: bool = False):
     """One query head (bf16 bits [512]) -> (exact values float64 [512], nearest-even bf16
-    bits, the other faithful bf16 bits)."""
+    bits, the other faithful bf16 bits), plus with bounds=True the lowest and highest bf16
+    (bits) an fp32 evaluation in any order may give."""
     q_row = np.ascontiguousarray(q_row, dtype=np.uint16)
     csc_row = np.ascontiguousarray(csc_row, dtype=np.float32)
     assert q_row.shape == (512,) and csc_row.shape == (64,)
     exact = np.zeros(512, np.float64)
-    rn = np.zeros(512, np.uint16)
-    alt = np.zeros(512, np.uint16)
+    rn, alt, lo, hi = (np.zeros(512, np.uint16) for _ in range(4))
     lib().oracle_q_head(_ptr(q_row), _ptr(csc_row), float(eps), int(bool(apply_norm)),
-                        _ptr(exact), _ptr(rn), _ptr(alt))
-    return exact, rn, alt
+                        _ptr(exact), _ptr(rn), _ptr(alt), _ptr(lo), _ptr(hi))
+    return (exact, rn, alt, lo, hi) if bounds else (exact, rn, alt)
 
 
 def qnorm_rope_kv_insert(q: np.ndarray, num_heads_padded: int, eps: float, apply_norm: bool,
@@ -261,8 +263,9 @@ def qnorm_rope_kv_insert(q: np.ndarray, num_heads_padded: int, eps: float, apply
                          positions: np.ndarray, csc: np.ndarray,
                          fp8_scale: float | None = None):
     """The fused op on the host: q bf16 bits [T, H, 512]; the KV rows go into the flat
-    cache in place.  Returns (q_rn, q_alt, error bits): the nearest-even bf16 query output
-    [T, num_heads_padded, 512] and the other faithful rounding of each value."""
+    cache in place.  Returns (q_rn, q_alt, q_lo, q_hi, error bits): the nearest-even bf16
+    query output [T, num_heads_padded, 512], the other faithful rounding of each value,
+    and the lowest / highest bf16 an fp32 evaluation in any order may give."""
     q = np.ascontiguousarray(q, dtype=np.uint16)
     T = int(np.asarray(slots).shape[0])
     q = q.reshape(T, -1, 512)
@@ -274,16 +277,16 @@ def qnorm_rope_kv_insert(q: np.ndarray, num_heads_padded: int, eps: float, apply
     csc = np.ascontiguousarray(csc, dtype=np.float32).reshape(-1, 64)
     assert cache.dtype == np.uint8 and cache.flags["C_CONTIGUOUS"]
     assert kv.shape[0] == T and positions.shape[0] == T
-    q_rn = np.zeros((T, num_heads_padded, 512), np.uint16)
-    q_alt = np.zeros((T, num_heads_padded, 512), np.uint16)
+    q_rn, q_alt, q_lo, q_hi = (np.zeros((T, num_heads_padded, 512), np.uint16)
+                               for _ in range(4))
     err = lib().oracle_qnorm_rope_kv_insert(
         _ptr(q), H, int(num_heads_padded), float(eps), int(bool(apply_norm)), _ptr(q_rn),
-        _ptr(q_alt), _ptr(kv), T, _ptr(cache), record, block_size, num_pages, page_stride,
-        _ptr(slots), _ptr(positions), _ptr(csc), csc.shape[0],
+        _ptr(q_alt), _ptr(q_lo), _ptr(q_hi), _ptr(kv), T, _ptr(cache), record, block_size,
+        num_pages, page_stride, _ptr(slots), _ptr(positions), _ptr(csc), csc.shape[0],
         1.0 if fp8_scale is None else fp8_scale)
     if err < 0:
         raise ValueError(f"unknown record width {record}")
-    return q_rn, q_alt, err
+    return q_rn, q_alt, q_lo, q_hi, err
 
 
 # --- sparse decode logits (the gather fused into its consumer) --------------------

@@ -562,9 +562,15 @@ ORACLE_EXPORT int oracle_kv_gather(const uint8_t *cache, int record, int block_s
  * the token's cos/sin row, as for the KV row; the result is written as bf16 to
  * q_out [T, Hp, 512]; heads H .. Hp-1 of q_out are written as +0.  The arithmetic
  * order inside the norm is not fixed by anything, so the oracle evaluates the
- * definition in double (every step exact or correctly rounded in binary64), and a
- * result counts as right when it is one of the two bf16 values around that exact
- * value (a faithful rounding); the rounded-to-nearest one is returned too. */
+ * definition in double (every step exact or correctly rounded in binary64) and gives,
+ * beside the exact value and its nearest bf16, the range of bf16 values that an fp32
+ * evaluation in any order may round to: [RD(y - delta), RU(y + delta)] with
+ * delta = 2^-19 * |y| for dims 0..447 and delta = 2^-19 * (|e c| + |o s|) (resp.
+ * |o c| + |e s|) for a rotated pair, e and o the normed values.  2^-19 bounds, with a
+ * factor 2 to spare, the fp32 errors of the sum of squares (at most 21 roundings on a
+ * positive sum), the added eps, the reciprocal square root, the scaling, and the two
+ * rounded products and the sum or difference of the rotation; the rotated dims take
+ * the size of the products, not of the result, because e c - o s can cancel. */
 
 /* The bf16 value next to `rn` in the direction of y (rn itself when it equals y).
  * rn is the nearest-even bf16 of y. */
@@ -580,14 +586,29 @@ static uint16_t bf16_toward(uint16_t rn, double y)
     return zero ? (uint16_t)0x8001 : (uint16_t)(neg ? rn + 1 : rn - 1);
 }
 
+/* The largest bf16 not above y, and the smallest not below it. */
+static uint16_t bf16_down(double y)
+{
+    uint16_t b = oracle_bf16_encode(y);
+    return oracle_bf16_value(b) > y ? bf16_toward(b, -INFINITY) : b;
+}
+
+static uint16_t bf16_up(double y)
+{
+    uint16_t b = oracle_bf16_encode(y);
+    return oracle_bf16_value(b) < y ? bf16_toward(b, INFINITY) : b;
+}
+
 /* One query head: exact[d] = the normed and rotated value of dim d (double);
  * rn[d] = its nearest-even bf16, alt[d] = the other faithful bf16 (== rn when the
- * value is a bf16).  eps >= 0; a zero row with eps = 0 is outside the contract. */
+ * value is a bf16); lo[d] .. hi[d] = the bf16 values an fp32 evaluation may give (see
+ * above).  eps >= 0; a zero row with eps = 0 is outside the contract. */
 ORACLE_EXPORT void oracle_q_head(const uint16_t *q_row, const float *csc_row, double eps,
                                  int apply_norm, double exact[512], uint16_t rn[512],
-                                 uint16_t alt[512])
+                                 uint16_t alt[512], uint16_t lo[512], uint16_t hi[512])
 {
-    double x[512], r = 1.0, ss = 0.0;
+    double x[512], size[512], r = 1.0, ss = 0.0;
+    const double rel = ldexp(1.0, -19);
     int d, j;
     for (d = 0; d < 512; d++)
         x[d] = oracle_bf16_value(q_row[d]);
@@ -598,16 +619,22 @@ ORACLE_EXPORT void oracle_q_head(const uint16_t *q_row, const float *csc_row, do
         for (d = 0; d < 512; d++)
             x[d] *= r;
     }
+    for (d = 0; d < 448; d++)
+        size[d] = fabs(x[d]);
     for (j = 0; j < 32; j++) {
         double e = x[448 + 2 * j], o = x[449 + 2 * j];
         double c = csc_row[j], s = csc_row[32 + j];
         x[448 + 2 * j] = e * c - o * s;
         x[449 + 2 * j] = o * c + e * s;
+        size[448 + 2 * j] = fabs(e * c) + fabs(o * s);
+        size[449 + 2 * j] = fabs(o * c) + fabs(e * s);
     }
     for (d = 0; d < 512; d++) {
         exact[d] = x[d];
         rn[d] = oracle_bf16_encode(x[d]);
         alt[d] = bf16_toward(rn[d], x[d]);
+        lo[d] = bf16_down(x[d] - rel * size[d]);
+        hi[d] = bf16_up(x[d] + rel * size[d]);
     }
 }
 
@@ -618,12 +645,14 @@ ORACLE_EXPORT void oracle_q_head(const uint16_t *q_row, const float *csc_row, do
  *   otherwise heads h < num_heads are written by oracle_q_head, heads
  *     num_heads .. num_heads_padded - 1 as +0;
  *   the KV row is inserted exactly as oracle_kv_insert does (slot < 0 skips it).
- * q_rn / q_alt: uint16 [T, num_heads_padded, 512].  Returns the error bits, or -1
- * for an unknown record width. */
+ * q_rn / q_alt / q_lo / q_hi: uint16 [T, num_heads_padded, 512] (see oracle_q_head;
+ * zero heads give 0 in all four).  Returns the error bits, or -1 for an unknown record
+ * width. */
 ORACLE_EXPORT int oracle_qnorm_rope_kv_insert(const uint16_t *q_in, int num_heads,
                                               int num_heads_padded, double eps,
                                               int apply_norm, uint16_t *q_rn,
-                                              uint16_t *q_alt, const uint16_t *kv,
+                                              uint16_t *q_alt, uint16_t *q_lo,
+                                              uint16_t *q_hi, const uint16_t *kv,
                                               int64_t num_tokens, uint8_t *cache, int record,
                                               int block_size, int64_t num_pages,
                                               int64_t page_stride, const int64_t *slots,
@@ -633,6 +662,7 @@ ORACLE_EXPORT int oracle_qnorm_rope_kv_insert(const uint16_t *q_in, int num_head
     int64_t t;
     int h, err;
     double exact[512];
+    uint16_t *out[4];
     err = insert_general(kv, num_tokens, cache, record, block_size, num_pages, page_stride,
                          slots, positions, csc, max_pos, 1, 0, fp8_scale);
     if (err < 0)
@@ -640,15 +670,19 @@ ORACLE_EXPORT int oracle_qnorm_rope_kv_insert(const uint16_t *q_in, int num_head
     for (t = 0; t < num_tokens; t++) {
         int64_t pos = positions[t];
         for (h = 0; h < num_heads_padded; h++) {
-            uint16_t *rn = q_rn + (t * num_heads_padded + h) * 512;
-            uint16_t *alt = q_alt + (t * num_heads_padded + h) * 512;
+            int64_t at = (t * num_heads_padded + h) * 512;
+            int k;
+            out[0] = q_rn + at;
+            out[1] = q_alt + at;
+            out[2] = q_lo + at;
+            out[3] = q_hi + at;
             if (h >= num_heads || pos < 0 || pos >= max_pos) {
-                memset(rn, 0, 512 * sizeof(uint16_t));
-                memset(alt, 0, 512 * sizeof(uint16_t));
+                for (k = 0; k < 4; k++)
+                    memset(out[k], 0, 512 * sizeof(uint16_t));
                 continue;
             }
             oracle_q_head(q_in + (t * num_heads + h) * 512, csc + pos * 64, eps, apply_norm,
-                          exact, rn, alt);
+                          exact, out[0], out[1], out[2], out[3]);
         }
         if (num_heads > 0 && (pos < 0 || pos >= max_pos))
             err |= ORACLE_ERR_POS;

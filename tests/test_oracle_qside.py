@@ -191,7 +191,7 @@ def test_zero_heads_is_the_kv_insert(oracle_mod, record):
     ps = oracle_mod.page_stride(record, c.block_size)
     a = np.full(c.num_pages * ps, 0xA5, np.uint8)
     b = a.copy()
-    rn, alt, err = oracle_mod.qnorm_rope_kv_insert(np.zeros((c.num_tokens, 0, HEAD), np.uint16),
+    rn, alt, _, _, err = oracle_mod.qnorm_rope_kv_insert(np.zeros((c.num_tokens, 0, HEAD), np.uint16),
                                                    0, 1e-6, True, c.kv, a, record, c.block_size,
                                                    c.num_pages, ps, c.slots, c.positions, c.csc)
     assert rn.shape == (c.num_tokens, 0, HEAD)
@@ -205,12 +205,13 @@ def test_heads_padded_and_kv_untouched_by_q(oracle_mod):
     ps = oracle_mod.page_stride(528, c.block_size)
     a = np.full(c.num_pages * ps, 0xA5, np.uint8)
     b = a.copy()
-    rn, alt, err = oracle_mod.qnorm_rope_kv_insert(q, 8, 1e-6, True, c.kv, a, 528, c.block_size,
+    rn, alt, lo, hi, err = oracle_mod.qnorm_rope_kv_insert(q, 8, 1e-6, True, c.kv, a, 528, c.block_size,
                                                    c.num_pages, ps, c.slots, c.positions, c.csc)
     oracle_mod.insert(c.kv, b, 528, c.block_size, c.num_pages, ps, c.slots, c.positions, c.csc)
     assert err == 0 and np.array_equal(a, b)
     assert rn.shape == (c.num_tokens, 8, HEAD)
     assert (rn[:, 3:] == 0).all() and (alt[:, 3:] == 0).all()
+    assert (lo[:, 3:] == 0).all() and (hi[:, 3:] == 0).all()
     # every token's heads (skipped slots too) are the per-head oracle at its position
     for t in (0, 1, c.num_tokens - 1):
         for h in range(3):
@@ -223,9 +224,38 @@ def test_bad_position_zeroes_the_heads_and_flags(oracle_mod):
     c, q = _op_case(bad_pos=True)
     ps = oracle_mod.page_stride(528, c.block_size)
     a = np.full(c.num_pages * ps, 0xA5, np.uint8)
-    rn, alt, err = oracle_mod.qnorm_rope_kv_insert(q, 3, 1e-6, False, c.kv, a, 528, c.block_size,
+    rn, alt, lo, hi, err = oracle_mod.qnorm_rope_kv_insert(q, 3, 1e-6, False, c.kv, a, 528, c.block_size,
                                                    c.num_pages, ps, c.slots, c.positions, c.csc)
     assert err == oracle_mod.ERR_POS
-    assert (rn[[3, 7]] == 0).all() and (alt[[3, 7]] == 0).all()
+    assert (rn[[3, 7]] == 0).all() and (alt[[3, 7]] == 0).all() and (hi[[3, 7]] == 0).all()
     assert (rn[[0, 1, 2, 4]] != 0).any()
 
+
+
+def test_fp32_evaluation_range(oracle_mod):
+    """lo .. hi (the bf16 values an fp32 evaluation may give) contain the faithful pair;
+    for dims 0..447 they are exactly that pair (2^-19 |y| is far inside half a bf16
+    step); for a rotated pair whose terms cancel the range follows the size of the
+    products; a slip in the rotation (the sine's sign flipped) leaves it."""
+    rng = np.random.default_rng(6)
+    csc = W.cos_sin_table(4096)
+    q = _random_head(rng)
+    row = csc[1234]
+    exact, rn, alt, lo, hi = oracle_mod.q_head(q, row, 1e-6, True, bounds=True)
+    vl, vh, vr, va = _value(lo), _value(hi), _value(rn), _value(alt)
+    assert (vl <= np.minimum(vr, va)).all() and (np.maximum(vr, va) <= vh).all()
+    assert np.array_equal(np.minimum(vr, va)[:448], vl[:448])
+    assert np.array_equal(np.maximum(vr, va)[:448], vh[:448])
+    # a pair that cancels: (e, o) = (1, 1) turned by 45 degrees: e c - o s = 0 exactly in
+    # real arithmetic but not for the fp32 cos/sin of 45 degrees
+    x = np.zeros(HEAD, np.float32)
+    x[448], x[449] = 1.0, 1.0
+    c45 = np.float32(np.cos(np.pi / 4))
+    s45 = np.float32(np.sin(np.pi / 4))
+    e2, _, _, lo2, hi2 = oracle_mod.q_head(bf16_bits(x), csc_row(c45, s45), 0.0, False,
+                                           bounds=True)
+    assert abs(e2[448]) < 1e-7 and _value(hi2)[448] - _value(lo2)[448] >= 2 * 2.0 ** -19
+    # the same head with the sine's sign flipped lands outside the range
+    wrong, _, _ = oracle_mod.q_head(q, np.concatenate([row[:32], -row[32:]]), 1e-6, True)
+    outside = (wrong[448:] < vl[448:]) | (wrong[448:] > vh[448:])
+    assert outside.mean() > 0.9
