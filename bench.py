@@ -300,6 +300,20 @@ def qside_bytes(slots: np.ndarray, record: int, num_heads: int, num_heads_padded
     return insert_bytes(slots, record) + T * 1024 * (num_heads + num_heads_padded)
 
 
+def logits_bytes(indices: np.ndarray, record: int, num_heads: int) -> int:
+    """Algorithmic bytes of one sparse-logits launch: per query its heads read (num_heads
+    x 1024 B) and its logits written (num_heads x topk x 4 B); per entry its index (4 B)
+    and, when valid, its record (or cache row) read."""
+    idx = np.asarray(indices)
+    Q, K = idx.shape
+    return Q * num_heads * (1024 + 4 * K) + 4 * idx.size + int((idx >= 0).sum()) * record
+
+
+def logits_flops(indices: np.ndarray, num_heads: int) -> int:
+    """Tensor-core FLOPs of one sparse-logits launch: 2 x 512 per (query, head, entry)."""
+    return 2 * 512 * num_heads * int(np.asarray(indices).size)
+
+
 def gather_bytes(indices: np.ndarray, record: int) -> int:
     """Algorithmic bytes of one gather: 4 B index + 1024 B bf16 row written per
     index, plus the record read for every valid index."""
@@ -901,6 +915,7 @@ def sweep(device, peak):
     idx = torch.from_numpy(case.indices).to(device)
     outs = [torch.empty(case.indices.shape + (512,), dtype=torch.bfloat16, device=device)
             for _ in range(2)]
+    res.update(sparse_logits_entries(torch, gkr, W, case, kv, idx, device, peak, timed))
     for record, name in ((528, "gather_v41_sparse"), (584, "gather_v4_sparse"),
                          (512, "gather_fp8_sparse"), (1024, "gather_bf16_sparse")):
         sc = scale if record == 512 else None
@@ -918,6 +933,43 @@ def sweep(device, peak):
                      if record == 528 else None}
         del cache
         torch.cuda.empty_cache()
+    return res
+
+
+def sparse_logits_entries(torch, gkr, W, case, kv, idx, device, peak, timed) -> dict:
+    """The dequant-gather fused into its consumer: logits of 128 decode queries x 128 heads
+    over their 2048 top-k records of the 1M-token V4.1 cache, against the same result
+    computed unfused (kv_gather to bf16 rows, then torch's bf16 batched matmul)."""
+    res = {}
+    cache = gkr.alloc_cache(case.num_pages, 64, 528, device, fill=0)
+    gkr.kv_insert(kv, cache, torch.from_numpy(case.slots).to(device),
+                  torch.from_numpy(case.positions).to(device),
+                  torch.from_numpy(case.csc).to(device), 64, 528)
+    Q, K = case.indices.shape
+    H = 128
+    q = torch.from_numpy(W.decode_queries(Q, H).view(np.int16)).view(torch.bfloat16).to(device)
+    outs = [torch.empty(Q, H, K, dtype=torch.float32, device=device) for _ in range(2)]
+    ms = timed(lambda o: gkr.sparse_logits(q, cache, idx, 512 ** -0.5, out=o), outs)
+    b, f = logits_bytes(case.indices, 528, H), logits_flops(case.indices, H)
+    res["sparse_logits_v41_128x2048_h128"] = {
+        "kernel": "sparse_logits_kernel", "queries": Q, "topk": K, "heads": H, "us": ms * 1e3,
+        "entries_per_s": Q * K / (ms * 1e-3), "alg_bytes": b, "alg_gbs": b / (ms * 1e-3) / 1e9,
+        "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak, "tflops": f / (ms * 1e-3) / 1e12,
+        "bound": "hbm"}
+    rows = torch.empty(Q, K, 512, dtype=torch.bfloat16, device=device)
+    outs_bf16 = [torch.empty(Q, H, K, dtype=torch.bfloat16, device=device) for _ in range(2)]
+
+    def unfused(o):
+        gkr.kv_gather(cache, idx, rows)
+        torch.bmm(q, rows.transpose(1, 2), out=o)
+    ms_u = timed(unfused, outs_bf16)
+    res["sparse_logits_unfused_gather_then_bmm"] = {
+        "us": ms_u * 1e3, "what": "kv_gather into bf16 [128, 2048, 512], then torch.bmm of the "
+                                  "same queries (bf16 logits: half the fused path's fp32 "
+                                  "output bytes): the unfused path",
+        "fused_speedup": ms_u / ms}
+    del cache, rows, outs, outs_bf16
+    torch.cuda.empty_cache()
     return res
 
 

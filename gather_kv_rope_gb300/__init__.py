@@ -11,20 +11,23 @@ ctypes.  PyTorch supplies device memory and streams only.
                       compress_ratio, sanitize_nans)
     qnorm_rope_kv_insert(q, kv, k_cache, slot_mapping, positions, cos_sin_cache,
                          num_heads_padded, eps, block_size, apply_q_norm)
+    sparse_logits(q, k_cache, indices, sm_scale)
 
 Every call takes launch_opts=LaunchOpts(...); `with launch_policy(...)` sets them for
 the calls of the current thread (context).
 """
 from .build import build as _build_lib
-from ._binding import (CacheDesc, ERR_INDEX, ERR_POS, ERR_SCALE, ERR_SLOT, GkrError, LaunchOpts,
+from ._binding import (CacheDesc, ERR_INDEX, ERR_POS, ERR_SCALE, ERR_SLOT, ERR_TIMEOUT, GkrError,
+                       LaunchOpts,
                        PACKED, RECORDS, alloc_cache, cache_bytes, get_early_metadata,
                        get_insert_staged_min, get_insert_stream_min, get_pdl,
                        insert_kernel_for, kv_gather, kv_insert, launch_policy, lib,
                        library_path, page_stride, qnorm_rope_kv_insert, record_rows,
                        rope_quant_insert, set_early_metadata, set_insert_staged_min,
-                       set_insert_stream_min, set_pdl, status_string)
+                       set_insert_stream_min, set_pdl, sparse_logits, status_string)
 
 __all__ = ["build", "kv_insert", "kv_gather", "rope_quant_insert", "qnorm_rope_kv_insert",
+           "sparse_logits", "ERR_TIMEOUT",
            "LaunchOpts", "launch_policy", "page_stride", "record_rows",
            "alloc_cache", "cache_bytes", "status_string", "set_pdl", "get_pdl",
            "set_early_metadata", "get_early_metadata", "set_insert_stream_min",

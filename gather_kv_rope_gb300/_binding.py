@@ -28,6 +28,7 @@ ERR_SLOT = 1
 ERR_POS = 2
 ERR_INDEX = 4
 ERR_SCALE = 8
+ERR_TIMEOUT = 16
 
 # cache formats by record width (bytes a token occupies): the packed MXFP8 records
 # (uint8 [pages, block, 528 | 584]) and the plain caches of 512 elements a row
@@ -141,6 +142,11 @@ def lib() -> ctypes.CDLL:
                                                        i64, vp, ctypes.POINTER(CacheDesc), vp, vp,
                                                        vp, i64, vp, vp, opt, vp]
                 L.gkr_qnorm_rope_kv_insert.restype = ctypes.c_int
+                # q, H, k_cache, desc, indices, Q, topk, sm_scale, fp8_scale, out, err, opts,
+                # stream
+                L.gkr_sparse_logits.argtypes = [vp, i32, vp, ctypes.POINTER(CacheDesc), vp, i64,
+                                                i64, ctypes.c_float, vp, vp, vp, opt, vp]
+                L.gkr_sparse_logits.restype = ctypes.c_int
                 L.gkr_status_string.argtypes, L.gkr_status_string.restype = [ctypes.c_int], \
                     ctypes.c_char_p
                 L.gkr_last_cuda_error.argtypes, L.gkr_last_cuda_error.restype = [], i32
@@ -468,3 +474,35 @@ def qnorm_rope_kv_insert(q: torch.Tensor, kv: torch.Tensor, k_cache: torch.Tenso
                                             _ptr(err_flag), _opts(launch_opts), stream)
     _raise(st)
     return q_out
+
+
+def sparse_logits(q: torch.Tensor, k_cache: torch.Tensor, indices: torch.Tensor,
+                  sm_scale: float, out: torch.Tensor | None = None,
+                  err_flag: torch.Tensor | None = None, fp8_scale: torch.Tensor | None = None,
+                  launch_opts: LaunchOpts | None = None) -> torch.Tensor:
+    """Sparse decode logits with the dequant-gather fused in: for query i, head h and
+    entry k, out[i, h, k] = sm_scale * q[i, h, :] . K, K the bf16 row kv_gather returns
+    for indices[i, k] (-1, or an index outside the cache: -inf).  q bf16 [Q, H, 512]
+    (H <= 128), indices int32 [Q, topk] (topk a multiple of 4), out fp32 [Q, H, topk]
+    (allocated when None).  Returns out."""
+    desc = _cache_desc(k_cache)
+    _check_fp8_scale(desc, fp8_scale)
+    _check(q.dtype == torch.bfloat16 and q.dim() == 3 and q.shape[2] == HEAD_DIM
+           and q.is_contiguous(), "q must be a contiguous bf16 tensor [queries, heads, 512]")
+    _check(indices.dtype == torch.int32 and indices.dim() == 2 and indices.is_contiguous()
+           and indices.shape[0] == q.shape[0],
+           "indices must be a contiguous int32 tensor [queries, topk]")
+    Q, H, K = int(q.shape[0]), int(q.shape[1]), int(indices.shape[1])
+    if out is None:
+        out = torch.empty(Q, H, K, dtype=torch.float32, device=q.device)
+    _check(out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (Q, H, K),
+           "out must be a contiguous fp32 tensor [queries, heads, topk]")
+    _check_err_flag(err_flag)
+    dev = _same_cuda_device(q, k_cache, indices, out, err_flag, fp8_scale)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        st = lib().gkr_sparse_logits(_ptr(q), H, _ptr(k_cache), ctypes.byref(desc), _ptr(indices),
+                                     Q, K, float(sm_scale), _ptr(fp8_scale), _ptr(out),
+                                     _ptr(err_flag), _opts(launch_opts), stream)
+    _raise(st)
+    return out

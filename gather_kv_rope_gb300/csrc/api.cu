@@ -341,6 +341,48 @@ GKR_API gkr_status gkr_qnorm_rope_kv_insert(const void* q_in, int32_t num_heads,
     return cuda_status(gkr::launch_qnorm_rope_kv_insert(cache->record, p, qp, stream));
 }
 
+GKR_API gkr_status gkr_sparse_logits(const void* q, int32_t num_heads, const void* k_cache,
+                                     const gkr_cache_desc* cache, const int32_t* indices,
+                                     int64_t num_queries, int64_t topk, float sm_scale,
+                                     const float* fp8_scale, float* out, int32_t* err_flag,
+                                     const gkr_launch_opts* opts, cudaStream_t stream) {
+    RecordRows rows;
+    gkr_status st = check_cache(cache, &rows);
+    if (st != GKR_OK) return st;
+    Policy pol;
+    st = resolve_policy(opts, &pol);
+    if (st != GKR_OK) return st;
+    if (num_queries < 0 || topk < 0 || topk % 4 != 0 || topk > INT64_C(0x7FFFFFFF) ||
+        num_heads < 1 || num_heads > gkr::logits_max_heads() ||
+        !(sm_scale >= -3.40282347e38f && sm_scale <= 3.40282347e38f))
+        return GKR_EINVAL;
+    if (num_queries == 0 || topk == 0) return GKR_OK;
+    if (!q || !k_cache || !indices || !out) return GKR_EINVAL;
+    const bool fp8 = cache->record == 512;
+    if (fp8 && !fp8_scale) return GKR_EINVAL;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(out, 16) || !aligned(indices, 4) ||
+        !aligned(err_flag, 4) || (fp8 && !aligned(fp8_scale, 4)))
+        return GKR_EALIGN;
+    gkr::LogitsParams p;
+    p.q = q;
+    p.num_heads = num_heads;
+    p.cache = static_cast<const uint8_t*>(k_cache);
+    p.page_stride = cache->page_stride;
+    p.block_size = cache->block_size;
+    p.num_slots = static_cast<int32_t>(cache->num_pages * cache->block_size);
+    p.indices = indices;
+    p.num_queries = num_queries;
+    p.topk = topk;
+    p.chunks = (topk + gkr::logits_chunk_keys() - 1) / gkr::logits_chunk_keys();
+    if (num_queries > INT64_C(0x7FFFFFFF) / p.chunks) return GKR_EINVAL;   // grid < 2^31
+    p.sm_scale = sm_scale;
+    p.fp8_scale = fp8 ? fp8_scale : nullptr;
+    p.out = out;
+    p.err = err_flag;
+    p.pdl = pol.pdl;
+    return cuda_status(gkr::launch_sparse_logits(cache->record, p, stream));
+}
+
 GKR_API const char* gkr_status_string(gkr_status status) {
     switch (status) {
         case GKR_OK: return "ok";
@@ -359,6 +401,6 @@ GKR_API const char* gkr_status_string(gkr_status status) {
 
 GKR_API int32_t gkr_last_cuda_error(void) { return g_last_cuda_error; }
 
-GKR_API int32_t gkr_version(void) { return 30000; }
+GKR_API int32_t gkr_version(void) { return 30100; }
 
 }  // extern "C"

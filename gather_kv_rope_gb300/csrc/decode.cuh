@@ -1,0 +1,106 @@
+// Record decode shared by the gather (gather.cu) and the fused gather + logits kernel
+// (logits.cu): one warp loads one cache record (any of the four formats) with the lane
+// layout of device.cuh and dequantises it to the bf16 row kv_gather returns.
+//
+// Operation (page "PR #56893 [DSv4.1] Store the whole KV in MXFP8 (FlashMLA V4.1
+// record)", section "实现拆解" item 4: the gather reads a record by its width and
+// dequantises e4m3 * 2^(scale - 127) per group -- 512 dims in 32-dim groups for V4.1,
+// 448 dims in 64-dim groups plus a copied bf16 tail for V4; the plain caches copy bf16
+// rows or multiply e4m3 rows by the cache's scale).
+#pragma once
+
+#include "device.cuh"
+#include "launch.h"
+
+namespace gkr {
+namespace {
+
+// Read-only loads that do not allocate in L1 (each record is read once).
+__device__ __forceinline__ uint2 ldg_na8(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint4 ldg_na16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_u8(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+struct Loaded {
+    uint4 a;        // codes of chunk A (.x, .y) or, for bf16 rows, 8 bf16
+    uint4 b;        // codes of chunk B (.x, .y) or, for the V4 tail lanes / bf16 rows, 8 bf16
+    uint32_t sa, sb;
+    bool valid;
+};
+
+// Per-lane base pointers: every load of a record is one 64-bit add away.
+struct LaneBases {
+    const uint8_t* a;      // cache + 8L (16L for bf16 rows): chunk A (chunk B at +256 / +512)
+    const uint8_t* tail;   // V4, lanes 24..31: cache + 448 + 16 (L - 24)
+    const uint8_t* s;      // cache + scale byte of chunk A (chunk B's at +8 / +4)
+};
+
+template <int kRecord>
+__device__ __forceinline__ void load_record(int64_t off, int64_t soff, const LaneBases& lb,
+                                            int lane, Loaded& r) {
+    r.valid = off >= 0;
+    if (!r.valid) return;
+    if constexpr (kRecord == 1024) {
+        r.a = ldg_na16(lb.a + off);
+        r.b = ldg_na16(lb.a + off + 512);
+        return;
+    }
+    const uint2 ta = ldg_na8(lb.a + off);
+    r.a = make_uint4(ta.x, ta.y, 0u, 0u);
+    if constexpr (kRecord == 512) {
+        const uint2 t = ldg_na8(lb.a + off + 256);
+        r.b = make_uint4(t.x, t.y, 0u, 0u);
+        return;
+    }
+    r.sa = ldg_u8(lb.s + soff);
+    if (kRecord == 528) {
+        const uint2 t = ldg_na8(lb.a + off + 256);
+        r.b = make_uint4(t.x, t.y, 0u, 0u);
+        r.sb = ldg_u8(lb.s + soff + 8);
+    } else if (lane < 24) {
+        const uint2 t = ldg_na8(lb.a + off + 256);
+        r.b = make_uint4(t.x, t.y, 0u, 0u);
+        r.sb = ldg_u8(lb.s + soff + 4);
+    } else {
+        r.b = ldg_na16(lb.tail + off);
+        r.sb = 0u;
+    }
+}
+
+// Dequantise a loaded record into this lane's two 16-byte pieces of the bf16 row (chunk
+// A = dims [8L, 8L+8), chunk B = dims [256+8L, 256+8L+8)); an invalid record gives zeros.
+template <int kRecord>
+__device__ __forceinline__ void convert(const Loaded& r, int lane, float scale, uint4& oa,
+                                        uint4& ob) {
+    oa = make_uint4(0u, 0u, 0u, 0u);
+    ob = oa;
+    if (r.valid) {
+        if constexpr (kRecord == 1024) {
+            oa = r.a;
+            ob = r.b;
+        } else if constexpr (kRecord == 512) {
+            oa = dequant8_scaled(make_uint2(r.a.x, r.a.y), scale);
+            ob = dequant8_scaled(make_uint2(r.b.x, r.b.y), scale);
+        } else {
+            oa = dequant8(make_uint2(r.a.x, r.a.y), r.sa);
+            if (kRecord == 528 || lane < 24) ob = dequant8(make_uint2(r.b.x, r.b.y), r.sb);
+            else ob = r.b;
+        }
+    }
+}
+
+}  // namespace
+}  // namespace gkr

@@ -53,6 +53,25 @@ struct QSideParams {
     int32_t apply_norm;        // 1: divide each head by sqrt(mean(x^2) + eps)
 };
 
+// Validated arguments of one fused gather + logits launch (gkr_sparse_logits).
+struct LogitsParams {
+    const void* q;             // bf16 [num_queries, num_heads, 512]
+    int32_t num_heads;         // 1 .. logits_max_heads()
+    const uint8_t* cache;
+    int64_t page_stride;
+    int32_t block_size;
+    int32_t num_slots;
+    const int32_t* indices;    // [num_queries, topk]
+    int64_t num_queries;
+    int64_t topk;              // a multiple of 4
+    int64_t chunks;            // ceil(topk / logits_chunk_keys())
+    float sm_scale;
+    const float* fp8_scale;    // fp8 rows (record 512): the cache's scale; else unused
+    float* out;                // fp32 [num_queries, num_heads, topk]
+    int32_t* err;              // nullable
+    int32_t pdl;
+};
+
 // Row geometry of the four cache formats ("record" = bytes a token occupies):
 //   528  V4.1 MXFP8 record: 512 B e4m3 data row + 16 B scale row;
 //   584  V4 record: 576 B data row (448 e4m3 + 64 bf16) + 8 B scale row;
@@ -163,6 +182,10 @@ cudaError_t launch_rope_quant_insert_v4(const InsertParams& p, bool sanitize,
 // the four cache formats), in one launch.
 cudaError_t launch_qnorm_rope_kv_insert(int32_t record, const InsertParams& p,
                                         const QSideParams& qp, cudaStream_t stream);
+// Sparse decode logits from the cache records, gathered and dequantised on chip.
+cudaError_t launch_sparse_logits(int32_t record, const LogitsParams& p, cudaStream_t stream);
+int32_t logits_chunk_keys();   // keys per CTA
+int32_t logits_max_heads();    // heads per query at most
 cudaError_t launch_gather_v41(const GatherParams& p, cudaStream_t stream);
 cudaError_t launch_gather_v4(const GatherParams& p, cudaStream_t stream);
 cudaError_t launch_gather_fp8(const GatherParams& p, cudaStream_t stream);

@@ -1,0 +1,349 @@
+// The dequant-gather fused into its consumer: sparse decode logits.
+//
+// Operation (FlashMLA overview page, DSA section: each decode query attends to the top-k
+// cache entries listed by its index row, -1 marking an invalid entry, and FP8 entries
+// are dequantised to bf16 before the matrix product; page "PR #56893 [DSv4.1] Store the
+// whole KV in MXFP8 (FlashMLA V4.1 record)", section "实现拆解" item 4, for the dequant):
+//   out[q, h, k] = sm_scale * sum_d Q[q, h, d] * K[q, k, d]
+// where K[q, k, :] is exactly the bf16 row kv_gather returns for index indices[q, k];
+// an invalid index (-1) gives -inf, and so does an index outside the cache (which also
+// sets GKR_ERR_INDEX).  The gathered rows never leave the SM: the bf16 intermediate that
+// kv_gather writes (1 KB per index) and a separate product kernel reads back is gone.
+//
+// Launch shape (sm_103a, 5th-generation tensor cores): one CTA of 8 warps per (query,
+// chunk of kChunk keys).  The query's heads (up to 128, zero-padded) are staged once
+// into shared memory as the A operand (M = 128 rows x K = 512, bf16, K-major, 128-byte
+// swizzle); the chunk's keys are gathered and dequantised by all warps, 32 keys at a
+// time, into one of two B buffers (N = 32 rows x K = 512, same layout).  One thread
+// issues the 32 tcgen05.mma (kind::f16, K = 16 each) of a buffer into its own 32 columns
+// of a tensor-memory accumulator and commits them to the buffer's mbarrier, so the
+// warps dequantise the next keys while the tensor cores multiply.  At the end each warp
+// reads its 32 accumulator lanes (tcgen05.ld) and writes the logits.  Every wait on an
+// mbarrier is bounded (20 ms of %globaltimer): past it the kernel sets GKR_ERR_TIMEOUT,
+// skips its logits, still frees its tensor memory and returns.
+#include "decode.cuh"
+#include "device.cuh"
+#include "launch.h"
+
+namespace gkr {
+
+namespace {
+
+constexpr int kM = 128;                  // heads per tile (MMA rows)
+constexpr int kN = 32;                   // keys per B buffer (MMA columns)
+constexpr int kChunk = 256;              // keys per CTA
+constexpr int kTiles = kChunk / kN;
+constexpr int kWarps = 8;
+constexpr int kLogitThreads = kWarps * 32;
+constexpr int kRowBytes = 128;           // one swizzle row: 64 bf16 of K
+constexpr int kABytes = kM * 1024;       // 128 KB
+constexpr int kBBytes = kN * 1024;       // 32 KB per buffer
+constexpr uint32_t kTmemCols = kChunk;   // fp32 accumulator columns
+constexpr int32_t kErrIndex = 4;
+constexpr int32_t kErrTimeout = 16;
+constexpr uint64_t kWaitNs = 20000000;    // a wait gives up after 20 ms (a normal one takes us)
+
+static_assert(kChunk % kN == 0 && (kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols >= 32,
+              "tensor memory is allocated in powers of two >= 32 columns");
+
+// ------------------------------------------------------------- tcgen05 / mbarrier PTX
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0u;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for the phase with the given parity to complete; false once kWaitNs have passed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitNs) return false;
+    return true;
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Make this thread's shared-memory stores visible to the tensor cores (async proxy).
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulator; one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the mbarrier once every tcgen05 operation this thread issued has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+// 32 consecutive fp32 accumulator columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A and B
+// (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at
+// bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (static_cast<uint32_t>(kN >> 3) << 17) |
+                            (static_cast<uint32_t>(kM >> 4) << 24);
+
+// Shared-memory matrix descriptor of a K-major operand with the 128-byte swizzle: start
+// address >> 4 (bits 0-13), leading offset (unused by this layout; 1) at bits 16-29,
+// stride between 8-row groups (1024 bytes) >> 4 at bits 32-45, descriptor version 1 at
+// bits 46-47, swizzle mode 128B (2) at bits 61-63.  The operand's rows are 128 bytes (64
+// bf16 of K); row r of an 8-row group sits at r * 128 in its 1024-byte group, and its
+// 16-byte piece c at position c ^ r.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// Byte offset of the 16-byte piece holding dims [8c, 8c+8) of K block kb (dims 64kb..) of
+// row r in an operand of `rows` rows: K blocks of rows x 128 bytes, 8-row swizzle groups.
+__device__ __forceinline__ uint32_t sw128_offset(int rows, int r, int kb, int c) {
+    return static_cast<uint32_t>(kb * rows * kRowBytes + (r >> 3) * 1024 + (r & 7) * kRowBytes +
+                                 ((c ^ (r & 7)) << 4));
+}
+
+// Lane L's two pieces of a 512-dim row (dims [8L, 8L+8) and [256+8L, 256+8L+8)) into
+// row r of a swizzled operand of `rows` rows.
+__device__ __forceinline__ void store_row_pieces(uint8_t* op, int rows, int r, int lane, uint4 a,
+                                                 uint4 b) {
+    *reinterpret_cast<uint4*>(op + sw128_offset(rows, r, lane >> 3, lane & 7)) = a;
+    *reinterpret_cast<uint4*>(op + sw128_offset(rows, r, 4 + (lane >> 3), lane & 7)) = b;
+}
+
+struct alignas(8) Barriers {
+    uint64_t mma_done[2];   // one per B buffer: its tile's products have completed
+    uint32_t tmem_base;
+    int32_t timed_out;
+};
+
+template <int kRecord>
+__global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const LogitsParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzle groups
+    uint8_t* const base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* const sA = base;
+    uint8_t* const sB = base + kABytes;                          // two buffers
+    Barriers* const bars = reinterpret_cast<Barriers*>(sB + 2 * kBBytes);
+    uint8_t* const key_ok = reinterpret_cast<uint8_t*>(bars + 1);   // kChunk flags
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t qi = blockIdx.x / p.chunks;
+    const int64_t k0 = static_cast<int64_t>(blockIdx.x % p.chunks) * kChunk;
+
+    if (warp == 0) {
+        tmem_alloc(smem_addr(&bars->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 32) {
+        mbar_init(smem_addr(&bars->mma_done[0]), 1);
+        mbar_init(smem_addr(&bars->mma_done[1]), 1);
+        bars->timed_out = 0;
+        mbar_init_fence();
+    }
+    pdl_wait_previous();   // q, the cache and the indices may come from the kernel ahead
+    pdl_release_next();
+
+    // A: the query's heads (rows >= num_heads are zero)
+    const uint8_t* const qrow = static_cast<const uint8_t*>(p.q) + qi * p.num_heads * 1024;
+    for (int h = warp; h < kM; h += kWarps) {
+        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+        if (h < p.num_heads) {
+            a = ld_ro16(qrow + h * 1024 + 16 * lane);
+            b = ld_ro16(qrow + h * 1024 + 512 + 16 * lane);
+        }
+        store_row_pieces(sA, kM, h, lane, a, b);
+    }
+
+    float scale = 1.0f;
+    bool scale_bad = false;
+    if constexpr (kRecord == 512) {
+        scale = __ldg(p.fp8_scale);
+        scale_bad = !scale_ok(scale);
+        if (scale_bad && threadIdx.x == 0) report(p.err, kErrScale);
+    }
+    LaneBases lb;
+    lb.a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
+    lb.tail = p.cache + 448 + 16 * (lane >= 24 ? lane - 24 : 0);
+    lb.s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
+    const int32_t* const idx_row = p.indices + qi * p.topk;
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t bar0 = smem_addr(&bars->mma_done[0]);
+    const uint32_t bar1 = smem_addr(&bars->mma_done[1]);
+    bool ok = true;
+    uint32_t bad_index = 0;
+
+    for (int t = 0; t < kTiles; ++t) {
+        const int buf = t & 1;
+        uint8_t* const B = sB + buf * kBBytes;
+        if (t >= 2 && ok) ok = mbar_wait(buf ? bar1 : bar0, ((t >> 1) - 1) & 1);   // tile t-2 done
+        // gather and dequantise keys t*kN .. t*kN+kN-1 of the chunk: 4 per warp
+#pragma unroll
+        for (int i = 0; i < kN / kWarps; ++i) {
+            const int n = warp * (kN / kWarps) + i;
+            const int64_t k = k0 + t * kN + n;
+            int64_t off = -1, soff = 0;
+            if (k < p.topk && !scale_bad) {
+                using R = Fmt<kRecord>;
+                const int32_t idx = __ldg(idx_row + k);
+                if (idx >= 0 && idx < p.num_slots) {
+                    const uint32_t s = static_cast<uint32_t>(idx);
+                    const uint32_t bs = static_cast<uint32_t>(p.block_size);
+                    const uint32_t page = s / bs, row = s - page * bs;
+                    const int64_t pbase = static_cast<int64_t>(page) * p.page_stride;
+                    off = pbase + row * R::D;
+                    soff = pbase + bs * R::D + row * R::S;
+                } else if (idx != -1) {
+                    bad_index = 1u;
+                }
+            }
+            Loaded r;
+            load_record<kRecord>(off, soff, lb, lane, r);
+            uint4 oa, ob;
+            convert<kRecord>(r, lane, scale, oa, ob);
+            store_row_pieces(B, kN, n, lane, oa, ob);
+            if (lane == 0) key_ok[t * kN + n] = off >= 0 ? 1 : 0;
+        }
+        fence_async_smem();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            tc_fence_after_sync();
+            const uint32_t a0 = smem_addr(sA), b0 = smem_addr(B);
+#pragma unroll
+            for (int s = 0; s < 512 / 16; ++s) {   // K = 16 per instruction
+                const uint32_t koff = (s & 3) * 32;
+                mma_bf16(tmem + t * kN, sw128_desc(a0 + (s >> 2) * kM * kRowBytes + koff),
+                         sw128_desc(b0 + (s >> 2) * kN * kRowBytes + koff), kIdesc, s > 0 ? 1u : 0u);
+            }
+            mma_commit(buf ? bar1 : bar0);
+        }
+    }
+    // the last tile's commit completes after every earlier product
+    if (ok) ok = mbar_wait(((kTiles - 1) & 1) ? bar1 : bar0, ((kTiles - 1) >> 1) & 1);
+    if (__any_sync(kFull, bad_index != 0u) && lane == 0) report(p.err, kErrIndex);
+    if (!ok) bars->timed_out = 1;
+    tc_fence_after_sync();
+    __syncthreads();
+
+    if (bars->timed_out == 0) {
+        // warp w reads accumulator lanes 32 (w % 4) .. +31 (heads), columns of half w / 4
+        const int h = 32 * (warp & 3) + lane;
+        const int col0 = (warp >> 2) * (kChunk / 2);
+        float* const orow = p.out + (qi * p.num_heads + h) * p.topk + k0;
+#pragma unroll 1
+        for (int c = 0; c < kChunk / 2; c += 32) {
+            float v[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + col0 + c, v);
+            if (h < p.num_heads) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const int64_t k = k0 + col0 + c + j;
+                    if (k >= p.topk) break;   // topk is a multiple of 4
+                    float4 o;
+                    const int kl = col0 + c + j;
+                    o.x = key_ok[kl] ? __fmul_rn(v[j], p.sm_scale) : -INFINITY;
+                    o.y = key_ok[kl + 1] ? __fmul_rn(v[j + 1], p.sm_scale) : -INFINITY;
+                    o.z = key_ok[kl + 2] ? __fmul_rn(v[j + 2], p.sm_scale) : -INFINITY;
+                    o.w = key_ok[kl + 3] ? __fmul_rn(v[j + 3], p.sm_scale) : -INFINITY;
+                    __stcs(reinterpret_cast<float4*>(orow + col0 + c + j), o);
+                }
+            }
+        }
+    } else if (threadIdx.x == 0) {
+        report(p.err, kErrTimeout);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int kRecord>
+cudaError_t launch(const LogitsParams& p, cudaStream_t stream) {
+    const size_t smem = kABytes + 2 * kBBytes + 1024 + sizeof(Barriers) + kChunk;
+    int64_t warps = 0;   // raises the kernel's dynamic shared-memory limit (once per device)
+    cudaError_t e = resident_warps(reinterpret_cast<const void*>(sparse_logits_kernel<kRecord>),
+                                   kLogitThreads, smem, &warps);
+    if (e != cudaSuccess) return e;
+    const int64_t blocks = p.num_queries * p.chunks;
+    return launch_kernel(sparse_logits_kernel<kRecord>, blocks, kLogitThreads, smem, stream, p.pdl,
+                         p);
+}
+
+}  // namespace
+
+int32_t logits_chunk_keys() { return kChunk; }
+int32_t logits_max_heads() { return kM; }
+
+cudaError_t launch_sparse_logits(int32_t record, const LogitsParams& p, cudaStream_t stream) {
+    switch (record) {
+        case 528: return launch<528>(p, stream);
+        case 584: return launch<584>(p, stream);
+        case 512: return launch<512>(p, stream);
+        default: return launch<1024>(p, stream);
+    }
+}
+
+}  // namespace gkr

@@ -10,7 +10,9 @@
  *                  compress_ratio positions, optional NaN sanitising);
  *   gkr_qnorm_rope_kv_insert: the fused attention write: query heads normed and
  *                  rotated (bf16 out, padded heads zeroed) beside the KV insert, in one
- *                  launch.
+ *                  launch;
+ *   gkr_sparse_logits: the dequant-gather fused into its consumer: sparse decode
+ *                  logits q . k over each query's top-k records, dequantised on chip.
  *
  * Operations follow these passages (page title, section):
  *   "PR #56893 [DSv4.1] Store the whole KV in MXFP8 (FlashMLA V4.1 record)",
@@ -75,6 +77,8 @@ typedef enum gkr_status {
 #define GKR_ERR_INDEX 4  /* gather: index < -1 or >= num_pages * block_size (row zeroed) */
 #define GKR_ERR_SCALE 8  /* fp8 cache: *fp8_scale not a positive finite number (nothing
                             written by the insert; every gathered row zeroed)           */
+#define GKR_ERR_TIMEOUT 16 /* sparse logits: a bounded wait for the tensor cores gave up
+                              (the launch's logits are not written); not expected      */
 
 /*
  * Paged cache geometry.  The cache is num_pages pages, page p starting at byte
@@ -284,6 +288,38 @@ GKR_API gkr_status gkr_kv_gather(const void *k_cache, const gkr_cache_desc *cach
                                  const gkr_launch_opts *opts, cudaStream_t stream);
 
 /*
+ * sparse_logits: the dequant-gather fused into its consumer (FlashMLA overview page, DSA
+ * section: a decode query attends to the top-k cache entries its index row lists, -1
+ * marking an invalid entry, and FP8 entries are dequantised to bf16 for the matrix
+ * product).  For query i, head h < num_heads and entry k < topk:
+ *   out[i, h, k] = fl32(sm_scale * sum_d q[i, h, d] * K[d])
+ * where K = the bf16 row gkr_kv_gather returns for indices[i, k] (any of the four
+ * records); indices[i, k] == -1 gives -inf, an index < -1 or past the cache gives -inf
+ * and sets GKR_ERR_INDEX; an fp8 cache whose scale is not a positive finite number gives
+ * -inf everywhere and GKR_ERR_SCALE.  The gathered rows stay on chip (shared memory) and
+ * the products run on the tensor cores (bf16 x bf16, fp32 accumulation over the 512
+ * dims in the hardware's order), so each value is within 2^-13 * |sm_scale| *
+ * sum_d |q[i, h, d] * K[d]| of the exact sum times sm_scale (a bound on fp32
+ * accumulation of 512 exact products, whatever its order).
+ *
+ * q            device, bf16 [num_queries, num_heads, 512] row-major, 16-byte aligned.
+ * num_heads    1 .. 128.
+ * k_cache      device, the cache described by *cache, 16-byte aligned; read only.
+ * indices      device, int32 [num_queries, topk] row-major.
+ * num_queries  >= 0; topk >= 0 and a multiple of 4 (0 of either enqueues nothing).
+ * sm_scale     finite; the logits' scale (e.g. the softmax scale).
+ * fp8_scale    as for gkr_kv_gather.
+ * out          device, fp32 [num_queries, num_heads, topk] row-major, 16-byte aligned.
+ * err_flag     device int32 or NULL; GKR_ERR_INDEX / GKR_ERR_SCALE / GKR_ERR_TIMEOUT.
+ * opts, stream as for the other entry points.
+ */
+GKR_API gkr_status gkr_sparse_logits(const void *q, int32_t num_heads, const void *k_cache,
+                                     const gkr_cache_desc *cache, const int32_t *indices,
+                                     int64_t num_queries, int64_t topk, float sm_scale,
+                                     const float *fp8_scale, float *out, int32_t *err_flag,
+                                     const gkr_launch_opts *opts, cudaStream_t stream);
+
+/*
  * Process-wide defaults of the launch options (gkr_launch_opts fields left at -1 take
  * them).  Setting them while another thread launches is safe (atomics) but changes that
  * thread's later calls too; per-call options do not.
@@ -341,7 +377,8 @@ GKR_API int32_t gkr_last_cuda_error(void);
  * gkr_kv_gather take fp8_scale (the plain fp8 / bf16 caches); gkr_rope_quant_insert and
  * gkr_set_insert_staged_min / gkr_get_insert_staged_min were added.  2.1.0:
  * gkr_set_early_metadata / gkr_get_early_metadata.  3.0.0: every launching entry point
- * takes a gkr_launch_opts pointer before the stream; gkr_qnorm_rope_kv_insert. */
+ * takes a gkr_launch_opts pointer before the stream; gkr_qnorm_rope_kv_insert.
+ * 3.1.0: gkr_sparse_logits. */
 GKR_API int32_t gkr_version(void);
 
 #ifdef __cplusplus

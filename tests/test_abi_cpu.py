@@ -27,7 +27,7 @@ def test_header_declares_the_boundary():
             "gkr_get_pdl", "gkr_set_insert_stream_min", "gkr_get_insert_stream_min",
             "gkr_set_insert_staged_min", "gkr_get_insert_staged_min",
             "gkr_rope_quant_insert", "gkr_set_early_metadata", "gkr_get_early_metadata",
-            "gkr_qnorm_rope_kv_insert"} <= syms
+            "gkr_qnorm_rope_kv_insert", "gkr_sparse_logits"} <= syms
 
 
 def test_library_exports_every_declared_symbol(gkr):
@@ -59,7 +59,7 @@ def test_page_stride_and_rows(gkr):
     assert gkr.page_stride(1024, 0) == -1
     with pytest.raises(ValueError):
         gkr.record_rows(500)
-    assert gkr.lib().gkr_version() == 30000
+    assert gkr.lib().gkr_version() == 30100
     assert gkr.get_insert_stream_min() == 131072
     assert gkr.get_insert_staged_min() == 24576
     assert gkr.insert_kernel_for(16384) == "insert_short_kernel"
@@ -128,7 +128,13 @@ def qinsert(gkr, d, T=8, q=A16b + 0x1000, H=2, Hp=4, qout=A16b + 0x2000, eps=1e-
                                               csc, max_pos, scale, err, _o(opts), None)
 
 
-@pytest.mark.parametrize("op", [insert, rq_insert, gather, qinsert])
+def logits(gkr, d, Q=2, H=8, topk=64, q=A16b + 0x1000, cache=A16b, idx=A16, out=A16,
+           scale=1.0, fp8=None, err=None, opts=None):
+    return gkr.lib().gkr_sparse_logits(q, H, cache, None if d is None else ctypes.byref(d), idx,
+                                       Q, topk, scale, fp8, out, err, _o(opts), None)
+
+
+@pytest.mark.parametrize("op", [insert, rq_insert, gather, qinsert, logits])
 def test_geometry_checks(gkr, op):
     assert op(gkr, None) == 1                                        # null descriptor
     assert op(gkr, desc(gkr, record=500)) == 2                       # unsupported record
@@ -229,7 +235,25 @@ def test_qnorm_rope_kv_insert_argument_checks(gkr):
     assert qinsert(gkr, desc(gkr, record=500)) == 2
 
 
-@pytest.mark.parametrize("op", [insert, rq_insert, gather, qinsert])
+def test_sparse_logits_argument_checks(gkr):
+    d = desc(gkr)
+    assert logits(gkr, d, H=0) == 1
+    assert logits(gkr, d, H=129) == 1                                 # heads beyond one tile
+    assert logits(gkr, d, topk=6) == 1                                # not a multiple of 4
+    assert logits(gkr, d, Q=-1) == 1
+    assert logits(gkr, d, scale=float("inf")) == 1
+    assert logits(gkr, d, scale=float("nan")) == 1
+    assert logits(gkr, d, Q=0, q=None, cache=None, idx=None, out=None) == 0
+    assert logits(gkr, d, topk=0, q=None, cache=None, idx=None, out=None) == 0
+    assert logits(gkr, d, q=None) == 1
+    assert logits(gkr, d, out=None) == 1
+    assert logits(gkr, d, q=A16 + 8) == 4
+    assert logits(gkr, d, out=A16 + 4) == 4
+    assert logits(gkr, d, idx=A16 + 2) == 4
+    assert logits(gkr, desc(gkr, record=512)) == 1                    # fp8 without a scale
+
+
+@pytest.mark.parametrize("op", [insert, rq_insert, gather, qinsert, logits])
 def test_launch_options_are_checked(gkr, op):
     """Per-call launch options: -1 takes the process default; other negative values and
     flags other than 0 / 1 are rejected before anything is enqueued."""
@@ -243,7 +267,8 @@ def test_launch_options_are_checked(gkr, op):
         assert op(gkr, desc(gkr), opts=o) == 1
     # valid options reach the next check (a misaligned pointer here), not a launch
     misaligned = {insert: dict(kv=A16 + 8), rq_insert: dict(kv=A16 + 8),
-                  gather: dict(out=A16 + 8), qinsert: dict(kv=A16 + 8)}[op]
+                  gather: dict(out=A16 + 8), qinsert: dict(kv=A16 + 8),
+                  logits: dict(out=A16 + 8)}[op]
     for o in (O(), O(pdl=False, early_metadata=True, insert_staged_min=0, insert_stream_min=7)):
         assert op(gkr, desc(gkr), opts=o, **misaligned) == 4
 

@@ -193,6 +193,13 @@ def roundtrip_v41_65536(seed: int = 1) -> InsertCase:
     return c
 
 
+def decode_queries(queries: int, heads: int, seed: int = 5) -> np.ndarray:
+    """Decode queries for the sparse logits: bf16 bit patterns [queries, heads, 512] drawn
+    from N(0,1) (the queries' values; the keys come from a cache workload)."""
+    rng = np.random.default_rng(seed)
+    return to_bf16_bits(rng.standard_normal((queries, heads, 512), dtype=np.float32))
+
+
 def gather_v41_sparse_262144(seed: int = 0) -> InsertCase:
     """Profiling-size sparse gather: a 262144-token cache (138 MB) and 32 queries x 2048."""
     c = gather_v41_sparse(seed, cache_tokens=1 << 18, queries=32, topk=2048, min_ctx=8192)
