@@ -1193,6 +1193,8 @@ def run_profile(args):
     if args.insert_stream_min is not None:
         gkr.set_insert_stream_min(args.insert_stream_min)
     name = args.profile
+    if name in ("sparse_logits", "sparse_logits_262144"):
+        return _profile_sparse_logits(args, torch, gkr, W, dev, name)
     fp8 = name.startswith("fp8_")                     # the same case into an fp8 cache
     case = W.PROFILE_WORKLOADS[name[4:] if fp8 else name]()
     record = 512 if fp8 else case.record
@@ -1227,6 +1229,37 @@ def run_profile(args):
         torch.cuda.synchronize()
         res[name + "_us"] = [round(a.elapsed_time(b) * 1e3, 2) for a, b in ts]
     print(json.dumps(res), flush=True)
+    return 0
+
+
+def _profile_sparse_logits(args, torch, gkr, W, dev, name):
+    """The sparse logits (128 heads) over the sparse-decode cache: the full workload
+    (1M-token cache, 128 queries x 2048) or its 262144-token profiling size (32 queries)."""
+    case = W.gather_v41_sparse() if name == "sparse_logits" else W.gather_v41_sparse_262144()
+    kv = torch.from_numpy(case.kv.view(np.int16)).view(torch.bfloat16).to(dev)
+    cache = gkr.alloc_cache(case.num_pages, 64, 528, dev, fill=0)
+    gkr.kv_insert(kv, cache, torch.from_numpy(case.slots).to(dev),
+                  torch.from_numpy(case.positions).to(dev), torch.from_numpy(case.csc).to(dev),
+                  64, 528)
+    del kv
+    Q = case.indices.shape[0]
+    q = torch.from_numpy(W.decode_queries(Q, 128).view(np.int16)).view(torch.bfloat16).to(dev)
+    idx = torch.from_numpy(case.indices).to(dev)
+    out = torch.empty(Q, 128, case.indices.shape[1], dtype=torch.float32, device=dev)
+    fn = lambda: gkr.sparse_logits(q, cache, idx, 512 ** -0.5, out=out)
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.launches):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    print(json.dumps({"workload": name, "sparse_logits_us": [round(a.elapsed_time(b) * 1e3, 2)
+                                                             for a, b in ts]}), flush=True)
     return 0
 
 

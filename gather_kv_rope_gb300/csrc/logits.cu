@@ -30,21 +30,29 @@ namespace gkr {
 namespace {
 
 constexpr int kM = 128;                  // heads per tile (MMA rows)
-constexpr int kN = 32;                   // keys per B buffer (MMA columns)
-constexpr int kChunk = 256;              // keys per CTA
-constexpr int kTiles = kChunk / kN;
-constexpr int kWarps = 8;
-constexpr int kLogitThreads = kWarps * 32;
+constexpr int kN = 32;                   // keys per B stage (MMA columns)
+constexpr int kChunk = 256;              // keys per work item
+constexpr int kTiles = kChunk / kN;      // B stages per item
+constexpr int kStages = 3;               // B ring depth
+constexpr int kEpilogueWarps = 4;        // warps 0..3: accumulator lanes 0..127
+constexpr int kProducerWarps = 8;        // warps 4..11: gather + dequantise
+constexpr int kFirstProducer = kEpilogueWarps;
+constexpr int kMmaWarp = kEpilogueWarps + kProducerWarps;   // warp 12: tcgen05.mma issue
+constexpr int kKeysPerWarp = kN / kProducerWarps;           // keys of a stage per producer
+constexpr int kLogitThreads = (kMmaWarp + 1) * 32;
 constexpr int kRowBytes = 128;           // one swizzle row: 64 bf16 of K
 constexpr int kABytes = kM * 1024;       // 128 KB
-constexpr int kBBytes = kN * 1024;       // 32 KB per buffer
-constexpr uint32_t kTmemCols = kChunk;   // fp32 accumulator columns
+constexpr int kBBytes = kN * 1024;       // 32 KB per stage
+constexpr uint32_t kTmemCols = 2 * kChunk;   // two fp32 accumulators (512 columns)
 constexpr int32_t kErrIndex = 4;
 constexpr int32_t kErrTimeout = 16;
 constexpr uint64_t kWaitNs = 20000000;    // a wait gives up after 20 ms (a normal one takes us)
 
-static_assert(kChunk % kN == 0 && (kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols >= 32,
-              "tensor memory is allocated in powers of two >= 32 columns");
+static_assert(kChunk % kN == 0 && (kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols >= 32 &&
+                  kTmemCols <= 512,
+              "tensor memory is allocated in powers of two of 32 .. 512 columns");
+static_assert(kKeysPerWarp == 4 && kTiles * 4 <= 32,
+              "a producer lane holds the index of one (tile, key) pair of an item");
 
 // ------------------------------------------------------------- tcgen05 / mbarrier PTX
 
@@ -168,11 +176,51 @@ __device__ __forceinline__ void store_row_pieces(uint8_t* op, int rows, int r, i
     *reinterpret_cast<uint4*>(op + sw128_offset(rows, r, 4 + (lane >> 3), lane & 7)) = b;
 }
 
+// One work item = (query, chunk of kChunk keys).  A CTA (one per SM) takes a contiguous
+// run of items in query-major order, so it reloads the query tile A only when its run
+// moves to the next query.
 struct alignas(8) Barriers {
-    uint64_t mma_done[2];   // one per B buffer: its tile's products have completed
+    uint64_t full[kStages];      // producers -> MMA: B stage holds its 32 keys
+    uint64_t empty[kStages];     // MMA -> producers: the stage's products are done
+    uint64_t acc_full[2];        // MMA -> epilogue: an item's accumulator is complete
+    uint64_t acc_empty[2];       // epilogue -> MMA: the accumulator has been read
     uint32_t tmem_base;
     int32_t timed_out;
 };
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    uint64_t state;
+    asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1];" : "=l"(state) : "r"(bar) : "memory");
+    (void)state;
+}
+
+// A wait that records a timeout instead of hanging: after the first failure the thread
+// stops waiting (its results are discarded, see GKR_ERR_TIMEOUT).
+__device__ __forceinline__ void wait_or_flag(uint32_t bar, uint32_t parity, bool& ok) {
+    if (ok) ok = mbar_wait(bar, parity);
+}
+
+// Decode key k of query row idx_row into the record's byte offsets (off = -1: not a
+// record: past topk, index -1, out of range (bad = 1), or a bad fp8 scale).
+template <int kRecord>
+__device__ __forceinline__ void key_offsets(const LogitsParams& p, int32_t idx, bool in_range,
+                                            bool scale_bad, int64_t& off, int64_t& soff,
+                                            uint32_t& bad) {
+    using R = Fmt<kRecord>;
+    off = -1;
+    soff = 0;
+    if (!in_range || scale_bad) return;
+    if (idx >= 0 && idx < p.num_slots) {
+        const uint32_t s = static_cast<uint32_t>(idx);
+        const uint32_t bs = static_cast<uint32_t>(p.block_size);
+        const uint32_t page = s / bs, row = s - page * bs;
+        const int64_t pbase = static_cast<int64_t>(page) * p.page_stride;
+        off = pbase + row * R::D;
+        soff = pbase + bs * R::D + row * R::S;
+    } else if (idx != -1) {
+        bad = 1u;
+    }
+}
 
 template <int kRecord>
 __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const LogitsParams p) {
@@ -181,153 +229,229 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
     uint8_t* const base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* const sA = base;
-    uint8_t* const sB = base + kABytes;                          // two buffers
-    Barriers* const bars = reinterpret_cast<Barriers*>(sB + 2 * kBBytes);
-    uint8_t* const key_ok = reinterpret_cast<uint8_t*>(bars + 1);   // kChunk flags
+    uint8_t* const sB = base + kABytes;                               // kStages buffers
+    Barriers* const bars = reinterpret_cast<Barriers*>(sB + kStages * kBBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t qi = blockIdx.x / p.chunks;
-    const int64_t k0 = static_cast<int64_t>(blockIdx.x % p.chunks) * kChunk;
+    const int64_t items = p.num_queries * p.chunks;
+    const int64_t i0 = items * blockIdx.x / gridDim.x;
+    const int64_t i1 = items * (blockIdx.x + 1) / gridDim.x;
 
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(&bars->tmem_base), kTmemCols);
         tmem_relinquish();
     }
-    if (threadIdx.x == 32) {
-        mbar_init(smem_addr(&bars->mma_done[0]), 1);
-        mbar_init(smem_addr(&bars->mma_done[1]), 1);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_addr(&bars->full[s]), kProducerWarps * 32);
+            mbar_init(smem_addr(&bars->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_addr(&bars->acc_full[a]), 1);
+            mbar_init(smem_addr(&bars->acc_empty[a]), kEpilogueWarps * 32);
+        }
         bars->timed_out = 0;
         mbar_init_fence();
     }
     pdl_wait_previous();   // q, the cache and the indices may come from the kernel ahead
     pdl_release_next();
-
-    // A: the query's heads (rows >= num_heads are zero)
-    const uint8_t* const qrow = static_cast<const uint8_t*>(p.q) + qi * p.num_heads * 1024;
-    for (int h = warp; h < kM; h += kWarps) {
-        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-        if (h < p.num_heads) {
-            a = ld_ro16(qrow + h * 1024 + 16 * lane);
-            b = ld_ro16(qrow + h * 1024 + 512 + 16 * lane);
-        }
-        store_row_pieces(sA, kM, h, lane, a, b);
-    }
-
-    float scale = 1.0f;
-    bool scale_bad = false;
-    if constexpr (kRecord == 512) {
-        scale = __ldg(p.fp8_scale);
-        scale_bad = !scale_ok(scale);
-        if (scale_bad && threadIdx.x == 0) report(p.err, kErrScale);
-    }
-    LaneBases lb;
-    lb.a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
-    lb.tail = p.cache + 448 + 16 * (lane >= 24 ? lane - 24 : 0);
-    lb.s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
-    const int32_t* const idx_row = p.indices + qi * p.topk;
-
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
-    const uint32_t bar0 = smem_addr(&bars->mma_done[0]);
-    const uint32_t bar1 = smem_addr(&bars->mma_done[1]);
     bool ok = true;
-    uint32_t bad_index = 0;
 
-    for (int t = 0; t < kTiles; ++t) {
-        const int buf = t & 1;
-        uint8_t* const B = sB + buf * kBBytes;
-        if (t >= 2 && ok) ok = mbar_wait(buf ? bar1 : bar0, ((t >> 1) - 1) & 1);   // tile t-2 done
-        // gather and dequantise keys t*kN .. t*kN+kN-1 of the chunk: 4 per warp
+    if (warp >= kFirstProducer && warp < kFirstProducer + kProducerWarps) {
+        // ------------------------------------------------------------- producers
+        const int pw = warp - kFirstProducer;
+        float scale = 1.0f;
+        bool scale_bad = false;
+        if constexpr (kRecord == 512) {
+            scale = __ldg(p.fp8_scale);
+            scale_bad = !scale_ok(scale);
+            if (scale_bad && pw == 0 && lane == 0 && i0 < i1) report(p.err, kErrScale);
+        }
+        LaneBases lb;
+        lb.a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
+        lb.tail = p.cache + 448 + 16 * (lane >= 24 ? lane - 24 : 0);
+        lb.s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
+        uint32_t bad = 0;
+        // lane L holds the index of this warp's key (L / 4, L % 4) = tile L / 4, key
+        // kKeysPerWarp * pw + L % 4 of an item; idx_cur for the current item, idx_nxt for
+        // the next one
+        auto load_indices = [&](int64_t item, int32_t& idx, bool& in_range) {
+            idx = -1;
+            in_range = false;
+            if (item >= i1) return;
+            const int64_t qi = item / p.chunks;
+            const int64_t k = (item % p.chunks) * kChunk + (lane >> 2) * kN +
+                              kKeysPerWarp * pw + (lane & 3);
+            in_range = k < p.topk;
+            if (in_range) idx = __ldg(p.indices + qi * p.topk + k);
+        };
+        int32_t idx_cur, idx_nxt;
+        bool rng_cur, rng_nxt;
+        load_indices(i0, idx_cur, rng_cur);
+        load_indices(i0 + 1, idx_nxt, rng_nxt);
+
+        Loaded cur[kKeysPerWarp], nxt[kKeysPerWarp];
+        // records of tile t of the current item (indices in idx_cur)
+        auto load_tile = [&](int t, int32_t idx_all, bool rng_all, Loaded (&r)[kKeysPerWarp]) {
 #pragma unroll
-        for (int i = 0; i < kN / kWarps; ++i) {
-            const int n = warp * (kN / kWarps) + i;
-            const int64_t k = k0 + t * kN + n;
-            int64_t off = -1, soff = 0;
-            if (k < p.topk && !scale_bad) {
-                using R = Fmt<kRecord>;
-                const int32_t idx = __ldg(idx_row + k);
-                if (idx >= 0 && idx < p.num_slots) {
-                    const uint32_t s = static_cast<uint32_t>(idx);
-                    const uint32_t bs = static_cast<uint32_t>(p.block_size);
-                    const uint32_t page = s / bs, row = s - page * bs;
-                    const int64_t pbase = static_cast<int64_t>(page) * p.page_stride;
-                    off = pbase + row * R::D;
-                    soff = pbase + bs * R::D + row * R::S;
-                } else if (idx != -1) {
-                    bad_index = 1u;
+            for (int i = 0; i < kKeysPerWarp; ++i) {
+                const int32_t idx = __shfl_sync(kFull, idx_all, t * 4 + i);
+                const bool rg = __shfl_sync(kFull, rng_all ? 1 : 0, t * 4 + i) != 0;
+                int64_t off, soff;
+                key_offsets<kRecord>(p, idx, rg, scale_bad, off, soff, bad);
+                load_record<kRecord>(off, soff, lb, lane, r[i]);
+            }
+        };
+        int64_t cur_q = -1;
+        uint32_t j = 0;                     // tiles produced so far (ring position)
+        if (i0 < i1) load_tile(0, idx_cur, rng_cur, cur);
+        for (int64_t item = i0; item < i1; ++item) {
+            const int64_t u = item - i0;
+            const int64_t qi = item / p.chunks;
+            if (qi != cur_q) {
+                // the query tile changes: every product that read the old one must be done
+                if (u > 0) wait_or_flag(smem_addr(&bars->acc_full[(u - 1) & 1]), ((u - 1) >> 1) & 1, ok);
+                // every row's copies in flight at once (cp.async into the swizzled places),
+                // one wait; rows past num_heads are zero
+                const uint8_t* const qrow = static_cast<const uint8_t*>(p.q) + qi * p.num_heads * 1024;
+                for (int h = pw; h < kM; h += kProducerWarps) {
+                    if (h < p.num_heads) {
+                        cp_async16(sA + sw128_offset(kM, h, lane >> 3, lane & 7),
+                                   qrow + h * 1024 + 16 * lane);
+                        cp_async16(sA + sw128_offset(kM, h, 4 + (lane >> 3), lane & 7),
+                                   qrow + h * 1024 + 512 + 16 * lane);
+                    } else {
+                        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                        store_row_pieces(sA, kM, h, lane, z, z);
+                    }
                 }
+                cp_async_commit();
+                cp_async_wait<0>();
+                cur_q = qi;
             }
-            Loaded r;
-            load_record<kRecord>(off, soff, lb, lane, r);
-            uint4 oa, ob;
-            convert<kRecord>(r, lane, scale, oa, ob);
-            store_row_pieces(B, kN, n, lane, oa, ob);
-            if (lane == 0) key_ok[t * kN + n] = off >= 0 ? 1 : 0;
-        }
-        fence_async_smem();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            tc_fence_after_sync();
-            const uint32_t a0 = smem_addr(sA), b0 = smem_addr(B);
-#pragma unroll
-            for (int s = 0; s < 512 / 16; ++s) {   // K = 16 per instruction
-                const uint32_t koff = (s & 3) * 32;
-                mma_bf16(tmem + t * kN, sw128_desc(a0 + (s >> 2) * kM * kRowBytes + koff),
-                         sw128_desc(b0 + (s >> 2) * kN * kRowBytes + koff), kIdesc, s > 0 ? 1u : 0u);
-            }
-            mma_commit(buf ? bar1 : bar0);
-        }
-    }
-    // the last tile's commit completes after every earlier product
-    if (ok) ok = mbar_wait(((kTiles - 1) & 1) ? bar1 : bar0, ((kTiles - 1) >> 1) & 1);
-    if (__any_sync(kFull, bad_index != 0u) && lane == 0) report(p.err, kErrIndex);
-    if (!ok) bars->timed_out = 1;
-    tc_fence_after_sync();
-    __syncthreads();
-
-    if (bars->timed_out == 0) {
-        // warp w reads accumulator lanes 32 (w % 4) .. +31 (heads), columns of half w / 4
-        const int h = 32 * (warp & 3) + lane;
-        const int col0 = (warp >> 2) * (kChunk / 2);
-        float* const orow = p.out + (qi * p.num_heads + h) * p.topk + k0;
 #pragma unroll 1
-        for (int c = 0; c < kChunk / 2; c += 32) {
-            float v[32];
-            tmem_ld32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + col0 + c, v);
-            if (h < p.num_heads) {
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const int64_t k = k0 + col0 + c + j;
-                    if (k >= p.topk) break;   // topk is a multiple of 4
-                    float4 o;
-                    const int kl = col0 + c + j;
-                    o.x = key_ok[kl] ? __fmul_rn(v[j], p.sm_scale) : -INFINITY;
-                    o.y = key_ok[kl + 1] ? __fmul_rn(v[j + 1], p.sm_scale) : -INFINITY;
-                    o.z = key_ok[kl + 2] ? __fmul_rn(v[j + 2], p.sm_scale) : -INFINITY;
-                    o.w = key_ok[kl + 3] ? __fmul_rn(v[j + 3], p.sm_scale) : -INFINITY;
-                    __stcs(reinterpret_cast<float4*>(orow + col0 + c + j), o);
+            for (int t = 0; t < kTiles; ++t, ++j) {
+                // the next tile's records (or the next item's first) fly while this one is
+                // converted
+                if (t + 1 < kTiles) {
+                    load_tile(t + 1, idx_cur, rng_cur, nxt);
+                } else if (item + 1 < i1) {
+                    load_tile(0, idx_nxt, rng_nxt, nxt);
                 }
+                const int s = j % kStages;
+                if (j >= kStages) wait_or_flag(smem_addr(&bars->empty[s]), ((j / kStages) - 1) & 1, ok);
+                uint8_t* const B = sB + s * kBBytes;
+#pragma unroll
+                for (int i = 0; i < kKeysPerWarp; ++i) {
+                    uint4 oa, ob;
+                    convert<kRecord>(cur[i], lane, scale, oa, ob);
+                    store_row_pieces(B, kN, kKeysPerWarp * pw + i, lane, oa, ob);
+                }
+                fence_async_smem();
+                mbar_arrive(smem_addr(&bars->full[s]));
+#pragma unroll
+                for (int i = 0; i < kKeysPerWarp; ++i) cur[i] = nxt[i];
+            }
+            idx_cur = idx_nxt;
+            rng_cur = rng_nxt;
+            load_indices(item + 2, idx_nxt, rng_nxt);
+        }
+        if (__any_sync(kFull, bad != 0u) && lane == 0) report(p.err, kErrIndex);
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            uint32_t j = 0;
+            for (int64_t item = i0; item < i1; ++item) {
+                const int64_t u = item - i0;
+                const int a = static_cast<int>(u & 1);
+                if (u >= 2) wait_or_flag(smem_addr(&bars->acc_empty[a]), ((u >> 1) - 1) & 1, ok);
+                tc_fence_after_sync();
+                const uint32_t d0 = tmem + a * kChunk;
+                for (int t = 0; t < kTiles; ++t, ++j) {
+                    const int s = j % kStages;
+                    wait_or_flag(smem_addr(&bars->full[s]), (j / kStages) & 1, ok);
+                    tc_fence_after_sync();
+                    const uint32_t a0 = smem_addr(sA), b0 = smem_addr(sB + s * kBBytes);
+#pragma unroll
+                    for (int k = 0; k < 512 / 16; ++k) {   // K = 16 per instruction
+                        const uint32_t koff = (k & 3) * 32;
+                        mma_bf16(d0 + t * kN, sw128_desc(a0 + (k >> 2) * kM * kRowBytes + koff),
+                                 sw128_desc(b0 + (k >> 2) * kN * kRowBytes + koff), kIdesc,
+                                 k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_addr(&bars->empty[s]));
+                }
+                mma_commit(smem_addr(&bars->acc_full[a]));
             }
         }
-    } else if (threadIdx.x == 0) {
-        report(p.err, kErrTimeout);
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------- epilogue
+        // Which entries are records (the rest are -inf) comes from the indices themselves:
+        // lane l reads the index of column c + l of each 32-column block, and a ballot
+        // gives every lane the block's mask.
+        const int h = 32 * warp + lane;             // warps 0..3: accumulator lanes
+        bool scale_bad = false;
+        if constexpr (kRecord == 512) scale_bad = !scale_ok(__ldg(p.fp8_scale));
+        for (int64_t item = i0; item < i1; ++item) {
+            const int64_t u = item - i0;
+            const int a = static_cast<int>(u & 1);
+            const int64_t qi = item / p.chunks;
+            const int64_t k0 = (item % p.chunks) * kChunk;
+            int32_t idx[kChunk / 32];
+#pragma unroll
+            for (int c = 0; c < kChunk / 32; ++c) {
+                const int64_t k = k0 + 32 * c + lane;
+                idx[c] = k < p.topk ? __ldg(p.indices + qi * p.topk + k) : -1;
+            }
+            wait_or_flag(smem_addr(&bars->acc_full[a]), (u >> 1) & 1, ok);
+            tc_fence_after_sync();
+            float* const orow = p.out + (qi * p.num_heads + h) * p.topk + k0;
+#pragma unroll
+            for (int c = 0; c < kChunk / 32; ++c) {
+                const uint32_t mask =
+                    __ballot_sync(kFull, !scale_bad && idx[c] >= 0 && idx[c] < p.num_slots);
+                float v[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + a * kChunk + 32 * c, v);
+                if (h < p.num_heads && ok) {
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj += 4) {
+                        if (k0 + 32 * c + jj >= p.topk) break;   // topk is a multiple of 4
+                        float4 o;
+                        o.x = (mask >> jj) & 1u ? __fmul_rn(v[jj], p.sm_scale) : -INFINITY;
+                        o.y = (mask >> (jj + 1)) & 1u ? __fmul_rn(v[jj + 1], p.sm_scale) : -INFINITY;
+                        o.z = (mask >> (jj + 2)) & 1u ? __fmul_rn(v[jj + 2], p.sm_scale) : -INFINITY;
+                        o.w = (mask >> (jj + 3)) & 1u ? __fmul_rn(v[jj + 3], p.sm_scale) : -INFINITY;
+                        __stcs(reinterpret_cast<float4*>(orow + 32 * c + jj), o);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(smem_addr(&bars->acc_empty[a]));
+        }
     }
+    if (!ok) atomicOr(&bars->timed_out, 1);
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    if (threadIdx.x == 0 && bars->timed_out != 0) report(p.err, kErrTimeout);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int kRecord>
 cudaError_t launch(const LogitsParams& p, cudaStream_t stream) {
-    const size_t smem = kABytes + 2 * kBBytes + 1024 + sizeof(Barriers) + kChunk;
+    const size_t smem = kABytes + kStages * kBBytes + 1024 + sizeof(Barriers);
     int64_t warps = 0;   // raises the kernel's dynamic shared-memory limit (once per device)
     cudaError_t e = resident_warps(reinterpret_cast<const void*>(sparse_logits_kernel<kRecord>),
                                    kLogitThreads, smem, &warps);
     if (e != cudaSuccess) return e;
-    const int64_t blocks = p.num_queries * p.chunks;
+    const int64_t ctas = warps / (kLogitThreads / 32);        // one CTA per SM
+    const int64_t items = p.num_queries * p.chunks;
+    const int64_t blocks = items < ctas ? items : ctas;
     return launch_kernel(sparse_logits_kernel<kRecord>, blocks, kLogitThreads, smem, stream, p.pdl,
                          p);
 }
