@@ -1195,6 +1195,8 @@ def run_profile(args):
     name = args.profile
     if name in ("sparse_logits", "sparse_logits_262144"):
         return _profile_sparse_logits(args, torch, gkr, W, dev, name)
+    if name == "qnorm_prefill_8192x16p64":
+        return _profile_qside(args, torch, gkr, W, dev, name)
     fp8 = name.startswith("fp8_")                     # the same case into an fp8 cache
     case = W.PROFILE_WORKLOADS[name[4:] if fp8 else name]()
     record = 512 if fp8 else case.record
@@ -1232,6 +1234,37 @@ def run_profile(args):
     return 0
 
 
+def _time_launches(torch, fn, n):
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return [round(a.elapsed_time(b) * 1e3, 2) for a, b in ts]
+
+
+def _profile_qside(args, torch, gkr, W, dev, name):
+    """The fused attention write at the prefill shape of the sweep (8192 tokens, 16 heads
+    padded to 64, V4.1 cache)."""
+    T, H, Hp = 8192, 16, 64
+    case = W.random_insert(name, T, 528, 64, 2 * T // 64 + 2, 8192, 0.05, seed=3)
+    s = device_sets(case, dev, 1)[0]
+    q = torch.randn(T, H, 512, generator=torch.Generator().manual_seed(0)).to(torch.bfloat16).to(dev)
+    q_out = torch.empty(T, Hp, 512, dtype=torch.bfloat16, device=dev)
+    fn = lambda: gkr.qnorm_rope_kv_insert(q, s["kv"], s["cache"], s["slots"], s["pos"], s["csc"],
+                                          Hp, 1e-6, 64, True, q_out=q_out)
+    print(json.dumps({"workload": name, "qnorm_rope_kv_insert_us": _time_launches(torch, fn,
+                                                                                 args.launches)}),
+          flush=True)
+    return 0
+
+
 def _profile_sparse_logits(args, torch, gkr, W, dev, name):
     """The sparse logits (128 heads) over the sparse-decode cache: the full workload
     (1M-token cache, 128 queries x 2048) or its 262144-token profiling size (32 queries)."""
@@ -1247,19 +1280,9 @@ def _profile_sparse_logits(args, torch, gkr, W, dev, name):
     idx = torch.from_numpy(case.indices).to(dev)
     out = torch.empty(Q, 128, case.indices.shape[1], dtype=torch.float32, device=dev)
     fn = lambda: gkr.sparse_logits(q, cache, idx, 512 ** -0.5, out=out)
-    for _ in range(2):
-        fn()
-    torch.cuda.synchronize()
-    ts = []
-    for _ in range(args.launches):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        ts.append((a, b))
-    torch.cuda.synchronize()
-    print(json.dumps({"workload": name, "sparse_logits_us": [round(a.elapsed_time(b) * 1e3, 2)
-                                                             for a, b in ts]}), flush=True)
+    print(json.dumps({"workload": name, "sparse_logits_us": _time_launches(torch, fn,
+                                                                          args.launches)}),
+          flush=True)
     return 0
 
 

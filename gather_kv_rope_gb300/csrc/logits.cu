@@ -10,17 +10,24 @@
 // sets GKR_ERR_INDEX).  The gathered rows never leave the SM: the bf16 intermediate that
 // kv_gather writes (1 KB per index) and a separate product kernel reads back is gone.
 //
-// Launch shape (sm_103a, 5th-generation tensor cores): one CTA of 8 warps per (query,
-// chunk of kChunk keys).  The query's heads (up to 128, zero-padded) are staged once
-// into shared memory as the A operand (M = 128 rows x K = 512, bf16, K-major, 128-byte
-// swizzle); the chunk's keys are gathered and dequantised by all warps, 32 keys at a
-// time, into one of two B buffers (N = 32 rows x K = 512, same layout).  One thread
-// issues the 32 tcgen05.mma (kind::f16, K = 16 each) of a buffer into its own 32 columns
-// of a tensor-memory accumulator and commits them to the buffer's mbarrier, so the
-// warps dequantise the next keys while the tensor cores multiply.  At the end each warp
-// reads its 32 accumulator lanes (tcgen05.ld) and writes the logits.  Every wait on an
-// mbarrier is bounded (20 ms of %globaltimer): past it the kernel sets GKR_ERR_TIMEOUT,
-// skips its logits, still frees its tensor memory and returns.
+// Launch shape (sm_103a, 5th-generation tensor cores): a persistent kernel, one CTA of 12
+// warps per SM, each CTA taking a contiguous run of work items (query, chunk of 256 keys)
+// in query-major order.
+//   * A: the query's heads (up to 128, zero-padded) in shared memory as the MMA's A
+//     operand (M = 128 x K = 512, bf16, K-major, 128-byte swizzle), copied with cp.async
+//     when the run reaches a new query, after the last product that read the old one.
+//   * 8 producer warps gather and dequantise the keys of a 32-key stage (4 each) into one
+//     of 3 B tiles (N = 32 x K = 512, same layout); a ring of registers keeps the record
+//     loads of the next 3 stages in flight while one is converted.
+//   * lane 0 of the first producer warp, once all producers have filled a stage, issues its
+//     32 tcgen05.mma (kind::f16, K = 16 each) into that stage's 32 columns of one of two
+//     256-column TMEM accumulators and commits them to the stage's mbarrier (the stage
+//     may then be refilled); after an item's last stage it commits the accumulator.
+//   * 4 epilogue warps read their 32 accumulator lanes (tcgen05.ld), mask the entries that
+//     are not records (a ballot over the indices) and stream the fp32 logits, while the
+//     next item is multiplied into the other accumulator.
+// Every wait on an mbarrier is bounded (20 ms of %globaltimer): past it the CTA sets
+// GKR_ERR_TIMEOUT, stops waiting, still frees its tensor memory and returns.
 #include "decode.cuh"
 #include "device.cuh"
 #include "launch.h"
@@ -35,11 +42,21 @@ constexpr int kChunk = 256;              // keys per work item
 constexpr int kTiles = kChunk / kN;      // B stages per item
 constexpr int kStages = 3;               // B ring depth
 constexpr int kEpilogueWarps = 4;        // warps 0..3: accumulator lanes 0..127
-constexpr int kProducerWarps = 8;        // warps 4..11: gather + dequantise
+constexpr int kProducerWarps = 8;        // warps 4..11: gather + dequantise; lane 0 of warp 4
+                                         // also issues the tensor-core products
 constexpr int kFirstProducer = kEpilogueWarps;
-constexpr int kMmaWarp = kEpilogueWarps + kProducerWarps;   // warp 12: tcgen05.mma issue
+constexpr int kMmaWarp = kFirstProducer;                    // allocates and frees TMEM too
 constexpr int kKeysPerWarp = kN / kProducerWarps;           // keys of a stage per producer
-constexpr int kLogitThreads = (kMmaWarp + 1) * 32;
+// Producer register ring: the records of kAhead stages; while one stage is converted the
+// loads of the next kAhead - 1 are in flight.  Four for the 8-byte-per-lane records (V4.1,
+// fp8 rows), two where a lane holds 16-byte pieces (the V4 bf16 tail, bf16 rows) and four
+// would spill.
+template <int kRecord>
+struct Ahead {
+    static constexpr int value = kRecord == 528 || kRecord == 512 ? 4 : 2;
+};
+constexpr int kLogitThreads = (kEpilogueWarps + kProducerWarps) * 32;   // 12 warps: 3 per
+                                         // SM sub-partition, up to 168 registers a thread
 constexpr int kRowBytes = 128;           // one swizzle row: 64 bf16 of K
 constexpr int kABytes = kM * 1024;       // 128 KB
 constexpr int kBBytes = kN * 1024;       // 32 KB per stage
@@ -51,8 +68,10 @@ constexpr uint64_t kWaitNs = 20000000;    // a wait gives up after 20 ms (a norm
 static_assert(kChunk % kN == 0 && (kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols >= 32 &&
                   kTmemCols <= 512,
               "tensor memory is allocated in powers of two of 32 .. 512 columns");
-static_assert(kKeysPerWarp == 4 && kTiles * 4 <= 32,
+static_assert(kKeysPerWarp * kTiles <= 32,
               "a producer lane holds the index of one (tile, key) pair of an item");
+static_assert(kTiles % Ahead<528>::value == 0 && kTiles % Ahead<584>::value == 0,
+              "ring slots repeat identically in every item");
 
 // ------------------------------------------------------------- tcgen05 / mbarrier PTX
 
@@ -189,9 +208,9 @@ struct alignas(8) Barriers {
 };
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    uint64_t state;
-    asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1];" : "=l"(state) : "r"(bar) : "memory");
-    (void)state;
+    asm volatile(
+        "{\n .reg .b64 state;\n mbarrier.arrive.shared::cta.b64 state, [%0];\n}\n" ::"r"(bar)
+        : "memory");
 }
 
 // A wait that records a timeout instead of hanging: after the first failure the thread
@@ -277,16 +296,17 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
         lb.tail = p.cache + 448 + 16 * (lane >= 24 ? lane - 24 : 0);
         lb.s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
         uint32_t bad = 0;
-        // lane L holds the index of this warp's key (L / 4, L % 4) = tile L / 4, key
-        // kKeysPerWarp * pw + L % 4 of an item; idx_cur for the current item, idx_nxt for
-        // the next one
+        // lane L < kTiles * kKeysPerWarp holds the index of this warp's key
+        // (L / kKeysPerWarp, L % kKeysPerWarp) = tile L / kKeysPerWarp, key
+        // kKeysPerWarp * pw + L % kKeysPerWarp of an item; idx_cur for the current item,
+        // idx_nxt for the next one
         auto load_indices = [&](int64_t item, int32_t& idx, bool& in_range) {
             idx = -1;
             in_range = false;
-            if (item >= i1) return;
+            if (item >= i1 || lane >= kTiles * kKeysPerWarp) return;
             const int64_t qi = item / p.chunks;
-            const int64_t k = (item % p.chunks) * kChunk + (lane >> 2) * kN +
-                              kKeysPerWarp * pw + (lane & 3);
+            const int64_t k = (item % p.chunks) * kChunk + (lane / kKeysPerWarp) * kN +
+                              kKeysPerWarp * pw + (lane % kKeysPerWarp);
             in_range = k < p.topk;
             if (in_range) idx = __ldg(p.indices + qi * p.topk + k);
         };
@@ -295,21 +315,28 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
         load_indices(i0, idx_cur, rng_cur);
         load_indices(i0 + 1, idx_nxt, rng_nxt);
 
-        Loaded cur[kKeysPerWarp], nxt[kKeysPerWarp];
-        // records of tile t of the current item (indices in idx_cur)
+        // the records of tile t (indices in idx_all)
         auto load_tile = [&](int t, int32_t idx_all, bool rng_all, Loaded (&r)[kKeysPerWarp]) {
 #pragma unroll
             for (int i = 0; i < kKeysPerWarp; ++i) {
-                const int32_t idx = __shfl_sync(kFull, idx_all, t * 4 + i);
-                const bool rg = __shfl_sync(kFull, rng_all ? 1 : 0, t * 4 + i) != 0;
+                const int src = t * kKeysPerWarp + i;
+                const int32_t idx = __shfl_sync(kFull, idx_all, src);
+                const bool rg = __shfl_sync(kFull, rng_all ? 1 : 0, src) != 0;
                 int64_t off, soff;
                 key_offsets<kRecord>(p, idx, rg, scale_bad, off, soff, bad);
                 load_record<kRecord>(off, soff, lb, lane, r[i]);
             }
         };
+        // register ring: tile t of an item lives in slot t % kAhead; while tile t is
+        // converted, the loads of tiles t + 1 .. t + kAhead - 1 (of this item or the next)
+        // are in flight
+        constexpr int kAhead = Ahead<kRecord>::value;
+        Loaded ring[kAhead][kKeysPerWarp];
+#pragma unroll
+        for (int t = 0; t < kAhead - 1; ++t)
+            if (i0 < i1) load_tile(t, idx_cur, rng_cur, ring[t]);
         int64_t cur_q = -1;
-        uint32_t j = 0;                     // tiles produced so far (ring position)
-        if (i0 < i1) load_tile(0, idx_cur, rng_cur, cur);
+        uint32_t j = 0;                     // tiles produced so far (B ring position)
         for (int64_t item = i0; item < i1; ++item) {
             const int64_t u = item - i0;
             const int64_t qi = item / p.chunks;
@@ -334,62 +361,50 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
                 cp_async_wait<0>();
                 cur_q = qi;
             }
-#pragma unroll 1
+#pragma unroll
             for (int t = 0; t < kTiles; ++t, ++j) {
-                // the next tile's records (or the next item's first) fly while this one is
-                // converted
-                if (t + 1 < kTiles) {
-                    load_tile(t + 1, idx_cur, rng_cur, nxt);
-                } else if (item + 1 < i1) {
-                    load_tile(0, idx_nxt, rng_nxt, nxt);
-                }
-                const int s = j % kStages;
+                const int tp = t + kAhead - 1;          // tile whose loads start now
+                if (tp < kTiles) load_tile(tp, idx_cur, rng_cur, ring[tp % kAhead]);
+                else if (item + 1 < i1) load_tile(tp - kTiles, idx_nxt, rng_nxt, ring[tp % kAhead]);
+                const int s = static_cast<int>(j % kStages);
                 if (j >= kStages) wait_or_flag(smem_addr(&bars->empty[s]), ((j / kStages) - 1) & 1, ok);
                 uint8_t* const B = sB + s * kBBytes;
 #pragma unroll
                 for (int i = 0; i < kKeysPerWarp; ++i) {
                     uint4 oa, ob;
-                    convert<kRecord>(cur[i], lane, scale, oa, ob);
+                    convert<kRecord>(ring[t % kAhead][i], lane, scale, oa, ob);
                     store_row_pieces(B, kN, kKeysPerWarp * pw + i, lane, oa, ob);
                 }
                 fence_async_smem();
                 mbar_arrive(smem_addr(&bars->full[s]));
+                if (pw == 0) {
+                    if (lane == 0) {
+                        // the products of this stage, once every producer has filled it
+                        const int a = static_cast<int>(u & 1);
+                        if (t == 0 && u >= 2)     // the epilogue has read item u - 2's accumulator
+                            wait_or_flag(smem_addr(&bars->acc_empty[a]), ((u >> 1) - 1) & 1, ok);
+                        wait_or_flag(smem_addr(&bars->full[s]), (j / kStages) & 1, ok);
+                        tc_fence_after_sync();
+                        const uint32_t a0 = smem_addr(sA), b0 = smem_addr(B);
+                        const uint32_t d = tmem + a * kChunk + t * kN;
 #pragma unroll
-                for (int i = 0; i < kKeysPerWarp; ++i) cur[i] = nxt[i];
+                        for (int k = 0; k < 512 / 16; ++k) {   // K = 16 per instruction
+                            const uint32_t koff = (k & 3) * 32;
+                            mma_bf16(d, sw128_desc(a0 + (k >> 2) * kM * kRowBytes + koff),
+                                     sw128_desc(b0 + (k >> 2) * kN * kRowBytes + koff), kIdesc,
+                                     k > 0 ? 1u : 0u);
+                        }
+                        mma_commit(smem_addr(&bars->empty[s]));
+                        if (t == kTiles - 1) mma_commit(smem_addr(&bars->acc_full[a]));
+                    }
+                    __syncwarp();
+                }
             }
             idx_cur = idx_nxt;
             rng_cur = rng_nxt;
             load_indices(item + 2, idx_nxt, rng_nxt);
         }
         if (__any_sync(kFull, bad != 0u) && lane == 0) report(p.err, kErrIndex);
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------- MMA issue
-        if (lane == 0) {
-            uint32_t j = 0;
-            for (int64_t item = i0; item < i1; ++item) {
-                const int64_t u = item - i0;
-                const int a = static_cast<int>(u & 1);
-                if (u >= 2) wait_or_flag(smem_addr(&bars->acc_empty[a]), ((u >> 1) - 1) & 1, ok);
-                tc_fence_after_sync();
-                const uint32_t d0 = tmem + a * kChunk;
-                for (int t = 0; t < kTiles; ++t, ++j) {
-                    const int s = j % kStages;
-                    wait_or_flag(smem_addr(&bars->full[s]), (j / kStages) & 1, ok);
-                    tc_fence_after_sync();
-                    const uint32_t a0 = smem_addr(sA), b0 = smem_addr(sB + s * kBBytes);
-#pragma unroll
-                    for (int k = 0; k < 512 / 16; ++k) {   // K = 16 per instruction
-                        const uint32_t koff = (k & 3) * 32;
-                        mma_bf16(d0 + t * kN, sw128_desc(a0 + (k >> 2) * kM * kRowBytes + koff),
-                                 sw128_desc(b0 + (k >> 2) * kN * kRowBytes + koff), kIdesc,
-                                 k > 0 ? 1u : 0u);
-                    }
-                    mma_commit(smem_addr(&bars->empty[s]));
-                }
-                mma_commit(smem_addr(&bars->acc_full[a]));
-            }
-        }
-        __syncwarp();
     } else {
         // ------------------------------------------------------------- epilogue
         // Which entries are records (the rest are -inf) comes from the indices themselves:
