@@ -9,6 +9,8 @@
 // rows or multiply e4m3 rows by the cache's scale).
 #pragma once
 
+#include <type_traits>
+
 #include "device.cuh"
 #include "launch.h"
 
@@ -34,10 +36,18 @@ __device__ __forceinline__ uint32_t ldg_u8(const void* p) {
     return v;
 }
 
+// The bytes one lane holds of a record: its 8-dim chunks A (dims [8L, 8L+8)) and B (dims
+// [256+8L, 256+8L+8)) -- 8 e4m3 codes each, or 8 bf16 values for bf16 rows and for the V4
+// rotated tail on lanes 24..31 -- and, for the packed records, the two chunks' scale bytes
+// (A's in bits 0..7, B's in bits 8..15).  Sized per format, so a kernel that keeps several
+// records in flight per lane holds no unused register.
+template <int kRecord>
 struct Loaded {
-    uint4 a;        // codes of chunk A (.x, .y) or, for bf16 rows, 8 bf16
-    uint4 b;        // codes of chunk B (.x, .y) or, for the V4 tail lanes / bf16 rows, 8 bf16
-    uint32_t sa, sb;
+    using PieceA = typename std::conditional<kRecord == 1024, uint4, uint2>::type;
+    using PieceB = typename std::conditional<kRecord == 1024 || kRecord == 584, uint4, uint2>::type;
+    PieceA a;
+    PieceB b;
+    uint32_t s;
     bool valid;
 };
 
@@ -50,41 +60,37 @@ struct LaneBases {
 
 template <int kRecord>
 __device__ __forceinline__ void load_record(int64_t off, int64_t soff, const LaneBases& lb,
-                                            int lane, Loaded& r) {
+                                            int lane, Loaded<kRecord>& r) {
     r.valid = off >= 0;
     if (!r.valid) return;
     if constexpr (kRecord == 1024) {
         r.a = ldg_na16(lb.a + off);
         r.b = ldg_na16(lb.a + off + 512);
-        return;
-    }
-    const uint2 ta = ldg_na8(lb.a + off);
-    r.a = make_uint4(ta.x, ta.y, 0u, 0u);
-    if constexpr (kRecord == 512) {
-        const uint2 t = ldg_na8(lb.a + off + 256);
-        r.b = make_uint4(t.x, t.y, 0u, 0u);
-        return;
-    }
-    r.sa = ldg_u8(lb.s + soff);
-    if (kRecord == 528) {
-        const uint2 t = ldg_na8(lb.a + off + 256);
-        r.b = make_uint4(t.x, t.y, 0u, 0u);
-        r.sb = ldg_u8(lb.s + soff + 8);
-    } else if (lane < 24) {
-        const uint2 t = ldg_na8(lb.a + off + 256);
-        r.b = make_uint4(t.x, t.y, 0u, 0u);
-        r.sb = ldg_u8(lb.s + soff + 4);
-    } else {
-        r.b = ldg_na16(lb.tail + off);
-        r.sb = 0u;
+    } else if constexpr (kRecord == 512) {
+        r.a = ldg_na8(lb.a + off);
+        r.b = ldg_na8(lb.a + off + 256);
+    } else if constexpr (kRecord == 528) {
+        r.a = ldg_na8(lb.a + off);
+        r.b = ldg_na8(lb.a + off + 256);
+        r.s = ldg_u8(lb.s + soff) | (ldg_u8(lb.s + soff + 8) << 8);
+    } else {   // 584
+        r.a = ldg_na8(lb.a + off);
+        if (lane < 24) {
+            const uint2 t = ldg_na8(lb.a + off + 256);
+            r.b = make_uint4(t.x, t.y, 0u, 0u);
+            r.s = ldg_u8(lb.s + soff) | (ldg_u8(lb.s + soff + 4) << 8);
+        } else {
+            r.b = ldg_na16(lb.tail + off);
+            r.s = ldg_u8(lb.s + soff);
+        }
     }
 }
 
 // Dequantise a loaded record into this lane's two 16-byte pieces of the bf16 row (chunk
 // A = dims [8L, 8L+8), chunk B = dims [256+8L, 256+8L+8)); an invalid record gives zeros.
 template <int kRecord>
-__device__ __forceinline__ void convert(const Loaded& r, int lane, float scale, uint4& oa,
-                                        uint4& ob) {
+__device__ __forceinline__ void convert(const Loaded<kRecord>& r, int lane, float scale,
+                                        uint4& oa, uint4& ob) {
     oa = make_uint4(0u, 0u, 0u, 0u);
     ob = oa;
     if (r.valid) {
@@ -92,11 +98,14 @@ __device__ __forceinline__ void convert(const Loaded& r, int lane, float scale, 
             oa = r.a;
             ob = r.b;
         } else if constexpr (kRecord == 512) {
-            oa = dequant8_scaled(make_uint2(r.a.x, r.a.y), scale);
-            ob = dequant8_scaled(make_uint2(r.b.x, r.b.y), scale);
+            oa = dequant8_scaled(r.a, scale);
+            ob = dequant8_scaled(r.b, scale);
+        } else if constexpr (kRecord == 528) {
+            oa = dequant8(r.a, r.s & 0xFFu);
+            ob = dequant8(r.b, r.s >> 8);
         } else {
-            oa = dequant8(make_uint2(r.a.x, r.a.y), r.sa);
-            if (kRecord == 528 || lane < 24) ob = dequant8(make_uint2(r.b.x, r.b.y), r.sb);
+            oa = dequant8(r.a, r.s & 0xFFu);
+            if (lane < 24) ob = dequant8(make_uint2(r.b.x, r.b.y), r.s >> 8);
             else ob = r.b;
         }
     }

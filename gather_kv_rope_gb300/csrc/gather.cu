@@ -28,7 +28,7 @@ constexpr int kPerWarp = GKR_GATHER_PER_WARP;   // records per warp
 
 // Dequantise one loaded record (zeros for an invalid one) and write its output row.
 template <int kRecord>
-__device__ __forceinline__ void convert_store(const Loaded& r, uint8_t* orow, int lane,
+__device__ __forceinline__ void convert_store(const Loaded<kRecord>& r, uint8_t* orow, int lane,
                                               float scale) {
     uint4 oa, ob;
     convert<kRecord>(r, lane, scale, oa, ob);
@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kThreads, kRecord == 584 ? 6 : 8)
     lb.a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
     lb.tail = p.cache + 448 + 16 * (lane >= 24 ? lane - 24 : 0);
     lb.s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
-    Loaded r[U];
+    Loaded<kRecord> r[U];
 #pragma unroll
     for (int u = 0; u < U; ++u)
         load_record<kRecord>(__shfl_sync(kFull, off, u), __shfl_sync(kFull, soff, u), lb, lane, r[u]);

@@ -10,24 +10,27 @@
 // sets GKR_ERR_INDEX).  The gathered rows never leave the SM: the bf16 intermediate that
 // kv_gather writes (1 KB per index) and a separate product kernel reads back is gone.
 //
-// Launch shape (sm_103a, 5th-generation tensor cores): a persistent kernel, one CTA of 12
+// Launch shape (sm_103a, 5th-generation tensor cores): a persistent kernel, one CTA of 17
 // warps per SM, each CTA taking a contiguous run of work items (query, chunk of 256 keys)
 // in query-major order.
 //   * A: the query's heads (up to 128, zero-padded) in shared memory as the MMA's A
 //     operand (M = 128 x K = 512, bf16, K-major, 128-byte swizzle), copied with cp.async
 //     when the run reaches a new query, after the last product that read the old one.
-//   * 8 producer warps gather and dequantise the keys of a 32-key stage (4 each) into one
+//   * 16 producer warps gather and dequantise the keys of a 32-key stage (2 each) into one
 //     of 3 B tiles (N = 32 x K = 512, same layout); a ring of registers keeps the record
 //     loads of the next 3 stages in flight while one is converted.
-//   * lane 0 of the first producer warp, once all producers have filled a stage, issues its
-//     32 tcgen05.mma (kind::f16, K = 16 each) into that stage's 32 columns of one of two
-//     256-column TMEM accumulators and commits them to the stage's mbarrier (the stage
-//     may then be refilled); after an item's last stage it commits the accumulator.
-//   * 4 epilogue warps read their 32 accumulator lanes (tcgen05.ld), mask the entries that
-//     are not records (a ballot over the indices) and stream the fp32 logits, while the
-//     next item is multiplied into the other accumulator.
+//   * one warp, once all producers have filled a stage, issues its 32 tcgen05.mma
+//     (kind::f16, K = 16 each) into that stage's 32 columns of one of two 256-column TMEM
+//     accumulators and commits them to the stage's mbarrier (the stage may then be
+//     refilled); after an item's last stage it commits the accumulator.
+//   * after producing an item the producers drain the accumulator of the item before (the
+//     tensor cores are then on the new item, in the other accumulator): each reads a slice
+//     of 32 lanes x 64 columns (tcgen05.ld), masks the entries that are not records (a
+//     ballot over the indices) and streams the fp32 logits.
 // Every wait on an mbarrier is bounded (20 ms of %globaltimer): past it the CTA sets
 // GKR_ERR_TIMEOUT, stops waiting, still frees its tensor memory and returns.
+#include <type_traits>
+
 #include "decode.cuh"
 #include "device.cuh"
 #include "launch.h"
@@ -38,29 +41,26 @@ namespace {
 
 constexpr int kM = 128;                  // heads per tile (MMA rows)
 constexpr int kN = 32;                   // keys per B stage (MMA columns)
-constexpr int kChunk = 256;              // keys per work item
-constexpr int kTiles = kChunk / kN;      // B stages per item
+#ifndef GKR_LOGITS_AHEAD
+#define GKR_LOGITS_AHEAD 4
+#endif
+constexpr int kAhead = GKR_LOGITS_AHEAD; // producer register ring: while one stage is
+                                         // converted, the loads of the next kAhead - 1 fly
+constexpr int kTiles = 2 * kAhead;       // B stages per item: two turns of the ring
+constexpr int kChunk = kTiles * kN;      // keys per work item
 constexpr int kStages = 3;               // B ring depth
-constexpr int kEpilogueWarps = 4;        // warps 0..3: accumulator lanes 0..127
-constexpr int kProducerWarps = 8;        // warps 4..11: gather + dequantise; lane 0 of warp 4
-                                         // also issues the tensor-core products
-constexpr int kFirstProducer = kEpilogueWarps;
-constexpr int kMmaWarp = kFirstProducer;                    // allocates and frees TMEM too
+constexpr int kProducerWarps = 16;       // warps 0..15: gather + dequantise, and drain
+                                         // the accumulator of the item before
+constexpr int kMmaWarp = kProducerWarps; // warp 16: tcgen05.mma issue; allocates and frees
+                                         // TMEM too
 constexpr int kKeysPerWarp = kN / kProducerWarps;           // keys of a stage per producer
-// Producer register ring: the records of kAhead stages; while one stage is converted the
-// loads of the next kAhead - 1 are in flight.  Four for the 8-byte-per-lane records (V4.1,
-// fp8 rows), two where a lane holds 16-byte pieces (the V4 bf16 tail, bf16 rows) and four
-// would spill.
-template <int kRecord>
-struct Ahead {
-    static constexpr int value = kRecord == 528 || kRecord == 512 ? 4 : 2;
-};
-constexpr int kLogitThreads = (kEpilogueWarps + kProducerWarps) * 32;   // 12 warps: 3 per
-                                         // SM sub-partition, up to 168 registers a thread
+constexpr int kDrainCols = kChunk / (kProducerWarps / 4);   // accumulator columns a warp
+                                                            // drains (its lanes: warp % 4)
+constexpr int kLogitThreads = (kMmaWarp + 1) * 32;          // 17 warps: up to 96 registers
 constexpr int kRowBytes = 128;           // one swizzle row: 64 bf16 of K
 constexpr int kABytes = kM * 1024;       // 128 KB
 constexpr int kBBytes = kN * 1024;       // 32 KB per stage
-constexpr uint32_t kTmemCols = 2 * kChunk;   // two fp32 accumulators (512 columns)
+constexpr uint32_t kTmemCols = 512;      // two fp32 accumulators of kChunk columns
 constexpr int32_t kErrIndex = 4;
 constexpr int32_t kErrTimeout = 16;
 constexpr uint64_t kWaitNs = 20000000;    // a wait gives up after 20 ms (a normal one takes us)
@@ -70,8 +70,9 @@ static_assert(kChunk % kN == 0 && (kTmemCols & (kTmemCols - 1)) == 0 && kTmemCol
               "tensor memory is allocated in powers of two of 32 .. 512 columns");
 static_assert(kKeysPerWarp * kTiles <= 32,
               "a producer lane holds the index of one (tile, key) pair of an item");
-static_assert(kTiles % Ahead<528>::value == 0 && kTiles % Ahead<584>::value == 0,
-              "ring slots repeat identically in every item");
+static_assert(kAhead == 3 || kAhead == 4, "the stage loop is written for rings of 3 or 4");
+static_assert(2 * kChunk <= static_cast<int>(kTmemCols) && kChunk % 64 == 0,
+              "two accumulators fit; each producer drains a whole number of 16-column loads");
 
 // ------------------------------------------------------------- tcgen05 / mbarrier PTX
 
@@ -161,6 +162,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive fp32 accumulator columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A and B
 // (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at
 // bits 24-28.
@@ -201,8 +217,8 @@ __device__ __forceinline__ void store_row_pieces(uint8_t* op, int rows, int r, i
 struct alignas(8) Barriers {
     uint64_t full[kStages];      // producers -> MMA: B stage holds its 32 keys
     uint64_t empty[kStages];     // MMA -> producers: the stage's products are done
-    uint64_t acc_full[2];        // MMA -> epilogue: an item's accumulator is complete
-    uint64_t acc_empty[2];       // epilogue -> MMA: the accumulator has been read
+    uint64_t acc_full[2];        // MMA -> producers: an item's accumulator is complete
+    uint64_t acc_empty[2];       // producers -> MMA: the accumulator has been read
     uint32_t tmem_base;
     int32_t timed_out;
 };
@@ -268,7 +284,7 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_addr(&bars->acc_full[a]), 1);
-            mbar_init(smem_addr(&bars->acc_empty[a]), kEpilogueWarps * 32);
+            mbar_init(smem_addr(&bars->acc_empty[a]), kProducerWarps * 32);
         }
         bars->timed_out = 0;
         mbar_init_fence();
@@ -281,9 +297,9 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
     const uint32_t tmem = bars->tmem_base;
     bool ok = true;
 
-    if (warp >= kFirstProducer && warp < kFirstProducer + kProducerWarps) {
+    if (warp < kProducerWarps) {
         // ------------------------------------------------------------- producers
-        const int pw = warp - kFirstProducer;
+        const int pw = warp;
         float scale = 1.0f;
         bool scale_bad = false;
         if constexpr (kRecord == 512) {
@@ -298,8 +314,7 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
         uint32_t bad = 0;
         // lane L < kTiles * kKeysPerWarp holds the index of this warp's key
         // (L / kKeysPerWarp, L % kKeysPerWarp) = tile L / kKeysPerWarp, key
-        // kKeysPerWarp * pw + L % kKeysPerWarp of an item; idx_cur for the current item,
-        // idx_nxt for the next one
+        // kKeysPerWarp * pw + L % kKeysPerWarp of an item
         auto load_indices = [&](int64_t item, int32_t& idx, bool& in_range) {
             idx = -1;
             in_range = false;
@@ -310,13 +325,8 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
             in_range = k < p.topk;
             if (in_range) idx = __ldg(p.indices + qi * p.topk + k);
         };
-        int32_t idx_cur, idx_nxt;
-        bool rng_cur, rng_nxt;
-        load_indices(i0, idx_cur, rng_cur);
-        load_indices(i0 + 1, idx_nxt, rng_nxt);
-
-        // the records of tile t (indices in idx_all)
-        auto load_tile = [&](int t, int32_t idx_all, bool rng_all, Loaded (&r)[kKeysPerWarp]) {
+        // the records of tile t of an item whose indices are in idx_all
+        auto load_tile = [&](int t, int32_t idx_all, bool rng_all, Loaded<kRecord> (&r)[kKeysPerWarp]) {
 #pragma unroll
             for (int i = 0; i < kKeysPerWarp; ++i) {
                 const int src = t * kKeysPerWarp + i;
@@ -327,128 +337,165 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
                 load_record<kRecord>(off, soff, lb, lane, r[i]);
             }
         };
-        // register ring: tile t of an item lives in slot t % kAhead; while tile t is
-        // converted, the loads of tiles t + 1 .. t + kAhead - 1 (of this item or the next)
-        // are in flight
-        constexpr int kAhead = Ahead<kRecord>::value;
-        Loaded ring[kAhead][kKeysPerWarp];
+        // idx_cur: the indices of the item being converted; idx_nxt: of the next one
+        int32_t idx_cur, idx_nxt;
+        bool rng_cur, rng_nxt;
+        load_indices(i0, idx_cur, rng_cur);
+        load_indices(i0 + 1, idx_nxt, rng_nxt);
+        // register ring over the CTA's stages g = 0, 1, ...: stage g (item g / kTiles, tile
+        // g % kTiles) lives in slot g % kAhead; while it is converted the loads of stages
+        // g + 1 .. g + kAhead - 1 (of this item or the next) are in flight
+        Loaded<kRecord> ring[kAhead][kKeysPerWarp];
 #pragma unroll
-        for (int t = 0; t < kAhead - 1; ++t)
-            if (i0 < i1) load_tile(t, idx_cur, rng_cur, ring[t]);
+        for (int t = 0; t < kAhead - 1; ++t) load_tile(t, idx_cur, rng_cur, ring[t]);
+        const uint32_t stages = static_cast<uint32_t>(i1 - i0) * kTiles;
         int64_t cur_q = -1;
-        uint32_t j = 0;                     // tiles produced so far (B ring position)
-        for (int64_t item = i0; item < i1; ++item) {
-            const int64_t u = item - i0;
+        // Read this warp's slice of item v's accumulator -- lanes 32 (pw % 4) .. +31 (heads),
+        // columns (pw / 4) * kDrainCols .. +kDrainCols-1 (entries) -- and write the logits;
+        // which entries are records comes from the indices (lane l reads the index of
+        // column c + l of each 32-column block, a ballot gives the block's mask).
+        auto drain = [&](int64_t v) {
+            const int a = static_cast<int>(v & 1);
+            const int64_t item = i0 + v;
             const int64_t qi = item / p.chunks;
-            if (qi != cur_q) {
-                // the query tile changes: every product that read the old one must be done
-                if (u > 0) wait_or_flag(smem_addr(&bars->acc_full[(u - 1) & 1]), ((u - 1) >> 1) & 1, ok);
-                // every row's copies in flight at once (cp.async into the swizzled places),
-                // one wait; rows past num_heads are zero
-                const uint8_t* const qrow = static_cast<const uint8_t*>(p.q) + qi * p.num_heads * 1024;
-                for (int h = pw; h < kM; h += kProducerWarps) {
-                    if (h < p.num_heads) {
-                        cp_async16(sA + sw128_offset(kM, h, lane >> 3, lane & 7),
-                                   qrow + h * 1024 + 16 * lane);
-                        cp_async16(sA + sw128_offset(kM, h, 4 + (lane >> 3), lane & 7),
-                                   qrow + h * 1024 + 512 + 16 * lane);
-                    } else {
-                        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                        store_row_pieces(sA, kM, h, lane, z, z);
-                    }
-                }
-                cp_async_commit();
-                cp_async_wait<0>();
-                cur_q = qi;
-            }
+            const int col0 = (pw >> 2) * kDrainCols;
+            const int64_t k0 = (item % p.chunks) * kChunk + col0;
+            int32_t idx[kDrainCols / 32];
 #pragma unroll
-            for (int t = 0; t < kTiles; ++t, ++j) {
-                const int tp = t + kAhead - 1;          // tile whose loads start now
-                if (tp < kTiles) load_tile(tp, idx_cur, rng_cur, ring[tp % kAhead]);
-                else if (item + 1 < i1) load_tile(tp - kTiles, idx_nxt, rng_nxt, ring[tp % kAhead]);
-                const int s = static_cast<int>(j % kStages);
-                if (j >= kStages) wait_or_flag(smem_addr(&bars->empty[s]), ((j / kStages) - 1) & 1, ok);
-                uint8_t* const B = sB + s * kBBytes;
-#pragma unroll
-                for (int i = 0; i < kKeysPerWarp; ++i) {
-                    uint4 oa, ob;
-                    convert<kRecord>(ring[t % kAhead][i], lane, scale, oa, ob);
-                    store_row_pieces(B, kN, kKeysPerWarp * pw + i, lane, oa, ob);
-                }
-                fence_async_smem();
-                mbar_arrive(smem_addr(&bars->full[s]));
-                if (pw == 0) {
-                    if (lane == 0) {
-                        // the products of this stage, once every producer has filled it
-                        const int a = static_cast<int>(u & 1);
-                        if (t == 0 && u >= 2)     // the epilogue has read item u - 2's accumulator
-                            wait_or_flag(smem_addr(&bars->acc_empty[a]), ((u >> 1) - 1) & 1, ok);
-                        wait_or_flag(smem_addr(&bars->full[s]), (j / kStages) & 1, ok);
-                        tc_fence_after_sync();
-                        const uint32_t a0 = smem_addr(sA), b0 = smem_addr(B);
-                        const uint32_t d = tmem + a * kChunk + t * kN;
-#pragma unroll
-                        for (int k = 0; k < 512 / 16; ++k) {   // K = 16 per instruction
-                            const uint32_t koff = (k & 3) * 32;
-                            mma_bf16(d, sw128_desc(a0 + (k >> 2) * kM * kRowBytes + koff),
-                                     sw128_desc(b0 + (k >> 2) * kN * kRowBytes + koff), kIdesc,
-                                     k > 0 ? 1u : 0u);
-                        }
-                        mma_commit(smem_addr(&bars->empty[s]));
-                        if (t == kTiles - 1) mma_commit(smem_addr(&bars->acc_full[a]));
-                    }
-                    __syncwarp();
-                }
-            }
-            idx_cur = idx_nxt;
-            rng_cur = rng_nxt;
-            load_indices(item + 2, idx_nxt, rng_nxt);
-        }
-        if (__any_sync(kFull, bad != 0u) && lane == 0) report(p.err, kErrIndex);
-    } else {
-        // ------------------------------------------------------------- epilogue
-        // Which entries are records (the rest are -inf) comes from the indices themselves:
-        // lane l reads the index of column c + l of each 32-column block, and a ballot
-        // gives every lane the block's mask.
-        const int h = 32 * warp + lane;             // warps 0..3: accumulator lanes
-        bool scale_bad = false;
-        if constexpr (kRecord == 512) scale_bad = !scale_ok(__ldg(p.fp8_scale));
-        for (int64_t item = i0; item < i1; ++item) {
-            const int64_t u = item - i0;
-            const int a = static_cast<int>(u & 1);
-            const int64_t qi = item / p.chunks;
-            const int64_t k0 = (item % p.chunks) * kChunk;
-            int32_t idx[kChunk / 32];
-#pragma unroll
-            for (int c = 0; c < kChunk / 32; ++c) {
+            for (int c = 0; c < kDrainCols / 32; ++c) {
                 const int64_t k = k0 + 32 * c + lane;
                 idx[c] = k < p.topk ? __ldg(p.indices + qi * p.topk + k) : -1;
             }
-            wait_or_flag(smem_addr(&bars->acc_full[a]), (u >> 1) & 1, ok);
+            wait_or_flag(smem_addr(&bars->acc_full[a]), (v >> 1) & 1, ok);
             tc_fence_after_sync();
+            const int h = 32 * (pw & 3) + lane;
             float* const orow = p.out + (qi * p.num_heads + h) * p.topk + k0;
-#pragma unroll
-            for (int c = 0; c < kChunk / 32; ++c) {
+#pragma unroll 1
+            for (int c = 0; c < kDrainCols / 16; ++c) {   // 16 columns at a time
                 const uint32_t mask =
-                    __ballot_sync(kFull, !scale_bad && idx[c] >= 0 && idx[c] < p.num_slots);
-                float v[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + a * kChunk + 32 * c, v);
+                    __ballot_sync(kFull, !scale_bad && idx[c >> 1] >= 0 && idx[c >> 1] < p.num_slots) >>
+                    (16 * (c & 1));
+                float val[16];
+                tmem_ld16(tmem + (static_cast<uint32_t>(32 * (pw & 3)) << 16) + a * kChunk + col0 +
+                              16 * c,
+                          val);
                 if (h < p.num_heads && ok) {
 #pragma unroll
-                    for (int jj = 0; jj < 32; jj += 4) {
-                        if (k0 + 32 * c + jj >= p.topk) break;   // topk is a multiple of 4
+                    for (int jj = 0; jj < 16; jj += 4) {
+                        if (k0 + 16 * c + jj >= p.topk) break;   // topk is a multiple of 4
                         float4 o;
-                        o.x = (mask >> jj) & 1u ? __fmul_rn(v[jj], p.sm_scale) : -INFINITY;
-                        o.y = (mask >> (jj + 1)) & 1u ? __fmul_rn(v[jj + 1], p.sm_scale) : -INFINITY;
-                        o.z = (mask >> (jj + 2)) & 1u ? __fmul_rn(v[jj + 2], p.sm_scale) : -INFINITY;
-                        o.w = (mask >> (jj + 3)) & 1u ? __fmul_rn(v[jj + 3], p.sm_scale) : -INFINITY;
-                        __stcs(reinterpret_cast<float4*>(orow + 32 * c + jj), o);
+                        o.x = (mask >> jj) & 1u ? __fmul_rn(val[jj], p.sm_scale) : -INFINITY;
+                        o.y = (mask >> (jj + 1)) & 1u ? __fmul_rn(val[jj + 1], p.sm_scale) : -INFINITY;
+                        o.z = (mask >> (jj + 2)) & 1u ? __fmul_rn(val[jj + 2], p.sm_scale) : -INFINITY;
+                        o.w = (mask >> (jj + 3)) & 1u ? __fmul_rn(val[jj + 3], p.sm_scale) : -INFINITY;
+                        __stcs(reinterpret_cast<float4*>(orow + 16 * c + jj), o);
                     }
                 }
             }
             tc_fence_before_sync();
             mbar_arrive(smem_addr(&bars->acc_empty[a]));
+        };
+        // one stage: slot R of the ring (static), stage number g
+        auto stage = [&](auto slot_c, uint32_t g) {
+            constexpr int R = decltype(slot_c)::value;
+            const int t = static_cast<int>(g % kTiles);
+            const int64_t u = g / kTiles;
+            const int64_t item = i0 + u;
+            if (t == 0) {
+                if (u > 0) {              // the next item's indices become current
+                    idx_cur = idx_nxt;
+                    rng_cur = rng_nxt;
+                    load_indices(item + 1, idx_nxt, rng_nxt);
+                }
+                const int64_t qi = item / p.chunks;
+                if (qi != cur_q) {
+                    // the query tile changes: every product that read the old one must be
+                    // done; then all of its rows' copies in flight at once (cp.async into
+                    // the swizzled places), one wait; rows past num_heads are zero
+                    if (u > 0)
+                        wait_or_flag(smem_addr(&bars->acc_full[(u - 1) & 1]), ((u - 1) >> 1) & 1, ok);
+                    const uint8_t* const qrow =
+                        static_cast<const uint8_t*>(p.q) + qi * p.num_heads * 1024;
+                    for (int h = pw; h < kM; h += kProducerWarps) {
+                        if (h < p.num_heads) {
+                            cp_async16(sA + sw128_offset(kM, h, lane >> 3, lane & 7),
+                                       qrow + h * 1024 + 16 * lane);
+                            cp_async16(sA + sw128_offset(kM, h, 4 + (lane >> 3), lane & 7),
+                                       qrow + h * 1024 + 512 + 16 * lane);
+                        } else {
+                            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                            store_row_pieces(sA, kM, h, lane, z, z);
+                        }
+                    }
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                    cur_q = qi;
+                }
+            }
+            // start the loads of stage g + kAhead - 1
+            {
+                constexpr int RP = (R + kAhead - 1) % kAhead;
+                const uint32_t gp = g + kAhead - 1;
+                if (gp < stages) {
+                    const int tp = static_cast<int>(gp % kTiles);
+                    if (gp / kTiles == static_cast<uint32_t>(u)) load_tile(tp, idx_cur, rng_cur, ring[RP]);
+                    else load_tile(tp, idx_nxt, rng_nxt, ring[RP]);
+                }
+            }
+            const int s = static_cast<int>(g % kStages);
+            if (g >= kStages) wait_or_flag(smem_addr(&bars->empty[s]), ((g / kStages) - 1) & 1, ok);
+            uint8_t* const B = sB + s * kBBytes;
+#pragma unroll
+            for (int i = 0; i < kKeysPerWarp; ++i) {
+                uint4 oa, ob;
+                convert<kRecord>(ring[R][i], lane, scale, oa, ob);
+                store_row_pieces(B, kN, kKeysPerWarp * pw + i, lane, oa, ob);
+            }
+            fence_async_smem();
+            mbar_arrive(smem_addr(&bars->full[s]));
+        };
+        for (uint32_t g = 0; g < stages; g += kTiles) {    // one item; kTiles = 2 * kAhead
+#pragma unroll 1
+            for (uint32_t h = 0; h < kTiles; h += kAhead) {
+                stage(std::integral_constant<int, 0>{}, g + h);
+                stage(std::integral_constant<int, 1>{}, g + h + 1);
+                stage(std::integral_constant<int, 2>{}, g + h + 2);
+                if constexpr (kAhead == 4) stage(std::integral_constant<int, 3>{}, g + h + 3);
+            }
+            // then drain the item before (the tensor cores are on this item's stages, in the
+            // other accumulator)
+            if (g > 0) drain(g / kTiles - 1);
         }
+        if (i1 > i0) drain(i1 - i0 - 1);
+        if (__any_sync(kFull, bad != 0u) && lane == 0) report(p.err, kErrIndex);
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            uint32_t j = 0;
+            for (int64_t item = i0; item < i1; ++item) {
+                const int64_t u = item - i0;
+                const int a = static_cast<int>(u & 1);
+                if (u >= 2) wait_or_flag(smem_addr(&bars->acc_empty[a]), ((u >> 1) - 1) & 1, ok);
+                tc_fence_after_sync();
+                const uint32_t d0 = tmem + a * kChunk;
+                for (int t = 0; t < kTiles; ++t, ++j) {
+                    const int s = static_cast<int>(j % kStages);
+                    wait_or_flag(smem_addr(&bars->full[s]), (j / kStages) & 1, ok);
+                    tc_fence_after_sync();
+                    const uint32_t a0 = smem_addr(sA), b0 = smem_addr(sB + s * kBBytes);
+#pragma unroll
+                    for (int k = 0; k < 512 / 16; ++k) {   // K = 16 per instruction
+                        const uint32_t koff = (k & 3) * 32;
+                        mma_bf16(d0 + t * kN, sw128_desc(a0 + (k >> 2) * kM * kRowBytes + koff),
+                                 sw128_desc(b0 + (k >> 2) * kN * kRowBytes + koff), kIdesc,
+                                 k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_addr(&bars->empty[s]));
+                }
+                mma_commit(smem_addr(&bars->acc_full[a]));
+            }
+        }
+        __syncwarp();
     }
     if (!ok) atomicOr(&bars->timed_out, 1);
     tc_fence_before_sync();
