@@ -235,6 +235,22 @@ __device__ __forceinline__ void wait_or_flag(uint32_t bar, uint32_t parity, bool
     if (ok) ok = mbar_wait(bar, parity);
 }
 
+// The same for a whole warp: lane 0 waits, the warp follows it (__syncwarp orders the
+// lanes' later accesses after lane 0's acquire); every lane gets the outcome.
+__device__ __forceinline__ void warp_wait_or_flag(uint32_t bar, uint32_t parity, bool& ok,
+                                                  int lane) {
+    if (lane == 0) wait_or_flag(bar, parity, ok);
+    ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+}
+
+// One arrival for a whole warp: every lane's earlier shared-memory writes (each lane has
+// fenced them for the async proxy) are ordered before lane 0's arrive by __syncwarp.
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+}
+
 // Decode key k of query row idx_row into the record's byte offsets (off = -1: not a
 // record: past topk, index -1, out of range (bad = 1), or a bad fp8 scale).
 template <int kRecord>
@@ -279,12 +295,12 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_addr(&bars->full[s]), kProducerWarps * 32);
+            mbar_init(smem_addr(&bars->full[s]), kProducerWarps);
             mbar_init(smem_addr(&bars->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_addr(&bars->acc_full[a]), 1);
-            mbar_init(smem_addr(&bars->acc_empty[a]), kProducerWarps * 32);
+            mbar_init(smem_addr(&bars->acc_empty[a]), kProducerWarps);
         }
         bars->timed_out = 0;
         mbar_init_fence();
@@ -366,7 +382,7 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
                 const int64_t k = k0 + 32 * c + lane;
                 idx[c] = k < p.topk ? __ldg(p.indices + qi * p.topk + k) : -1;
             }
-            wait_or_flag(smem_addr(&bars->acc_full[a]), (v >> 1) & 1, ok);
+            warp_wait_or_flag(smem_addr(&bars->acc_full[a]), (v >> 1) & 1, ok, lane);
             tc_fence_after_sync();
             const int h = 32 * (pw & 3) + lane;
             float* const orow = p.out + (qi * p.num_heads + h) * p.topk + k0;
@@ -393,7 +409,7 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
                 }
             }
             tc_fence_before_sync();
-            mbar_arrive(smem_addr(&bars->acc_empty[a]));
+            warp_arrive(smem_addr(&bars->acc_empty[a]), lane);
         };
         // one stage: slot R of the ring (static), stage number g
         auto stage = [&](auto slot_c, uint32_t g) {
@@ -413,7 +429,8 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
                     // done; then all of its rows' copies in flight at once (cp.async into
                     // the swizzled places), one wait; rows past num_heads are zero
                     if (u > 0)
-                        wait_or_flag(smem_addr(&bars->acc_full[(u - 1) & 1]), ((u - 1) >> 1) & 1, ok);
+                        warp_wait_or_flag(smem_addr(&bars->acc_full[(u - 1) & 1]),
+                                          ((u - 1) >> 1) & 1, ok, lane);
                     const uint8_t* const qrow =
                         static_cast<const uint8_t*>(p.q) + qi * p.num_heads * 1024;
                     for (int h = pw; h < kM; h += kProducerWarps) {
@@ -443,7 +460,8 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
                 }
             }
             const int s = static_cast<int>(g % kStages);
-            if (g >= kStages) wait_or_flag(smem_addr(&bars->empty[s]), ((g / kStages) - 1) & 1, ok);
+            if (g >= kStages)
+                warp_wait_or_flag(smem_addr(&bars->empty[s]), ((g / kStages) - 1) & 1, ok, lane);
             uint8_t* const B = sB + s * kBBytes;
 #pragma unroll
             for (int i = 0; i < kKeysPerWarp; ++i) {
@@ -452,7 +470,7 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
                 store_row_pieces(B, kN, kKeysPerWarp * pw + i, lane, oa, ob);
             }
             fence_async_smem();
-            mbar_arrive(smem_addr(&bars->full[s]));
+            warp_arrive(smem_addr(&bars->full[s]), lane);
         };
         for (uint32_t g = 0; g < stages; g += kTiles) {    // one item; kTiles = 2 * kAhead
 #pragma unroll 1
