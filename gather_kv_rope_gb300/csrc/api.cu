@@ -373,7 +373,8 @@ GKR_API gkr_status gkr_sparse_logits(const void* q, int32_t num_heads, const voi
     p.indices = indices;
     p.num_queries = num_queries;
     p.topk = topk;
-    p.chunks = (topk + gkr::logits_chunk_keys() - 1) / gkr::logits_chunk_keys();
+    const int64_t chunk = gkr::logits_chunk_keys(cache->record);
+    p.chunks = (topk + chunk - 1) / chunk;
     if (num_queries > INT64_C(0x7FFFFFFF) / p.chunks) return GKR_EINVAL;   // grid < 2^31
     p.sm_scale = sm_scale;
     p.fp8_scale = fp8 ? fp8_scale : nullptr;

@@ -184,7 +184,7 @@ cudaError_t launch_qnorm_rope_kv_insert(int32_t record, const InsertParams& p,
                                         const QSideParams& qp, cudaStream_t stream);
 // Sparse decode logits from the cache records, gathered and dequantised on chip.
 cudaError_t launch_sparse_logits(int32_t record, const LogitsParams& p, cudaStream_t stream);
-int32_t logits_chunk_keys();   // keys per CTA
+int32_t logits_chunk_keys(int32_t record);   // keys per work item
 int32_t logits_max_heads();    // heads per query at most
 cudaError_t launch_gather_v41(const GatherParams& p, cudaStream_t stream);
 cudaError_t launch_gather_v4(const GatherParams& p, cudaStream_t stream);

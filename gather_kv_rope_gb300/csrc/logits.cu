@@ -10,13 +10,13 @@
 // sets GKR_ERR_INDEX).  The gathered rows never leave the SM: the bf16 intermediate that
 // kv_gather writes (1 KB per index) and a separate product kernel reads back is gone.
 //
-// Launch shape (sm_103a, 5th-generation tensor cores): a persistent kernel, one CTA of 17
+// Launch shape (sm_103a, 5th-generation tensor cores): a persistent kernel, one CTA of 9
 // warps per SM, each CTA taking a contiguous run of work items (query, chunk of 256 keys)
 // in query-major order.
 //   * A: the query's heads (up to 128, zero-padded) in shared memory as the MMA's A
 //     operand (M = 128 x K = 512, bf16, K-major, 128-byte swizzle), copied with cp.async
 //     when the run reaches a new query, after the last product that read the old one.
-//   * 16 producer warps gather and dequantise the keys of a 32-key stage (2 each) into one
+//   * 8 producer warps gather and dequantise the keys of a 32-key stage (4 each) into one
 //     of 3 B tiles (N = 32 x K = 512, same layout); a ring of registers keeps the record
 //     loads of the next 3 stages in flight while one is converted.
 //   * one warp, once all producers have filled a stage, issues its 32 tcgen05.mma
@@ -25,7 +25,7 @@
 //     refilled); after an item's last stage it commits the accumulator.
 //   * after producing an item the producers drain the accumulator of the item before (the
 //     tensor cores are then on the new item, in the other accumulator): each reads a slice
-//     of 32 lanes x 64 columns (tcgen05.ld), masks the entries that are not records (a
+//     of 32 lanes x 128 columns (tcgen05.ld), masks the entries that are not records (a
 //     ballot over the indices) and streams the fp32 logits.
 // Every wait on an mbarrier is bounded (20 ms of %globaltimer): past it the CTA sets
 // GKR_ERR_TIMEOUT, stops waiting, still frees its tensor memory and returns.
@@ -41,22 +41,25 @@ namespace {
 
 constexpr int kM = 128;                  // heads per tile (MMA rows)
 constexpr int kN = 32;                   // keys per B stage (MMA columns)
-#ifndef GKR_LOGITS_AHEAD
-#define GKR_LOGITS_AHEAD 4
-#endif
-constexpr int kAhead = GKR_LOGITS_AHEAD; // producer register ring: while one stage is
-                                         // converted, the loads of the next kAhead - 1 fly
-constexpr int kTiles = 2 * kAhead;       // B stages per item: two turns of the ring
-constexpr int kChunk = kTiles * kN;      // keys per work item
+// Per record format: the producers' register ring (while one stage is converted, the
+// record loads of the next ahead - 1 stages are in flight) and, from it, the work item
+// (two turns of the ring: tiles stages of 32 keys).  Three slots for the records a lane
+// holds 8 bytes of per chunk (V4.1, fp8 rows), two where it holds 16-byte pieces (the V4
+// bf16 tail, bf16 rows), the most that fit the 168 registers without spilling.
+template <int kRecord>
+struct Shape {
+    static constexpr int ahead = kRecord == 528 || kRecord == 512 ? 3 : 2;
+    static constexpr int tiles = 2 * ahead;
+    static constexpr int chunk = tiles * kN;                 // keys per work item
+    static constexpr int drain_cols = chunk / (8 / 4);       // accumulator columns a producer
+};                                                           // warp drains
 constexpr int kStages = 3;               // B ring depth
-constexpr int kProducerWarps = 16;       // warps 0..15: gather + dequantise, and drain
-                                         // the accumulator of the item before
-constexpr int kMmaWarp = kProducerWarps; // warp 16: tcgen05.mma issue; allocates and frees
+constexpr int kProducerWarps = 8;        // warps 0..7: gather + dequantise, and drain the
+                                         // accumulator of the item before
+constexpr int kMmaWarp = kProducerWarps; // warp 8: tcgen05.mma issue; allocates and frees
                                          // TMEM too
 constexpr int kKeysPerWarp = kN / kProducerWarps;           // keys of a stage per producer
-constexpr int kDrainCols = kChunk / (kProducerWarps / 4);   // accumulator columns a warp
-                                                            // drains (its lanes: warp % 4)
-constexpr int kLogitThreads = (kMmaWarp + 1) * 32;          // 17 warps: up to 96 registers
+constexpr int kLogitThreads = (kMmaWarp + 1) * 32;          // 9 warps: up to 168 registers
 constexpr int kRowBytes = 128;           // one swizzle row: 64 bf16 of K
 constexpr int kABytes = kM * 1024;       // 128 KB
 constexpr int kBBytes = kN * 1024;       // 32 KB per stage
@@ -65,14 +68,12 @@ constexpr int32_t kErrIndex = 4;
 constexpr int32_t kErrTimeout = 16;
 constexpr uint64_t kWaitNs = 20000000;    // a wait gives up after 20 ms (a normal one takes us)
 
-static_assert(kChunk % kN == 0 && (kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols >= 32 &&
-                  kTmemCols <= 512,
-              "tensor memory is allocated in powers of two of 32 .. 512 columns");
-static_assert(kKeysPerWarp * kTiles <= 32,
+static_assert(kProducerWarps == 8, "two producer warps drain each quarter of the lanes");
+static_assert(kKeysPerWarp * Shape<528>::tiles <= 32 && kKeysPerWarp * Shape<584>::tiles <= 32,
               "a producer lane holds the index of one (tile, key) pair of an item");
-static_assert(kAhead == 3 || kAhead == 4, "the stage loop is written for rings of 3 or 4");
-static_assert(2 * kChunk <= static_cast<int>(kTmemCols) && kChunk % 64 == 0,
-              "two accumulators fit; each producer drains a whole number of 16-column loads");
+static_assert(2 * Shape<528>::chunk <= static_cast<int>(kTmemCols) &&
+                  Shape<528>::drain_cols % 32 == 0 && Shape<584>::drain_cols % 32 == 0,
+              "two accumulators fit; a producer drains whole 32-column index blocks");
 
 // ------------------------------------------------------------- tcgen05 / mbarrier PTX
 
@@ -275,6 +276,10 @@ __device__ __forceinline__ void key_offsets(const LogitsParams& p, int32_t idx, 
 
 template <int kRecord>
 __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const LogitsParams p) {
+    constexpr int kAhead = Shape<kRecord>::ahead;
+    constexpr int kTiles = Shape<kRecord>::tiles;
+    constexpr int kChunk = Shape<kRecord>::chunk;
+    constexpr int kDrainCols = Shape<kRecord>::drain_cols;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the swizzle groups
     uint8_t* const base = reinterpret_cast<uint8_t*>(
@@ -477,8 +482,7 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
             for (uint32_t h = 0; h < kTiles; h += kAhead) {
                 stage(std::integral_constant<int, 0>{}, g + h);
                 stage(std::integral_constant<int, 1>{}, g + h + 1);
-                stage(std::integral_constant<int, 2>{}, g + h + 2);
-                if constexpr (kAhead == 4) stage(std::integral_constant<int, 3>{}, g + h + 3);
+                if constexpr (kAhead > 2) stage(std::integral_constant<int, 2>{}, g + h + 2);
             }
             // then drain the item before (the tensor cores are on this item's stages, in the
             // other accumulator)
@@ -538,7 +542,9 @@ cudaError_t launch(const LogitsParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-int32_t logits_chunk_keys() { return kChunk; }
+int32_t logits_chunk_keys(int32_t record) {
+    return record == 528 || record == 512 ? Shape<528>::chunk : Shape<584>::chunk;
+}
 int32_t logits_max_heads() { return kM; }
 
 cudaError_t launch_sparse_logits(int32_t record, const LogitsParams& p, cudaStream_t stream) {
