@@ -10,28 +10,31 @@
 // sets GKR_ERR_INDEX).  The gathered rows never leave the SM: the bf16 intermediate that
 // kv_gather writes (1 KB per index) and a separate product kernel reads back is gone.
 //
-// Launch shape (sm_103a, 5th-generation tensor cores): a persistent kernel, one CTA of 9
-// warps per SM, each CTA taking a contiguous run of work items (query, chunk of 256 keys)
+// Launch shape (sm_103a, 5th-generation tensor cores): a persistent kernel, one CTA of 21
+// warps per SM, each CTA taking a contiguous run of work items (query, chunk of 128 keys)
 // in query-major order.
-//   * A: the query's heads (up to 128, zero-padded) in shared memory as the MMA's A
-//     operand (M = 128 x K = 512, bf16, K-major, 128-byte swizzle), copied with cp.async
-//     when the run reaches a new query, after the last product that read the old one.
-//   * 8 producer warps gather and dequantise the keys of a 32-key stage (4 each) into one
-//     of 3 B tiles (N = 32 x K = 512, same layout); a ring of registers keeps the record
-//     loads of the next 3 stages in flight while one is converted.
+//   * A, the query's heads (up to 128, zero-padded; M = 128 x K = 512, bf16), lives in
+//     tensor memory next to the accumulators, so shared memory is left to the records.
+//     The 4 epilogue warps write it (tcgen05.st) when the run reaches a new query, once
+//     the products that read the old one are done.
+//   * 16 producer warps keep a ring of raw records per warp in shared memory, filled
+//     with cp.async several stages ahead (the loads in flight cost no registers), and
+//     dequantise each 32-key stage (2 keys a warp) into one of 3 bf16 B tiles (N = 32 x
+//     K = 512, K-major, 128-byte swizzle).
 //   * one warp, once all producers have filled a stage, issues its 32 tcgen05.mma
-//     (kind::f16, K = 16 each) into that stage's 32 columns of one of two 256-column TMEM
-//     accumulators and commits them to the stage's mbarrier (the stage may then be
-//     refilled); after an item's last stage it commits the accumulator.
-//   * after producing an item the producers drain the accumulator of the item before (the
-//     tensor cores are then on the new item, in the other accumulator): each reads a slice
-//     of 32 lanes x 128 columns (tcgen05.ld), masks the entries that are not records (a
-//     ballot over the indices) and streams the fp32 logits.
+//     (kind::f16, K = 16 each, A from tensor memory) into that stage's 32 columns of one
+//     of two 128-column accumulators and commits them to the stage's mbarrier (the stage
+//     may then be refilled); after an item's last stage it commits the accumulator.
+//   * the 4 epilogue warps, one per quarter of the tensor-memory lanes (heads), drain
+//     each item's accumulator while the next item is multiplied into the other one: 32
+//     columns (entries) at a time through a padded shared-memory tile, so that every
+//     store writes a whole 128-byte line of a head's row of logits (entries that are not
+//     records: -inf).
 // Every wait on an mbarrier is bounded (20 ms of %globaltimer): past it the CTA sets
 // GKR_ERR_TIMEOUT, stops waiting, still frees its tensor memory and returns.
-#include <type_traits>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
-#include "decode.cuh"
 #include "device.cuh"
 #include "launch.h"
 
@@ -40,40 +43,59 @@ namespace gkr {
 namespace {
 
 constexpr int kM = 128;                  // heads per tile (MMA rows)
-constexpr int kN = 32;                   // keys per B stage (MMA columns)
-// Per record format: the producers' register ring (while one stage is converted, the
-// record loads of the next ahead - 1 stages are in flight) and, from it, the work item
-// (two turns of the ring: tiles stages of 32 keys).  Three slots for the records a lane
-// holds 8 bytes of per chunk (V4.1, fp8 rows), two where it holds 16-byte pieces (the V4
-// bf16 tail, bf16 rows), the most that fit the 168 registers without spilling.
-template <int kRecord>
-struct Shape {
-    static constexpr int ahead = kRecord == 528 || kRecord == 512 ? 3 : 2;
-    static constexpr int tiles = 2 * ahead;
-    static constexpr int chunk = tiles * kN;                 // keys per work item
-    static constexpr int drain_cols = chunk / (8 / 4);       // accumulator columns a producer
-};                                                           // warp drains
-constexpr int kStages = 3;               // B ring depth
-constexpr int kProducerWarps = 8;        // warps 0..7: gather + dequantise, and drain the
-                                         // accumulator of the item before
-constexpr int kMmaWarp = kProducerWarps; // warp 8: tcgen05.mma issue; allocates and frees
-                                         // TMEM too
-constexpr int kKeysPerWarp = kN / kProducerWarps;           // keys of a stage per producer
-constexpr int kLogitThreads = (kMmaWarp + 1) * 32;          // 9 warps: up to 168 registers
+constexpr int kN = 64;                   // keys per group (MMA columns)
+constexpr int kHalfK = 256;              // dims per B stage: a group's keys, half of K
+constexpr int kStages = 3;               // B ring depth (half-groups)
+constexpr int kChunk = 128;              // keys per work item
+constexpr int kGroups = kChunk / kN;     // groups per item
+constexpr int kTiles = 2 * kGroups;      // B stages per item (low, high half per group)
+constexpr int kProducerWarps = 16;       // warps 0..15: gather + dequantise
+constexpr int kEpilogueWarps = 4;        // warps 16..19: A in, accumulators out (warp w
+                                         // owns tensor-memory lanes 32 (w % 4) .. +31)
+constexpr int kFirstEpilogue = kProducerWarps;
+constexpr int kMmaWarp = kProducerWarps + kEpilogueWarps;   // warp 20: tcgen05.mma issue;
+                                                            // allocates and frees TMEM too
+constexpr int kKeysPerWarp = kN / kProducerWarps;           // keys of a group per producer
+constexpr int kLogitThreads = (kMmaWarp + 1) * 32;          // 21 warps: up to 80 registers
 constexpr int kRowBytes = 128;           // one swizzle row: 64 bf16 of K
-constexpr int kABytes = kM * 1024;       // 128 KB
-constexpr int kBBytes = kN * 1024;       // 32 KB per stage
-constexpr uint32_t kTmemCols = 512;      // two fp32 accumulators of kChunk columns
+constexpr int kBBytes = kN * kHalfK * 2; // 32 KB per stage
+constexpr uint32_t kTmemCols = 512;      // accumulators at columns 0 and 128, A at 256
+constexpr uint32_t kACol = 2 * kChunk;   // A: 512 bf16 a row, two to a column
+constexpr int kTileCols = 32;            // entries per drain step
+constexpr int kTileWarpBytes = 32 * kTileCols * 4;   // an epilogue warp's 32 x 32 fp32 tile
+constexpr int kTileBytes = kEpilogueWarps * kTileWarpBytes;
+constexpr int kWindow = 32 / kKeysPerWarp;  // groups whose indices one register holds
+constexpr int kSmemLimit = 227 * 1024;   // shared memory a CTA may use
 constexpr int32_t kErrIndex = 4;
 constexpr int32_t kErrTimeout = 16;
 constexpr uint64_t kWaitNs = 20000000;    // a wait gives up after 20 ms (a normal one takes us)
 
-static_assert(kProducerWarps == 8, "two producer warps drain each quarter of the lanes");
-static_assert(kKeysPerWarp * Shape<528>::tiles <= 32 && kKeysPerWarp * Shape<584>::tiles <= 32,
-              "a producer lane holds the index of one (tile, key) pair of an item");
-static_assert(2 * Shape<528>::chunk <= static_cast<int>(kTmemCols) &&
-                  Shape<528>::drain_cols % 32 == 0 && Shape<584>::drain_cols % 32 == 0,
-              "two accumulators fit; a producer drains whole 32-column index blocks");
+// A producer warp's ring of raw records: kSlots groups of kKeysPerWarp records, each as
+// the cache holds it (data row, then scale row) at a 16-byte aligned stride; as many
+// groups as the shared memory left by the B stages and the drain tiles holds.
+template <int kRecord>
+struct Raw {
+    static constexpr int stride = kRecord == 584 ? 592 : kRecord;   // 576 data + 8 scale
+    static constexpr int fixed = 1024 + kStages * kBBytes + 1024 + kTileBytes + 256;
+    static constexpr int slots =
+        (kSmemLimit - fixed) / (kProducerWarps * kKeysPerWarp * stride);
+    static constexpr int bytes = kProducerWarps * slots * kKeysPerWarp * stride;
+    // the drain tiles follow the rings, 1024-byte aligned (the TMA's 128-byte swizzle)
+    static constexpr int tile_off = (kStages * kBBytes + bytes + 1023) / 1024 * 1024;
+    static constexpr int smem = 1024 + tile_off + kTileBytes;   // + the barriers
+};
+
+static_assert(kN % kProducerWarps == 0 && kN % 16 == 0 && kN <= 256 && kEpilogueWarps == 4 &&
+                  kFirstEpilogue % 4 == 0,
+              "whole keys per producer; N of an M = 128 product is a multiple of 16; one "
+              "epilogue warp per quarter of the tensor-memory lanes, in order");
+static_assert(kChunk % kN == 0 && kChunk % kTileCols == 0 && 2 * kChunk + 256 <= kTmemCols,
+              "whole groups and drain steps per item; two accumulators and A fit");
+static_assert(Raw<528>::slots >= 3 && Raw<584>::slots >= 3 && Raw<512>::slots >= 3 &&
+                  Raw<1024>::slots >= 1 && Raw<528>::slots * kKeysPerWarp <= 32 &&
+                  Raw<512>::slots * kKeysPerWarp <= 32 && kKeysPerWarp * kWindow == 32,
+              "a ring of at least one group; one validity bit per ring record; whole "
+              "groups per index window");
 
 // ------------------------------------------------------------- tcgen05 / mbarrier PTX
 
@@ -129,13 +151,15 @@ __device__ __forceinline__ void tc_fence_after_sync() {
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulator; one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulator; one thread.  A sits in
+// tensor memory with row i in lane i and its K values two to a 32-bit column (the lower
+// half holds the even k), so the K = 16 of one instruction span 8 columns.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Arrive on the mbarrier once every tcgen05 operation this thread issued has completed.
@@ -144,25 +168,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                      bar)
                  : "memory");
 }
-// 32 consecutive fp32 accumulator columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-        "%28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // 16 consecutive fp32 accumulator columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
@@ -178,6 +183,21 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive 32-bit columns of this thread's lane (tcgen05.wait::st before handing
+// them to the tensor cores).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint4 (&v)[4]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y),
+        "r"(v[1].z), "r"(v[1].w), "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w),
+        "r"(v[3].x), "r"(v[3].y), "r"(v[3].z), "r"(v[3].w)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A and B
 // (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at
 // bits 24-28.
@@ -185,7 +205,7 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             (static_cast<uint32_t>(kN >> 3) << 17) |
                             (static_cast<uint32_t>(kM >> 4) << 24);
 
-// Shared-memory matrix descriptor of a K-major operand with the 128-byte swizzle: start
+// Shared-memory matrix descriptor of the K-major B operand with the 128-byte swizzle: start
 // address >> 4 (bits 0-13), leading offset (unused by this layout; 1) at bits 16-29,
 // stride between 8-row groups (1024 bytes) >> 4 at bits 32-45, descriptor version 1 at
 // bits 46-47, swizzle mode 128B (2) at bits 61-63.  The operand's rows are 128 bytes (64
@@ -204,22 +224,20 @@ __device__ __forceinline__ uint32_t sw128_offset(int rows, int r, int kb, int c)
                                  ((c ^ (r & 7)) << 4));
 }
 
-// Lane L's two pieces of a 512-dim row (dims [8L, 8L+8) and [256+8L, 256+8L+8)) into
-// row r of a swizzled operand of `rows` rows.
-__device__ __forceinline__ void store_row_pieces(uint8_t* op, int rows, int r, int lane, uint4 a,
-                                                 uint4 b) {
-    *reinterpret_cast<uint4*>(op + sw128_offset(rows, r, lane >> 3, lane & 7)) = a;
-    *reinterpret_cast<uint4*>(op + sw128_offset(rows, r, 4 + (lane >> 3), lane & 7)) = b;
+// Lane L's piece of half h of a 512-dim row (dims [256h + 8L, 256h + 8L + 8)) into row r of
+// a swizzled half-K operand of kN rows: K block L / 8 (of 64 dims), 16-byte piece L % 8.
+__device__ __forceinline__ void store_piece(uint8_t* op, int r, int lane, uint4 v) {
+    *reinterpret_cast<uint4*>(op + sw128_offset(kN, r, lane >> 3, lane & 7)) = v;
 }
 
-// One work item = (query, chunk of kChunk keys).  A CTA (one per SM) takes a contiguous
-// run of items in query-major order, so it reloads the query tile A only when its run
-// moves to the next query.
+// A CTA (one per SM) takes a contiguous run of work items (query, chunk of kChunk keys)
+// in query-major order, so A changes only when its run moves to the next query.
 struct alignas(8) Barriers {
-    uint64_t full[kStages];      // producers -> MMA: B stage holds its 32 keys
+    uint64_t full[kStages];      // producers -> MMA: B stage holds its half-group
     uint64_t empty[kStages];     // MMA -> producers: the stage's products are done
-    uint64_t acc_full[2];        // MMA -> producers: an item's accumulator is complete
-    uint64_t acc_empty[2];       // producers -> MMA: the accumulator has been read
+    uint64_t acc_full[2];        // MMA -> epilogue: an item's accumulator is complete
+    uint64_t acc_empty[2];       // epilogue -> MMA: the accumulator has been read
+    uint64_t a_ready;            // epilogue -> MMA: A holds the next query
     uint32_t tmem_base;
     int32_t timed_out;
 };
@@ -252,16 +270,53 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
     if (lane == 0) mbar_arrive(bar);
 }
 
-// Decode key k of query row idx_row into the record's byte offsets (off = -1: not a
-// record: past topk, index -1, out of range (bad = 1), or a bad fp8 scale).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// TMA store (async proxy) of a 32 x 32 fp32 box from shared memory to the logits at
+// (entry x, head y, query z), in this thread's bulk group; entries past topk and heads past
+// num_heads are not written.  The tile holds row r (head y + r) at r * 128 bytes, its
+// 16-byte piece c at position c ^ (r % 8) (the map's 128-byte swizzle).
+__device__ __forceinline__ void tma_store_tile(const CUtensorMap* map, const void* tile, int32_t x,
+                                               int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(smem_addr(tile))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until none of this thread's bulk groups still reads its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until all of this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared16(void* p, float4 v) {
+    *reinterpret_cast<float4*>(p) = v;
+}
+// Four logits: sm_scale * accumulator for a record (bit i of recs), -inf otherwise.
+__device__ __forceinline__ float4 logit4(const float* v, uint32_t recs, float sm_scale) {
+    return make_float4(recs & 1u ? __fmul_rn(v[0], sm_scale) : -INFINITY,
+                       recs & 2u ? __fmul_rn(v[1], sm_scale) : -INFINITY,
+                       recs & 4u ? __fmul_rn(v[2], sm_scale) : -INFINITY,
+                       recs & 8u ? __fmul_rn(v[3], sm_scale) : -INFINITY);
+}
+
+// Decode index idx into the record's byte offsets (off = -1: not a record -- index -1,
+// out of range (bad = 1), or a bad fp8 scale).
 template <int kRecord>
-__device__ __forceinline__ void key_offsets(const LogitsParams& p, int32_t idx, bool in_range,
-                                            bool scale_bad, int64_t& off, int64_t& soff,
-                                            uint32_t& bad) {
+__device__ __forceinline__ void key_offsets(const LogitsParams& p, int32_t idx, bool scale_bad,
+                                            int64_t& off, int64_t& soff, uint32_t& bad) {
     using R = Fmt<kRecord>;
     off = -1;
     soff = 0;
-    if (!in_range || scale_bad) return;
+    if (scale_bad) return;
     if (idx >= 0 && idx < p.num_slots) {
         const uint32_t s = static_cast<uint32_t>(idx);
         const uint32_t bs = static_cast<uint32_t>(p.block_size);
@@ -274,19 +329,83 @@ __device__ __forceinline__ void key_offsets(const LogitsParams& p, int32_t idx, 
     }
 }
 
+// One record's cp.async copies into its ring place, spread over the warp (data rows and
+// V4.1 scale rows are 16-byte aligned in every valid cache, V4 scale rows 8-byte).
 template <int kRecord>
-__global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const LogitsParams p) {
-    constexpr int kAhead = Shape<kRecord>::ahead;
-    constexpr int kTiles = Shape<kRecord>::tiles;
-    constexpr int kChunk = Shape<kRecord>::chunk;
-    constexpr int kDrainCols = Shape<kRecord>::drain_cols;
+__device__ __forceinline__ void copy_record(uint8_t* dst, const uint8_t* cache, int64_t off,
+                                            int64_t soff, int lane) {
+    cp_async16(dst + 16 * lane, cache + off + 16 * lane);
+    if constexpr (kRecord == 1024) cp_async16(dst + 512 + 16 * lane, cache + off + 512 + 16 * lane);
+    if constexpr (kRecord == 528) {
+        if (lane == 0) cp_async16(dst + 512, cache + soff);
+    }
+    if constexpr (kRecord == 584) {
+        if (lane < 4) cp_async16(dst + 512 + 16 * lane, cache + off + 512 + 16 * lane);
+        if (lane == 0) cp_async8(dst + 576, cache + soff);
+    }
+}
+
+// Lane L's piece of half h of a ring record, dequantised to bf16 exactly as kv_gather
+// does (zeros for an invalid record): dims [256h + 8L, 256h + 8L + 8), from the e4m3 codes
+// and the scale byte of their 32-dim (V4.1) or 64-dim (V4) group; the V4 rotated tail
+// (dims 448..511, lanes 24..31 of the high half) and bf16 rows are copied.
+template <int kRecord>
+__device__ __forceinline__ uint4 convert_half(const uint8_t* src, bool valid, int lane, int h,
+                                              float scale) {
+    if (!valid) return make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (kRecord == 1024) {
+        return lds16(src + 512 * h + 16 * lane);
+    } else if constexpr (kRecord == 512) {
+        return dequant8_scaled(lds8(src + 256 * h + 8 * lane), scale);
+    } else if constexpr (kRecord == 528) {
+        return dequant8(lds8(src + 256 * h + 8 * lane), src[512 + 8 * h + (lane >> 2)]);
+    } else {   // 584: data 0..575 (bf16 tail at 448), scale bytes at 576
+        if (h == 1 && lane >= 24) return lds16(src + 448 + 16 * (lane - 24));
+        return dequant8(lds8(src + 256 * h + 8 * lane), src[576 + 4 * h + (lane >> 3)]);
+    }
+}
+
+// The epilogue warp's quarter of A: lane L writes row h0 + L = head h0 + L of query qi
+// (zeros past num_heads) into tensor memory at `dst` (its lanes, A's first column), 16
+// columns (32 bf16) a step, the next step's loads in flight during each store; then it
+// makes the stores visible to the tensor cores and arrives on `ready`.  Kept out of line:
+// its registers would otherwise add to the drain loop's.
+__device__ __noinline__ void load_a(const uint8_t* qbase, int64_t qi, int32_t num_heads, int h0,
+                                    int lane, bool live, uint32_t dst, uint32_t ready) {
+    const uint4* const row =
+        reinterpret_cast<const uint4*>(qbase + (qi * num_heads + h0 + lane) * 1024);
+    uint4 cur[4], nxt[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cur[i] = live ? __ldg(row + i) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+        if (b < 15) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                nxt[i] = live ? __ldg(row + 4 * (b + 1) + i) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        tmem_st16(dst + 16 * b, cur);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+    }
+    tmem_st_wait();
+    tc_fence_before_sync();
+    warp_arrive(ready, lane);
+}
+
+template <int kRecord>
+__global__ void __launch_bounds__(kLogitThreads, 1)
+    sparse_logits_kernel(const LogitsParams p, const __grid_constant__ CUtensorMap out_map) {
+    using RawRing = Raw<kRecord>;
+    constexpr int kSlots = RawRing::slots;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the swizzle groups
     uint8_t* const base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* const sA = base;
-    uint8_t* const sB = base + kABytes;                               // kStages buffers
-    Barriers* const bars = reinterpret_cast<Barriers*>(sB + kStages * kBBytes);
+    uint8_t* const sB = base;                                   // kStages B stages
+    uint8_t* const sRaw = sB + kStages * kBBytes;               // the producers' rings
+    uint8_t* const sTile = base + RawRing::tile_off;            // drain tiles
+    Barriers* const bars = reinterpret_cast<Barriers*>(sTile + kTileBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -305,8 +424,9 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_addr(&bars->acc_full[a]), 1);
-            mbar_init(smem_addr(&bars->acc_empty[a]), kProducerWarps);
+            mbar_init(smem_addr(&bars->acc_empty[a]), kEpilogueWarps);
         }
+        mbar_init(smem_addr(&bars->a_ready), kEpilogueWarps);
         bars->timed_out = 0;
         mbar_init_fence();
     }
@@ -328,195 +448,185 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
             scale_bad = !scale_ok(scale);
             if (scale_bad && pw == 0 && lane == 0 && i0 < i1) report(p.err, kErrScale);
         }
-        LaneBases lb;
-        lb.a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
-        lb.tail = p.cache + 448 + 16 * (lane >= 24 ? lane - 24 : 0);
-        lb.s = p.cache + (kRecord == 528 ? (lane >> 2) : (lane >> 3));
+        uint8_t* const ring = sRaw + pw * kSlots * kKeysPerWarp * RawRing::stride;
+        const uint32_t groups = static_cast<uint32_t>(i1 - i0) * kGroups;
         uint32_t bad = 0;
-        // lane L < kTiles * kKeysPerWarp holds the index of this warp's key
-        // (L / kKeysPerWarp, L % kKeysPerWarp) = tile L / kKeysPerWarp, key
-        // kKeysPerWarp * pw + L % kKeysPerWarp of an item
-        auto load_indices = [&](int64_t item, int32_t& idx, bool& in_range) {
-            idx = -1;
-            in_range = false;
-            if (item >= i1 || lane >= kTiles * kKeysPerWarp) return;
+        // The CTA's groups g = 0, 1, ... (item i0 + g / kGroups, keys (g % kGroups) * kN ..
+        // of its chunk); this warp's keys of a group are kKeysPerWarp * pw + i.  Lane L of
+        // window w holds the index of key i = L % kKeysPerWarp of group
+        // w * kWindow + L / kKeysPerWarp (-1 past the CTA's groups or past topk).
+        auto window = [&](uint32_t w) -> int32_t {
+            const uint32_t g = w * kWindow + lane / kKeysPerWarp;
+            if (g >= groups) return -1;
+            const int64_t item = i0 + g / kGroups;
             const int64_t qi = item / p.chunks;
-            const int64_t k = (item % p.chunks) * kChunk + (lane / kKeysPerWarp) * kN +
-                              kKeysPerWarp * pw + (lane % kKeysPerWarp);
-            in_range = k < p.topk;
-            if (in_range) idx = __ldg(p.indices + qi * p.topk + k);
+            const int64_t k = (item % p.chunks) * kChunk + (g % kGroups) * kN +
+                              kKeysPerWarp * pw + lane % kKeysPerWarp;
+            return k < p.topk ? __ldg(p.indices + qi * p.topk + k) : -1;
         };
-        // the records of tile t of an item whose indices are in idx_all
-        auto load_tile = [&](int t, int32_t idx_all, bool rng_all, Loaded<kRecord> (&r)[kKeysPerWarp]) {
+        int32_t win_cur = window(0), win_nxt = window(1);
+        uint32_t vmask = 0;   // bit slot * kKeysPerWarp + i: that ring record is valid
+        // start the copies of group g into ring slot g % kSlots (groups are issued in order)
+        auto issue = [&](uint32_t g) {
+            if (g >= groups) return;
+            if (g % kWindow == 0 && g > 0) {
+                win_cur = win_nxt;
+                win_nxt = window(g / kWindow + 1);
+            }
+            const int slot = static_cast<int>(g % kSlots);
 #pragma unroll
             for (int i = 0; i < kKeysPerWarp; ++i) {
-                const int src = t * kKeysPerWarp + i;
-                const int32_t idx = __shfl_sync(kFull, idx_all, src);
-                const bool rg = __shfl_sync(kFull, rng_all ? 1 : 0, src) != 0;
+                const int32_t idx =
+                    __shfl_sync(kFull, win_cur, static_cast<int>(g % kWindow) * kKeysPerWarp + i);
                 int64_t off, soff;
-                key_offsets<kRecord>(p, idx, rg, scale_bad, off, soff, bad);
-                load_record<kRecord>(off, soff, lb, lane, r[i]);
+                key_offsets<kRecord>(p, idx, scale_bad, off, soff, bad);
+                const uint32_t bit = 1u << (slot * kKeysPerWarp + i);
+                vmask = off >= 0 ? (vmask | bit) : (vmask & ~bit);
+                if (off >= 0)
+                    copy_record<kRecord>(ring + (slot * kKeysPerWarp + i) * RawRing::stride,
+                                         p.cache, off, soff, lane);
             }
         };
-        // idx_cur: the indices of the item being converted; idx_nxt: of the next one
-        int32_t idx_cur, idx_nxt;
-        bool rng_cur, rng_nxt;
-        load_indices(i0, idx_cur, rng_cur);
-        load_indices(i0 + 1, idx_nxt, rng_nxt);
-        // register ring over the CTA's stages g = 0, 1, ...: stage g (item g / kTiles, tile
-        // g % kTiles) lives in slot g % kAhead; while it is converted the loads of stages
-        // g + 1 .. g + kAhead - 1 (of this item or the next) are in flight
-        Loaded<kRecord> ring[kAhead][kKeysPerWarp];
-#pragma unroll
-        for (int t = 0; t < kAhead - 1; ++t) load_tile(t, idx_cur, rng_cur, ring[t]);
-        const uint32_t stages = static_cast<uint32_t>(i1 - i0) * kTiles;
-        int64_t cur_q = -1;
-        // Read this warp's slice of item v's accumulator -- lanes 32 (pw % 4) .. +31 (heads),
-        // columns (pw / 4) * kDrainCols .. +kDrainCols-1 (entries) -- and write the logits;
-        // which entries are records comes from the indices (lane l reads the index of
-        // column c + l of each 32-column block, a ballot gives the block's mask).
-        auto drain = [&](int64_t v) {
-            const int a = static_cast<int>(v & 1);
-            const int64_t item = i0 + v;
-            const int64_t qi = item / p.chunks;
-            const int col0 = (pw >> 2) * kDrainCols;
-            const int64_t k0 = (item % p.chunks) * kChunk + col0;
-            int32_t idx[kDrainCols / 32];
-#pragma unroll
-            for (int c = 0; c < kDrainCols / 32; ++c) {
-                const int64_t k = k0 + 32 * c + lane;
-                idx[c] = k < p.topk ? __ldg(p.indices + qi * p.topk + k) : -1;
-            }
-            warp_wait_or_flag(smem_addr(&bars->acc_full[a]), (v >> 1) & 1, ok, lane);
-            tc_fence_after_sync();
-            const int h = 32 * (pw & 3) + lane;
-            float* const orow = p.out + (qi * p.num_heads + h) * p.topk + k0;
 #pragma unroll 1
-            for (int c = 0; c < kDrainCols / 16; ++c) {   // 16 columns at a time
-                const uint32_t mask =
-                    __ballot_sync(kFull, !scale_bad && idx[c >> 1] >= 0 && idx[c >> 1] < p.num_slots) >>
-                    (16 * (c & 1));
-                float val[16];
-                tmem_ld16(tmem + (static_cast<uint32_t>(32 * (pw & 3)) << 16) + a * kChunk + col0 +
-                              16 * c,
-                          val);
-                if (h < p.num_heads && ok) {
-#pragma unroll
-                    for (int jj = 0; jj < 16; jj += 4) {
-                        if (k0 + 16 * c + jj >= p.topk) break;   // topk is a multiple of 4
-                        float4 o;
-                        o.x = (mask >> jj) & 1u ? __fmul_rn(val[jj], p.sm_scale) : -INFINITY;
-                        o.y = (mask >> (jj + 1)) & 1u ? __fmul_rn(val[jj + 1], p.sm_scale) : -INFINITY;
-                        o.z = (mask >> (jj + 2)) & 1u ? __fmul_rn(val[jj + 2], p.sm_scale) : -INFINITY;
-                        o.w = (mask >> (jj + 3)) & 1u ? __fmul_rn(val[jj + 3], p.sm_scale) : -INFINITY;
-                        __stcs(reinterpret_cast<float4*>(orow + 16 * c + jj), o);
-                    }
-                }
-            }
-            tc_fence_before_sync();
-            warp_arrive(smem_addr(&bars->acc_empty[a]), lane);
-        };
-        // one stage: slot R of the ring (static), stage number g
-        auto stage = [&](auto slot_c, uint32_t g) {
-            constexpr int R = decltype(slot_c)::value;
-            const int t = static_cast<int>(g % kTiles);
-            const int64_t u = g / kTiles;
-            const int64_t item = i0 + u;
-            if (t == 0) {
-                if (u > 0) {              // the next item's indices become current
-                    idx_cur = idx_nxt;
-                    rng_cur = rng_nxt;
-                    load_indices(item + 1, idx_nxt, rng_nxt);
-                }
-                const int64_t qi = item / p.chunks;
-                if (qi != cur_q) {
-                    // the query tile changes: every product that read the old one must be
-                    // done; then all of its rows' copies in flight at once (cp.async into
-                    // the swizzled places), one wait; rows past num_heads are zero
-                    if (u > 0)
-                        warp_wait_or_flag(smem_addr(&bars->acc_full[(u - 1) & 1]),
-                                          ((u - 1) >> 1) & 1, ok, lane);
-                    const uint8_t* const qrow =
-                        static_cast<const uint8_t*>(p.q) + qi * p.num_heads * 1024;
-                    for (int h = pw; h < kM; h += kProducerWarps) {
-                        if (h < p.num_heads) {
-                            cp_async16(sA + sw128_offset(kM, h, lane >> 3, lane & 7),
-                                       qrow + h * 1024 + 16 * lane);
-                            cp_async16(sA + sw128_offset(kM, h, 4 + (lane >> 3), lane & 7),
-                                       qrow + h * 1024 + 512 + 16 * lane);
-                        } else {
-                            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                            store_row_pieces(sA, kM, h, lane, z, z);
-                        }
-                    }
-                    cp_async_commit();
-                    cp_async_wait<0>();
-                    cur_q = qi;
-                }
-            }
-            // start the loads of stage g + kAhead - 1
-            {
-                constexpr int RP = (R + kAhead - 1) % kAhead;
-                const uint32_t gp = g + kAhead - 1;
-                if (gp < stages) {
-                    const int tp = static_cast<int>(gp % kTiles);
-                    if (gp / kTiles == static_cast<uint32_t>(u)) load_tile(tp, idx_cur, rng_cur, ring[RP]);
-                    else load_tile(tp, idx_nxt, rng_nxt, ring[RP]);
-                }
-            }
-            const int s = static_cast<int>(g % kStages);
-            if (g >= kStages)
-                warp_wait_or_flag(smem_addr(&bars->empty[s]), ((g / kStages) - 1) & 1, ok, lane);
-            uint8_t* const B = sB + s * kBBytes;
-#pragma unroll
-            for (int i = 0; i < kKeysPerWarp; ++i) {
-                uint4 oa, ob;
-                convert<kRecord>(ring[R][i], lane, scale, oa, ob);
-                store_row_pieces(B, kN, kKeysPerWarp * pw + i, lane, oa, ob);
-            }
-            fence_async_smem();
-            warp_arrive(smem_addr(&bars->full[s]), lane);
-        };
-        for (uint32_t g = 0; g < stages; g += kTiles) {    // one item; kTiles = 2 * kAhead
-#pragma unroll 1
-            for (uint32_t h = 0; h < kTiles; h += kAhead) {
-                stage(std::integral_constant<int, 0>{}, g + h);
-                stage(std::integral_constant<int, 1>{}, g + h + 1);
-                if constexpr (kAhead > 2) stage(std::integral_constant<int, 2>{}, g + h + 2);
-            }
-            // then drain the item before (the tensor cores are on this item's stages, in the
-            // other accumulator)
-            if (g > 0) drain(g / kTiles - 1);
+        for (int t = 0; t < kSlots - 1; ++t) {
+            issue(static_cast<uint32_t>(t));
+            cp_async_commit();
         }
-        if (i1 > i0) drain(i1 - i0 - 1);
+#pragma unroll 1
+        for (uint32_t g = 0; g < groups; ++g) {
+            __syncwarp();                  // every lane has read slot (g - 1) % kSlots
+            issue(g + kSlots - 1);         // ... which now takes group g + kSlots - 1
+            cp_async_commit();
+            cp_async_wait<kSlots - 1>();   // this lane's copies of group g have landed
+            __syncwarp();                  // ... and every lane's
+            const uint8_t* const grp = ring + static_cast<int>(g % kSlots) * kKeysPerWarp *
+                                                  RawRing::stride;
+            const uint32_t valid = vmask >> (static_cast<int>(g % kSlots) * kKeysPerWarp);
+            // the group's low half (dims 0..255), then its high half, each into a B stage
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t j = 2 * g + h;
+                const int s = static_cast<int>(j % kStages);
+                if (j >= kStages)
+                    warp_wait_or_flag(smem_addr(&bars->empty[s]), ((j / kStages) - 1) & 1, ok,
+                                      lane);
+                uint8_t* const B = sB + s * kBBytes;
+#pragma unroll
+                for (int i = 0; i < kKeysPerWarp; ++i)
+                    store_piece(B, kKeysPerWarp * pw + i, lane,
+                                convert_half<kRecord>(grp + i * RawRing::stride,
+                                                      ((valid >> i) & 1u) != 0u, lane, h, scale));
+                fence_async_smem();
+                warp_arrive(smem_addr(&bars->full[s]), lane);
+            }
+        }
+        cp_async_wait<0>();
         if (__any_sync(kFull, bad != 0u) && lane == 0) report(p.err, kErrIndex);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------- MMA issue
         if (lane == 0) {
-            uint32_t j = 0;
+            uint32_t j = 0, loads = 0;
+            int64_t cur_q = -1;
             for (int64_t item = i0; item < i1; ++item) {
                 const int64_t u = item - i0;
                 const int a = static_cast<int>(u & 1);
                 if (u >= 2) wait_or_flag(smem_addr(&bars->acc_empty[a]), ((u >> 1) - 1) & 1, ok);
+                const int64_t qi = item / p.chunks;
+                if (qi != cur_q) {   // A is rewritten for each new query of the run
+                    wait_or_flag(smem_addr(&bars->a_ready), loads & 1, ok);
+                    ++loads;
+                    cur_q = qi;
+                }
                 tc_fence_after_sync();
-                const uint32_t d0 = tmem + a * kChunk;
                 for (int t = 0; t < kTiles; ++t, ++j) {
                     const int s = static_cast<int>(j % kStages);
+                    const int h = t & 1;   // half of K: the group's products accumulate both
                     wait_or_flag(smem_addr(&bars->full[s]), (j / kStages) & 1, ok);
                     tc_fence_after_sync();
-                    const uint32_t a0 = smem_addr(sA), b0 = smem_addr(sB + s * kBBytes);
+                    const uint32_t d = tmem + a * kChunk + (t >> 1) * kN;
+                    const uint32_t b0 = smem_addr(sB + s * kBBytes);
 #pragma unroll
-                    for (int k = 0; k < 512 / 16; ++k) {   // K = 16 per instruction
-                        const uint32_t koff = (k & 3) * 32;
-                        mma_bf16(d0 + t * kN, sw128_desc(a0 + (k >> 2) * kM * kRowBytes + koff),
-                                 sw128_desc(b0 + (k >> 2) * kN * kRowBytes + koff), kIdesc,
-                                 k > 0 ? 1u : 0u);
-                    }
+                    for (int k = 0; k < kHalfK / 16; ++k)   // K = 16 per instruction
+                        mma_bf16_ts(d, tmem + kACol + (kHalfK / 2) * h + 8 * k,
+                                    sw128_desc(b0 + (k >> 2) * kN * kRowBytes + (k & 3) * 32),
+                                    kIdesc, (h | k) != 0 ? 1u : 0u);
                     mma_commit(smem_addr(&bars->empty[s]));
                 }
                 mma_commit(smem_addr(&bars->acc_full[a]));
             }
         }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------- epilogue
+        // Warp w owns tensor-memory lanes h0 .. h0 + 31, h0 = 32 (w % 4): the heads it
+        // writes into A and whose accumulator rows it drains, 32 columns (entries) at a
+        // time: each lane puts its head's 32 logits into the warp's swizzled tile and one
+        // lane hands the tile to the TMA (entries that are not records: -inf).
+        const int h0 = 32 * (warp & 3);
+        const uint32_t lanes = static_cast<uint32_t>(h0) << 16;
+        uint8_t* const tile = sTile + (warp - kFirstEpilogue) * kTileWarpBytes;
+        uint8_t* const trow = tile + lane * 128;   // this lane's row
+        bool scale_bad = false;
+        if constexpr (kRecord == 512) scale_bad = !scale_ok(__ldg(p.fp8_scale));
+        const uint8_t* const qbase = static_cast<const uint8_t*>(p.q);
+        const bool live = h0 + lane < p.num_heads;   // this lane's head exists
+        const bool stores = h0 < p.num_heads;        // this warp has heads to store
+        const uint32_t a_ready = smem_addr(&bars->a_ready);
+        const uint32_t a_dst = tmem + lanes + kACol;
+        if (i0 < i1) load_a(qbase, i0 / p.chunks, p.num_heads, h0, lane, live, a_dst, a_ready);
+        for (int64_t item = i0; item < i1; ++item) {
+            const int64_t v = item - i0;
+            const int a = static_cast<int>(v & 1);
+            const int64_t qi = item / p.chunks;
+            const int64_t k0 = (item % p.chunks) * kChunk;
+            const bool next_query = item + 1 < i1 && (item + 1) / p.chunks != qi;
+            if (next_query && live) {   // warm L2 with the next query's rows
+                const uint8_t* const nrow = qbase + ((qi + 1) * p.num_heads + h0 + lane) * 1024;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) prefetch_l2(nrow + 128 * i);
+            }
+            // the item's indices (lane L: entries k0 + L, k0 + 32 + L, ...), read before the
+            // wait so that no drain step waits on a load
+            int32_t idx[kChunk / kTileCols];
+#pragma unroll
+            for (int c = 0; c < kChunk / kTileCols; ++c) {
+                const int64_t k = k0 + c * kTileCols + lane;
+                idx[c] = k < p.topk ? __ldg(p.indices + qi * p.topk + k) : -1;
+            }
+            warp_wait_or_flag(smem_addr(&bars->acc_full[a]), (v >> 1) & 1, ok, lane);
+            tc_fence_after_sync();
+            // every product of this item is done, so A may take the next query now
+            if (next_query) load_a(qbase, qi + 1, p.num_heads, h0, lane, live, a_dst, a_ready);
+#pragma unroll 1
+            for (int c = 0; c < kChunk; c += kTileCols) {
+                // bit j: entry k0 + c + j is a record (lane j read its index)
+                const uint32_t recs =
+                    __ballot_sync(kFull, !scale_bad && idx[0] >= 0 && idx[0] < p.num_slots);
+#pragma unroll
+                for (int i = 0; i + 1 < kChunk / kTileCols; ++i) idx[i] = idx[i + 1];
+                float v0[16], v1[16];
+                tmem_ld16(tmem + lanes + a * kChunk + c, v0);
+                tmem_ld16(tmem + lanes + a * kChunk + c + 16, v1);
+                if (lane == 0) bulk_wait_read_all();   // the last store has read the tile
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    st_shared16(trow + ((j ^ (lane & 7)) << 4), logit4(v0 + 4 * j, recs >> (4 * j), p.sm_scale));
+                    st_shared16(trow + (((4 + j) ^ (lane & 7)) << 4),
+                                logit4(v1 + 4 * j, recs >> (16 + 4 * j), p.sm_scale));
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0 && ok && stores) {
+                    tma_store_tile(&out_map, tile, static_cast<int32_t>(k0 + c), h0,
+                                   static_cast<int32_t>(qi));
+                    bulk_commit();
+                }
+            }
+            tc_fence_before_sync();
+            warp_arrive(smem_addr(&bars->acc_empty[a]), lane);
+        }
+        if (lane == 0) bulk_wait_all();   // every logits store has completed
         __syncwarp();
     }
     if (!ok) atomicOr(&bars->timed_out, 1);
@@ -526,25 +636,61 @@ __global__ void __launch_bounds__(kLogitThreads, 1) sparse_logits_kernel(const L
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to the driver
+// library); null when the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// The logits [num_queries, num_heads, topk] fp32 as a 3-D tensor map with 32 x 32 x 1 boxes
+// and the 128-byte swizzle (topk % 4 == 0 and a 16-byte aligned base make the strides legal).
+cudaError_t out_tensor_map(const LogitsParams& p, CUtensorMap* map) {
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.topk),
+                                static_cast<cuuint64_t>(p.num_heads),
+                                static_cast<cuuint64_t>(p.num_queries)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.topk) * 4,
+                                   static_cast<cuuint64_t>(p.topk) * 4 * p.num_heads};
+    const cuuint32_t box[3] = {kTileCols, 32, 1};
+    const cuuint32_t step[3] = {1, 1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.out, dims, strides, box,
+                              step, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int kRecord>
 cudaError_t launch(const LogitsParams& p, cudaStream_t stream) {
-    const size_t smem = kABytes + kStages * kBBytes + 1024 + sizeof(Barriers);
+    const size_t smem = Raw<kRecord>::smem + sizeof(Barriers);
+    static_assert(Raw<kRecord>::smem + sizeof(Barriers) <= kSmemLimit,
+                  "the CTA's shared memory fits");
+    CUtensorMap map;
+    cudaError_t e = out_tensor_map(p, &map);
+    if (e != cudaSuccess) return e;
     int64_t warps = 0;   // raises the kernel's dynamic shared-memory limit (once per device)
-    cudaError_t e = resident_warps(reinterpret_cast<const void*>(sparse_logits_kernel<kRecord>),
-                                   kLogitThreads, smem, &warps);
+    e = resident_warps(reinterpret_cast<const void*>(sparse_logits_kernel<kRecord>), kLogitThreads,
+                       smem, &warps);
     if (e != cudaSuccess) return e;
     const int64_t ctas = warps / (kLogitThreads / 32);        // one CTA per SM
     const int64_t items = p.num_queries * p.chunks;
     const int64_t blocks = items < ctas ? items : ctas;
     return launch_kernel(sparse_logits_kernel<kRecord>, blocks, kLogitThreads, smem, stream, p.pdl,
-                         p);
+                         p, map);
 }
 
 }  // namespace
 
-int32_t logits_chunk_keys(int32_t record) {
-    return record == 528 || record == 512 ? Shape<528>::chunk : Shape<584>::chunk;
-}
+int32_t logits_chunk_keys(int32_t) { return kChunk; }
 int32_t logits_max_heads() { return kM; }
 
 cudaError_t launch_sparse_logits(int32_t record, const LogitsParams& p, cudaStream_t stream) {
