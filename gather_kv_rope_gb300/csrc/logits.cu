@@ -273,6 +273,10 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
+// Prefetch `bytes` (a multiple of 16) from a 16-byte aligned address into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 
 // TMA store (async proxy) of a 32 x 32 fp32 box from shared memory to the logits at
 // (entry x, head y, query z), in this thread's bulk group; entries past topk and heads past
@@ -432,6 +436,11 @@ __global__ void __launch_bounds__(kLogitThreads, 1)
     }
     pdl_wait_previous();   // q, the cache and the indices may come from the kernel ahead
     pdl_release_next();
+    if (threadIdx.x == 0 && i0 < i1) {   // the run's query tiles into L2 for the A loads
+        for (int64_t qi = i0 / p.chunks; qi <= (i1 - 1) / p.chunks; ++qi)
+            prefetch_l2_bulk(static_cast<const uint8_t*>(p.q) + qi * p.num_heads * 1024,
+                             static_cast<uint32_t>(p.num_heads) * 1024);
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -453,18 +462,26 @@ __global__ void __launch_bounds__(kLogitThreads, 1)
         uint32_t bad = 0;
         // The CTA's groups g = 0, 1, ... (item i0 + g / kGroups, keys (g % kGroups) * kN ..
         // of its chunk); this warp's keys of a group are kKeysPerWarp * pw + i.  Lane L of
-        // window w holds the index of key i = L % kKeysPerWarp of group
-        // w * kWindow + L / kKeysPerWarp (-1 past the CTA's groups or past topk).
-        auto window = [&](uint32_t w) -> int32_t {
+        // window w decodes key i = L % kKeysPerWarp of group w * kWindow + L / kKeysPerWarp
+        // into its record's offsets (off = -1: not a record -- past the CTA's groups, past
+        // topk, index -1 or out of range, or a bad fp8 scale).
+        struct Window {
+            int64_t off, soff;
+        };
+        auto window = [&](uint32_t w) -> Window {
+            Window r{-1, 0};
             const uint32_t g = w * kWindow + lane / kKeysPerWarp;
-            if (g >= groups) return -1;
+            if (g >= groups) return r;
             const int64_t item = i0 + g / kGroups;
             const int64_t qi = item / p.chunks;
             const int64_t k = (item % p.chunks) * kChunk + (g % kGroups) * kN +
                               kKeysPerWarp * pw + lane % kKeysPerWarp;
-            return k < p.topk ? __ldg(p.indices + qi * p.topk + k) : -1;
+            if (k < p.topk)
+                key_offsets<kRecord>(p, __ldg(p.indices + qi * p.topk + k), scale_bad, r.off,
+                                     r.soff, bad);
+            return r;
         };
-        int32_t win_cur = window(0), win_nxt = window(1);
+        Window win_cur = window(0), win_nxt = window(1);
         uint32_t vmask = 0;   // bit slot * kKeysPerWarp + i: that ring record is valid
         // start the copies of group g into ring slot g % kSlots (groups are issued in order)
         auto issue = [&](uint32_t g) {
@@ -476,10 +493,9 @@ __global__ void __launch_bounds__(kLogitThreads, 1)
             const int slot = static_cast<int>(g % kSlots);
 #pragma unroll
             for (int i = 0; i < kKeysPerWarp; ++i) {
-                const int32_t idx =
-                    __shfl_sync(kFull, win_cur, static_cast<int>(g % kWindow) * kKeysPerWarp + i);
-                int64_t off, soff;
-                key_offsets<kRecord>(p, idx, scale_bad, off, soff, bad);
+                const int src = static_cast<int>(g % kWindow) * kKeysPerWarp + i;
+                const int64_t off = __shfl_sync(kFull, win_cur.off, src);
+                const int64_t soff = __shfl_sync(kFull, win_cur.soff, src);
                 const uint32_t bit = 1u << (slot * kKeysPerWarp + i);
                 vmask = off >= 0 ? (vmask | bit) : (vmask & ~bit);
                 if (off >= 0)
