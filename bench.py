@@ -906,7 +906,10 @@ def sweep(device, peak):
                      "heads_padded": Hp, "us": ms * 1e3, "tokens_per_s": T / (ms * 1e-3),
                      "alg_bytes": b, "alg_gbs": b / (ms * 1e-3) / 1e9,
                      "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
-                     "l2": f"{len(sets)} rotating input sets"}
+                     "l2": f"{len(sets)} rotating input sets",
+                     "ncu": ncu_dram_rate("qnorm_rope_kv_insert_kernel",
+                                          "qnorm_prefill_8192x16p64", peak)
+                     if name.endswith("prefill_8192x16p64") else None}
         del sets
         torch.cuda.empty_cache()
 
@@ -955,7 +958,7 @@ def sparse_logits_entries(torch, gkr, W, case, kv, idx, device, peak, timed) -> 
         "kernel": "sparse_logits_kernel", "queries": Q, "topk": K, "heads": H, "us": ms * 1e3,
         "entries_per_s": Q * K / (ms * 1e-3), "alg_bytes": b, "alg_gbs": b / (ms * 1e-3) / 1e9,
         "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak, "tflops": f / (ms * 1e-3) / 1e12,
-        "bound": "hbm"}
+        "bound": "hbm", "ncu": ncu_dram_rate("sparse_logits_kernel", "sparse_logits", peak)}
     rows = torch.empty(Q, K, 512, dtype=torch.bfloat16, device=device)
     outs_bf16 = [torch.empty(Q, H, K, dtype=torch.bfloat16, device=device) for _ in range(2)]
 
