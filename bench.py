@@ -830,7 +830,9 @@ def sweep(device, peak):
                                   "alg_gbs": b / (ms * 1e-3) / 1e9,
                                   "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
                                   "csc_bytes": csc_bytes(case.slots, case.positions),
-                                  "l2": f"{len(sets)} rotating input sets"}
+                                  "l2": f"{len(sets)} rotating input sets",
+                                  "ncu": ncu_dram_rate(gkr.insert_kernel_for(T),
+                                                       f"roundtrip_v41_{T}", peak)}
         if T == 65536:   # the round trip's gather at this size: the slots just written
             for st in sets:
                 st["idx"] = st["slots"].to(torch.int32)
@@ -841,7 +843,9 @@ def sweep(device, peak):
                                       "indices_per_s": T / (ms * 1e-3), "alg_bytes": b,
                                       "alg_gbs": b / (ms * 1e-3) / 1e9,
                                       "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
-                                      "l2": f"{len(sets)} rotating input sets"}
+                                      "l2": f"{len(sets)} rotating input sets",
+                                      "ncu": ncu_dram_rate("gather_kernel",
+                                                           f"roundtrip_v41_{T}", peak)}
         del sets
         torch.cuda.empty_cache()
 
