@@ -148,12 +148,38 @@ def measured_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
 
 
+def code_only(text: str) -> str:
+    """C++ source without its comments, whitespace runs collapsed to one space: what the
+    compiler sees, so that a comment edit leaves a capture's record valid."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":                                   # string or character literal
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code (every .cu / .cuh / .h of the extension, comments
+    and whitespace removed)."""
     h = hashlib.sha256()
     csrc = ROOT / "gather_kv_rope_gb300" / "csrc"
     for f in sorted(list(csrc.glob("*.cu")) + list(csrc.glob("*.cuh")) + list(csrc.glob("*.h"))):
         h.update(f.name.encode())
-        h.update(f.read_bytes())
+        h.update(code_only(f.read_text(encoding="utf-8")).encode())
     return h.hexdigest()[:16]
 
 

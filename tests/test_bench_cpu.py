@@ -148,3 +148,14 @@ def test_timed_region_runs_exactly_k_steps_and_continues_the_rotation(monkeypatc
             r.run()
         assert len(captured) == n_captured          # every graph was captured up front
         assert seen == [j % bench.ROTATE for j in range(4 * K)]
+
+
+def test_code_only_drops_comments_and_whitespace_only():
+    """The kernel-source hash ignores comments and layout, not code (string and character
+    literals that look like comments stay)."""
+    import bench
+    a = 'int a = 1; // one\n/* two\n lines */ const char* s = "//x/*"; char c = \'/\';\n'
+    b = 'int a = 1;\n\n   const char* s = "//x/*";   char c = \'/\';'
+    assert bench.code_only(a) == bench.code_only(b) == \
+        'int a = 1; const char* s = "//x/*"; char c = \'/\';'
+    assert bench.code_only("int a = 1;") != bench.code_only("int a = 2;")
