@@ -1,6 +1,6 @@
-// Record decode shared by the gather (gather.cu) and the fused gather + logits kernel
-// (logits.cu): one warp loads one cache record (any of the four formats) with the lane
-// layout of device.cuh and dequantises it to the bf16 row kv_gather returns.
+// Record decode of the gather (gather.cu): one warp loads one cache record (any of the
+// four formats) with the lane layout of device.cuh and dequantises it to the bf16 row
+// kv_gather returns.
 //
 // Operation (page "PR #56893 [DSv4.1] Store the whole KV in MXFP8 (FlashMLA V4.1
 // record)", section "实现拆解" item 4: the gather reads a record by its width and

@@ -14,22 +14,23 @@
 // warps per SM, each CTA taking a contiguous run of work items (query, chunk of 128 keys)
 // in query-major order.
 //   * A, the query's heads (up to 128, zero-padded; M = 128 x K = 512, bf16), lives in
-//     tensor memory next to the accumulators, so shared memory is left to the records.
-//     The 4 epilogue warps write it (tcgen05.st) when the run reaches a new query, once
-//     the products that read the old one are done.
-//   * 16 producer warps keep a ring of raw records per warp in shared memory, filled
-//     with cp.async several stages ahead (the loads in flight cost no registers), and
-//     dequantise each 32-key stage (2 keys a warp) into one of 3 bf16 B tiles (N = 32 x
-//     K = 512, K-major, 128-byte swizzle).
-//   * one warp, once all producers have filled a stage, issues its 32 tcgen05.mma
-//     (kind::f16, K = 16 each, A from tensor memory) into that stage's 32 columns of one
-//     of two 128-column accumulators and commits them to the stage's mbarrier (the stage
-//     may then be refilled); after an item's last stage it commits the accumulator.
+//     tensor memory next to the two accumulators, so shared memory is left to the records.
+//     The 4 epilogue warps write it (tcgen05.st) at launch and when the run reaches a new
+//     query, once the products that read the old one are done; one thread prefetches the
+//     run's query tiles into L2 at launch.
+//   * 16 producer warps, 4 keys of each 64-key group each: a ring of raw records per warp
+//     in shared memory, filled with cp.async two groups ahead (the loads in flight cost no
+//     registers); each group is dequantised twice, its low 256 dims and then its high 256,
+//     into B stages of 64 keys x 256 dims (K-major, 128-byte swizzle, a ring of 3).
+//   * one warp, once all producers have filled a stage, issues its 16 tcgen05.mma
+//     (kind::f16, N = 64, K = 16 each, A from tensor memory) into the group's 64 columns of
+//     one of two 128-column accumulators and commits them to the stage's mbarrier (the
+//     stage may then be refilled); after an item's last stage it commits the accumulator.
 //   * the 4 epilogue warps, one per quarter of the tensor-memory lanes (heads), drain
-//     each item's accumulator while the next item is multiplied into the other one: 32
-//     columns (entries) at a time through a padded shared-memory tile, so that every
-//     store writes a whole 128-byte line of a head's row of logits (entries that are not
-//     records: -inf).
+//     each item's accumulator while the next item is multiplied into the other one, 32
+//     columns (entries) at a time: each lane writes its head's 32 logits (entries that are
+//     not records: -inf) into the warp's swizzled tile and one lane hands the tile to a
+//     TMA tensor store.
 // Every wait on an mbarrier is bounded (20 ms of %globaltimer): past it the CTA sets
 // GKR_ERR_TIMEOUT, stops waiting, still frees its tensor memory and returns.
 #include <cuda.h>
