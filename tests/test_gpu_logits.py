@@ -104,6 +104,26 @@ def test_bad_fp8_scale_gives_minus_inf(gkr, oracle_mod):
     assert torch.isneginf(out).all() and int(err.item()) == gkr.ERR_SCALE
 
 
+@pytest.mark.parametrize("record", [528, 584])
+def test_many_queries_per_cta(gkr, oracle_mod, record):
+    """400 queries of 132 entries: two items per query (the second one 4 entries long), so
+    every CTA's run crosses several queries and reloads the query tile between products;
+    40 heads leave the last head quarter partly empty."""
+    bs, pages, Q, H, K = 64, 40, 400, 40, 132
+    c, flat, ps = _host_cache(oracle_mod, record, pages * bs, bs, pages, seed=21)
+    rng = np.random.default_rng(22)
+    idx = _indices(rng, Q, K, np.arange(pages * bs), bad_rate=0.005, num_slots=pages * bs)
+    q = bf16_bits(rng.standard_normal((Q, H, 512)).astype(np.float32))
+    cache = _to_device_cache(gkr, flat, pages, bs, record, ps)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = gkr.sparse_logits(torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).to(DEV),
+                            cache, torch.from_numpy(idx).to(DEV), -0.03, err_flag=err)
+    torch.cuda.synchronize()
+    exact, bound, ref_err = oracle_mod.sparse_logits(q, flat, record, bs, pages, ps, idx, -0.03)
+    _check(out.cpu().numpy(), exact, bound)
+    assert int(err.item()) == ref_err
+
+
 def test_graph_replay_and_launch_options(gkr, oracle_mod):
     """Captured once (programmatic dependent launch off by option), replayed over new
     queries and indices copied into the captured buffers."""
