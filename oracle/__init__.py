@@ -104,6 +104,11 @@ def lib() -> ctypes.CDLL:
                                                   i64, vp, i32, i32, i64, i64, vp, vp, vp, i64,
                                                   f32]
         L.oracle_qnorm_rope_kv_insert.restype = i32
+        L.oracle_q_head_fp8.argtypes = [vp, vp, f64, i32, f32, vp, vp, vp]
+        L.oracle_q_head_fp8.restype = None
+        L.oracle_qnorm_rope_fp8q.argtypes = [vp, i32, i32, f64, i32, f32, i64, vp, vp, i64,
+                                             vp, vp, vp]
+        L.oracle_qnorm_rope_fp8q.restype = i32
         _lib = L
     return _lib
 
@@ -287,6 +292,42 @@ def qnorm_rope_kv_insert(q: np.ndarray, num_heads_padded: int, eps: float, apply
     if err < 0:
         raise ValueError(f"unknown record width {record}")
     return q_rn, q_alt, q_lo, q_hi, err
+
+
+def q_head_fp8(q_row: np.ndarray, csc_row: np.ndarray, eps: float, q_scale: float,
+               apply_norm: bool = True):
+    """One query head (bf16 bits [512]) cast to e4m3 with the fp32 scale q_scale ->
+    (nearest codes, lowest codes, highest codes) uint8 [512]: e4m3(RN32(x / q_scale)) for
+    x = the fp32 nearest the exact value, and for the smallest / largest fp32 an fp32
+    evaluation of the head in any order may give (lowest / highest by value)."""
+    q_row = np.ascontiguousarray(q_row, dtype=np.uint16)
+    csc_row = np.ascontiguousarray(csc_row, dtype=np.float32)
+    assert q_row.shape == (512,) and csc_row.shape == (64,)
+    rn, lo, hi = (np.zeros(512, np.uint8) for _ in range(3))
+    lib().oracle_q_head_fp8(_ptr(q_row), _ptr(csc_row), float(eps), int(bool(apply_norm)),
+                            float(q_scale), _ptr(rn), _ptr(lo), _ptr(hi))
+    return rn, lo, hi
+
+
+def qnorm_rope_fp8q(q: np.ndarray, num_heads_padded: int, eps: float, apply_norm: bool,
+                    q_scale: float, positions: np.ndarray, csc: np.ndarray):
+    """The query side of the fused op with an e4m3 output: q bf16 bits [T, H, 512] ->
+    (codes_rn, codes_lo, codes_hi, error bits), codes uint8 [T, num_heads_padded, 512]
+    (see q_head_fp8; padded heads, heads of a token with a position outside the table, and
+    every head under a q_scale that is not a positive finite number are +0)."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    positions = np.ascontiguousarray(positions, dtype=np.int64).reshape(-1)
+    T = positions.shape[0]
+    q = q.reshape(T, -1, 512)
+    H = q.shape[1]
+    assert num_heads_padded >= H
+    csc = np.ascontiguousarray(csc, dtype=np.float32).reshape(-1, 64)
+    rn, lo, hi = (np.zeros((T, num_heads_padded, 512), np.uint8) for _ in range(3))
+    err = lib().oracle_qnorm_rope_fp8q(_ptr(q), H, int(num_heads_padded), float(eps),
+                                       int(bool(apply_norm)), float(q_scale), T,
+                                       _ptr(positions), _ptr(csc), csc.shape[0], _ptr(rn),
+                                       _ptr(lo), _ptr(hi))
+    return rn, lo, hi, err
 
 
 # --- sparse decode logits (the gather fused into its consumer) --------------------

@@ -599,16 +599,12 @@ static uint16_t bf16_up(double y)
     return oracle_bf16_value(b) < y ? bf16_toward(b, INFINITY) : b;
 }
 
-/* One query head: exact[d] = the normed and rotated value of dim d (double);
- * rn[d] = its nearest-even bf16, alt[d] = the other faithful bf16 (== rn when the
- * value is a bf16); lo[d] .. hi[d] = the bf16 values an fp32 evaluation may give (see
- * above).  eps >= 0; a zero row with eps = 0 is outside the contract. */
-ORACLE_EXPORT void oracle_q_head(const uint16_t *q_row, const float *csc_row, double eps,
-                                 int apply_norm, double exact[512], uint16_t rn[512],
-                                 uint16_t alt[512], uint16_t lo[512], uint16_t hi[512])
+/* The normed (when apply_norm) and rotated values of one query head in double, and
+ * the size each one's fp32 evaluation error scales with (see above). */
+static void q_head_values(const uint16_t *q_row, const float *csc_row, double eps,
+                          int apply_norm, double x[512], double size[512])
 {
-    double x[512], size[512], r = 1.0, ss = 0.0;
-    const double rel = ldexp(1.0, -19);
+    double r = 1.0, ss = 0.0;
     int d, j;
     for (d = 0; d < 512; d++)
         x[d] = oracle_bf16_value(q_row[d]);
@@ -629,6 +625,20 @@ ORACLE_EXPORT void oracle_q_head(const uint16_t *q_row, const float *csc_row, do
         size[448 + 2 * j] = fabs(e * c) + fabs(o * s);
         size[449 + 2 * j] = fabs(o * c) + fabs(e * s);
     }
+}
+
+/* One query head: exact[d] = the normed and rotated value of dim d (double);
+ * rn[d] = its nearest-even bf16, alt[d] = the other faithful bf16 (== rn when the
+ * value is a bf16); lo[d] .. hi[d] = the bf16 values an fp32 evaluation may give (see
+ * above).  eps >= 0; a zero row with eps = 0 is outside the contract. */
+ORACLE_EXPORT void oracle_q_head(const uint16_t *q_row, const float *csc_row, double eps,
+                                 int apply_norm, double exact[512], uint16_t rn[512],
+                                 uint16_t alt[512], uint16_t lo[512], uint16_t hi[512])
+{
+    double x[512], size[512];
+    const double rel = ldexp(1.0, -19);
+    int d;
+    q_head_values(q_row, csc_row, eps, apply_norm, x, size);
     for (d = 0; d < 512; d++) {
         exact[d] = x[d];
         rn[d] = oracle_bf16_encode(x[d]);
@@ -636,6 +646,79 @@ ORACLE_EXPORT void oracle_q_head(const uint16_t *q_row, const float *csc_row, do
         lo[d] = bf16_down(x[d] - rel * size[d]);
         hi[d] = bf16_up(x[d] + rel * size[d]);
     }
+}
+
+/* The largest fp32 not above v, and the smallest not below it. */
+static float f32_down(double v)
+{
+    float f = (float)v;
+    return (double)f > v ? nextafterf(f, -INFINITY) : f;
+}
+
+static float f32_up(double v)
+{
+    float f = (float)v;
+    return (double)f < v ? nextafterf(f, INFINITY) : f;
+}
+
+/* One query head cast to e4m3 with the fp32 scale q_scale (a positive finite number),
+ * as the fp8 cache casts its rows: code = e4m3(RN32(x / q_scale)), x the head's fp32
+ * value.  rn[d] takes x = RN32(exact); lo[d] .. hi[d] (by value) are the codes of the
+ * smallest and the largest fp32 x within the range of oracle_q_head (the quotient and
+ * the cast are monotone, so every fp32 evaluation gives a code between them). */
+ORACLE_EXPORT void oracle_q_head_fp8(const uint16_t *q_row, const float *csc_row, double eps,
+                                     int apply_norm, float q_scale, uint8_t rn[512],
+                                     uint8_t lo[512], uint8_t hi[512])
+{
+    double x[512], size[512];
+    const double rel = ldexp(1.0, -19);
+    int d;
+    q_head_values(q_row, csc_row, eps, apply_norm, x, size);
+    for (d = 0; d < 512; d++) {
+        float q;
+        q = (float)x[d] / q_scale;
+        rn[d] = oracle_e4m3_encode((double)q);
+        q = f32_down(x[d] - rel * size[d]) / q_scale;
+        lo[d] = oracle_e4m3_encode((double)q);
+        q = f32_up(x[d] + rel * size[d]) / q_scale;
+        hi[d] = oracle_e4m3_encode((double)q);
+    }
+}
+
+/* The query side of the fused op with an e4m3 output (q_out [T, Hp, 512] codes): heads
+ * h < num_heads of a token whose position is in [0, max_pos) by oracle_q_head_fp8, every
+ * other head (padded, or a bad position: ORACLE_ERR_POS) +0 (code 0).  A q_scale that is
+ * not a positive finite number writes every head as +0 and returns ORACLE_ERR_SCALE.
+ * The KV side is oracle_kv_insert's.  Returns the error bits. */
+ORACLE_EXPORT int oracle_qnorm_rope_fp8q(const uint16_t *q_in, int num_heads,
+                                         int num_heads_padded, double eps, int apply_norm,
+                                         float q_scale, int64_t num_tokens,
+                                         const int64_t *positions, const float *csc,
+                                         int64_t max_pos, uint8_t *q_rn, uint8_t *q_lo,
+                                         uint8_t *q_hi)
+{
+    int64_t t;
+    int h, err = 0;
+    int good = scale_ok(q_scale);
+    if (!good && num_tokens > 0 && num_heads_padded > 0)
+        err |= ORACLE_ERR_SCALE;
+    for (t = 0; t < num_tokens; t++) {
+        int64_t pos = positions[t];
+        for (h = 0; h < num_heads_padded; h++) {
+            int64_t at = (t * num_heads_padded + h) * 512;
+            if (!good || h >= num_heads || pos < 0 || pos >= max_pos) {
+                memset(q_rn + at, 0, 512);
+                memset(q_lo + at, 0, 512);
+                memset(q_hi + at, 0, 512);
+                continue;
+            }
+            oracle_q_head_fp8(q_in + (t * num_heads + h) * 512, csc + pos * 64, eps, apply_norm,
+                              q_scale, q_rn + at, q_lo + at, q_hi + at);
+        }
+        if (num_heads > 0 && (pos < 0 || pos >= max_pos))
+            err |= ORACLE_ERR_POS;
+    }
+    return err;
 }
 
 /* The fused op: for every token t (slot and position checks as the KV insert, but the

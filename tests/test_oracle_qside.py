@@ -259,3 +259,76 @@ def test_fp32_evaluation_range(oracle_mod):
     wrong, _, _ = oracle_mod.q_head(q, np.concatenate([row[:32], -row[32:]]), 1e-6, True)
     outside = (wrong[448:] < vl[448:]) | (wrong[448:] > vh[448:])
     assert outside.mean() > 0.9
+
+
+# ---------------------------------------------------------------- e4m3 query output
+
+def _e4m3_value(codes: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(torch.float8_e4m3fn) \
+        .double().numpy()
+
+
+@pytest.mark.parametrize("c,s,code", [(0.5, 0.25, 0x48), (3.0, 1.0, 0x38), (-7.0, 2.0, 0xB0),
+                                      (250.0, 1e-3, 0x7E), (-1e-3, 1e-3, 0xFE)])
+def test_fp8_q_constant_row_closed_form(oracle_mod, c, s, code):
+    """eps = 0: a constant row normalises to sign(c) exactly, so every code is that of
+    sign(c) / s: 1/0.25 = 4 = 1.0 * 2^2 (exponent field 9: 0x48), 1.0 (0x38), -0.5 (sign
+    bit, exponent field 6: 0xB0), and 1/1e-3 = 1000 saturating to 448 (0x7E, or 0xFE
+    negative); the three codes agree."""
+    rn, lo, hi = oracle_mod.q_head_fp8(bf16_bits(np.full(HEAD, c)), csc_row(1.0, 0.0), 0.0, s)
+    assert (rn == code).all() and (lo == code).all() and (hi == code).all()
+
+
+def test_fp8_q_without_norm_is_the_fp8_cache_row(oracle_mod):
+    """apply_q_norm off: a query head is rotated like a KV row, and the fp8 cache encodes
+    e4m3(RN32(x / scale)) of that row with one fp32 evaluation of the rotation, so the
+    cache row's codes lie in the query range (and equal the nearest codes on the
+    unrotated dims 0..447, where x is the bf16 input itself)."""
+    rng = np.random.default_rng(11)
+    csc = W.cos_sin_table(512)
+    for k in range(6):
+        row = bf16_bits(rng.standard_normal(HEAD).astype(np.float32) * np.float32(3.0))
+        pos, s = int(rng.integers(0, 512)), float(np.float32(10.0 ** rng.uniform(-2, 1)))
+        ps = oracle_mod.page_stride(512, 32)
+        cache = np.zeros(ps, np.uint8)
+        assert oracle_mod.insert(row.reshape(1, HEAD), cache, 512, 32, 1, ps,
+                                 np.array([5]), np.array([pos]), csc, fp8_scale=np.float32(s)) == 0
+        cache_row = cache[5 * 512:6 * 512]
+        rn, lo, hi = oracle_mod.q_head_fp8(row, csc[pos], 0.0, s, apply_norm=False)
+        v, vl, vh = _e4m3_value(cache_row), _e4m3_value(lo), _e4m3_value(hi)
+        assert ((vl <= v) & (v <= vh)).all()
+        assert np.array_equal(cache_row[:448], rn[:448])
+
+
+def test_fp8_q_range_and_planted_slip(oracle_mod):
+    """The nearest codes lie within lo .. hi; on the unrotated dims the range is almost
+    always one code (2^-19 of the value is far inside an e4m3 step); multiplying by the
+    scale instead of dividing lands outside the range."""
+    rng = np.random.default_rng(12)
+    csc = W.cos_sin_table(4096)
+    q = _random_head(rng, 2.0)
+    s = 0.0625
+    rn, lo, hi = oracle_mod.q_head_fp8(q, csc[77], 1e-6, s)
+    v, vl, vh = _e4m3_value(rn), _e4m3_value(lo), _e4m3_value(hi)
+    assert ((vl <= v) & (v <= vh)).all()
+    assert (lo[:448] == hi[:448]).mean() > 0.99
+    exact, _, _ = oracle_mod.q_head(q, csc[77], 1e-6, True)
+    wrong = np.array([oracle_mod.e4m3_encode(x * s) for x in exact], np.uint8)
+    vw = _e4m3_value(wrong)
+    assert ((vw < vl) | (vw > vh)).mean() > 0.9
+
+
+def test_fp8_q_op_padding_positions_and_bad_scale(oracle_mod):
+    """Padded heads and the heads of a token whose position is outside the table are +0
+    (code 0) with ORACLE_ERR_POS for the latter; a scale that is not a positive finite
+    number writes every head as +0 with ORACLE_ERR_SCALE; otherwise each head is
+    q_head_fp8's."""
+    c, q = _op_case(T=12, H=3, bad_pos=True)
+    rn, lo, hi, err = oracle_mod.qnorm_rope_fp8q(q, 5, 1e-6, True, 0.5, c.positions, c.csc)
+    assert rn.shape == (12, 5, HEAD) and err == oracle_mod.ERR_POS
+    assert (rn[:, 3:] == 0).all() and (rn[3] == 0).all() and (rn[7] == 0).all()
+    r1, l1, h1 = oracle_mod.q_head_fp8(q[0, 1], c.csc[c.positions[0]], 1e-6, 0.5)
+    assert np.array_equal(rn[0, 1], r1) and np.array_equal(lo[0, 1], l1) and np.array_equal(hi[0, 1], h1)
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        rn, lo, hi, err = oracle_mod.qnorm_rope_fp8q(q, 5, 1e-6, True, bad, c.positions, c.csc)
+        assert err & oracle_mod.ERR_SCALE and (rn == 0).all() and (lo == 0).all() and (hi == 0).all()
