@@ -688,8 +688,9 @@ ORACLE_EXPORT void oracle_q_head_fp8(const uint16_t *q_row, const float *csc_row
 /* The query side of the fused op with an e4m3 output (q_out [T, Hp, 512] codes): heads
  * h < num_heads of a token whose position is in [0, max_pos) by oracle_q_head_fp8, every
  * other head (padded, or a bad position: ORACLE_ERR_POS) +0 (code 0).  A q_scale that is
- * not a positive finite number writes every head as +0 and returns ORACLE_ERR_SCALE.
- * The KV side is oracle_kv_insert's.  Returns the error bits. */
+ * not a positive finite number writes every head as +0, and returns ORACLE_ERR_SCALE
+ * when there is a head to cast (num_heads > 0 and a token with its position in the
+ * table).  The KV side is oracle_kv_insert's.  Returns the error bits. */
 ORACLE_EXPORT int oracle_qnorm_rope_fp8q(const uint16_t *q_in, int num_heads,
                                          int num_heads_padded, double eps, int apply_norm,
                                          float q_scale, int64_t num_tokens,
@@ -700,10 +701,10 @@ ORACLE_EXPORT int oracle_qnorm_rope_fp8q(const uint16_t *q_in, int num_heads,
     int64_t t;
     int h, err = 0;
     int good = scale_ok(q_scale);
-    if (!good && num_tokens > 0 && num_heads_padded > 0)
-        err |= ORACLE_ERR_SCALE;
     for (t = 0; t < num_tokens; t++) {
         int64_t pos = positions[t];
+        if (!good && num_heads > 0 && pos >= 0 && pos < max_pos)
+            err |= ORACLE_ERR_SCALE;
         for (h = 0; h < num_heads_padded; h++) {
             int64_t at = (t * num_heads_padded + h) * 512;
             if (!good || h >= num_heads || pos < 0 || pos >= max_pos) {

@@ -332,3 +332,9 @@ def test_fp8_q_op_padding_positions_and_bad_scale(oracle_mod):
     for bad in (0.0, -1.0, float("inf"), float("nan")):
         rn, lo, hi, err = oracle_mod.qnorm_rope_fp8q(q, 5, 1e-6, True, bad, c.positions, c.csc)
         assert err & oracle_mod.ERR_SCALE and (rn == 0).all() and (lo == 0).all() and (hi == 0).all()
+    # no head to cast (padded heads only, or every position outside the table): no scale
+    # is read, so no scale error
+    empty = np.zeros((12, 0, HEAD), np.uint16)
+    assert oracle_mod.qnorm_rope_fp8q(empty, 4, 1e-6, True, 0.0, c.positions, c.csc)[3] == 0
+    far = np.full(12, 10 ** 6, np.int64)
+    assert oracle_mod.qnorm_rope_fp8q(q, 5, 1e-6, True, 0.0, far, c.csc)[3] == oracle_mod.ERR_POS
