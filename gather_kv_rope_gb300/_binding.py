@@ -137,10 +137,11 @@ def lib() -> ctypes.CDLL:
                 L.gkr_kv_gather.argtypes = [vp, ctypes.POINTER(CacheDesc), vp, i64, vp, vp, vp,
                                             opt, vp]
                 L.gkr_kv_gather.restype = ctypes.c_int
-                # q_in, H, Hp, q_out, eps, apply_q_norm, then gkr_kv_insert's arguments
-                L.gkr_qnorm_rope_kv_insert.argtypes = [vp, i32, i32, vp, ctypes.c_float, i32, vp,
-                                                       i64, vp, ctypes.POINTER(CacheDesc), vp, vp,
-                                                       vp, i64, vp, vp, opt, vp]
+                # q_in, H, Hp, q_out, q_scale, eps, apply_q_norm, then gkr_kv_insert's
+                # arguments
+                L.gkr_qnorm_rope_kv_insert.argtypes = [vp, i32, i32, vp, vp, ctypes.c_float, i32,
+                                                       vp, i64, vp, ctypes.POINTER(CacheDesc), vp,
+                                                       vp, vp, i64, vp, vp, opt, vp]
                 L.gkr_qnorm_rope_kv_insert.restype = ctypes.c_int
                 # q, H, k_cache, desc, indices, Q, topk, sm_scale, fp8_scale, out, err, opts,
                 # stream
@@ -443,12 +444,15 @@ def qnorm_rope_kv_insert(q: torch.Tensor, kv: torch.Tensor, k_cache: torch.Tenso
                          q_out: torch.Tensor | None = None, record: int | None = None,
                          err_flag: torch.Tensor | None = None,
                          fp8_scale: torch.Tensor | None = None,
+                         q_scale: torch.Tensor | None = None,
                          launch_opts: LaunchOpts | None = None) -> torch.Tensor:
     """The fused attention write: each query head of q (bf16 [T, H, 512]) divided by
     sqrt(mean(q^2) + eps) when apply_q_norm, dims 448..511 rotated with the token's
     cos/sin row, written as bf16 to q_out [T, num_heads_padded, 512] (padded heads +0),
     and the KV rows inserted into k_cache exactly as kv_insert does, in one launch.
-    q_out may be q itself when num_heads_padded == H.  Returns q_out (allocated when
+    q_out may be q itself when num_heads_padded == H.  With q_scale (a float32 CUDA
+    tensor of one element) q_out holds e4m3 codes instead, e4m3(x / q_scale) of each fp32
+    value (float8_e4m3fn or uint8, not overlapping q).  Returns q_out (allocated when
     None).  The other arguments are kv_insert's."""
     _check(q.dtype == torch.bfloat16 and q.dim() == 3 and q.shape[2] == HEAD_DIM
            and q.is_contiguous(), "q must be a contiguous bf16 tensor [tokens, heads, 512]")
@@ -458,15 +462,21 @@ def qnorm_rope_kv_insert(q: torch.Tensor, kv: torch.Tensor, k_cache: torch.Tenso
     H, Hp = int(q.shape[1]), int(num_heads_padded)
     _check(q.shape[0] >= T, "q has fewer tokens than slot_mapping")
     _check(Hp >= H, "num_heads_padded must be at least q.shape[1]")
+    fp8_q = q_scale is not None
+    if fp8_q:
+        _check(q_scale.dtype == torch.float32 and q_scale.numel() == 1 and q_scale.is_cuda,
+               "q_scale must be a float32 CUDA tensor of one element")
+    out_types = (torch.float8_e4m3fn, torch.uint8) if fp8_q else (torch.bfloat16,)
     if q_out is None:
-        q_out = torch.empty(T, Hp, HEAD_DIM, dtype=torch.bfloat16, device=dev)
-    _check(q_out.dtype == torch.bfloat16 and q_out.is_contiguous() and q_out.dim() == 3
+        q_out = torch.empty(T, Hp, HEAD_DIM, dtype=out_types[0], device=dev)
+    _check(q_out.dtype in out_types and q_out.is_contiguous() and q_out.dim() == 3
            and q_out.shape[0] >= T and q_out.shape[1] == Hp and q_out.shape[2] == HEAD_DIM,
-           "q_out must be a contiguous bf16 tensor [tokens, num_heads_padded, 512]")
-    _same_cuda_device(kv, q, q_out, fp8_scale)
+           "q_out must be a contiguous tensor [tokens, num_heads_padded, 512] of bf16 "
+           "(e4m3 codes: float8_e4m3fn or uint8 with q_scale)")
+    _same_cuda_device(kv, q, q_out, fp8_scale, q_scale)
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
-        st = lib().gkr_qnorm_rope_kv_insert(_ptr(q), H, Hp, _ptr(q_out), float(eps),
+        st = lib().gkr_qnorm_rope_kv_insert(_ptr(q), H, Hp, _ptr(q_out), _ptr(q_scale), float(eps),
                                             1 if apply_q_norm else 0, _ptr(kv), T, _ptr(k_cache),
                                             ctypes.byref(desc), _ptr(slot_mapping),
                                             _ptr(positions), _ptr(cos_sin_cache),

@@ -310,7 +310,8 @@ GKR_API gkr_status gkr_kv_gather(const void* k_cache, const gkr_cache_desc* cach
 }
 
 GKR_API gkr_status gkr_qnorm_rope_kv_insert(const void* q_in, int32_t num_heads,
-                                            int32_t num_heads_padded, void* q_out, float eps,
+                                            int32_t num_heads_padded, void* q_out,
+                                            const float* q_scale, float eps,
                                             int32_t apply_q_norm, const void* kv,
                                             int64_t num_tokens, void* k_cache,
                                             const gkr_cache_desc* cache,
@@ -330,10 +331,20 @@ GKR_API gkr_status gkr_qnorm_rope_kv_insert(const void* q_in, int32_t num_heads,
     if (st != GKR_OK || p.num_tokens == 0) return st;
     if (num_heads_padded == 0) return cuda_status(launch_insert(cache->record, p, stream));
     if ((num_heads > 0 && q_in == nullptr) || q_out == nullptr) return GKR_EINVAL;
-    if ((num_heads > 0 && !aligned(q_in, 16)) || !aligned(q_out, 16)) return GKR_EALIGN;
+    if ((num_heads > 0 && !aligned(q_in, 16)) || !aligned(q_out, 16) ||
+        (q_scale != nullptr && !aligned(q_scale, 4)))
+        return GKR_EALIGN;
+    if (q_scale != nullptr && num_heads > 0) {   // e4m3 rows of 512 B must not overlap q_in
+        const uintptr_t in0 = reinterpret_cast<uintptr_t>(q_in);
+        const uintptr_t out0 = reinterpret_cast<uintptr_t>(q_out);
+        const uintptr_t in1 = in0 + static_cast<uintptr_t>(p.num_tokens) * num_heads * 1024;
+        const uintptr_t out1 = out0 + static_cast<uintptr_t>(p.num_tokens) * num_heads_padded * 512;
+        if (out0 < in1 && in0 < out1) return GKR_EINVAL;
+    }
     gkr::QSideParams qp;
     qp.q_in = q_in;
     qp.q_out = q_out;
+    qp.q_scale = q_scale;
     qp.num_heads = num_heads;
     qp.num_heads_padded = num_heads_padded;
     qp.eps = eps;
@@ -402,6 +413,6 @@ GKR_API const char* gkr_status_string(gkr_status status) {
 
 GKR_API int32_t gkr_last_cuda_error(void) { return g_last_cuda_error; }
 
-GKR_API int32_t gkr_version(void) { return 30100; }
+GKR_API int32_t gkr_version(void) { return 30200; }
 
 }  // extern "C"

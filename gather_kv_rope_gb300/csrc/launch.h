@@ -46,7 +46,8 @@ struct GatherParams {
 // Query side of the fused attention write (gkr_qnorm_rope_kv_insert).
 struct QSideParams {
     const void* q_in;          // bf16 [num_tokens, num_heads, 512]
-    void* q_out;               // bf16 [num_tokens, num_heads_padded, 512]
+    void* q_out;               // bf16 [num_tokens, num_heads_padded, 512], or e4m3 codes
+    const float* q_scale;      // nullptr: bf16 q_out; else the e4m3 q_out's fp32 scale
     int32_t num_heads;
     int32_t num_heads_padded;  // >= num_heads, > 0 (0 is the plain KV insert)
     float eps;

@@ -10,7 +10,8 @@
 //   query heads h < H: x = q_in[t, h, :] in fp32; with the norm, x /= sqrt(mean(x^2) + eps)
 //     (an RMS norm without a weight: the pages print neither the norm nor the q layout,
 //     this is the reading the library takes); dims 448..511 rotated in adjacent pairs
-//     with cos/sin row p, exactly as the KV row; q_out[t, h, :] = bf16(x);
+//     with cos/sin row p, exactly as the KV row; q_out[t, h, :] = bf16(x), or with a query
+//     scale the e4m3 codes of RN32(x / q_scale) (the fp8 cache's cast of its rows);
 //   heads H .. Hp-1 of q_out: +0;  a position outside the table: every head of the
 //     token +0 and GKR_ERR_POS;
 //   the KV row: as gkr_kv_insert (slot -1 skips it).
@@ -37,14 +38,13 @@ constexpr int kRowsPerWarp = 2;
 enum RowKind : int32_t { kNone = 0, kKvRow = 1, kQHead = 2, kZeroHead = 3 };
 
 // One query head on one warp: chunks A and B of the head (16 bf16 per lane) -> normed
-// (optionally) and rotated -> 16 bf16 per lane.  The sum of squares is taken per lane in
-// dim order, then over the warp by a butterfly (every lane ends with the same sum);
-// mean = sum * 2^-9 (exact); factor = the correctly rounded 1/sqrt(mean + eps); every
-// operation is one fp32 operation rounded to nearest even (no contraction).
+// (optionally) and rotated -> 16 fp32 values per lane.  The sum of squares is taken per
+// lane in dim order, then over the warp by a butterfly (every lane ends with the same
+// sum); mean = sum * 2^-9 (exact); factor = the correctly rounded 1/sqrt(mean + eps);
+// every operation is one fp32 operation rounded to nearest even (no contraction).
 __device__ __forceinline__ void q_head(const uint4 ta, const uint4 tb, const float4 c,
                                        const float4 s, bool norm, float eps, int lane,
-                                       uint4& oa, uint4& ob) {
-    float a[8], b[8];
+                                       float (&a)[8], float (&b)[8]) {
     unpack_bf16x8(ta, a);
     unpack_bf16x8(tb, b);
     if (norm) {
@@ -63,13 +63,26 @@ __device__ __forceinline__ void q_head(const uint4 ta, const uint4 tb, const flo
         }
     }
     if (lane >= 24) rope4(b, c, s);   // dims 448..511 = pairs 4(L-24) .. 4(L-24)+3
-    oa = make_uint4(pack_bf16x2_rn(a[0], a[1]), pack_bf16x2_rn(a[2], a[3]),
-                    pack_bf16x2_rn(a[4], a[5]), pack_bf16x2_rn(a[6], a[7]));
-    ob = make_uint4(pack_bf16x2_rn(b[0], b[1]), pack_bf16x2_rn(b[2], b[3]),
-                    pack_bf16x2_rn(b[4], b[5]), pack_bf16x2_rn(b[6], b[7]));
 }
 
-template <int kRecord>
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2_rn(f[0], f[1]), pack_bf16x2_rn(f[2], f[3]),
+                      pack_bf16x2_rn(f[4], f[5]), pack_bf16x2_rn(f[6], f[7]));
+}
+
+// Eight values -> e4m3(RN32(x / q_scale)), the cast the fp8 cache applies to its rows
+// (the scale's reciprocal prepared as load_scale does).
+__device__ __forceinline__ uint2 quantise_q(const float (&f)[8], const Scale& qs) {
+    if (qs.y == 0.0f) return quantise8_ieee_div(f, qs.s);   // warp-uniform branches
+    if (qs.pow2) return quantise8_pow2(f, qs.y);
+    return quantise8_div(f, qs.s, qs.y);
+}
+
+__device__ __forceinline__ void st_stream8(void* p, uint2 v) {
+    __stcs(reinterpret_cast<uint2*>(p), v);
+}
+
+template <int kRecord, bool kFp8Q>
 __global__ void __launch_bounds__(kThreads, GKR_QSIDE_MIN_BLOCKS)
     qnorm_rope_kv_insert_kernel(const InsertParams p, const QSideParams qp) {
     constexpr int U = kRowsPerWarp;
@@ -142,6 +155,21 @@ __global__ void __launch_bounds__(kThreads, GKR_QSIDE_MIN_BLOCKS)
             kind = kZeroHead;
         }
     }
+    // the e4m3 query output's scale, read once by a warp with query heads; one that is not
+    // a positive finite number turns them into zero heads
+    Scale qs{1.0f, 1.0f, false};
+    if constexpr (kFp8Q) {
+        if (__ballot_sync(kFull, kind == kQHead) != 0u) {
+            qs.s = __ldg(qp.q_scale);
+            if (!scale_ok(qs.s)) {
+                if (kind == kQHead) kind = kZeroHead;
+                err |= static_cast<uint32_t>(kErrScale);
+            } else {
+                qs.pow2 = exact_power_of_two(qs.s);
+                qs.y = qs.pow2 ? __frcp_rn(qs.s) : quotient_reciprocal(qs.s);
+            }
+        }
+    }
     err = __reduce_or_sync(kFull, err);
     if (err != 0u && lane == 0) report(p.err, static_cast<int32_t>(err));
 
@@ -182,12 +210,30 @@ __global__ void __launch_bounds__(kThreads, GKR_QSIDE_MIN_BLOCKS)
             const int64_t so = __shfl_sync(kFull, soff, u);
             encode_store<kRecord>(L[u], cache_a + o, cache_s + so, lane, scale);
         } else if (kinds[u] == kQHead || kinds[u] == kZeroHead) {
-            uint4 oa = make_uint4(0u, 0u, 0u, 0u), ob = oa;
-            if (kinds[u] == kQHead)
-                q_head(L[u].a, L[u].b, L[u].c, L[u].s, qp.apply_norm != 0, qp.eps, lane, oa, ob);
-            uint8_t* dst = qout + (tok[u] * qp.num_heads_padded + head[u]) * 1024 + 16 * lane;
-            st_stream16(dst, oa);
-            st_stream16(dst + 512, ob);
+            const int64_t row = tok[u] * qp.num_heads_padded + head[u];
+            if constexpr (kFp8Q) {   // e4m3 codes: dims 8L.. at byte 8L, 256 + 8L.. at 256 + 8L
+                uint2 ca = make_uint2(0u, 0u), cb = ca;
+                if (kinds[u] == kQHead) {
+                    float a[8], b[8];
+                    q_head(L[u].a, L[u].b, L[u].c, L[u].s, qp.apply_norm != 0, qp.eps, lane, a, b);
+                    ca = quantise_q(a, qs);
+                    cb = quantise_q(b, qs);
+                }
+                uint8_t* dst = qout + row * 512 + 8 * lane;
+                st_stream8(dst, ca);
+                st_stream8(dst + 256, cb);
+            } else {
+                uint4 oa = make_uint4(0u, 0u, 0u, 0u), ob = oa;
+                if (kinds[u] == kQHead) {
+                    float a[8], b[8];
+                    q_head(L[u].a, L[u].b, L[u].c, L[u].s, qp.apply_norm != 0, qp.eps, lane, a, b);
+                    oa = pack_bf16x8(a);
+                    ob = pack_bf16x8(b);
+                }
+                uint8_t* dst = qout + row * 1024 + 16 * lane;
+                st_stream16(dst, oa);
+                st_stream16(dst + 512, ob);
+            }
         }
     }
 }
@@ -198,8 +244,11 @@ cudaError_t launch(const InsertParams& p, const QSideParams& qp, cudaStream_t st
     const int64_t rows = p.num_tokens * (static_cast<int64_t>(qp.num_heads_padded) + 1);
     const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * kRowsPerWarp;
     const int64_t blocks = (rows + per_block - 1) / per_block;
-    return launch_kernel(qnorm_rope_kv_insert_kernel<kRecord>, blocks, kThreads, 0, stream,
-                         p.pdl, p, qp);
+    return qp.q_scale != nullptr
+               ? launch_kernel(qnorm_rope_kv_insert_kernel<kRecord, true>, blocks, kThreads, 0,
+                               stream, p.pdl, p, qp)
+               : launch_kernel(qnorm_rope_kv_insert_kernel<kRecord, false>, blocks, kThreads, 0,
+                               stream, p.pdl, p, qp);
 }
 
 }  // namespace

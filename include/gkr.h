@@ -230,6 +230,13 @@ GKR_API gkr_status gkr_rope_quant_insert(const void *kv, int64_t num_tokens, voi
  *     GKR_ERR_POS is set;
  *   the KV row: exactly gkr_kv_insert (slot -1 skips it; the query heads are written
  *     whatever the slot).
+ * With q_scale (an extension reading the pages' fp8 query scale like the fp8 cache's
+ * scale; its meaning is not on the pages), q_out holds e4m3 codes instead of bf16:
+ * q_out[t, h, d] = e4m3(RN32(x_d / q_scale)), saturating, nearest even, x_d the fp32
+ * value whose bf16 rounding is the bf16 output -- the cast the fp8 cache applies to its
+ * rows.  A q_scale that is not a positive finite number writes every query head as +0
+ * and sets GKR_ERR_SCALE (when there is a query head to cast: num_heads > 0 and a token
+ * whose position is in the table); the KV rows are not affected.
  * Accuracy: the norm's arithmetic order is the kernel's (per-lane sums, a warp
  * butterfly, a correctly rounded reciprocal square root), so each q_out value is one of
  * the two bf16 values around the exact result (a faithful rounding; nearest in all but
@@ -241,15 +248,20 @@ GKR_API gkr_status gkr_rope_quant_insert(const void *kv, int64_t num_tokens, voi
  *                   aligned; read only (may be NULL when num_heads == 0).
  * num_heads         >= 0.
  * num_heads_padded  num_heads <= num_heads_padded <= 4096.
- * q_out             device, bf16 [num_tokens, num_heads_padded, 512], 16-byte aligned.
- *                   It may be q_in itself when num_heads_padded == num_heads (in place);
- *                   any other overlap with an input races.
+ * q_out             device, bf16 [num_tokens, num_heads_padded, 512] (uint8 e4m3 codes of
+ *                   the same shape with q_scale), 16-byte aligned.  Without q_scale it
+ *                   may be q_in itself when num_heads_padded == num_heads (in place);
+ *                   with q_scale any overlap with q_in is rejected (GKR_EINVAL); any
+ *                   other overlap with an input races.
+ * q_scale           device, one fp32, 4-byte aligned, read by the kernel; or NULL for a
+ *                   bf16 q_out.
  * eps               finite, >= 0.
  * apply_q_norm      0 or 1.
  * The other arguments are gkr_kv_insert's, for the KV row (any of the four records).
  */
 GKR_API gkr_status gkr_qnorm_rope_kv_insert(const void *q_in, int32_t num_heads,
-                                            int32_t num_heads_padded, void *q_out, float eps,
+                                            int32_t num_heads_padded, void *q_out,
+                                            const float *q_scale, float eps,
                                             int32_t apply_q_norm, const void *kv,
                                             int64_t num_tokens, void *k_cache,
                                             const gkr_cache_desc *cache,
@@ -378,7 +390,8 @@ GKR_API int32_t gkr_last_cuda_error(void);
  * gkr_set_insert_staged_min / gkr_get_insert_staged_min were added.  2.1.0:
  * gkr_set_early_metadata / gkr_get_early_metadata.  3.0.0: every launching entry point
  * takes a gkr_launch_opts pointer before the stream; gkr_qnorm_rope_kv_insert.
- * 3.1.0: gkr_sparse_logits. */
+ * 3.1.0: gkr_sparse_logits.  3.2.0: gkr_qnorm_rope_kv_insert takes q_scale (an e4m3
+ * query output). */
 GKR_API int32_t gkr_version(void);
 
 #ifdef __cplusplus

@@ -59,7 +59,7 @@ def test_page_stride_and_rows(gkr):
     assert gkr.page_stride(1024, 0) == -1
     with pytest.raises(ValueError):
         gkr.record_rows(500)
-    assert gkr.lib().gkr_version() == 30100
+    assert gkr.lib().gkr_version() == 30200
     assert gkr.get_insert_stream_min() == 131072
     assert gkr.get_insert_staged_min() == 24576
     assert gkr.insert_kernel_for(16384) == "insert_short_kernel"
@@ -122,8 +122,8 @@ def gather(gkr, d, N=8, cache=A16b, idx=A16, out=A16, err=None, scale=None, opts
 
 def qinsert(gkr, d, T=8, q=A16b + 0x1000, H=2, Hp=4, qout=A16b + 0x2000, eps=1e-6, norm=1,
             kv=A16, cache=A16b, slots=A16, pos=A16, csc=A16, max_pos=16, err=None, scale=None,
-            opts=None):
-    return gkr.lib().gkr_qnorm_rope_kv_insert(q, H, Hp, qout, eps, norm, kv, T, cache,
+            opts=None, qscale=None):
+    return gkr.lib().gkr_qnorm_rope_kv_insert(q, H, Hp, qout, qscale, eps, norm, kv, T, cache,
                                               None if d is None else ctypes.byref(d), slots, pos,
                                               csc, max_pos, scale, err, _o(opts), None)
 
@@ -233,6 +233,10 @@ def test_qnorm_rope_kv_insert_argument_checks(gkr):
     assert qinsert(gkr, d, kv=None) == 1
     assert qinsert(gkr, desc(gkr, record=512)) == 1                   # fp8 without a scale
     assert qinsert(gkr, desc(gkr, record=500)) == 2
+    # an e4m3 query output: its scale 4-byte aligned, its 512-byte rows clear of q_in
+    assert qinsert(gkr, d, qscale=A16 + 2) == 4
+    assert qinsert(gkr, d, qscale=A16, qout=A16b + 0x2000) == 1       # inside q_in
+    assert qinsert(gkr, d, qscale=A16, qout=A16b) == 1                # ends inside q_in
 
 
 def test_sparse_logits_argument_checks(gkr):

@@ -207,3 +207,81 @@ def test_cuda_graph_replay(gkr, oracle_mod):
         rn, lo, hi, _ = _oracle(oracle_mod, q, Hp, 1e-6, True, c, ref, 528, ps)
         assert first_mismatch(cache_bytes.cpu().numpy(), ref)[0] == 0, r
         _assert_faithful(bits_of(out), rn, (lo, hi))
+
+
+# ---------------------------------------------------------------- e4m3 query output
+
+def _e4m3_value(codes: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(torch.float8_e4m3fn) \
+        .double().numpy()
+
+
+def _run_fp8q(gkr, oracle_mod, c, q, Hp, eps, norm, record, q_scale, fp8_scale=None):
+    ps = oracle_mod.page_stride(record, c.block_size)
+    kv, slots, pos, csc = device_inputs(c, DEV)
+    cache = gkr.alloc_cache(c.num_pages, c.block_size, record, DEV, fill=SENTINEL)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sc = None if fp8_scale is None else torch.tensor([fp8_scale], dtype=torch.float32, device=DEV)
+    qs = torch.tensor([q_scale], dtype=torch.float32, device=DEV)
+    q_out = torch.full((c.num_tokens, Hp, 512), 0x5A, dtype=torch.uint8, device=DEV)
+    gkr.qnorm_rope_kv_insert(bf16_from_bits(q, DEV), kv, cache, slots, pos, csc, Hp, eps,
+                             c.block_size, norm, q_out=q_out, record=record, err_flag=err,
+                             fp8_scale=sc, q_scale=qs)
+    torch.cuda.synchronize()
+    ref = np.full(c.num_pages * ps, SENTINEL, np.uint8)
+    kv_err = oracle_mod.insert(c.kv, ref, record, c.block_size, c.num_pages, ps, c.slots,
+                               c.positions, c.csc,
+                               fp8_scale=None if fp8_scale is None else np.float32(fp8_scale))
+    rn, lo, hi, q_err = oracle_mod.qnorm_rope_fp8q(q, Hp, eps, norm, np.float32(q_scale),
+                                                   c.positions, c.csc)
+    return (gkr.cache_bytes(cache).cpu().numpy(), ref, q_out.cpu().numpy(), rn, lo, hi,
+            int(err.item()), kv_err | q_err)
+
+
+def _assert_codes(got, rn, lo, hi, min_nearest=0.999):
+    """Every code between the codes of the oracle's fp32-evaluation range (by value),
+    nearly all equal to the code of the nearest fp32."""
+    g, vl, vh = _e4m3_value(got), _e4m3_value(lo), _e4m3_value(hi)
+    bad = np.nonzero(~((vl <= g) & (g <= vh)))
+    assert bad[0].size == 0, (f"{bad[0].size} codes outside the range; first "
+                              f"{list(zip(*bad))[:4]} got {got[bad][:4]} rn {rn[bad][:4]}")
+    if got.size:
+        assert np.mean(got == rn) >= min_nearest
+
+
+@pytest.mark.parametrize("record", [528, 512])
+@pytest.mark.parametrize("T,H,Hp", [(1, 1, 1), (37, 3, 8), (300, 16, 16), (700, 5, 64)])
+@pytest.mark.parametrize("norm", [True, False])
+def test_fp8_q_matches_oracle(gkr, oracle_mod, record, T, H, Hp, norm):
+    c, q = _q_case(T, H, seed=T + H + 11 * record)
+    fp8 = 0.05 if record == 512 else None
+    got, ref, qo, rn, lo, hi, err, ref_err = _run_fp8q(gkr, oracle_mod, c, q, Hp, 1e-6, norm,
+                                                       record, 0.03, fp8_scale=fp8)
+    n, first = first_mismatch(got, ref)
+    assert n == 0, f"cache: {n} bytes differ, first {first}"
+    assert err == ref_err == 0
+    _assert_codes(qo, rn, lo, hi)
+    assert (qo[:, H:] == 0).all()
+
+
+@pytest.mark.parametrize("q_scale", [1.0, 2.0 ** -7, 7.3e-4, 1e-30, 3e25])
+def test_fp8_q_scale_paths(gkr, oracle_mod, q_scale):
+    """Powers of two (one product per value), a general scale (the corrected quotient),
+    scales outside [2^-64, 2^64] (IEEE division): saturation at 1e-30, all-zero codes and
+    underflow at 3e25."""
+    c, q = _q_case(120, 4, seed=21, sigma=3.0)
+    got, ref, qo, rn, lo, hi, err, ref_err = _run_fp8q(gkr, oracle_mod, c, q, 4, 1e-6, True,
+                                                       528, q_scale)
+    assert first_mismatch(got, ref)[0] == 0 and err == ref_err == 0
+    _assert_codes(qo, rn, lo, hi)
+
+
+@pytest.mark.parametrize("bad", [0.0, -2.0, float("inf"), float("nan")])
+def test_fp8_q_bad_scale_zeroes_the_heads(gkr, oracle_mod, bad):
+    """A query scale that is not a positive finite number: every query head +0 and
+    GKR_ERR_SCALE; the KV records are inserted as ever."""
+    c, q = _q_case(64, 3, seed=22)
+    got, ref, qo, rn, lo, hi, err, ref_err = _run_fp8q(gkr, oracle_mod, c, q, 4, 1e-6, True,
+                                                       528, bad)
+    assert first_mismatch(got, ref)[0] == 0
+    assert (qo == 0).all() and err == ref_err == gkr.ERR_SCALE
