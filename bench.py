@@ -318,12 +318,13 @@ def csc_bytes(slots: np.ndarray, positions: np.ndarray, ratio: int = 1) -> int:
     return 256 * int(np.unique(positions[w] + 1 - ratio).size)
 
 
-def qside_bytes(slots: np.ndarray, record: int, num_heads: int, num_heads_padded: int) -> int:
+def qside_bytes(slots: np.ndarray, record: int, num_heads: int, num_heads_padded: int,
+                q_out_bytes: int = 1024) -> int:
     """Algorithmic bytes of one fused attention write: the KV insert's bytes plus, per
     token, the query heads read (num_heads x 1024 B) and written (num_heads_padded x
-    1024 B, padded heads included)."""
+    q_out_bytes: 1024 B bf16 or 512 B e4m3, padded heads included)."""
     T = int(np.asarray(slots).size)
-    return insert_bytes(slots, record) + T * 1024 * (num_heads + num_heads_padded)
+    return insert_bytes(slots, record) + T * (1024 * num_heads + q_out_bytes * num_heads_padded)
 
 
 def logits_bytes(indices: np.ndarray, record: int, num_heads: int) -> int:
@@ -940,6 +941,29 @@ def sweep(device, peak):
                      "ncu": ncu_dram_rate("qnorm_rope_kv_insert_kernel",
                                           "qnorm_prefill_8192x16p64", peak)
                      if name.endswith("prefill_8192x16p64") else None}
+        del sets
+        torch.cuda.empty_cache()
+
+    # the same two shapes with the e4m3 query output (one fp32 query scale)
+    for name, T, H, Hp in (("qnorm_rope_kv_insert_fp8q_decode_256x128", 256, 128, 128),
+                           ("qnorm_rope_kv_insert_fp8q_prefill_8192x16p64", 8192, 16, 64)):
+        case = W.random_insert(name, T, 528, 64, 2 * T // 64 + 2, 8192, 0.05, seed=3)
+        b = qside_bytes(case.slots, 528, H, Hp, q_out_bytes=512)
+        sets = device_sets(case, device, int(max(1, -(-320_000_000 // b))))
+        g = torch.Generator(device="cpu").manual_seed(0)
+        qs = torch.tensor([0.05], dtype=torch.float32, device=device)
+        for st in sets:
+            st["q"] = torch.randn(T, H, 512, generator=g).to(torch.bfloat16).to(device)
+            st["q_out"] = torch.empty(T, Hp, 512, dtype=torch.float8_e4m3fn, device=device)
+        ms = timed(lambda st: gkr.qnorm_rope_kv_insert(
+            st["q"], st["kv"], st["cache"], st["slots"], st["pos"], st["csc"], Hp, 1e-6, 64,
+            True, q_out=st["q_out"], q_scale=qs), sets)
+        res[name] = {"kernel": "qnorm_rope_kv_insert (e4m3 q_out)", "tokens": T, "heads": H,
+                     "heads_padded": Hp, "q_scale": 0.05, "us": ms * 1e3,
+                     "tokens_per_s": T / (ms * 1e-3), "alg_bytes": b,
+                     "alg_gbs": b / (ms * 1e-3) / 1e9,
+                     "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+                     "l2": f"{len(sets)} rotating input sets"}
         del sets
         torch.cuda.empty_cache()
 

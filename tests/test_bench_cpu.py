@@ -30,6 +30,9 @@ def test_algorithmic_bytes():
     # padded heads written (skipped slots still carry their query heads)
     assert bench.qside_bytes(slots, 528, 3, 8) == bench.insert_bytes(slots, 528) + 5 * 11 * 1024
     assert bench.qside_bytes(slots, 584, 0, 0) == bench.insert_bytes(slots, 584)
+    # an e4m3 query output writes 512 B per padded head
+    assert bench.qside_bytes(slots, 528, 3, 8, q_out_bytes=512) == \
+        bench.insert_bytes(slots, 528) + 5 * (3 * 1024 + 8 * 512)
     # cos/sin rows: one per distinct row among the written tokens (tokens 1 and 2 share
     # position 3's row; the skipped token's position 5 is not read)
     pos = np.array([3, 3, 3, 5, 11], np.int64)
