@@ -322,6 +322,7 @@ __device__ __forceinline__ uint32_t decode_compressed(const InsertParams& p, int
 template <int kRecord, int U>
 __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
     insert_staged_kernel(const InsertParams p) {
+    static_assert(U >= 1 && U <= 3, "one cp.async group per token, at most 3 in flight");
     extern __shared__ __align__(16) uint8_t smem[];
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
@@ -378,9 +379,8 @@ __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
                 cp_async16(dst + 1024 + 128 - 16 * 24, cs + 32);
             }
         }
+        cp_async_commit();   // one group per token (empty for a skipped one)
     }
-    cp_async_commit();
-    cp_async_wait<0>();  // this lane's copies have landed; each lane reads only its own
 
     uint8_t* const cache_a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
     uint8_t* const cache_s = p.cache + ScaleRows<kRecord>::lane_byte(lane);
@@ -388,6 +388,11 @@ __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
     for (int u = 0; u < U; ++u) {
         const int64_t o = __shfl_sync(kFull, off, u);
         const int64_t so = __shfl_sync(kFull, soff, u);
+        // token u's copies have landed (this lane's; each lane reads only its own), the
+        // later tokens' may still be on their way while this one is encoded
+        if (U - 1 - u == 0) cp_async_wait<0>();
+        else if (U - 1 - u == 1) cp_async_wait<1>();
+        else cp_async_wait<2>();
         if (o >= 0) {  // warp-uniform
             const uint8_t* src = ring_lane + u * kSlotBytes;
             TokenLoads L;
