@@ -32,13 +32,7 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
     return __ldcs(reinterpret_cast<const uint4*>(p));
 }
-// Read-only 16 / 8-byte loads through the non-coherent path.
-__device__ __forceinline__ uint4 ld_ro16(const void* p) {
-    return __ldg(reinterpret_cast<const uint4*>(p));
-}
-__device__ __forceinline__ uint2 ld_ro8(const void* p) {
-    return __ldg(reinterpret_cast<const uint2*>(p));
-}
+// Read-only 16-byte load through the non-coherent path.
 __device__ __forceinline__ float4 ld_ro_f4(const float* p) {
     return __ldg(reinterpret_cast<const float4*>(p));
 }

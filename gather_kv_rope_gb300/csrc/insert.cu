@@ -457,6 +457,8 @@ cudaError_t launch(const InsertParams& p, cudaStream_t stream) {
 #define GKR_SPARSE_BATCH 3
 #endif
 constexpr int kSparseBatch = GKR_SPARSE_BATCH;  // tokens staged at once by the compressed insert
+static_assert(kSparseBatch >= 1 && kSparseBatch <= 3,
+              "one cp.async group per staged token, at most 3 in flight");
 
 // The compressed insert: the grid is at most one wave, and each warp takes chunks of
 // `chunk` (<= 32) consecutive tokens, striding by the grid's token count.  In a chunk,
@@ -527,11 +529,14 @@ __global__ void __launch_bounds__(kThreads, GKR_SPARSE_MIN_BLOCKS)
                         cp_async16(dst + 1024 + 128 - 16 * 24, cs + 32);
                     }
                 }
+                cp_async_commit();   // one group per batch place (empty when unused)
             }
-            cp_async_commit();
-            cp_async_wait<0>();  // this lane's copies have landed; each lane reads only its own
 #pragma unroll
             for (int v = 0; v < kSparseBatch; ++v) {
+                // place v's copies have landed (this lane's; each lane reads only its own)
+                if (kSparseBatch - 1 - v == 0) cp_async_wait<0>();
+                else if (kSparseBatch - 1 - v == 1) cp_async_wait<1>();
+                else cp_async_wait<2>();
                 if (u[v] >= 0) {                         // warp-uniform
                     const int64_t o = __shfl_sync(kFull, off, u[v]);
                     const int64_t so = __shfl_sync(kFull, soff, u[v]);
