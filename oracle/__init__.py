@@ -30,6 +30,10 @@ Pinning status (what each function is checked against, on the CPU):
                            formula itself is a reading of the pages (they print only the
                            op's name and arguments): parity unpinned against the pages
                            for the norm, pinned for everything else.
+  e4m3 query output     -- closed-form codes of hand-built heads, the fp8 cache row
+                           it reduces to without the norm, the scale's edge cases.
+                           The scale's meaning (one fp32 divisor per call) is a
+                           reading: parity unpinned against the pages for it.
 """
 from __future__ import annotations
 

@@ -45,6 +45,10 @@
  *        q_head_padded, eps, apply_q_norm) removed; [P1] section "实现拆解" item 3
  *        and the attention.py listing call that op with q, the padded head count
  *        and eps beside the KV insert arguments.
+ *        The optional e4m3 query output casts each head as the plain fp8 cache
+ *        casts its rows; the pages name a query scale for the fp8 path but not its
+ *        meaning, so "one fp32 divisor per call" is a reading (parity unpinned
+ *        against the pages for the scale).
  * Readings where the pages are silent (exact scale rule, amax 0 -> byte 0,
  * RNE + saturation, fp32 RoPE op order, V4 page layout, pad byte 0, NaN
  * output pattern, out-of-range handling) are listed in the design notes.
