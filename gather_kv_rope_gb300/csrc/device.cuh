@@ -262,14 +262,72 @@ __device__ __forceinline__ float quotient_reciprocal(float s) {
     return (s >= 5.42101086e-20f && s <= 1.84467441e19f) ? __frcp_rn(s) : 0.0f;
 }
 
-// Eight values -> e4m3(x / scale): the IEEE fp32 quotient (nearest even) by the corrected
-// reciprocal y, then the saturating nearest-even e4m3 cast.
-__device__ __forceinline__ uint2 quantise8_div(const float* f, float scale, float y) {
+// Eight values -> e4m3(x / scale) by quotient() one value at a time.
+__device__ __forceinline__ uint2 quantise8_div_exact(const float* f, float scale, float y) {
     uint2 q;
     q.x = e4m3x4(quotient(f[0], scale, y), quotient(f[1], scale, y), quotient(f[2], scale, y),
                  quotient(f[3], scale, y));
     q.y = e4m3x4(quotient(f[4], scale, y), quotient(f[5], scale, y), quotient(f[6], scale, y),
                  quotient(f[7], scale, y));
+    return q;
+}
+
+// Two fp32 values in one 64-bit register pair (lo in the low half), for the two-wide
+// fp32 multiply and fused multiply-add: one instruction rounds each half to nearest
+// even exactly as the scalar instruction would, subnormals kept.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// True when one of the eight codes is an e4m3 NaN (low seven bits all ones): adding 1 to
+// each byte's low seven bits carries into its bit 7 only then, and never into the next
+// byte.
+__device__ __forceinline__ bool any_nan_code(uint2 q) {
+    const uint32_t a = (q.x & 0x7F7F7F7Fu) + 0x01010101u;
+    const uint32_t b = (q.y & 0x7F7F7F7Fu) + 0x01010101u;
+    return ((a | b) & 0x80808080u) != 0u;
+}
+
+// Eight values -> e4m3(x / scale): the IEEE fp32 quotient (nearest even) by the corrected
+// reciprocal y, then the saturating nearest-even e4m3 cast.  The steps of quotient() run
+// on the signed values with the negated reciprocal -y, two values per instruction:
+// p0 = RN(x (-y)), p' = RN(p + RN(x + p s) (-y)).  Nearest-even rounding is symmetric,
+// so every p is the exact negation of quotient()'s step for x, and flipping the sign
+// bit of each code gives the code of x / s.  Zeros come out with the sign opposite to
+// x's (+0 gives -0 at every step, -0 gives +0), so the flip gives them x's sign, as the
+// division does.  An input that is not finite, or a product x y that overflows, leaves
+// a NaN code; those eight values go through quotient() instead.
+__device__ __forceinline__ uint2 quantise8_div(const float* f, float scale, float y) {
+    const uint64_t s2 = f32x2(scale, scale);
+    const uint64_t n2 = f32x2(-y, -y);
+    float p[8];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        const uint64_t x = f32x2(f[i], f[i + 1]);
+        const uint64_t p0 = mul_f32x2(x, n2);
+        const uint64_t p1 = fma_f32x2(fma_f32x2(p0, s2, x), n2, p0);
+        const uint64_t p2 = fma_f32x2(fma_f32x2(p1, s2, x), n2, p1);
+        f32x2_split(p2, p[i], p[i + 1]);
+    }
+    uint2 q;
+    q.x = e4m3x4(p[0], p[1], p[2], p[3]) ^ 0x80808080u;
+    q.y = e4m3x4(p[4], p[5], p[6], p[7]) ^ 0x80808080u;
+    if (any_nan_code(q)) q = quantise8_div_exact(f, scale, y);
     return q;
 }
 
@@ -284,7 +342,7 @@ __device__ __forceinline__ bool exact_power_of_two(float s) {
 // Eight values -> e4m3(x / scale) for a power-of-two scale: with y = 1/scale exact, the
 // rounded product |x| * y is the rounded quotient, so one multiply per value replaces
 // the corrected reciprocal; the sign is carried as in quotient().
-__device__ __forceinline__ uint2 quantise8_pow2(const float* f, float y) {
+__device__ __forceinline__ uint2 quantise8_pow2_exact(const float* f, float y) {
     float q[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) q[i] = copysignf(__fmul_rn(fabsf(f[i]), y), f[i]);
@@ -292,6 +350,22 @@ __device__ __forceinline__ uint2 quantise8_pow2(const float* f, float y) {
     r.x = e4m3x4(q[0], q[1], q[2], q[3]);
     r.y = e4m3x4(q[4], q[5], q[6], q[7]);
     return r;
+}
+
+// The same two products per instruction: as in quantise8_div, each product is taken with
+// -y and each code's sign bit flipped, which gives zeros and underflows x's sign.  An
+// infinite product saturates to the largest code either way; a NaN input (a NaN code)
+// sends the eight values through the form above, whose NaN codes carry the input's sign.
+__device__ __forceinline__ uint2 quantise8_pow2(const float* f, float y) {
+    const uint64_t n2 = f32x2(-y, -y);
+    float p[8];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) f32x2_split(mul_f32x2(f32x2(f[i], f[i + 1]), n2), p[i], p[i + 1]);
+    uint2 q;
+    q.x = e4m3x4(p[0], p[1], p[2], p[3]) ^ 0x80808080u;
+    q.y = e4m3x4(p[4], p[5], p[6], p[7]) ^ 0x80808080u;
+    if (any_nan_code(q)) q = quantise8_pow2_exact(f, y);
+    return q;
 }
 
 // The same with one IEEE division per value (scales outside [2^-64, 2^64]).

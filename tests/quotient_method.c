@@ -7,8 +7,17 @@
  * elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
  * 1990), for scales in [2^-64, 2^64].  This program restates that method with C's fmaf
  * and compares the resulting e4m3 codes with those of the IEEE quotient |x| / s, over
- * every positive finite bf16 x and random fp32 x, for a list of scales.  It prints the
- * number of pairs and of code mismatches.
+ * every positive finite bf16 x and random fp32 x, for a list of scales.
+ *
+ * The kernels evaluate the same steps on the signed value with the negated reciprocal
+ * -y: p0 = RN(x (-y)), p' = RN(p + RN(x + p s) (-y)).  Each p is the exact negation of
+ * the step above for x (nearest-even rounding is symmetric), so the codes of x / s are
+ * those of p2 with the sign bit flipped; zeros come out with the opposite sign of x,
+ * which the flip turns into the sign of x.  A NaN code (a non-finite x, or a product
+ * that overflows) sends the value to the unsigned form with the sign carried.  The
+ * second check compares that form's signed codes with those of the IEEE quotient x / s
+ * over every finite and infinite bf16 x of both signs and random fp32 x of both signs.
+ * It prints the number of pairs and of code mismatches, summed over both checks.
  */
 #include <math.h>
 #include <stdint.h>
@@ -50,6 +59,30 @@ static float method(float a, float s, float y)
     return q2;
 }
 
+/* e4m3 code of any float, sign kept (NaN: sign | 0x7F) */
+static int e4m3_signed(float v)
+{
+    return (signbit(v) ? 0x80 : 0) | e4m3_code(fabsf(v));
+}
+
+/* The signed form with the negated reciprocal ny = -y, and its fallback. */
+static int method_signed_code(float x, float s, float y)
+{
+    float ny = -y;
+    float p0 = x * ny;
+    float p1 = fmaf(fmaf(p0, s, x), ny, p0);
+    float p2 = fmaf(fmaf(p1, s, x), ny, p1);
+    int code = e4m3_signed(p2) ^ 0x80;
+    if ((code & 0x7F) == 0x7F)
+        code = e4m3_signed(copysignf(method(fabsf(x), s, y), x));
+    return code;
+}
+
+static long long check_signed(float x, float s, float y)
+{
+    return e4m3_signed(x / s) != method_signed_code(x, s, y);
+}
+
 int main(int argc, char **argv)
 {
     int nscales = argc > 1 ? atoi(argv[1]) : 200, nrand = argc > 2 ? atoi(argv[2]) : 20000;
@@ -73,6 +106,17 @@ int main(int argc, char **argv)
             float a = f_of((uint32_t)(next() % 0x7F800000u));
             pairs++;
             if (e4m3_code(a / s) != e4m3_code(method(a, s, y))) bad++;
+        }
+        for (h = 0; h < 0x10000; h++) {         /* every bf16 but NaN, both signs */
+            float x = f_of(h << 16);
+            if (isnan(x)) continue;
+            pairs++;
+            bad += check_signed(x, s, y);
+        }
+        for (i = 0; i < nrand; i++) {            /* random finite fp32, both signs */
+            float x = f_of((uint32_t)(next() % 0x7F800000u) | (uint32_t)(next() & 1) << 31);
+            pairs++;
+            bad += check_signed(x, s, y);
         }
     }
     printf("%lld %lld\n", pairs, bad);

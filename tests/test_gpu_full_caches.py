@@ -167,6 +167,54 @@ def test_plain_cache_full_size(gkr, oracle_mod, record):
     assert int(err.item()) == ref_err == 0
 
 
+def _e4m3_midpoints() -> np.ndarray:
+    """The 126 midpoints between consecutive finite non-negative e4m3 values."""
+    v = np.array([0.0] + [m * 2.0 ** -9 for m in range(1, 8)] +
+                 [(1 + m / 8) * 2.0 ** (e - 7) for e in range(1, 16) for m in range(8)
+                  if not (e == 15 and m == 7)])
+    return (v[:-1] + v[1:]) / 2
+
+
+@pytest.mark.parametrize("scale", [3.0, 0.37, 2.0 ** -7, 1.0])
+def test_fp8_signed_zeros_ties_and_overflow(gkr, oracle_mod, scale):
+    """Values whose codes hinge on the quotient's sign handling and on its non-finite
+    fallback: +-0 (two whole rows and scattered entries), quotients that underflow to a
+    signed zero, exact e4m3 midpoints times the scale (ties to even; exact in bf16 at
+    scales 3, 2^-7 and 1), products x / scale that overflow fp32 (+-3e38), and +-inf in
+    dims 0..447; byte for byte against the oracle at general and power-of-two scales."""
+    T = 600
+    case = _case(T, 64, seed=31)
+    rng = np.random.default_rng(32)
+    s32 = float(np.float32(scale))
+    x = (rng.standard_normal((T, 512)) * 20 * s32).astype(np.float32)
+    x[0] = 0.0
+    x[1] = -0.0
+    flat = x.reshape(-1)
+    nope = np.flatnonzero(np.arange(flat.size) % 512 < 448)
+    nope = nope[nope >= 2 * 512]
+    cut = rng.permutation(nope)
+    sign = lambda k: np.where(rng.integers(0, 2, k) == 1, -1.0, 1.0)
+    mids = _e4m3_midpoints()
+    groups = [(1500, lambda k: sign(k) * 0.0),
+              (1500, lambda k: sign(k) * s32 * 2.0 ** -12),
+              (6000, lambda k: sign(k) * rng.choice(mids, k) * s32),
+              (300, lambda k: sign(k) * 3e38),
+              (200, lambda k: sign(k) * np.inf)]
+    at = 0
+    for k, make in groups:
+        flat[cut[at:at + k]] = make(k).astype(np.float32)
+        at += k
+    rope = np.flatnonzero(np.arange(flat.size) % 512 >= 448)   # zeros and huge values there too
+    cut = rng.permutation(rope[rope >= 2 * 512])
+    flat[cut[:500]] = (sign(500) * 0.0).astype(np.float32)
+    flat[cut[500:600]] = (sign(100) * 3e38).astype(np.float32)
+    case.kv = W.to_bf16_bits(x)
+    assert int((case.kv == 0x8000).sum()) > 1000 and int((case.kv == 0xFF80).sum()) > 50
+    cache, got, ref, err, ref_err, ps = _insert(gkr, oracle_mod, case, 512, s32)
+    n, first = first_mismatch(got, ref)
+    assert n == 0 and err == ref_err == 0, f"scale={scale}: {n} bytes differ, first {first}"
+
+
 @pytest.mark.parametrize("scale", [1e-30, 2.0 ** -64, float(np.nextafter(np.float32(2.0 ** -64), 0)),
                                    2.0 ** 64, float(np.nextafter(np.float32(2.0 ** 64), np.inf)),
                                    1e30, 7.0 / 3.0, 1.0, 2.0 ** -126, 2.0 ** 126, 2.0 ** 127,
