@@ -16,11 +16,15 @@
 //     token +0 and GKR_ERR_POS;
 //   the KV row: as gkr_kv_insert (slot -1 skips it).
 //
-// Launch shape: rows of 512 dims, one warp per row at a time and two rows per warp (the
-// lane layout of device.cuh).  Token t owns rows t*(Hp+1) .. t*(Hp+1)+Hp: first its KV
-// row, then its Hp query heads, so a warp's rows are consecutive in q_in / q_out and the
-// grid depends only on T * (Hp + 1).  Lanes 0..1 decode their row (token, kind, slot,
+// Launch shape: two block ranges.  The first covers rows of 512 dims, one warp per row at
+// a time and two rows per warp (the lane layout of device.cuh).  Token t owns rows
+// t*(H+1) .. t*(H+1)+H: first its KV row, then its H query heads, so a warp's rows are
+// consecutive in q_in / q_out.  Lanes 0..1 decode their row (token, kind, slot,
 // position) in parallel; every row's loads are issued before the first is converted.
+// The second range writes the padded heads H .. Hp-1, which are zeros whatever the
+// inputs: one contiguous span of (Hp - H) rows per token in q_out, cut into 512-byte
+// pieces (16 bytes per lane), 16 consecutive pieces per warp.  A padded head thus costs
+// one or two store instructions, not a warp of its own.
 #include "device.cuh"
 #include "encode.cuh"
 #include "launch.h"
@@ -30,6 +34,7 @@ namespace gkr {
 namespace {
 
 constexpr int kRowsPerWarp = 2;
+constexpr int kZeroPieces = 16;   // 512-byte pieces of padded heads per warp
 
 #ifndef GKR_QSIDE_MIN_BLOCKS
 #define GKR_QSIDE_MIN_BLOCKS 4
@@ -39,27 +44,40 @@ enum RowKind : int32_t { kNone = 0, kKvRow = 1, kQHead = 2, kZeroHead = 3 };
 
 // One query head on one warp: chunks A and B of the head (16 bf16 per lane) -> normed
 // (optionally) and rotated -> 16 fp32 values per lane.  The sum of squares is taken per
-// lane in dim order, then over the warp by a butterfly (every lane ends with the same
-// sum); mean = sum * 2^-9 (exact); factor = the correctly rounded 1/sqrt(mean + eps);
-// every operation is one fp32 operation rounded to nearest even (no contraction).
+// lane in two fp32 accumulators (the lane's even and odd dims) by fused multiply-adds,
+// two per instruction, then the two are added and summed over the warp by a butterfly
+// (every lane ends with the same sum); mean = sum * 2^-9 (exact); factor = the correctly
+// rounded 1/sqrt(mean + eps); each value times the factor is one rounded product, two per
+// instruction.  Every sum of squares so formed goes through at most 14 roundings, and the
+// results stay within the fp32-evaluation range of the exact values.
 __device__ __forceinline__ void q_head(const uint4 ta, const uint4 tb, const float4 c,
                                        const float4 s, bool norm, float eps, int lane,
                                        float (&a)[8], float (&b)[8]) {
     unpack_bf16x8(ta, a);
     unpack_bf16x8(tb, b);
     if (norm) {
-        float ss = 0.0f;
+        uint64_t acc = mul_f32x2(f32x2(a[0], a[1]), f32x2(a[0], a[1]));
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(a[i], a[i]));
+        for (int i = 2; i < 8; i += 2) {
+            const uint64_t x = f32x2(a[i], a[i + 1]);
+            acc = fma_f32x2(x, x, acc);
+        }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(b[i], b[i]));
+        for (int i = 0; i < 8; i += 2) {
+            const uint64_t x = f32x2(b[i], b[i + 1]);
+            acc = fma_f32x2(x, x, acc);
+        }
+        float even, odd;
+        f32x2_split(acc, even, odd);
+        float ss = __fadd_rn(even, odd);
 #pragma unroll
         for (int x = 16; x >= 1; x >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, x));
         const float r = __frsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / 512.0f), eps));
+        const uint64_t r2 = f32x2(r, r);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            a[i] = __fmul_rn(a[i], r);
-            b[i] = __fmul_rn(b[i], r);
+        for (int i = 0; i < 8; i += 2) {
+            f32x2_split(mul_f32x2(f32x2(a[i], a[i + 1]), r2), a[i], a[i + 1]);
+            f32x2_split(mul_f32x2(f32x2(b[i], b[i + 1]), r2), b[i], b[i + 1]);
         }
     }
     if (lane >= 24) rope4(b, c, s);   // dims 448..511 = pairs 4(L-24) .. 4(L-24)+3
@@ -82,28 +100,75 @@ __device__ __forceinline__ void st_stream8(void* p, uint2 v) {
     __stcs(reinterpret_cast<uint2*>(p), v);
 }
 
+// 512-byte pieces of padded heads per token.
+__host__ __device__ __forceinline__ int64_t zero_pieces_per_token(const QSideParams& qp,
+                                                                   bool fp8q) {
+    return static_cast<int64_t>(qp.num_heads_padded - qp.num_heads) * (fp8q ? 1 : 2);
+}
+
+// Heads H .. Hp-1 of every token (bytes [(t*Hp + H) * rb, (t*Hp + Hp) * rb) of q_out, rb
+// the row's bytes): warp w of the range writes pieces 16w .. 16w+15 of the spans taken
+// token after token, each piece 512 bytes at 16 per lane.
+template <bool kFp8Q>
+__device__ __forceinline__ void zero_padded_heads(const QSideParams& qp, int64_t num_tokens,
+                                                  int64_t block, int lane) {
+    constexpr int64_t kRowBytes = kFp8Q ? 512 : 1024;
+    const int64_t per_token = zero_pieces_per_token(qp, kFp8Q);
+    const int64_t total = num_tokens * per_token;
+    const int64_t k0 = (block * kWarpsPerBlock + (threadIdx.x >> 5)) * kZeroPieces;
+    if (k0 >= total) return;  // warp-uniform
+    pdl_wait_previous();
+    pdl_release_next();
+    int64_t t = k0 / per_token;
+    int64_t w = k0 - t * per_token;
+    uint8_t* const out = static_cast<uint8_t*>(qp.q_out) + qp.num_heads * kRowBytes + 16 * lane;
+    const int64_t n = total - k0;
+#pragma unroll
+    for (int i = 0; i < kZeroPieces; ++i) {
+        if (i < n) st_stream16(out + t * qp.num_heads_padded * kRowBytes + w * 512,
+                               make_uint4(0u, 0u, 0u, 0u));
+        if (++w == per_token) {
+            w = 0;
+            ++t;
+        }
+    }
+}
+
 template <int kRecord, bool kFp8Q>
 __global__ void __launch_bounds__(kThreads, GKR_QSIDE_MIN_BLOCKS)
-    qnorm_rope_kv_insert_kernel(const InsertParams p, const QSideParams qp) {
+    qnorm_rope_kv_insert_kernel(const InsertParams p, const QSideParams qp,
+                                const int64_t blocks_of_rows) {
     constexpr int U = kRowsPerWarp;
     constexpr uint32_t D = Fmt<kRecord>::D;
     constexpr uint32_t S = Fmt<kRecord>::S;
     const int lane = threadIdx.x & 31;
-    const int64_t per_token = static_cast<int64_t>(qp.num_heads_padded) + 1;
+    if (blockIdx.x >= blocks_of_rows) {  // block-uniform: a block of padded heads
+        zero_padded_heads<kFp8Q>(qp, p.num_tokens, blockIdx.x - blocks_of_rows, lane);
+        return;
+    }
+    const int64_t per_token = static_cast<int64_t>(qp.num_heads) + 1;
     const int64_t n_rows = p.num_tokens * per_token;
     const int64_t r0 = (static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5)) * U;
     if (r0 >= n_rows) return;  // warp-uniform
 
     // lane u < U decodes row r0 + u: its token and kind (j = 0: the KV row; 1..H: query
-    // head j - 1; H+1..Hp: a padded head)
+    // head j - 1)
     const bool mine = lane < U && r0 + lane < n_rows;
     int64_t t = 0;
     int32_t j = -1;
     if (mine) {
-        t = (r0 + lane) / per_token;
-        j = static_cast<int32_t>(r0 + lane - t * per_token);
+        if (n_rows <= 0xFFFFFFFFll) {  // uniform: the 32-bit division is a fraction of the 64-bit one
+            const uint32_t r = static_cast<uint32_t>(r0 + lane);
+            const uint32_t pt = static_cast<uint32_t>(per_token);
+            const uint32_t tt = r / pt;
+            t = tt;
+            j = static_cast<int32_t>(r - tt * pt);
+        } else {
+            t = (r0 + lane) / per_token;
+            j = static_cast<int32_t>(r0 + lane - t * per_token);
+        }
     }
-    const bool reads_pos = mine && j <= qp.num_heads;   // the KV row and the query heads
+    const bool reads_pos = mine;   // the KV row and the query heads
     int64_t slot = -1, q = 0;
     if (p.early_metadata != 0 && reads_pos) {
         if (j == 0) slot = __ldg(p.slots + t);
@@ -143,16 +208,12 @@ __global__ void __launch_bounds__(kThreads, GKR_QSIDE_MIN_BLOCKS)
                     }
                 }
             }
-        } else if (j <= qp.num_heads) {
-            if (q < 0 || q >= p.max_pos) {
-                err = 2;
-                kind = kZeroHead;
-            } else {
-                pos = static_cast<int32_t>(q);
-                kind = kQHead;
-            }
-        } else {
+        } else if (q < 0 || q >= p.max_pos) {
+            err = 2;
             kind = kZeroHead;
+        } else {
+            pos = static_cast<int32_t>(q);
+            kind = kQHead;
         }
     }
     // the e4m3 query output's scale, read once by a warp with query heads; one that is not
@@ -241,14 +302,17 @@ __global__ void __launch_bounds__(kThreads, GKR_QSIDE_MIN_BLOCKS)
 template <int kRecord>
 cudaError_t launch(const InsertParams& p, const QSideParams& qp, cudaStream_t stream) {
     if (p.num_tokens <= 0) return cudaSuccess;
-    const int64_t rows = p.num_tokens * (static_cast<int64_t>(qp.num_heads_padded) + 1);
+    const int64_t rows = p.num_tokens * (static_cast<int64_t>(qp.num_heads) + 1);
     const int64_t per_block = static_cast<int64_t>(kWarpsPerBlock) * kRowsPerWarp;
-    const int64_t blocks = (rows + per_block - 1) / per_block;
+    const int64_t pieces = p.num_tokens * zero_pieces_per_token(qp, qp.q_scale != nullptr);
+    const int64_t zero_per_block = static_cast<int64_t>(kWarpsPerBlock) * kZeroPieces;
+    const int64_t row_blocks = (rows + per_block - 1) / per_block;
+    const int64_t blocks = row_blocks + (pieces + zero_per_block - 1) / zero_per_block;
     return qp.q_scale != nullptr
                ? launch_kernel(qnorm_rope_kv_insert_kernel<kRecord, true>, blocks, kThreads, 0,
-                               stream, p.pdl, p, qp)
+                               stream, p.pdl, p, qp, row_blocks)
                : launch_kernel(qnorm_rope_kv_insert_kernel<kRecord, false>, blocks, kThreads, 0,
-                               stream, p.pdl, p, qp);
+                               stream, p.pdl, p, qp, row_blocks);
 }
 
 }  // namespace

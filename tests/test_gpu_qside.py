@@ -285,3 +285,36 @@ def test_fp8_q_bad_scale_zeroes_the_heads(gkr, oracle_mod, bad):
                                                        528, bad)
     assert first_mismatch(got, ref)[0] == 0
     assert (qo == 0).all() and err == ref_err == gkr.ERR_SCALE
+
+
+@pytest.mark.parametrize("fp8q", [False, True])
+@pytest.mark.parametrize("T,H,Hp", [(37, 3, 8), (33, 0, 5), (129, 7, 23)])
+def test_padded_heads_stay_inside_q_out(gkr, oracle_mod, fp8q, T, H, Hp):
+    """The padded heads are written in 512-byte pieces, 16 per warp, across token
+    boundaries: every padded head of q_out is +0, the query heads match the oracle, and
+    the rows just before and after q_out (q_out is a view into a larger buffer) keep their
+    fill."""
+    c, q = _q_case(T, H, seed=T + H + Hp)
+    kv, slots, pos, csc = device_inputs(c, DEV)
+    cache = gkr.alloc_cache(c.num_pages, c.block_size, 528, DEV, fill=SENTINEL)
+    dtype = torch.uint8 if fp8q else torch.int16
+    fill = 0x5A if fp8q else 0x5A5A
+    big = torch.full((T + 2, Hp, 512), fill, dtype=dtype, device=DEV)
+    q_out = big[1:T + 1] if fp8q else big[1:T + 1].view(torch.bfloat16)
+    qs = torch.tensor([0.03], dtype=torch.float32, device=DEV) if fp8q else None
+    gkr.qnorm_rope_kv_insert(bf16_from_bits(q, DEV), kv, cache, slots, pos, csc, Hp, 1e-6,
+                             c.block_size, True, q_out=q_out, record=528, q_scale=qs)
+    torch.cuda.synchronize()
+    b = big.cpu()
+    assert (b[0] == fill).all() and (b[T + 1] == fill).all()
+    got = b[1:T + 1].numpy()
+    assert (got[:, H:] == 0).all()
+    if fp8q:
+        rn, lo, hi, _ = oracle_mod.qnorm_rope_fp8q(q, Hp, 1e-6, True, np.float32(0.03),
+                                                   c.positions, c.csc)
+        _assert_codes(got, rn, lo, hi)
+    else:
+        ref = np.full(c.num_pages * oracle_mod.page_stride(528, c.block_size), SENTINEL, np.uint8)
+        rn, lo, hi, _ = _oracle(oracle_mod, q, Hp, 1e-6, True, c, ref, 528,
+                                oracle_mod.page_stride(528, c.block_size))
+        _assert_faithful(got.view(np.uint16), rn, (lo, hi))
