@@ -124,14 +124,6 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
     return lo | (hi << 16);
 }
 
-// Quantise 8 values with their block's scale byte -> 8 e4m3 bytes.
-__device__ __forceinline__ uint2 quantise8(const float* f, uint32_t byte) {
-    const float k = inv_scale(byte);
-    uint2 q;
-    q.x = e4m3x4(__fmul_rn(f[0], k), __fmul_rn(f[1], k), __fmul_rn(f[2], k), __fmul_rn(f[3], k));
-    q.y = e4m3x4(__fmul_rn(f[4], k), __fmul_rn(f[5], k), __fmul_rn(f[6], k), __fmul_rn(f[7], k));
-    return q;
-}
 
 // ---------------------------------------------------------------- MXFP8 decode
 
@@ -292,6 +284,29 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
+}
+
+// Quantise 8 values with their block's scale byte -> 8 e4m3 bytes: each value times the
+// exact power of two 2^(127 - byte), one rounded product, then the saturating nearest-
+// even cast.  kPacked: two products per instruction (the same results); the scalar form
+// is for kernels at a tight register budget, where the register pairs cost a spill.
+template <bool kPacked = true>
+__device__ __forceinline__ uint2 quantise8(const float* f, uint32_t byte) {
+    const float k = inv_scale(byte);
+    float p[8];
+    if constexpr (kPacked) {
+        const uint64_t k2 = f32x2(k, k);
+#pragma unroll
+        for (int i = 0; i < 8; i += 2)
+            f32x2_split(mul_f32x2(f32x2(f[i], f[i + 1]), k2), p[i], p[i + 1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p[i] = __fmul_rn(f[i], k);
+    }
+    uint2 q;
+    q.x = e4m3x4(p[0], p[1], p[2], p[3]);
+    q.y = e4m3x4(p[4], p[5], p[6], p[7]);
+    return q;
 }
 
 // True when one of the eight codes is an e4m3 NaN (low seven bits all ones): adding 1 to

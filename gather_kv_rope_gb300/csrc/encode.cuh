@@ -29,8 +29,9 @@ struct TokenLoads {
 
 // V4.1: 16 blocks of 32 dims.  Chunk A of lane L is in block L/4, chunk B in 8 + L/4.
 // `da` = data row + 8L (chunk B's codes go to da + 256); `sl` = scale row + L/4.
-// kSanitize: NaN -> +0 over the whole rotated row before the block maxima.
-template <bool kSanitize = false>
+// kSanitize: NaN -> +0 over the whole rotated row before the block maxima.  kPackedQ:
+// quantise8's two-wide products (see there).
+template <bool kSanitize = false, bool kPackedQ = true>
 __device__ __forceinline__ void encode_store_v41(const TokenLoads& L, uint8_t* da, uint8_t* sl,
                                                  int lane) {
     float a[8], b[8];
@@ -49,8 +50,8 @@ __device__ __forceinline__ void encode_store_v41(const TokenLoads& L, uint8_t* d
     mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 2));
     const uint32_t ba = ue8m0_byte(ma), bb = ue8m0_byte(mb);
 
-    st8(da, quantise8(a, ba));
-    st8(da + 256, quantise8(b, bb));
+    st8(da, quantise8<kPackedQ>(a, ba));
+    st8(da + 256, quantise8<kPackedQ>(b, bb));
     if ((lane & 3) == 0) {
         sl[0] = static_cast<uint8_t>(ba);
         sl[8] = static_cast<uint8_t>(bb);
@@ -61,7 +62,7 @@ __device__ __forceinline__ void encode_store_v41(const TokenLoads& L, uint8_t* d
 // in block 4 + L/8), rotated dims 448..511 (chunk B of lanes 24..31) stored as bf16.
 // `da` = data row + 8L; `sl` = scale row + L/8 (all 8 bytes of the row are written,
 // the pad byte 7 by lane 24).
-template <bool kSanitize = false>
+template <bool kSanitize = false, bool kPackedQ = true>
 __device__ __forceinline__ void encode_store_v4(const TokenLoads& L, uint8_t* da, uint8_t* sl,
                                                 int lane) {
     float a[8], b[8];
@@ -82,9 +83,9 @@ __device__ __forceinline__ void encode_store_v4(const TokenLoads& L, uint8_t* da
     }
     const uint32_t ba = ue8m0_byte(ma), bb = ue8m0_byte(mb);
 
-    st8(da, quantise8(a, ba));
+    st8(da, quantise8<kPackedQ>(a, ba));
     if (!rope_lane) {
-        st8(da + 256, quantise8(b, bb));
+        st8(da + 256, quantise8<kPackedQ>(b, bb));
     } else {  // dims 448 + 8(L-24) .. as bf16 at data + 448 + 16(L-24) = da + 64 + 8L
         st16(da + 64 + 8 * lane,
              make_uint4(pack_bf16x2_rn(b[0], b[1]), pack_bf16x2_rn(b[2], b[3]),
@@ -157,11 +158,11 @@ __device__ __forceinline__ void encode_store_fp8(const TokenLoads& L, uint8_t* d
     st8(da + 256, quantise8_div(b, sc.s, sc.y));
 }
 
-template <int kRecord, bool kSanitize = false>
+template <int kRecord, bool kSanitize = false, bool kPackedQ = true>
 __device__ __forceinline__ void encode_store(const TokenLoads& L, uint8_t* da, uint8_t* sl,
                                              int lane, Scale sc) {
-    if constexpr (kRecord == 528) encode_store_v41<kSanitize>(L, da, sl, lane);
-    else if constexpr (kRecord == 584) encode_store_v4<kSanitize>(L, da, sl, lane);
+    if constexpr (kRecord == 528) encode_store_v41<kSanitize, kPackedQ>(L, da, sl, lane);
+    else if constexpr (kRecord == 584) encode_store_v4<kSanitize, kPackedQ>(L, da, sl, lane);
     else if constexpr (kRecord == 1024) encode_store_bf16(L, da, lane);
     else encode_store_fp8(L, da, lane, sc);
 }

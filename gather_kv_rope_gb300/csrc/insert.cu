@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, GKR_SHORT_MIN_BLOCKS)
     for (int u = 0; u < U; ++u) {
         const int64_t o = __shfl_sync(kFull, off, u);
         const int64_t so = __shfl_sync(kFull, soff, u);
-        if (valid[u]) encode_store<kRecord>(L[u], cache_a + o, cache_s + so, lane, scale);
+        // scalar products: at 48 registers the two-wide form spills here
+        if (valid[u]) encode_store<kRecord, false, false>(L[u], cache_a + o, cache_s + so, lane, scale);
     }
 }
 
