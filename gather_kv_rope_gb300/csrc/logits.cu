@@ -16,8 +16,10 @@
 //   * A, the query's heads (up to 128, zero-padded; M = 128 x K = 512, bf16), lives in
 //     tensor memory next to the two accumulators, so shared memory is left to the records.
 //     The 4 epilogue warps write it (tcgen05.st) at launch and when the run reaches a new
-//     query, once the products that read the old one are done; one thread prefetches the
-//     run's query tiles into L2 at launch.
+//     query, once the products that read the old one are done, and signal each half of K
+//     as soon as it is written, so that the new query's first low-half products start
+//     while the high half is loaded; one thread prefetches the run's query tiles into L2
+//     at launch.
 //   * 16 producer warps, 4 keys of each 64-key group each: a ring of raw records per warp
 //     in shared memory, filled with cp.async two groups ahead (the loads in flight cost no
 //     registers); each group is dequantised twice, its low 256 dims and then its high 256,
@@ -238,7 +240,8 @@ struct alignas(8) Barriers {
     uint64_t empty[kStages];     // MMA -> producers: the stage's products are done
     uint64_t acc_full[2];        // MMA -> epilogue: an item's accumulator is complete
     uint64_t acc_empty[2];       // epilogue -> MMA: the accumulator has been read
-    uint64_t a_ready;            // epilogue -> MMA: A holds the next query
+    uint64_t a_ready[2];         // epilogue -> MMA: A's low / high half of K holds the
+                                 // next query
     uint32_t tmem_base;
     int32_t timed_out;
 };
@@ -372,11 +375,15 @@ __device__ __forceinline__ uint4 convert_half(const uint8_t* src, bool valid, in
 
 // The epilogue warp's quarter of A: lane L writes row h0 + L = head h0 + L of query qi
 // (zeros past num_heads) into tensor memory at `dst` (its lanes, A's first column), 16
-// columns (32 bf16) a step, the next step's loads in flight during each store; then it
-// makes the stores visible to the tensor cores and arrives on `ready`.  Kept out of line:
+// columns (32 bf16) a step, the next step's loads in flight during each store (a deeper
+// register ring spills at the call).
+// After the first 8 steps (dims 0..255, the low half of K) it makes them visible to the
+// tensor cores and arrives on `ready_lo`, so that the products of a low-half stage may
+// start while the high half is loaded; after the last, on `ready_hi`.  Kept out of line:
 // its registers would otherwise add to the drain loop's.
 __device__ __noinline__ void load_a(const uint8_t* qbase, int64_t qi, int32_t num_heads, int h0,
-                                    int lane, bool live, uint32_t dst, uint32_t ready) {
+                                    int lane, bool live, uint32_t dst, uint32_t ready_lo,
+                                    uint32_t ready_hi) {
     const uint4* const row =
         reinterpret_cast<const uint4*>(qbase + (qi * num_heads + h0 + lane) * 1024);
     uint4 cur[4], nxt[4];
@@ -390,12 +397,17 @@ __device__ __noinline__ void load_a(const uint8_t* qbase, int64_t qi, int32_t nu
                 nxt[i] = live ? __ldg(row + 4 * (b + 1) + i) : make_uint4(0u, 0u, 0u, 0u);
         }
         tmem_st16(dst + 16 * b, cur);
+        if (b == 7) {
+            tmem_st_wait();
+            tc_fence_before_sync();
+            warp_arrive(ready_lo, lane);
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
     }
     tmem_st_wait();
     tc_fence_before_sync();
-    warp_arrive(ready, lane);
+    warp_arrive(ready_hi, lane);
 }
 
 template <int kRecord>
@@ -431,7 +443,8 @@ __global__ void __launch_bounds__(kLogitThreads, 1)
             mbar_init(smem_addr(&bars->acc_full[a]), 1);
             mbar_init(smem_addr(&bars->acc_empty[a]), kEpilogueWarps);
         }
-        mbar_init(smem_addr(&bars->a_ready), kEpilogueWarps);
+        mbar_init(smem_addr(&bars->a_ready[0]), kEpilogueWarps);
+        mbar_init(smem_addr(&bars->a_ready[1]), kEpilogueWarps);
         bars->timed_out = 0;
         mbar_init_fence();
     }
@@ -549,15 +562,21 @@ __global__ void __launch_bounds__(kLogitThreads, 1)
                 const int a = static_cast<int>(u & 1);
                 if (u >= 2) wait_or_flag(smem_addr(&bars->acc_empty[a]), ((u >> 1) - 1) & 1, ok);
                 const int64_t qi = item / p.chunks;
-                if (qi != cur_q) {   // A is rewritten for each new query of the run
-                    wait_or_flag(smem_addr(&bars->a_ready), loads & 1, ok);
-                    ++loads;
+                // A is rewritten for each new query of the run: the item's first stage of
+                // each half of K waits for that half of A
+                uint32_t need = 0u;
+                if (qi != cur_q) {
+                    need = 3u;
                     cur_q = qi;
                 }
-                tc_fence_after_sync();
                 for (int t = 0; t < kTiles; ++t, ++j) {
                     const int s = static_cast<int>(j % kStages);
                     const int h = t & 1;   // half of K: the group's products accumulate both
+                    if ((need >> h) & 1u) {
+                        wait_or_flag(smem_addr(&bars->a_ready[h]), loads & 1, ok);
+                        need &= ~(1u << h);
+                        if (h == 1) ++loads;
+                    }
                     wait_or_flag(smem_addr(&bars->full[s]), (j / kStages) & 1, ok);
                     tc_fence_after_sync();
                     const uint32_t d = tmem + a * kChunk + (t >> 1) * kN;
@@ -588,9 +607,9 @@ __global__ void __launch_bounds__(kLogitThreads, 1)
         const uint8_t* const qbase = static_cast<const uint8_t*>(p.q);
         const bool live = h0 + lane < p.num_heads;   // this lane's head exists
         const bool stores = h0 < p.num_heads;        // this warp has heads to store
-        const uint32_t a_ready = smem_addr(&bars->a_ready);
+        const uint32_t a_lo = smem_addr(&bars->a_ready[0]), a_hi = smem_addr(&bars->a_ready[1]);
         const uint32_t a_dst = tmem + lanes + kACol;
-        if (i0 < i1) load_a(qbase, i0 / p.chunks, p.num_heads, h0, lane, live, a_dst, a_ready);
+        if (i0 < i1) load_a(qbase, i0 / p.chunks, p.num_heads, h0, lane, live, a_dst, a_lo, a_hi);
         for (int64_t item = i0; item < i1; ++item) {
             const int64_t v = item - i0;
             const int a = static_cast<int>(v & 1);
@@ -613,7 +632,7 @@ __global__ void __launch_bounds__(kLogitThreads, 1)
             warp_wait_or_flag(smem_addr(&bars->acc_full[a]), (v >> 1) & 1, ok, lane);
             tc_fence_after_sync();
             // every product of this item is done, so A may take the next query now
-            if (next_query) load_a(qbase, qi + 1, p.num_heads, h0, lane, live, a_dst, a_ready);
+            if (next_query) load_a(qbase, qi + 1, p.num_heads, h0, lane, live, a_dst, a_lo, a_hi);
 #pragma unroll 1
             for (int c = 0; c < kChunk; c += kTileCols) {
                 // bit j: entry k0 + c + j is a record (lane j read its index)
