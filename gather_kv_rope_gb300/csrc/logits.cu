@@ -586,12 +586,20 @@ __global__ void __launch_bounds__(kLogitThreads, 1)
                     wait_or_flag(smem_addr(&bars->full[s]), (j / kStages) & 1, ok);
                     tc_fence_after_sync();
                     const uint32_t d = tmem + a * kChunk + (t >> 1) * kN;
-                    const uint32_t b0 = smem_addr(sB + s * kBBytes);
+                    // the stage's descriptor once; each K step adds its offset / 16 to the
+                    // start-address field (bits 0-13), which cannot carry: every stage lies
+                    // below 227 KB, so address / 16 < 2^14
+                    const uint64_t desc0 = sw128_desc(smem_addr(sB + s * kBBytes));
+                    const uint32_t lo = static_cast<uint32_t>(desc0);
+                    const uint32_t hi = static_cast<uint32_t>(desc0 >> 32);
+                    const uint32_t a0 = tmem + kACol + (kHalfK / 2) * h;
 #pragma unroll
-                    for (int k = 0; k < kHalfK / 16; ++k)   // K = 16 per instruction
-                        mma_bf16_ts(d, tmem + kACol + (kHalfK / 2) * h + 8 * k,
-                                    sw128_desc(b0 + (k >> 2) * kN * kRowBytes + (k & 3) * 32),
-                                    kIdesc, (h | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < kHalfK / 16; ++k) {   // K = 16 per instruction
+                        const uint32_t step = ((k >> 2) * kN * kRowBytes + (k & 3) * 32) >> 4;
+                        mma_bf16_ts(d, a0 + 8 * k,
+                                    (static_cast<uint64_t>(hi) << 32) | (lo + step), kIdesc,
+                                    (h | k) != 0 ? 1u : 0u);
+                    }
                     mma_commit(smem_addr(&bars->empty[s]));
                 }
                 mma_commit(smem_addr(&bars->acc_full[a]));
