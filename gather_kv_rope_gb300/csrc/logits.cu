@@ -562,19 +562,18 @@ __global__ void __launch_bounds__(kLogitThreads, 1)
         // ------------------------------------------------------------- MMA issue
         if (lane == 0) {
             uint32_t j = 0, loads = 0;
-            int64_t cur_q = -1;
-            for (int64_t item = i0; item < i1; ++item) {
+            // the item's chunk within its query, counted rather than divided per item (a
+            // 64-bit division costs this warp, which shares its scheduler with four producers,
+            // more issue slots than the item's products)
+            int64_t chunk = i0 % p.chunks;
+            for (int64_t item = i0; item < i1; ++item, ++chunk) {
                 const int64_t u = item - i0;
                 const int a = static_cast<int>(u & 1);
                 if (u >= 2) wait_or_flag(smem_addr(&bars->acc_empty[a]), ((u >> 1) - 1) & 1, ok);
-                const int64_t qi = item / p.chunks;
+                if (chunk == p.chunks) chunk = 0;
                 // A is rewritten for each new query of the run: the item's first stage of
                 // each half of K waits for that half of A
-                uint32_t need = 0u;
-                if (qi != cur_q) {
-                    need = 3u;
-                    cur_q = qi;
-                }
+                uint32_t need = (u == 0 || chunk == 0) ? 3u : 0u;
                 for (int t = 0; t < kTiles; ++t, ++j) {
                     const int s = static_cast<int>(j % kStages);
                     const int h = t & 1;   // half of K: the group's products accumulate both
@@ -624,12 +623,16 @@ __global__ void __launch_bounds__(kLogitThreads, 1)
         const uint32_t a_lo = smem_addr(&bars->a_ready[0]), a_hi = smem_addr(&bars->a_ready[1]);
         const uint32_t a_dst = tmem + lanes + kACol;
         if (i0 < i1) load_a(qbase, i0 / p.chunks, p.num_heads, h0, lane, live, a_dst, a_lo, a_hi);
-        for (int64_t item = i0; item < i1; ++item) {
+        int64_t qi = i0 / p.chunks, chunk = i0 - qi * p.chunks;   // counted, not divided, per item
+        for (int64_t item = i0; item < i1; ++item, ++chunk) {
             const int64_t v = item - i0;
             const int a = static_cast<int>(v & 1);
-            const int64_t qi = item / p.chunks;
-            const int64_t k0 = (item % p.chunks) * kChunk;
-            const bool next_query = item + 1 < i1 && (item + 1) / p.chunks != qi;
+            if (chunk == p.chunks) {
+                chunk = 0;
+                ++qi;
+            }
+            const int64_t k0 = chunk * kChunk;
+            const bool next_query = item + 1 < i1 && chunk + 1 == p.chunks;
             if (next_query && live) {   // warm L2 with the next query's rows
                 const uint8_t* const nrow = qbase + ((qi + 1) * p.num_heads + h0 + lane) * 1024;
 #pragma unroll
