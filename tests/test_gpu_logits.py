@@ -124,6 +124,28 @@ def test_many_queries_per_cta(gkr, oracle_mod, record):
     assert int(err.item()) == ref_err
 
 
+@pytest.mark.parametrize("record", [528, 512])
+def test_one_chunk_per_query(gkr, oracle_mod, record):
+    """700 queries of 100 entries: one item per query, several per CTA, so every item
+    starts a new query (the chunk count wraps at each item) and reloads the query tile."""
+    bs, pages, Q, H, K = 64, 40, 700, 16, 100
+    scale = 0.05 if record == 512 else None
+    c, flat, ps = _host_cache(oracle_mod, record, pages * bs, bs, pages, seed=31, scale=scale)
+    rng = np.random.default_rng(32)
+    idx = _indices(rng, Q, K, np.arange(pages * bs), bad_rate=0.01, num_slots=pages * bs)
+    q = bf16_bits(rng.standard_normal((Q, H, 512)).astype(np.float32))
+    cache = _to_device_cache(gkr, flat, pages, bs, record, ps)
+    kw = {} if scale is None else {"fp8_scale": torch.tensor([scale], dtype=torch.float32, device=DEV)}
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = gkr.sparse_logits(torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).to(DEV),
+                            cache, torch.from_numpy(idx).to(DEV), 0.07, err_flag=err, **kw)
+    torch.cuda.synchronize()
+    exact, bound, ref_err = oracle_mod.sparse_logits(q, flat, record, bs, pages, ps, idx, 0.07,
+                                                     fp8_scale=scale)
+    _check(out.cpu().numpy(), exact, bound)
+    assert int(err.item()) == ref_err
+
+
 def test_graph_replay_and_launch_options(gkr, oracle_mod):
     """Captured once (programmatic dependent launch off by option), replayed over new
     queries and indices copied into the captured buffers."""
