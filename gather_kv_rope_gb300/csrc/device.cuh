@@ -124,6 +124,7 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
     return lo | (hi << 16);
 }
 
+// (quantise8, the MXFP8 block quantiser, follows the two-wide fp32 helpers below.)
 
 // ---------------------------------------------------------------- MXFP8 decode
 
@@ -264,6 +265,8 @@ __device__ __forceinline__ uint2 quantise8_div_exact(const float* f, float scale
     return q;
 }
 
+// ---------------------------------------------------------------- two-wide fp32
+
 // Two fp32 values in one 64-bit register pair (lo in the low half), for the two-wide
 // fp32 multiply and fused multiply-add: one instruction rounds each half to nearest
 // even exactly as the scalar instruction would, subnormals kept.
@@ -286,9 +289,9 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
     return d;
 }
 
-// Quantise 8 values with their block's scale byte -> 8 e4m3 bytes: each value times the
-// exact power of two 2^(127 - byte), one rounded product, then the saturating nearest-
-// even cast.  kPacked: two products per instruction (the same results); the scalar form
+// MXFP8 encode: 8 values with their block's scale byte -> 8 e4m3 bytes.  Each value times
+// the exact power of two 2^(127 - byte), one rounded product, then the saturating
+// nearest-even cast.  kPacked: two products per instruction (the same results); the scalar form
 // is for kernels at a tight register budget, where the register pairs cost a spill.
 template <bool kPacked = true>
 __device__ __forceinline__ uint2 quantise8(const float* f, uint32_t byte) {
@@ -308,6 +311,8 @@ __device__ __forceinline__ uint2 quantise8(const float* f, uint32_t byte) {
     q.y = e4m3x4(p[4], p[5], p[6], p[7]);
     return q;
 }
+
+// ---------------------------------------------------------------- fp8 rows, two values per instruction
 
 // True when one of the eight codes is an e4m3 NaN (low seven bits all ones): adding 1 to
 // each byte's low seven bits carries into its bit 7 only then, and never into the next
