@@ -289,7 +289,9 @@ __device__ __forceinline__ uint32_t decode_compressed(const InsertParams& p, int
     if (q < 0) return 2u;
     const uint64_t q1 = static_cast<uint64_t>(q) + 1u;
     const uint64_t R = static_cast<uint64_t>(p.ratio);
-    const uint64_t rem = (q1 | R) >> 32 == 0u
+    // a power-of-two ratio (the usual case) takes a mask instead of a division
+    const uint64_t rem = (R & (R - 1u)) == 0u ? (q1 & (R - 1u))
+                         : (q1 | R) >> 32 == 0u
                              ? static_cast<uint64_t>(static_cast<uint32_t>(q1) %
                                                      static_cast<uint32_t>(R))
                              : q1 % R;
