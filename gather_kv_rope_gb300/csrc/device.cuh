@@ -43,6 +43,20 @@ __device__ __forceinline__ void st_stream16(void* p, uint4 v) {
     __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
+// ---------------------------------------------------------------- slot decode
+
+// Page and row of slot s in pages of bs slots.  A power-of-two block size (the usual case)
+// takes a shift and a mask; any other size, a 32-bit division.
+__device__ __forceinline__ void page_row(uint32_t s, uint32_t bs, uint32_t& page, uint32_t& row) {
+    if ((bs & (bs - 1u)) == 0u) {
+        page = s >> (__ffs(static_cast<int>(bs)) - 1);
+        row = s & (bs - 1u);
+    } else {
+        page = s / bs;
+        row = s - page * bs;
+    }
+}
+
 // ---------------------------------------------------------------- bf16 <-> fp32
 
 // Eight bf16 values packed in a uint4 -> fp32 (exact: bf16 is the top half of fp32).

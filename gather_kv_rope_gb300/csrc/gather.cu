@@ -75,7 +75,8 @@ __global__ void __launch_bounds__(kThreads, kRecord == 584 ? 6 : 8)
         if (idx >= 0 && idx < p.num_slots) {
             const uint32_t s = static_cast<uint32_t>(idx);
             const uint32_t bs = static_cast<uint32_t>(p.block_size);
-            const uint32_t page = s / bs, row = s - page * bs;
+            uint32_t page, row;
+            page_row(s, bs, page, row);
             const int64_t base = static_cast<int64_t>(page) * p.page_stride;
             off = base + row * R::D;
             soff = base + bs * R::D + row * R::S;

@@ -75,7 +75,8 @@ __device__ __forceinline__ void decode_group(const InsertParams& p, const WarpIt
             } else {
                 const uint32_t s = static_cast<uint32_t>(slot);
                 const uint32_t bs = static_cast<uint32_t>(p.block_size);
-                const uint32_t page = s / bs, row = s - page * bs;
+                uint32_t page, row;
+                page_row(s, bs, page, row);
                 const int64_t base = static_cast<int64_t>(page) * p.page_stride;
                 off = base + row * D;
                 soff = base + bs * D + row * S;
@@ -225,7 +226,8 @@ __global__ void __launch_bounds__(kThreads, GKR_SHORT_MIN_BLOCKS)
             } else {
                 const uint32_t s = static_cast<uint32_t>(slot);
                 const uint32_t bs = static_cast<uint32_t>(p.block_size);
-                const uint32_t page = s / bs, row = s - page * bs;
+                uint32_t page, row;
+                page_row(s, bs, page, row);
                 const int64_t base = static_cast<int64_t>(page) * p.page_stride;
                 off = base + row * D;
                 soff = base + bs * D + row * S;
@@ -300,7 +302,8 @@ __device__ __forceinline__ uint32_t decode_compressed(const InsertParams& p, int
     if (g >= static_cast<uint64_t>(p.max_pos)) return 2u;
     const uint32_t s = static_cast<uint32_t>(slot);
     const uint32_t bs = static_cast<uint32_t>(p.block_size);
-    const uint32_t page = s / bs, r = s - page * bs;
+    uint32_t page, r;
+    page_row(s, bs, page, r);
     const int64_t base = static_cast<int64_t>(page) * p.page_stride;
     off = base + r * D;
     soff = base + bs * D + r * S;
@@ -356,7 +359,8 @@ __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
             } else {
                 const uint32_t s = static_cast<uint32_t>(slot);
                 const uint32_t bs = static_cast<uint32_t>(p.block_size);
-                const uint32_t page = s / bs, row = s - page * bs;
+                uint32_t page, row;
+                page_row(s, bs, page, row);
                 const int64_t base = static_cast<int64_t>(page) * p.page_stride;
                 off = base + row * D;
                 soff = base + bs * D + row * S;

@@ -334,7 +334,8 @@ __device__ __forceinline__ void key_offsets(const LogitsParams& p, int32_t idx, 
     if (idx >= 0 && idx < p.num_slots) {
         const uint32_t s = static_cast<uint32_t>(idx);
         const uint32_t bs = static_cast<uint32_t>(p.block_size);
-        const uint32_t page = s / bs, row = s - page * bs;
+        uint32_t page, row;
+        page_row(s, bs, page, row);
         const int64_t pbase = static_cast<int64_t>(page) * p.page_stride;
         off = pbase + row * R::D;
         soff = pbase + bs * R::D + row * R::S;

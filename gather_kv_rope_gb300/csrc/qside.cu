@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, GKR_QSIDE_MIN_BLOCKS)
                     } else {
                         const uint32_t s = static_cast<uint32_t>(slot);
                         const uint32_t bs = static_cast<uint32_t>(p.block_size);
-                        const uint32_t page = s / bs, row = s - page * bs;
+                        uint32_t page, row;
+                        page_row(s, bs, page, row);
                         const int64_t base = static_cast<int64_t>(page) * p.page_stride;
                         off = base + row * D;
                         soff = base + bs * D + row * S;
