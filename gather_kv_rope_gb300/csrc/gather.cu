@@ -84,8 +84,6 @@ __global__ void __launch_bounds__(kThreads, kRecord == 584 ? 6 : 8)
             bad = idx != -1;
         }
     }
-    if (__ballot_sync(kFull, bad) != 0u && lane == 0) report(p.err, 4);
-
     LaneBases lb;
     lb.a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
     lb.tail = p.cache + 448 + 16 * (lane >= 24 ? lane - 24 : 0);
@@ -94,6 +92,8 @@ __global__ void __launch_bounds__(kThreads, kRecord == 584 ? 6 : 8)
 #pragma unroll
     for (int u = 0; u < U; ++u)
         load_record<kRecord>(__shfl_sync(kFull, off, u), __shfl_sync(kFull, soff, u), lb, lane, r[u]);
+    // the error bit while the record loads are in flight
+    if (__ballot_sync(kFull, bad) != 0u && lane == 0) report(p.err, 4);
     uint8_t* orow = static_cast<uint8_t*>(p.out) + i0 * 1024 + 16 * lane;
 #pragma unroll
     for (int u = 0; u < U; ++u)

@@ -235,9 +235,6 @@ __global__ void __launch_bounds__(kThreads, GKR_SHORT_MIN_BLOCKS)
             }
         }
     }
-    err = __reduce_or_sync(kFull, err);
-    if (err != 0u && lane == 0) report(p.err, static_cast<int32_t>(err));
-
     const uint8_t* kv_lane = static_cast<const uint8_t*>(p.kv) + t0 * 1024 + 16 * lane;
     const float* csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
     TokenLoads L[U];
@@ -256,6 +253,9 @@ __global__ void __launch_bounds__(kThreads, GKR_SHORT_MIN_BLOCKS)
             }
         }
     }
+    // the error bits while the row loads are in flight
+    err = __reduce_or_sync(kFull, err);
+    if (err != 0u && lane == 0) report(p.err, static_cast<int32_t>(err));
     uint8_t* const cache_a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
     uint8_t* const cache_s = p.cache + ScaleRows<kRecord>::lane_byte(lane);
 #pragma unroll
