@@ -368,9 +368,6 @@ __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
             }
         }
     }
-    err = __reduce_or_sync(kFull, err);
-    if (err != 0u && lane == 0) report(p.err, static_cast<int32_t>(err));
-
     const float* const csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -388,6 +385,9 @@ __global__ void __launch_bounds__(kThreads, GKR_STAGE_MIN_BLOCKS)
         }
         cp_async_commit();   // one group per token (empty for a skipped one)
     }
+    // the error bits while the copies are in flight
+    err = __reduce_or_sync(kFull, err);
+    if (err != 0u && lane == 0) report(p.err, static_cast<int32_t>(err));
 
     uint8_t* const cache_a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
     uint8_t* const cache_s = p.cache + ScaleRows<kRecord>::lane_byte(lane);

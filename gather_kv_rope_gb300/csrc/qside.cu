@@ -232,9 +232,6 @@ __global__ void __launch_bounds__(kThreads, GKR_QSIDE_MIN_BLOCKS)
             }
         }
     }
-    err = __reduce_or_sync(kFull, err);
-    if (err != 0u && lane == 0) report(p.err, static_cast<int32_t>(err));
-
     // every row's loads first: the KV row or the query head, and the cos/sin row
     const float* const csc_lane = p.csc + 4 * (lane >= 24 ? lane - 24 : 0);
     const uint8_t* const kv = static_cast<const uint8_t*>(p.kv);
@@ -263,6 +260,9 @@ __global__ void __launch_bounds__(kThreads, GKR_QSIDE_MIN_BLOCKS)
             }
         }
     }
+    // the error bits while the loads are in flight
+    err = __reduce_or_sync(kFull, err);
+    if (err != 0u && lane == 0) report(p.err, static_cast<int32_t>(err));
     uint8_t* const cache_a = p.cache + Fmt<kRecord>::kLaneBytes * lane;
     uint8_t* const cache_s = p.cache + ScaleRows<kRecord>::lane_byte(lane);
 #pragma unroll
