@@ -75,8 +75,10 @@ __device__ __forceinline__ void decode_group(const InsertParams& p, const WarpIt
             } else {
                 const uint32_t s = static_cast<uint32_t>(slot);
                 const uint32_t bs = static_cast<uint32_t>(p.block_size);
-                uint32_t page, row;
-                page_row(s, bs, page, row);
+                // a plain division here: one decode per 32 tokens is off the streaming
+                // kernel's critical path, and page_row's branch measured slower in its
+                // fp8 instantiation
+                const uint32_t page = s / bs, row = s - page * bs;
                 const int64_t base = static_cast<int64_t>(page) * p.page_stride;
                 off = base + row * D;
                 soff = base + bs * D + row * S;
