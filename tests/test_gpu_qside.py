@@ -318,3 +318,27 @@ def test_padded_heads_stay_inside_q_out(gkr, oracle_mod, fp8q, T, H, Hp):
         rn, lo, hi, _ = _oracle(oracle_mod, q, Hp, 1e-6, True, c, ref, 528,
                                 oracle_mod.page_stride(528, c.block_size))
         _assert_faithful(got.view(np.uint16), rn, (lo, hi))
+
+
+@pytest.mark.parametrize("norm", [False, True])
+@pytest.mark.parametrize("q_scale", [0.03, 0.25])
+def test_fp8_q_signed_zeros(gkr, oracle_mod, norm, q_scale):
+    """Query heads with exact +0 and -0 entries and whole zero heads, cast to e4m3 at a
+    general and a power-of-two scale: the codes keep the sign of zero (0x00 / 0x80), which
+    the two-wide quotient gets by flipping the sign bit of codes computed with -1/scale."""
+    c, q = _q_case(96, 4, seed=41)
+    rng = np.random.default_rng(42)
+    flat = q.reshape(-1)
+    pick = rng.permutation(flat.size)[:4000]
+    flat[pick[:2000]] = 0x8000          # -0
+    flat[pick[2000:]] = 0x0000          # +0
+    q[5, 1] = 0x8000                    # a whole head of -0
+    q[9, 2] = 0x0000                    # and of +0
+    got, ref, qo, rn, lo, hi, err, ref_err = _run_fp8q(gkr, oracle_mod, c, q, 6, 1e-6, norm,
+                                                       528, q_scale)
+    assert first_mismatch(got, ref)[0] == 0 and err == ref_err == 0
+    _assert_codes(qo, rn, lo, hi)
+    zero = (lo == hi) & ((rn & 0x7F) == 0)
+    assert zero.sum() > 1000
+    assert np.array_equal(qo[zero], rn[zero])
+    assert (qo[5, 1] == rn[5, 1]).all() and (qo[:, 4:] == 0).all()
