@@ -146,6 +146,40 @@ def test_one_chunk_per_query(gkr, oracle_mod, record):
     assert int(err.item()) == ref_err
 
 
+@pytest.mark.parametrize("seed", range(48))
+def test_random_configurations(gkr, oracle_mod, seed):
+    """48 seeded draws over the record formats, block sizes, cache sizes, query counts
+    (runs within one query and across many), head counts (full and partial lane
+    quarters), top-k (multiples of 4 from 4 to 700, one to six chunks), fp8 scales, query
+    magnitudes, sm_scale signs and invalid-index rates."""
+    rng = np.random.default_rng(7000 + seed)
+    record = int(rng.choice([528, 584, 512, 1024]))
+    bs = int(rng.choice([32, 64, 96])) if record in (528, 584) else int(rng.choice([16, 48, 64]))
+    pages = int(rng.integers(4, 40))
+    Q = int(rng.choice([1, 3, 40, 300]))
+    H = int(rng.choice([1, 16, 33, 64, 100, 128]))
+    K = int(rng.choice([4, 8, 100, 128, 132, 260, 700]))
+    pages = max(pages, -(-K // bs) + 1)   # enough slots for K distinct indices
+    scale = float(np.float32(2.0 ** rng.uniform(-8, 2))) if record == 512 else None
+    sm = float(rng.choice([0.0625, -0.03, 1.0]))
+    c, flat, ps = _host_cache(oracle_mod, record, pages * bs, bs, pages, seed=seed, scale=scale)
+    idx = _indices(rng, Q, K, np.arange(pages * bs), bad_rate=float(rng.choice([0.0, 0.02])),
+                   num_slots=pages * bs)
+    q = bf16_bits((rng.standard_normal((Q, H, 512)) * rng.choice([0.1, 1.0, 30.0]))
+                  .astype(np.float32))
+    cache = _to_device_cache(gkr, flat, pages, bs, record, ps)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kw = {} if scale is None else {"fp8_scale": torch.tensor([scale], dtype=torch.float32,
+                                                             device=DEV)}
+    out = gkr.sparse_logits(torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).to(DEV),
+                            cache, torch.from_numpy(idx).to(DEV), sm, err_flag=err, **kw)
+    torch.cuda.synchronize()
+    exact, bound, ref_err = oracle_mod.sparse_logits(q, flat, record, bs, pages, ps, idx, sm,
+                                                     fp8_scale=scale)
+    _check(out.cpu().numpy(), exact, bound)
+    assert int(err.item()) == ref_err
+
+
 def test_graph_replay_and_launch_options(gkr, oracle_mod):
     """Captured once (programmatic dependent launch off by option), replayed over new
     queries and indices copied into the captured buffers."""
