@@ -342,3 +342,36 @@ def test_fp8_q_signed_zeros(gkr, oracle_mod, norm, q_scale):
     assert zero.sum() > 1000
     assert np.array_equal(qo[zero], rn[zero])
     assert (qo[5, 1] == rn[5, 1]).all() and (qo[:, 4:] == 0).all()
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_random_configurations(gkr, oracle_mod, seed):
+    """32 seeded draws over the record formats, token counts, head counts and padding
+    (including none and query-free tokens), the norm on or off, eps, head magnitudes, the
+    fp8 cache's scale and the query output (bf16, or e4m3 at a random scale)."""
+    rng = np.random.default_rng(9000 + seed)
+    record = int(rng.choice([528, 584, 512, 1024]))
+    T = int(rng.choice([1, 17, 300, 1500]))
+    H = int(rng.choice([0, 1, 4, 16, 33]))
+    Hp = H + int(rng.choice([0, 0, 1, 7, 48]))
+    if Hp == 0:
+        Hp = 1
+    norm = bool(rng.random() < 0.7)
+    eps = float(rng.choice([0.0, 1e-6, 0.5])) if H > 0 else 1e-6
+    c, q = _q_case(T, H, record=record, seed=seed, sigma=float(rng.choice([0.01, 1.0, 50.0])))
+    if norm and eps == 0.0:
+        q[..., 0] = 0x3F80                    # dim 0 = 1.0: no all-zero head when eps is 0
+    fp8 = float(np.float32(2.0 ** rng.uniform(-6, 3))) if record == 512 else None
+    if rng.random() < 0.5:
+        qs = float(np.float32(2.0 ** rng.uniform(-8, 4)))
+        got, ref, qo, rn, lo, hi, err, ref_err = _run_fp8q(gkr, oracle_mod, c, q, Hp, eps, norm,
+                                                           record, qs, fp8_scale=fp8)
+        _assert_codes(qo, rn, lo, hi)
+    else:
+        got, ref, qo, rn, bounds, err, ref_err = _run(gkr, oracle_mod, c, q, Hp, eps, norm, record,
+                                                   scale=fp8)
+        _assert_faithful(qo, rn, bounds)
+    n, first = first_mismatch(got, ref)
+    assert n == 0, f"cache: {n} bytes differ, first {first}"
+    assert err == ref_err
+    assert (qo[:, H:] == 0).all()
