@@ -137,7 +137,8 @@ __device__ __forceinline__ void zero_padded_heads(const QSideParams& qp, int64_t
 template <int kRecord, bool kFp8Q>
 __global__ void __launch_bounds__(kThreads, GKR_QSIDE_MIN_BLOCKS)
     qnorm_rope_kv_insert_kernel(const InsertParams p, const QSideParams qp,
-                                const int64_t blocks_of_rows) {
+                                const int64_t blocks_of_rows, const uint64_t row_magic,
+                                const uint32_t row_shift) {
     constexpr int U = kRowsPerWarp;
     constexpr uint32_t D = Fmt<kRecord>::D;
     constexpr uint32_t S = Fmt<kRecord>::S;
@@ -157,12 +158,11 @@ __global__ void __launch_bounds__(kThreads, GKR_QSIDE_MIN_BLOCKS)
     int64_t t = 0;
     int32_t j = -1;
     if (mine) {
-        if (n_rows <= 0xFFFFFFFFll) {  // uniform: the 32-bit division is a fraction of the 64-bit one
-            const uint32_t r = static_cast<uint32_t>(r0 + lane);
-            const uint32_t pt = static_cast<uint32_t>(per_token);
-            const uint32_t tt = r / pt;
-            t = tt;
-            j = static_cast<int32_t>(r - tt * pt);
+        if (row_magic != 0u) {  // uniform: rows < 2^31, a multiply and a shift (see the launch)
+            const uint64_t r = static_cast<uint64_t>(r0 + lane);
+            const uint64_t tt = (r * row_magic) >> row_shift;
+            t = static_cast<int64_t>(tt);
+            j = static_cast<int32_t>(r - tt * static_cast<uint64_t>(per_token));
         } else {
             t = (r0 + lane) / per_token;
             j = static_cast<int32_t>(r0 + lane - t * per_token);
@@ -309,11 +309,23 @@ cudaError_t launch(const InsertParams& p, const QSideParams& qp, cudaStream_t st
     const int64_t zero_per_block = static_cast<int64_t>(kWarpsPerBlock) * kZeroPieces;
     const int64_t row_blocks = (rows + per_block - 1) / per_block;
     const int64_t blocks = row_blocks + (pieces + zero_per_block - 1) / zero_per_block;
+    // row r's token r / d (d = H + 1 rows per token) as (r * M) >> S with S = 32 + ceil(log2 d)
+    // and M = ceil(2^S / d): exact for every r < 2^31 (the error n (M d - 2^S) / (d 2^S) stays
+    // below 1 / d), and r * M < 2^64 since M <= 2^33.  M = 0 (more rows): a division.
+    uint64_t magic = 0;
+    uint32_t shift = 0;
+    const uint64_t d = static_cast<uint64_t>(qp.num_heads) + 1;
+    if (rows < (INT64_C(1) << 31)) {
+        uint32_t lg = 0;
+        while ((UINT64_C(1) << lg) < d) ++lg;
+        shift = 32 + lg;
+        magic = ((UINT64_C(1) << shift) + d - 1) / d;
+    }
     return qp.q_scale != nullptr
                ? launch_kernel(qnorm_rope_kv_insert_kernel<kRecord, true>, blocks, kThreads, 0,
-                               stream, p.pdl, p, qp, row_blocks)
+                               stream, p.pdl, p, qp, row_blocks, magic, shift)
                : launch_kernel(qnorm_rope_kv_insert_kernel<kRecord, false>, blocks, kThreads, 0,
-                               stream, p.pdl, p, qp, row_blocks);
+                               stream, p.pdl, p, qp, row_blocks, magic, shift);
 }
 
 }  // namespace
